@@ -1,0 +1,222 @@
+/*
+ * usaf.h - C ABI of the GB300 (sm_103a) hot path of USAF sparse MoE fine-tuning.
+ *
+ * One MoE layer's train step, as the USAF README describes it: the router is trained in full
+ * ("The router is leverage" paragraph), 0.5% of the native expert weights, picked by gradient
+ * magnitude ("Not all weights matter" paragraph), are trained in place with Adam state kept only
+ * for them (A100 operations table: "SparseAdam (26M)"), and the active set is reselected
+ * RigL-style every 50 steps ("Sparsity adapts" paragraph; RESELECT_EVERY in the environment
+ * variable table). The fused expert layouts gate_up_proj [E, 2I, H] and down_proj [E, H, I] and the
+ * act(gate) * up epilogue are the ones stated on the experts4bit-qlora page ("The abstraction that
+ * fails, and what replaces it" section, and its epilogue-contract bullet).
+ *
+ * Conventions shared by every entry point:
+ *  - Every pointer argument is a DEVICE pointer owned by the caller, unless a comment says "host".
+ *    The library allocates no device memory: scratch comes from a caller-provided workspace whose
+ *    size the matching *_workspace_size() query returns (a host-only computation).
+ *  - Tensors are dense and row-major. Element types are given by usaf_dtype.
+ *  - `stream` is a cudaStream_t passed as void*. Every call only enqueues work on that stream and
+ *    never synchronises the host. Calls keep no state between them and are thread-safe.
+ *  - Host-side argument checks run before anything is enqueued; a failed check returns
+ *    USAF_ERR_INVALID_ARG (or USAF_ERR_UNSUPPORTED / USAF_ERR_WORKSPACE) and enqueues nothing.
+ *    A failed kernel launch returns USAF_ERR_CUDA. Conditions that only the device can see
+ *    (non-finite gradients, a selection that had to take the exact multi-pass path) are OR-ed
+ *    as bits into the caller's `dev_status` word (device memory, may be NULL); no kernel traps.
+ *  - Flat expert-weight index f (int64): f < N_gu = E*2I*H addresses gate_up_proj row-major,
+ *    N_gu <= f < N = E*3*I*H addresses down_proj row-major at f - N_gu. Active sets are sorted
+ *    ascending and free of duplicates.
+ */
+#ifndef USAF_H
+#define USAF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define USAF_ABI_VERSION 1
+
+/* Each expert's rows in the permuted (expert-sorted) order start at a multiple of this. */
+#define USAF_ROW_ALIGN 16
+
+typedef enum {
+  USAF_OK = 0,
+  USAF_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad enum, aliasing that is not allowed */
+  USAF_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels handle (see each call) */
+  USAF_ERR_WORKSPACE = 3,   /* workspace pointer NULL or smaller than the query says */
+  USAF_ERR_CUDA = 4,        /* a CUDA runtime/driver call or a kernel launch failed */
+  USAF_ERR_TIMEOUT = 5      /* reserved: a bounded device wait gave up */
+} usaf_status;
+
+typedef enum { USAF_F32 = 0, USAF_BF16 = 1 } usaf_dtype;
+
+/* Bits OR-ed into *dev_status by the device. */
+#define USAF_DEV_NONFINITE 1u       /* a gradient (or selection key) was NaN or Inf */
+#define USAF_DEV_SELECT_EXACT_PATH 2u /* informational: the sampled one-pass selection fell back
+                                       * to the exact multi-pass radix select */
+#define USAF_DEV_TIMEOUT 4u         /* reserved for bounded device waits */
+
+/* MoE layer dimensions: T tokens, H hidden size, E experts, k experts per token, I expert
+ * intermediate size. */
+typedef struct {
+  int64_t T, H, E, k, I;
+} usaf_moe_shape;
+
+/* Routing tables written by usaf_route_topk and read by usaf_moe_fwd / usaf_moe_bwd_sparse.
+ * R = T*k routed slots; slot s = t*k + j is the j-th expert of token t.
+ * The permuted order lists, for e = 0..E-1, the slots routed to e in ascending token order;
+ * expert e's segment starts at row expert_offset[e] (a multiple of USAF_ROW_ALIGN) and its
+ * rows past expert_count[e] up to the next offset are padding rows (perm_tok = 0, perm_slot = -1).
+ * R_cap = usaf_routed_rows_capacity(shape) is the number of rows every permuted array holds. */
+typedef struct {
+  int32_t* topk_idx;      /* [T*k]   expert of each slot, in descending-logit order per token   */
+  float* topk_w;          /* [T*k]   routing weight of each slot                                */
+  int32_t* expert_count;  /* [E]     tokens routed to each expert                               */
+  int32_t* expert_offset; /* [E+1]   first permuted row of each expert; [E] = padded total rows */
+  int32_t* perm_tok;      /* [R_cap] token of each permuted row                                 */
+  int32_t* perm_slot;     /* [R_cap] slot of each permuted row, -1 for padding                  */
+  int32_t* slot_row;      /* [T*k]   permuted row of each slot                                  */
+} usaf_routing;
+
+int usaf_abi_version(void);
+const char* usaf_status_string(usaf_status s); /* host string, static storage */
+
+/* Rows every permuted array (perm_tok, perm_slot, saved activations) must hold:
+ * T*k + E*(USAF_ROW_ALIGN-1) rounded up to 256, plus 256 rows of read-ahead slack. Host only. */
+int64_t usaf_routed_rows_capacity(const usaf_moe_shape* shape);
+
+/* ---------------------------------------------------------------------------------------------
+ * usaf_route_topk - router logits, top-k with renormalised softmax weights, token permutation.
+ * Router logits logits[t,e] = sum_h x[t,h] * w_router[e,h] (fp32 arithmetic, x upcast exactly).
+ * Per token the k experts with the largest fp32 logits are taken, ties to the lower expert index,
+ * in descending order. renorm=1: w_j = softmax over the k selected logits (equal to softmax over
+ * all E, top-k, renormalised); renorm=0: w_j = softmax over all E at the selected experts.
+ * The router is the gating network the USAF README trains in full ("The router is leverage").
+ *   x          [T,H] of x_dtype (USAF_F32 or USAF_BF16); ignored when logits_in != NULL
+ *   w_router   [E,H] fp32; ignored when logits_in != NULL
+ *   logits_in  [T,E] fp32 or NULL: use these logits instead of computing them
+ *   logits_out [T,E] fp32 or NULL: where computed logits are written
+ *   rt         routing tables (all seven arrays required)
+ * Limits: 1 <= k <= E <= 1024, k <= 32, T*k < 2^31. Errors: INVALID_ARG, WORKSPACE, CUDA.
+ * ------------------------------------------------------------------------------------------- */
+size_t usaf_route_topk_workspace_size(const usaf_moe_shape* shape);
+usaf_status usaf_route_topk(const usaf_moe_shape* shape, const void* x, usaf_dtype x_dtype,
+                            const float* w_router, const float* logits_in, float* logits_out,
+                            int renorm, const usaf_routing* rt, void* ws, size_t ws_bytes,
+                            void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * usaf_moe_fwd - grouped SwiGLU expert forward over the permuted rows.
+ * For every routed slot (t, j) with expert e: h = gate_up_proj[e] . x[t]  (2I values; the first I
+ * rows of gate_up_proj[e] are the gate, the last I the up projection), A = silu(gate) * up,
+ * y = down_proj[e] . A, and Y[t] = sum_j w[t,j] * y_j. Layouts per the experts4bit-qlora page
+ * (gate_up_proj [E,2I,H], down_proj [E,H,I]); act(gate)*up per its epilogue-contract bullet.
+ *   dtype        USAF_BF16: x, weights, saved activations and y are bf16, accumulation fp32, on
+ *                tcgen05 tensor cores (needs H % 64 == 0, I % 64 == 0).
+ *                USAF_F32: everything fp32 on CUDA cores (any sizes).
+ *   x            [T,H];  w_gate_up [E,2I,H];  w_down [E,H,I]
+ *   x_perm_save  [R_cap,H]  out: x rows in permuted order (kept for the backward)
+ *   h_save       [R_cap,2I] out: gate|up pre-activations per permuted row
+ *   wa_save      [R_cap,I]  out: w * A per permuted row (0 in padding rows)
+ *   y            [T,H]      out
+ * Errors: INVALID_ARG, UNSUPPORTED (bf16 shape limits), WORKSPACE, CUDA.
+ * ------------------------------------------------------------------------------------------- */
+size_t usaf_moe_fwd_workspace_size(const usaf_moe_shape* shape, usaf_dtype dtype);
+usaf_status usaf_moe_fwd(const usaf_moe_shape* shape, usaf_dtype dtype, const void* x,
+                         const void* w_gate_up, const void* w_down, const usaf_routing* rt,
+                         void* x_perm_save, void* h_save, void* wa_save, void* y, void* ws,
+                         size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * usaf_moe_bwd_sparse - sparse backward of the layer for upstream gradient dy = dL/dY.
+ * Per slot: gvec = down_proj[e]^T dy[t], dw = <gvec, A>, dA = w*gvec, dgate = dA*up*silu'(gate),
+ * dup = dA*silu(gate). Router: dlogit[t,e_j] = w_j*(dw_j - sum_i w_i dw_i) (renorm=1; renorm=0
+ * uses the all-E softmax form), g_router = dlogit^T x. dx = sum_j gate_up_proj[e_j]^T dh_j +
+ * dlogit . w_router. Expert weight gradients are formed only at the active set
+ * (the news article's "updates only a subset of weights within each activated expert";
+ * the README's "Backward ~30ms/layer (26M params)"):
+ *   g_act[a] = sum over rows of expert e of dh[row, r] * x[tok, c]         (gate_up entry e,r,c)
+ *   g_act[a] = sum over rows of expert e of dy[tok, r] * w * A[row, c]      (down entry e,r,c)
+ * Experts that received no token get zero gradient.
+ *   renorm       must match the routing call; logits [T,E] fp32 needed only when renorm == 0
+ *   x_perm_save, h_save, wa_save   as written by usaf_moe_fwd with the same routing
+ *   dy           [T,H] of dtype
+ *   act_idx      [K] sorted flat indices (int64), 0 <= K <= N
+ *   g_act        [K] fp32 out;  g_router [E,H] fp32 out
+ *   dx           [T,H] of dtype out, or NULL to skip the input gradient
+ *   dw_slot      [T*k] fp32 out (dL/dw per slot), or NULL
+ *   dev_status   gets USAF_DEV_NONFINITE if any produced gradient is NaN/Inf (may be NULL)
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
+ * ------------------------------------------------------------------------------------------- */
+size_t usaf_moe_bwd_workspace_size(const usaf_moe_shape* shape, usaf_dtype dtype, int64_t K);
+usaf_status usaf_moe_bwd_sparse(const usaf_moe_shape* shape, usaf_dtype dtype, int renorm,
+                                const void* x, const float* w_router, const void* w_gate_up,
+                                const void* w_down, const usaf_routing* rt, const float* logits,
+                                const void* x_perm_save, const void* h_save, const void* wa_save,
+                                const void* dy, const int64_t* act_idx, int64_t K, float* g_act,
+                                float* g_router, void* dx, float* dw_slot, uint32_t* dev_status,
+                                void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * usaf_sparse_adam_step - fused gather / Adam update / scatter over n entries (the README's
+ * "SparseAdam (26M)" optimizer, torch.optim.SparseAdam semantics, no weight decay):
+ *   m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*g^2;
+ *   p -= lr*sqrt(1-b2^step)/(1-b1^step) * m/(sqrt(v)+eps)
+ * then the dense weight at the entry's flat index receives p (rounded to nearest-even for bf16).
+ *   idx          [n] flat indices, or NULL for the dense identity 0..n-1
+ *   g, p, m, v   [n] fp32 (p is the fp32 master copy of the trained entries; p, m, v in place)
+ *   w_seg0       dense weights holding flat indices [0, n_seg0); w_seg1 holds [n_seg0, ...) and
+ *                may be NULL when every index is below n_seg0; both of w_dtype
+ *   step         1-based step count
+ *   skip_if_nonfinite  if nonzero, the entry point first scans g, and no entry is updated when
+ *                this scan or an earlier call (a bit already set in *dev_status, e.g. by
+ *                usaf_moe_bwd_sparse) found a non-finite gradient (the README's NaN step skip)
+ * Errors: INVALID_ARG, CUDA.
+ * ------------------------------------------------------------------------------------------- */
+usaf_status usaf_sparse_adam_step(int64_t n, const int64_t* idx, const float* g, float* p,
+                                  float* m, float* v, void* w_seg0, int64_t n_seg0, void* w_seg1,
+                                  usaf_dtype w_dtype, float lr, float beta1, float beta2,
+                                  float eps, int64_t step, int skip_if_nonfinite,
+                                  uint32_t* dev_status, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * usaf_importance_select - the importance phase of the USAF README ("Not all weights matter":
+ * the 0.5% of weights with the highest gradient magnitude). Exact top-K of |g| over N entries,
+ * ordered by (|g| descending, index ascending); the K winners are written sorted ascending.
+ * |g| is compared as its fp32 bit pattern with the sign cleared.
+ *   g        [N] fp32 dense gradient
+ *   out_idx  [K] int64 out
+ * Limits: 1 <= K <= N < 2^32. Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
+ * ------------------------------------------------------------------------------------------- */
+size_t usaf_importance_select_workspace_size(int64_t N, int64_t K);
+usaf_status usaf_importance_select(const float* g, int64_t N, int64_t K, int64_t* out_idx,
+                                   uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * usaf_rigl_swap - RigL reselection of the active set (USAF README, "Sparsity adapts"):
+ * drop the D active entries with the smallest |p| (ties: lower flat index dropped first), grow
+ * the D inactive entries (not in the old set) with the largest |g| (ties: lower flat index
+ * first). new_idx = (act_idx minus dropped) union grown, sorted. Kept entries carry p, m, v
+ * unchanged; grown entries start with p = the dense weight value and m = v = 0.
+ *   g          [N] fp32 dense gradient;  act_idx [K] sorted
+ *   p_in, m_in, v_in   [K] fp32 state aligned with act_idx
+ *   w_seg0/n_seg0/w_seg1/w_dtype   dense weights, as for usaf_sparse_adam_step
+ *   new_idx, p_out, m_out, v_out   [K] out; must not overlap the inputs
+ *   n_swapped  [1] int64 out: number of entries of act_idx not in new_idx (= D)
+ * Limits: 0 <= D <= K, D <= N - K, N < 2^32. Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
+ * ------------------------------------------------------------------------------------------- */
+size_t usaf_rigl_swap_workspace_size(int64_t N, int64_t K, int64_t D);
+usaf_status usaf_rigl_swap(const float* g, int64_t N, const int64_t* act_idx, int64_t K,
+                           int64_t D, const float* p_in, const float* m_in, const float* v_in,
+                           const void* w_seg0, int64_t n_seg0, const void* w_seg1,
+                           usaf_dtype w_dtype, int64_t* new_idx, float* p_out, float* m_out,
+                           float* v_out, int64_t* n_swapped, uint32_t* dev_status, void* ws,
+                           size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* USAF_H */

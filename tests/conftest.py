@@ -1,0 +1,18 @@
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+
+def pytest_configure(config):
+    config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
+    config.addinivalue_line("markers", "slow: long-running CPU check")
+
+
+def pytest_collection_modifyitems(config, items):
+    # keep tests/test_zz_*.py last whatever order files are given in
+    items.sort(key=lambda it: os.path.basename(str(it.fspath)).startswith("test_zz_"))
