@@ -1,0 +1,412 @@
+"""Benchmark of the USAF MoE-layer train step on GB300.
+
+A step is one pass of the whole hot path over one batch: route (router logits, top-k,
+permutation) -> grouped SwiGLU forward -> sparse backward (router gradient, dx, expert gradients
+at the 0.5% active set) -> SparseAdam on the active expert entries and on the router.
+Workload: the Qwen3-30B-A3B-shaped layer (T=4096 tokens, H=2048, E=128, top-8, I=768, bf16,
+router fp32, K = ceil(0.005 * 603,979,776) = 3,019,899 active entries chosen by the importance
+selection of a seeded Student-t(3) dense gradient). Inputs are seeded synthetic data; the
+weights (1.2 GB) are larger than L2, so no flush is needed between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints one JSON line. Under torchrun each rank runs its own replica (weak scaling, no
+collective on the data path); rank 0 prints.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from sparse_moe_fine_gb300 import synth  # noqa: E402
+
+METRIC = "MoE-layer train-step tokens/s (fwd+sparse bwd+SparseAdam); % of roofline"
+WORKLOAD = "qwen3_30b_a3b"
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), \
+            "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def algorithmic(cfg):
+    """Algorithmic FLOPs and HBM bytes of one step (unpadded, SDDMM-counted masked dW)."""
+    T, H, E, k, I, K = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.K
+    R = T * k
+    fl = (2 * R * 2 * I * H + 2 * R * I * H          # forward GEMMs
+          + 2 * R * I * H + 2 * R * 2 * I * H        # dgrad through down, dx
+          + 2 * T * E * H * 3                        # router logits, g_router, dx router term
+          + 2 * K * (R / E))                         # masked dW at the active set
+    by = (2 * cfg.N * 2                             # expert weights, read in fwd and in bwd
+          + 2 * T * H * 2                            # x
+          + 2 * R * 2 * I * 2 + 2 * R * I * 2        # h, A (write + read)
+          + 3 * T * H * 2                            # y, dy, dx
+          + 2 * R * 2 * I * 2                        # dh (write + read)
+          + 2 * T * E * 4                            # logits
+          + 2 * (K + E * H) * 4                      # gradients at the active set and router
+          + 34 * (K + E * H))                        # SparseAdam: idx, g, p/m/v, weight scatter
+    return fl, by
+
+
+def kernel_units(cfg):
+    """Per-launch algorithmic work of the tensor-core kernels: (bound, flops, bytes)."""
+    T, H, E, k, I = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I
+    R = T * k
+    Wgu, Wd = E * 2 * I * H * 2, E * H * I * 2
+    return {
+        "tc_gate_up_swiglu": (2 * R * 2 * I * H, Wgu + R * H * 2 + R * 2 * I * 2 + R * I * 2),
+        "tc_down_combine": (2 * R * I * H, Wd + R * I * 2),
+        "tc_gvec_swiglu_bwd": (2 * R * I * H, Wd + R * H * 2 + 2 * R * 2 * I * 2),
+        "tc_dx": (2 * R * 2 * I * H, Wgu + R * 2 * I * 2),
+        "tc_wgrad_gate_up": (2 * R * 2 * I * H, R * 2 * I * 2 + R * H * 2),
+        "tc_wgrad_down": (2 * R * I * H, R * H * 2 + R * I * 2),
+    }
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        return dist, ws, rank, local
+    return None, 1, 0, local
+
+
+def max_over_ranks(dist, value: float, device) -> float:
+    """Largest value over all ranks (the slowest rank sets the time)."""
+    if dist is None:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def oracle_step_sample(cfg, inp, act, p0, tokens):
+    """The CPU oracle's layer step on the first `tokens` tokens of the workload (same weights,
+    router, active set and its fp32 master values p0): routing, forward, backward, gradients at
+    the active entries of the experts those tokens reach, SparseAdam. Returns seconds."""
+    import oracle
+    x = inp["x"][:tokens]
+    dy = inp["dy"][:tokens]
+    t0 = time.perf_counter()
+    logits = oracle.router_logits(x, inp["w_router"])
+    idx, w = oracle.route_topk(logits, cfg.k)
+    b = oracle.moe_backward(x, inp["w_router"], inp["w_gate_up"], inp["w_down"], idx, w, logits,
+                            dy)
+    hit = sorted(set(idx.reshape(-1).tolist()))
+    g = oracle.masked_expert_grad(act, x, inp["w_gate_up"], inp["w_down"], idx, w, dy,
+                                  experts=hit)
+    g = np.nan_to_num(g, nan=0.0)  # entries of experts no sampled token reaches
+    oracle.sparse_adam(g, p0, np.zeros_like(p0), np.zeros_like(p0), cfg.lr, 0.9, 0.999, 1e-8, 1)
+    oracle.sparse_adam(b["g_router"].reshape(-1), inp["w_router"].reshape(-1),
+                       np.zeros(cfg.E * cfg.H), np.zeros(cfg.E * cfg.H), cfg.lr, 0.9, 0.999,
+                       1e-8, 1)
+    return time.perf_counter() - t0
+
+
+def master_values(inp, act, N_gu):
+    gu = act < N_gu
+    p0 = np.empty(act.size, np.float32)
+    p0[gu] = inp["w_gate_up"].reshape(-1)[act[gu]]
+    p0[~gu] = inp["w_down"].reshape(-1)[act[~gu] - N_gu]
+    return p0
+
+
+def cpu_threads():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        return max(int(i.get("num_threads", 1)) for i in info) if info else os.cpu_count()
+    except Exception:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    """The oracle on the host cores: the same metric on bounded samples of the workload."""
+    dist, ws, rank, local = dist_setup()
+    if rank != 0:
+        return
+    cfg = synth.CONFIGS[WORKLOAD]
+    inp = synth.moe_inputs(cfg, seed=0)
+    act = synth.uniform_mask(cfg.N, cfg.K, seed=0)
+    p0 = master_values(inp, act, cfg.N_gu)
+    inp = {k: v.astype(np.float64) for k, v in inp.items()}  # exact upcast of the bf16 inputs
+    # per-step sample: fewer tokens when more steps are asked for, so the run stays in minutes
+    tokens = args.cpu_tokens if args.steps <= 10 else (64 if args.steps <= 100 else 16)
+    for _ in range(min(args.warmup, 1)):
+        oracle_step_sample(cfg, inp, act, p0, tokens)
+    times = [oracle_step_sample(cfg, inp, act, p0, tokens) for _ in range(max(1, args.steps))]
+    sec = sum(times)
+    value = tokens * len(times) / sec
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": ws, "steps": len(times), "warmup": args.warmup,
+            "ms_per_step": 1e3 * sec / len(times) * (cfg.T / tokens),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": f"{WORKLOAD} layer step, oracle on a {tokens}-token sample",
+                       "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I,
+                       "active": cfg.K},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads(),
+                             "kind": "oracle",
+                             "sample": f"first {tokens} of {cfg.T} tokens per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run(args):
+    from sparse_moe_fine_gb300 import binding as B
+    from sparse_moe_fine_gb300.layer import MoELayer
+
+    dist, ws, rank, local = dist_setup()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    B.lib()
+    hbm, tf_burst, tf_sus, peak_src = peaks()
+    cfg = synth.CONFIGS[WORKLOAD]
+    inp = synth.moe_inputs(cfg, seed=0)
+    bf = lambda a: torch.from_numpy(a).to(dev).to(torch.bfloat16)
+    x, dy = bf(inp["x"]), bf(inp["dy"])
+    wgu, wd = bf(inp["w_gate_up"]), bf(inp["w_down"])
+    wr = torch.from_numpy(inp["w_router"]).to(dev)
+    stream = torch.cuda.current_stream()
+
+    # ---- importance pass: the active set is the top 0.5% |g| of a dense gradient
+    g_dense = torch.from_numpy(synth.student_t3(cfg.N, seed=0)).to(dev)
+    act = torch.empty(cfg.K, dtype=torch.int64, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_sel = torch.empty(B.importance_select_workspace_size(cfg.N, cfg.K), dtype=torch.uint8,
+                         device=dev)
+    for _ in range(2):
+        B.importance_select(g_dense, cfg.K, act, dev_status=st, ws=ws_sel)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    reps = 5
+    ev[0].record()
+    for _ in range(reps):
+        B.importance_select(g_dense, cfg.K, act, dev_status=st, ws=ws_sel)
+    ev[1].record()
+    torch.cuda.synchronize()
+    sel_ms = ev[0].elapsed_time(ev[1]) / reps
+    # RigL reselection on the same layer (drop 30% by |p|, grow by |g|)
+    D = int(0.3 * cfg.K)
+    layer = MoELayer(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, wgu, wd, wr, act, lr=cfg.lr, device=dev)
+    outs = [torch.empty(cfg.K, dtype=torch.int64, device=dev)] + \
+        [torch.empty(cfg.K, device=dev) for _ in range(3)]
+    ns = torch.zeros(1, dtype=torch.int64, device=dev)
+    ws_rigl = torch.empty(B.rigl_swap_workspace_size(cfg.N, cfg.K, D), dtype=torch.uint8,
+                          device=dev)
+    rigl = lambda: B.rigl_swap(g_dense, act, D, layer.p, layer.m, layer.v, wgu, cfg.N_gu, wd,
+                               *outs, ns, ws=ws_rigl)
+    rigl()
+    ev[0].record()
+    for _ in range(reps):
+        rigl()
+    ev[1].record()
+    torch.cuda.synchronize()
+    rigl_ms = ev[0].elapsed_time(ev[1]) / reps
+    del ws_rigl, ws_sel, outs
+    g_bytes = cfg.N * 4
+    importance = {
+        "select_ms": sel_ms, "select_gbs": g_bytes / sel_ms / 1e6,
+        "select_frac": g_bytes / sel_ms / 1e6 / hbm,
+        "rigl_ms": rigl_ms, "rigl_gbs": (g_bytes + cfg.N / 8 + cfg.K * 40) / rigl_ms / 1e6,
+        "select_exact_path": bool(int(st.item()) & B.DEV_SELECT_EXACT_PATH),
+        "N": cfg.N, "K": cfg.K, "D": D}
+    del g_dense
+    torch.cuda.empty_cache()
+
+    # ---- train steps
+    for _ in range(args.warmup):
+        layer.status.zero_()
+        layer.train_step(x, dy)
+    torch.cuda.synchronize()
+    n0 = B.launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for _ in range(args.steps):
+            layer.train_step(x, dy)
+        e1.record(stream)
+        torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    launches = (B.launch_count() - n0) // max(1, args.steps)
+    ms = max_over_ranks(dist, e0.elapsed_time(e1) / args.steps, dev)
+    value = ws * cfg.T / (ms / 1e3)
+
+    # ---- per-kernel times over a second timed region of the same steps (event-bracketed)
+    B.trace_enable(True)
+    for _ in range(args.steps):
+        layer.train_step(x, dy)
+    torch.cuda.synchronize()
+    trace = B.trace_summary()
+    B.trace_enable(False)
+    tot = sum(t for _, _, t in trace)
+    units = kernel_units(cfg)
+    dominant = max(trace, key=lambda r: r[2])
+    name, nl, tms = dominant
+    avg_ms = tms / nl
+    if name in units:
+        fl, by = units[name]
+        t_fl, t_by = fl / (tf_burst * 1e12), by / (hbm * 1e9)
+        if t_fl >= t_by:
+            roof = {"bound": "tensor", "achieved": fl / (avg_ms / 1e3) / 1e12, "peak": tf_burst,
+                    "unit": "TFLOP/s"}
+        else:
+            roof = {"bound": "hbm", "achieved": by / (avg_ms / 1e3) / 1e9, "peak": hbm,
+                    "unit": "GB/s"}
+    else:
+        roof = {"bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"] if roof["achieved"] else None
+    roof.update({"kernel": name, "kernel_ms": avg_ms, "traffic": None,
+                 "peak_source": peak_src, "share": tms / tot if tot else None})
+    fl, by = algorithmic(cfg)
+    step_roof_ms = max(fl / (tf_sus * 1e12), by / (hbm * 1e9)) * 1e3
+
+    # ---- end to end: x, dy from pinned host memory, y and dx back, through the layer API
+    xh = x.cpu().pin_memory()
+    dyh = dy.cpu().pin_memory()
+    yh = torch.empty_like(xh).pin_memory()
+    dxh = torch.empty_like(xh).pin_memory()
+    xd, dyd = torch.empty_like(x), torch.empty_like(dy)
+    for _ in range(2):
+        layer.train_step_host(xh, dyh, yh, dxh, xd, dyd)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        layer.train_step_host(xh, dyh, yh, dxh, xd, dyd)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / args.steps, dev)
+    nbytes = x.numel() * 2
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD} layer step", "T": cfg.T, "H": cfg.H, "E": cfg.E,
+                   "k": cfg.k, "I": cfg.I, "active": cfg.K, "router": "fp32",
+                   "optimizer": "SparseAdam (experts at the active set, router dense)",
+                   "parallelism": f"replicas x{ws}",
+                   "l2": "inputs larger than L2 (1.2 GB of expert weights per step)"},
+        "step_roofline": {"ms": step_roof_ms, "frac": step_roof_ms / ms,
+                          "algorithmic_gflop": fl / 1e9, "algorithmic_gb": by / 1e9},
+        "roofline": roof,
+        "kernels": [{"name": n, "launches": l, "ms": t, "share": t / tot} for n, l, t in trace],
+        "importance_pass": importance,
+        "e2e": {"value": ws * cfg.T / (e2e_ms / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": 2 * nbytes, "d2h_bytes_per_step": 2 * nbytes,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": int(launches) * args.steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        tokens = args.cpu_tokens
+        a = act.cpu().numpy()
+        p0 = master_values(inp, a, cfg.N_gu)
+        del layer, wgu, wd
+        inp = {k: v.astype(np.float64) for k, v in inp.items()}  # exact upcast of bf16 values
+        t = oracle_step_sample(cfg, inp, a, p0, tokens)
+        line["cpu_baseline"] = {"value": tokens / t, "unit": "tokens/s", "cores": cpu_threads(),
+                                "kind": "oracle",
+                                "sample": f"one step on the first {tokens} of {cfg.T} tokens"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-tokens", type=int, default=512)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -215,6 +215,26 @@ usaf_status usaf_rigl_swap(const float* g, int64_t N, const int64_t* act_idx, in
                            float* v_out, int64_t* n_swapped, uint32_t* dev_status, void* ws,
                            size_t ws_bytes, void* stream);
 
+/* ---------------------------------------------------------------------------------------------
+ * Kernel timing trace (host side, off by default). While enabled, every kernel launch of the hot
+ * path is bracketed by two CUDA events recorded on its stream, so per-kernel device time can be
+ * read without a profiler. usaf_trace_enable(1) clears earlier records; usaf_trace_summary
+ * waits for the recorded events, then fills up to `cap` entries (one per kernel name, in order
+ * of first launch) and returns how many names were seen, or -1 on a CUDA error.
+ * ------------------------------------------------------------------------------------------- */
+typedef struct {
+  char name[48];
+  int64_t launches;
+  double total_ms;
+} usaf_trace_entry;
+
+usaf_status usaf_trace_enable(int on);
+int usaf_trace_summary(usaf_trace_entry* out, int cap);
+
+/* Number of kernel launches the library has issued since it was loaded (all threads). A caller
+ * can difference two readings to count the device work behind a sequence of calls. */
+int64_t usaf_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -1,0 +1,326 @@
+// The extern "C" entry points declared in include/usaf.h: argument checks, workspace carving,
+// and the launch sequence of each call. Everything here is host code; the arithmetic is in the
+// kernel files.
+#include <atomic>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace usaf {
+
+int device_sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();  // clear the sticky-free error of a machine without a GPU
+    return 152;
+  }
+  return n;
+}
+
+// ------------------------------------------------------------------ kernel timing trace
+namespace {
+struct TraceRec {
+  std::string name;
+  cudaEvent_t a, b;
+};
+std::atomic<bool> g_trace{false};
+std::mutex g_trace_mu;
+std::vector<TraceRec> g_recs;
+std::vector<cudaEvent_t> g_pool;
+thread_local std::vector<size_t> t_open;
+
+cudaEvent_t pool_event() {
+  if (!g_pool.empty()) {
+    cudaEvent_t e = g_pool.back();
+    g_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+void recycle_locked() {
+  for (auto& r : g_recs) {
+    g_pool.push_back(r.a);
+    g_pool.push_back(r.b);
+  }
+  g_recs.clear();
+}
+}  // namespace
+
+bool trace_on() { return g_trace.load(std::memory_order_relaxed); }
+
+static std::atomic<long long> g_launches{0};
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
+
+void trace_begin(const char* name, cudaStream_t st) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  TraceRec r{name, pool_event(), pool_event()};
+  cudaEventRecord(r.a, st);
+  t_open.push_back(g_recs.size());
+  g_recs.push_back(r);
+}
+
+void trace_end(cudaStream_t st) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  if (t_open.empty()) return;
+  const size_t i = t_open.back();
+  t_open.pop_back();
+  if (i < g_recs.size()) cudaEventRecord(g_recs[i].b, st);
+}
+
+void route_ws_layout(const usaf_moe_shape& s, Carver& c, RouteWs& w) {
+  w.logits = c.take<float>(s.T * s.E);
+  w.chunk_hist = c.take<int32_t>(ceil_div(s.T * s.k, PERM_CHUNK) * s.E);
+}
+
+static bool shape_ok(const usaf_moe_shape* s) {
+  if (!s) return false;
+  if (s->T < 1 || s->H < 1 || s->E < 1 || s->k < 1 || s->I < 1) return false;
+  if (s->k > s->E || s->E > 1024 || s->k > 32) return false;
+  if (s->T * s->k >= (int64_t(1) << 31) - 65536) return false;
+  if (s->E * 3 * s->I * s->H >= (int64_t(1) << 40)) return false;
+  return true;
+}
+
+static bool routing_ok(const usaf_routing* r) {
+  return r && r->topk_idx && r->topk_w && r->expert_count && r->expert_offset && r->perm_tok &&
+         r->perm_slot && r->slot_row;
+}
+
+static bool dtype_ok(usaf_dtype d) { return d == USAF_F32 || d == USAF_BF16; }
+
+}  // namespace usaf
+
+using namespace usaf;
+
+extern "C" {
+
+int usaf_abi_version(void) { return USAF_ABI_VERSION; }
+
+int64_t usaf_launch_count(void) { return (int64_t)g_launches.load(); }
+
+usaf_status usaf_trace_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  recycle_locked();
+  t_open.clear();
+  g_trace.store(on != 0);
+  return USAF_OK;
+}
+
+int usaf_trace_summary(usaf_trace_entry* out, int cap) {
+  std::lock_guard<std::mutex> lk(g_trace_mu);
+  std::vector<std::string> names;
+  std::vector<int64_t> cnt;
+  std::vector<double> ms;
+  for (auto& r : g_recs) {
+    if (cudaEventSynchronize(r.b) != cudaSuccess) return -1;
+    float t = 0.f;
+    if (cudaEventElapsedTime(&t, r.a, r.b) != cudaSuccess) return -1;
+    size_t k = 0;
+    while (k < names.size() && names[k] != r.name) ++k;
+    if (k == names.size()) {
+      names.push_back(r.name);
+      cnt.push_back(0);
+      ms.push_back(0.0);
+    }
+    cnt[k] += 1;
+    ms[k] += t;
+  }
+  for (size_t k = 0; k < names.size() && (int)k < cap && out; ++k) {
+    std::memset(out[k].name, 0, sizeof(out[k].name));
+    std::strncpy(out[k].name, names[k].c_str(), sizeof(out[k].name) - 1);
+    out[k].launches = cnt[k];
+    out[k].total_ms = ms[k];
+  }
+  return (int)names.size();
+}
+
+const char* usaf_status_string(usaf_status s) {
+  switch (s) {
+    case USAF_OK: return "ok";
+    case USAF_ERR_INVALID_ARG: return "invalid argument";
+    case USAF_ERR_UNSUPPORTED: return "unsupported shape or type";
+    case USAF_ERR_WORKSPACE: return "workspace missing or too small";
+    case USAF_ERR_CUDA: return "CUDA error";
+    case USAF_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+int64_t usaf_routed_rows_capacity(const usaf_moe_shape* s) {
+  if (!shape_ok(s)) return -1;
+  return round_up(s->T * s->k + s->E * (USAF_ROW_ALIGN - 1), 256) + 256;
+}
+
+size_t usaf_route_topk_workspace_size(const usaf_moe_shape* s) {
+  if (!shape_ok(s)) return 0;
+  Carver c(nullptr);
+  RouteWs w;
+  route_ws_layout(*s, c, w);
+  return c.size();
+}
+
+usaf_status usaf_route_topk(const usaf_moe_shape* s, const void* x, usaf_dtype x_dtype,
+                            const float* w_router, const float* logits_in, float* logits_out,
+                            int renorm, const usaf_routing* rt, void* ws, size_t ws_bytes,
+                            void* stream) {
+  if (!shape_ok(s) || !routing_ok(rt)) return USAF_ERR_INVALID_ARG;
+  if (!logits_in && (!x || !w_router || !dtype_ok(x_dtype))) return USAF_ERR_INVALID_ARG;
+  if (renorm != 0 && renorm != 1) return USAF_ERR_INVALID_ARG;
+  const size_t need = usaf_route_topk_workspace_size(s);
+  if (!ws || ws_bytes < need) return USAF_ERR_WORKSPACE;
+  Carver c(ws);
+  RouteWs w;
+  route_ws_layout(*s, c, w);
+  return route_launch(*s, x, x_dtype, w_router, logits_in, logits_out, renorm, *rt, w,
+                      static_cast<cudaStream_t>(stream));
+}
+
+size_t usaf_moe_fwd_workspace_size(const usaf_moe_shape* s, usaf_dtype dt) {
+  if (!shape_ok(s) || !dtype_ok(dt)) return 0;
+  Carver c(nullptr);
+  FwdWs w;
+  fwd_ws_layout(*s, dt, c, w);
+  return c.size();
+}
+
+static usaf_status fill_args(MoeArgs& a, const usaf_moe_shape* s, usaf_dtype dt, const void* x,
+                             const float* wr, const void* wgu, const void* wd,
+                             const usaf_routing* rt) {
+  if (!shape_ok(s) || !dtype_ok(dt) || !routing_ok(rt) || !x || !wgu || !wd)
+    return USAF_ERR_INVALID_ARG;
+  if (dt == USAF_BF16 && !tc_shape_ok(*s)) return USAF_ERR_UNSUPPORTED;
+  a.s = *s;
+  a.dt = dt;
+  a.R_cap = usaf_routed_rows_capacity(s);
+  a.x = x;
+  a.w_router = wr;
+  a.w_gate_up = wgu;
+  a.w_down = wd;
+  a.rt = *rt;
+  return USAF_OK;
+}
+
+usaf_status usaf_moe_fwd(const usaf_moe_shape* s, usaf_dtype dt, const void* x,
+                         const void* w_gate_up, const void* w_down, const usaf_routing* rt,
+                         void* x_perm_save, void* h_save, void* wa_save, void* y, void* ws,
+                         size_t ws_bytes, void* stream) {
+  MoeArgs a;
+  USAF_TRY(fill_args(a, s, dt, x, nullptr, w_gate_up, w_down, rt));
+  if (!x_perm_save || !h_save || !wa_save || !y) return USAF_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < usaf_moe_fwd_workspace_size(s, dt)) return USAF_ERR_WORKSPACE;
+  Carver c(ws);
+  FwdWs w;
+  fwd_ws_layout(*s, dt, c, w);
+  return moe_fwd_launch(a, x_perm_save, h_save, wa_save, y, w,
+                        static_cast<cudaStream_t>(stream));
+}
+
+size_t usaf_moe_bwd_workspace_size(const usaf_moe_shape* s, usaf_dtype dt, int64_t K) {
+  if (!shape_ok(s) || !dtype_ok(dt) || K < 0) return 0;
+  Carver c(nullptr);
+  BwdWs w;
+  bwd_ws_layout(*s, dt, K, c, w);
+  return c.size();
+}
+
+usaf_status usaf_moe_bwd_sparse(const usaf_moe_shape* s, usaf_dtype dt, int renorm,
+                                const void* x, const float* w_router, const void* w_gate_up,
+                                const void* w_down, const usaf_routing* rt, const float* logits,
+                                const void* x_perm_save, const void* h_save, const void* wa_save,
+                                const void* dy, const int64_t* act_idx, int64_t K, float* g_act,
+                                float* g_router, void* dx, float* dw_slot, uint32_t* dev_status,
+                                void* ws, size_t ws_bytes, void* stream) {
+  MoeArgs a;
+  USAF_TRY(fill_args(a, s, dt, x, w_router, w_gate_up, w_down, rt));
+  if (renorm != 0 && renorm != 1) return USAF_ERR_INVALID_ARG;
+  if (!w_router || !x_perm_save || !h_save || !wa_save || !dy || !g_router)
+    return USAF_ERR_INVALID_ARG;
+  if (renorm == 0 && !logits) return USAF_ERR_INVALID_ARG;
+  const int64_t N = s->E * 3 * s->I * s->H;
+  if (K < 0 || K > N || (K > 0 && (!act_idx || !g_act))) return USAF_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < usaf_moe_bwd_workspace_size(s, dt, K)) return USAF_ERR_WORKSPACE;
+  Carver c(ws);
+  BwdWs w;
+  bwd_ws_layout(*s, dt, K, c, w);
+  return moe_bwd_launch(a, renorm, logits, x_perm_save, h_save, wa_save, dy, act_idx, K, g_act,
+                        g_router, dx, dw_slot, dev_status, w, static_cast<cudaStream_t>(stream));
+}
+
+usaf_status usaf_sparse_adam_step(int64_t n, const int64_t* idx, const float* g, float* p,
+                                  float* m, float* v, void* w_seg0, int64_t n_seg0, void* w_seg1,
+                                  usaf_dtype w_dtype, float lr, float beta1, float beta2,
+                                  float eps, int64_t step, int skip_if_nonfinite,
+                                  uint32_t* dev_status, void* stream) {
+  if (n < 0 || step < 1 || !dtype_ok(w_dtype) || n_seg0 < 0) return USAF_ERR_INVALID_ARG;
+  if (n > 0 && (!g || !p || !m || !v || !w_seg0)) return USAF_ERR_INVALID_ARG;
+  if (!idx && n > n_seg0) return USAF_ERR_INVALID_ARG;
+  if (skip_if_nonfinite && !dev_status) return USAF_ERR_INVALID_ARG;
+  if (!(beta1 >= 0.f && beta1 < 1.f && beta2 >= 0.f && beta2 < 1.f && eps >= 0.f))
+    return USAF_ERR_INVALID_ARG;
+  return adam_launch(n, idx, g, p, m, v, w_seg0, n_seg0, w_seg1, w_dtype, lr, beta1, beta2, eps,
+                     step, skip_if_nonfinite, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+size_t usaf_importance_select_workspace_size(int64_t N, int64_t K) {
+  if (N < 1 || K < 1 || K > N || N >= (int64_t(1) << 32)) return 0;
+  return select_ws_bytes(N, K, false);
+}
+
+usaf_status usaf_importance_select(const float* g, int64_t N, int64_t K, int64_t* out_idx,
+                                   uint32_t* dev_status, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  if (!g || !out_idx || N < 1 || K < 1 || K > N) return USAF_ERR_INVALID_ARG;
+  if (N >= (int64_t(1) << 32)) return USAF_ERR_UNSUPPORTED;
+  if (!ws || ws_bytes < usaf_importance_select_workspace_size(N, K)) return USAF_ERR_WORKSPACE;
+  return importance_select_launch(g, N, K, out_idx, dev_status, ws,
+                                  static_cast<cudaStream_t>(stream));
+}
+
+size_t usaf_rigl_swap_workspace_size(int64_t N, int64_t K, int64_t D) {
+  if (N < 1 || K < 0 || K > N || D < 0 || D > K || D > N - K || N >= (int64_t(1) << 32))
+    return 0;
+  return rigl_ws_bytes(N, K, D);
+}
+
+static bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  if (!a || !b || na == 0 || nb == 0) return false;
+  const char* pa = static_cast<const char*>(a);
+  const char* pb = static_cast<const char*>(b);
+  return pa < pb + nb && pb < pa + na;
+}
+
+usaf_status usaf_rigl_swap(const float* g, int64_t N, const int64_t* act_idx, int64_t K,
+                           int64_t D, const float* p_in, const float* m_in, const float* v_in,
+                           const void* w_seg0, int64_t n_seg0, const void* w_seg1,
+                           usaf_dtype w_dtype, int64_t* new_idx, float* p_out, float* m_out,
+                           float* v_out, int64_t* n_swapped, uint32_t* dev_status, void* ws,
+                           size_t ws_bytes, void* stream) {
+  if (!g || N < 1 || K < 0 || K > N || D < 0 || D > K || D > N - K || !n_swapped)
+    return USAF_ERR_INVALID_ARG;
+  if (!dtype_ok(w_dtype) || n_seg0 < 0) return USAF_ERR_INVALID_ARG;
+  if (K > 0 && (!act_idx || !p_in || !m_in || !v_in || !new_idx || !p_out || !m_out || !v_out))
+    return USAF_ERR_INVALID_ARG;
+  if (D > 0 && (!w_seg0 || (N > n_seg0 && !w_seg1))) return USAF_ERR_INVALID_ARG;
+  if (N >= (int64_t(1) << 32)) return USAF_ERR_UNSUPPORTED;
+  const size_t kb = size_t(K) * 4;
+  const void* ins[4] = {p_in, m_in, v_in, act_idx};
+  const size_t insz[4] = {kb, kb, kb, size_t(K) * 8};
+  const void* outs[4] = {p_out, m_out, v_out, new_idx};
+  const size_t outsz[4] = {kb, kb, kb, size_t(K) * 8};
+  for (int i = 0; i < 4; ++i)
+    for (int j = 0; j < 4; ++j)
+      if (overlaps(ins[i], insz[i], outs[j], outsz[j])) return USAF_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < usaf_rigl_swap_workspace_size(N, K, D)) return USAF_ERR_WORKSPACE;
+  return rigl_launch(g, N, act_idx, K, D, p_in, m_in, v_in, w_seg0, n_seg0, w_seg1, w_dtype,
+                     new_idx, p_out, m_out, v_out, n_swapped, dev_status, ws,
+                     static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

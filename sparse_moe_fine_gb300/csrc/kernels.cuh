@@ -1,0 +1,89 @@
+// Internal launch interfaces between the ABI layer and the kernel files.
+#pragma once
+
+#include "common.cuh"
+
+namespace usaf {
+
+constexpr int PERM_CHUNK = 1024;
+
+// ---------------------------------------------------------------- routing
+struct RouteWs {
+  float* logits;        // [T,E] when the caller gives no logits_out
+  int32_t* chunk_hist;  // [nchunks, E]
+};
+void route_ws_layout(const usaf_moe_shape& s, Carver& c, RouteWs& w);
+usaf_status route_launch(const usaf_moe_shape& s, const void* x, usaf_dtype xdt, const float* wr,
+                         const float* logits_in, float* logits_out, int renorm,
+                         const usaf_routing& rt, RouteWs& w, cudaStream_t st);
+
+// ---------------------------------------------------------------- expert forward / backward
+struct FwdWs {
+  float* y_acc;  // [T,H] fp32 accumulator of the routing-weighted combine
+  int32_t* plan; // [E+1] prefix of token tiles per expert (tensor-core path)
+};
+struct BwdWs {
+  float* dw;          // [T*k] when the caller gives no dw_slot
+  float* dl;          // [T*k] dlogit at the selected experts (renorm = 1)
+  float* dlogit;      // [T,E] dense dlogit (renorm = 0)
+  void* dh;           // [R_cap, 2I] of dtype
+  float* dx_acc;      // [T,H]
+  float* gvec;        // [R_cap, I] (fp32 path only)
+  int32_t* row_ptr;   // [E*2I + E*H + 1] first active of each weight row (tensor-core path)
+  int32_t* plan;      // [E+1] prefix of token tiles per expert (tensor-core path)
+  void* dy_perm;      // [R_cap, H] dy rows in permuted order (tensor-core path)
+};
+void fwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, Carver& c, FwdWs& w);
+void bwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, int64_t K, Carver& c, BwdWs& w);
+
+struct MoeArgs {
+  usaf_moe_shape s;
+  usaf_dtype dt;
+  int64_t R_cap;
+  const void* x;
+  const float* w_router;
+  const void* w_gate_up;
+  const void* w_down;
+  usaf_routing rt;
+  int32_t* plan;  // token-tile prefix written by tc_plan (tensor-core path)
+};
+
+usaf_status moe_fwd_launch(const MoeArgs& a, void* x_perm, void* h, void* wa, void* y, FwdWs& w,
+                           cudaStream_t st);
+usaf_status moe_bwd_launch(const MoeArgs& a, int renorm, const float* logits, const void* x_perm,
+                           const void* h, const void* wa, const void* dy, const int64_t* act_idx,
+                           int64_t K, float* g_act, float* g_router, void* dx, float* dw_slot,
+                           uint32_t* dev_status, BwdWs& w, cudaStream_t st);
+
+// tensor-core (tcgen05) grouped GEMM stages, bf16 only
+bool tc_shape_ok(const usaf_moe_shape& s);
+usaf_status tc_plan(const MoeArgs& a, cudaStream_t st);
+usaf_status tc_fwd_gate_up(const MoeArgs& a, const void* x_perm, void* h, void* wa,
+                           cudaStream_t st);
+usaf_status tc_fwd_down(const MoeArgs& a, const void* wa, float* y_acc, cudaStream_t st);
+usaf_status tc_bwd_gvec(const MoeArgs& a, const void* dy_perm, const void* h, void* dh,
+                        float* dw, cudaStream_t st);
+usaf_status tc_bwd_dx(const MoeArgs& a, const void* dh, float* dx_acc, cudaStream_t st);
+usaf_status tc_bwd_wgrad(const MoeArgs& a, const void* x_perm, const void* dy_perm, const void* dh,
+                         const void* wa, const int64_t* act_idx, int64_t K,
+                         const int32_t* row_ptr, float* g_act, uint32_t* dev_status,
+                         cudaStream_t st);
+
+// ---------------------------------------------------------------- optimizer
+usaf_status adam_launch(int64_t n, const int64_t* idx, const float* g, float* p, float* m,
+                        float* v, void* w0, int64_t n0, void* w1, usaf_dtype wdt, float lr,
+                        float b1, float b2, float eps, int64_t step, int skip,
+                        uint32_t* dev_status, cudaStream_t st);
+
+// ---------------------------------------------------------------- selection / RigL
+size_t select_ws_bytes(int64_t N, int64_t K, bool with_bitmap);
+usaf_status importance_select_launch(const float* g, int64_t N, int64_t K, int64_t* out_idx,
+                                     uint32_t* dev_status, void* ws, cudaStream_t st);
+size_t rigl_ws_bytes(int64_t N, int64_t K, int64_t D);
+usaf_status rigl_launch(const float* g, int64_t N, const int64_t* act_idx, int64_t K, int64_t D,
+                        const float* p_in, const float* m_in, const float* v_in, const void* w0,
+                        int64_t n0, const void* w1, usaf_dtype wdt, int64_t* new_idx,
+                        float* p_out, float* m_out, float* v_out, int64_t* n_swapped,
+                        uint32_t* dev_status, void* ws, cudaStream_t st);
+
+}  // namespace usaf

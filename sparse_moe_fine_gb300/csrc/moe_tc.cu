@@ -1,0 +1,741 @@
+// bf16 grouped expert GEMMs on 5th-generation tensor cores (tcgen05.mma, accumulators in TMEM),
+// fed by TMA (cp.async.bulk.tensor) through a 4-stage mbarrier pipeline. One persistent CTA per SM
+// with three roles: warp 0 issues TMA loads, warp 1 issues MMAs (one thread) and owns the TMEM
+// allocation, warps 2-5 run the fused epilogue out of a double-buffered TMEM accumulator.
+//
+// Every GEMM is arranged with the weight dimension as M (128 rows per tile) and the routed
+// tokens as N (16..256 per tile) or as K, so each expert's ragged token count only pads to 16.
+//   S4 gate_up: h^T = gate_up[e] x_perm^T   A = gate/up rows interleaved (K-major), B = x rows
+//               epilogue: SwiGLU (act(gate)*up, experts4bit-qlora epilogue contract), scaled by
+//               the routing weight; writes h and w*A
+//   S5 down:    y^T = down[e] (wA)^T         epilogue: scatter-add into the fp32 combine buffer
+//   S6 gvec:    g^T = down[e]^T dy_perm^T    A = down[e] MN-major; epilogue: SwiGLU backward,
+//               dw (routing-weight gradient), dh
+//   S8 dx:      dx^T = gate_up[e]^T dh^T     A = gate_up[e] MN-major; epilogue: scatter-add
+//   S9/S10 masked wgrad: dW = dh^T x_perm and dy_perm^T (wA) per expert, tokens as K, both
+//               operands MN-major; the epilogue keeps only the active entries (USAF README:
+//               only the selected 0.5% of expert weights are trained).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace usaf {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int BN = 256;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;
+constexpr int B_BYTES = BN * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 192;
+constexpr int TMEM_COLS = 512;
+constexpr int MAX_E = 1024;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + 2 * (MAX_E + 1) * 4;
+constexpr long long TIMEOUT_CYCLES = 1ll << 32;  // about two seconds
+
+enum Var { V_GATEUP = 0, V_DOWN = 1, V_GVEC = 2, V_DX = 3, V_WG_GU = 4, V_WG_D = 5 };
+
+struct Params {
+  const int32_t* cnt;
+  const int32_t* off;
+  const int32_t* ptok;
+  const int32_t* pslot;
+  const float* topk_w;
+  const int32_t* plan;
+  int E, H, I;
+  int MT, NT;
+  __nv_bfloat16* h;
+  __nv_bfloat16* wa;
+  float* acc_out;  // y_acc (S5) or dx_acc (S8)
+  float* dw;
+  __nv_bfloat16* dh;
+  const __nv_bfloat16* hin;
+  const int64_t* act;
+  const int32_t* row_ptr;
+  float* g_act;
+  int64_t Ngu;
+  uint32_t* status;
+};
+
+// ---------------------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false when the phase did not complete within the limit or another role gave up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > TIMEOUT_CYCLES) return false;
+  }
+}
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                       int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
+                                       int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void umma_bf16(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+      "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+      "%30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor: 128-byte swizzle, start address, LBO and SBO in bytes.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFF) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFF) << 32;
+  d |= (uint64_t)1 << 46;  // descriptor version of this architecture
+  d |= (uint64_t)2 << 61;  // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 accumulate, M = 128.
+__device__ __forceinline__ uint32_t idesc_bf16(int n, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+// ---------------------------------------------------------------------------- tiles
+struct Tile {
+  int live;
+  int e;
+  int m0;     // first M row of the tile (feature / weight row)
+  int row0;   // first permuted row (token tiles) or the expert's first row (wgrad K base)
+  int nrows;  // tokens in a token tile (multiple of 16)
+  int n0;     // first N column (wgrad)
+  int klen;   // K extent
+};
+
+template <int VAR>
+struct VarTraits {
+  static constexpr bool token_tiled = VAR <= V_DX;
+  static constexpr bool a_mn = VAR >= V_GVEC;
+  static constexpr bool b_mn = VAR >= V_WG_GU;
+};
+
+__device__ __forceinline__ int upper_bound_i32(const int32_t* a, int n, int v) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    int mid = (lo + hi) >> 1;
+    if (a[mid] <= v) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+template <int VAR>
+__device__ __forceinline__ Tile get_tile(const Params& p, const int32_t* s_plan,
+                                         const int32_t* s_off, int t) {
+  Tile ti{};
+  if constexpr (VarTraits<VAR>::token_tiled) {
+    const int e = upper_bound_i32(s_plan, p.E + 1, t / p.MT) - 1;
+    const int nts = s_plan[e + 1] - s_plan[e];
+    const int local = t - p.MT * s_plan[e];
+    const int mt = local / nts, nt = local % nts;
+    const int npad = s_off[e + 1] - s_off[e];
+    const int base = ((npad + nts - 1) / nts + 15) / 16 * 16;
+    ti.live = 1;
+    ti.e = e;
+    ti.m0 = mt * (VAR == V_GATEUP ? 64 : BM);
+    ti.row0 = s_off[e] + nt * base;
+    ti.nrows = min(base, npad - nt * base);
+    ti.n0 = 0;
+    ti.klen = (VAR == V_GATEUP || VAR == V_GVEC) ? p.H : (VAR == V_DOWN ? p.I : 2 * p.I);
+  } else {
+    const int per = p.MT * p.NT;
+    const int e = t / per, local = t % per;
+    const int npad = s_off[e + 1] - s_off[e];
+    ti.live = npad > 0;
+    ti.e = e;
+    ti.m0 = (local / p.NT) * BM;
+    ti.n0 = (local % p.NT) * BN;
+    ti.row0 = s_off[e];
+    ti.nrows = BN;
+    ti.klen = npad;
+  }
+  return ti;
+}
+
+template <int VAR>
+__device__ __forceinline__ int total_tiles(const Params& p, const int32_t* s_plan) {
+  if constexpr (VarTraits<VAR>::token_tiled) return p.MT * s_plan[p.E];
+  else return p.E * p.MT * p.NT;
+}
+
+// ---------------------------------------------------------------------------- epilogues
+__device__ __forceinline__ float pick32(const float (&v)[32], int j) {
+  float r = v[0];
+#pragma unroll
+  for (int q = 1; q < 32; ++q) r = (j == q) ? v[q] : r;
+  return r;
+}
+
+template <int VAR>
+__device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32_t taddr, int row,
+                                         int lane) {
+  constexpr unsigned FULL = 0xffffffffu;
+  const int H = p.H, I = p.I;
+  if constexpr (VarTraits<VAR>::token_tiled) {
+    const int nch = (ti.nrows + 31) / 32;
+    for (int ch = 0; ch < nch; ++ch) {
+      float v[32];
+      tmem_ld32(taddr + ch * 32, v);
+      const int cbase = ch * 32;
+      const int col = cbase + lane;
+      int slot = -1, tok = 0;
+      if (col < ti.nrows) {
+        slot = p.pslot[ti.row0 + col];
+        tok = p.ptok[ti.row0 + col];
+      }
+      const float wl = slot >= 0 ? p.topk_w[slot] : 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        if (cbase + j >= ti.nrows) break;
+        const int64_t r = ti.row0 + cbase + j;
+        const int sj = __shfl_sync(FULL, slot, j);
+        if constexpr (VAR == V_GATEUP) {
+          const int i = ti.m0 + (row >> 1);
+          const int g = row & 1;
+          const float mine = v[j];
+          const float other = __shfl_xor_sync(FULL, mine, 1);
+          const float wj = __shfl_sync(FULL, wl, j);
+          p.h[r * 2 * I + g * I + i] = __float2bfloat16_rn(mine);
+          if (g == 0) p.wa[r * I + i] = __float2bfloat16_rn(wj * silu_f(mine) * other);
+        } else if constexpr (VAR == V_DOWN || VAR == V_DX) {
+          const int tj = __shfl_sync(FULL, tok, j);
+          const int hh = ti.m0 + row;
+          if (sj >= 0 && hh < H) atomicAdd(&p.acc_out[(int64_t)tj * H + hh], v[j]);
+        } else {  // V_GVEC
+          const int i = ti.m0 + row;
+          const bool iv = i < I;
+          const float wj = __shfl_sync(FULL, wl, j);
+          float gt = 0.f, ut = 0.f;
+          if (iv) {
+            gt = __bfloat162float(p.hin[r * 2 * I + i]);
+            ut = __bfloat162float(p.hin[r * 2 * I + I + i]);
+          }
+          const float gv = v[j];
+          const float sg = silu_f(gt);
+          float part = iv ? gv * sg * ut : 0.f;
+#pragma unroll
+          for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(FULL, part, o);
+          if (lane == 0 && sj >= 0) atomicAdd(&p.dw[sj], part);
+          if (iv) {
+            const float dA = wj * gv;
+            p.dh[r * 2 * I + i] = __float2bfloat16_rn(dA * ut * silu_grad_f(gt));
+            p.dh[r * 2 * I + I + i] = __float2bfloat16_rn(dA * sg);
+          }
+        }
+      }
+    }
+  } else {
+    // masked weight gradient: keep the active entries of this row inside the tile's columns
+    const bool gu = VAR == V_WG_GU;
+    const int mrows = gu ? 2 * I : H;
+    const int ncols = gu ? H : I;
+    const int j = ti.m0 + row;
+    const bool rv = j < mrows;
+    const int64_t rid = gu ? (int64_t)ti.e * 2 * I + j : (int64_t)p.E * 2 * I + (int64_t)ti.e * H + j;
+    const int64_t base = gu ? rid * H : p.Ngu + ((int64_t)ti.e * H + j) * I;
+    int64_t cur = 0, end = 0;
+    if (rv) {
+      cur = p.row_ptr[rid];
+      end = p.row_ptr[rid + 1];
+      while (cur < end && p.act[cur] - base < ti.n0) ++cur;
+    }
+    const int nvalid = min(BN, ncols - ti.n0);
+    const int nch = (nvalid + 31) / 32;
+    bool bad = false;
+    for (int ch = 0; ch < nch; ++ch) {
+      float v[32];
+      tmem_ld32(taddr + ch * 32, v);
+      const int64_t lo = ti.n0 + ch * 32;
+      while (cur < end) {
+        const int64_t c = p.act[cur] - base;
+        if (c >= lo + 32) break;
+        const float val = pick32(v, (int)(c - lo));
+        p.g_act[cur] = val;
+        bad |= !isfinite(val);
+        ++cur;
+      }
+    }
+    if (bad) flag_status(p.status, USAF_DEV_NONFINITE);
+  }
+}
+
+// ---------------------------------------------------------------------------- the kernel
+template <int VAR>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain[1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int32_t* s_plan = reinterpret_cast<int32_t*>(smem + STAGES * STAGE_BYTES + 256);
+  int32_t* s_off = s_plan + (MAX_E + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES;
+  const uint32_t tfull0 = empty0 + 8 * STAGES, tempty0 = tfull0 + 16, drain = tempty0 + 16;
+
+  for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
+    s_off[i] = p.off[i];
+    if (VarTraits<VAR>::token_tiled) s_plan[i] = p.plan[i];
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = total_tiles<VAR>(p, s_plan);
+  bool failed = false;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0;
+      for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
+        const Tile ti = get_tile<VAR>(p, s_plan, s_off, t);
+        if (!ti.live) continue;
+        const int nkb = (ti.klen + BK - 1) / BK;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) {
+            failed = true;
+            break;
+          }
+          const uint32_t a_dst = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t b_dst = a_dst + A_BYTES;
+          const uint32_t fb = full0 + 8 * stage;
+          const int k0 = kb * BK;
+          uint32_t bytes = A_BYTES;
+          if constexpr (VarTraits<VAR>::token_tiled) bytes += (ti.nrows > 128 ? 2 : 1) * 16384;
+          else bytes += B_BYTES;
+          mbar_expect_tx(fb, bytes);
+          if constexpr (VAR == V_GATEUP) {
+            tma_4d(a_dst, &tmA, fb, k0, 0, ti.m0, ti.e);
+          } else if constexpr (VAR == V_DOWN) {
+            tma_2d(a_dst, &tmA, fb, k0, ti.e * p.H + ti.m0);
+          } else if constexpr (VAR == V_GVEC) {
+            tma_2d(a_dst, &tmA, fb, ti.m0, ti.e * p.H + k0);
+            tma_2d(a_dst + 8192, &tmA, fb, ti.m0 + 64, ti.e * p.H + k0);
+          } else if constexpr (VAR == V_DX) {
+            tma_2d(a_dst, &tmA, fb, ti.m0, ti.e * 2 * p.I + k0);
+            tma_2d(a_dst + 8192, &tmA, fb, ti.m0 + 64, ti.e * 2 * p.I + k0);
+          } else {
+            tma_2d(a_dst, &tmA, fb, ti.m0, ti.row0 + k0);
+            tma_2d(a_dst + 8192, &tmA, fb, ti.m0 + 64, ti.row0 + k0);
+          }
+          if constexpr (VarTraits<VAR>::token_tiled) {
+            tma_2d(b_dst, &tmB, fb, k0, ti.row0);
+            if (ti.nrows > 128) tma_2d(b_dst + 16384, &tmB, fb, k0, ti.row0 + 128);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) tma_2d(b_dst + q * 8192, &tmB, fb, ti.n0 + 64 * q, ti.row0 + k0);
+          }
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (failed) {
+        *abort_flag = 1;
+        flag_status(p.status, USAF_DEV_TIMEOUT);
+      }
+      // let every issued copy land before the CTA can exit
+      for (int s = 0; s < STAGES && (uint32_t)s < issued; ++s) {
+        // the last fill of stage s was fill number (issued - 1 - ((issued - 1 - s) % STAGES))
+        const uint32_t last = issued - 1 - ((issued - 1 - s) % STAGES);
+        mbar_wait(full0 + 8 * s, (last / STAGES) & 1, abort_flag);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      const uint32_t a_step = VarTraits<VAR>::a_mn ? 2048 : 32;
+      const uint32_t b_step = VarTraits<VAR>::b_mn ? 2048 : 32;
+      const uint32_t a_lbo = VarTraits<VAR>::a_mn ? 8192 : 16;
+      const uint32_t b_lbo = VarTraits<VAR>::b_mn ? 8192 : 16;
+      for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
+        const Tile ti = get_tile<VAR>(p, s_plan, s_off, t);
+        if (!ti.live) continue;
+        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * BN;
+        const int n_mma = VarTraits<VAR>::token_tiled ? ti.nrows : BN;
+        const uint32_t idesc = idesc_bf16(n_mma, VarTraits<VAR>::a_mn, VarTraits<VAR>::b_mn);
+        const int nkb = (ti.klen + BK - 1) / BK;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t b_base = a_base + A_BYTES;
+          const int ksteps = min(BK, ti.klen - kb * BK) / 16;
+          for (int ks = 0; ks < ksteps; ++ks) {
+            const uint64_t ad = sdesc(a_base + ks * a_step, a_lbo, 1024);
+            const uint64_t bd = sdesc(b_base + ks * b_step, b_lbo, 1024);
+            umma_bf16(d, ad, bd, idesc, (kb | ks) != 0 ? 1u : 0u);
+          }
+          umma_commit(empty0 + 8 * stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (failed) break;
+        umma_commit(tfull0 + 8 * acc);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      if (failed) {
+        *abort_flag = 1;
+        flag_status(p.status, USAF_DEV_TIMEOUT);
+      }
+      // wait for every MMA this thread issued before TMEM is released
+      umma_commit(drain);
+      mbar_wait(drain, 0, abort_flag);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue warps 2..5
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const Tile ti = get_tile<VAR>(p, s_plan, s_off, t);
+      if (!ti.live) continue;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      epilogue<VAR>(p, ti, tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN, row, lane);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------- plan kernel
+// Token tiles per expert: ceil(padded rows / 256), exclusive prefix over experts (E <= 1024).
+__global__ void __launch_bounds__(1024) token_plan_kernel(const int32_t* __restrict__ off, int E,
+                                                          int32_t* __restrict__ plan) {
+  __shared__ int32_t wsum[32];
+  const int e = threadIdx.x, lane = e & 31, wid = e >> 5;
+  int32_t n = 0;
+  if (e < E) n = (off[e + 1] - off[e] + BN - 1) / BN;
+  int32_t v = n;
+  for (int o = 1; o < 32; o <<= 1) {
+    int32_t y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  if (lane == 31) wsum[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    int32_t w = wsum[lane];
+    for (int o = 1; o < 32; o <<= 1) {
+      int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    wsum[lane] = w;
+  }
+  __syncthreads();
+  const int32_t incl = v + (wid > 0 ? wsum[wid - 1] : 0);
+  if (e < E) plan[e] = incl - n;
+  if (e == E - 1) plan[E] = incl;
+}
+
+// ---------------------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+bool map_2d(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+            uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// gate_up_proj [E, 2I, H] viewed as (h, gate|up, i, e) so a 128-row box interleaves gate row i
+// and up row i (rows 2i and 2i+1 of the tile).
+bool map_gate_up_interleaved(CUtensorMap* m, const void* base, uint64_t E, uint64_t I,
+                             uint64_t H) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {H, 2, I, E};
+  cuuint64_t strides[3] = {I * H * 2, H * 2, 2 * I * H * 2};
+  cuuint32_t box[4] = {64, 2, 64, 1};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+            es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr const char* VAR_NAME[6] = {"tc_gate_up_swiglu", "tc_down_combine", "tc_gvec_swiglu_bwd",
+                                     "tc_dx", "tc_wgrad_gate_up", "tc_wgrad_down"};
+
+template <int VAR>
+usaf_status launch(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStream_t st) {
+  USAF_TRACE(VAR_NAME[VAR], st);
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(tc_gemm_kernel<VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SMEM_BYTES) != cudaSuccess)
+      return USAF_ERR_CUDA;
+    attr_done = true;
+  }
+  tc_gemm_kernel<VAR><<<device_sm_count(), NUM_THREADS, SMEM_BYTES, st>>>(a, b, p);
+  USAF_CHECK_LAUNCH();
+  return USAF_OK;
+}
+
+Params base_params(const MoeArgs& a) {
+  Params p{};
+  p.cnt = a.rt.expert_count;
+  p.off = a.rt.expert_offset;
+  p.ptok = a.rt.perm_tok;
+  p.pslot = a.rt.perm_slot;
+  p.topk_w = a.rt.topk_w;
+  p.plan = a.plan;
+  p.E = (int)a.s.E;
+  p.H = (int)a.s.H;
+  p.I = (int)a.s.I;
+  p.Ngu = a.s.E * 2 * a.s.I * a.s.H;
+  return p;
+}
+
+}  // namespace
+
+bool tc_shape_ok(const usaf_moe_shape& s) {
+  return s.H % 64 == 0 && s.I % 64 == 0 && s.E <= MAX_E && s.H <= (1 << 20) &&
+         s.I <= (1 << 20) && s.E * s.H < (int64_t(1) << 31) && s.E * 2 * s.I < (int64_t(1) << 31);
+}
+
+usaf_status tc_plan(const MoeArgs& a, cudaStream_t st) {
+  USAF_TRACE("tc_plan", st);
+  token_plan_kernel<<<1, 1024, 0, st>>>(a.rt.expert_offset, (int)a.s.E, a.plan);
+  USAF_CHECK_LAUNCH();
+  return USAF_OK;
+}
+
+usaf_status tc_fwd_gate_up(const MoeArgs& a, const void* x_perm, void* h, void* wa,
+                           cudaStream_t st) {
+  CUtensorMap ma, mb;
+  if (!map_gate_up_interleaved(&ma, a.w_gate_up, a.s.E, a.s.I, a.s.H) ||
+      !map_2d(&mb, x_perm, a.s.H, a.R_cap, 64, 128))
+    return USAF_ERR_CUDA;
+  Params p = base_params(a);
+  p.MT = (int)(a.s.I / 64);
+  p.h = static_cast<__nv_bfloat16*>(h);
+  p.wa = static_cast<__nv_bfloat16*>(wa);
+  return launch<V_GATEUP>(ma, mb, p, st);
+}
+
+usaf_status tc_fwd_down(const MoeArgs& a, const void* wa, float* y_acc, cudaStream_t st) {
+  CUtensorMap ma, mb;
+  if (!map_2d(&ma, a.w_down, a.s.I, a.s.E * a.s.H, 64, 128) ||
+      !map_2d(&mb, wa, a.s.I, a.R_cap, 64, 128))
+    return USAF_ERR_CUDA;
+  Params p = base_params(a);
+  p.MT = (int)ceil_div(a.s.H, BM);
+  p.acc_out = y_acc;
+  return launch<V_DOWN>(ma, mb, p, st);
+}
+
+usaf_status tc_bwd_gvec(const MoeArgs& a, const void* dy_perm, const void* h, void* dh,
+                        float* dw, cudaStream_t st) {
+  CUtensorMap ma, mb;
+  if (!map_2d(&ma, a.w_down, a.s.I, a.s.E * a.s.H, 64, 64) ||
+      !map_2d(&mb, dy_perm, a.s.H, a.R_cap, 64, 128))
+    return USAF_ERR_CUDA;
+  Params p = base_params(a);
+  p.MT = (int)ceil_div(a.s.I, BM);
+  p.hin = static_cast<const __nv_bfloat16*>(h);
+  p.dh = static_cast<__nv_bfloat16*>(dh);
+  p.dw = dw;
+  return launch<V_GVEC>(ma, mb, p, st);
+}
+
+usaf_status tc_bwd_dx(const MoeArgs& a, const void* dh, float* dx_acc, cudaStream_t st) {
+  CUtensorMap ma, mb;
+  if (!map_2d(&ma, a.w_gate_up, a.s.H, a.s.E * 2 * a.s.I, 64, 64) ||
+      !map_2d(&mb, dh, 2 * a.s.I, a.R_cap, 64, 128))
+    return USAF_ERR_CUDA;
+  Params p = base_params(a);
+  p.MT = (int)ceil_div(a.s.H, BM);
+  p.acc_out = dx_acc;
+  return launch<V_DX>(ma, mb, p, st);
+}
+
+__global__ void zero_f32_tc_kernel(float* __restrict__ p, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    p[i] = 0.f;
+}
+
+usaf_status tc_bwd_wgrad(const MoeArgs& a, const void* x_perm, const void* dy_perm, const void* dh,
+                         const void* wa, const int64_t* act_idx, int64_t K,
+                         const int32_t* row_ptr, float* g_act, uint32_t* dev_status,
+                         cudaStream_t st) {
+  // experts without tokens run no tile, so their active entries must read 0
+  zero_f32_tc_kernel<<<grid_dim_for(K), 256, 0, st>>>(g_act, K);
+  USAF_CHECK_LAUNCH();
+  CUtensorMap ma, mb;
+  Params p = base_params(a);
+  p.act = act_idx;
+  p.row_ptr = row_ptr;
+  p.g_act = g_act;
+  p.status = dev_status;
+  // S9: gate_up entries, M = 2I weight rows, N = H columns, K = the expert's tokens
+  if (!map_2d(&ma, dh, 2 * a.s.I, a.R_cap, 64, 64) || !map_2d(&mb, x_perm, a.s.H, a.R_cap, 64, 64))
+    return USAF_ERR_CUDA;
+  p.MT = (int)(2 * a.s.I / BM);
+  p.NT = (int)ceil_div(a.s.H, BN);
+  USAF_TRY(launch<V_WG_GU>(ma, mb, p, st));
+  // S10: down entries, M = H weight rows, N = I columns
+  if (!map_2d(&ma, dy_perm, a.s.H, a.R_cap, 64, 64) || !map_2d(&mb, wa, a.s.I, a.R_cap, 64, 64))
+    return USAF_ERR_CUDA;
+  p.MT = (int)ceil_div(a.s.H, BM);
+  p.NT = (int)ceil_div(a.s.I, BN);
+  return launch<V_WG_D>(ma, mb, p, st);
+}
+
+}  // namespace usaf

@@ -1,0 +1,296 @@
+// Routing: router logits, warp-shuffle top-k with renormalised softmax weights, and the
+// deterministic counting-sort permutation into padded per-expert segments.
+//
+// The router is the gating network the USAF README trains in full ("The router is leverage").
+// The routing rule (softmax over experts, top-k, renormalise) is the Qwen3-MoE gating of the
+// model the README benchmarks; the pages do not spell it out.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace usaf {
+
+// ------------------------------------------------------------------------------------------------
+// S1: logits[t,e] = sum_h x[t,h] * Wr[e,h]  (fp32 FFMA, x upcast exactly)
+// Tile: 32 tokens x 64 experts per block, 256 threads, each thread 2 tokens x 4 experts.
+// ------------------------------------------------------------------------------------------------
+template <typename T>
+__global__ void __launch_bounds__(256) router_logits_kernel(const T* __restrict__ x,
+                                                            const float* __restrict__ wr,
+                                                            float* __restrict__ logits, int Tn,
+                                                            int H, int E) {
+  constexpr int BT = 32, BE = 64, BK = 32;
+  __shared__ float xs[BK][BT + 1];
+  __shared__ float ws[BK][BE + 1];
+  const int t0 = blockIdx.y * BT, e0 = blockIdx.x * BE;
+  const int tid = threadIdx.x;
+  const int tr = tid / 16;  // 0..15 -> tokens tr*2, tr*2+1
+  const int ec = tid % 16;  // 0..15 -> experts ec*4 .. +3
+  float acc[2][4] = {};
+  for (int k0 = 0; k0 < H; k0 += BK) {
+    for (int i = tid; i < BT * BK; i += 256) {
+      int tt = i / BK, kk = i % BK;
+      int t = t0 + tt, k = k0 + kk;
+      xs[kk][tt] = (t < Tn && k < H) ? to_f32(x[(int64_t)t * H + k]) : 0.f;
+    }
+    for (int i = tid; i < BE * BK; i += 256) {
+      int ee = i / BK, kk = i % BK;
+      int e = e0 + ee, k = k0 + kk;
+      ws[kk][ee] = (e < E && k < H) ? wr[(int64_t)e * H + k] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < BK; ++kk) {
+      float a0 = xs[kk][tr * 2], a1 = xs[kk][tr * 2 + 1];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        float b = ws[kk][ec * 4 + j];
+        acc[0][j] = fmaf(a0, b, acc[0][j]);
+        acc[1][j] = fmaf(a1, b, acc[1][j]);
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    int t = t0 + tr * 2 + i;
+    if (t >= Tn) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      int e = e0 + ec * 4 + j;
+      if (e < E) logits[(int64_t)t * E + e] = acc[i][j];
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// S2: one warp per token. k rounds of a warp argmax over the logits not yet taken; order is
+// (logit descending, expert ascending) with floating-point comparison (so -0 == +0).
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ bool better(float v, int e, float bv, int be) {
+  return v > bv || (v == bv && e < be);
+}
+
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int Tn,
+                                                   int E, int k, int renorm,
+                                                   int32_t* __restrict__ topk_idx,
+                                                   float* __restrict__ topk_w) {
+  extern __shared__ unsigned char smem_raw[];
+  const int warps = blockDim.x / 32;
+  const int wid = threadIdx.x / 32, lane = threadIdx.x % 32;
+  float* lw = reinterpret_cast<float*>(smem_raw) + wid * E;
+  unsigned char* taken = smem_raw + sizeof(float) * warps * E + wid * E;
+  const int t = blockIdx.x * warps + wid;
+  if (t >= Tn) return;
+  const float* row = logits + (int64_t)t * E;
+  float mx = -INFINITY;
+  for (int e = lane; e < E; e += 32) {
+    float v = row[e];
+    lw[e] = v;
+    taken[e] = 0;
+    mx = fmaxf(mx, v);
+  }
+  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  __syncwarp();
+  float sel_l[32];
+  int sel_e[32];
+#pragma unroll 1
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int be = 0x7fffffff;
+    for (int e = lane; e < E; e += 32) {
+      if (!taken[e] && better(lw[e], e, bv, be)) {
+        bv = lw[e];
+        be = e;
+      }
+    }
+    for (int o = 16; o; o >>= 1) {
+      float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (better(ov, oe, bv, be)) {
+        bv = ov;
+        be = oe;
+      }
+    }
+    // every lane holds the same winner now
+    if (be == 0x7fffffff) be = 0;  // only if all remaining logits are NaN
+    if (lane == 0) taken[be] = 1;
+    __syncwarp();
+    sel_l[j & 31] = bv;
+    sel_e[j & 31] = be;
+  }
+  float denom = 0.f;
+  const float ref = sel_l[0];
+  if (renorm) {
+    for (int j = 0; j < k; ++j) denom += expf(sel_l[j] - ref);
+  } else {
+    float s = 0.f;
+    for (int e = lane; e < E; e += 32) s += expf(lw[e] - mx);
+    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    denom = s;
+  }
+  for (int j = lane; j < k; j += 32) {
+    float num = renorm ? expf(sel_l[j] - ref) : expf(sel_l[j] - mx);
+    topk_idx[(int64_t)t * k + j] = sel_e[j];
+    topk_w[(int64_t)t * k + j] = num / denom;
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// S3: counting sort of the R = T*k slots by expert; within an expert, ascending slot (= token).
+// Chunks of PERM_CHUNK consecutive slots: per-chunk histograms, one scan, one ordered fill.
+// ------------------------------------------------------------------------------------------------
+__global__ void perm_count_kernel(const int32_t* __restrict__ topk_idx, int64_t R, int E,
+                                  int32_t* __restrict__ chunk_hist) {
+  extern __shared__ int32_t hist[];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int64_t s0 = (int64_t)blockIdx.x * PERM_CHUNK;
+  for (int64_t s = s0 + threadIdx.x; s < min(R, s0 + PERM_CHUNK); s += blockDim.x)
+    atomicAdd(&hist[topk_idx[s]], 1);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    chunk_hist[(int64_t)blockIdx.x * E + e] = hist[e];
+}
+
+// One block of 1024 threads: per expert totals and per-chunk bases, then padded offsets.
+__global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ chunk_hist,
+                                                         int nchunks, int E,
+                                                         int32_t* __restrict__ expert_count,
+                                                         int32_t* __restrict__ expert_offset) {
+  __shared__ int32_t padded[1024];
+  __shared__ int32_t warp_sums[32];
+  const int e = threadIdx.x;
+  int32_t total = 0;
+  if (e < E) {
+    for (int b = 0; b < nchunks; ++b) {
+      int32_t c = chunk_hist[(int64_t)b * E + e];
+      chunk_hist[(int64_t)b * E + e] = total;  // exclusive base of chunk b within expert e
+      total += c;
+    }
+    expert_count[e] = total;
+  }
+  int32_t pad = (e < E) ? (int32_t)((total + USAF_ROW_ALIGN - 1) / USAF_ROW_ALIGN * USAF_ROW_ALIGN)
+                        : 0;
+  // block exclusive scan of pad
+  const int lane = e & 31, wid = e >> 5;
+  int32_t v = pad;
+  for (int o = 1; o < 32; o <<= 1) {
+    int32_t n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) warp_sums[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    int32_t w = warp_sums[lane];
+    for (int o = 1; o < 32; o <<= 1) {
+      int32_t n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    warp_sums[lane] = w;  // inclusive
+  }
+  __syncthreads();
+  int32_t incl = v + (wid > 0 ? warp_sums[wid - 1] : 0);
+  padded[e] = incl - pad;
+  __syncthreads();
+  if (e < E) expert_offset[e] = padded[e];
+  if (e == E - 1) expert_offset[E] = incl;
+}
+
+// One warp per chunk: ranks within the chunk by __match_any_sync, in slot order.
+__global__ void __launch_bounds__(32) perm_fill_kernel(const int32_t* __restrict__ topk_idx,
+                                                       int64_t R, int E, int k,
+                                                       const int32_t* __restrict__ chunk_base,
+                                                       const int32_t* __restrict__ expert_offset,
+                                                       int32_t* __restrict__ perm_tok,
+                                                       int32_t* __restrict__ perm_slot,
+                                                       int32_t* __restrict__ slot_row) {
+  extern __shared__ int32_t cnt[];
+  const int lane = threadIdx.x;
+  for (int e = lane; e < E; e += 32)
+    cnt[e] = expert_offset[e] + chunk_base[(int64_t)blockIdx.x * E + e];
+  __syncwarp();
+  const int64_t s0 = (int64_t)blockIdx.x * PERM_CHUNK;
+  const int64_t s1 = min(R, s0 + PERM_CHUNK);
+  for (int64_t base = s0; base < s1; base += 32) {
+    int64_t s = base + lane;
+    bool ok = s < s1;
+    int e = ok ? topk_idx[s] : -1 - lane;  // unique dummies for idle lanes
+    unsigned peers = __match_any_sync(0xffffffffu, e);
+    int rank = __popc(peers & ((1u << lane) - 1));
+    int pos = ok ? cnt[e] + rank : 0;
+    __syncwarp();
+    if (ok && rank == 0) cnt[e] += __popc(peers);
+    __syncwarp();
+    if (ok) {
+      perm_tok[pos] = (int32_t)(s / k);
+      perm_slot[pos] = (int32_t)s;
+      slot_row[s] = pos;
+    }
+  }
+}
+
+// Padding rows of each segment and the tail up to R_cap: perm_tok = 0, perm_slot = -1.
+__global__ void perm_pad_kernel(const int32_t* __restrict__ expert_count,
+                                const int32_t* __restrict__ expert_offset, int E, int64_t R_cap,
+                                int32_t* __restrict__ perm_tok, int32_t* __restrict__ perm_slot) {
+  const int e = blockIdx.x;
+  int64_t lo, hi;
+  if (e < E) {
+    lo = expert_offset[e] + expert_count[e];
+    hi = expert_offset[e + 1];
+  } else {
+    lo = expert_offset[E];
+    hi = R_cap;
+  }
+  for (int64_t r = lo + threadIdx.x; r < hi; r += blockDim.x) {
+    perm_tok[r] = 0;
+    perm_slot[r] = -1;
+  }
+}
+
+usaf_status route_launch(const usaf_moe_shape& s, const void* x, usaf_dtype xdt,
+                         const float* wr, const float* logits_in, float* logits_out, int renorm,
+                         const usaf_routing& rt, RouteWs& w, cudaStream_t st) {
+  const int Tn = (int)s.T, H = (int)s.H, E = (int)s.E, k = (int)s.k;
+  const int64_t R = s.T * s.k;
+  const float* logits = logits_in;
+  if (!logits_in) {
+    USAF_TRACE("route_logits", st);
+    float* out = logits_out ? logits_out : w.logits;
+    dim3 grid((unsigned)ceil_div(E, 64), (unsigned)ceil_div(Tn, 32));
+    if (xdt == USAF_BF16)
+      router_logits_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
+          static_cast<const __nv_bfloat16*>(x), wr, out, Tn, H, E);
+    else
+      router_logits_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(x), wr, out,
+                                                        Tn, H, E);
+    USAF_CHECK_LAUNCH();
+    logits = out;
+  }
+  {
+    USAF_TRACE("route_topk", st);
+    const int warps = 8;
+    size_t sm = (size_t)warps * E * (sizeof(float) + 1);
+    topk_kernel<<<(unsigned)ceil_div(Tn, warps), warps * 32, sm, st>>>(logits, Tn, E, k, renorm,
+                                                                       rt.topk_idx, rt.topk_w);
+    USAF_CHECK_LAUNCH();
+  }
+  USAF_TRACE("route_permute", st);
+  const int nchunks = (int)ceil_div(R, PERM_CHUNK);
+  perm_count_kernel<<<nchunks, 256, E * sizeof(int32_t), st>>>(rt.topk_idx, R, E, w.chunk_hist);
+  USAF_CHECK_LAUNCH();
+  perm_scan_kernel<<<1, 1024, 0, st>>>(w.chunk_hist, nchunks, E, rt.expert_count,
+                                       rt.expert_offset);
+  USAF_CHECK_LAUNCH();
+  perm_fill_kernel<<<nchunks, 32, E * sizeof(int32_t), st>>>(
+      rt.topk_idx, R, E, k, w.chunk_hist, rt.expert_offset, rt.perm_tok, rt.perm_slot,
+      rt.slot_row);
+  USAF_CHECK_LAUNCH();
+  perm_pad_kernel<<<E + 1, 256, 0, st>>>(rt.expert_count, rt.expert_offset, E,
+                                         usaf_routed_rows_capacity(&s), rt.perm_tok,
+                                         rt.perm_slot);
+  USAF_CHECK_LAUNCH();
+  return USAF_OK;
+}
+
+}  // namespace usaf

@@ -1,0 +1,629 @@
+// Exact top-K selection by magnitude (the importance phase) and RigL drop/grow.
+//
+// USAF README: "Not all weights matter" (the importance phase keeps the 0.5% of weights with the
+// highest gradient magnitude) and "Sparsity adapts" (RigL reselection replaces underperforming
+// weights every 50 steps). Order: key descending, flat index ascending among equal keys; the key
+// of |g| is its fp32 bit pattern with the sign cleared.
+//
+// Fast path, one read of g: a strided sample gives a candidate threshold tau0 a safe margin below
+// the K-th largest key; one coalesced pass compacts every (key, index) with key >= tau0 into
+// per-block regions in index order; an exact radix select (4 digit rounds) and an ordered
+// compaction then run on the candidates only. If a region overflows or fewer than K candidates
+// exist, the same kernels run on the full array instead (exact multi-pass path); the choice is
+// taken on the device, so the launch sequence is fixed and needs no host synchronisation.
+#include "common.cuh"
+#include "kernels.cuh"
+
+namespace usaf {
+
+namespace {
+
+constexpr int SEL_THREADS = 256;
+constexpr int SAMPLE_S = 32768;
+// radix rounds over the 31-bit key, most significant digit first: bits 30..23, 22..15, 14..7, 6..0
+__host__ __device__ constexpr int round_shift(int r) { return r == 0 ? 23 : r == 1 ? 15 : r == 2 ? 7 : 0; }
+__host__ __device__ constexpr int round_bits(int r) { return r == 3 ? 7 : 8; }
+
+struct SelCtrl {
+  uint32_t tau0;
+  uint32_t mode;  // 0 full array, 1 candidate regions, 2 drop keys from |p|
+  uint32_t overflow;
+  uint32_t ticket;
+  unsigned long long total;
+  uint32_t prefix;  // radix state: the K-th key's bits found so far
+  uint32_t k_rem;   // rank still to find among keys matching prefix
+  uint32_t hist[256];
+  unsigned long long n_swapped;
+};
+
+// Where block b's part of the source lives.
+struct Src {
+  const float* g;          // modes 0, 2
+  const uint32_t* excl;    // mode 0: bitmap of excluded indices, or null
+  int64_t n;               // modes 0, 2: element count
+  int64_t L;               // modes 0, 2: elements per block (multiple of 4)
+  const uint32_t* ckeys;   // mode 1
+  const uint32_t* cids;
+  const uint32_t* ccnt;
+  int64_t cap;
+  int drop;                // 1: keys are complemented |p| (mode 2 source)
+};
+
+struct SelPlan {
+  int G;            // blocks (= regions)
+  int64_t L;        // elements per block on the full array
+  int64_t cap;      // region capacity
+  int q;            // sample rank for tau0 (0: no sampling)
+  bool sampling;
+};
+
+struct SelWs {
+  SelCtrl* ctrl;
+  uint32_t* samples;
+  uint32_t* ckeys;
+  uint32_t* cids;
+  uint32_t* ccnt;
+  uint32_t* blk_gt;
+  uint32_t* blk_eq;
+  uint32_t* base_gt;
+  uint32_t* base_eq;
+};
+
+SelPlan make_plan(int64_t N, int64_t K) {
+  SelPlan p{};
+  const int64_t sms = device_sm_count();
+  int64_t G = ceil_div(N, 16384);
+  if (G > sms * 4) G = sms * 4;
+  if (G < 1) G = 1;
+  p.G = (int)G;
+  p.L = round_up(ceil_div(N, G), 1024);
+  p.sampling = N >= (int64_t)4 * 1024 * 1024 && K * 16 <= N;
+  if (p.sampling) {
+    const double q = std::ceil((double)SAMPLE_S * (double)K / (double)N);
+    const double qq = q + 8.0 * std::sqrt(q) + 32.0;
+    p.q = (int)std::min<double>(qq, SAMPLE_S);
+    const double frac = (double)p.q / SAMPLE_S;
+    p.cap = round_up((int64_t)((double)p.L * frac * 1.5) + 2048, 256);
+    if (p.q >= SAMPLE_S / 8) p.sampling = false;
+  }
+  if (!p.sampling) {
+    p.q = 0;
+    p.cap = 0;
+  }
+  return p;
+}
+
+void sel_layout(const SelPlan& p, Carver& c, SelWs& w) {
+  w.ctrl = c.take<SelCtrl>(1);
+  w.samples = c.take<uint32_t>(p.sampling ? SAMPLE_S : 0);
+  w.ckeys = c.take<uint32_t>(p.G * p.cap);
+  w.cids = c.take<uint32_t>(p.G * p.cap);
+  w.ccnt = c.take<uint32_t>(p.G);
+  w.blk_gt = c.take<uint32_t>(p.G);
+  w.blk_eq = c.take<uint32_t>(p.G);
+  w.base_gt = c.take<uint32_t>(p.G);
+  w.base_eq = c.take<uint32_t>(p.G);
+}
+
+// ------------------------------------------------------------------------------------------------
+// block-level helpers
+// ------------------------------------------------------------------------------------------------
+// Exclusive scan of one value per thread over the block; returns the prefix, *total the sum.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* total) {
+  __shared__ uint32_t wsum[32];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  uint32_t x = v;
+  for (int o = 1; o < 32; o <<= 1) {
+    uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  __syncthreads();
+  if (lane == 31) wsum[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    uint32_t s = lane < nw ? wsum[lane] : 0;
+    for (int o = 1; o < 32; o <<= 1) {
+      uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += y;
+    }
+    wsum[lane] = s;
+  }
+  __syncthreads();
+  const uint32_t before = (wid > 0 ? wsum[wid - 1] : 0) + x - v;
+  *total = wsum[nw - 1];
+  __syncthreads();
+  return before;
+}
+
+__device__ __forceinline__ bool excluded(const uint32_t* excl, int64_t i) {
+  return excl && ((excl[i >> 5] >> (i & 31)) & 1u);
+}
+
+// key of element i of a modes-0/2 source
+__device__ __forceinline__ uint32_t src_key(const Src& s, int64_t i) {
+  const uint32_t k = abs_key(s.g[i]);
+  return s.drop ? (~k & 0x7FFFFFFFu) : k;
+}
+
+// Visit block b's part in index order, blockDim elements per step: f(key, id, valid).
+template <class F>
+__device__ __forceinline__ void for_part(const Src& s, int mode, int b, F f) {
+  if (mode == 1) {
+    const int64_t n = s.ccnt[b];
+    const uint32_t* kk = s.ckeys + (int64_t)b * s.cap;
+    const uint32_t* ii = s.cids + (int64_t)b * s.cap;
+    for (int64_t j0 = 0; j0 < n; j0 += blockDim.x) {
+      const int64_t j = j0 + threadIdx.x;
+      const bool ok = j < n;
+      f(ok ? kk[j] : 0u, ok ? (int64_t)ii[j] : 0, ok);
+    }
+  } else {
+    const int64_t lo = (int64_t)b * s.L;
+    const int64_t hi = min(s.n, lo + s.L);
+    for (int64_t i0 = lo; i0 < hi; i0 += blockDim.x) {
+      const int64_t i = i0 + threadIdx.x;
+      const bool ok = i < hi && !(mode == 0 && excluded(s.excl, i));
+      f(ok ? src_key(s, i) : 0u, i, ok);
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// kernels
+// ------------------------------------------------------------------------------------------------
+__global__ void sel_init_kernel(SelCtrl* c, int64_t K, uint32_t* ccnt, int G) {
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) c->hist[i] = 0;
+  for (int i = threadIdx.x; i < G; i += blockDim.x) ccnt[i] = 0;
+  if (threadIdx.x == 0) {
+    c->tau0 = 0;
+    c->mode = 0;
+    c->overflow = 0;
+    c->ticket = 0;
+    c->total = 0;
+    c->prefix = 0;
+    c->k_rem = (uint32_t)K;
+    c->n_swapped = 0;
+  }
+}
+
+__global__ void sel_sample_kernel(const float* __restrict__ g, int64_t N,
+                                  const uint32_t* __restrict__ excl,
+                                  uint32_t* __restrict__ samples) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= SAMPLE_S) return;
+  const int64_t pos = (int64_t)(((unsigned long long)i * (unsigned long long)N) / SAMPLE_S);
+  samples[i] = excluded(excl, pos) ? 0u : abs_key(g[pos]);
+}
+
+// One block: the q-th largest sample (1-based) by 4 digit rounds; tau0 := that key.
+__global__ void __launch_bounds__(1024) sel_sample_tau_kernel(const uint32_t* __restrict__ samples,
+                                                              int q, SelCtrl* c) {
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t s_prefix, s_krem;
+  if (threadIdx.x == 0) {
+    s_prefix = 0;
+    s_krem = (uint32_t)q;
+  }
+  for (int r = 0; r < 4; ++r) {
+    const int shift = round_shift(r), bits = round_bits(r);
+    const uint32_t dmask = (1u << bits) - 1;
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+    const uint32_t prefix = s_prefix;
+    const int hs = shift + bits;
+    for (int i0 = 0; i0 < SAMPLE_S; i0 += blockDim.x) {
+      const int i = i0 + threadIdx.x;
+      const uint32_t key = samples[i];
+      const bool m = hs >= 32 || (key >> hs) == (prefix >> hs);
+      const int d = m ? (int)((key >> shift) & dmask) : -1 - (int)(threadIdx.x & 31);
+      const unsigned peers = __match_any_sync(0xffffffffu, d);
+      if (m && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[d], __popc(peers));
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      uint32_t krem = s_krem, cum = 0;
+      int d = (int)dmask;
+      for (; d > 0; --d) {
+        if (cum + hist[d] >= krem) break;
+        cum += hist[d];
+      }
+      s_krem = krem - cum;
+      s_prefix = prefix | ((uint32_t)d << shift);
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) c->tau0 = s_prefix;
+}
+
+// The one pass over g: compact (key, index) with key >= tau0 (and not excluded) per block region.
+__global__ void __launch_bounds__(SEL_THREADS) sel_compact_kernel(
+    const float* __restrict__ g, int64_t N, int64_t L, const uint32_t* __restrict__ excl,
+    int64_t cap, uint32_t* __restrict__ ckeys, uint32_t* __restrict__ cids,
+    uint32_t* __restrict__ ccnt, SelCtrl* c, int vec_ok, uint32_t* dev_status) {
+  const uint32_t tau0 = c->tau0;
+  const int b = blockIdx.x;
+  const int64_t lo = (int64_t)b * L;
+  const int64_t hi = min(N, lo + L);
+  uint32_t* rk = ckeys + (int64_t)b * cap;
+  uint32_t* ri = cids + (int64_t)b * cap;
+  uint32_t count = 0;
+  bool over = false, bad = false;
+  constexpr int TILE = SEL_THREADS * 4;
+  for (int64_t t0 = lo; t0 < hi; t0 += TILE) {
+    uint32_t key[4];
+    bool ok[4];
+    const int64_t i0 = t0 + (int64_t)threadIdx.x * 4;
+    if (vec_ok && i0 + 3 < hi) {
+      const float4 v = __ldcs(reinterpret_cast<const float4*>(g + i0));
+      key[0] = abs_key(v.x);
+      key[1] = abs_key(v.y);
+      key[2] = abs_key(v.z);
+      key[3] = abs_key(v.w);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) ok[j] = true;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        ok[j] = i0 + j < hi;
+        key[j] = ok[j] ? abs_key(g[i0 + j]) : 0u;
+      }
+    }
+    uint32_t mine = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      bad |= ok[j] && key[j] >= 0x7F800000u;
+      ok[j] = ok[j] && key[j] >= tau0 && !excluded(excl, i0 + j);
+      mine += ok[j];
+    }
+    uint32_t tot;
+    uint32_t pos = count + block_excl_scan(mine, &tot);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      if (ok[j]) {
+        if (pos < cap) {
+          rk[pos] = key[j];
+          ri[pos] = (uint32_t)(i0 + j);
+        } else {
+          over = true;
+        }
+        ++pos;
+      }
+    }
+    count += tot;
+  }
+  if (threadIdx.x == 0) {
+    ccnt[b] = count < cap ? count : (uint32_t)cap;
+    atomicAdd(&c->total, (unsigned long long)count);
+  }
+  if (over) c->overflow = 1;
+  flag_status_warp(dev_status, bad, USAF_DEV_NONFINITE);
+}
+
+__global__ void sel_decide_kernel(SelCtrl* c, int64_t K, int sampling, uint32_t* dev_status) {
+  if (threadIdx.x != 0) return;
+  const bool ok = sampling && !c->overflow && c->total >= (unsigned long long)K;
+  c->mode = ok ? 1u : 0u;
+  if (sampling && !ok) flag_status(dev_status, USAF_DEV_SELECT_EXACT_PATH);
+}
+
+// One radix round over the source. The last block to finish picks the digit.
+__global__ void __launch_bounds__(SEL_THREADS) sel_round_kernel(Src s, SelCtrl* c, int shift,
+                                                                int bits, int fixed_mode) {
+  __shared__ uint32_t hist[256];
+  __shared__ bool last;
+  const int mode = fixed_mode >= 0 ? fixed_mode : (int)c->mode;
+  const uint32_t dmask = (1u << bits) - 1;
+  const int hs = shift + bits;
+  const uint32_t prefix = c->prefix;
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+  __syncthreads();
+  for_part(s, mode, blockIdx.x, [&](uint32_t key, int64_t, bool ok) {
+    const bool m = ok && (hs >= 32 || (key >> hs) == (prefix >> hs));
+    const int d = m ? (int)((key >> shift) & dmask) : -1 - (int)(threadIdx.x & 31);
+    const unsigned peers = __match_any_sync(0xffffffffu, d);
+    if (m && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[d], __popc(peers));
+  });
+  __syncthreads();
+  for (int i = threadIdx.x; i <= (int)dmask; i += blockDim.x)
+    if (hist[i]) atomicAdd(&c->hist[i], hist[i]);
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(&c->ticket, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  if (threadIdx.x == 0) {
+    volatile uint32_t* gh = c->hist;
+    uint32_t krem = c->k_rem, cum = 0;
+    int d = (int)dmask;
+    for (; d > 0; --d) {
+      const uint32_t h = gh[d];
+      if (cum + h >= krem) break;
+      cum += h;
+    }
+    c->k_rem = krem - cum;
+    c->prefix = prefix | ((uint32_t)d << shift);
+    c->ticket = 0;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) c->hist[i] = 0;
+}
+
+// Per block: elements strictly above tau and equal to tau.
+__global__ void __launch_bounds__(SEL_THREADS) sel_count_kernel(Src s, const SelCtrl* c,
+                                                                uint32_t* blk_gt, uint32_t* blk_eq,
+                                                                int fixed_mode) {
+  const int mode = fixed_mode >= 0 ? fixed_mode : (int)c->mode;
+  const uint32_t tau = c->prefix;
+  uint32_t gt = 0, eq = 0;
+  for_part(s, mode, blockIdx.x, [&](uint32_t key, int64_t, bool ok) {
+    gt += ok && key > tau;
+    eq += ok && key == tau;
+  });
+  uint32_t tg, te;
+  block_excl_scan(gt, &tg);
+  block_excl_scan(eq, &te);
+  if (threadIdx.x == 0) {
+    blk_gt[blockIdx.x] = tg;
+    blk_eq[blockIdx.x] = te;
+  }
+}
+
+__global__ void __launch_bounds__(1024) sel_scan_kernel(const uint32_t* blk_gt,
+                                                        const uint32_t* blk_eq, int G,
+                                                        uint32_t* base_gt, uint32_t* base_eq) {
+  uint32_t run_gt = 0, run_eq = 0;
+  for (int c0 = 0; c0 < G; c0 += blockDim.x) {
+    const int i = c0 + threadIdx.x;
+    const uint32_t a = i < G ? blk_gt[i] : 0, b = i < G ? blk_eq[i] : 0;
+    uint32_t ta, tb;
+    const uint32_t pa = block_excl_scan(a, &ta);
+    const uint32_t pb = block_excl_scan(b, &tb);
+    if (i < G) {
+      base_gt[i] = run_gt + pa;
+      base_eq[i] = run_eq + pb;
+    }
+    run_gt += ta;
+    run_eq += tb;
+  }
+}
+
+// Ordered write: selected = key > tau, or key == tau among the first need_eq such (by index).
+__global__ void __launch_bounds__(SEL_THREADS) sel_write_kernel(Src s, const SelCtrl* c,
+                                                                const uint32_t* base_gt,
+                                                                const uint32_t* base_eq,
+                                                                int64_t* __restrict__ out,
+                                                                int fixed_mode) {
+  const int mode = fixed_mode >= 0 ? fixed_mode : (int)c->mode;
+  const uint32_t tau = c->prefix;
+  const uint32_t need = c->k_rem;
+  uint32_t gt_run = base_gt[blockIdx.x], eq_run = base_eq[blockIdx.x];
+  for_part(s, mode, blockIdx.x, [&](uint32_t key, int64_t id, bool ok) {
+    const uint32_t isgt = ok && key > tau, iseq = ok && key == tau;
+    uint32_t tg, te;
+    const uint32_t pg = gt_run + block_excl_scan(isgt, &tg);
+    const uint32_t pe = eq_run + block_excl_scan(iseq, &te);
+    if (isgt || (iseq && pe < need)) out[pg + min(pe, need)] = id;
+    gt_run += tg;
+    eq_run += te;
+  });
+}
+
+__global__ void bitmap_zero_kernel(uint32_t* bm, int64_t words) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < words;
+       i += (int64_t)gridDim.x * blockDim.x)
+    bm[i] = 0;
+}
+
+__global__ void bitmap_set_kernel(const int64_t* __restrict__ idx, int64_t K, uint32_t* bm) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < K;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t f = idx[i];
+    atomicOr(&bm[f >> 5], 1u << (f & 31));
+  }
+}
+
+// The fixed sequence of launches that selects the top-K of `s` (see file comment).
+usaf_status run_select(const SelPlan& p, const SelWs& w, Src s, int64_t K, int64_t* out,
+                       uint32_t* dev_status, bool fixed_drop, cudaStream_t st) {
+  {
+    USAF_TRACE("select_init", st);
+    sel_init_kernel<<<1, 256, 0, st>>>(w.ctrl, K, w.ccnt, p.G);
+    USAF_CHECK_LAUNCH();
+  }
+  if (p.sampling && !fixed_drop) {
+    USAF_TRACE("select_sample_compact", st);
+    sel_sample_kernel<<<SAMPLE_S / 256, 256, 0, st>>>(s.g, s.n, s.excl, w.samples);
+    USAF_CHECK_LAUNCH();
+    sel_sample_tau_kernel<<<1, 1024, 0, st>>>(w.samples, p.q, w.ctrl);
+    USAF_CHECK_LAUNCH();
+    const int vec_ok = (reinterpret_cast<uintptr_t>(s.g) & 15) == 0;
+    sel_compact_kernel<<<p.G, SEL_THREADS, 0, st>>>(s.g, s.n, p.L, s.excl, p.cap, w.ckeys,
+                                                    w.cids, w.ccnt, w.ctrl, vec_ok, dev_status);
+    USAF_CHECK_LAUNCH();
+  }
+  USAF_TRACE("select_exact", st);
+  sel_decide_kernel<<<1, 32, 0, st>>>(w.ctrl, K, p.sampling && !fixed_drop ? 1 : 0, dev_status);
+  USAF_CHECK_LAUNCH();
+  s.ckeys = w.ckeys;
+  s.cids = w.cids;
+  s.ccnt = w.ccnt;
+  s.cap = p.cap;
+  const int fm = fixed_drop ? 2 : -1;
+  for (int r = 0; r < 4; ++r) {
+    sel_round_kernel<<<p.G, SEL_THREADS, 0, st>>>(s, w.ctrl, round_shift(r), round_bits(r), fm);
+    USAF_CHECK_LAUNCH();
+  }
+  sel_count_kernel<<<p.G, SEL_THREADS, 0, st>>>(s, w.ctrl, w.blk_gt, w.blk_eq, fm);
+  USAF_CHECK_LAUNCH();
+  sel_scan_kernel<<<1, 1024, 0, st>>>(w.blk_gt, w.blk_eq, p.G, w.base_gt, w.base_eq);
+  USAF_CHECK_LAUNCH();
+  sel_write_kernel<<<p.G, SEL_THREADS, 0, st>>>(s, w.ctrl, w.base_gt, w.base_eq, out, fm);
+  USAF_CHECK_LAUNCH();
+  return USAF_OK;
+}
+
+__device__ __forceinline__ int64_t lower_bound_i64(const int64_t* a, int64_t n, int64_t key) {
+  int64_t lo = 0, hi = n;
+  while (lo < hi) {
+    const int64_t mid = (lo + hi) >> 1;
+    if (a[mid] < key) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// dropped flat indices below f: count q with act_idx[drop_pos[q]] < f (sorted in q)
+__device__ __forceinline__ int64_t dropped_below(const int64_t* act, const int64_t* dpos,
+                                                 int64_t D, int64_t f) {
+  int64_t lo = 0, hi = D;
+  while (lo < hi) {
+    const int64_t mid = (lo + hi) >> 1;
+    if (act[dpos[mid]] < f) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+template <typename W>
+__global__ void rigl_merge_kernel(const int64_t* __restrict__ act, int64_t K,
+                                  const int64_t* __restrict__ dpos,
+                                  const int64_t* __restrict__ grown, int64_t D,
+                                  const float* __restrict__ p_in, const float* __restrict__ m_in,
+                                  const float* __restrict__ v_in, const W* __restrict__ w0,
+                                  int64_t n0, const W* __restrict__ w1,
+                                  int64_t* __restrict__ new_idx, float* __restrict__ p_out,
+                                  float* __restrict__ m_out, float* __restrict__ v_out,
+                                  SelCtrl* c) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t < K) {
+    const int64_t nd = lower_bound_i64(dpos, D, t);
+    const bool dropped = nd < D && dpos[nd] == t;
+    if (dropped) {
+      atomicAdd(&c->n_swapped, 1ull);
+    } else {
+      const int64_t f = act[t];
+      const int64_t pos = (t - nd) + lower_bound_i64(grown, D, f);
+      new_idx[pos] = f;
+      p_out[pos] = p_in[t];
+      m_out[pos] = m_in[t];
+      v_out[pos] = v_in[t];
+    }
+  } else if (t < K + D) {
+    const int64_t j = t - K;
+    const int64_t f = grown[j];
+    const int64_t kept_before = lower_bound_i64(act, K, f) - dropped_below(act, dpos, D, f);
+    const int64_t pos = j + kept_before;
+    new_idx[pos] = f;
+    p_out[pos] = to_f32(f < n0 ? w0[f] : w1[f - n0]);
+    m_out[pos] = 0.f;
+    v_out[pos] = 0.f;
+  }
+}
+
+__global__ void rigl_finish_kernel(const SelCtrl* c, int64_t* n_swapped) {
+  if (threadIdx.x == 0) *n_swapped = (int64_t)c->n_swapped;
+}
+
+}  // namespace
+
+size_t select_ws_bytes(int64_t N, int64_t K, bool with_bitmap) {
+  const SelPlan p = make_plan(N, K);
+  Carver c(nullptr);
+  SelWs w;
+  sel_layout(p, c, w);
+  if (with_bitmap) c.take<uint32_t>(ceil_div(N, 32));
+  return c.size();
+}
+
+usaf_status importance_select_launch(const float* g, int64_t N, int64_t K, int64_t* out_idx,
+                                     uint32_t* dev_status, void* ws, cudaStream_t st) {
+  const SelPlan p = make_plan(N, K);
+  Carver c(ws);
+  SelWs w;
+  sel_layout(p, c, w);
+  Src s{};
+  s.g = g;
+  s.n = N;
+  s.L = p.L;
+  s.excl = nullptr;
+  s.drop = 0;
+  return run_select(p, w, s, K, out_idx, dev_status, false, st);
+}
+
+size_t rigl_ws_bytes(int64_t N, int64_t K, int64_t D) {
+  Carver c(nullptr);
+  c.take<int64_t>(D);  // dropped positions
+  c.take<int64_t>(D);  // grown indices
+  c.take<char>(select_ws_bytes(K > 0 ? K : 1, D > 0 ? D : 1, false));
+  c.take<char>(select_ws_bytes(N, D > 0 ? D : 1, true));
+  return c.size();
+}
+
+usaf_status rigl_launch(const float* g, int64_t N, const int64_t* act_idx, int64_t K, int64_t D,
+                        const float* p_in, const float* m_in, const float* v_in, const void* w0,
+                        int64_t n0, const void* w1, usaf_dtype wdt, int64_t* new_idx,
+                        float* p_out, float* m_out, float* v_out, int64_t* n_swapped,
+                        uint32_t* dev_status, void* ws, cudaStream_t st) {
+  Carver c(ws);
+  int64_t* dpos = c.take<int64_t>(D);
+  int64_t* grown = c.take<int64_t>(D);
+  const int64_t Ks = K > 0 ? K : 1, Ds = D > 0 ? D : 1;
+  char* ws_drop = c.take<char>(select_ws_bytes(Ks, Ds, false));
+  char* ws_grow = c.take<char>(select_ws_bytes(N, Ds, true));
+  // drop: the D smallest |p| among the K actives (complemented keys, exact path)
+  const SelPlan pd = make_plan(Ks, Ds);
+  Carver cd(ws_drop);
+  SelWs wd;
+  sel_layout(pd, cd, wd);
+  // grow: the D largest |g| outside the active set (sampled path with an exclusion bitmap)
+  const SelPlan pg = make_plan(N, Ds);
+  Carver cg(ws_grow);
+  SelWs wg;
+  sel_layout(pg, cg, wg);
+  uint32_t* bitmap = cg.take<uint32_t>(ceil_div(N, 32));
+  if (D > 0) {
+    Src sd{};
+    sd.g = p_in;
+    sd.n = K;
+    sd.L = pd.L;
+    sd.drop = 1;
+    USAF_TRY(run_select(pd, wd, sd, D, dpos, dev_status, true, st));
+    const int64_t words = ceil_div(N, 32);
+    {
+      USAF_TRACE("rigl_bitmap", st);
+      bitmap_zero_kernel<<<grid_dim_for(words), 256, 0, st>>>(bitmap, words);
+      USAF_CHECK_LAUNCH();
+      bitmap_set_kernel<<<grid_dim_for(K), 256, 0, st>>>(act_idx, K, bitmap);
+      USAF_CHECK_LAUNCH();
+    }
+    Src sg{};
+    sg.g = g;
+    sg.n = N;
+    sg.L = pg.L;
+    sg.excl = bitmap;
+    sg.drop = 0;
+    USAF_TRY(run_select(pg, wg, sg, D, grown, dev_status, false, st));
+  } else {
+    sel_init_kernel<<<1, 256, 0, st>>>(wd.ctrl, 0, wd.ccnt, pd.G);
+    USAF_CHECK_LAUNCH();
+  }
+  const int64_t n = K + D;
+  USAF_TRACE("rigl_merge", st);
+  if (n > 0) {
+    if (wdt == USAF_BF16)
+      rigl_merge_kernel<__nv_bfloat16><<<(unsigned)ceil_div(n, 256), 256, 0, st>>>(
+          act_idx, K, dpos, grown, D, p_in, m_in, v_in, static_cast<const __nv_bfloat16*>(w0),
+          n0, static_cast<const __nv_bfloat16*>(w1), new_idx, p_out, m_out, v_out, wd.ctrl);
+    else
+      rigl_merge_kernel<float><<<(unsigned)ceil_div(n, 256), 256, 0, st>>>(
+          act_idx, K, dpos, grown, D, p_in, m_in, v_in, static_cast<const float*>(w0), n0,
+          static_cast<const float*>(w1), new_idx, p_out, m_out, v_out, wd.ctrl);
+    USAF_CHECK_LAUNCH();
+  }
+  rigl_finish_kernel<<<1, 32, 0, st>>>(wd.ctrl, n_swapped);
+  USAF_CHECK_LAUNCH();
+  return USAF_OK;
+}
+
+}  // namespace usaf

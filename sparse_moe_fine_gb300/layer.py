@@ -1,0 +1,121 @@
+"""One USAF MoE layer held on the GPU: weights, router, active set and its SparseAdam state, and
+the buffers of a train step. Each method is a sequence of C-ABI calls (see include/usaf.h); this
+module only allocates with PyTorch and passes pointers.
+
+A train step is: route (router logits, top-k, permutation) -> grouped SwiGLU forward -> sparse
+backward (router gradient, input gradient, expert gradients at the active set) -> SparseAdam on
+the active expert entries -> SparseAdam on the router (USAF README: the router is trained in
+full, expert weights at a 0.5% active set, both under SparseAdam).
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import binding as B
+
+
+class MoELayer:
+    def __init__(self, T, H, E, k, I, w_gate_up, w_down, w_router, act_idx, lr=1e-4,
+                 betas=(0.9, 0.999), eps=1e-8, renorm=1, device="cuda"):
+        self.dev = torch.device(device)
+        self.s = B.shape(T, H, E, k, I)
+        self.T, self.H, self.E, self.k, self.I = T, H, E, k, I
+        self.dtype = w_gate_up.dtype
+        self.dt = B.BF16 if self.dtype == torch.bfloat16 else B.F32
+        self.w_gate_up = w_gate_up.contiguous()
+        self.w_down = w_down.contiguous()
+        self.w_router = w_router.contiguous().float()
+        self.N_gu = E * 2 * I * H
+        self.N = E * 3 * I * H
+        self.lr, self.betas, self.eps, self.renorm = lr, betas, eps, renorm
+        self.step_count = 0
+        d = self.dev
+        cap = B.routed_rows_capacity(self.s)
+        self.rt = B.Routing.empty(self.s, d)
+        self.logits = torch.empty(T, E, device=d)
+        self.x_perm = torch.empty(cap, H, dtype=self.dtype, device=d)
+        self.h = torch.empty(cap, 2 * I, dtype=self.dtype, device=d)
+        self.wa = torch.empty(cap, I, dtype=self.dtype, device=d)
+        self.y = torch.empty(T, H, dtype=self.dtype, device=d)
+        self.dx = torch.empty(T, H, dtype=self.dtype, device=d)
+        self.g_router = torch.empty(E, H, device=d)
+        self.status = torch.zeros(1, dtype=torch.int32, device=d)
+        self.ws_route = torch.empty(B.route_topk_workspace_size(self.s), dtype=torch.uint8,
+                                    device=d)
+        self.ws_fwd = torch.empty(B.moe_fwd_workspace_size(self.s, self.dt), dtype=torch.uint8,
+                                  device=d)
+        # router SparseAdam state (dense over all E*H entries)
+        self.r_p = self.w_router.reshape(-1).clone()
+        self.r_m = torch.zeros_like(self.r_p)
+        self.r_v = torch.zeros_like(self.r_p)
+        self.set_active(act_idx)
+
+    # ------------------------------------------------------------------ active set
+    def set_active(self, act_idx, p=None, m=None, v=None):
+        """Install a sorted active set; fresh state starts from the weight values."""
+        self.act = act_idx.to(self.dev, torch.int64).contiguous()
+        K = self.act.numel()
+        self.K = K
+        if p is None:
+            flat_gu = self.w_gate_up.reshape(-1)
+            flat_d = self.w_down.reshape(-1)
+            gu = self.act < self.N_gu
+            p = torch.empty(K, device=self.dev)
+            p[gu] = flat_gu[self.act[gu]].float()
+            p[~gu] = flat_d[self.act[~gu] - self.N_gu].float()
+            m = torch.zeros(K, device=self.dev)
+            v = torch.zeros(K, device=self.dev)
+        self.p, self.m, self.v = p, m, v
+        self.g_act = torch.empty(K, device=self.dev)
+        self.ws_bwd = torch.empty(B.moe_bwd_workspace_size(self.s, self.dt, K),
+                                  dtype=torch.uint8, device=self.dev)
+
+    # ------------------------------------------------------------------ the step
+    def route(self, x, stream=None):
+        B.route_topk(self.s, x, self.w_router, self.rt, logits_out=self.logits,
+                     renorm=self.renorm, ws=self.ws_route, stream=stream)
+
+    def forward(self, x, stream=None):
+        B.moe_fwd(self.s, x, self.w_gate_up, self.w_down, self.rt, self.x_perm, self.h, self.wa,
+                  self.y, ws=self.ws_fwd, stream=stream)
+        return self.y
+
+    def backward(self, x, dy, want_dx=True, stream=None):
+        B.moe_bwd_sparse(self.s, x, self.w_router, self.w_gate_up, self.w_down, self.rt,
+                         self.x_perm, self.h, self.wa, dy, self.act, self.g_act, self.g_router,
+                         dx=self.dx if want_dx else None, logits=self.logits,
+                         renorm=self.renorm, dev_status=self.status, ws=self.ws_bwd,
+                         stream=stream)
+
+    def optimizer_step(self, stream=None, skip_if_nonfinite=1):
+        self.step_count += 1
+        b1, b2 = self.betas
+        B.sparse_adam_step(self.act, self.g_act, self.p, self.m, self.v, self.w_gate_up,
+                           self.N_gu, self.w_down, self.lr, b1, b2, self.eps, self.step_count,
+                           skip_if_nonfinite, self.status, stream=stream)
+        B.sparse_adam_step(None, self.g_router, self.r_p, self.r_m, self.r_v, self.w_router,
+                           self.E * self.H, None, self.lr, b1, b2, self.eps, self.step_count,
+                           skip_if_nonfinite, self.status, stream=stream)
+
+    def train_step(self, x, dy, stream=None):
+        """route -> forward -> sparse backward -> SparseAdam (experts, router)."""
+        self.status.zero_()  # per-step non-finite flag (a non-finite gradient skips this step)
+        self.route(x, stream)
+        self.forward(x, stream)
+        self.backward(x, dy, stream=stream)
+        self.optimizer_step(stream)
+        return self.y, self.dx
+
+    def train_step_host(self, x_host, dy_host, y_host, dx_host, x_dev, dy_dev, stream=None):
+        """The same step fed from (pinned) host memory: copy x and dy in, run, copy y and dx out."""
+        x_dev.copy_(x_host, non_blocking=True)
+        dy_dev.copy_(dy_host, non_blocking=True)
+        self.train_step(x_dev, dy_dev, stream)
+        y_host.copy_(self.y, non_blocking=True)
+        dx_host.copy_(self.dx, non_blocking=True)
+
+
+def active_count(N: int, frac: float = 0.005) -> int:
+    return int(math.ceil(frac * N))

@@ -1,0 +1,78 @@
+"""The C-ABI library loads without a GPU, exports every symbol include/usaf.h declares, and its
+host-side argument checks and workspace queries behave as the header states (nothing is launched
+in these calls)."""
+import ctypes
+import math
+
+import pytest
+
+from sparse_moe_fine_gb300 import binding as B
+
+
+def test_library_exports_every_header_symbol():
+    L = B.lib()
+    syms = B.header_symbols()
+    assert len(syms) == 17
+    for s in syms:
+        assert hasattr(L, s), s
+    assert L.usaf_abi_version() == 1
+    assert L.usaf_status_string(0) == b"ok"
+    assert L.usaf_status_string(3) == b"workspace missing or too small"
+
+
+def test_capacity_and_workspace_queries():
+    s = B.shape(4096, 2048, 128, 8, 768)
+    cap = B.routed_rows_capacity(s)
+    assert cap >= 4096 * 8 + 128 * 15 and cap % 256 == 0
+    assert B.route_topk_workspace_size(s) > 4096 * 128 * 4
+    assert B.moe_fwd_workspace_size(s, B.BF16) >= 4096 * 2048 * 4
+    assert B.moe_bwd_workspace_size(s, B.BF16, 3019899) > 0
+    N = 603979776
+    K = math.ceil(0.005 * N)
+    ws = B.importance_select_workspace_size(N, K)
+    assert 0 < ws < 0.2 * N * 4  # candidates only, not a copy of g
+    assert B.rigl_swap_workspace_size(N, K, int(0.3 * K)) > N // 8  # holds the N-bit bitmap
+    bad = B.shape(0, 2048, 128, 8, 768)
+    assert B.routed_rows_capacity(bad) == -1
+    assert B.importance_select_workspace_size(10, 11) == 0
+    assert B.rigl_swap_workspace_size(10, 8, 3) == 0  # D > N - K
+
+
+def _call(name, *args):
+    return getattr(B.lib(), name)(*args)
+
+
+def test_host_argument_checks_return_codes():
+    s = B.shape(8, 64, 4, 2, 64)
+    r = B._Routing()
+    # null routing arrays
+    assert _call("usaf_route_topk", ctypes.byref(s), 1, 0, 1, None, None, 1, ctypes.byref(r),
+                 1, 1 << 20, None) == 1
+    # k > E
+    s2 = B.shape(8, 64, 4, 5, 64)
+    assert _call("usaf_routed_rows_capacity", ctypes.byref(s2)) == -1
+    # SparseAdam: step 0, skip without a status word, betas out of range
+    assert _call("usaf_sparse_adam_step", 4, None, 1, 1, 1, 1, 1, 4, None, 0, 1e-3, 0.9, 0.999,
+                 1e-8, 0, 0, None, None) == 1
+    assert _call("usaf_sparse_adam_step", 4, None, 1, 1, 1, 1, 1, 4, None, 0, 1e-3, 0.9, 0.999,
+                 1e-8, 1, 1, None, None) == 1
+    assert _call("usaf_sparse_adam_step", 4, None, 1, 1, 1, 1, 1, 4, None, 0, 1e-3, 1.0, 0.999,
+                 1e-8, 1, 0, None, None) == 1
+    # dense form needs n <= n_seg0
+    assert _call("usaf_sparse_adam_step", 8, None, 1, 1, 1, 1, 1, 4, None, 0, 1e-3, 0.9, 0.999,
+                 1e-8, 1, 0, None, None) == 1
+    # n = 0 is a no-op
+    assert _call("usaf_sparse_adam_step", 0, None, None, None, None, None, None, 0, None, 0, 1e-3,
+                 0.9, 0.999, 1e-8, 1, 0, None, None) == 0
+    # selection: K > N, workspace too small
+    assert _call("usaf_importance_select", 1, 10, 11, 1, None, 1, 1 << 20, None) == 1
+    assert _call("usaf_importance_select", 1, 1 << 20, 10, 1, None, 1, 16, None) == 3
+    # RigL: overlapping input/output state, D > K
+    assert _call("usaf_rigl_swap", 1, 100, 4096, 10, 2, 8192, 16384, 24576, 1, 100, None, 0,
+                 40960, 8192, 49152, 57344, 1, None, 1, 1 << 30, None) == 1
+    assert _call("usaf_rigl_swap", 1, 100, 4096, 10, 11, 8192, 16384, 24576, 1, 100, None, 0,
+                 40960, 65536, 49152, 57344, 1, None, 1, 1 << 30, None) == 1
+    # bf16 layers need H and I multiples of 64
+    s3 = B.shape(8, 96, 4, 2, 64)
+    assert _call("usaf_moe_fwd", ctypes.byref(s3), 1, 1, 1, 1, ctypes.byref(B._Routing(*[1] * 7)),
+                 1, 1, 1, 1, 1, 1 << 30, None) == 2

@@ -1,0 +1,150 @@
+"""GPU expert forward / sparse backward against the oracle, fed the same routing logits.
+
+Tolerances: fp32 layers rel-L2 <= 1e-5; bf16 layers (bf16 inputs, fp32 accumulation, h, w*A and
+dh stored in bf16) rel-L2 <= 1e-2, the bound the workload states for bf16-input GEMM outputs and
+gradients."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from sparse_moe_fine_gb300 import binding as B
+from sparse_moe_fine_gb300 import synth
+
+from _gpu import device, rel_l2, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def run_layer(cfg, inp, act_idx, logits, dev, renorm=1, want_dx=True):
+    s = B.shape(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I)
+    bf = cfg.bf16
+    dt = torch.bfloat16 if bf else torch.float32
+    x = to_dev(inp["x"], dev, bf)
+    wr = to_dev(inp["w_router"], dev)
+    wgu = to_dev(inp["w_gate_up"], dev, bf)
+    wd = to_dev(inp["w_down"], dev, bf)
+    dy = to_dev(inp["dy"], dev, bf)
+    li = to_dev(logits, dev)
+    rt = B.Routing.empty(s, dev)
+    B.route_topk(s, x, wr, rt, logits_in=li, renorm=renorm)
+    cap = B.routed_rows_capacity(s)
+    xp = torch.empty(cap, cfg.H, dtype=dt, device=dev)
+    h = torch.empty(cap, 2 * cfg.I, dtype=dt, device=dev)
+    wa = torch.empty(cap, cfg.I, dtype=dt, device=dev)
+    y = torch.empty(cfg.T, cfg.H, dtype=dt, device=dev)
+    B.moe_fwd(s, x, wgu, wd, rt, xp, h, wa, y)
+    act = to_dev(act_idx, dev)
+    K = act.numel()
+    g_act = torch.full((K,), float("nan"), device=dev)
+    g_r = torch.full((cfg.E, cfg.H), float("nan"), device=dev)
+    dx = torch.empty(cfg.T, cfg.H, dtype=dt, device=dev) if want_dx else None
+    dw = torch.empty(cfg.T * cfg.k, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    B.moe_bwd_sparse(s, x, wr, wgu, wd, rt, xp, h, wa, dy, act, g_act, g_r, dx=dx, dw_slot=dw,
+                     logits=li, renorm=renorm, dev_status=st)
+    torch.cuda.synchronize()
+    out = {"Y": y.float().cpu().numpy(), "g_act": g_act.cpu().numpy(),
+           "g_router": g_r.cpu().numpy(), "dw": dw.cpu().numpy().reshape(cfg.T, cfg.k),
+           "status": int(st.item()), "idx": rt.topk_idx.cpu().numpy().reshape(cfg.T, cfg.k),
+           "count": rt.expert_count.cpu().numpy()}
+    if want_dx:
+        out["dx"] = dx.float().cpu().numpy()
+    return out
+
+
+def oracle_layer(cfg, inp, act_idx, logits, renorm=1):
+    idx, w = oracle.route_topk(logits, cfg.k, renorm)
+    b = oracle.moe_backward(inp["x"], inp["w_router"], inp["w_gate_up"], inp["w_down"], idx, w,
+                            logits, inp["dy"], renorm=renorm)
+    g = oracle.masked_expert_grad(act_idx, inp["x"], inp["w_gate_up"], inp["w_down"], idx, w,
+                                  inp["dy"])
+    return idx, b, g
+
+
+def compare(cfg, got, idx, b, g, tol):
+    assert (got["idx"] == idx).all()
+    assert got["status"] == 0
+    assert rel_l2(got["Y"], b["Y"]) <= tol
+    assert rel_l2(got["dx"], b["dx"]) <= tol
+    assert rel_l2(got["dw"], b["dw"]) <= tol
+    assert rel_l2(got["g_router"], b["g_router"]) <= tol
+    assert rel_l2(got["g_act"], g) <= tol
+
+
+@pytest.mark.parametrize("renorm", [1, 0])
+def test_tiny_fp32_layer(renorm):
+    dev = device()
+    cfg = synth.CONFIGS["tiny_fp32"]
+    inp = synth.moe_inputs(cfg, seed=0)
+    logits = oracle.router_logits(inp["x"], inp["w_router"])
+    act = synth.uniform_mask(cfg.N, cfg.K, seed=0)
+    got = run_layer(cfg, inp, act, logits, dev, renorm)
+    idx, b, g = oracle_layer(cfg, inp, act, logits, renorm)
+    compare(cfg, got, idx, b, g, 1e-5)
+
+
+SMALL_BF16 = [
+    # several tiles in M and K, ragged token counts below one tile
+    dict(T=300, H=256, E=8, k=2, I=256),
+    # H and I not multiples of 128 (ragged M and N tiles), experts above 256 tokens
+    dict(T=1000, H=192, E=4, k=2, I=192),
+    # top-8 of 16 with a wide hidden size
+    dict(T=96, H=512, E=16, k=8, I=128),
+]
+
+
+@pytest.mark.parametrize("dims", SMALL_BF16)
+def test_small_bf16_layers(dims):
+    dev = device()
+    cfg = synth.small_config("small", bf16=True, frac=0.05, dy_std=1e-2, **dims)
+    inp = synth.moe_inputs(cfg, seed=5)
+    logits = oracle.router_logits(inp["x"], inp["w_router"])
+    act = synth.uniform_mask(cfg.N, cfg.K, seed=5)
+    got = run_layer(cfg, inp, act, logits, dev)
+    idx, b, g = oracle_layer(cfg, inp, act, logits)
+    compare(cfg, got, idx, b, g, 1e-2)
+
+
+def test_bf16_empty_and_crowded_experts():
+    dev = device()
+    cfg = synth.small_config("skew", T=700, H=128, E=6, k=2, I=128, bf16=True, frac=0.05)
+    inp = synth.moe_inputs(cfg, seed=6)
+    logits = oracle.router_logits(inp["x"], inp["w_router"])
+    logits[:, 5] = -1e3   # expert 5 never routed
+    logits[:, 0] += 1e3   # expert 0 takes every token (700 rows: three token tiles)
+    act = synth.uniform_mask(cfg.N, cfg.K, seed=6)
+    got = run_layer(cfg, inp, act, logits, dev)
+    assert got["count"][5] == 0 and got["count"][0] == cfg.T
+    idx, b, g = oracle_layer(cfg, inp, act, logits)
+    compare(cfg, got, idx, b, g, 1e-2)
+    t_, e_, _, _ = oracle.split_flat_index(act, cfg.E, cfg.I, cfg.H)
+    assert (got["g_act"][e_ == 5] == 0).all()
+
+
+def test_qwen3_shaped_layer_sampled():
+    """Full Qwen3-30B-A3B-shaped layer (T=4096, H=2048, E=128, top-8, I=768, 0.5% active) in the
+    launch configuration the benchmark times; the oracle checks every output of the forward and
+    backward and the masked gradients of a sample of experts."""
+    dev = device()
+    cfg = synth.CONFIGS["qwen3_30b_a3b"]
+    inp = synth.moe_inputs(cfg, seed=0)
+    logits = oracle.router_logits(inp["x"], inp["w_router"])
+    act = synth.uniform_mask(cfg.N, cfg.K, seed=0)
+    got = run_layer(cfg, inp, act, logits, dev)
+    idx, w = oracle.route_topk(logits, cfg.k)
+    assert (got["idx"] == idx).all() and got["status"] == 0
+    b = oracle.moe_backward(inp["x"], inp["w_router"], inp["w_gate_up"], inp["w_down"], idx, w,
+                            logits, inp["dy"])
+    assert rel_l2(got["Y"], b["Y"]) <= 1e-2
+    assert rel_l2(got["dx"], b["dx"]) <= 1e-2
+    assert rel_l2(got["dw"], b["dw"]) <= 1e-2
+    assert rel_l2(got["g_router"], b["g_router"]) <= 1e-2
+    counts = got["count"]
+    experts = sorted({0, int(np.argmax(counts)), int(np.argmin(counts)), 77, cfg.E - 1})
+    g = oracle.masked_expert_grad(act, inp["x"], inp["w_gate_up"], inp["w_down"], idx, w,
+                                  inp["dy"], experts=experts)
+    sel = ~np.isnan(g)
+    assert sel.sum() > 1000
+    assert rel_l2(got["g_act"][sel], g[sel]) <= 1e-2
+    assert np.isfinite(got["g_act"]).all()
