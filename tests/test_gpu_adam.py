@@ -1,4 +1,5 @@
-"""GPU SparseAdam against the oracle (same g fed to both sides): fp32 state max-rel <= 1e-5, the
+"""GPU SparseAdam against the oracle (same g fed to both sides): fp32 state max-rel <= 1e-5 (for
+m, whose update b1*m + (1-b1)*g can cancel, relative to the magnitude of the terms), the
 dense weight at each index equals the nearest bf16 of the oracle's p (or is 1 bf16 ulp away where
 p sits on a rounding boundary), entries outside the index set bit-unchanged, NaN steps skipped."""
 import numpy as np
@@ -34,15 +35,18 @@ def test_sparse_adam_multi_step_two_segments(n_gu, n_d, K):
     gi = to_dev(idx, dev)
     gp, gm, gv = to_dev(p, dev), to_dev(m, dev), to_dev(v, dev)
     rng = np.random.default_rng(9)
+    m_scale = np.zeros(K)
     for step in range(1, 4):
         g = (rng.standard_normal(K) * 1e-3).astype(np.float32)
         g[::5] = 0.0
         B.sparse_adam_step(gi, to_dev(g, dev), gp, gm, gv, gwgu, n_gu, gwd, 1e-4, 0.9, 0.999,
                            1e-8, step)
+        m_scale = np.maximum(m_scale, 0.9 * np.abs(m) + 0.1 * np.abs(g))
         p, m, v = oracle.sparse_adam(g, p, m, v, 1e-4, 0.9, 0.999, 1e-8, step)
     torch.cuda.synchronize()
     assert max_rel(gp.cpu().numpy(), p) <= 1e-5
-    assert max_rel(gm.cpu().numpy(), m) <= 1e-5
+    gm_ = gm.cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(gm_ - m) / np.maximum(np.abs(m), m_scale)) <= 1e-5
     assert max_rel(gv.cpu().numpy(), v) <= 1e-5
     Wg = np.concatenate([gwgu.float().cpu().numpy(), gwd.float().cpu().numpy()])
     assert (_bf16_ulp_diff(Wg[idx], oracle.bf16_round(p)) <= 1).all()
