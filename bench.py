@@ -246,6 +246,10 @@ def run(args):
     stream = torch.cuda.current_stream()
 
     # ---- importance pass: the active set is the top 0.5% |g| of a dense gradient
+    if args.no_importance:
+        return run_steps(args, B, MoELayer, dist, ws, rank, local, dev, cfg, inp, x, dy, wgu, wd,
+                         wr, torch.from_numpy(synth.uniform_mask(cfg.N, cfg.K, 0)).to(dev),
+                         None, hbm, tf_burst, tf_sus, peak_src, stream)
     g_dense = torch.from_numpy(synth.student_t3(cfg.N, seed=0)).to(dev)
     act = torch.empty(cfg.K, dtype=torch.int64, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -286,9 +290,15 @@ def run(args):
         "rigl_ms": rigl_ms, "rigl_gbs": (g_bytes + cfg.N / 8 + cfg.K * 40) / rigl_ms / 1e6,
         "select_exact_path": bool(int(st.item()) & B.DEV_SELECT_EXACT_PATH),
         "N": cfg.N, "K": cfg.K, "D": D}
-    del g_dense
+    del g_dense, layer
     torch.cuda.empty_cache()
+    return run_steps(args, B, MoELayer, dist, ws, rank, local, dev, cfg, inp, x, dy, wgu, wd, wr,
+                     act, importance, hbm, tf_burst, tf_sus, peak_src, stream)
 
+
+def run_steps(args, B, MoELayer, dist, ws, rank, local, dev, cfg, inp, x, dy, wgu, wd, wr, act,
+              importance, hbm, tf_burst, tf_sus, peak_src, stream):
+    layer = MoELayer(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, wgu, wd, wr, act, lr=cfg.lr, device=dev)
     # ---- train steps
     for _ in range(args.warmup):
         layer.status.zero_()
@@ -341,6 +351,30 @@ def run(args):
     step_roof_ms = max(fl / (tf_sus * 1e12), by / (hbm * 1e9)) * 1e3
 
     # ---- end to end: x, dy from pinned host memory, y and dx back, through the layer API
+    if args.no_e2e:
+        e2e_ms = float("nan")
+    else:
+        e2e_ms = e2e_time(args, layer, x, dy, e0, e1, stream, dist, dev)
+    nbytes = x.numel() * 2
+    line = make_line(args, cfg, ws, ms, value, step_roof_ms, fl, by, roof, trace, tot,
+                     importance, e2e_ms, nbytes, launches, clk)
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        tokens = args.cpu_tokens
+        a = act.cpu().numpy()
+        p0 = master_values(inp, a, cfg.N_gu)
+        del layer, wgu, wd
+        inp = {k: v.astype(np.float64) for k, v in inp.items()}  # exact upcast of bf16 values
+        t = oracle_step_sample(cfg, inp, a, p0, tokens)
+        line["cpu_baseline"] = {"value": tokens / t, "unit": "tokens/s", "cores": cpu_threads(),
+                                "kind": "oracle",
+                                "sample": f"one step on the first {tokens} of {cfg.T} tokens"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def e2e_time(args, layer, x, dy, e0, e1, stream, dist, dev):
     xh = x.cpu().pin_memory()
     dyh = dy.cpu().pin_memory()
     yh = torch.empty_like(xh).pin_memory()
@@ -354,9 +388,11 @@ def run(args):
         layer.train_step_host(xh, dyh, yh, dxh, xd, dyd)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(dist, e0.elapsed_time(e1) / args.steps, dev)
-    nbytes = x.numel() * 2
+    return max_over_ranks(dist, e0.elapsed_time(e1) / args.steps, dev)
 
+
+def make_line(args, cfg, ws, ms, value, step_roof_ms, fl, by, roof, trace, tot, importance,
+              e2e_ms, nbytes, launches, clk):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -377,20 +413,7 @@ def run(args):
         "gpu_launches": int(launches) * args.steps,
         "clocks": clk.summary(),
     }
-    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        tokens = args.cpu_tokens
-        a = act.cpu().numpy()
-        p0 = master_values(inp, a, cfg.N_gu)
-        del layer, wgu, wd
-        inp = {k: v.astype(np.float64) for k, v in inp.items()}  # exact upcast of bf16 values
-        t = oracle_step_sample(cfg, inp, a, p0, tokens)
-        line["cpu_baseline"] = {"value": tokens / t, "unit": "tokens/s", "cores": cpu_threads(),
-                                "kind": "oracle",
-                                "sample": f"one step on the first {tokens} of {cfg.T} tokens"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if dist is not None:
-        dist.destroy_process_group()
+    return line
 
 
 def main():
@@ -401,6 +424,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-tokens", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-importance", action="store_true",
+                    help="skip the importance/RigL timing; use a seeded uniform 0.5%% mask")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer timing")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -29,7 +29,7 @@ struct BwdWs {
   void* dh;           // [R_cap, 2I] of dtype
   float* dx_acc;      // [T,H]
   float* gvec;        // [R_cap, I] (fp32 path only)
-  int32_t* row_ptr;   // [E*2I + E*H + 1] first active of each weight row (tensor-core path)
+  int32_t* tile_ptr;  // first active entry of each (weight row, 256-column tile) (tensor cores)
   int32_t* plan;      // [E+1] prefix of token tiles per expert (tensor-core path)
   void* dy_perm;      // [R_cap, H] dy rows in permuted order (tensor-core path)
 };
@@ -58,6 +58,7 @@ usaf_status moe_bwd_launch(const MoeArgs& a, int renorm, const float* logits, co
 // tensor-core (tcgen05) grouped GEMM stages, bf16 only
 bool tc_shape_ok(const usaf_moe_shape& s);
 usaf_status tc_plan(const MoeArgs& a, cudaStream_t st);
+int64_t tile_ptr_entries(const usaf_moe_shape& s);
 usaf_status tc_fwd_gate_up(const MoeArgs& a, const void* x_perm, void* h, void* wa,
                            cudaStream_t st);
 usaf_status tc_fwd_down(const MoeArgs& a, const void* wa, float* y_acc, cudaStream_t st);
@@ -66,7 +67,7 @@ usaf_status tc_bwd_gvec(const MoeArgs& a, const void* dy_perm, const void* h, vo
 usaf_status tc_bwd_dx(const MoeArgs& a, const void* dh, float* dx_acc, cudaStream_t st);
 usaf_status tc_bwd_wgrad(const MoeArgs& a, const void* x_perm, const void* dy_perm, const void* dh,
                          const void* wa, const int64_t* act_idx, int64_t K,
-                         const int32_t* row_ptr, float* g_act, uint32_t* dev_status,
+                         const int32_t* tile_ptr, float* g_act, uint32_t* dev_status,
                          cudaStream_t st);
 
 // ---------------------------------------------------------------- optimizer

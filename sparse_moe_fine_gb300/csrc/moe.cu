@@ -425,7 +425,7 @@ void bwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, int64_t K, Carver& c,
   w.dh = c.take<char>(R_cap * 2 * s.I * (int64_t)es);
   w.dx_acc = c.take<float>(s.T * s.H);
   w.gvec = dt == USAF_F32 ? c.take<float>(R_cap * s.I) : nullptr;
-  w.row_ptr = dt == USAF_BF16 ? c.take<int32_t>(s.E * 2 * s.I + s.E * s.H + 1) : nullptr;
+  w.tile_ptr = dt == USAF_BF16 ? c.take<int32_t>(tile_ptr_entries(s)) : nullptr;
   w.plan = dt == USAF_BF16 ? c.take<int32_t>(s.E + 1) : nullptr;
   w.dy_perm = dt == USAF_BF16 ? (void*)c.take<char>(R_cap * s.H * 2) : nullptr;
 }
@@ -492,23 +492,35 @@ usaf_status moe_fwd_launch(const MoeArgs& a, void* x_perm, void* h, void* wa, vo
                           static_cast<float*>(wa), static_cast<float*>(y), w, st);
 }
 
-// first active entry of every weight row (gate_up rows then down rows), by binary search
-__global__ void row_ptr_kernel(const int64_t* __restrict__ act_idx, int64_t K, int64_t n_gu_rows,
-                               int64_t n_rows, int H, int I, int64_t Ngu,
-                               int32_t* __restrict__ row_ptr) {
+// For every weight row (gate_up rows, then down rows) and every 256-column tile of it, the first
+// active entry at or after the tile's first column; entry NT of a row is the row's end.
+__global__ void tile_ptr_kernel(const int64_t* __restrict__ act, int64_t K, int64_t n_gu_rows,
+                                int64_t n_rows, int H, int I, int64_t Ngu, int nt_gu, int nt_d,
+                                int32_t* __restrict__ tp) {
   const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (r > n_rows) return;
-  int64_t key;
-  if (r < n_gu_rows) key = r * H;
-  else key = Ngu + (r - n_gu_rows) * I;
-  if (r == n_rows) key = INT64_MAX;
+  if (r >= n_rows) return;
+  const bool gu = r < n_gu_rows;
+  const int64_t base = gu ? r * H : Ngu + (r - n_gu_rows) * I;
+  const int ncols = gu ? H : I;
+  const int NT = gu ? nt_gu : nt_d;
+  int32_t* out = tp + (gu ? r * (nt_gu + 1) : n_gu_rows * (nt_gu + 1) + (r - n_gu_rows) * (nt_d + 1));
   int64_t lo = 0, hi = K;
   while (lo < hi) {
-    int64_t mid = (lo + hi) >> 1;
-    if (act_idx[mid] < key) lo = mid + 1;
+    const int64_t mid = (lo + hi) >> 1;
+    if (act[mid] < base) lo = mid + 1;
     else hi = mid;
   }
-  row_ptr[r] = (int32_t)lo;
+  int64_t cur = lo;
+  for (int nt = 0; nt < NT; ++nt) {
+    out[nt] = (int32_t)cur;
+    const int64_t lim = base + min((nt + 1) * 256, ncols);
+    while (cur < K && act[cur] < lim) ++cur;
+  }
+  out[NT] = (int32_t)cur;
+}
+
+int64_t tile_ptr_entries(const usaf_moe_shape& s) {
+  return s.E * 2 * s.I * (ceil_div(s.H, 256) + 1) + s.E * s.H * (ceil_div(s.I, 256) + 1);
 }
 
 template <typename T>
@@ -594,12 +606,13 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
     if (a.dt == USAF_BF16) {
       const int64_t n_gu_rows = s.E * 2 * s.I, n_rows = n_gu_rows + s.E * s.H;
       {
-      USAF_TRACE("wgrad_row_ptr", st);
-      row_ptr_kernel<<<(unsigned)ceil_div(n_rows + 1, 256), 256, 0, st>>>(
-          act_idx, K, n_gu_rows, n_rows, H, I, Ngu, w.row_ptr);
+      USAF_TRACE("wgrad_tile_ptr", st);
+      tile_ptr_kernel<<<(unsigned)ceil_div(n_rows, 256), 256, 0, st>>>(
+          act_idx, K, n_gu_rows, n_rows, H, I, Ngu, (int)ceil_div(H, 256), (int)ceil_div(I, 256),
+          w.tile_ptr);
       USAF_CHECK_LAUNCH();
       }
-      USAF_TRY(tc_bwd_wgrad(a, xp, dyp, dh, wa, act_idx, K, w.row_ptr, g_act, dev_status, st));
+      USAF_TRY(tc_bwd_wgrad(a, xp, dyp, dh, wa, act_idx, K, w.tile_ptr, g_act, dev_status, st));
     } else {
       USAF_TRACE("simt_wgrad", st);
       masked_wgrad_simt_kernel<T><<<(unsigned)ceil_div(K, 128), 128, 0, st>>>(

@@ -32,7 +32,9 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NUM_THREADS = 192;
+constexpr int EPI_WARPS = 8;  // two warps per TMEM lane quarter, alternating 32-column chunks
+constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
+constexpr int WG_PREFETCH = 8;  // active entries per row and tile held in registers
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_E = 1024;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + 2 * (MAX_E + 1) * 4;
@@ -56,7 +58,8 @@ struct Params {
   __nv_bfloat16* dh;
   const __nv_bfloat16* hin;
   const int64_t* act;
-  const int32_t* row_ptr;
+  const int32_t* tile_ptr;  // per weight row and N tile: first active entry (wgrad)
+  int64_t tp_base;          // offset of this variant's rows in tile_ptr
   float* g_act;
   int64_t Ngu;
   uint32_t* status;
@@ -173,6 +176,7 @@ struct Tile {
   int row0;   // first permuted row (token tiles) or the expert's first row (wgrad K base)
   int nrows;  // tokens in a token tile (multiple of 16)
   int n0;     // first N column (wgrad)
+  int nt;     // N tile index (wgrad)
   int klen;   // K extent
 };
 
@@ -218,7 +222,8 @@ __device__ __forceinline__ Tile get_tile(const Params& p, const int32_t* s_plan,
     ti.live = npad > 0;
     ti.e = e;
     ti.m0 = (local / p.NT) * BM;
-    ti.n0 = (local % p.NT) * BN;
+    ti.nt = local % p.NT;
+    ti.n0 = ti.nt * BN;
     ti.row0 = s_off[e];
     ti.nrows = BN;
     ti.klen = npad;
@@ -240,16 +245,62 @@ __device__ __forceinline__ float pick32(const float (&v)[32], int j) {
   return r;
 }
 
+// Column sums of a 32x32 block held one column per register: after 31 shuffles lane l holds the
+// sum over the warp's lanes of column l.
+__device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int j = 0; j < off; ++j) {
+      const float send = upper ? x[j] : x[j + off];
+      const float keep = upper ? x[j + off] : x[j];
+      x[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  return x[0];
+}
+
+__device__ __forceinline__ float sigmoid_fast(float z) { return __fdividef(1.f, 1.f + __expf(-z)); }
+
+// Per-thread state of the masked-gradient epilogue, filled before the accumulator is ready.
+struct WgRow {
+  int64_t a0, a1;  // active entries of this row inside the tile
+  int cols[WG_PREFETCH];
+  int64_t base;
+  bool rv;
+};
+
+template <int VAR>
+__device__ __forceinline__ WgRow wg_prefetch(const Params& p, const Tile& ti, int row) {
+  WgRow w{};
+  const bool gu = VAR == V_WG_GU;
+  const int mrows = gu ? 2 * p.I : p.H;
+  const int ncols = gu ? p.H : p.I;
+  const int j = ti.m0 + row;
+  w.rv = j < mrows;
+  w.base = gu ? ((int64_t)ti.e * 2 * p.I + j) * p.H : p.Ngu + ((int64_t)ti.e * p.H + j) * p.I;
+  w.a0 = w.a1 = 0;
+  if (w.rv) {
+    const int64_t tp = p.tp_base + ((int64_t)ti.e * mrows + j) * (p.NT + 1) + ti.nt;
+    w.a0 = p.tile_ptr[tp];
+    w.a1 = p.tile_ptr[tp + 1];
+  }
+#pragma unroll
+  for (int q = 0; q < WG_PREFETCH; ++q)
+    w.cols[q] = (w.a0 + q < w.a1) ? (int)(p.act[w.a0 + q] - w.base - ti.n0) : -1;
+  (void)ncols;
+  return w;
+}
+
 template <int VAR>
 __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32_t taddr, int row,
-                                         int lane) {
+                                         int lane, int half, const WgRow& wg) {
   constexpr unsigned FULL = 0xffffffffu;
   const int H = p.H, I = p.I;
   if constexpr (VarTraits<VAR>::token_tiled) {
     const int nch = (ti.nrows + 31) / 32;
-    for (int ch = 0; ch < nch; ++ch) {
-      float v[32];
-      tmem_ld32(taddr + ch * 32, v);
+    for (int ch = half; ch < nch; ch += 2) {
       const int cbase = ch * 32;
       const int col = cbase + lane;
       int slot = -1, tok = 0;
@@ -258,74 +309,90 @@ __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32
         tok = p.ptok[ti.row0 + col];
       }
       const float wl = slot >= 0 ? p.topk_w[slot] : 0.f;
+      const int ncol = min(32, ti.nrows - cbase);
+      if constexpr (VAR == V_GATEUP) {
+        float v[32];
+        tmem_ld32(taddr + ch * 32, v);
+        const int i = ti.m0 + (row >> 1);
+        const int g = row & 1;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        if (cbase + j >= ti.nrows) break;
-        const int64_t r = ti.row0 + cbase + j;
-        const int sj = __shfl_sync(FULL, slot, j);
-        if constexpr (VAR == V_GATEUP) {
-          const int i = ti.m0 + (row >> 1);
-          const int g = row & 1;
+        for (int j = 0; j < 32; ++j) {
+          if (j >= ncol) break;
+          const int64_t r = ti.row0 + cbase + j;
           const float mine = v[j];
           const float other = __shfl_xor_sync(FULL, mine, 1);
           const float wj = __shfl_sync(FULL, wl, j);
           p.h[r * 2 * I + g * I + i] = __float2bfloat16_rn(mine);
-          if (g == 0) p.wa[r * I + i] = __float2bfloat16_rn(wj * silu_f(mine) * other);
-        } else if constexpr (VAR == V_DOWN || VAR == V_DX) {
-          const int tj = __shfl_sync(FULL, tok, j);
-          const int hh = ti.m0 + row;
-          if (sj >= 0 && hh < H) atomicAdd(&p.acc_out[(int64_t)tj * H + hh], v[j]);
-        } else {  // V_GVEC
-          const int i = ti.m0 + row;
-          const bool iv = i < I;
-          const float wj = __shfl_sync(FULL, wl, j);
-          float gt = 0.f, ut = 0.f;
-          if (iv) {
-            gt = __bfloat162float(p.hin[r * 2 * I + i]);
-            ut = __bfloat162float(p.hin[r * 2 * I + I + i]);
-          }
-          const float gv = v[j];
-          const float sg = silu_f(gt);
-          float part = iv ? gv * sg * ut : 0.f;
+          if (g == 0)
+            p.wa[r * I + i] = __float2bfloat16_rn(wj * mine * sigmoid_fast(mine) * other);
+        }
+      } else if constexpr (VAR == V_DOWN || VAR == V_DX) {
+        float v[32];
+        tmem_ld32(taddr + ch * 32, v);
+        const int hh = ti.m0 + row;
 #pragma unroll
-          for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(FULL, part, o);
-          if (lane == 0 && sj >= 0) atomicAdd(&p.dw[sj], part);
-          if (iv) {
-            const float dA = wj * gv;
-            p.dh[r * 2 * I + i] = __float2bfloat16_rn(dA * ut * silu_grad_f(gt));
+        for (int j = 0; j < 32; ++j) {
+          if (j >= ncol) break;
+          const int sj = __shfl_sync(FULL, slot, j);
+          const int tj = __shfl_sync(FULL, tok, j);
+          if (sj >= 0 && hh < H) atomicAdd(&p.acc_out[(int64_t)tj * H + hh], v[j]);
+        }
+      } else {  // V_GVEC: SwiGLU backward, dh and the routing-weight gradient dw
+        const int i = ti.m0 + row;
+        const bool iv = i < I;
+        float gt[32], ut[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const bool ok = iv && j < ncol;
+          const int64_t r = ti.row0 + cbase + j;
+          gt[j] = ok ? __bfloat162float(__ldg(p.hin + r * 2 * I + i)) : 0.f;
+          ut[j] = ok ? __bfloat162float(__ldg(p.hin + r * 2 * I + I + i)) : 0.f;
+        }
+        float v[32];
+        tmem_ld32(taddr + ch * 32, v);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float wj = __shfl_sync(FULL, wl, j);
+          const float s = sigmoid_fast(gt[j]);
+          const float sg = gt[j] * s;
+          if (iv && j < ncol) {
+            const int64_t r = ti.row0 + cbase + j;
+            const float dA = wj * v[j];
+            p.dh[r * 2 * I + i] = __float2bfloat16_rn(dA * ut[j] * s * (1.f + gt[j] * (1.f - s)));
             p.dh[r * 2 * I + I + i] = __float2bfloat16_rn(dA * sg);
           }
+          v[j] = v[j] * sg * ut[j];
         }
+        const float dwsum = transpose_reduce32(v, lane);
+        if (slot >= 0) atomicAdd(&p.dw[slot], dwsum);
       }
     }
   } else {
     // masked weight gradient: keep the active entries of this row inside the tile's columns
-    const bool gu = VAR == V_WG_GU;
-    const int mrows = gu ? 2 * I : H;
-    const int ncols = gu ? H : I;
-    const int j = ti.m0 + row;
-    const bool rv = j < mrows;
-    const int64_t rid = gu ? (int64_t)ti.e * 2 * I + j : (int64_t)p.E * 2 * I + (int64_t)ti.e * H + j;
-    const int64_t base = gu ? rid * H : p.Ngu + ((int64_t)ti.e * H + j) * I;
-    int64_t cur = 0, end = 0;
-    if (rv) {
-      cur = p.row_ptr[rid];
-      end = p.row_ptr[rid + 1];
-      while (cur < end && p.act[cur] - base < ti.n0) ++cur;
-    }
+    const int ncols = VAR == V_WG_GU ? H : I;
     const int nvalid = min(BN, ncols - ti.n0);
     const int nch = (nvalid + 31) / 32;
     bool bad = false;
-    for (int ch = 0; ch < nch; ++ch) {
+    int64_t cur = wg.a0 + WG_PREFETCH;  // entries beyond the prefetched ones, loaded on the fly
+    for (int ch = half; ch < nch; ch += 2) {
       float v[32];
       tmem_ld32(taddr + ch * 32, v);
-      const int64_t lo = ti.n0 + ch * 32;
-      while (cur < end) {
-        const int64_t c = p.act[cur] - base;
-        if (c >= lo + 32) break;
-        const float val = pick32(v, (int)(c - lo));
-        p.g_act[cur] = val;
-        bad |= !isfinite(val);
+#pragma unroll
+      for (int q = 0; q < WG_PREFETCH; ++q) {
+        if (wg.cols[q] >= 0 && (wg.cols[q] >> 5) == ch) {
+          const float val = pick32(v, wg.cols[q] & 31);
+          p.g_act[wg.a0 + q] = val;
+          bad |= !isfinite(val);
+        }
+      }
+      while (cur < wg.a1) {
+        const int c = (int)(p.act[cur] - wg.base - ti.n0);
+        if ((c >> 5) > ch) break;
+        if ((c >> 5) == ch) {
+          const float val = pick32(v, c & 31);
+          p.g_act[cur] = val;
+          bad |= !isfinite(val);
+        }
         ++cur;
       }
     }
@@ -363,7 +430,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
-      mbar_init(tempty0 + 8 * a, 4);
+      mbar_init(tempty0 + 8 * a, EPI_WARPS);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -505,20 +572,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_wait(drain, 0, abort_flag);
     }
   } else {
-    // -------------------------------------------------------------- epilogue warps 2..5
+    // -------------------------------------------------------------- epilogue warps 2..9
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    const int half = (warp - 2) >> 2;
     const int row = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile ti = get_tile<VAR>(p, s_plan, s_off, t);
       if (!ti.live) continue;
+      WgRow wg{};
+      if constexpr (!VarTraits<VAR>::token_tiled) wg = wg_prefetch<VAR>(p, ti, row);
       int ok = 1;
       if (lane == 0) ok = mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      epilogue<VAR>(p, ti, tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN, row, lane);
+      epilogue<VAR>(p, ti, tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN, row, lane, half, wg);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
@@ -713,7 +783,7 @@ __global__ void zero_f32_tc_kernel(float* __restrict__ p, int64_t n) {
 
 usaf_status tc_bwd_wgrad(const MoeArgs& a, const void* x_perm, const void* dy_perm, const void* dh,
                          const void* wa, const int64_t* act_idx, int64_t K,
-                         const int32_t* row_ptr, float* g_act, uint32_t* dev_status,
+                         const int32_t* tile_ptr, float* g_act, uint32_t* dev_status,
                          cudaStream_t st) {
   // experts without tokens run no tile, so their active entries must read 0
   zero_f32_tc_kernel<<<grid_dim_for(K), 256, 0, st>>>(g_act, K);
@@ -721,7 +791,7 @@ usaf_status tc_bwd_wgrad(const MoeArgs& a, const void* x_perm, const void* dy_pe
   CUtensorMap ma, mb;
   Params p = base_params(a);
   p.act = act_idx;
-  p.row_ptr = row_ptr;
+  p.tile_ptr = tile_ptr;
   p.g_act = g_act;
   p.status = dev_status;
   // S9: gate_up entries, M = 2I weight rows, N = H columns, K = the expert's tokens
@@ -729,7 +799,9 @@ usaf_status tc_bwd_wgrad(const MoeArgs& a, const void* x_perm, const void* dy_pe
     return USAF_ERR_CUDA;
   p.MT = (int)(2 * a.s.I / BM);
   p.NT = (int)ceil_div(a.s.H, BN);
+  p.tp_base = 0;
   USAF_TRY(launch<V_WG_GU>(ma, mb, p, st));
+  p.tp_base = a.s.E * 2 * a.s.I * (p.NT + 1);
   // S10: down entries, M = H weight rows, N = I columns
   if (!map_2d(&ma, dy_perm, a.s.H, a.R_cap, 64, 64) || !map_2d(&mb, wa, a.s.I, a.R_cap, 64, 64))
     return USAF_ERR_CUDA;

@@ -11,52 +11,54 @@ namespace usaf {
 
 // ------------------------------------------------------------------------------------------------
 // S1: logits[t,e] = sum_h x[t,h] * Wr[e,h]  (fp32 FFMA, x upcast exactly)
-// Tile: 32 tokens x 64 experts per block, 256 threads, each thread 2 tokens x 4 experts.
+// Tile: 64 tokens x 64 experts per block, 256 threads, each thread 4 tokens x 4 experts; the
+// k-major shared tiles are read as float4, two vector loads per 16 FMAs.
 // ------------------------------------------------------------------------------------------------
 template <typename T>
 __global__ void __launch_bounds__(256) router_logits_kernel(const T* __restrict__ x,
                                                             const float* __restrict__ wr,
                                                             float* __restrict__ logits, int Tn,
                                                             int H, int E) {
-  constexpr int BT = 32, BE = 64, BK = 32;
-  __shared__ float xs[BK][BT + 1];
-  __shared__ float ws[BK][BE + 1];
+  constexpr int BT = 64, BE = 64, BK = 32, LD = 68;
+  __shared__ __align__(16) float xs[BK][LD];
+  __shared__ __align__(16) float ws[BK][LD];
   const int t0 = blockIdx.y * BT, e0 = blockIdx.x * BE;
   const int tid = threadIdx.x;
-  const int tr = tid / 16;  // 0..15 -> tokens tr*2, tr*2+1
-  const int ec = tid % 16;  // 0..15 -> experts ec*4 .. +3
-  float acc[2][4] = {};
+  const int tr = tid / 16;  // tokens tr*4 .. +3
+  const int ec = tid % 16;  // experts ec*4 .. +3
+  float acc[4][4] = {};
   for (int k0 = 0; k0 < H; k0 += BK) {
     for (int i = tid; i < BT * BK; i += 256) {
-      int tt = i / BK, kk = i % BK;
-      int t = t0 + tt, k = k0 + kk;
+      const int tt = i / BK, kk = i % BK;
+      const int t = t0 + tt, k = k0 + kk;
       xs[kk][tt] = (t < Tn && k < H) ? to_f32(x[(int64_t)t * H + k]) : 0.f;
     }
     for (int i = tid; i < BE * BK; i += 256) {
-      int ee = i / BK, kk = i % BK;
-      int e = e0 + ee, k = k0 + kk;
+      const int ee = i / BK, kk = i % BK;
+      const int e = e0 + ee, k = k0 + kk;
       ws[kk][ee] = (e < E && k < H) ? wr[(int64_t)e * H + k] : 0.f;
     }
     __syncthreads();
 #pragma unroll 8
     for (int kk = 0; kk < BK; ++kk) {
-      float a0 = xs[kk][tr * 2], a1 = xs[kk][tr * 2 + 1];
+      const float4 a = *reinterpret_cast<const float4*>(&xs[kk][tr * 4]);
+      const float4 b = *reinterpret_cast<const float4*>(&ws[kk][ec * 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w};
+      const float bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float b = ws[kk][ec * 4 + j];
-        acc[0][j] = fmaf(a0, b, acc[0][j]);
-        acc[1][j] = fmaf(a1, b, acc[1][j]);
-      }
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
     }
     __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    int t = t0 + tr * 2 + i;
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + tr * 4 + i;
     if (t >= Tn) continue;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      int e = e0 + ec * 4 + j;
+      const int e = e0 + ec * 4 + j;
       if (e < E) logits[(int64_t)t * E + e] = acc[i][j];
     }
   }
@@ -257,7 +259,7 @@ usaf_status route_launch(const usaf_moe_shape& s, const void* x, usaf_dtype xdt,
   if (!logits_in) {
     USAF_TRACE("route_logits", st);
     float* out = logits_out ? logits_out : w.logits;
-    dim3 grid((unsigned)ceil_div(E, 64), (unsigned)ceil_div(Tn, 32));
+    dim3 grid((unsigned)ceil_div(E, 64), (unsigned)ceil_div(Tn, 64));
     if (xdt == USAF_BF16)
       router_logits_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
           static_cast<const __nv_bfloat16*>(x), wr, out, Tn, H, E);
