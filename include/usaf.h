@@ -169,6 +169,8 @@ usaf_status usaf_moe_bwd_sparse(const usaf_moe_shape* shape, usaf_dtype dtype, i
  *   g, p, m, v   [n] fp32 (p is the fp32 master copy of the trained entries; p, m, v in place)
  *   w_seg0       dense weights holding flat indices [0, n_seg0); w_seg1 holds [n_seg0, ...) and
  *                may be NULL when every index is below n_seg0; both of w_dtype
+ *   lr, beta1, beta2, eps  host scalars; 1-b1, 1-b2 and the bias-corrected step size are formed
+ *                in double on the host and passed to the kernel as fp32
  *   step         1-based step count
  *   skip_if_nonfinite  if nonzero, the entry point first scans g, and no entry is updated when
  *                this scan or an earlier call (a bit already set in *dev_status, e.g. by
@@ -177,8 +179,8 @@ usaf_status usaf_moe_bwd_sparse(const usaf_moe_shape* shape, usaf_dtype dtype, i
  * ------------------------------------------------------------------------------------------- */
 usaf_status usaf_sparse_adam_step(int64_t n, const int64_t* idx, const float* g, float* p,
                                   float* m, float* v, void* w_seg0, int64_t n_seg0, void* w_seg1,
-                                  usaf_dtype w_dtype, float lr, float beta1, float beta2,
-                                  float eps, int64_t step, int skip_if_nonfinite,
+                                  usaf_dtype w_dtype, double lr, double beta1, double beta2,
+                                  double eps, int64_t step, int skip_if_nonfinite,
                                   uint32_t* dev_status, void* stream);
 
 /* ---------------------------------------------------------------------------------------------

@@ -50,6 +50,7 @@ class _Routing(ctypes.Structure):
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
 _F = ctypes.c_float
+_D = ctypes.c_double
 _INT = ctypes.c_int
 _SZ = ctypes.c_size_t
 
@@ -64,7 +65,7 @@ _SIGS = {
     "usaf_moe_bwd_workspace_size": (_SZ, [_P, _INT, _I64]),
     "usaf_moe_bwd_sparse": (_INT, [_P, _INT, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    _I64, _P, _P, _P, _P, _P, _P, _SZ, _P]),
-    "usaf_sparse_adam_step": (_INT, [_I64, _P, _P, _P, _P, _P, _P, _I64, _P, _INT, _F, _F, _F, _F,
+    "usaf_sparse_adam_step": (_INT, [_I64, _P, _P, _P, _P, _P, _P, _I64, _P, _INT, _D, _D, _D, _D,
                                      _I64, _INT, _P, _P]),
     "usaf_importance_select_workspace_size": (_SZ, [_I64, _I64]),
     "usaf_importance_select": (_INT, [_P, _I64, _I64, _P, _P, _P, _SZ, _P]),

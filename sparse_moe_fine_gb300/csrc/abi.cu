@@ -77,6 +77,7 @@ void trace_end(cudaStream_t st) {
 void route_ws_layout(const usaf_moe_shape& s, Carver& c, RouteWs& w) {
   w.logits = c.take<float>(s.T * s.E);
   w.chunk_hist = c.take<int32_t>(ceil_div(s.T * s.k, PERM_CHUNK) * s.E);
+  w.wr3 = c.take<char>(s.E * 3 * s.H * 2);
 }
 
 static bool shape_ok(const usaf_moe_shape* s) {
@@ -255,14 +256,14 @@ usaf_status usaf_moe_bwd_sparse(const usaf_moe_shape* s, usaf_dtype dt, int reno
 
 usaf_status usaf_sparse_adam_step(int64_t n, const int64_t* idx, const float* g, float* p,
                                   float* m, float* v, void* w_seg0, int64_t n_seg0, void* w_seg1,
-                                  usaf_dtype w_dtype, float lr, float beta1, float beta2,
-                                  float eps, int64_t step, int skip_if_nonfinite,
+                                  usaf_dtype w_dtype, double lr, double beta1, double beta2,
+                                  double eps, int64_t step, int skip_if_nonfinite,
                                   uint32_t* dev_status, void* stream) {
   if (n < 0 || step < 1 || !dtype_ok(w_dtype) || n_seg0 < 0) return USAF_ERR_INVALID_ARG;
   if (n > 0 && (!g || !p || !m || !v || !w_seg0)) return USAF_ERR_INVALID_ARG;
   if (!idx && n > n_seg0) return USAF_ERR_INVALID_ARG;
   if (skip_if_nonfinite && !dev_status) return USAF_ERR_INVALID_ARG;
-  if (!(beta1 >= 0.f && beta1 < 1.f && beta2 >= 0.f && beta2 < 1.f && eps >= 0.f))
+  if (!(beta1 >= 0.0 && beta1 < 1.0 && beta2 >= 0.0 && beta2 < 1.0 && eps >= 0.0))
     return USAF_ERR_INVALID_ARG;
   return adam_launch(n, idx, g, p, m, v, w_seg0, n_seg0, w_seg1, w_dtype, lr, beta1, beta2, eps,
                      step, skip_if_nonfinite, dev_status, static_cast<cudaStream_t>(stream));

@@ -45,8 +45,8 @@ __global__ void __launch_bounds__(256) adam_kernel(int64_t n, const int64_t* __r
 }
 
 usaf_status adam_launch(int64_t n, const int64_t* idx, const float* g, float* p, float* m,
-                        float* v, void* w0, int64_t n0, void* w1, usaf_dtype wdt, float lr,
-                        float b1, float b2, float eps, int64_t step, int skip,
+                        float* v, void* w0, int64_t n0, void* w1, usaf_dtype wdt, double lr,
+                        double b1, double b2, double eps, int64_t step, int skip,
                         uint32_t* dev_status, cudaStream_t st) {
   if (n == 0) return USAF_OK;
   USAF_TRACE("sparse_adam", st);
@@ -59,18 +59,19 @@ usaf_status adam_launch(int64_t n, const int64_t* idx, const float* g, float* p,
     USAF_CHECK_LAUNCH();
   }
   // bias corrections in double on the host, as one fp32 step size
-  const double bc1 = 1.0 - std::pow((double)b1, (double)step);
-  const double bc2 = 1.0 - std::pow((double)b2, (double)step);
-  const float step_size = (float)((double)lr * std::sqrt(bc2) / bc1);
-  const float om_b1 = (float)(1.0 - (double)b1), om_b2 = (float)(1.0 - (double)b2);
+  const double bc1 = 1.0 - std::pow(b1, (double)step);
+  const double bc2 = 1.0 - std::pow(b2, (double)step);
+  const float step_size = (float)(lr * std::sqrt(bc2) / bc1);
+  const float om_b1 = (float)(1.0 - b1), om_b2 = (float)(1.0 - b2);
+  const float b1f = (float)b1, b2f = (float)b2, epsf = (float)eps;
   if (wdt == USAF_BF16)
     adam_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, 0, st>>>(
         n, idx, g, p, m, v, static_cast<__nv_bfloat16*>(w0), n0,
-        static_cast<__nv_bfloat16*>(w1), b1, b2, om_b1, om_b2, eps, step_size, skip, dev_status);
+        static_cast<__nv_bfloat16*>(w1), b1f, b2f, om_b1, om_b2, epsf, step_size, skip, dev_status);
   else
     adam_kernel<float><<<(unsigned)blocks, threads, 0, st>>>(
-        n, idx, g, p, m, v, static_cast<float*>(w0), n0, static_cast<float*>(w1), b1, b2, om_b1,
-        om_b2, eps, step_size, skip, dev_status);
+        n, idx, g, p, m, v, static_cast<float*>(w0), n0, static_cast<float*>(w1), b1f, b2f, om_b1,
+        om_b2, epsf, step_size, skip, dev_status);
   USAF_CHECK_LAUNCH();
   return USAF_OK;
 }

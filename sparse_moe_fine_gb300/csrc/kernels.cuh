@@ -11,6 +11,7 @@ constexpr int PERM_CHUNK = 1024;
 struct RouteWs {
   float* logits;        // [T,E] when the caller gives no logits_out
   int32_t* chunk_hist;  // [nchunks, E]
+  void* wr3;            // [E, 3H] bf16 split of the router weight (tensor-core logits)
 };
 void route_ws_layout(const usaf_moe_shape& s, Carver& c, RouteWs& w);
 usaf_status route_launch(const usaf_moe_shape& s, const void* x, usaf_dtype xdt, const float* wr,
@@ -57,6 +58,8 @@ usaf_status moe_bwd_launch(const MoeArgs& a, int renorm, const float* logits, co
 
 // tensor-core (tcgen05) grouped GEMM stages, bf16 only
 bool tc_shape_ok(const usaf_moe_shape& s);
+usaf_status tc_router_logits(const usaf_moe_shape& s, const void* x, const float* wr, void* wr3,
+                             float* logits, cudaStream_t st);
 usaf_status tc_plan(const MoeArgs& a, cudaStream_t st);
 int64_t tile_ptr_entries(const usaf_moe_shape& s);
 usaf_status tc_fwd_gate_up(const MoeArgs& a, const void* x_perm, void* h, void* wa,
@@ -72,8 +75,8 @@ usaf_status tc_bwd_wgrad(const MoeArgs& a, const void* x_perm, const void* dy_pe
 
 // ---------------------------------------------------------------- optimizer
 usaf_status adam_launch(int64_t n, const int64_t* idx, const float* g, float* p, float* m,
-                        float* v, void* w0, int64_t n0, void* w1, usaf_dtype wdt, float lr,
-                        float b1, float b2, float eps, int64_t step, int skip,
+                        float* v, void* w0, int64_t n0, void* w1, usaf_dtype wdt, double lr,
+                        double b1, double b2, double eps, int64_t step, int skip,
                         uint32_t* dev_status, cudaStream_t st);
 
 // ---------------------------------------------------------------- selection / RigL

@@ -40,7 +40,7 @@ constexpr int MAX_E = 1024;
 constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + 2 * (MAX_E + 1) * 4;
 constexpr long long TIMEOUT_CYCLES = 1ll << 32;  // about two seconds
 
-enum Var { V_GATEUP = 0, V_DOWN = 1, V_GVEC = 2, V_DX = 3, V_WG_GU = 4, V_WG_D = 5 };
+enum Var { V_GATEUP = 0, V_DOWN = 1, V_GVEC = 2, V_DX = 3, V_WG_GU = 4, V_WG_D = 5, V_ROUTER = 6 };
 
 struct Params {
   const int32_t* cnt;
@@ -49,11 +49,11 @@ struct Params {
   const int32_t* pslot;
   const float* topk_w;
   const int32_t* plan;
-  int E, H, I;
+  int E, H, I, T;
   int MT, NT;
   __nv_bfloat16* h;
   __nv_bfloat16* wa;
-  float* acc_out;  // y_acc (S5) or dx_acc (S8)
+  float* acc_out;  // y_acc (S5), dx_acc (S8) or the router logits
   float* dw;
   __nv_bfloat16* dh;
   const __nv_bfloat16* hin;
@@ -182,10 +182,13 @@ struct Tile {
 
 template <int VAR>
 struct VarTraits {
-  static constexpr bool token_tiled = VAR <= V_DX;
-  static constexpr bool a_mn = VAR >= V_GVEC;
-  static constexpr bool b_mn = VAR >= V_WG_GU;
+  static constexpr bool token_tiled = VAR <= V_DX;        // N = an expert's routed tokens
+  static constexpr bool wgrad = VAR == V_WG_GU || VAR == V_WG_D;  // K = an expert's tokens
+  static constexpr bool router = VAR == V_ROUTER;         // plain GEMM over all tokens
+  static constexpr bool a_mn = VAR == V_GVEC || VAR == V_DX || wgrad;
+  static constexpr bool b_mn = wgrad;
 };
+constexpr int ROUTER_BN = 128;
 
 __device__ __forceinline__ int upper_bound_i32(const int32_t* a, int n, int v) {
   int lo = 0, hi = n;
@@ -215,6 +218,13 @@ __device__ __forceinline__ Tile get_tile(const Params& p, const int32_t* s_plan,
     ti.nrows = min(base, npad - nt * base);
     ti.n0 = 0;
     ti.klen = (VAR == V_GATEUP || VAR == V_GVEC) ? p.H : (VAR == V_DOWN ? p.I : 2 * p.I);
+  } else if constexpr (VarTraits<VAR>::router) {
+    const int mt = t / p.NT, nt = t % p.NT;
+    ti.live = 1;
+    ti.m0 = mt * BM;
+    ti.n0 = nt * ROUTER_BN;
+    ti.nrows = min(ROUTER_BN, (p.T - ti.n0 + 15) / 16 * 16);
+    ti.klen = 3 * p.H;
   } else {
     const int per = p.MT * p.NT;
     const int e = t / per, local = t % per;
@@ -234,6 +244,7 @@ __device__ __forceinline__ Tile get_tile(const Params& p, const int32_t* s_plan,
 template <int VAR>
 __device__ __forceinline__ int total_tiles(const Params& p, const int32_t* s_plan) {
   if constexpr (VarTraits<VAR>::token_tiled) return p.MT * s_plan[p.E];
+  else if constexpr (VarTraits<VAR>::router) return p.MT * p.NT;
   else return p.E * p.MT * p.NT;
 }
 
@@ -367,6 +378,19 @@ __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32
         if (slot >= 0) atomicAdd(&p.dw[slot], dwsum);
       }
     }
+  } else if constexpr (VarTraits<VAR>::router) {
+    // router logits: row = expert, columns = tokens
+    const int e = ti.m0 + row;
+    const int nch = (ti.nrows + 31) / 32;
+    for (int ch = half; ch < nch; ch += 2) {
+      float v[32];
+      tmem_ld32(taddr + ch * 32, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int tok = ti.n0 + ch * 32 + j;
+        if (e < p.E && tok < p.T) p.acc_out[(int64_t)tok * p.E + e] = v[j];
+      }
+    }
   } else {
     // masked weight gradient: keep the active entries of this row inside the tile's columns
     const int ncols = VAR == V_WG_GU ? H : I;
@@ -419,9 +443,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES;
   const uint32_t tfull0 = empty0 + 8 * STAGES, tempty0 = tfull0 + 16, drain = tempty0 + 16;
 
-  for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
-    s_off[i] = p.off[i];
-    if (VarTraits<VAR>::token_tiled) s_plan[i] = p.plan[i];
+  if constexpr (!VarTraits<VAR>::router) {
+    for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
+      s_off[i] = p.off[i];
+      if (VarTraits<VAR>::token_tiled) s_plan[i] = p.plan[i];
+    }
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -472,6 +498,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int k0 = kb * BK;
           uint32_t bytes = A_BYTES;
           if constexpr (VarTraits<VAR>::token_tiled) bytes += (ti.nrows > 128 ? 2 : 1) * 16384;
+          else if constexpr (VarTraits<VAR>::router) bytes += 16384;
           else bytes += B_BYTES;
           mbar_expect_tx(fb, bytes);
           if constexpr (VAR == V_GATEUP) {
@@ -481,6 +508,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           } else if constexpr (VAR == V_GVEC) {
             tma_2d(a_dst, &tmA, fb, ti.m0, ti.e * p.H + k0);
             tma_2d(a_dst + 8192, &tmA, fb, ti.m0 + 64, ti.e * p.H + k0);
+          } else if constexpr (VAR == V_ROUTER) {
+            tma_2d(a_dst, &tmA, fb, k0, ti.m0);
           } else if constexpr (VAR == V_DX) {
             tma_2d(a_dst, &tmA, fb, ti.m0, ti.e * 2 * p.I + k0);
             tma_2d(a_dst + 8192, &tmA, fb, ti.m0 + 64, ti.e * 2 * p.I + k0);
@@ -491,6 +520,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if constexpr (VarTraits<VAR>::token_tiled) {
             tma_2d(b_dst, &tmB, fb, k0, ti.row0);
             if (ti.nrows > 128) tma_2d(b_dst + 16384, &tmB, fb, k0, ti.row0 + 128);
+          } else if constexpr (VarTraits<VAR>::router) {
+            tma_2d(b_dst, &tmB, fb, k0 % p.H, ti.n0);  // x repeated for each split of Wr
           } else {
 #pragma unroll
             for (int q = 0; q < 4; ++q) tma_2d(b_dst + q * 8192, &tmB, fb, ti.n0 + 64 * q, ti.row0 + k0);
@@ -533,7 +564,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
-        const int n_mma = VarTraits<VAR>::token_tiled ? ti.nrows : BN;
+        const int n_mma = (VarTraits<VAR>::token_tiled || VarTraits<VAR>::router) ? ti.nrows : BN;
         const uint32_t idesc = idesc_bf16(n_mma, VarTraits<VAR>::a_mn, VarTraits<VAR>::b_mn);
         const int nkb = (ti.klen + BK - 1) / BK;
         for (int kb = 0; kb < nkb; ++kb) {
@@ -582,7 +613,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const Tile ti = get_tile<VAR>(p, s_plan, s_off, t);
       if (!ti.live) continue;
       WgRow wg{};
-      if constexpr (!VarTraits<VAR>::token_tiled) wg = wg_prefetch<VAR>(p, ti, row);
+      if constexpr (VarTraits<VAR>::wgrad) wg = wg_prefetch<VAR>(p, ti, row);
       int ok = 1;
       if (lane == 0) ok = mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -679,8 +710,9 @@ bool map_gate_up_interleaved(CUtensorMap* m, const void* base, uint64_t E, uint6
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr const char* VAR_NAME[6] = {"tc_gate_up_swiglu", "tc_down_combine", "tc_gvec_swiglu_bwd",
-                                     "tc_dx", "tc_wgrad_gate_up", "tc_wgrad_down"};
+constexpr const char* VAR_NAME[7] = {"tc_gate_up_swiglu", "tc_down_combine", "tc_gvec_swiglu_bwd",
+                                     "tc_dx", "tc_wgrad_gate_up", "tc_wgrad_down",
+                                     "tc_router_logits"};
 
 template <int VAR>
 usaf_status launch(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStream_t st) {
@@ -713,6 +745,31 @@ Params base_params(const MoeArgs& a) {
 }
 
 }  // namespace
+
+__global__ void router_split_kernel(const float* __restrict__ wr, int64_t E, int64_t H,
+                                    __nv_bfloat16* __restrict__ wr3);
+
+usaf_status tc_router_logits(const usaf_moe_shape& s, const void* x, const float* wr,
+                             void* wr3, float* logits, cudaStream_t st) {
+  {
+    USAF_TRACE("router_split", st);
+    router_split_kernel<<<grid_dim_for(s.E * s.H), 256, 0, st>>>(
+        wr, s.E, s.H, static_cast<__nv_bfloat16*>(wr3));
+    USAF_CHECK_LAUNCH();
+  }
+  CUtensorMap ma, mb;
+  if (!map_2d(&ma, wr3, 3 * s.H, s.E, 64, 128) || !map_2d(&mb, x, s.H, s.T, 64, 128))
+    return USAF_ERR_CUDA;
+  Params p{};
+  p.E = (int)s.E;
+  p.H = (int)s.H;
+  p.I = (int)s.I;
+  p.T = (int)s.T;
+  p.MT = (int)ceil_div(s.E, BM);
+  p.NT = (int)ceil_div(s.T, ROUTER_BN);
+  p.acc_out = logits;
+  return launch<V_ROUTER>(ma, mb, p, st);
+}
 
 bool tc_shape_ok(const usaf_moe_shape& s) {
   return s.H % 64 == 0 && s.I % 64 == 0 && s.E <= MAX_E && s.H <= (1 << 20) &&
@@ -773,6 +830,25 @@ usaf_status tc_bwd_dx(const MoeArgs& a, const void* dh, float* dx_acc, cudaStrea
   p.MT = (int)ceil_div(a.s.H, BM);
   p.acc_out = dx_acc;
   return launch<V_DX>(ma, mb, p, st);
+}
+
+// Router weight split for the tensor-core logits: w = hi + mid + lo, each part bf16 and each
+// residual exact in fp32, so x . w is carried by three bf16 products with fp32 accumulation.
+__global__ void router_split_kernel(const float* __restrict__ wr, int64_t E, int64_t H,
+                                    __nv_bfloat16* __restrict__ wr3) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < E * H;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = i / H, k = i % H;
+    const float w = wr[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    __nv_bfloat16* row = wr3 + e * 3 * H;
+    row[k] = hi;
+    row[H + k] = mid;
+    row[2 * H + k] = __float2bfloat16_rn(r2);
+  }
 }
 
 __global__ void zero_f32_tc_kernel(float* __restrict__ p, int64_t n) {

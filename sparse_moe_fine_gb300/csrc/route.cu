@@ -256,7 +256,12 @@ usaf_status route_launch(const usaf_moe_shape& s, const void* x, usaf_dtype xdt,
   const int Tn = (int)s.T, H = (int)s.H, E = (int)s.E, k = (int)s.k;
   const int64_t R = s.T * s.k;
   const float* logits = logits_in;
-  if (!logits_in) {
+  if (!logits_in && xdt == USAF_BF16 && tc_shape_ok(s)) {
+    // bf16 tokens: three bf16 tensor-core products of the split fp32 router weight
+    float* out = logits_out ? logits_out : w.logits;
+    USAF_TRY(tc_router_logits(s, x, wr, w.wr3, out, st));
+    logits = out;
+  } else if (!logits_in) {
     USAF_TRACE("route_logits", st);
     float* out = logits_out ? logits_out : w.logits;
     dim3 grid((unsigned)ceil_div(E, 64), (unsigned)ceil_div(Tn, 64));

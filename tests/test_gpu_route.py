@@ -64,10 +64,18 @@ def test_topk_bit_exact_given_logits(name, renorm):
     _check_perm(cfg, rt, oi)
 
 
-@pytest.mark.parametrize("name", ["tiny_fp32", "qwen3_30b_a3b"])
+SMALL = {"bf16_ragged": dict(T=300, H=256, E=8, k=2, I=64),
+         "bf16_two_m_tiles": dict(T=1000, H=128, E=160, k=4, I=64)}
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "qwen3_30b_a3b", "bf16_ragged",
+                                  "bf16_two_m_tiles"])
 def test_router_logits_and_routing_from_x(name):
+    """fp32 tokens: CUDA-core FFMA logits; bf16 tokens: three bf16 tensor-core products of the
+    split fp32 router weight. Both within the fp32 dot-product error bound of the oracle."""
     dev = device()
-    cfg = synth.CONFIGS[name]
+    cfg = synth.CONFIGS[name] if name in synth.CONFIGS else synth.small_config(
+        name, bf16=True, **SMALL[name])
     inp = synth.moe_inputs(cfg, seed=0)
     s, rt, gl = _route(cfg, inp, dev)
     ol = oracle.router_logits(inp["x"], inp["w_router"])
