@@ -274,43 +274,101 @@ __device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
 
 __device__ __forceinline__ float sigmoid_fast(float z) { return __fdividef(1.f, 1.f + __expf(-z)); }
 
-// Per-thread state of the masked-gradient epilogue, filled before the accumulator is ready.
-struct WgRow {
+// Operands an epilogue thread loads before its tile's accumulator is ready. The masked-gradient
+// epilogues need the active entries of their row in the tile (the range from tile_ptr, then the
+// columns from the active list: two dependent loads, issued two and one tiles ahead); the SwiGLU
+// backward needs gate and up of its feature for the tile's first 32 tokens.
+struct WgRange {
   int64_t a0, a1;  // active entries of this row inside the tile
-  int cols[WG_PREFETCH];
-  int64_t base;
-  bool rv;
+  int64_t base;    // flat index of the row's column 0
+};
+struct Pre {
+  WgRange r;
+  int cols[WG_PREFETCH];  // tile-relative columns of the first WG_PREFETCH entries (-1: none)
+  uint32_t hg[32];        // bf16 gate (low half) and up (high half) per token column
 };
 
 template <int VAR>
-__device__ __forceinline__ WgRow wg_prefetch(const Params& p, const Tile& ti, int row) {
-  WgRow w{};
+__device__ __forceinline__ WgRange wg_range(const Params& p, const Tile& ti, int row) {
+  WgRange w{0, 0, 0};
   const bool gu = VAR == V_WG_GU;
   const int mrows = gu ? 2 * p.I : p.H;
-  const int ncols = gu ? p.H : p.I;
   const int j = ti.m0 + row;
-  w.rv = j < mrows;
   w.base = gu ? ((int64_t)ti.e * 2 * p.I + j) * p.H : p.Ngu + ((int64_t)ti.e * p.H + j) * p.I;
-  w.a0 = w.a1 = 0;
-  if (w.rv) {
+  if (j < mrows) {
     const int64_t tp = p.tp_base + ((int64_t)ti.e * mrows + j) * (p.NT + 1) + ti.nt;
     w.a0 = p.tile_ptr[tp];
     w.a1 = p.tile_ptr[tp + 1];
   }
-#pragma unroll
-  for (int q = 0; q < WG_PREFETCH; ++q)
-    w.cols[q] = (w.a0 + q < w.a1) ? (int)(p.act[w.a0 + q] - w.base - ti.n0) : -1;
-  (void)ncols;
   return w;
+}
+
+// gate|up of feature i for the 32 token columns of chunk ch (0 outside the tile)
+__device__ __forceinline__ void load_h_chunk(const Params& p, const Tile& ti, int ch, int i,
+                                             uint32_t (&dst)[32]) {
+  const unsigned short* hb = reinterpret_cast<const unsigned short*>(p.hin);
+  const int I = p.I;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const bool ok = i < I && ch * 32 + j < ti.nrows;
+    const int64_t r = ti.row0 + ch * 32 + j;
+    const uint32_t g = ok ? __ldg(hb + r * 2 * I + i) : 0u;
+    const uint32_t u = ok ? __ldg(hb + r * 2 * I + I + i) : 0u;
+    dst[j] = g | (u << 16);
+  }
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+
+template <int VAR>
+__device__ __forceinline__ int next_live(const Params& p, const int32_t* s_plan,
+                                         const int32_t* s_off, int t, int total) {
+  if constexpr (VarTraits<VAR>::wgrad) {
+    while (t < total && !get_tile<VAR>(p, s_plan, s_off, t).live) t += gridDim.x;
+  }
+  return t < total ? t : total;
+}
+
+// first level of the lookahead: the wgrad row range of tile t
+template <int VAR>
+__device__ __forceinline__ WgRange prefetch_a(const Params& p, const int32_t* s_plan,
+                                              const int32_t* s_off, int t, int total, int row) {
+  if constexpr (VarTraits<VAR>::wgrad) {
+    if (t < total) return wg_range<VAR>(p, get_tile<VAR>(p, s_plan, s_off, t), row);
+  }
+  return WgRange{0, 0, 0};
+}
+
+// second level: wgrad active columns (from the range), or the first chunk of gate|up
+template <int VAR>
+__device__ __forceinline__ void prefetch_b(const Params& p, const int32_t* s_plan,
+                                           const int32_t* s_off, int t, int total, int row,
+                                           int half, const WgRange& r, Pre& out) {
+  out.r = r;
+  if constexpr (VarTraits<VAR>::wgrad) {
+    const int64_t n0 = t < total ? get_tile<VAR>(p, s_plan, s_off, t).n0 : 0;
+#pragma unroll
+    for (int q = 0; q < WG_PREFETCH; ++q)
+      out.cols[q] = (r.a0 + q < r.a1) ? (int)(p.act[r.a0 + q] - r.base - n0) : -1;
+  } else if constexpr (VAR == V_GVEC) {
+    if (t < total) {
+      const Tile ti = get_tile<VAR>(p, s_plan, s_off, t);
+      load_h_chunk(p, ti, half, ti.m0 + row, out.hg);
+    }
+  }
 }
 
 template <int VAR>
 __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32_t taddr, int row,
-                                         int lane, int half, const WgRow& wg) {
+                                         int lane, int half, const Pre& pre) {
   constexpr unsigned FULL = 0xffffffffu;
   const int H = p.H, I = p.I;
   if constexpr (VarTraits<VAR>::token_tiled) {
     const int nch = (ti.nrows + 31) / 32;
+    uint32_t hcur[32];  // gate|up of the chunk being processed (V_GVEC only)
+#pragma unroll
+    for (int j = 0; j < 32; ++j) hcur[j] = pre.hg[j];
     for (int ch = half; ch < nch; ch += 2) {
       const int cbase = ch * 32;
       const int col = cbase + lane;
@@ -351,31 +409,30 @@ __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32
       } else {  // V_GVEC: SwiGLU backward, dh and the routing-weight gradient dw
         const int i = ti.m0 + row;
         const bool iv = i < I;
-        float gt[32], ut[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const bool ok = iv && j < ncol;
-          const int64_t r = ti.row0 + cbase + j;
-          gt[j] = ok ? __bfloat162float(__ldg(p.hin + r * 2 * I + i)) : 0.f;
-          ut[j] = ok ? __bfloat162float(__ldg(p.hin + r * 2 * I + I + i)) : 0.f;
-        }
+        uint32_t nxt[32];
+        if (ch + 2 < nch) load_h_chunk(p, ti, ch + 2, i, nxt);  // in flight during this chunk
         float v[32];
         tmem_ld32(taddr + ch * 32, v);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const float wj = __shfl_sync(FULL, wl, j);
-          const float s = sigmoid_fast(gt[j]);
-          const float sg = gt[j] * s;
+          const float gt = bf_lo(hcur[j]), ut = bf_hi(hcur[j]);
+          const float s = sigmoid_fast(gt);
+          const float sg = gt * s;
           if (iv && j < ncol) {
             const int64_t r = ti.row0 + cbase + j;
             const float dA = wj * v[j];
-            p.dh[r * 2 * I + i] = __float2bfloat16_rn(dA * ut[j] * s * (1.f + gt[j] * (1.f - s)));
+            p.dh[r * 2 * I + i] = __float2bfloat16_rn(dA * ut * s * (1.f + gt * (1.f - s)));
             p.dh[r * 2 * I + I + i] = __float2bfloat16_rn(dA * sg);
           }
-          v[j] = v[j] * sg * ut[j];
+          v[j] = v[j] * sg * ut;
         }
         const float dwsum = transpose_reduce32(v, lane);
         if (slot >= 0) atomicAdd(&p.dw[slot], dwsum);
+        if (ch + 2 < nch) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) hcur[j] = nxt[j];
+        }
       }
     }
   } else if constexpr (VarTraits<VAR>::router) {
@@ -397,20 +454,21 @@ __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32
     const int nvalid = min(BN, ncols - ti.n0);
     const int nch = (nvalid + 31) / 32;
     bool bad = false;
-    int64_t cur = wg.a0 + WG_PREFETCH;  // entries beyond the prefetched ones, loaded on the fly
+    const WgRange& wr = pre.r;
+    int64_t cur = wr.a0 + WG_PREFETCH;  // entries beyond the prefetched ones, loaded on the fly
     for (int ch = half; ch < nch; ch += 2) {
       float v[32];
       tmem_ld32(taddr + ch * 32, v);
 #pragma unroll
       for (int q = 0; q < WG_PREFETCH; ++q) {
-        if (wg.cols[q] >= 0 && (wg.cols[q] >> 5) == ch) {
-          const float val = pick32(v, wg.cols[q] & 31);
-          p.g_act[wg.a0 + q] = val;
+        if (pre.cols[q] >= 0 && (pre.cols[q] >> 5) == ch) {
+          const float val = pick32(v, pre.cols[q] & 31);
+          p.g_act[wr.a0 + q] = val;
           bad |= !isfinite(val);
         }
       }
-      while (cur < wg.a1) {
-        const int c = (int)(p.act[cur] - wg.base - ti.n0);
+      while (cur < wr.a1) {
+        const int c = (int)(p.act[cur] - wr.base - ti.n0);
         if ((c >> 5) > ch) break;
         if ((c >> 5) == ch) {
           const float val = pick32(v, c & 31);
@@ -609,17 +667,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int row = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+    // this CTA's live tiles in order, with operand prefetches one and two tiles ahead
+    int t = next_live<VAR>(p, s_plan, s_off, blockIdx.x, total);
+    int t1 = t < total ? next_live<VAR>(p, s_plan, s_off, t + gridDim.x, total) : total;
+    Pre pre;
+    prefetch_b<VAR>(p, s_plan, s_off, t, total, row, half,
+                    prefetch_a<VAR>(p, s_plan, s_off, t, total, row), pre);
+    WgRange ra1 = prefetch_a<VAR>(p, s_plan, s_off, t1, total, row);
+    while (t < total) {
       const Tile ti = get_tile<VAR>(p, s_plan, s_off, t);
-      if (!ti.live) continue;
-      WgRow wg{};
-      if constexpr (VarTraits<VAR>::wgrad) wg = wg_prefetch<VAR>(p, ti, row);
+      const int t2 = t1 < total ? next_live<VAR>(p, s_plan, s_off, t1 + gridDim.x, total) : total;
+      Pre pre1;
+      prefetch_b<VAR>(p, s_plan, s_off, t1, total, row, half, ra1, pre1);
+      const WgRange ra2 = prefetch_a<VAR>(p, s_plan, s_off, t2, total, row);
       int ok = 1;
       if (lane == 0) ok = mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      epilogue<VAR>(p, ti, tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN, row, lane, half, wg);
+      epilogue<VAR>(p, ti, tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN, row, lane, half,
+                    pre);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
@@ -627,6 +694,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         acc = 0;
         acc_phase ^= 1;
       }
+      t = t1;
+      t1 = t2;
+      pre = pre1;
+      ra1 = ra2;
     }
   }
   tc_fence_before();
