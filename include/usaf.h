@@ -108,6 +108,32 @@ usaf_status usaf_route_topk(const usaf_moe_shape* shape, const void* x, usaf_dty
                             void* stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * usaf_route_topk_noalloc - usaf_route_topk for callers that cannot allocate device memory.
+ * The pages have no counterpart to this call; it exists for deployments in which the routing
+ * call site must not reach any allocator: servers whose device-memory pool is fixed once at
+ * start-up, code invoked from inside another runtime's memory manager (where allocating again
+ * would recurse or deadlock), and embedded targets that forbid dynamic device allocation after
+ * initialisation. Such callers cannot size and pass a workspace, so this call takes none.
+ * Same inputs, outputs and results as usaf_route_topk, except that logits_in or logits_out must
+ * be given (the logits are never kept in scratch).
+ * Scratch: a fixed device array of USAF_NOALLOC_SCRATCH_BYTES inside the library, which every
+ * GPU that loads the library holds until the process exits. It needs
+ * ceil(T*k/1024)*E*4 bytes (rounded up to 256) + 6*E*H bytes; a layer needing more is refused
+ * with USAF_ERR_WORKSPACE before anything is enqueued. The first call on each device looks up
+ * the array's device address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture. All calls share the one array and leave their scratch in it;
+ * every byte a call reads from it was written earlier by the same call, so nothing needs
+ * clearing, but calls whose work overlaps on the GPU (other streams, other host threads) race
+ * on it and must be serialised by the caller. No cudaMalloc, cudaFree or allocating library
+ * routine is called. Errors: INVALID_ARG, WORKSPACE, CUDA.
+ * ------------------------------------------------------------------------------------------- */
+#define USAF_NOALLOC_SCRATCH_BYTES (4u << 20)
+usaf_status usaf_route_topk_noalloc(const usaf_moe_shape* shape, const void* x,
+                                    usaf_dtype x_dtype, const float* w_router,
+                                    const float* logits_in, float* logits_out, int renorm,
+                                    const usaf_routing* rt, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
  * usaf_moe_fwd - grouped SwiGLU expert forward over the permuted rows.
  * For every routed slot (t, j) with expert e: h = gate_up_proj[e] . x[t]  (2I values; the first I
  * rows of gate_up_proj[e] are the gate, the last I the up projection), A = silu(gate) * up,

@@ -60,6 +60,7 @@ _SIGS = {
     "usaf_routed_rows_capacity": (_I64, [_P]),
     "usaf_route_topk_workspace_size": (_SZ, [_P]),
     "usaf_route_topk": (_INT, [_P, _P, _INT, _P, _P, _P, _INT, _P, _P, _SZ, _P]),
+    "usaf_route_topk_noalloc": (_INT, [_P, _P, _INT, _P, _P, _P, _INT, _P, _P]),
     "usaf_moe_fwd_workspace_size": (_SZ, [_P, _INT]),
     "usaf_moe_fwd": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "usaf_moe_bwd_workspace_size": (_SZ, [_P, _INT, _I64]),
@@ -181,6 +182,16 @@ def route_topk(s: Shape, x, w_router, rt: Routing, logits_in=None, logits_out=No
     _check("usaf_route_topk", lib().usaf_route_topk(
         ctypes.byref(s), _ptr(x), xdt, _ptr(w_router), _ptr(logits_in), _ptr(logits_out),
         int(renorm), ctypes.byref(r), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def route_topk_noalloc(s: Shape, x, w_router, rt: Routing, logits_in=None, logits_out=None,
+                       renorm=1, stream=None):
+    """usaf_route_topk_noalloc: no workspace argument; scratch is the library's fixed array."""
+    xdt = _dt(x) if x is not None else F32
+    r = rt.c()
+    _check("usaf_route_topk_noalloc", lib().usaf_route_topk_noalloc(
+        ctypes.byref(s), _ptr(x), xdt, _ptr(w_router), _ptr(logits_in), _ptr(logits_out),
+        int(renorm), ctypes.byref(r), _stream(stream)))
 
 
 def moe_fwd_workspace_size(s: Shape, dt: int) -> int:

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT, "libusaf.so")
-SOURCES = ["abi.cu", "route.cu", "moe.cu", "moe_tc.cu", "adam.cu", "select.cu"]
+SOURCES = ["abi.cu", "route.cu", "moe.cu", "moe_tc.cu", "adam.cu", "select.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
