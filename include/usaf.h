@@ -144,7 +144,8 @@ usaf_status usaf_route_topk_noalloc(const usaf_moe_shape* shape, const void* x,
  *                USAF_F32: everything fp32 on CUDA cores (any sizes).
  *   x            [T,H];  w_gate_up [E,2I,H];  w_down [E,H,I]
  *   x_perm_save  [R_cap,H]  out: x rows in permuted order (kept for the backward)
- *   h_save       [R_cap,2I] out: gate|up pre-activations per permuted row
+ *   h_save       [2I,R_cap] out: gate|up pre-activations, feature-major: element (j, row) is
+ *                feature j (gate for j < I, up for j >= I) of permuted row `row`
  *   wa_save      [R_cap,I]  out: w * A per permuted row (0 in padding rows)
  *   y            [T,H]      out
  * Errors: INVALID_ARG, UNSUPPORTED (bf16 shape limits), WORKSPACE, CUDA.

@@ -59,7 +59,7 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(P p) {
     }
 }
 
-// S4 (CUDA cores): h[row, n] = sum_k x_perm[row, k] * gate_up[e, n, k]
+// S4 (CUDA cores): h[n, row] = sum_k x_perm[row, k] * gate_up[e, n, k]  (h feature-major)
 template <typename T>
 struct ProbGateUp {
   const T* xp;
@@ -68,6 +68,7 @@ struct ProbGateUp {
   const int32_t* cnt;
   const int32_t* off;
   int H, I2;
+  int64_t rcap;
   __device__ void dims(int e, int& M, int& N, int& K) const {
     M = cnt[e];
     N = I2;
@@ -80,7 +81,7 @@ struct ProbGateUp {
     return to_f32(wgu[((int64_t)e * I2 + n) * H + k]);
   }
   __device__ void store(int e, int m, int n, float v) const {
-    h[(int64_t)(off[e] + m) * I2 + n] = from_f32<T>(v);
+    h[(int64_t)n * rcap + off[e] + m] = from_f32<T>(v);
   }
 };
 
@@ -166,14 +167,14 @@ struct ProbDx {
 template <typename T>
 __global__ void swiglu_fwd_rows_kernel(const T* __restrict__ h, const int32_t* __restrict__ pslot,
                                        const float* __restrict__ topk_w,
-                                       const int32_t* __restrict__ off_end, int I,
+                                       const int32_t* __restrict__ off_end, int I, int64_t rcap,
                                        T* __restrict__ wa) {
   const int64_t row = blockIdx.x;
   if (row >= *off_end) return;
   const int slot = pslot[row];
   const float w = slot >= 0 ? topk_w[slot] : 0.f;
   for (int j = threadIdx.x; j < I; j += blockDim.x) {
-    float g = to_f32(h[row * 2 * I + j]), u = to_f32(h[row * 2 * I + I + j]);
+    float g = to_f32(h[j * rcap + row]), u = to_f32(h[(I + j) * rcap + row]);
     wa[row * I + j] = from_f32<T>(slot >= 0 ? w * silu_f(g) * u : 0.f);
   }
 }
@@ -183,7 +184,7 @@ template <typename T>
 __global__ void swiglu_bwd_rows_kernel(const float* __restrict__ gvec, const T* __restrict__ h,
                                        const int32_t* __restrict__ pslot,
                                        const float* __restrict__ topk_w,
-                                       const int32_t* __restrict__ off_end, int I,
+                                       const int32_t* __restrict__ off_end, int I, int64_t rcap,
                                        T* __restrict__ dh, float* __restrict__ dw) {
   const int64_t row = blockIdx.x;
   if (row >= *off_end) return;
@@ -196,7 +197,7 @@ __global__ void swiglu_bwd_rows_kernel(const float* __restrict__ gvec, const T* 
   const float w = topk_w[slot];
   float part = 0.f;
   for (int j = threadIdx.x; j < I; j += blockDim.x) {
-    float g = to_f32(h[row * 2 * I + j]), u = to_f32(h[row * 2 * I + I + j]);
+    float g = to_f32(h[j * rcap + row]), u = to_f32(h[(I + j) * rcap + row]);
     float gv = gvec[row * I + j];
     float sg = silu_f(g);
     part = fmaf(gv, sg * u, part);
@@ -438,12 +439,12 @@ static usaf_status fwd_simt(const MoeArgs& a, T* xp, T* h, T* wa, float* yacc, c
   const int H = (int)s.H, I = (int)s.I, E = (int)s.E;
   const int32_t* cnt = a.rt.expert_count;
   const int32_t* off = a.rt.expert_offset;
-  ProbGateUp<T> p1{xp, static_cast<const T*>(a.w_gate_up), h, cnt, off, H, 2 * I};
+  ProbGateUp<T> p1{xp, static_cast<const T*>(a.w_gate_up), h, cnt, off, H, 2 * I, a.R_cap};
   dim3 g1((unsigned)ceil_div(2 * I, 64), (unsigned)ceil_div(s.T, 64), (unsigned)E);
   simt_gemm_kernel<<<g1, 256, 0, st>>>(p1);
   USAF_CHECK_LAUNCH();
   swiglu_fwd_rows_kernel<T><<<(unsigned)a.R_cap, 128, 0, st>>>(h, a.rt.perm_slot, a.rt.topk_w,
-                                                               off + E, I, wa);
+                                                               off + E, I, a.R_cap, wa);
   USAF_CHECK_LAUNCH();
   ProbDown<T> p2{wa, static_cast<const T*>(a.w_down), yacc, cnt, off, a.rt.perm_tok, H, I};
   dim3 g2((unsigned)ceil_div(H, 64), (unsigned)ceil_div(s.T, 64), (unsigned)E);
@@ -559,7 +560,7 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
     simt_gemm_kernel<<<g, 256, 0, st>>>(p);
     USAF_CHECK_LAUNCH();
     swiglu_bwd_rows_kernel<T><<<(unsigned)a.R_cap, 128, 0, st>>>(w.gvec, h, pslot, a.rt.topk_w,
-                                                                 off + E, I, dh, dw);
+                                                                 off + E, I, a.R_cap, dh, dw);
     USAF_CHECK_LAUNCH();
   }
   // S7: router gradient

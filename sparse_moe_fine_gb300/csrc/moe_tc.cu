@@ -35,9 +35,12 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_WARPS = 8;  // two warps per TMEM lane quarter, alternating 32-column chunks
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr int WG_PREFETCH = 8;  // active entries per row and tile held in registers
+constexpr int WG_PITCH = 20;    // floats per staged row: 16 columns + 4 (bank-conflict-free)
+constexpr int WG_STAGE_BYTES = EPI_WARPS * 32 * WG_PITCH * 4;
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_E = 1024;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + 2 * (MAX_E + 1) * 4;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + 2 * (MAX_E + 1) * 4 +
+                           WG_STAGE_BYTES;
 constexpr long long TIMEOUT_CYCLES = 1ll << 32;  // about two seconds
 
 enum Var { V_GATEUP = 0, V_DOWN = 1, V_GVEC = 2, V_DX = 3, V_WG_GU = 4, V_WG_D = 5, V_ROUTER = 6 };
@@ -62,6 +65,7 @@ struct Params {
   int64_t tp_base;          // offset of this variant's rows in tile_ptr
   float* g_act;
   int64_t Ngu;
+  int64_t R_cap;  // row pitch of the feature-major h (gate|up) array
   uint32_t* status;
 };
 
@@ -285,7 +289,8 @@ struct WgRange {
 struct Pre {
   WgRange r;
   int cols[WG_PREFETCH];  // tile-relative columns of the first WG_PREFETCH entries (-1: none)
-  uint32_t hg[32];        // bf16 gate (low half) and up (high half) per token column
+  uint32_t hg[16];        // gate of the first 32 token columns, two bf16 per word
+  uint32_t hu[16];        // up, likewise
 };
 
 template <int VAR>
@@ -303,23 +308,29 @@ __device__ __forceinline__ WgRange wg_range(const Params& p, const Tile& ti, int
   return w;
 }
 
-// gate|up of feature i for the 32 token columns of chunk ch (0 outside the tile)
+// gate and up of feature i for the 32 token columns of chunk ch, read from the feature-major h
+// as 16-byte vectors (two tokens per word; zero outside the tile)
 __device__ __forceinline__ void load_h_chunk(const Params& p, const Tile& ti, int ch, int i,
-                                             uint32_t (&dst)[32]) {
-  const unsigned short* hb = reinterpret_cast<const unsigned short*>(p.hin);
-  const int I = p.I;
+                                             uint32_t (&g)[16], uint32_t (&u)[16]) {
+  const int ncol = min(32, ti.nrows - ch * 32);
+  const bool iv = i < p.I;
+  const int64_t off = ti.row0 + ch * 32;
+  const uint4* gp = reinterpret_cast<const uint4*>(p.hin + (int64_t)i * p.R_cap + off);
+  const uint4* up = reinterpret_cast<const uint4*>(p.hin + (int64_t)(p.I + i) * p.R_cap + off);
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const bool ok = i < I && ch * 32 + j < ti.nrows;
-    const int64_t r = ti.row0 + ch * 32 + j;
-    const uint32_t g = ok ? __ldg(hb + r * 2 * I + i) : 0u;
-    const uint32_t u = ok ? __ldg(hb + r * 2 * I + I + i) : 0u;
-    dst[j] = g | (u << 16);
+  for (int q = 0; q < 4; ++q) {
+    const bool ok = iv && q * 8 < ncol;
+    const uint4 a = ok ? __ldg(gp + q) : make_uint4(0, 0, 0, 0);
+    const uint4 b = ok ? __ldg(up + q) : make_uint4(0, 0, 0, 0);
+    g[4 * q] = a.x; g[4 * q + 1] = a.y; g[4 * q + 2] = a.z; g[4 * q + 3] = a.w;
+    u[4 * q] = b.x; u[4 * q + 1] = b.y; u[4 * q + 2] = b.z; u[4 * q + 3] = b.w;
   }
 }
 
-__device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xFFFF0000u); }
+// bf16 number j (0..31) of a packed array of 16 words
+__device__ __forceinline__ float bf_at(const uint32_t (&a)[16], int j) {
+  return (j & 1) ? __uint_as_float(a[j >> 1] & 0xFFFF0000u) : __uint_as_float(a[j >> 1] << 16);
+}
 
 template <int VAR>
 __device__ __forceinline__ int next_live(const Params& p, const int32_t* s_plan,
@@ -354,21 +365,24 @@ __device__ __forceinline__ void prefetch_b(const Params& p, const int32_t* s_pla
   } else if constexpr (VAR == V_GVEC) {
     if (t < total) {
       const Tile ti = get_tile<VAR>(p, s_plan, s_off, t);
-      load_h_chunk(p, ti, half, ti.m0 + row, out.hg);
+      load_h_chunk(p, ti, half, ti.m0 + row, out.hg, out.hu);
     }
   }
 }
 
 template <int VAR>
 __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32_t taddr, int row,
-                                         int lane, int half, const Pre& pre) {
+                                         int lane, int half, const Pre& pre, float* stage) {
   constexpr unsigned FULL = 0xffffffffu;
   const int H = p.H, I = p.I;
   if constexpr (VarTraits<VAR>::token_tiled) {
     const int nch = (ti.nrows + 31) / 32;
-    uint32_t hcur[32];  // gate|up of the chunk being processed (V_GVEC only)
+    uint32_t hg[16], hu[16];  // gate and up of the chunk being processed (V_GVEC only)
 #pragma unroll
-    for (int j = 0; j < 32; ++j) hcur[j] = pre.hg[j];
+    for (int j = 0; j < 16; ++j) {
+      hg[j] = pre.hg[j];
+      hu[j] = pre.hu[j];
+    }
     for (int ch = half; ch < nch; ch += 2) {
       const int cbase = ch * 32;
       const int col = cbase + lane;
@@ -384,16 +398,30 @@ __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32
         tmem_ld32(taddr + ch * 32, v);
         const int i = ti.m0 + (row >> 1);
         const int g = row & 1;
+        // h is feature-major: this thread's 32 tokens of row g*I+i are 64 contiguous bytes
+        uint4* hp = reinterpret_cast<uint4*>(p.h + (int64_t)(g * I + i) * p.R_cap + ti.row0 + cbase);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (q * 8 < ncol) {
+            uint32_t w4[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const __nv_bfloat162 pr = __floats2bfloat162_rn(v[q * 8 + 2 * k], v[q * 8 + 2 * k + 1]);
+              w4[k] = *reinterpret_cast<const uint32_t*>(&pr);
+            }
+            hp[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           if (j >= ncol) break;
-          const int64_t r = ti.row0 + cbase + j;
           const float mine = v[j];
           const float other = __shfl_xor_sync(FULL, mine, 1);
           const float wj = __shfl_sync(FULL, wl, j);
-          p.h[r * 2 * I + g * I + i] = __float2bfloat16_rn(mine);
-          if (g == 0)
+          if (g == 0) {
+            const int64_t r = ti.row0 + cbase + j;
             p.wa[r * I + i] = __float2bfloat16_rn(wj * mine * sigmoid_fast(mine) * other);
+          }
         }
       } else if constexpr (VAR == V_DOWN || VAR == V_DX) {
         float v[32];
@@ -409,14 +437,14 @@ __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32
       } else {  // V_GVEC: SwiGLU backward, dh and the routing-weight gradient dw
         const int i = ti.m0 + row;
         const bool iv = i < I;
-        uint32_t nxt[32];
-        if (ch + 2 < nch) load_h_chunk(p, ti, ch + 2, i, nxt);  // in flight during this chunk
+        uint32_t ng[16], nu[16];
+        if (ch + 2 < nch) load_h_chunk(p, ti, ch + 2, i, ng, nu);  // in flight during this chunk
         float v[32];
         tmem_ld32(taddr + ch * 32, v);
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
           const float wj = __shfl_sync(FULL, wl, j);
-          const float gt = bf_lo(hcur[j]), ut = bf_hi(hcur[j]);
+          const float gt = bf_at(hg, j), ut = bf_at(hu, j);
           const float s = sigmoid_fast(gt);
           const float sg = gt * s;
           if (iv && j < ncol) {
@@ -431,7 +459,10 @@ __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32
         if (slot >= 0) atomicAdd(&p.dw[slot], dwsum);
         if (ch + 2 < nch) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) hcur[j] = nxt[j];
+          for (int j = 0; j < 16; ++j) {
+            hg[j] = ng[j];
+            hu[j] = nu[j];
+          }
         }
       }
     }
@@ -456,26 +487,39 @@ __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32
     bool bad = false;
     const WgRange& wr = pre.r;
     int64_t cur = wr.a0 + WG_PREFETCH;  // entries beyond the prefetched ones, loaded on the fly
+    float* my = stage + lane * WG_PITCH;  // this thread's staged row (16 columns)
     for (int ch = half; ch < nch; ch += 2) {
       float v[32];
       tmem_ld32(taddr + ch * 32, v);
 #pragma unroll
-      for (int q = 0; q < WG_PREFETCH; ++q) {
-        if (pre.cols[q] >= 0 && (pre.cols[q] >> 5) == ch) {
-          const float val = pick32(v, pre.cols[q] & 31);
-          p.g_act[wr.a0 + q] = val;
-          bad |= !isfinite(val);
+      for (int hh = 0; hh < 2; ++hh) {  // two halves of 16 columns through shared memory
+        const int lo = ch * 32 + hh * 16;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          *reinterpret_cast<float4*>(my + 4 * k) =
+              make_float4(v[hh * 16 + 4 * k], v[hh * 16 + 4 * k + 1], v[hh * 16 + 4 * k + 2],
+                          v[hh * 16 + 4 * k + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < WG_PREFETCH; ++q) {
+          const int c = pre.cols[q] - lo;
+          if (c >= 0 && c < 16) {
+            const float val = my[c];
+            p.g_act[wr.a0 + q] = val;
+            bad |= !isfinite(val);
+          }
         }
-      }
-      while (cur < wr.a1) {
-        const int c = (int)(p.act[cur] - wr.base - ti.n0);
-        if ((c >> 5) > ch) break;
-        if ((c >> 5) == ch) {
-          const float val = pick32(v, c & 31);
-          p.g_act[cur] = val;
-          bad |= !isfinite(val);
+        while (cur < wr.a1) {
+          const int c = (int)(p.act[cur] - wr.base - ti.n0) - lo;
+          if (c >= 16) break;
+          if (c >= 0) {
+            const float val = my[c];
+            p.g_act[cur] = val;
+            bad |= !isfinite(val);
+          }
+          ++cur;
         }
-        ++cur;
+        __syncwarp();
       }
     }
     if (bad) flag_status(p.status, USAF_DEV_NONFINITE);
@@ -496,6 +540,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int32_t* s_plan = reinterpret_cast<int32_t*>(smem + STAGES * STAGE_BYTES + 256);
   int32_t* s_off = s_plan + (MAX_E + 1);
+  float* s_stage = reinterpret_cast<float*>(s_off + (MAX_E + 1));  // wgrad staging, per warp
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES;
@@ -686,7 +731,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       epilogue<VAR>(p, ti, tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN, row, lane, half,
-                    pre);
+                    pre, s_stage + (warp - 2) * 32 * WG_PITCH);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
@@ -812,6 +857,7 @@ Params base_params(const MoeArgs& a) {
   p.H = (int)a.s.H;
   p.I = (int)a.s.I;
   p.Ngu = a.s.E * 2 * a.s.I * a.s.H;
+  p.R_cap = a.R_cap;
   return p;
 }
 

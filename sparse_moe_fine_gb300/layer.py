@@ -36,7 +36,7 @@ class MoELayer:
         self.rt = B.Routing.empty(self.s, d)
         self.logits = torch.empty(T, E, device=d)
         self.x_perm = torch.empty(cap, H, dtype=self.dtype, device=d)
-        self.h = torch.empty(cap, 2 * I, dtype=self.dtype, device=d)
+        self.h = torch.empty(2 * I, cap, dtype=self.dtype, device=d)  # feature-major
         self.wa = torch.empty(cap, I, dtype=self.dtype, device=d)
         self.y = torch.empty(T, H, dtype=self.dtype, device=d)
         self.dx = torch.empty(T, H, dtype=self.dtype, device=d)
