@@ -39,8 +39,9 @@ constexpr int WG_PITCH = 20;    // floats per staged row: 16 columns + 4 (bank-c
 constexpr int WG_STAGE_BYTES = EPI_WARPS * 32 * WG_PITCH * 4;
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_E = 1024;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + 2 * (MAX_E + 1) * 4 +
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + 2 * (MAX_E + 1) * 4 + 128 +
                            WG_STAGE_BYTES;
+static_assert(SMEM_BYTES <= 232448, "shared memory of the tensor-core kernel");
 constexpr long long TIMEOUT_CYCLES = 1ll << 32;  // about two seconds
 
 enum Var { V_GATEUP = 0, V_DOWN = 1, V_GVEC = 2, V_DX = 3, V_WG_GU = 4, V_WG_D = 5, V_ROUTER = 6 };
@@ -54,6 +55,7 @@ struct Params {
   const int32_t* plan;
   int E, H, I, T;
   int MT, NT;
+  int cl;  // CTAs per cluster along M; they share each B tile by TMA multicast
   __nv_bfloat16* h;
   __nv_bfloat16* wa;
   float* acc_out;  // y_acc (S5), dx_acc (S8) or the router logits
@@ -111,6 +113,23 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, uin
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
 }
+__device__ __forceinline__ void tma_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                          int c0, int c1, uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ uint32_t cta_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
 __device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
                                        int c1, int c2, int c3) {
   asm volatile(
@@ -136,6 +155,14 @@ __device__ __forceinline__ void umma_bf16(uint32_t d, uint64_t a, uint64_t b, ui
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+// arrive on the same barrier in every CTA of the cluster named by mask once the MMAs complete
+__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"(mask)
       : "memory");
 }
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
@@ -209,10 +236,12 @@ __device__ __forceinline__ Tile get_tile(const Params& p, const int32_t* s_plan,
                                          const int32_t* s_off, int t) {
   Tile ti{};
   if constexpr (VarTraits<VAR>::token_tiled) {
-    const int e = upper_bound_i32(s_plan, p.E + 1, t / p.MT) - 1;
+    // t counts cluster tiles (e, M group, token tile); this CTA takes M tile group * cl + rank
+    const int mtc = p.MT / p.cl;
+    const int e = upper_bound_i32(s_plan, p.E + 1, t / mtc) - 1;
     const int nts = s_plan[e + 1] - s_plan[e];
-    const int local = t - p.MT * s_plan[e];
-    const int mt = local / nts, nt = local % nts;
+    const int local = t - mtc * s_plan[e];
+    const int mt = (local / nts) * p.cl + (int)cta_rank(), nt = local % nts;
     const int npad = s_off[e + 1] - s_off[e];
     const int base = ((npad + nts - 1) / nts + 15) / 16 * 16;
     ti.live = 1;
@@ -230,12 +259,12 @@ __device__ __forceinline__ Tile get_tile(const Params& p, const int32_t* s_plan,
     ti.nrows = min(ROUTER_BN, (p.T - ti.n0 + 15) / 16 * 16);
     ti.klen = 3 * p.H;
   } else {
-    const int per = p.MT * p.NT;
+    const int per = (p.MT / p.cl) * p.NT;
     const int e = t / per, local = t % per;
     const int npad = s_off[e + 1] - s_off[e];
     ti.live = npad > 0;
     ti.e = e;
-    ti.m0 = (local / p.NT) * BM;
+    ti.m0 = ((local / p.NT) * p.cl + (int)cta_rank()) * BM;
     ti.nt = local % p.NT;
     ti.n0 = ti.nt * BN;
     ti.row0 = s_off[e];
@@ -247,9 +276,9 @@ __device__ __forceinline__ Tile get_tile(const Params& p, const int32_t* s_plan,
 
 template <int VAR>
 __device__ __forceinline__ int total_tiles(const Params& p, const int32_t* s_plan) {
-  if constexpr (VarTraits<VAR>::token_tiled) return p.MT * s_plan[p.E];
+  if constexpr (VarTraits<VAR>::token_tiled) return (p.MT / p.cl) * s_plan[p.E];
   else if constexpr (VarTraits<VAR>::router) return p.MT * p.NT;
-  else return p.E * p.MT * p.NT;
+  else return p.E * (p.MT / p.cl) * p.NT;
 }
 
 // ---------------------------------------------------------------------------- epilogues
@@ -336,7 +365,7 @@ template <int VAR>
 __device__ __forceinline__ int next_live(const Params& p, const int32_t* s_plan,
                                          const int32_t* s_off, int t, int total) {
   if constexpr (VarTraits<VAR>::wgrad) {
-    while (t < total && !get_tile<VAR>(p, s_plan, s_off, t).live) t += gridDim.x;
+    while (t < total && !get_tile<VAR>(p, s_plan, s_off, t).live) t += gridDim.x / p.cl;
   }
   return t < total ? t : total;
 }
@@ -540,7 +569,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int32_t* s_plan = reinterpret_cast<int32_t*>(smem + STAGES * STAGE_BYTES + 256);
   int32_t* s_off = s_plan + (MAX_E + 1);
-  float* s_stage = reinterpret_cast<float*>(s_off + (MAX_E + 1));  // wgrad staging, per warp
+  // wgrad staging, per warp; float4 stores need 16-byte alignment
+  float* s_stage = reinterpret_cast<float*>(
+      (reinterpret_cast<uintptr_t>(s_off + (MAX_E + 1)) + 127) & ~uintptr_t(127));
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES;
@@ -555,7 +586,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, p.cl);  // one release from every CTA of the cluster
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
@@ -575,8 +606,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (p.cl > 1) cluster_sync();  // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  const int cid = blockIdx.x / p.cl, ncl = gridDim.x / p.cl;
+  const uint32_t rank = cta_rank();
+  const uint16_t mc_mask = (uint16_t)((1u << p.cl) - 1);
   const int total = total_tiles<VAR>(p, s_plan);
   bool failed = false;
 
@@ -586,7 +621,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;
-      for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
+      for (int t = cid; t < total && !failed; t += ncl) {
         const Tile ti = get_tile<VAR>(p, s_plan, s_off, t);
         if (!ti.live) continue;
         const int nkb = (ti.klen + BK - 1) / BK;
@@ -621,13 +656,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tma_2d(a_dst + 8192, &tmA, fb, ti.m0 + 64, ti.row0 + k0);
           }
           if constexpr (VarTraits<VAR>::token_tiled) {
-            tma_2d(b_dst, &tmB, fb, k0, ti.row0);
-            if (ti.nrows > 128) tma_2d(b_dst + 16384, &tmB, fb, k0, ti.row0 + 128);
+            // the cluster's CTAs split the B boxes; each multicasts its box to all of them
+            const int nbox = ti.nrows > 128 ? 2 : 1;
+            for (int bx = 0; bx < nbox; ++bx) {
+              if (p.cl == 1) tma_2d(b_dst + bx * 16384, &tmB, fb, k0, ti.row0 + 128 * bx);
+              else if (bx % p.cl == (int)rank)
+                tma_2d_mc(b_dst + bx * 16384, &tmB, fb, k0, ti.row0 + 128 * bx, mc_mask);
+            }
           } else if constexpr (VarTraits<VAR>::router) {
             tma_2d(b_dst, &tmB, fb, k0 % p.H, ti.n0);  // x repeated for each split of Wr
           } else {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tma_2d(b_dst + q * 8192, &tmB, fb, ti.n0 + 64 * q, ti.row0 + k0);
+            for (int q = 0; q < 4; ++q) {
+              if (p.cl == 1) tma_2d(b_dst + q * 8192, &tmB, fb, ti.n0 + 64 * q, ti.row0 + k0);
+              else if (q % p.cl == (int)rank)
+                tma_2d_mc(b_dst + q * 8192, &tmB, fb, ti.n0 + 64 * q, ti.row0 + k0, mc_mask);
+            }
           }
           ++issued;
           if (++stage == STAGES) {
@@ -658,7 +702,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t b_step = VarTraits<VAR>::b_mn ? 2048 : 32;
       const uint32_t a_lbo = VarTraits<VAR>::a_mn ? 8192 : 16;
       const uint32_t b_lbo = VarTraits<VAR>::b_mn ? 8192 : 16;
-      for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
+      for (int t = cid; t < total && !failed; t += ncl) {
         const Tile ti = get_tile<VAR>(p, s_plan, s_off, t);
         if (!ti.live) continue;
         if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag)) {
@@ -684,7 +728,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint64_t bd = sdesc(b_base + ks * b_step, b_lbo, 1024);
             umma_bf16(d, ad, bd, idesc, (kb | ks) != 0 ? 1u : 0u);
           }
-          umma_commit(empty0 + 8 * stage);
+          if (p.cl > 1) umma_commit_mc(empty0 + 8 * stage, mc_mask);
+          else umma_commit(empty0 + 8 * stage);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -713,15 +758,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     // this CTA's live tiles in order, with operand prefetches one and two tiles ahead
-    int t = next_live<VAR>(p, s_plan, s_off, blockIdx.x, total);
-    int t1 = t < total ? next_live<VAR>(p, s_plan, s_off, t + gridDim.x, total) : total;
+    int t = next_live<VAR>(p, s_plan, s_off, cid, total);
+    int t1 = t < total ? next_live<VAR>(p, s_plan, s_off, t + ncl, total) : total;
     Pre pre;
     prefetch_b<VAR>(p, s_plan, s_off, t, total, row, half,
                     prefetch_a<VAR>(p, s_plan, s_off, t, total, row), pre);
     WgRange ra1 = prefetch_a<VAR>(p, s_plan, s_off, t1, total, row);
     while (t < total) {
       const Tile ti = get_tile<VAR>(p, s_plan, s_off, t);
-      const int t2 = t1 < total ? next_live<VAR>(p, s_plan, s_off, t1 + gridDim.x, total) : total;
+      const int t2 = t1 < total ? next_live<VAR>(p, s_plan, s_off, t1 + ncl, total) : total;
       Pre pre1;
       prefetch_b<VAR>(p, s_plan, s_off, t1, total, row, half, ra1, pre1);
       const WgRange ra2 = prefetch_a<VAR>(p, s_plan, s_off, t2, total, row);
@@ -747,6 +792,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (p.cl > 1) cluster_sync();  // no peer multicasts into or arrives on this CTA any more
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
@@ -831,16 +877,42 @@ constexpr const char* VAR_NAME[7] = {"tc_gate_up_swiglu", "tc_down_combine", "tc
                                      "tc_router_logits"};
 
 template <int VAR>
-usaf_status launch(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStream_t st) {
+usaf_status launch(const CUtensorMap& a, const CUtensorMap& b, Params p, cudaStream_t st) {
   USAF_TRACE(VAR_NAME[VAR], st);
   static bool attr_done = false;
+  static int grid_for_cl[3] = {0, 0, 0};
   if (!attr_done) {
     if (cudaFuncSetAttribute(tc_gemm_kernel<VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              SMEM_BYTES) != cudaSuccess)
       return USAF_ERR_CUDA;
     attr_done = true;
   }
-  tc_gemm_kernel<VAR><<<device_sm_count(), NUM_THREADS, SMEM_BYTES, st>>>(a, b, p);
+  // clusters of two along M when the M tiles pair up (they share every B tile)
+  if (p.cl != 1 && p.cl != 2) p.cl = 1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int& grid = grid_for_cl[p.cl];
+  if (grid == 0) {
+    int clusters = 0;
+    cfg.gridDim = dim3(device_sm_count());
+    if (cudaOccupancyMaxActiveClusters(&clusters, tc_gemm_kernel<VAR>, &cfg) != cudaSuccess ||
+        clusters <= 0) {
+      cudaGetLastError();
+      clusters = device_sm_count() / p.cl;
+    }
+    grid = clusters * p.cl;
+  }
+  cfg.gridDim = dim3(grid);
+  if (cudaLaunchKernelEx(&cfg, tc_gemm_kernel<VAR>, a, b, p) != cudaSuccess) return USAF_ERR_CUDA;
   USAF_CHECK_LAUNCH();
   return USAF_OK;
 }
@@ -858,6 +930,7 @@ Params base_params(const MoeArgs& a) {
   p.I = (int)a.s.I;
   p.Ngu = a.s.E * 2 * a.s.I * a.s.H;
   p.R_cap = a.R_cap;
+  p.cl = 1;
   return p;
 }
 
@@ -908,6 +981,7 @@ usaf_status tc_fwd_gate_up(const MoeArgs& a, const void* x_perm, void* h, void* 
     return USAF_ERR_CUDA;
   Params p = base_params(a);
   p.MT = (int)(a.s.I / 64);
+  p.cl = p.MT % 2 == 0 ? 2 : 1;
   p.h = static_cast<__nv_bfloat16*>(h);
   p.wa = static_cast<__nv_bfloat16*>(wa);
   return launch<V_GATEUP>(ma, mb, p, st);
@@ -920,6 +994,7 @@ usaf_status tc_fwd_down(const MoeArgs& a, const void* wa, float* y_acc, cudaStre
     return USAF_ERR_CUDA;
   Params p = base_params(a);
   p.MT = (int)ceil_div(a.s.H, BM);
+  p.cl = p.MT % 2 == 0 ? 2 : 1;
   p.acc_out = y_acc;
   return launch<V_DOWN>(ma, mb, p, st);
 }
@@ -932,6 +1007,7 @@ usaf_status tc_bwd_gvec(const MoeArgs& a, const void* dy_perm, const void* h, vo
     return USAF_ERR_CUDA;
   Params p = base_params(a);
   p.MT = (int)ceil_div(a.s.I, BM);
+  p.cl = p.MT % 2 == 0 ? 2 : 1;
   p.hin = static_cast<const __nv_bfloat16*>(h);
   p.dh = static_cast<__nv_bfloat16*>(dh);
   p.dw = dw;
@@ -945,6 +1021,7 @@ usaf_status tc_bwd_dx(const MoeArgs& a, const void* dh, float* dx_acc, cudaStrea
     return USAF_ERR_CUDA;
   Params p = base_params(a);
   p.MT = (int)ceil_div(a.s.H, BM);
+  p.cl = p.MT % 2 == 0 ? 2 : 1;
   p.acc_out = dx_acc;
   return launch<V_DX>(ma, mb, p, st);
 }
@@ -991,6 +1068,7 @@ usaf_status tc_bwd_wgrad(const MoeArgs& a, const void* x_perm, const void* dy_pe
   if (!map_2d(&ma, dh, 2 * a.s.I, a.R_cap, 64, 64) || !map_2d(&mb, x_perm, a.s.H, a.R_cap, 64, 64))
     return USAF_ERR_CUDA;
   p.MT = (int)(2 * a.s.I / BM);
+  p.cl = p.MT % 2 == 0 ? 2 : 1;
   p.NT = (int)ceil_div(a.s.H, BN);
   p.tp_base = 0;
   USAF_TRY(launch<V_WG_GU>(ma, mb, p, st));
@@ -999,6 +1077,7 @@ usaf_status tc_bwd_wgrad(const MoeArgs& a, const void* x_perm, const void* dy_pe
   if (!map_2d(&ma, dy_perm, a.s.H, a.R_cap, 64, 64) || !map_2d(&mb, wa, a.s.I, a.R_cap, 64, 64))
     return USAF_ERR_CUDA;
   p.MT = (int)ceil_div(a.s.H, BM);
+  p.cl = p.MT % 2 == 0 ? 2 : 1;
   p.NT = (int)ceil_div(a.s.I, BN);
   return launch<V_WG_D>(ma, mb, p, st);
 }
