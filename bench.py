@@ -313,6 +313,7 @@ def run_steps(args, B, MoELayer, dist, ws, rank, local, dev, cfg, inp, x, dy, wg
         e0.record(stream)
         for _ in range(args.steps):
             layer.train_step(x, dy)
+        layer.wait_optimizer(stream)
         e1.record(stream)
         torch.cuda.synchronize()
     if dist is not None:
@@ -386,6 +387,7 @@ def e2e_time(args, layer, x, dy, e0, e1, stream, dist, dev):
     e0.record(stream)
     for _ in range(args.steps):
         layer.train_step_host(xh, dyh, yh, dxh, xd, dyd)
+    layer.wait_optimizer(stream)
     e1.record(stream)
     torch.cuda.synchronize()
     return max_over_ranks(dist, e0.elapsed_time(e1) / args.steps, dev)

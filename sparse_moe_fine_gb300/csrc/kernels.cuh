@@ -5,7 +5,7 @@
 
 namespace usaf {
 
-constexpr int PERM_CHUNK = 1024;
+constexpr int PERM_CHUNK = 256;
 
 // ---------------------------------------------------------------- routing
 struct RouteWs {
@@ -26,6 +26,7 @@ struct FwdWs {
 struct BwdWs {
   float* dw;          // [T*k] when the caller gives no dw_slot
   float* dl;          // [T*k] dlogit at the selected experts (renorm = 1)
+  float* dl_perm;     // [R_cap] the same in permuted row order
   float* dlogit;      // [T,E] dense dlogit (renorm = 0)
   void* dh;           // [R_cap, 2I] of dtype
   float* dx_acc;      // [T,H]

@@ -258,26 +258,27 @@ __global__ void masked_wgrad_simt_kernel(const int64_t* __restrict__ act_idx, in
 // Shared element-wise kernels
 // ================================================================================================
 
-// x_perm[row] = x[perm_tok[row]] for routed rows, 0 for padding and tail rows.
+// x_perm[row] = x[perm_tok[row]] for routed rows, 0 for padding and tail rows. One warp per row,
+// 16-byte vectors when a row is a whole number of them.
+constexpr int GATHER_ROWS = 8;
 template <typename T>
-__global__ void gather_rows_kernel(const T* __restrict__ x, const int32_t* __restrict__ ptok,
-                                   const int32_t* __restrict__ pslot,
-                                   const int32_t* __restrict__ off_end, int64_t R_cap, int H,
-                                   T* __restrict__ xp) {
-  const int64_t row = blockIdx.x;
+__global__ void __launch_bounds__(32 * GATHER_ROWS) gather_rows_kernel(
+    const T* __restrict__ x, const int32_t* __restrict__ ptok, const int32_t* __restrict__ pslot,
+    const int32_t* __restrict__ off_end, int64_t R_cap, int H, T* __restrict__ xp) {
+  const int lane = threadIdx.x & 31;
+  const int64_t row = (int64_t)blockIdx.x * GATHER_ROWS + (threadIdx.x >> 5);
+  if (row >= R_cap) return;
   const bool live = row < *off_end && pslot[row] >= 0;
   const int64_t src = live ? (int64_t)ptok[row] * H : 0;
   if (((H * sizeof(T)) & 15) == 0) {
     const int nv = (int)(H * sizeof(T) / 16);
-    const uint4* s = reinterpret_cast<const uint4*>(x + src);
-    uint4* d = reinterpret_cast<uint4*>(xp + row * H);
-    for (int i = threadIdx.x; i < nv; i += blockDim.x)
-      d[i] = live ? s[i] : make_uint4(0, 0, 0, 0);
+    const uint4* sp = reinterpret_cast<const uint4*>(x + src);
+    uint4* dp = reinterpret_cast<uint4*>(xp + row * H);
+#pragma unroll 4
+    for (int i = lane; i < nv; i += 32) dp[i] = live ? __ldg(sp + i) : make_uint4(0, 0, 0, 0);
   } else {
-    for (int i = threadIdx.x; i < H; i += blockDim.x)
-      xp[row * H + i] = live ? x[src + i] : from_f32<T>(0.f);
+    for (int i = lane; i < H; i += 32) xp[row * H + i] = live ? x[src + i] : from_f32<T>(0.f);
   }
-  (void)R_cap;
 }
 
 __global__ void zero_f32_kernel(float* __restrict__ p, int64_t n) {
@@ -295,14 +296,17 @@ __global__ void f32_to_kernel(const float* __restrict__ src, T* __restrict__ dst
 
 // dlogit at the selected experts, renormalised routing: w_j (dw_j - sum_i w_i dw_i).
 __global__ void dlogit_sel_kernel(const float* __restrict__ w, const float* __restrict__ dw,
-                                  int Tn, int k, float* __restrict__ dl) {
+                                  const int32_t* __restrict__ slot_row, int Tn, int k,
+                                  float* __restrict__ dl, float* __restrict__ dl_perm) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= Tn) return;
   float s = 0.f;
   for (int j = 0; j < k; ++j) s = fmaf(w[(int64_t)t * k + j], dw[(int64_t)t * k + j], s);
   for (int j = 0; j < k; ++j) {
     const int64_t q = (int64_t)t * k + j;
-    dl[q] = w[q] * (dw[q] - s);
+    const float d = w[q] * (dw[q] - s);
+    dl[q] = d;
+    dl_perm[slot_row[q]] = d;  // the same value at the slot's permuted row
   }
 }
 
@@ -350,24 +354,52 @@ __global__ void dlogit_dense_kernel(const float* __restrict__ logits,
   }
 }
 
-// g_router[e, h] = sum over rows routed to e of dl[slot] * x[tok, h]   (renormalised routing)
+// g_router[e, h] = sum over the rows routed to e of dl[row] * x_perm[row, h] (renormalised
+// routing); each thread owns 16 bytes of h, rows in order, four rows in flight.
 template <typename T>
-__global__ void g_router_sel_kernel(const T* __restrict__ x, const float* __restrict__ dl,
-                                    const int32_t* __restrict__ cnt,
-                                    const int32_t* __restrict__ off,
-                                    const int32_t* __restrict__ ptok,
-                                    const int32_t* __restrict__ pslot, int H,
-                                    float* __restrict__ g_router, uint32_t* dev_status) {
+__global__ void __launch_bounds__(256) g_router_sel_kernel(
+    const T* __restrict__ xp, const float* __restrict__ dl_perm, const int32_t* __restrict__ cnt,
+    const int32_t* __restrict__ off, int H, float* __restrict__ g_router, uint32_t* dev_status) {
+  constexpr int VW = 16 / sizeof(T);
   const int e = blockIdx.y;
-  const int h = blockIdx.x * blockDim.x + threadIdx.x;
-  float acc = 0.f;
-  if (h < H) {
+  const int h0 = (blockIdx.x * blockDim.x + threadIdx.x) * VW;
+  const bool on = h0 + VW <= H;
+  float acc[VW];
+#pragma unroll
+  for (int q = 0; q < VW; ++q) acc[q] = 0.f;
+  if (on) {
     const int n = cnt[e], o = off[e];
-    for (int i = 0; i < n; ++i)
-      acc = fmaf(dl[pslot[o + i]], to_f32(x[(int64_t)ptok[o + i] * H + h]), acc);
-    g_router[(int64_t)e * H + h] = acc;
+    const T* base = xp + (int64_t)o * H + h0;
+    int i = 0;
+    for (; i + 4 <= n; i += 4) {
+      uint4 v[4];
+      float d[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        v[u] = __ldg(reinterpret_cast<const uint4*>(base + (int64_t)(i + u) * H));
+        d[u] = dl_perm[o + i + u];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const T* tv = reinterpret_cast<const T*>(&v[u]);
+#pragma unroll
+        for (int q = 0; q < VW; ++q) acc[q] = fmaf(d[u], to_f32(tv[q]), acc[q]);
+      }
+    }
+    for (; i < n; ++i) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(base + (int64_t)i * H));
+      const float d = dl_perm[o + i];
+      const T* tv = reinterpret_cast<const T*>(&v);
+#pragma unroll
+      for (int q = 0; q < VW; ++q) acc[q] = fmaf(d, to_f32(tv[q]), acc[q]);
+    }
+#pragma unroll
+    for (int q = 0; q < VW; ++q) g_router[(int64_t)e * H + h0 + q] = acc[q];
   }
-  flag_status_warp(dev_status, h < H && !finite_f(acc), USAF_DEV_NONFINITE);
+  bool bad = false;
+#pragma unroll
+  for (int q = 0; q < VW; ++q) bad |= on && !finite_f(acc[q]);
+  flag_status_warp(dev_status, bad, USAF_DEV_NONFINITE);
 }
 
 // g_router[e, h] = sum_t dlogit[t, e] * x[t, h]   (softmax-over-all-E routing)
@@ -386,26 +418,59 @@ __global__ void g_router_dense_kernel(const T* __restrict__ x, const float* __re
   flag_status_warp(dev_status, h < H && !finite_f(acc), USAF_DEV_NONFINITE);
 }
 
-// dx[t, h] = dx_acc[t, h] + router term
+// dx[t, h] = dx_acc[t, h] + router term: sum_j dl[t,j] Wr[e_j, h] (renormalised routing) or
+// sum_e dlogit[t,e] Wr[e, h]. One token per block, four h per thread.
 template <typename T>
-__global__ void dx_finalize_kernel(const float* __restrict__ dx_acc, const float* __restrict__ wr,
-                                   const int32_t* __restrict__ idx, const float* __restrict__ dl,
-                                   const float* __restrict__ dlogit, int Tn, int H, int E, int k,
-                                   int renorm, T* __restrict__ dx, uint32_t* dev_status) {
-  const int t = blockIdx.y;
-  const int h = blockIdx.x * blockDim.x + threadIdx.x;
-  float v = 0.f;
-  if (h < H) {
-    v = dx_acc[(int64_t)t * H + h];
-    if (renorm) {
-      for (int j = 0; j < k; ++j)
-        v = fmaf(dl[(int64_t)t * k + j], wr[(int64_t)idx[(int64_t)t * k + j] * H + h], v);
-    } else {
-      for (int e = 0; e < E; ++e) v = fmaf(dlogit[(int64_t)t * E + e], wr[(int64_t)e * H + h], v);
+__global__ void __launch_bounds__(256) dx_finalize_kernel(
+    const float* __restrict__ dx_acc, const float* __restrict__ wr, const int32_t* __restrict__ idx,
+    const float* __restrict__ dl, const float* __restrict__ dlogit, int Tn, int H, int E, int k,
+    int renorm, T* __restrict__ dx, uint32_t* dev_status) {
+  __shared__ float s_d[1024];
+  __shared__ int s_e[32];
+  const int t = blockIdx.x;
+  if (renorm) {
+    for (int j = threadIdx.x; j < k; j += blockDim.x) {
+      s_d[j] = dl[(int64_t)t * k + j];
+      s_e[j] = idx[(int64_t)t * k + j];
     }
-    dx[(int64_t)t * H + h] = from_f32<T>(v);
+  } else {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) s_d[e] = dlogit[(int64_t)t * E + e];
   }
-  flag_status_warp(dev_status, h < H && !finite_f(v), USAF_DEV_NONFINITE);
+  __syncthreads();
+  bool bad = false;
+  const bool vec = (H & 3) == 0;
+  for (int h0 = threadIdx.x * 4; h0 < H; h0 += blockDim.x * 4) {
+    float v[4];
+    if (vec) {
+      const float4 a = *reinterpret_cast<const float4*>(dx_acc + (int64_t)t * H + h0);
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) v[q] = h0 + q < H ? dx_acc[(int64_t)t * H + h0 + q] : 0.f;
+    }
+    const int nterm = renorm ? k : E;
+    for (int j = 0; j < nterm; ++j) {
+      const float d = s_d[j];
+      const float* wrow = wr + (int64_t)(renorm ? s_e[j] : j) * H + h0;
+      if (vec) {
+        const float4 b = __ldg(reinterpret_cast<const float4*>(wrow));
+        v[0] = fmaf(d, b.x, v[0]); v[1] = fmaf(d, b.y, v[1]);
+        v[2] = fmaf(d, b.z, v[2]); v[3] = fmaf(d, b.w, v[3]);
+      } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (h0 + q < H) v[q] = fmaf(d, wrow[q], v[q]);
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (h0 + q < H) {
+        dx[(int64_t)t * H + h0 + q] = from_f32<T>(v[q]);
+        bad |= !finite_f(v[q]);
+      }
+    }
+  }
+  flag_status_warp(dev_status, bad, USAF_DEV_NONFINITE);
 }
 
 // ================================================================================================
@@ -422,6 +487,7 @@ void bwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, int64_t K, Carver& c,
   const size_t es = dt == USAF_BF16 ? 2 : 4;
   w.dw = c.take<float>(s.T * s.k);
   w.dl = c.take<float>(s.T * s.k);
+  w.dl_perm = c.take<float>(R_cap);
   w.dlogit = c.take<float>(s.T * s.E);
   w.dh = c.take<char>(R_cap * 2 * s.I * (int64_t)es);
   w.dx_acc = c.take<float>(s.T * s.H);
@@ -460,7 +526,7 @@ static usaf_status moe_fwd_t(const MoeArgs& a, T* xp, T* h, T* wa, T* y, FwdWs& 
   const int64_t TH = s.T * s.H;
   {
   USAF_TRACE("gather_x", st);
-  gather_rows_kernel<T><<<(unsigned)a.R_cap, 128, 0, st>>>(
+  gather_rows_kernel<T><<<(unsigned)ceil_div(a.R_cap, GATHER_ROWS), 32 * GATHER_ROWS, 0, st>>>(
       static_cast<const T*>(a.x), a.rt.perm_tok, a.rt.perm_slot, a.rt.expert_offset + s.E,
       a.R_cap, (int)s.H, xp);
   USAF_CHECK_LAUNCH();
@@ -494,30 +560,30 @@ usaf_status moe_fwd_launch(const MoeArgs& a, void* x_perm, void* h, void* wa, vo
 }
 
 // For every weight row (gate_up rows, then down rows) and every 256-column tile of it, the first
-// active entry at or after the tile's first column; entry NT of a row is the row's end.
+// active entry at or after the tile's first column; entry NT of a row is the row's end. The
+// actives are sorted, so their (row, tile) positions are too: active a fills the entries between
+// its predecessor's position and its own, and the entries after the last active get K.
+__device__ __forceinline__ int64_t tile_pos(int64_t f, int64_t Ngu, int64_t n_gu_rows, int H,
+                                            int I, int nt_gu, int nt_d) {
+  if (f < Ngu) return (f / H) * (nt_gu + 1) + (f % H) / 256;
+  const int64_t fd = f - Ngu;
+  return n_gu_rows * (nt_gu + 1) + (fd / I) * (nt_d + 1) + (fd % I) / 256;
+}
+
 __global__ void tile_ptr_kernel(const int64_t* __restrict__ act, int64_t K, int64_t n_gu_rows,
-                                int64_t n_rows, int H, int I, int64_t Ngu, int nt_gu, int nt_d,
+                                int64_t n_entries, int H, int I, int64_t Ngu, int nt_gu, int nt_d,
                                 int32_t* __restrict__ tp) {
-  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= n_rows) return;
-  const bool gu = r < n_gu_rows;
-  const int64_t base = gu ? r * H : Ngu + (r - n_gu_rows) * I;
-  const int ncols = gu ? H : I;
-  const int NT = gu ? nt_gu : nt_d;
-  int32_t* out = tp + (gu ? r * (nt_gu + 1) : n_gu_rows * (nt_gu + 1) + (r - n_gu_rows) * (nt_d + 1));
-  int64_t lo = 0, hi = K;
-  while (lo < hi) {
-    const int64_t mid = (lo + hi) >> 1;
-    if (act[mid] < base) lo = mid + 1;
-    else hi = mid;
+  const int64_t tail = K > 0 ? tile_pos(act[K - 1], Ngu, n_gu_rows, H, I, nt_gu, nt_d) + 1 : 0;
+  const int64_t n = K > n_entries ? K : n_entries;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    if (i < K) {
+      const int64_t pos = tile_pos(act[i], Ngu, n_gu_rows, H, I, nt_gu, nt_d);
+      const int64_t prev = i > 0 ? tile_pos(act[i - 1], Ngu, n_gu_rows, H, I, nt_gu, nt_d) : -1;
+      for (int64_t x = prev + 1; x <= pos; ++x) tp[x] = (int32_t)i;
+    }
+    if (i >= tail && i < n_entries) tp[i] = (int32_t)K;
   }
-  int64_t cur = lo;
-  for (int nt = 0; nt < NT; ++nt) {
-    out[nt] = (int32_t)cur;
-    const int64_t lim = base + min((nt + 1) * 256, ncols);
-    while (cur < K && act[cur] < lim) ++cur;
-  }
-  out[NT] = (int32_t)cur;
 }
 
 int64_t tile_ptr_entries(const usaf_moe_shape& s) {
@@ -546,8 +612,8 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
   if (a.dt == USAF_BF16) {
     {
       USAF_TRACE("gather_dy", st);
-      gather_rows_kernel<T><<<(unsigned)a.R_cap, 128, 0, st>>>(dy, ptok, pslot, off + E, a.R_cap,
-                                                               H, dyp);
+      gather_rows_kernel<T><<<(unsigned)ceil_div(a.R_cap, GATHER_ROWS), 32 * GATHER_ROWS, 0,
+                              st>>>(dy, ptok, pslot, off + E, a.R_cap, H, dyp);
       USAF_CHECK_LAUNCH();
       zero_f32_kernel<<<grid_dim_for(s.T * s.k), 256, 0, st>>>(dw, s.T * s.k);
       USAF_CHECK_LAUNCH();
@@ -567,10 +633,12 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
   {
   USAF_TRACE("router_bwd", st);
   if (renorm) {
-    dlogit_sel_kernel<<<(unsigned)ceil_div(Tn, 128), 128, 0, st>>>(a.rt.topk_w, dw, Tn, k, w.dl);
+    dlogit_sel_kernel<<<(unsigned)ceil_div(Tn, 128), 128, 0, st>>>(a.rt.topk_w, dw, a.rt.slot_row,
+                                                                  Tn, k, w.dl, w.dl_perm);
     USAF_CHECK_LAUNCH();
-    g_router_sel_kernel<T><<<dim3((unsigned)ceil_div(H, 128), (unsigned)E), 128, 0, st>>>(
-        static_cast<const T*>(a.x), w.dl, cnt, off, ptok, pslot, H, g_router, dev_status);
+    constexpr int VW = 16 / sizeof(T);
+    g_router_sel_kernel<T><<<dim3((unsigned)ceil_div(ceil_div(H, VW), 256), (unsigned)E), 256, 0,
+                             st>>>(xp, w.dl_perm, cnt, off, H, g_router, dev_status);
     USAF_CHECK_LAUNCH();
   } else {
     dlogit_dense_kernel<<<(unsigned)Tn, 128, 0, st>>>(logits, a.rt.topk_idx, a.rt.topk_w, dw, Tn,
@@ -597,7 +665,7 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
       USAF_CHECK_LAUNCH();
     }
     USAF_TRACE("dx_finalize", st);
-    dx_finalize_kernel<T><<<dim3((unsigned)ceil_div(H, 256), (unsigned)Tn), 256, 0, st>>>(
+    dx_finalize_kernel<T><<<(unsigned)Tn, 256, 0, st>>>(
         w.dx_acc, a.w_router, a.rt.topk_idx, w.dl, w.dlogit, Tn, H, E, k, renorm, dx,
         dev_status);
     USAF_CHECK_LAUNCH();
@@ -608,9 +676,9 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
       const int64_t n_gu_rows = s.E * 2 * s.I, n_rows = n_gu_rows + s.E * s.H;
       {
       USAF_TRACE("wgrad_tile_ptr", st);
-      tile_ptr_kernel<<<(unsigned)ceil_div(n_rows, 256), 256, 0, st>>>(
-          act_idx, K, n_gu_rows, n_rows, H, I, Ngu, (int)ceil_div(H, 256), (int)ceil_div(I, 256),
-          w.tile_ptr);
+      tile_ptr_kernel<<<grid_dim_for(std::max<int64_t>(K, tile_ptr_entries(s))), 256, 0, st>>>(
+          act_idx, K, n_gu_rows, tile_ptr_entries(s), H, I, Ngu, (int)ceil_div(H, 256),
+          (int)ceil_div(I, 256), w.tile_ptr);
       USAF_CHECK_LAUNCH();
       }
       USAF_TRY(tc_bwd_wgrad(a, xp, dyp, dh, wa, act_idx, K, w.tile_ptr, g_act, dev_status, st));

@@ -41,7 +41,15 @@ class MoELayer:
         self.y = torch.empty(T, H, dtype=self.dtype, device=d)
         self.dx = torch.empty(T, H, dtype=self.dtype, device=d)
         self.g_router = torch.empty(E, H, device=d)
-        self.status = torch.zeros(1, dtype=torch.int32, device=d)
+        # one status word per step parity: the expert update of step i may still be reading its
+        # word on the side stream while step i+1 clears and fills the other one
+        self.status2 = torch.zeros(2, dtype=torch.int32, device=d)
+        self.status = self.status2[0:1]
+        # the expert SparseAdam update runs on a side stream, overlapping the next step's routing
+        self.side = torch.cuda.Stream(device=d)
+        self.ev_bwd = torch.cuda.Event()
+        self.ev_opt = torch.cuda.Event()
+        self.pending_opt = False
         self.ws_route = torch.empty(B.route_topk_workspace_size(self.s), dtype=torch.uint8,
                                     device=d)
         self.ws_fwd = torch.empty(B.moe_fwd_workspace_size(self.s, self.dt), dtype=torch.uint8,
@@ -77,7 +85,17 @@ class MoELayer:
         B.route_topk(self.s, x, self.w_router, self.rt, logits_out=self.logits,
                      renorm=self.renorm, ws=self.ws_route, stream=stream)
 
+    def _main(self, stream):
+        return torch.cuda.current_stream(self.dev) if stream is None else stream
+
+    def wait_optimizer(self, stream=None):
+        """Make `stream` wait for the last expert update (the weights it writes)."""
+        if self.pending_opt:
+            self._main(stream).wait_event(self.ev_opt)
+            self.pending_opt = False
+
     def forward(self, x, stream=None):
+        self.wait_optimizer(stream)
         B.moe_fwd(self.s, x, self.w_gate_up, self.w_down, self.rt, self.x_perm, self.h, self.wa,
                   self.y, ws=self.ws_fwd, stream=stream)
         return self.y
@@ -90,18 +108,27 @@ class MoELayer:
                          stream=stream)
 
     def optimizer_step(self, stream=None, skip_if_nonfinite=1):
+        """Router update on the calling stream (the next routing reads it); expert update on the
+        side stream, which the next forward waits for."""
         self.step_count += 1
         b1, b2 = self.betas
+        main = self._main(stream)
+        self.ev_bwd.record(main)
+        self.side.wait_event(self.ev_bwd)
         B.sparse_adam_step(self.act, self.g_act, self.p, self.m, self.v, self.w_gate_up,
                            self.N_gu, self.w_down, self.lr, b1, b2, self.eps, self.step_count,
-                           skip_if_nonfinite, self.status, stream=stream)
+                           skip_if_nonfinite, self.status, stream=self.side)
+        self.ev_opt.record(self.side)
+        self.pending_opt = True
         B.sparse_adam_step(None, self.g_router, self.r_p, self.r_m, self.r_v, self.w_router,
                            self.E * self.H, None, self.lr, b1, b2, self.eps, self.step_count,
-                           skip_if_nonfinite, self.status, stream=stream)
+                           skip_if_nonfinite, self.status, stream=main)
 
     def train_step(self, x, dy, stream=None):
         """route -> forward -> sparse backward -> SparseAdam (experts, router)."""
-        self.status.zero_()  # per-step non-finite flag (a non-finite gradient skips this step)
+        # per-step non-finite flag (a non-finite gradient skips this step), alternating words
+        self.status = self.status2[self.step_count % 2:self.step_count % 2 + 1]
+        self.status.zero_()
         self.route(x, stream)
         self.forward(x, stream)
         self.backward(x, dy, stream=stream)
