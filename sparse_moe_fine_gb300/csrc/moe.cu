@@ -355,51 +355,42 @@ __global__ void dlogit_dense_kernel(const float* __restrict__ logits,
 }
 
 // g_router[e, h] = sum over the rows routed to e of dl[row] * x_perm[row, h] (renormalised
-// routing); each thread owns 16 bytes of h, rows in order, four rows in flight.
+// routing); each thread owns two adjacent h, rows in order, eight rows in flight.
 template <typename T>
 __global__ void __launch_bounds__(256) g_router_sel_kernel(
     const T* __restrict__ xp, const float* __restrict__ dl_perm, const int32_t* __restrict__ cnt,
     const int32_t* __restrict__ off, int H, float* __restrict__ g_router, uint32_t* dev_status) {
-  constexpr int VW = 16 / sizeof(T);
   const int e = blockIdx.y;
-  const int h0 = (blockIdx.x * blockDim.x + threadIdx.x) * VW;
-  const bool on = h0 + VW <= H;
-  float acc[VW];
-#pragma unroll
-  for (int q = 0; q < VW; ++q) acc[q] = 0.f;
-  if (on) {
+  const int h0 = (blockIdx.x * blockDim.x + threadIdx.x) * 2;
+  float a0 = 0.f, a1 = 0.f;
+  if (h0 < H) {
+    const bool two = h0 + 1 < H;
     const int n = cnt[e], o = off[e];
     const T* base = xp + (int64_t)o * H + h0;
     int i = 0;
-    for (; i + 4 <= n; i += 4) {
-      uint4 v[4];
-      float d[4];
+    for (; i + 8 <= n; i += 8) {
+      float x0[8], x1[8], d[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        v[u] = __ldg(reinterpret_cast<const uint4*>(base + (int64_t)(i + u) * H));
+      for (int u = 0; u < 8; ++u) {
+        x0[u] = to_f32(base[(int64_t)(i + u) * H]);
+        x1[u] = two ? to_f32(base[(int64_t)(i + u) * H + 1]) : 0.f;
         d[u] = dl_perm[o + i + u];
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const T* tv = reinterpret_cast<const T*>(&v[u]);
-#pragma unroll
-        for (int q = 0; q < VW; ++q) acc[q] = fmaf(d[u], to_f32(tv[q]), acc[q]);
+      for (int u = 0; u < 8; ++u) {
+        a0 = fmaf(d[u], x0[u], a0);
+        a1 = fmaf(d[u], x1[u], a1);
       }
     }
     for (; i < n; ++i) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(base + (int64_t)i * H));
       const float d = dl_perm[o + i];
-      const T* tv = reinterpret_cast<const T*>(&v);
-#pragma unroll
-      for (int q = 0; q < VW; ++q) acc[q] = fmaf(d, to_f32(tv[q]), acc[q]);
+      a0 = fmaf(d, to_f32(base[(int64_t)i * H]), a0);
+      if (two) a1 = fmaf(d, to_f32(base[(int64_t)i * H + 1]), a1);
     }
-#pragma unroll
-    for (int q = 0; q < VW; ++q) g_router[(int64_t)e * H + h0 + q] = acc[q];
+    g_router[(int64_t)e * H + h0] = a0;
+    if (two) g_router[(int64_t)e * H + h0 + 1] = a1;
   }
-  bool bad = false;
-#pragma unroll
-  for (int q = 0; q < VW; ++q) bad |= on && !finite_f(acc[q]);
-  flag_status_warp(dev_status, bad, USAF_DEV_NONFINITE);
+  flag_status_warp(dev_status, h0 < H && (!finite_f(a0) || !finite_f(a1)), USAF_DEV_NONFINITE);
 }
 
 // g_router[e, h] = sum_t dlogit[t, e] * x[t, h]   (softmax-over-all-E routing)
@@ -636,8 +627,7 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
     dlogit_sel_kernel<<<(unsigned)ceil_div(Tn, 128), 128, 0, st>>>(a.rt.topk_w, dw, a.rt.slot_row,
                                                                   Tn, k, w.dl, w.dl_perm);
     USAF_CHECK_LAUNCH();
-    constexpr int VW = 16 / sizeof(T);
-    g_router_sel_kernel<T><<<dim3((unsigned)ceil_div(ceil_div(H, VW), 256), (unsigned)E), 256, 0,
+    g_router_sel_kernel<T><<<dim3((unsigned)ceil_div(ceil_div(H, 2), 256), (unsigned)E), 256, 0,
                              st>>>(xp, w.dl_perm, cnt, off, H, g_router, dev_status);
     USAF_CHECK_LAUNCH();
   } else {

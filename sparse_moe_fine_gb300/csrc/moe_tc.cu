@@ -29,7 +29,6 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int BN = 256;
 constexpr int STAGES = 4;
-constexpr int PF_BLOCKS = 8;  // k-blocks of the A (weight) stream prefetched into L2 ahead
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -121,20 +120,6 @@ __device__ __forceinline__ void tma_2d_mc(uint32_t dst, const CUtensorMap* map, 
       ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(mask)
       : "memory");
-}
-// L2 prefetch of a tile ahead of its load (no shared memory, no barrier)
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int c0, int c1) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1)
-               : "memory");
-}
-__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int c0, int c1, int c2,
-                                                int c3) {
-  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-               : "memory");
 }
 __device__ __forceinline__ uint32_t cta_rank() {
   uint32_t r;
@@ -570,35 +555,6 @@ __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32
   }
 }
 
-// L2 prefetch of the operands of k-block k0 of tile ti (the same boxes the loads use)
-template <int VAR>
-__device__ __forceinline__ void prefetch_ops(const Params& p, const CUtensorMap* tmA,
-                                             const CUtensorMap* tmB, const Tile& ti, int k0) {
-  if constexpr (VAR == V_GATEUP) {
-    tma_prefetch_4d(tmA, k0, 0, ti.m0, ti.e);
-  } else if constexpr (VAR == V_DOWN) {
-    tma_prefetch_2d(tmA, k0, ti.e * p.H + ti.m0);
-  } else if constexpr (VAR == V_GVEC) {
-    tma_prefetch_2d(tmA, ti.m0, ti.e * p.H + k0);
-    tma_prefetch_2d(tmA, ti.m0 + 64, ti.e * p.H + k0);
-  } else if constexpr (VAR == V_DX) {
-    tma_prefetch_2d(tmA, ti.m0, ti.e * 2 * p.I + k0);
-    tma_prefetch_2d(tmA, ti.m0 + 64, ti.e * 2 * p.I + k0);
-  } else if constexpr (VAR == V_ROUTER) {
-    tma_prefetch_2d(tmA, k0, ti.m0);
-  } else {
-    tma_prefetch_2d(tmA, ti.m0, ti.row0 + k0);
-    tma_prefetch_2d(tmA, ti.m0 + 64, ti.row0 + k0);
-  }
-  if constexpr (VarTraits<VAR>::token_tiled) {
-    tma_prefetch_2d(tmB, k0, ti.row0);
-    if (ti.nrows > 128) tma_prefetch_2d(tmB, k0, ti.row0 + 128);
-  } else if constexpr (VarTraits<VAR>::wgrad) {
-#pragma unroll
-    for (int q = 0; q < 4; ++q) tma_prefetch_2d(tmB, ti.n0 + 64 * q, ti.row0 + k0);
-  }
-}
-
 // ---------------------------------------------------------------------------- the kernel
 template <int VAR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -665,35 +621,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;
-      // a second cursor over the same (tile, k-block) sequence, PF_BLOCKS ahead, issues L2
-      // prefetches of the operands so the loads below hit L2 instead of waiting on HBM
-      int pt = cid, pkb = 0, pnkb = 0;
-      Tile pti{};
-      auto pf_advance = [&]() {
-        while (pt < total) {
-          if (pkb == 0) {
-            pti = get_tile<VAR>(p, s_plan, s_off, pt);
-            pnkb = pti.live ? (pti.klen + BK - 1) / BK : 0;
-          }
-          if (pkb < pnkb) {
-            prefetch_ops<VAR>(p, &tmA, &tmB, pti, pkb * BK);
-            if (++pkb == pnkb) {
-              pkb = 0;
-              pt += ncl;
-            }
-            return;
-          }
-          pkb = 0;
-          pt += ncl;
-        }
-      };
-      for (int i = 0; i < PF_BLOCKS; ++i) pf_advance();
       for (int t = cid; t < total && !failed; t += ncl) {
         const Tile ti = get_tile<VAR>(p, s_plan, s_off, t);
         if (!ti.live) continue;
         const int nkb = (ti.klen + BK - 1) / BK;
         for (int kb = 0; kb < nkb; ++kb) {
-          pf_advance();
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) {
             failed = true;
             break;
