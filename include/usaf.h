@@ -143,10 +143,10 @@ usaf_status usaf_route_topk_noalloc(const usaf_moe_shape* shape, const void* x,
  *                tcgen05 tensor cores (needs H % 64 == 0, I % 64 == 0).
  *                USAF_F32: everything fp32 on CUDA cores (any sizes).
  *   x            [T,H];  w_gate_up [E,2I,H];  w_down [E,H,I]
- *   x_perm_save  [R_cap,H]  out: x rows in permuted order (kept for the backward)
+ *   x_perm_save  [H,R_cap]  out: x in permuted row order, feature-major (kept for the backward)
  *   h_save       [2I,R_cap] out: gate|up pre-activations, feature-major: element (j, row) is
  *                feature j (gate for j < I, up for j >= I) of permuted row `row`
- *   wa_save      [R_cap,I]  out: w * A per permuted row (0 in padding rows)
+ *   wa_save      [I,R_cap]  out: w * A per permuted row, feature-major (0 in padding rows)
  *   y            [T,H]      out
  * Errors: INVALID_ARG, UNSUPPORTED (bf16 shape limits), WORKSPACE, CUDA.
  * ------------------------------------------------------------------------------------------- */

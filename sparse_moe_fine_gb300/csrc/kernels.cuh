@@ -28,12 +28,12 @@ struct BwdWs {
   float* dl;          // [T*k] dlogit at the selected experts (renorm = 1)
   float* dl_perm;     // [R_cap] the same in permuted row order
   float* dlogit;      // [T,E] dense dlogit (renorm = 0)
-  void* dh;           // [R_cap, 2I] of dtype
+  void* dh;           // dh^T [2I, R_cap] of dtype
   float* dx_acc;      // [T,H]
   float* gvec;        // [R_cap, I] (fp32 path only)
-  int32_t* tile_ptr;  // first active entry of each (weight row, 256-column tile) (tensor cores)
+  int32_t* row_ptr;   // [E*2I + E*H + 1] first active entry of each weight row
   int32_t* plan;      // [E+1] prefix of token tiles per expert (tensor-core path)
-  void* dy_perm;      // [R_cap, H] dy rows in permuted order (tensor-core path)
+  void* dy_perm;      // dy^T [H, R_cap]: dy in permuted order, feature-major
 };
 void fwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, Carver& c, FwdWs& w);
 void bwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, int64_t K, Carver& c, BwdWs& w);
@@ -62,17 +62,13 @@ bool tc_shape_ok(const usaf_moe_shape& s);
 usaf_status tc_router_logits(const usaf_moe_shape& s, const void* x, const float* wr, void* wr3,
                              float* logits, cudaStream_t st);
 usaf_status tc_plan(const MoeArgs& a, cudaStream_t st);
-int64_t tile_ptr_entries(const usaf_moe_shape& s);
-usaf_status tc_fwd_gate_up(const MoeArgs& a, const void* x_perm, void* h, void* wa,
+usaf_status tc_fwd_gate_up(const MoeArgs& a, const void* xT, void* hT, void* waT,
                            cudaStream_t st);
 usaf_status tc_fwd_down(const MoeArgs& a, const void* wa, float* y_acc, cudaStream_t st);
-usaf_status tc_bwd_gvec(const MoeArgs& a, const void* dy_perm, const void* h, void* dh,
-                        float* dw, cudaStream_t st);
+usaf_status tc_bwd_gvec(const MoeArgs& a, const void* dyT, const void* hT, void* dhT, float* dw,
+                        cudaStream_t st);
 usaf_status tc_bwd_dx(const MoeArgs& a, const void* dh, float* dx_acc, cudaStream_t st);
-usaf_status tc_bwd_wgrad(const MoeArgs& a, const void* x_perm, const void* dy_perm, const void* dh,
-                         const void* wa, const int64_t* act_idx, int64_t K,
-                         const int32_t* tile_ptr, float* g_act, uint32_t* dev_status,
-                         cudaStream_t st);
+
 
 // ---------------------------------------------------------------- optimizer
 usaf_status adam_launch(int64_t n, const int64_t* idx, const float* g, float* p, float* m,

@@ -6,9 +6,16 @@
 // forms expert weight gradients only at the active set (USAF README, "Not all weights matter";
 // news article, key differences: a subset of weights inside each activated expert).
 //
-// This file holds the element-wise, gather/scatter and router kernels shared by both element
+// Per-row activations are feature-major: x^T [H, R_cap], h^T [2I, R_cap], (w*A)^T [I, R_cap],
+// dy^T [H, R_cap], dh^T [2I, R_cap], each row one feature over the permuted rows, so an expert's
+// tokens are contiguous. The masked weight gradient is then, for every active entry, one dot
+// product of two contiguous token vectors (a sampled dense-dense product on CUDA cores).
+//
+// This file holds the gathers, the masked-gradient and router kernels shared by both element
 // types, the CUDA-core grouped GEMMs used for fp32 layers, and the host orchestration. The bf16
 // grouped GEMMs run on tcgen05 tensor cores (moe_tc.cu).
+#include <algorithm>
+
 #include "common.cuh"
 #include "kernels.cuh"
 
@@ -59,12 +66,14 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(P p) {
     }
 }
 
-// S4 (CUDA cores): h[n, row] = sum_k x_perm[row, k] * gate_up[e, n, k]  (h feature-major)
+// The fp32 GEMMs: M = the expert's tokens, N = features. Feature-major operands are read at
+// X[k * rcap + off[e] + m].
+// S4: h^T[n, row] = sum_k x^T[k, row] * gate_up[e, n, k]
 template <typename T>
 struct ProbGateUp {
-  const T* xp;
+  const T* xT;
   const T* wgu;
-  T* h;
+  T* hT;
   const int32_t* cnt;
   const int32_t* off;
   int H, I2;
@@ -74,87 +83,77 @@ struct ProbGateUp {
     N = I2;
     K = H;
   }
-  __device__ float a(int e, int m, int k) const {
-    return to_f32(xp[(int64_t)(off[e] + m) * H + k]);
-  }
+  __device__ float a(int e, int m, int k) const { return to_f32(xT[(int64_t)k * rcap + off[e] + m]); }
   __device__ float b(int e, int k, int n) const {
     return to_f32(wgu[((int64_t)e * I2 + n) * H + k]);
   }
   __device__ void store(int e, int m, int n, float v) const {
-    h[(int64_t)n * rcap + off[e] + m] = from_f32<T>(v);
+    hT[(int64_t)n * rcap + off[e] + m] = from_f32<T>(v);
   }
 };
 
-// S5 (CUDA cores): y_acc[tok, n] += sum_k wa[row, k] * down[e, n, k]
+// S5: y_acc[tok, n] += sum_k (wA)^T[k, row] * down[e, n, k]
 template <typename T>
 struct ProbDown {
-  const T* wa;
+  const T* waT;
   const T* wd;
   float* yacc;
   const int32_t* cnt;
   const int32_t* off;
   const int32_t* ptok;
   int H, I;
+  int64_t rcap;
   __device__ void dims(int e, int& M, int& N, int& K) const {
     M = cnt[e];
     N = H;
     K = I;
   }
-  __device__ float a(int e, int m, int k) const {
-    return to_f32(wa[(int64_t)(off[e] + m) * I + k]);
-  }
-  __device__ float b(int e, int k, int n) const {
-    return to_f32(wd[((int64_t)e * H + n) * I + k]);
-  }
+  __device__ float a(int e, int m, int k) const { return to_f32(waT[(int64_t)k * rcap + off[e] + m]); }
+  __device__ float b(int e, int k, int n) const { return to_f32(wd[((int64_t)e * H + n) * I + k]); }
   __device__ void store(int e, int m, int n, float v) const {
     atomicAdd(&yacc[(int64_t)ptok[off[e] + m] * H + n], v);
   }
 };
 
-// S6 (CUDA cores): gvec[row, n] = sum_k dy[tok, k] * down[e, k, n]
+// S6: gvec[row, n] = sum_k dy^T[k, row] * down[e, k, n]
 template <typename T>
 struct ProbGvec {
-  const T* dy;
+  const T* dyT;
   const T* wd;
   float* gvec;
   const int32_t* cnt;
   const int32_t* off;
-  const int32_t* ptok;
   int H, I;
+  int64_t rcap;
   __device__ void dims(int e, int& M, int& N, int& K) const {
     M = cnt[e];
     N = I;
     K = H;
   }
-  __device__ float a(int e, int m, int k) const {
-    return to_f32(dy[(int64_t)ptok[off[e] + m] * H + k]);
-  }
-  __device__ float b(int e, int k, int n) const {
-    return to_f32(wd[((int64_t)e * H + k) * I + n]);
-  }
+  __device__ float a(int e, int m, int k) const { return to_f32(dyT[(int64_t)k * rcap + off[e] + m]); }
+  __device__ float b(int e, int k, int n) const { return to_f32(wd[((int64_t)e * H + k) * I + n]); }
   __device__ void store(int e, int m, int n, float v) const {
     gvec[(int64_t)(off[e] + m) * I + n] = v;
   }
 };
 
-// S8 (CUDA cores): dx_acc[tok, n] += sum_k dh[row, k] * gate_up[e, k, n]
+// S8: dx_acc[tok, n] += sum_k dh^T[k, row] * gate_up[e, k, n]
 template <typename T>
 struct ProbDx {
-  const T* dh;
+  const T* dhT;
   const T* wgu;
   float* dxacc;
   const int32_t* cnt;
   const int32_t* off;
   const int32_t* ptok;
   int H, I2;
+  int64_t rcap;
   __device__ void dims(int e, int& M, int& N, int& K) const {
     M = cnt[e];
     N = H;
     K = I2;
   }
-  __device__ float a(int e, int m, int k) const {
-    return to_f32(dh[(int64_t)(off[e] + m) * I2 + k]);
-  }
+  __device__ float a(int e, int m, int k) const { return to_f32(dhT[(int64_t)k * rcap + off[e] + m]); }
   __device__ float b(int e, int k, int n) const {
     return to_f32(wgu[((int64_t)e * I2 + k) * H + n]);
   }
@@ -163,47 +162,47 @@ struct ProbDx {
   }
 };
 
-// SwiGLU after S4 on CUDA cores: wa[row, j] = w * silu(gate) * up (0 in padding rows).
+// SwiGLU after S4 on CUDA cores: (wA)^T[j, row] = w * silu(gate) * up (0 in padding rows).
 template <typename T>
-__global__ void swiglu_fwd_rows_kernel(const T* __restrict__ h, const int32_t* __restrict__ pslot,
+__global__ void swiglu_fwd_rows_kernel(const T* __restrict__ hT, const int32_t* __restrict__ pslot,
                                        const float* __restrict__ topk_w,
                                        const int32_t* __restrict__ off_end, int I, int64_t rcap,
-                                       T* __restrict__ wa) {
+                                       T* __restrict__ waT) {
   const int64_t row = blockIdx.x;
   if (row >= *off_end) return;
   const int slot = pslot[row];
   const float w = slot >= 0 ? topk_w[slot] : 0.f;
   for (int j = threadIdx.x; j < I; j += blockDim.x) {
-    float g = to_f32(h[j * rcap + row]), u = to_f32(h[(I + j) * rcap + row]);
-    wa[row * I + j] = from_f32<T>(slot >= 0 ? w * silu_f(g) * u : 0.f);
+    const float g = to_f32(hT[j * rcap + row]), u = to_f32(hT[(I + j) * rcap + row]);
+    waT[j * rcap + row] = from_f32<T>(slot >= 0 ? w * silu_f(g) * u : 0.f);
   }
 }
 
-// SwiGLU backward after S6 on CUDA cores: dw, dh per permuted row.
+// SwiGLU backward after S6 on CUDA cores: dw per slot and dh^T per permuted row.
 template <typename T>
-__global__ void swiglu_bwd_rows_kernel(const float* __restrict__ gvec, const T* __restrict__ h,
+__global__ void swiglu_bwd_rows_kernel(const float* __restrict__ gvec, const T* __restrict__ hT,
                                        const int32_t* __restrict__ pslot,
                                        const float* __restrict__ topk_w,
                                        const int32_t* __restrict__ off_end, int I, int64_t rcap,
-                                       T* __restrict__ dh, float* __restrict__ dw) {
+                                       T* __restrict__ dhT, float* __restrict__ dw) {
   const int64_t row = blockIdx.x;
   if (row >= *off_end) return;
   const int slot = pslot[row];
   __shared__ float red[32];
   if (slot < 0) {
-    for (int j = threadIdx.x; j < 2 * I; j += blockDim.x) dh[row * 2 * I + j] = from_f32<T>(0.f);
+    for (int j = threadIdx.x; j < 2 * I; j += blockDim.x) dhT[j * rcap + row] = from_f32<T>(0.f);
     return;
   }
   const float w = topk_w[slot];
   float part = 0.f;
   for (int j = threadIdx.x; j < I; j += blockDim.x) {
-    float g = to_f32(h[j * rcap + row]), u = to_f32(h[(I + j) * rcap + row]);
-    float gv = gvec[row * I + j];
-    float sg = silu_f(g);
+    const float g = to_f32(hT[j * rcap + row]), u = to_f32(hT[(I + j) * rcap + row]);
+    const float gv = gvec[row * I + j];
+    const float sg = silu_f(g);
     part = fmaf(gv, sg * u, part);
-    float dA = w * gv;
-    dh[row * 2 * I + j] = from_f32<T>(dA * u * silu_grad_f(g));
-    dh[row * 2 * I + I + j] = from_f32<T>(dA * sg);
+    const float dA = w * gv;
+    dhT[j * rcap + row] = from_f32<T>(dA * u * silu_grad_f(g));
+    dhT[(I + j) * rcap + row] = from_f32<T>(dA * sg);
   }
   for (int o = 16; o; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = part;
@@ -215,70 +214,198 @@ __global__ void swiglu_bwd_rows_kernel(const float* __restrict__ gvec, const T* 
   }
 }
 
-// Masked expert gradient on CUDA cores: one thread per active entry (fp32 layers).
+// ================================================================================================
+// Gathers, masked gradient, router
+// ================================================================================================
+
+// Gather-transpose: xT[h, row] = x[perm_tok[row], h] for routed rows, 0 for padding and tail
+// rows. A block moves a 32-row x 64-feature tile through shared memory with 16-byte accesses.
 template <typename T>
-__global__ void masked_wgrad_simt_kernel(const int64_t* __restrict__ act_idx, int64_t K,
-                                         const T* __restrict__ xp, const T* __restrict__ dy,
-                                         const T* __restrict__ dh, const T* __restrict__ wa,
-                                         const int32_t* __restrict__ cnt,
-                                         const int32_t* __restrict__ off,
-                                         const int32_t* __restrict__ ptok, int H, int I,
-                                         int64_t Ngu, float* __restrict__ g_act,
-                                         uint32_t* dev_status) {
-  const int64_t a = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  bool bad = false;
-  if (a < K) {
-    const int64_t f = act_idx[a];
-    float acc = 0.f;
-    if (f < Ngu) {
-      const int e = (int)(f / ((int64_t)2 * I * H));
-      const int r = (int)((f / H) % (2 * I));
-      const int c = (int)(f % H);
-      const int n = cnt[e], o = off[e];
-      for (int i = 0; i < n; ++i)
-        acc = fmaf(to_f32(dh[(int64_t)(o + i) * 2 * I + r]), to_f32(xp[(int64_t)(o + i) * H + c]),
-                   acc);
+__global__ void __launch_bounds__(256) gather_transpose_kernel(
+    const T* __restrict__ x, const int32_t* __restrict__ ptok, const int32_t* __restrict__ pslot,
+    const int32_t* __restrict__ off_end, int64_t R_cap, int H, T* __restrict__ xT) {
+  constexpr int VW = 16 / sizeof(T);  // elements per 16-byte vector
+  __shared__ T tile[64][32 + VW];
+  const int64_t r0 = (int64_t)blockIdx.x * 32;
+  const int h0 = blockIdx.y * 64;
+  const int64_t end = *off_end;
+  const bool vec = (H % VW) == 0;
+  // load: 32 rows x (64 / VW) vectors
+  for (int v = threadIdx.x; v < 32 * (64 / VW); v += blockDim.x) {
+    const int r = v / (64 / VW), f = (v % (64 / VW)) * VW;
+    const int64_t row = r0 + r;
+    const bool live = row < end && pslot[row] >= 0;
+    const int64_t src = live ? (int64_t)ptok[row] * H : 0;
+    alignas(16) T buf[VW];
+    if (vec && h0 + f + VW <= H) {
+      const uint4 u = live ? __ldg(reinterpret_cast<const uint4*>(x + src + h0 + f))
+                           : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(buf) = u;
     } else {
-      const int64_t fd = f - Ngu;
-      const int e = (int)(fd / ((int64_t)H * I));
-      const int r = (int)((fd / I) % H);
-      const int c = (int)(fd % I);
-      const int n = cnt[e], o = off[e];
-      for (int i = 0; i < n; ++i)
-        acc = fmaf(to_f32(dy[(int64_t)ptok[o + i] * H + r]), to_f32(wa[(int64_t)(o + i) * I + c]),
-                   acc);
+#pragma unroll
+      for (int q = 0; q < VW; ++q)
+        buf[q] = (live && h0 + f + q < H) ? x[src + h0 + f + q] : from_f32<T>(0.f);
     }
-    g_act[a] = acc;
-    bad = !finite_f(acc);
+#pragma unroll
+    for (int q = 0; q < VW; ++q) tile[f + q][r] = buf[q];
+  }
+  __syncthreads();
+  // store: 64 features x (32 / VW) vectors of consecutive rows
+  for (int v = threadIdx.x; v < 64 * (32 / VW); v += blockDim.x) {
+    const int f = v / (32 / VW), r = (v % (32 / VW)) * VW;
+    if (h0 + f >= H) continue;
+    alignas(16) T buf[VW];
+#pragma unroll
+    for (int q = 0; q < VW; ++q) buf[q] = tile[f][r + q];
+    *reinterpret_cast<uint4*>(xT + (int64_t)(h0 + f) * R_cap + r0 + r) =
+        *reinterpret_cast<const uint4*>(buf);
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ float dot_vec(const uint4& a, const uint4& b);
+template <>
+__device__ __forceinline__ float dot_vec<__nv_bfloat16>(const uint4& a, const uint4& b) {
+  const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+  float s = 0.f;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    s = fmaf(__uint_as_float(aw[q] << 16), __uint_as_float(bw[q] << 16), s);
+    s = fmaf(__uint_as_float(aw[q] & 0xFFFF0000u), __uint_as_float(bw[q] & 0xFFFF0000u), s);
+  }
+  return s;
+}
+template <>
+__device__ __forceinline__ float dot_vec<float>(const uint4& a, const uint4& b) {
+  return fmaf(__uint_as_float(a.x), __uint_as_float(b.x),
+              fmaf(__uint_as_float(a.y), __uint_as_float(b.y),
+                   fmaf(__uint_as_float(a.z), __uint_as_float(b.z),
+                        __uint_as_float(a.w) * __uint_as_float(b.w))));
+}
+
+// S9/S10 masked weight gradient (sampled dense-dense product). One warp per weight row; its four
+// groups of eight lanes take the row's active entries four at a time, each group a dot product
+// over the expert's tokens (16-byte vectors, then a 3-step shuffle reduction):
+//   gate_up row (e, j), column c:  g = sum_t dh^T[j, t] * x^T[c, t]
+//   down row (e, h), column c:     g = sum_t dy^T[h, t] * (wA)^T[c, t]
+template <typename T>
+__global__ void __launch_bounds__(256) sddmm_kernel(
+    const int64_t* __restrict__ act, const int32_t* __restrict__ rp, int64_t n_rows,
+    int64_t n_gu_rows, const int32_t* __restrict__ cnt, const int32_t* __restrict__ off, int H,
+    int I, int64_t Ngu, int64_t rcap, const T* __restrict__ dhT, const T* __restrict__ xT,
+    const T* __restrict__ dyT, const T* __restrict__ waT, float* __restrict__ g_act,
+    uint32_t* dev_status) {
+  constexpr int VW = 16 / sizeof(T);
+  const int lane = threadIdx.x & 31, grp = lane >> 3, gl = lane & 7;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  bool bad = false;
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < n_rows;
+       r += warps) {
+    const int64_t a0 = rp[r], a1 = rp[r + 1];
+    if (a0 >= a1) continue;
+    const T* av;
+    const T* bbase;
+    int64_t base;
+    int e;
+    if (r < n_gu_rows) {
+      e = (int)(r / (2 * I));
+      av = dhT + (r % (2 * I)) * rcap;
+      bbase = xT;
+      base = r * H;
+    } else {
+      const int64_t rd = r - n_gu_rows;
+      e = (int)(rd / H);
+      av = dyT + (rd % H) * rcap;
+      bbase = waT;
+      base = Ngu + rd * I;
+    }
+    const int o = off[e];
+    const int n = (cnt[e] + VW - 1) / VW * VW;  // padding rows hold zeros in every operand
+    av += o;
+    for (int64_t q0 = a0; q0 < a1; q0 += 4) {
+      const int64_t q = q0 + grp;
+      float acc = 0.f;
+      if (q < a1) {
+        const T* bv = bbase + (act[q] - base) * rcap + o;
+        for (int t = gl * VW; t < n; t += 8 * VW)
+          acc += dot_vec<T>(__ldg(reinterpret_cast<const uint4*>(av + t)),
+                            __ldg(reinterpret_cast<const uint4*>(bv + t)));
+      }
+      acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      if (gl == 0 && q < a1) {
+        g_act[q] = acc;
+        bad |= !finite_f(acc);
+      }
+    }
   }
   flag_status_warp(dev_status, bad, USAF_DEV_NONFINITE);
 }
 
-// ================================================================================================
-// Shared element-wise kernels
-// ================================================================================================
+// First active entry of every weight row (gate_up rows, then down rows); entry n_rows = K. The
+// actives are sorted, so their rows are too: active a fills the entries between its
+// predecessor's row and its own, and the entries after the last active's row get K.
+__device__ __forceinline__ int64_t weight_row(int64_t f, int64_t Ngu, int64_t n_gu_rows, int H,
+                                              int I) {
+  return f < Ngu ? f / H : n_gu_rows + (f - Ngu) / I;
+}
 
-// x_perm[row] = x[perm_tok[row]] for routed rows, 0 for padding and tail rows. One warp per row,
-// 16-byte vectors when a row is a whole number of them.
-constexpr int GATHER_ROWS = 8;
-template <typename T>
-__global__ void __launch_bounds__(32 * GATHER_ROWS) gather_rows_kernel(
-    const T* __restrict__ x, const int32_t* __restrict__ ptok, const int32_t* __restrict__ pslot,
-    const int32_t* __restrict__ off_end, int64_t R_cap, int H, T* __restrict__ xp) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = (int64_t)blockIdx.x * GATHER_ROWS + (threadIdx.x >> 5);
-  if (row >= R_cap) return;
-  const bool live = row < *off_end && pslot[row] >= 0;
-  const int64_t src = live ? (int64_t)ptok[row] * H : 0;
-  if (((H * sizeof(T)) & 15) == 0) {
-    const int nv = (int)(H * sizeof(T) / 16);
-    const uint4* sp = reinterpret_cast<const uint4*>(x + src);
-    uint4* dp = reinterpret_cast<uint4*>(xp + row * H);
-#pragma unroll 4
-    for (int i = lane; i < nv; i += 32) dp[i] = live ? __ldg(sp + i) : make_uint4(0, 0, 0, 0);
-  } else {
-    for (int i = lane; i < H; i += 32) xp[row * H + i] = live ? x[src + i] : from_f32<T>(0.f);
+__global__ void row_ptr_kernel(const int64_t* __restrict__ act, int64_t K, int64_t n_gu_rows,
+                               int64_t n_rows, int H, int I, int64_t Ngu,
+                               int32_t* __restrict__ rp) {
+  const int64_t tail = K > 0 ? weight_row(act[K - 1], Ngu, n_gu_rows, H, I) + 1 : 0;
+  const int64_t n = K > n_rows + 1 ? K : n_rows + 1;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    if (i < K) {
+      const int64_t pos = weight_row(act[i], Ngu, n_gu_rows, H, I);
+      const int64_t prev = i > 0 ? weight_row(act[i - 1], Ngu, n_gu_rows, H, I) : -1;
+      for (int64_t x = prev + 1; x <= pos; ++x) rp[x] = (int32_t)i;
+    }
+    if (i >= tail && i <= n_rows) rp[i] = (int32_t)K;
   }
+}
+
+// g_router[e, h] = sum over the rows routed to e of dl[row] * x^T[h, row] (renormalised routing):
+// one group of eight lanes per (e, h), 16-byte vectors of x^T.
+template <typename T>
+__global__ void __launch_bounds__(256) g_router_sel_kernel(
+    const T* __restrict__ xT, const float* __restrict__ dl_perm, const int32_t* __restrict__ cnt,
+    const int32_t* __restrict__ off, int E, int H, int64_t rcap, float* __restrict__ g_router,
+    uint32_t* dev_status) {
+  constexpr int VW = 16 / sizeof(T);
+  const int lane = threadIdx.x & 31, grp = lane >> 3, gl = lane & 7;
+  const int64_t groups = (int64_t)gridDim.x * (blockDim.x >> 3);
+  bool bad = false;
+  for (int64_t u0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 4;
+       u0 < (int64_t)E * H; u0 += groups) {
+    const int64_t u = u0 + grp;
+    float acc = 0.f;
+    if (u < (int64_t)E * H) {
+      const int e = (int)(u / H), h = (int)(u % H);
+      const int o = off[e];
+      const int n = (cnt[e] + VW - 1) / VW * VW;
+      const T* xr = xT + (int64_t)h * rcap + o;
+      const float* d = dl_perm + o;
+      const int cn = cnt[e];  // dl_perm holds no value past the expert's routed rows
+      for (int t = gl * VW; t < n; t += 8 * VW) {
+        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xr + t));
+        const T* xe = reinterpret_cast<const T*>(&xv);
+#pragma unroll
+        for (int q = 0; q < VW; ++q)
+          if (t + q < cn) acc = fmaf(d[t + q], to_f32(xe[q]), acc);
+      }
+    }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    if (gl == 0 && u < (int64_t)E * H) {
+      g_router[u] = acc;
+      bad |= !finite_f(acc);
+    }
+  }
+  flag_status_warp(dev_status, bad, USAF_DEV_NONFINITE);
 }
 
 __global__ void zero_f32_kernel(float* __restrict__ p, int64_t n) {
@@ -357,44 +484,6 @@ __global__ void dlogit_dense_kernel(const float* __restrict__ logits,
 // g_router[e, h] = sum over the rows routed to e of dl[row] * x_perm[row, h] (renormalised
 // routing); each thread owns two adjacent h, rows in order, eight rows in flight.
 template <typename T>
-__global__ void __launch_bounds__(256) g_router_sel_kernel(
-    const T* __restrict__ xp, const float* __restrict__ dl_perm, const int32_t* __restrict__ cnt,
-    const int32_t* __restrict__ off, int H, float* __restrict__ g_router, uint32_t* dev_status) {
-  const int e = blockIdx.y;
-  const int h0 = (blockIdx.x * blockDim.x + threadIdx.x) * 2;
-  float a0 = 0.f, a1 = 0.f;
-  if (h0 < H) {
-    const bool two = h0 + 1 < H;
-    const int n = cnt[e], o = off[e];
-    const T* base = xp + (int64_t)o * H + h0;
-    int i = 0;
-    for (; i + 8 <= n; i += 8) {
-      float x0[8], x1[8], d[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        x0[u] = to_f32(base[(int64_t)(i + u) * H]);
-        x1[u] = two ? to_f32(base[(int64_t)(i + u) * H + 1]) : 0.f;
-        d[u] = dl_perm[o + i + u];
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        a0 = fmaf(d[u], x0[u], a0);
-        a1 = fmaf(d[u], x1[u], a1);
-      }
-    }
-    for (; i < n; ++i) {
-      const float d = dl_perm[o + i];
-      a0 = fmaf(d, to_f32(base[(int64_t)i * H]), a0);
-      if (two) a1 = fmaf(d, to_f32(base[(int64_t)i * H + 1]), a1);
-    }
-    g_router[(int64_t)e * H + h0] = a0;
-    if (two) g_router[(int64_t)e * H + h0 + 1] = a1;
-  }
-  flag_status_warp(dev_status, h0 < H && (!finite_f(a0) || !finite_f(a1)), USAF_DEV_NONFINITE);
-}
-
-// g_router[e, h] = sum_t dlogit[t, e] * x[t, h]   (softmax-over-all-E routing)
-template <typename T>
 __global__ void g_router_dense_kernel(const T* __restrict__ x, const float* __restrict__ dlogit,
                                       int Tn, int E, int H, float* __restrict__ g_router,
                                       uint32_t* dev_status) {
@@ -464,6 +553,7 @@ __global__ void __launch_bounds__(256) dx_finalize_kernel(
   flag_status_warp(dev_status, bad, USAF_DEV_NONFINITE);
 }
 
+
 // ================================================================================================
 // Host orchestration
 // ================================================================================================
@@ -483,27 +573,37 @@ void bwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, int64_t K, Carver& c,
   w.dh = c.take<char>(R_cap * 2 * s.I * (int64_t)es);
   w.dx_acc = c.take<float>(s.T * s.H);
   w.gvec = dt == USAF_F32 ? c.take<float>(R_cap * s.I) : nullptr;
-  w.tile_ptr = dt == USAF_BF16 ? c.take<int32_t>(tile_ptr_entries(s)) : nullptr;
+  w.row_ptr = c.take<int32_t>(s.E * 2 * s.I + s.E * s.H + 1);
   w.plan = dt == USAF_BF16 ? c.take<int32_t>(s.E + 1) : nullptr;
-  w.dy_perm = dt == USAF_BF16 ? (void*)c.take<char>(R_cap * s.H * 2) : nullptr;
+  w.dy_perm = c.take<char>(R_cap * s.H * (int64_t)es);
 }
 
+template <typename T>
+static usaf_status gather_t(const MoeArgs& a, const T* src, T* dstT, cudaStream_t st) {
+  const dim3 grid((unsigned)ceil_div(a.R_cap, 32), (unsigned)ceil_div(a.s.H, 64));
+  gather_transpose_kernel<T><<<grid, 256, 0, st>>>(src, a.rt.perm_tok, a.rt.perm_slot,
+                                                   a.rt.expert_offset + a.s.E, a.R_cap,
+                                                   (int)a.s.H, dstT);
+  USAF_CHECK_LAUNCH();
+  return USAF_OK;
+}
 
 template <typename T>
-static usaf_status fwd_simt(const MoeArgs& a, T* xp, T* h, T* wa, float* yacc, cudaStream_t st) {
+static usaf_status fwd_simt(const MoeArgs& a, T* xT, T* hT, T* waT, float* yacc, cudaStream_t st) {
   USAF_TRACE("simt_fwd", st);
   const auto& s = a.s;
   const int H = (int)s.H, I = (int)s.I, E = (int)s.E;
   const int32_t* cnt = a.rt.expert_count;
   const int32_t* off = a.rt.expert_offset;
-  ProbGateUp<T> p1{xp, static_cast<const T*>(a.w_gate_up), h, cnt, off, H, 2 * I, a.R_cap};
+  ProbGateUp<T> p1{xT, static_cast<const T*>(a.w_gate_up), hT, cnt, off, H, 2 * I, a.R_cap};
   dim3 g1((unsigned)ceil_div(2 * I, 64), (unsigned)ceil_div(s.T, 64), (unsigned)E);
   simt_gemm_kernel<<<g1, 256, 0, st>>>(p1);
   USAF_CHECK_LAUNCH();
-  swiglu_fwd_rows_kernel<T><<<(unsigned)a.R_cap, 128, 0, st>>>(h, a.rt.perm_slot, a.rt.topk_w,
-                                                               off + E, I, a.R_cap, wa);
+  swiglu_fwd_rows_kernel<T><<<(unsigned)a.R_cap, 128, 0, st>>>(hT, a.rt.perm_slot, a.rt.topk_w,
+                                                               off + E, I, a.R_cap, waT);
   USAF_CHECK_LAUNCH();
-  ProbDown<T> p2{wa, static_cast<const T*>(a.w_down), yacc, cnt, off, a.rt.perm_tok, H, I};
+  ProbDown<T> p2{waT, static_cast<const T*>(a.w_down), yacc, cnt, off, a.rt.perm_tok, H, I,
+                 a.R_cap};
   dim3 g2((unsigned)ceil_div(H, 64), (unsigned)ceil_div(s.T, 64), (unsigned)E);
   simt_gemm_kernel<<<g2, 256, 0, st>>>(p2);
   USAF_CHECK_LAUNCH();
@@ -511,27 +611,24 @@ static usaf_status fwd_simt(const MoeArgs& a, T* xp, T* h, T* wa, float* yacc, c
 }
 
 template <typename T>
-static usaf_status moe_fwd_t(const MoeArgs& a, T* xp, T* h, T* wa, T* y, FwdWs& w,
+static usaf_status moe_fwd_t(const MoeArgs& a, T* xT, T* hT, T* waT, T* y, FwdWs& w,
                              cudaStream_t st) {
   const auto& s = a.s;
   const int64_t TH = s.T * s.H;
   {
-  USAF_TRACE("gather_x", st);
-  gather_rows_kernel<T><<<(unsigned)ceil_div(a.R_cap, GATHER_ROWS), 32 * GATHER_ROWS, 0, st>>>(
-      static_cast<const T*>(a.x), a.rt.perm_tok, a.rt.perm_slot, a.rt.expert_offset + s.E,
-      a.R_cap, (int)s.H, xp);
-  USAF_CHECK_LAUNCH();
-  zero_f32_kernel<<<grid_dim_for(TH), 256, 0, st>>>(w.y_acc, TH);
-  USAF_CHECK_LAUNCH();
+    USAF_TRACE("gather_x", st);
+    USAF_TRY(gather_t<T>(a, static_cast<const T*>(a.x), xT, st));
+    zero_f32_kernel<<<grid_dim_for(TH), 256, 0, st>>>(w.y_acc, TH);
+    USAF_CHECK_LAUNCH();
   }
   if (a.dt == USAF_BF16) {
     MoeArgs b = a;
     b.plan = w.plan;
     USAF_TRY(tc_plan(b, st));
-    USAF_TRY(tc_fwd_gate_up(b, xp, h, wa, st));
-    USAF_TRY(tc_fwd_down(b, wa, w.y_acc, st));
+    USAF_TRY(tc_fwd_gate_up(b, xT, hT, waT, st));
+    USAF_TRY(tc_fwd_down(b, waT, w.y_acc, st));
   } else {
-    USAF_TRY(fwd_simt<T>(a, xp, h, wa, w.y_acc, st));
+    USAF_TRY(fwd_simt<T>(a, xT, hT, waT, w.y_acc, st));
   }
   USAF_TRACE("combine_finalize", st);
   f32_to_kernel<T><<<grid_dim_for(TH), 256, 0, st>>>(w.y_acc, y, TH);
@@ -550,40 +647,9 @@ usaf_status moe_fwd_launch(const MoeArgs& a, void* x_perm, void* h, void* wa, vo
                           static_cast<float*>(wa), static_cast<float*>(y), w, st);
 }
 
-// For every weight row (gate_up rows, then down rows) and every 256-column tile of it, the first
-// active entry at or after the tile's first column; entry NT of a row is the row's end. The
-// actives are sorted, so their (row, tile) positions are too: active a fills the entries between
-// its predecessor's position and its own, and the entries after the last active get K.
-__device__ __forceinline__ int64_t tile_pos(int64_t f, int64_t Ngu, int64_t n_gu_rows, int H,
-                                            int I, int nt_gu, int nt_d) {
-  if (f < Ngu) return (f / H) * (nt_gu + 1) + (f % H) / 256;
-  const int64_t fd = f - Ngu;
-  return n_gu_rows * (nt_gu + 1) + (fd / I) * (nt_d + 1) + (fd % I) / 256;
-}
-
-__global__ void tile_ptr_kernel(const int64_t* __restrict__ act, int64_t K, int64_t n_gu_rows,
-                                int64_t n_entries, int H, int I, int64_t Ngu, int nt_gu, int nt_d,
-                                int32_t* __restrict__ tp) {
-  const int64_t tail = K > 0 ? tile_pos(act[K - 1], Ngu, n_gu_rows, H, I, nt_gu, nt_d) + 1 : 0;
-  const int64_t n = K > n_entries ? K : n_entries;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    if (i < K) {
-      const int64_t pos = tile_pos(act[i], Ngu, n_gu_rows, H, I, nt_gu, nt_d);
-      const int64_t prev = i > 0 ? tile_pos(act[i - 1], Ngu, n_gu_rows, H, I, nt_gu, nt_d) : -1;
-      for (int64_t x = prev + 1; x <= pos; ++x) tp[x] = (int32_t)i;
-    }
-    if (i >= tail && i < n_entries) tp[i] = (int32_t)K;
-  }
-}
-
-int64_t tile_ptr_entries(const usaf_moe_shape& s) {
-  return s.E * 2 * s.I * (ceil_div(s.H, 256) + 1) + s.E * s.H * (ceil_div(s.I, 256) + 1);
-}
-
 template <typename T>
-static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits, const T* xp,
-                             const T* h, const T* wa, const T* dy, const int64_t* act_idx,
+static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits, const T* xT,
+                             const T* hT, const T* waT, const T* dy, const int64_t* act_idx,
                              int64_t K, float* g_act, float* g_router, T* dx, float* dw_out,
                              uint32_t* dev_status, BwdWs& w, cudaStream_t st) {
   MoeArgs a = a0;
@@ -592,52 +658,50 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
   const int H = (int)s.H, I = (int)s.I, E = (int)s.E, Tn = (int)s.T, k = (int)s.k;
   const int32_t* cnt = a.rt.expert_count;
   const int32_t* off = a.rt.expert_offset;
-  const int32_t* ptok = a.rt.perm_tok;
   const int32_t* pslot = a.rt.perm_slot;
   float* dw = dw_out ? dw_out : w.dw;
-  T* dh = static_cast<T*>(w.dh);
-  T* dyp = static_cast<T*>(w.dy_perm);
+  T* dhT = static_cast<T*>(w.dh);
+  T* dyT = static_cast<T*>(w.dy_perm);
   const int64_t Ngu = s.E * 2 * s.I * s.H;
 
   // S6: gvec, dw, dh
+  {
+    USAF_TRACE("gather_dy", st);
+    USAF_TRY(gather_t<T>(a, dy, dyT, st));
+    zero_f32_kernel<<<grid_dim_for(s.T * s.k), 256, 0, st>>>(dw, s.T * s.k);
+    USAF_CHECK_LAUNCH();
+  }
   if (a.dt == USAF_BF16) {
-    {
-      USAF_TRACE("gather_dy", st);
-      gather_rows_kernel<T><<<(unsigned)ceil_div(a.R_cap, GATHER_ROWS), 32 * GATHER_ROWS, 0,
-                              st>>>(dy, ptok, pslot, off + E, a.R_cap, H, dyp);
-      USAF_CHECK_LAUNCH();
-      zero_f32_kernel<<<grid_dim_for(s.T * s.k), 256, 0, st>>>(dw, s.T * s.k);
-      USAF_CHECK_LAUNCH();
-    }
     USAF_TRY(tc_plan(a, st));
-    USAF_TRY(tc_bwd_gvec(a, dyp, h, dh, dw, st));
+    USAF_TRY(tc_bwd_gvec(a, dyT, hT, dhT, dw, st));
   } else {
-    ProbGvec<T> p{dy, static_cast<const T*>(a.w_down), w.gvec, cnt, off, ptok, H, I};
+    USAF_TRACE("simt_gvec", st);
+    ProbGvec<T> p{dyT, static_cast<const T*>(a.w_down), w.gvec, cnt, off, H, I, a.R_cap};
     dim3 g((unsigned)ceil_div(I, 64), (unsigned)ceil_div(Tn, 64), (unsigned)E);
     simt_gemm_kernel<<<g, 256, 0, st>>>(p);
     USAF_CHECK_LAUNCH();
-    swiglu_bwd_rows_kernel<T><<<(unsigned)a.R_cap, 128, 0, st>>>(w.gvec, h, pslot, a.rt.topk_w,
-                                                                 off + E, I, a.R_cap, dh, dw);
+    swiglu_bwd_rows_kernel<T><<<(unsigned)a.R_cap, 128, 0, st>>>(w.gvec, hT, pslot, a.rt.topk_w,
+                                                                 off + E, I, a.R_cap, dhT, dw);
     USAF_CHECK_LAUNCH();
   }
   // S7: router gradient
   {
-  USAF_TRACE("router_bwd", st);
-  if (renorm) {
-    dlogit_sel_kernel<<<(unsigned)ceil_div(Tn, 128), 128, 0, st>>>(a.rt.topk_w, dw, a.rt.slot_row,
-                                                                  Tn, k, w.dl, w.dl_perm);
-    USAF_CHECK_LAUNCH();
-    g_router_sel_kernel<T><<<dim3((unsigned)ceil_div(ceil_div(H, 2), 256), (unsigned)E), 256, 0,
-                             st>>>(xp, w.dl_perm, cnt, off, H, g_router, dev_status);
-    USAF_CHECK_LAUNCH();
-  } else {
-    dlogit_dense_kernel<<<(unsigned)Tn, 128, 0, st>>>(logits, a.rt.topk_idx, a.rt.topk_w, dw, Tn,
-                                                      E, k, w.dlogit);
-    USAF_CHECK_LAUNCH();
-    g_router_dense_kernel<T><<<dim3((unsigned)ceil_div(H, 128), (unsigned)E), 128, 0, st>>>(
-        static_cast<const T*>(a.x), w.dlogit, Tn, E, H, g_router, dev_status);
-    USAF_CHECK_LAUNCH();
-  }
+    USAF_TRACE("router_bwd", st);
+    if (renorm) {
+      dlogit_sel_kernel<<<(unsigned)ceil_div(Tn, 128), 128, 0, st>>>(
+          a.rt.topk_w, dw, a.rt.slot_row, Tn, k, w.dl, w.dl_perm);
+      USAF_CHECK_LAUNCH();
+      g_router_sel_kernel<T><<<(unsigned)ceil_div(s.E * s.H, 32), 256, 0, st>>>(
+          xT, w.dl_perm, cnt, off, E, H, a.R_cap, g_router, dev_status);
+      USAF_CHECK_LAUNCH();
+    } else {
+      dlogit_dense_kernel<<<(unsigned)Tn, 128, 0, st>>>(logits, a.rt.topk_idx, a.rt.topk_w, dw,
+                                                        Tn, E, k, w.dlogit);
+      USAF_CHECK_LAUNCH();
+      g_router_dense_kernel<T><<<dim3((unsigned)ceil_div(H, 128), (unsigned)E), 128, 0, st>>>(
+          static_cast<const T*>(a.x), w.dlogit, Tn, E, H, g_router, dev_status);
+      USAF_CHECK_LAUNCH();
+    }
   }
   // S8: dx
   if (dx) {
@@ -647,37 +711,35 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
       USAF_CHECK_LAUNCH();
     }
     if (a.dt == USAF_BF16) {
-      USAF_TRY(tc_bwd_dx(a, dh, w.dx_acc, st));
+      USAF_TRY(tc_bwd_dx(a, dhT, w.dx_acc, st));
     } else {
-      ProbDx<T> p{dh, static_cast<const T*>(a.w_gate_up), w.dx_acc, cnt, off, ptok, H, 2 * I};
+      USAF_TRACE("simt_dx", st);
+      ProbDx<T> p{dhT, static_cast<const T*>(a.w_gate_up), w.dx_acc, cnt, off, a.rt.perm_tok,
+                  H, 2 * I, a.R_cap};
       dim3 g((unsigned)ceil_div(H, 64), (unsigned)ceil_div(Tn, 64), (unsigned)E);
       simt_gemm_kernel<<<g, 256, 0, st>>>(p);
       USAF_CHECK_LAUNCH();
     }
     USAF_TRACE("dx_finalize", st);
-    dx_finalize_kernel<T><<<(unsigned)Tn, 256, 0, st>>>(
-        w.dx_acc, a.w_router, a.rt.topk_idx, w.dl, w.dlogit, Tn, H, E, k, renorm, dx,
-        dev_status);
+    dx_finalize_kernel<T><<<(unsigned)Tn, 256, 0, st>>>(w.dx_acc, a.w_router, a.rt.topk_idx, w.dl,
+                                                        w.dlogit, Tn, H, E, k, renorm, dx,
+                                                        dev_status);
     USAF_CHECK_LAUNCH();
   }
   // S9, S10: expert weight gradients at the active set
   if (K > 0) {
-    if (a.dt == USAF_BF16) {
-      const int64_t n_gu_rows = s.E * 2 * s.I, n_rows = n_gu_rows + s.E * s.H;
-      {
-      USAF_TRACE("wgrad_tile_ptr", st);
-      tile_ptr_kernel<<<grid_dim_for(std::max<int64_t>(K, tile_ptr_entries(s))), 256, 0, st>>>(
-          act_idx, K, n_gu_rows, tile_ptr_entries(s), H, I, Ngu, (int)ceil_div(H, 256),
-          (int)ceil_div(I, 256), w.tile_ptr);
-      USAF_CHECK_LAUNCH();
-      }
-      USAF_TRY(tc_bwd_wgrad(a, xp, dyp, dh, wa, act_idx, K, w.tile_ptr, g_act, dev_status, st));
-    } else {
-      USAF_TRACE("simt_wgrad", st);
-      masked_wgrad_simt_kernel<T><<<(unsigned)ceil_div(K, 128), 128, 0, st>>>(
-          act_idx, K, xp, dy, dh, wa, cnt, off, ptok, H, I, Ngu, g_act, dev_status);
+    const int64_t n_gu_rows = s.E * 2 * s.I, n_rows = n_gu_rows + s.E * s.H;
+    {
+      USAF_TRACE("wgrad_row_ptr", st);
+      row_ptr_kernel<<<grid_dim_for(std::max<int64_t>(K, n_rows + 1)), 256, 0, st>>>(
+          act_idx, K, n_gu_rows, n_rows, H, I, Ngu, w.row_ptr);
       USAF_CHECK_LAUNCH();
     }
+    USAF_TRACE("wgrad_sddmm", st);
+    const unsigned blocks = (unsigned)std::min<int64_t>(ceil_div(n_rows, 8), device_sm_count() * 16);
+    sddmm_kernel<T><<<blocks, 256, 0, st>>>(act_idx, w.row_ptr, n_rows, n_gu_rows, cnt, off, H, I,
+                                            Ngu, a.R_cap, dhT, xT, dyT, waT, g_act, dev_status);
+    USAF_CHECK_LAUNCH();
   }
   return USAF_OK;
 }

@@ -1,20 +1,21 @@
 // bf16 grouped expert GEMMs on 5th-generation tensor cores (tcgen05.mma, accumulators in TMEM),
 // fed by TMA (cp.async.bulk.tensor) through a 4-stage mbarrier pipeline. One persistent CTA per SM
 // with three roles: warp 0 issues TMA loads, warp 1 issues MMAs (one thread) and owns the TMEM
-// allocation, warps 2-5 run the fused epilogue out of a double-buffered TMEM accumulator.
+// allocation, eight epilogue warps run the fused epilogue out of a double-buffered TMEM
+// accumulator (two warps per TMEM lane quarter, alternating 32-column chunks).
 //
-// Every GEMM is arranged with the weight dimension as M (128 rows per tile) and the routed
-// tokens as N (16..256 per tile) or as K, so each expert's ragged token count only pads to 16.
-//   S4 gate_up: h^T = gate_up[e] x_perm^T   A = gate/up rows interleaved (K-major), B = x rows
-//               epilogue: SwiGLU (act(gate)*up, experts4bit-qlora epilogue contract), scaled by
-//               the routing weight; writes h and w*A
-//   S5 down:    y^T = down[e] (wA)^T         epilogue: scatter-add into the fp32 combine buffer
-//   S6 gvec:    g^T = down[e]^T dy_perm^T    A = down[e] MN-major; epilogue: SwiGLU backward,
-//               dw (routing-weight gradient), dh
-//   S8 dx:      dx^T = gate_up[e]^T dh^T     A = gate_up[e] MN-major; epilogue: scatter-add
-//   S9/S10 masked wgrad: dW = dh^T x_perm and dy_perm^T (wA) per expert, tokens as K, both
-//               operands MN-major; the epilogue keeps only the active entries (USAF README:
-//               only the selected 0.5% of expert weights are trained).
+// Every GEMM puts the weight dimension on M (128 rows per tile) and the routed tokens on N
+// (16..256 per tile), so an expert's ragged token count only pads to 16. The token operand is
+// feature-major (one row per feature, the expert's permuted tokens contiguous) and is loaded as
+// the MN-major B operand in boxes of 64 tokens.
+//   S4 gate_up: h^T = gate_up[e] x^T     A = gate/up rows interleaved (K-major), B = x^T
+//               epilogue: SwiGLU (act(gate)*up, experts4bit-qlora epilogue contract) times the
+//               routing weight; writes h^T and (w*A)^T with 16-byte stores
+//   S5 down:    y^T = down[e] (wA)^T      epilogue: scatter-add into the fp32 combine buffer
+//   S6 gvec:    g^T = down[e]^T dy^T      A = down[e] MN-major; epilogue: SwiGLU backward,
+//               dw (routing-weight gradient), dh^T
+//   S8 dx:      dx^T = gate_up[e]^T dh^T  A = gate_up[e] MN-major; epilogue: scatter-add
+//   router:     logits^T = [Wr_hi|Wr_mid|Wr_lo] [x|x|x]^T, three bf16 parts of the fp32 router
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -31,23 +32,19 @@ constexpr int BN = 256;
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
+constexpr int B_BOX = 64 * BK * 2;  // one MN-major box: 64 tokens x 64 k
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int EPI_WARPS = 8;  // two warps per TMEM lane quarter, alternating 32-column chunks
+constexpr int EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
-constexpr int WG_PREFETCH = 8;  // active entries per row and tile held in registers
-constexpr int WG_PITCH = 20;    // floats per staged row: 16 columns + 4 (bank-conflict-free)
-constexpr int WG_STAGE_BYTES = EPI_WARPS * 32 * WG_PITCH * 4;
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_E = 1024;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + 2 * (MAX_E + 1) * 4 + 128 +
-                           WG_STAGE_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + 2 * (MAX_E + 1) * 4;
 static_assert(SMEM_BYTES <= 232448, "shared memory of the tensor-core kernel");
 constexpr long long TIMEOUT_CYCLES = 1ll << 32;  // about two seconds
 
-enum Var { V_GATEUP = 0, V_DOWN = 1, V_GVEC = 2, V_DX = 3, V_WG_GU = 4, V_WG_D = 5, V_ROUTER = 6 };
+enum Var { V_GATEUP = 0, V_DOWN = 1, V_GVEC = 2, V_DX = 3, V_ROUTER = 4 };
 
 struct Params {
-  const int32_t* cnt;
   const int32_t* off;
   const int32_t* ptok;
   const int32_t* pslot;
@@ -55,19 +52,13 @@ struct Params {
   const int32_t* plan;
   int E, H, I, T;
   int MT, NT;
-  int cl;  // CTAs per cluster along M; they share each B tile by TMA multicast
-  __nv_bfloat16* h;
-  __nv_bfloat16* wa;
-  float* acc_out;  // y_acc (S5), dx_acc (S8) or the router logits
-  float* dw;
-  __nv_bfloat16* dh;
-  const __nv_bfloat16* hin;
-  const int64_t* act;
-  const int32_t* tile_ptr;  // per weight row and N tile: first active entry (wgrad)
-  int64_t tp_base;          // offset of this variant's rows in tile_ptr
-  float* g_act;
-  int64_t Ngu;
-  int64_t R_cap;  // row pitch of the feature-major h (gate|up) array
+  int64_t R_cap;  // row pitch of the feature-major arrays
+  __nv_bfloat16* h;       // h^T out (S4)
+  __nv_bfloat16* wa;      // (w*A)^T out (S4)
+  float* acc_out;         // y_acc (S5), dx_acc (S8) or the router logits
+  float* dw;              // S6
+  __nv_bfloat16* dh;      // dh^T out (S6)
+  const __nv_bfloat16* hin;  // h^T in (S6)
   uint32_t* status;
 };
 
@@ -113,23 +104,6 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, uin
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
 }
-__device__ __forceinline__ void tma_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                          int c0, int c1, uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(mask)
-      : "memory");
-}
-__device__ __forceinline__ uint32_t cta_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
 __device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
                                        int c1, int c2, int c3) {
   asm volatile(
@@ -155,14 +129,6 @@ __device__ __forceinline__ void umma_bf16(uint32_t d, uint64_t a, uint64_t b, ui
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-// arrive on the same barrier in every CTA of the cluster named by mask once the MMAs complete
-__device__ __forceinline__ void umma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(mask)
       : "memory");
 }
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
@@ -201,23 +167,17 @@ __device__ __forceinline__ uint32_t idesc_bf16(int n, bool a_mn, bool b_mn) {
 
 // ---------------------------------------------------------------------------- tiles
 struct Tile {
-  int live;
   int e;
   int m0;     // first M row of the tile (feature / weight row)
-  int row0;   // first permuted row (token tiles) or the expert's first row (wgrad K base)
-  int nrows;  // tokens in a token tile (multiple of 16)
-  int n0;     // first N column (wgrad)
-  int nt;     // N tile index (wgrad)
+  int row0;   // first permuted row (token) of the tile
+  int nrows;  // tokens in the tile (multiple of 16)
   int klen;   // K extent
 };
 
 template <int VAR>
 struct VarTraits {
-  static constexpr bool token_tiled = VAR <= V_DX;        // N = an expert's routed tokens
-  static constexpr bool wgrad = VAR == V_WG_GU || VAR == V_WG_D;  // K = an expert's tokens
-  static constexpr bool router = VAR == V_ROUTER;         // plain GEMM over all tokens
-  static constexpr bool a_mn = VAR == V_GVEC || VAR == V_DX || wgrad;
-  static constexpr bool b_mn = wgrad;
+  static constexpr bool router = VAR == V_ROUTER;
+  static constexpr bool a_mn = VAR == V_GVEC || VAR == V_DX;
 };
 constexpr int ROUTER_BN = 128;
 
@@ -231,64 +191,41 @@ __device__ __forceinline__ int upper_bound_i32(const int32_t* a, int n, int v) {
   return lo;
 }
 
+// Tile t: (expert, M tile, token tile) with token tiles fastest; experts' token tiles come from
+// the plan (a prefix over experts of ceil(padded rows / 256)), split into equal 16-row multiples.
 template <int VAR>
 __device__ __forceinline__ Tile get_tile(const Params& p, const int32_t* s_plan,
                                          const int32_t* s_off, int t) {
   Tile ti{};
-  if constexpr (VarTraits<VAR>::token_tiled) {
-    // t counts cluster tiles (e, M group, token tile); this CTA takes M tile group * cl + rank
-    const int mtc = p.MT / p.cl;
-    const int e = upper_bound_i32(s_plan, p.E + 1, t / mtc) - 1;
+  if constexpr (VarTraits<VAR>::router) {
+    const int mt = t / p.NT, nt = t % p.NT;
+    ti.m0 = mt * BM;
+    ti.row0 = nt * ROUTER_BN;
+    ti.nrows = min(ROUTER_BN, (p.T - ti.row0 + 15) / 16 * 16);
+    ti.klen = 3 * p.H;
+  } else {
+    const int e = upper_bound_i32(s_plan, p.E + 1, t / p.MT) - 1;
     const int nts = s_plan[e + 1] - s_plan[e];
-    const int local = t - mtc * s_plan[e];
-    const int mt = (local / nts) * p.cl + (int)cta_rank(), nt = local % nts;
+    const int local = t - p.MT * s_plan[e];
+    const int mt = local / nts, nt = local % nts;
     const int npad = s_off[e + 1] - s_off[e];
     const int base = ((npad + nts - 1) / nts + 15) / 16 * 16;
-    ti.live = 1;
     ti.e = e;
     ti.m0 = mt * (VAR == V_GATEUP ? 64 : BM);
     ti.row0 = s_off[e] + nt * base;
     ti.nrows = min(base, npad - nt * base);
-    ti.n0 = 0;
     ti.klen = (VAR == V_GATEUP || VAR == V_GVEC) ? p.H : (VAR == V_DOWN ? p.I : 2 * p.I);
-  } else if constexpr (VarTraits<VAR>::router) {
-    const int mt = t / p.NT, nt = t % p.NT;
-    ti.live = 1;
-    ti.m0 = mt * BM;
-    ti.n0 = nt * ROUTER_BN;
-    ti.nrows = min(ROUTER_BN, (p.T - ti.n0 + 15) / 16 * 16);
-    ti.klen = 3 * p.H;
-  } else {
-    const int per = (p.MT / p.cl) * p.NT;
-    const int e = t / per, local = t % per;
-    const int npad = s_off[e + 1] - s_off[e];
-    ti.live = npad > 0;
-    ti.e = e;
-    ti.m0 = ((local / p.NT) * p.cl + (int)cta_rank()) * BM;
-    ti.nt = local % p.NT;
-    ti.n0 = ti.nt * BN;
-    ti.row0 = s_off[e];
-    ti.nrows = BN;
-    ti.klen = npad;
   }
   return ti;
 }
 
 template <int VAR>
 __device__ __forceinline__ int total_tiles(const Params& p, const int32_t* s_plan) {
-  if constexpr (VarTraits<VAR>::token_tiled) return (p.MT / p.cl) * s_plan[p.E];
-  else if constexpr (VarTraits<VAR>::router) return p.MT * p.NT;
-  else return p.E * (p.MT / p.cl) * p.NT;
+  if constexpr (VarTraits<VAR>::router) return p.MT * p.NT;
+  else return p.MT * s_plan[p.E];
 }
 
 // ---------------------------------------------------------------------------- epilogues
-__device__ __forceinline__ float pick32(const float (&v)[32], int j) {
-  float r = v[0];
-#pragma unroll
-  for (int q = 1; q < 32; ++q) r = (j == q) ? v[q] : r;
-  return r;
-}
-
 // Column sums of a 32x32 block held one column per register: after 31 shuffles lane l holds the
 // sum over the warp's lanes of column l.
 __device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
@@ -307,251 +244,155 @@ __device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
 
 __device__ __forceinline__ float sigmoid_fast(float z) { return __fdividef(1.f, 1.f + __expf(-z)); }
 
-// Operands an epilogue thread loads before its tile's accumulator is ready. The masked-gradient
-// epilogues need the active entries of their row in the tile (the range from tile_ptr, then the
-// columns from the active list: two dependent loads, issued two and one tiles ahead); the SwiGLU
-// backward needs gate and up of its feature for the tile's first 32 tokens.
-struct WgRange {
-  int64_t a0, a1;  // active entries of this row inside the tile
-  int64_t base;    // flat index of the row's column 0
-};
-struct Pre {
-  WgRange r;
-  int cols[WG_PREFETCH];  // tile-relative columns of the first WG_PREFETCH entries (-1: none)
-  uint32_t hg[16];        // gate of the first 32 token columns, two bf16 per word
-  uint32_t hu[16];        // up, likewise
-};
-
-template <int VAR>
-__device__ __forceinline__ WgRange wg_range(const Params& p, const Tile& ti, int row) {
-  WgRange w{0, 0, 0};
-  const bool gu = VAR == V_WG_GU;
-  const int mrows = gu ? 2 * p.I : p.H;
-  const int j = ti.m0 + row;
-  w.base = gu ? ((int64_t)ti.e * 2 * p.I + j) * p.H : p.Ngu + ((int64_t)ti.e * p.H + j) * p.I;
-  if (j < mrows) {
-    const int64_t tp = p.tp_base + ((int64_t)ti.e * mrows + j) * (p.NT + 1) + ti.nt;
-    w.a0 = p.tile_ptr[tp];
-    w.a1 = p.tile_ptr[tp + 1];
-  }
-  return w;
+// 16 bytes = 8 bf16 of a feature-major row; `cnt` of the 8 tokens are valid (0 elsewhere)
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 pr = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&pr);
 }
 
-// gate and up of feature i for the 32 token columns of chunk ch, read from the feature-major h
-// as 16-byte vectors (two tokens per word; zero outside the tile)
-__device__ __forceinline__ void load_h_chunk(const Params& p, const Tile& ti, int ch, int i,
-                                             uint32_t (&g)[16], uint32_t (&u)[16]) {
-  const int ncol = min(32, ti.nrows - ch * 32);
-  const bool iv = i < p.I;
-  const int64_t off = ti.row0 + ch * 32;
-  const uint4* gp = reinterpret_cast<const uint4*>(p.hin + (int64_t)i * p.R_cap + off);
-  const uint4* up = reinterpret_cast<const uint4*>(p.hin + (int64_t)(p.I + i) * p.R_cap + off);
+// store v[0..31] as bf16 to row[0..ncol) (ncol a multiple of 8; row 16-byte aligned)
+__device__ __forceinline__ void store_row32(__nv_bfloat16* row, const float (&v)[32], int ncol) {
+  uint4* dst = reinterpret_cast<uint4*>(row);
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    if (q * 8 < ncol)
+      dst[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                          pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
+                          pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+}
+
+// load row[0..32) bf16 as 16 words (two tokens each); 0 beyond ncol or when !ok
+__device__ __forceinline__ void load_row32(const __nv_bfloat16* row, bool ok, int ncol,
+                                           uint32_t (&w)[16]) {
+  const uint4* src = reinterpret_cast<const uint4*>(row);
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
-    const bool ok = iv && q * 8 < ncol;
-    const uint4 a = ok ? __ldg(gp + q) : make_uint4(0, 0, 0, 0);
-    const uint4 b = ok ? __ldg(up + q) : make_uint4(0, 0, 0, 0);
-    g[4 * q] = a.x; g[4 * q + 1] = a.y; g[4 * q + 2] = a.z; g[4 * q + 3] = a.w;
-    u[4 * q] = b.x; u[4 * q + 1] = b.y; u[4 * q + 2] = b.z; u[4 * q + 3] = b.w;
+    const uint4 a = (ok && q * 8 < ncol) ? __ldg(src + q) : make_uint4(0, 0, 0, 0);
+    w[4 * q] = a.x;
+    w[4 * q + 1] = a.y;
+    w[4 * q + 2] = a.z;
+    w[4 * q + 3] = a.w;
   }
 }
 
-// bf16 number j (0..31) of a packed array of 16 words
 __device__ __forceinline__ float bf_at(const uint32_t (&a)[16], int j) {
   return (j & 1) ? __uint_as_float(a[j >> 1] & 0xFFFF0000u) : __uint_as_float(a[j >> 1] << 16);
 }
 
 template <int VAR>
-__device__ __forceinline__ int next_live(const Params& p, const int32_t* s_plan,
-                                         const int32_t* s_off, int t, int total) {
-  if constexpr (VarTraits<VAR>::wgrad) {
-    while (t < total && !get_tile<VAR>(p, s_plan, s_off, t).live) t += gridDim.x / p.cl;
-  }
-  return t < total ? t : total;
-}
-
-// first level of the lookahead: the wgrad row range of tile t
-template <int VAR>
-__device__ __forceinline__ WgRange prefetch_a(const Params& p, const int32_t* s_plan,
-                                              const int32_t* s_off, int t, int total, int row) {
-  if constexpr (VarTraits<VAR>::wgrad) {
-    if (t < total) return wg_range<VAR>(p, get_tile<VAR>(p, s_plan, s_off, t), row);
-  }
-  return WgRange{0, 0, 0};
-}
-
-// second level: wgrad active columns (from the range), or the first chunk of gate|up
-template <int VAR>
-__device__ __forceinline__ void prefetch_b(const Params& p, const int32_t* s_plan,
-                                           const int32_t* s_off, int t, int total, int row,
-                                           int half, const WgRange& r, Pre& out) {
-  out.r = r;
-  if constexpr (VarTraits<VAR>::wgrad) {
-    const int64_t n0 = t < total ? get_tile<VAR>(p, s_plan, s_off, t).n0 : 0;
-#pragma unroll
-    for (int q = 0; q < WG_PREFETCH; ++q)
-      out.cols[q] = (r.a0 + q < r.a1) ? (int)(p.act[r.a0 + q] - r.base - n0) : -1;
-  } else if constexpr (VAR == V_GVEC) {
-    if (t < total) {
-      const Tile ti = get_tile<VAR>(p, s_plan, s_off, t);
-      load_h_chunk(p, ti, half, ti.m0 + row, out.hg, out.hu);
-    }
-  }
-}
-
-template <int VAR>
 __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32_t taddr, int row,
-                                         int lane, int half, const Pre& pre, float* stage) {
+                                         int lane, int half) {
   constexpr unsigned FULL = 0xffffffffu;
   const int H = p.H, I = p.I;
-  if constexpr (VarTraits<VAR>::token_tiled) {
-    const int nch = (ti.nrows + 31) / 32;
-    uint32_t hg[16], hu[16];  // gate and up of the chunk being processed (V_GVEC only)
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      hg[j] = pre.hg[j];
-      hu[j] = pre.hu[j];
-    }
-    for (int ch = half; ch < nch; ch += 2) {
-      const int cbase = ch * 32;
-      const int col = cbase + lane;
-      int slot = -1, tok = 0;
-      if (col < ti.nrows) {
-        slot = p.pslot[ti.row0 + col];
-        tok = p.ptok[ti.row0 + col];
-      }
-      const float wl = slot >= 0 ? p.topk_w[slot] : 0.f;
-      const int ncol = min(32, ti.nrows - cbase);
-      if constexpr (VAR == V_GATEUP) {
-        float v[32];
-        tmem_ld32(taddr + ch * 32, v);
-        const int i = ti.m0 + (row >> 1);
-        const int g = row & 1;
-        // h is feature-major: this thread's 32 tokens of row g*I+i are 64 contiguous bytes
-        uint4* hp = reinterpret_cast<uint4*>(p.h + (int64_t)(g * I + i) * p.R_cap + ti.row0 + cbase);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (q * 8 < ncol) {
-            uint32_t w4[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const __nv_bfloat162 pr = __floats2bfloat162_rn(v[q * 8 + 2 * k], v[q * 8 + 2 * k + 1]);
-              w4[k] = *reinterpret_cast<const uint32_t*>(&pr);
-            }
-            hp[q] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (j >= ncol) break;
-          const float mine = v[j];
-          const float other = __shfl_xor_sync(FULL, mine, 1);
-          const float wj = __shfl_sync(FULL, wl, j);
-          if (g == 0) {
-            const int64_t r = ti.row0 + cbase + j;
-            p.wa[r * I + i] = __float2bfloat16_rn(wj * mine * sigmoid_fast(mine) * other);
-          }
-        }
-      } else if constexpr (VAR == V_DOWN || VAR == V_DX) {
-        float v[32];
-        tmem_ld32(taddr + ch * 32, v);
-        const int hh = ti.m0 + row;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          if (j >= ncol) break;
-          const int sj = __shfl_sync(FULL, slot, j);
-          const int tj = __shfl_sync(FULL, tok, j);
-          if (sj >= 0 && hh < H) atomicAdd(&p.acc_out[(int64_t)tj * H + hh], v[j]);
-        }
-      } else {  // V_GVEC: SwiGLU backward, dh and the routing-weight gradient dw
-        const int i = ti.m0 + row;
-        const bool iv = i < I;
-        uint32_t ng[16], nu[16];
-        if (ch + 2 < nch) load_h_chunk(p, ti, ch + 2, i, ng, nu);  // in flight during this chunk
-        float v[32];
-        tmem_ld32(taddr + ch * 32, v);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float wj = __shfl_sync(FULL, wl, j);
-          const float gt = bf_at(hg, j), ut = bf_at(hu, j);
-          const float s = sigmoid_fast(gt);
-          const float sg = gt * s;
-          if (iv && j < ncol) {
-            const int64_t r = ti.row0 + cbase + j;
-            const float dA = wj * v[j];
-            p.dh[r * 2 * I + i] = __float2bfloat16_rn(dA * ut * s * (1.f + gt * (1.f - s)));
-            p.dh[r * 2 * I + I + i] = __float2bfloat16_rn(dA * sg);
-          }
-          v[j] = v[j] * sg * ut;
-        }
-        const float dwsum = transpose_reduce32(v, lane);
-        if (slot >= 0) atomicAdd(&p.dw[slot], dwsum);
-        if (ch + 2 < nch) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            hg[j] = ng[j];
-            hu[j] = nu[j];
-          }
-        }
-      }
-    }
-  } else if constexpr (VarTraits<VAR>::router) {
-    // router logits: row = expert, columns = tokens
+  const int nch = (ti.nrows + 31) / 32;
+  if constexpr (VarTraits<VAR>::router) {
     const int e = ti.m0 + row;
-    const int nch = (ti.nrows + 31) / 32;
     for (int ch = half; ch < nch; ch += 2) {
       float v[32];
       tmem_ld32(taddr + ch * 32, v);
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
-        const int tok = ti.n0 + ch * 32 + j;
+        const int tok = ti.row0 + ch * 32 + j;
         if (e < p.E && tok < p.T) p.acc_out[(int64_t)tok * p.E + e] = v[j];
       }
     }
-  } else {
-    // masked weight gradient: keep the active entries of this row inside the tile's columns
-    const int ncols = VAR == V_WG_GU ? H : I;
-    const int nvalid = min(BN, ncols - ti.n0);
-    const int nch = (nvalid + 31) / 32;
-    bool bad = false;
-    const WgRange& wr = pre.r;
-    int64_t cur = wr.a0 + WG_PREFETCH;  // entries beyond the prefetched ones, loaded on the fly
-    float* my = stage + lane * WG_PITCH;  // this thread's staged row (16 columns)
-    for (int ch = half; ch < nch; ch += 2) {
+    return;
+  }
+  uint32_t hg[16], hu[16];  // V_GVEC: gate and up of the chunk being processed
+  if constexpr (VAR == V_GVEC) {
+    const int i = ti.m0 + row;
+    const int ncol = min(32, ti.nrows - half * 32);
+    load_row32(p.hin + (int64_t)i * p.R_cap + ti.row0 + half * 32, i < I && half < nch, ncol, hg);
+    load_row32(p.hin + (int64_t)(I + i) * p.R_cap + ti.row0 + half * 32, i < I && half < nch,
+               ncol, hu);
+  }
+  for (int ch = half; ch < nch; ch += 2) {
+    const int cbase = ch * 32;
+    const int col = cbase + lane;
+    int slot = -1, tok = 0;
+    if (col < ti.nrows) {
+      slot = p.pslot[ti.row0 + col];
+      tok = p.ptok[ti.row0 + col];
+    }
+    const float wl = slot >= 0 ? p.topk_w[slot] : 0.f;
+    const int ncol = min(32, ti.nrows - cbase);
+    if constexpr (VAR == V_GATEUP) {
       float v[32];
       tmem_ld32(taddr + ch * 32, v);
+      const int i = ti.m0 + (row >> 1);
+      const int g = row & 1;  // rows alternate gate (even lane) and up (odd lane) of feature i
+      store_row32(p.h + (int64_t)(g * I + i) * p.R_cap + ti.row0 + cbase, v, ncol);
+      float wa[32];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {  // two halves of 16 columns through shared memory
-        const int lo = ch * 32 + hh * 16;
+      for (int j = 0; j < 32; ++j) {
+        const float other = __shfl_xor_sync(FULL, v[j], 1);
+        const float gate = g ? other : v[j], up = g ? v[j] : other;
+        wa[j] = __shfl_sync(FULL, wl, j) * gate * sigmoid_fast(gate) * up;
+      }
+      // both lanes of the pair hold w*A of feature i; the even lane stores it
+      if (g == 0) store_row32(p.wa + (int64_t)i * p.R_cap + ti.row0 + cbase, wa, ncol);
+    } else if constexpr (VAR == V_DOWN || VAR == V_DX) {
+      float v[32];
+      tmem_ld32(taddr + ch * 32, v);
+      const int hh = ti.m0 + row;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          *reinterpret_cast<float4*>(my + 4 * k) =
-              make_float4(v[hh * 16 + 4 * k], v[hh * 16 + 4 * k + 1], v[hh * 16 + 4 * k + 2],
-                          v[hh * 16 + 4 * k + 3]);
-        __syncwarp();
+      for (int j = 0; j < 32; ++j) {
+        if (j >= ncol) break;
+        const int sj = __shfl_sync(FULL, slot, j);
+        const int tj = __shfl_sync(FULL, tok, j);
+        if (sj >= 0 && hh < H) atomicAdd(&p.acc_out[(int64_t)tj * H + hh], v[j]);
+      }
+    } else {  // V_GVEC: SwiGLU backward, dh^T and the routing-weight gradient dw
+      const int i = ti.m0 + row;
+      const bool iv = i < I;
+      uint32_t ng[16], nu[16];
+      if (ch + 2 < nch) {  // next chunk of gate/up in flight during this one
+        const int nc = min(32, ti.nrows - (ch + 2) * 32);
+        load_row32(p.hin + (int64_t)i * p.R_cap + ti.row0 + cbase + 64, iv, nc, ng);
+        load_row32(p.hin + (int64_t)(I + i) * p.R_cap + ti.row0 + cbase + 64, iv, nc, nu);
+      }
+      float v[32];
+      tmem_ld32(taddr + ch * 32, v);
+      uint32_t pg[16], pu[16];  // dgate, dup of two tokens per word
 #pragma unroll
-        for (int q = 0; q < WG_PREFETCH; ++q) {
-          const int c = pre.cols[q] - lo;
-          if (c >= 0 && c < 16) {
-            const float val = my[c];
-            p.g_act[wr.a0 + q] = val;
-            bad |= !isfinite(val);
+      for (int j2 = 0; j2 < 16; ++j2) {
+        float dgv[2], duv[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int j = 2 * j2 + u;
+          const float wj = __shfl_sync(FULL, wl, j);
+          const float gt = bf_at(hg, j), ut = bf_at(hu, j);
+          const float s = sigmoid_fast(gt);
+          const float sg = gt * s;
+          const float dA = wj * v[j];
+          dgv[u] = dA * ut * s * (1.f + gt * (1.f - s));
+          duv[u] = dA * sg;
+          v[j] = v[j] * sg * ut;
+        }
+        pg[j2] = pack_bf16x2(dgv[0], dgv[1]);
+        pu[j2] = pack_bf16x2(duv[0], duv[1]);
+      }
+      if (iv) {
+        uint4* dg4 = reinterpret_cast<uint4*>(p.dh + (int64_t)i * p.R_cap + ti.row0 + cbase);
+        uint4* du4 = reinterpret_cast<uint4*>(p.dh + (int64_t)(I + i) * p.R_cap + ti.row0 + cbase);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (q * 8 < ncol) {
+            dg4[q] = make_uint4(pg[4 * q], pg[4 * q + 1], pg[4 * q + 2], pg[4 * q + 3]);
+            du4[q] = make_uint4(pu[4 * q], pu[4 * q + 1], pu[4 * q + 2], pu[4 * q + 3]);
           }
         }
-        while (cur < wr.a1) {
-          const int c = (int)(p.act[cur] - wr.base - ti.n0) - lo;
-          if (c >= 16) break;
-          if (c >= 0) {
-            const float val = my[c];
-            p.g_act[cur] = val;
-            bad |= !isfinite(val);
-          }
-          ++cur;
+      }
+      const float dwsum = transpose_reduce32(v, lane);
+      if (slot >= 0) atomicAdd(&p.dw[slot], dwsum);
+      if (ch + 2 < nch) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          hg[j] = ng[j];
+          hu[j] = nu[j];
         }
-        __syncwarp();
       }
     }
-    if (bad) flag_status(p.status, USAF_DEV_NONFINITE);
   }
 }
 
@@ -569,9 +410,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int32_t* s_plan = reinterpret_cast<int32_t*>(smem + STAGES * STAGE_BYTES + 256);
   int32_t* s_off = s_plan + (MAX_E + 1);
-  // wgrad staging, per warp; float4 stores need 16-byte alignment
-  float* s_stage = reinterpret_cast<float*>(
-      (reinterpret_cast<uintptr_t>(s_off + (MAX_E + 1)) + 127) & ~uintptr_t(127));
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES;
@@ -580,13 +418,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if constexpr (!VarTraits<VAR>::router) {
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
       s_off[i] = p.off[i];
-      if (VarTraits<VAR>::token_tiled) s_plan[i] = p.plan[i];
+      s_plan[i] = p.plan[i];
     }
   }
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, p.cl);  // one release from every CTA of the cluster
+      mbar_init(empty0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
@@ -606,12 +444,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (p.cl > 1) cluster_sync();  // peers' barriers are initialised before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int cid = blockIdx.x / p.cl, ncl = gridDim.x / p.cl;
-  const uint32_t rank = cta_rank();
-  const uint16_t mc_mask = (uint16_t)((1u << p.cl) - 1);
   const int total = total_tiles<VAR>(p, s_plan);
   bool failed = false;
 
@@ -621,10 +455,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0;
       uint32_t issued = 0;
-      for (int t = cid; t < total && !failed; t += ncl) {
+      for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
         const Tile ti = get_tile<VAR>(p, s_plan, s_off, t);
-        if (!ti.live) continue;
         const int nkb = (ti.klen + BK - 1) / BK;
+        const int nbox = VarTraits<VAR>::router ? 0 : (ti.nrows + 63) / 64;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) {
             failed = true;
@@ -634,44 +468,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t b_dst = a_dst + A_BYTES;
           const uint32_t fb = full0 + 8 * stage;
           const int k0 = kb * BK;
-          uint32_t bytes = A_BYTES;
-          if constexpr (VarTraits<VAR>::token_tiled) bytes += (ti.nrows > 128 ? 2 : 1) * 16384;
-          else if constexpr (VarTraits<VAR>::router) bytes += 16384;
-          else bytes += B_BYTES;
-          mbar_expect_tx(fb, bytes);
-          if constexpr (VAR == V_GATEUP) {
-            tma_4d(a_dst, &tmA, fb, k0, 0, ti.m0, ti.e);
-          } else if constexpr (VAR == V_DOWN) {
-            tma_2d(a_dst, &tmA, fb, k0, ti.e * p.H + ti.m0);
-          } else if constexpr (VAR == V_GVEC) {
-            tma_2d(a_dst, &tmA, fb, ti.m0, ti.e * p.H + k0);
-            tma_2d(a_dst + 8192, &tmA, fb, ti.m0 + 64, ti.e * p.H + k0);
-          } else if constexpr (VAR == V_ROUTER) {
+          if constexpr (VarTraits<VAR>::router) {
+            mbar_expect_tx(fb, A_BYTES + ROUTER_BN * BK * 2);
             tma_2d(a_dst, &tmA, fb, k0, ti.m0);
-          } else if constexpr (VAR == V_DX) {
-            tma_2d(a_dst, &tmA, fb, ti.m0, ti.e * 2 * p.I + k0);
-            tma_2d(a_dst + 8192, &tmA, fb, ti.m0 + 64, ti.e * 2 * p.I + k0);
+            tma_2d(b_dst, &tmB, fb, k0 % p.H, ti.row0);  // x, once for each part of Wr
           } else {
-            tma_2d(a_dst, &tmA, fb, ti.m0, ti.row0 + k0);
-            tma_2d(a_dst + 8192, &tmA, fb, ti.m0 + 64, ti.row0 + k0);
-          }
-          if constexpr (VarTraits<VAR>::token_tiled) {
-            // the cluster's CTAs split the B boxes; each multicasts its box to all of them
-            const int nbox = ti.nrows > 128 ? 2 : 1;
-            for (int bx = 0; bx < nbox; ++bx) {
-              if (p.cl == 1) tma_2d(b_dst + bx * 16384, &tmB, fb, k0, ti.row0 + 128 * bx);
-              else if (bx % p.cl == (int)rank)
-                tma_2d_mc(b_dst + bx * 16384, &tmB, fb, k0, ti.row0 + 128 * bx, mc_mask);
+            mbar_expect_tx(fb, A_BYTES + nbox * B_BOX);
+            if constexpr (VAR == V_GATEUP) {
+              tma_4d(a_dst, &tmA, fb, k0, 0, ti.m0, ti.e);
+            } else if constexpr (VAR == V_DOWN) {
+              tma_2d(a_dst, &tmA, fb, k0, ti.e * p.H + ti.m0);
+            } else if constexpr (VAR == V_GVEC) {
+              tma_2d(a_dst, &tmA, fb, ti.m0, ti.e * p.H + k0);
+              tma_2d(a_dst + 8192, &tmA, fb, ti.m0 + 64, ti.e * p.H + k0);
+            } else {  // V_DX
+              tma_2d(a_dst, &tmA, fb, ti.m0, ti.e * 2 * p.I + k0);
+              tma_2d(a_dst + 8192, &tmA, fb, ti.m0 + 64, ti.e * 2 * p.I + k0);
             }
-          } else if constexpr (VarTraits<VAR>::router) {
-            tma_2d(b_dst, &tmB, fb, k0 % p.H, ti.n0);  // x repeated for each split of Wr
-          } else {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              if (p.cl == 1) tma_2d(b_dst + q * 8192, &tmB, fb, ti.n0 + 64 * q, ti.row0 + k0);
-              else if (q % p.cl == (int)rank)
-                tma_2d_mc(b_dst + q * 8192, &tmB, fb, ti.n0 + 64 * q, ti.row0 + k0, mc_mask);
-            }
+            // B: feature-major tokens, boxes of 64 tokens x 64 k (MN-major, 8 KB apart)
+            for (int q = 0; q < nbox; ++q) tma_2d(b_dst + q * B_BOX, &tmB, fb, ti.row0 + 64 * q, k0);
           }
           ++issued;
           if (++stage == STAGES) {
@@ -686,7 +501,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       // let every issued copy land before the CTA can exit
       for (int s = 0; s < STAGES && (uint32_t)s < issued; ++s) {
-        // the last fill of stage s was fill number (issued - 1 - ((issued - 1 - s) % STAGES))
         const uint32_t last = issued - 1 - ((issued - 1 - s) % STAGES);
         mbar_wait(full0 + 8 * s, (last / STAGES) & 1, abort_flag);
       }
@@ -698,21 +512,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      const uint32_t a_step = VarTraits<VAR>::a_mn ? 2048 : 32;
-      const uint32_t b_step = VarTraits<VAR>::b_mn ? 2048 : 32;
-      const uint32_t a_lbo = VarTraits<VAR>::a_mn ? 8192 : 16;
-      const uint32_t b_lbo = VarTraits<VAR>::b_mn ? 8192 : 16;
-      for (int t = cid; t < total && !failed; t += ncl) {
+      constexpr bool a_mn = VarTraits<VAR>::a_mn;
+      constexpr bool b_mn = !VarTraits<VAR>::router;
+      const uint32_t a_step = a_mn ? 2048 : 32, b_step = b_mn ? 2048 : 32;
+      const uint32_t a_lbo = a_mn ? 8192 : 16, b_lbo = b_mn ? B_BOX : 16;
+      for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
         const Tile ti = get_tile<VAR>(p, s_plan, s_off, t);
-        if (!ti.live) continue;
         if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag)) {
           failed = true;
           break;
         }
         tc_fence_after();
         const uint32_t d = tmem_base + acc * BN;
-        const int n_mma = (VarTraits<VAR>::token_tiled || VarTraits<VAR>::router) ? ti.nrows : BN;
-        const uint32_t idesc = idesc_bf16(n_mma, VarTraits<VAR>::a_mn, VarTraits<VAR>::b_mn);
+        const uint32_t idesc = idesc_bf16(ti.nrows, a_mn, b_mn);
         const int nkb = (ti.klen + BK - 1) / BK;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) {
@@ -722,14 +534,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after();
           const uint32_t a_base = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t b_base = a_base + A_BYTES;
-          const int ksteps = min(BK, ti.klen - kb * BK) / 16;
-          for (int ks = 0; ks < ksteps; ++ks) {
+#pragma unroll
+          for (int ks = 0; ks < BK / 16; ++ks) {
             const uint64_t ad = sdesc(a_base + ks * a_step, a_lbo, 1024);
             const uint64_t bd = sdesc(b_base + ks * b_step, b_lbo, 1024);
             umma_bf16(d, ad, bd, idesc, (kb | ks) != 0 ? 1u : 0u);
           }
-          if (p.cl > 1) umma_commit_mc(empty0 + 8 * stage, mc_mask);
-          else umma_commit(empty0 + 8 * stage);
+          umma_commit(empty0 + 8 * stage);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1;
@@ -757,26 +568,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int row = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
-    // this CTA's live tiles in order, with operand prefetches one and two tiles ahead
-    int t = next_live<VAR>(p, s_plan, s_off, cid, total);
-    int t1 = t < total ? next_live<VAR>(p, s_plan, s_off, t + ncl, total) : total;
-    Pre pre;
-    prefetch_b<VAR>(p, s_plan, s_off, t, total, row, half,
-                    prefetch_a<VAR>(p, s_plan, s_off, t, total, row), pre);
-    WgRange ra1 = prefetch_a<VAR>(p, s_plan, s_off, t1, total, row);
-    while (t < total) {
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile ti = get_tile<VAR>(p, s_plan, s_off, t);
-      const int t2 = t1 < total ? next_live<VAR>(p, s_plan, s_off, t1 + ncl, total) : total;
-      Pre pre1;
-      prefetch_b<VAR>(p, s_plan, s_off, t1, total, row, half, ra1, pre1);
-      const WgRange ra2 = prefetch_a<VAR>(p, s_plan, s_off, t2, total, row);
       int ok = 1;
       if (lane == 0) ok = mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      epilogue<VAR>(p, ti, tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN, row, lane, half,
-                    pre, s_stage + (warp - 2) * 32 * WG_PITCH);
+      epilogue<VAR>(p, ti, tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN, row, lane, half);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
@@ -784,15 +583,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         acc = 0;
         acc_phase ^= 1;
       }
-      t = t1;
-      t1 = t2;
-      pre = pre1;
-      ra1 = ra2;
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (p.cl > 1) cluster_sync();  // no peer multicasts into or arrives on this CTA any more
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
@@ -828,6 +622,25 @@ __global__ void __launch_bounds__(1024) token_plan_kernel(const int32_t* __restr
   const int32_t incl = v + (wid > 0 ? wsum[wid - 1] : 0);
   if (e < E) plan[e] = incl - n;
   if (e == E - 1) plan[E] = incl;
+}
+
+// Router weight split for the tensor-core logits: w = hi + mid + lo, each part bf16 and each
+// residual exact in fp32, so x . w is carried by three bf16 products with fp32 accumulation.
+__global__ void router_split_kernel(const float* __restrict__ wr, int64_t E, int64_t H,
+                                    __nv_bfloat16* __restrict__ wr3) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < E * H;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = i / H, k = i % H;
+    const float w = wr[i];
+    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(hi);
+    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(mid);
+    __nv_bfloat16* row = wr3 + e * 3 * H;
+    row[k] = hi;
+    row[H + k] = mid;
+    row[2 * H + k] = __float2bfloat16_rn(r2);
+  }
 }
 
 // ---------------------------------------------------------------------------- host side
@@ -872,54 +685,31 @@ bool map_gate_up_interleaved(CUtensorMap* m, const void* base, uint64_t E, uint6
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-constexpr const char* VAR_NAME[7] = {"tc_gate_up_swiglu", "tc_down_combine", "tc_gvec_swiglu_bwd",
-                                     "tc_dx", "tc_wgrad_gate_up", "tc_wgrad_down",
-                                     "tc_router_logits"};
+// feature-major token operand [rows = K features, cols = R_cap tokens], boxes of 64 x 64
+bool map_tokens(CUtensorMap* m, const void* base, uint64_t features, uint64_t R_cap) {
+  return map_2d(m, base, R_cap, features, 64, 64);
+}
+
+constexpr const char* VAR_NAME[5] = {"tc_gate_up_swiglu", "tc_down_combine", "tc_gvec_swiglu_bwd",
+                                     "tc_dx", "tc_router_logits"};
 
 template <int VAR>
-usaf_status launch(const CUtensorMap& a, const CUtensorMap& b, Params p, cudaStream_t st) {
+usaf_status launch(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStream_t st) {
   USAF_TRACE(VAR_NAME[VAR], st);
   static bool attr_done = false;
-  static int grid_for_cl[3] = {0, 0, 0};
   if (!attr_done) {
     if (cudaFuncSetAttribute(tc_gemm_kernel<VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              SMEM_BYTES) != cudaSuccess)
       return USAF_ERR_CUDA;
     attr_done = true;
   }
-  // clusters of two along M when the M tiles pair up (they share every B tile)
-  if (p.cl != 1 && p.cl != 2) p.cl = 1;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = p.cl;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
-  cfg.stream = st;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int& grid = grid_for_cl[p.cl];
-  if (grid == 0) {
-    int clusters = 0;
-    cfg.gridDim = dim3(device_sm_count());
-    if (cudaOccupancyMaxActiveClusters(&clusters, tc_gemm_kernel<VAR>, &cfg) != cudaSuccess ||
-        clusters <= 0) {
-      cudaGetLastError();
-      clusters = device_sm_count() / p.cl;
-    }
-    grid = clusters * p.cl;
-  }
-  cfg.gridDim = dim3(grid);
-  if (cudaLaunchKernelEx(&cfg, tc_gemm_kernel<VAR>, a, b, p) != cudaSuccess) return USAF_ERR_CUDA;
+  tc_gemm_kernel<VAR><<<device_sm_count(), NUM_THREADS, SMEM_BYTES, st>>>(a, b, p);
   USAF_CHECK_LAUNCH();
   return USAF_OK;
 }
 
 Params base_params(const MoeArgs& a) {
   Params p{};
-  p.cnt = a.rt.expert_count;
   p.off = a.rt.expert_offset;
   p.ptok = a.rt.perm_tok;
   p.pslot = a.rt.perm_slot;
@@ -928,16 +718,24 @@ Params base_params(const MoeArgs& a) {
   p.E = (int)a.s.E;
   p.H = (int)a.s.H;
   p.I = (int)a.s.I;
-  p.Ngu = a.s.E * 2 * a.s.I * a.s.H;
+  p.T = (int)a.s.T;
   p.R_cap = a.R_cap;
-  p.cl = 1;
   return p;
 }
 
 }  // namespace
 
-__global__ void router_split_kernel(const float* __restrict__ wr, int64_t E, int64_t H,
-                                    __nv_bfloat16* __restrict__ wr3);
+bool tc_shape_ok(const usaf_moe_shape& s) {
+  return s.H % 64 == 0 && s.I % 64 == 0 && s.E <= MAX_E && s.H <= (1 << 20) &&
+         s.I <= (1 << 20) && s.E * s.H < (int64_t(1) << 31) && s.E * 2 * s.I < (int64_t(1) << 31);
+}
+
+usaf_status tc_plan(const MoeArgs& a, cudaStream_t st) {
+  USAF_TRACE("tc_plan", st);
+  token_plan_kernel<<<1, 1024, 0, st>>>(a.rt.expert_offset, (int)a.s.E, a.plan);
+  USAF_CHECK_LAUNCH();
+  return USAF_OK;
+}
 
 usaf_status tc_router_logits(const usaf_moe_shape& s, const void* x, const float* wr,
                              void* wr3, float* logits, cudaStream_t st) {
@@ -961,125 +759,51 @@ usaf_status tc_router_logits(const usaf_moe_shape& s, const void* x, const float
   return launch<V_ROUTER>(ma, mb, p, st);
 }
 
-bool tc_shape_ok(const usaf_moe_shape& s) {
-  return s.H % 64 == 0 && s.I % 64 == 0 && s.E <= MAX_E && s.H <= (1 << 20) &&
-         s.I <= (1 << 20) && s.E * s.H < (int64_t(1) << 31) && s.E * 2 * s.I < (int64_t(1) << 31);
-}
-
-usaf_status tc_plan(const MoeArgs& a, cudaStream_t st) {
-  USAF_TRACE("tc_plan", st);
-  token_plan_kernel<<<1, 1024, 0, st>>>(a.rt.expert_offset, (int)a.s.E, a.plan);
-  USAF_CHECK_LAUNCH();
-  return USAF_OK;
-}
-
-usaf_status tc_fwd_gate_up(const MoeArgs& a, const void* x_perm, void* h, void* wa,
+usaf_status tc_fwd_gate_up(const MoeArgs& a, const void* xT, void* hT, void* waT,
                            cudaStream_t st) {
   CUtensorMap ma, mb;
   if (!map_gate_up_interleaved(&ma, a.w_gate_up, a.s.E, a.s.I, a.s.H) ||
-      !map_2d(&mb, x_perm, a.s.H, a.R_cap, 64, 128))
+      !map_tokens(&mb, xT, a.s.H, a.R_cap))
     return USAF_ERR_CUDA;
   Params p = base_params(a);
   p.MT = (int)(a.s.I / 64);
-  p.cl = 1;  // clusters of two (p.MT even) share B tiles by multicast; measured slower
-  p.h = static_cast<__nv_bfloat16*>(h);
-  p.wa = static_cast<__nv_bfloat16*>(wa);
+  p.h = static_cast<__nv_bfloat16*>(hT);
+  p.wa = static_cast<__nv_bfloat16*>(waT);
   return launch<V_GATEUP>(ma, mb, p, st);
 }
 
-usaf_status tc_fwd_down(const MoeArgs& a, const void* wa, float* y_acc, cudaStream_t st) {
+usaf_status tc_fwd_down(const MoeArgs& a, const void* waT, float* y_acc, cudaStream_t st) {
   CUtensorMap ma, mb;
-  if (!map_2d(&ma, a.w_down, a.s.I, a.s.E * a.s.H, 64, 128) ||
-      !map_2d(&mb, wa, a.s.I, a.R_cap, 64, 128))
+  if (!map_2d(&ma, a.w_down, a.s.I, a.s.E * a.s.H, 64, 128) || !map_tokens(&mb, waT, a.s.I, a.R_cap))
     return USAF_ERR_CUDA;
   Params p = base_params(a);
   p.MT = (int)ceil_div(a.s.H, BM);
-  p.cl = 1;  // clusters of two (p.MT even) share B tiles by multicast; measured slower
   p.acc_out = y_acc;
   return launch<V_DOWN>(ma, mb, p, st);
 }
 
-usaf_status tc_bwd_gvec(const MoeArgs& a, const void* dy_perm, const void* h, void* dh,
-                        float* dw, cudaStream_t st) {
+usaf_status tc_bwd_gvec(const MoeArgs& a, const void* dyT, const void* hT, void* dhT, float* dw,
+                        cudaStream_t st) {
   CUtensorMap ma, mb;
-  if (!map_2d(&ma, a.w_down, a.s.I, a.s.E * a.s.H, 64, 64) ||
-      !map_2d(&mb, dy_perm, a.s.H, a.R_cap, 64, 128))
+  if (!map_2d(&ma, a.w_down, a.s.I, a.s.E * a.s.H, 64, 64) || !map_tokens(&mb, dyT, a.s.H, a.R_cap))
     return USAF_ERR_CUDA;
   Params p = base_params(a);
   p.MT = (int)ceil_div(a.s.I, BM);
-  p.cl = 1;  // clusters of two (p.MT even) share B tiles by multicast; measured slower
-  p.hin = static_cast<const __nv_bfloat16*>(h);
-  p.dh = static_cast<__nv_bfloat16*>(dh);
+  p.hin = static_cast<const __nv_bfloat16*>(hT);
+  p.dh = static_cast<__nv_bfloat16*>(dhT);
   p.dw = dw;
   return launch<V_GVEC>(ma, mb, p, st);
 }
 
-usaf_status tc_bwd_dx(const MoeArgs& a, const void* dh, float* dx_acc, cudaStream_t st) {
+usaf_status tc_bwd_dx(const MoeArgs& a, const void* dhT, float* dx_acc, cudaStream_t st) {
   CUtensorMap ma, mb;
   if (!map_2d(&ma, a.w_gate_up, a.s.H, a.s.E * 2 * a.s.I, 64, 64) ||
-      !map_2d(&mb, dh, 2 * a.s.I, a.R_cap, 64, 128))
+      !map_tokens(&mb, dhT, 2 * a.s.I, a.R_cap))
     return USAF_ERR_CUDA;
   Params p = base_params(a);
   p.MT = (int)ceil_div(a.s.H, BM);
-  p.cl = 1;  // clusters of two (p.MT even) share B tiles by multicast; measured slower
   p.acc_out = dx_acc;
   return launch<V_DX>(ma, mb, p, st);
-}
-
-// Router weight split for the tensor-core logits: w = hi + mid + lo, each part bf16 and each
-// residual exact in fp32, so x . w is carried by three bf16 products with fp32 accumulation.
-__global__ void router_split_kernel(const float* __restrict__ wr, int64_t E, int64_t H,
-                                    __nv_bfloat16* __restrict__ wr3) {
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < E * H;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t e = i / H, k = i % H;
-    const float w = wr[i];
-    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
-    const float r1 = w - __bfloat162float(hi);
-    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-    const float r2 = r1 - __bfloat162float(mid);
-    __nv_bfloat16* row = wr3 + e * 3 * H;
-    row[k] = hi;
-    row[H + k] = mid;
-    row[2 * H + k] = __float2bfloat16_rn(r2);
-  }
-}
-
-__global__ void zero_f32_tc_kernel(float* __restrict__ p, int64_t n) {
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * blockDim.x)
-    p[i] = 0.f;
-}
-
-usaf_status tc_bwd_wgrad(const MoeArgs& a, const void* x_perm, const void* dy_perm, const void* dh,
-                         const void* wa, const int64_t* act_idx, int64_t K,
-                         const int32_t* tile_ptr, float* g_act, uint32_t* dev_status,
-                         cudaStream_t st) {
-  // experts without tokens run no tile, so their active entries must read 0
-  zero_f32_tc_kernel<<<grid_dim_for(K), 256, 0, st>>>(g_act, K);
-  USAF_CHECK_LAUNCH();
-  CUtensorMap ma, mb;
-  Params p = base_params(a);
-  p.act = act_idx;
-  p.tile_ptr = tile_ptr;
-  p.g_act = g_act;
-  p.status = dev_status;
-  // S9: gate_up entries, M = 2I weight rows, N = H columns, K = the expert's tokens
-  if (!map_2d(&ma, dh, 2 * a.s.I, a.R_cap, 64, 64) || !map_2d(&mb, x_perm, a.s.H, a.R_cap, 64, 64))
-    return USAF_ERR_CUDA;
-  p.MT = (int)(2 * a.s.I / BM);
-  p.cl = 1;  // clusters of two (p.MT even) share B tiles by multicast; measured slower
-  p.NT = (int)ceil_div(a.s.H, BN);
-  p.tp_base = 0;
-  USAF_TRY(launch<V_WG_GU>(ma, mb, p, st));
-  p.tp_base = a.s.E * 2 * a.s.I * (p.NT + 1);
-  // S10: down entries, M = H weight rows, N = I columns
-  if (!map_2d(&ma, dy_perm, a.s.H, a.R_cap, 64, 64) || !map_2d(&mb, wa, a.s.I, a.R_cap, 64, 64))
-    return USAF_ERR_CUDA;
-  p.MT = (int)ceil_div(a.s.H, BM);
-  p.cl = 1;  // clusters of two (p.MT even) share B tiles by multicast; measured slower
-  p.NT = (int)ceil_div(a.s.I, BN);
-  return launch<V_WG_D>(ma, mb, p, st);
 }
 
 }  // namespace usaf

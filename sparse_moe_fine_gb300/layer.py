@@ -35,9 +35,10 @@ class MoELayer:
         cap = B.routed_rows_capacity(self.s)
         self.rt = B.Routing.empty(self.s, d)
         self.logits = torch.empty(T, E, device=d)
-        self.x_perm = torch.empty(cap, H, dtype=self.dtype, device=d)
-        self.h = torch.empty(2 * I, cap, dtype=self.dtype, device=d)  # feature-major
-        self.wa = torch.empty(cap, I, dtype=self.dtype, device=d)
+        # per-row activations are feature-major: [features, R_cap]
+        self.x_perm = torch.empty(H, cap, dtype=self.dtype, device=d)
+        self.h = torch.empty(2 * I, cap, dtype=self.dtype, device=d)
+        self.wa = torch.empty(I, cap, dtype=self.dtype, device=d)
         self.y = torch.empty(T, H, dtype=self.dtype, device=d)
         self.dx = torch.empty(T, H, dtype=self.dtype, device=d)
         self.g_router = torch.empty(E, H, device=d)

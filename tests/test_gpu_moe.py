@@ -29,9 +29,9 @@ def run_layer(cfg, inp, act_idx, logits, dev, renorm=1, want_dx=True):
     rt = B.Routing.empty(s, dev)
     B.route_topk(s, x, wr, rt, logits_in=li, renorm=renorm)
     cap = B.routed_rows_capacity(s)
-    xp = torch.empty(cap, cfg.H, dtype=dt, device=dev)
+    xp = torch.empty(cfg.H, cap, dtype=dt, device=dev)
     h = torch.empty(2 * cfg.I, cap, dtype=dt, device=dev)
-    wa = torch.empty(cap, cfg.I, dtype=dt, device=dev)
+    wa = torch.empty(cfg.I, cap, dtype=dt, device=dev)
     y = torch.empty(cfg.T, cfg.H, dtype=dt, device=dev)
     B.moe_fwd(s, x, wgu, wd, rt, xp, h, wa, y)
     act = to_dev(act_idx, dev)
