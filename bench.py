@@ -66,19 +66,37 @@ def algorithmic(cfg):
     return fl, by
 
 
-def kernel_units(cfg):
-    """Per-launch algorithmic work of the tensor-core kernels: (bound, flops, bytes)."""
-    T, H, E, k, I = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I
+def kernel_units(cfg, sddmm_pairs=None):
+    """Per-launch algorithmic work of the main kernels: (flops, HBM bytes).
+
+    Tensor-core GEMMs count 2*M*N*K over the routed rows (no padding) and each operand read or
+    result written once; the gathers count one read of the source rows and one write of the
+    transposed rows; the masked expert gradient counts 2 flops per (active entry, routed token)
+    pair (`sddmm_pairs`, from the live routing) and one read of its four operands, the active
+    indices and the gradient it writes.
+    """
+    T, H, E, k, I, K = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.K
     R = T * k
     Wgu, Wd = E * 2 * I * H * 2, E * H * I * 2
+    pairs = sddmm_pairs if sddmm_pairs is not None else K * R / E
     return {
         "tc_gate_up_swiglu": (2 * R * 2 * I * H, Wgu + R * H * 2 + R * 2 * I * 2 + R * I * 2),
         "tc_down_combine": (2 * R * I * H, Wd + R * I * 2),
         "tc_gvec_swiglu_bwd": (2 * R * I * H, Wd + R * H * 2 + 2 * R * 2 * I * 2),
         "tc_dx": (2 * R * 2 * I * H, Wgu + R * 2 * I * 2),
-        "tc_wgrad_gate_up": (2 * R * 2 * I * H, R * 2 * I * 2 + R * H * 2),
-        "tc_wgrad_down": (2 * R * I * H, R * H * 2 + R * I * 2),
+        "gather_x": (0, T * H * 2 + R * H * 2),
+        "gather_dy": (0, T * H * 2 + R * H * 2),
+        "wgrad_sddmm": (2 * pairs, R * (2 * I + H + H + I) * 2 + K * (8 + 4)),
     }
+
+
+def sddmm_pairs(layer, cfg):
+    """Sum over active entries of the routed-token count of the entry's expert."""
+    cnt = layer.rt.expert_count.to(torch.int64)
+    a = layer.act
+    gu = a < cfg.N_gu
+    e = torch.where(gu, a // (2 * cfg.I * cfg.H), (a - cfg.N_gu) // (cfg.H * cfg.I))
+    return int(cnt[e].sum().item())
 
 
 class ClockSampler:
@@ -330,14 +348,14 @@ def run_steps(args, B, MoELayer, dist, ws, rank, local, dev, cfg, inp, x, dy, wg
     trace = B.trace_summary()
     B.trace_enable(False)
     tot = sum(t for _, _, t in trace)
-    units = kernel_units(cfg)
+    units = kernel_units(cfg, sddmm_pairs(layer, cfg))
     dominant = max(trace, key=lambda r: r[2])
     name, nl, tms = dominant
     avg_ms = tms / nl
     if name in units:
         fl, by = units[name]
         t_fl, t_by = fl / (tf_burst * 1e12), by / (hbm * 1e9)
-        if t_fl >= t_by:
+        if t_fl >= t_by and name.startswith("tc_"):
             roof = {"bound": "tensor", "achieved": fl / (avg_ms / 1e3) / 1e12, "peak": tf_burst,
                     "unit": "TFLOP/s"}
         else:
@@ -358,7 +376,7 @@ def run_steps(args, B, MoELayer, dist, ws, rank, local, dev, cfg, inp, x, dy, wg
         e2e_ms = e2e_time(args, layer, x, dy, e0, e1, stream, dist, dev)
     nbytes = x.numel() * 2
     line = make_line(args, cfg, ws, ms, value, step_roof_ms, fl, by, roof, trace, tot,
-                     importance, e2e_ms, nbytes, launches, clk)
+                     importance, e2e_ms, nbytes, launches, clk, units, hbm, tf_burst)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         tokens = args.cpu_tokens
         a = act.cpu().numpy()
@@ -393,8 +411,21 @@ def e2e_time(args, layer, x, dy, e0, e1, stream, dist, dev):
     return max_over_ranks(dist, e0.elapsed_time(e1) / args.steps, dev)
 
 
+def kernel_entry(n, l, t, tot, units, hbm, tf_burst):
+    e = {"name": n, "launches": l, "ms": t, "share": t / tot}
+    if n in units:
+        fl, by = units[n]
+        avg_s = t / l / 1e3
+        e["gbs"] = by / avg_s / 1e9
+        e["hbm_frac"] = e["gbs"] / hbm
+        if n.startswith("tc_"):
+            e["tflops"] = fl / avg_s / 1e12
+            e["tensor_frac"] = e["tflops"] / tf_burst
+    return e
+
+
 def make_line(args, cfg, ws, ms, value, step_roof_ms, fl, by, roof, trace, tot, importance,
-              e2e_ms, nbytes, launches, clk):
+              e2e_ms, nbytes, launches, clk, units, hbm, tf_burst):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -407,7 +438,7 @@ def make_line(args, cfg, ws, ms, value, step_roof_ms, fl, by, roof, trace, tot, 
         "step_roofline": {"ms": step_roof_ms, "frac": step_roof_ms / ms,
                           "algorithmic_gflop": fl / 1e9, "algorithmic_gb": by / 1e9},
         "roofline": roof,
-        "kernels": [{"name": n, "launches": l, "ms": t, "share": t / tot} for n, l, t in trace],
+        "kernels": [kernel_entry(n, l, t, tot, units, hbm, tf_burst) for n, l, t in trace],
         "importance_pass": importance,
         "e2e": {"value": ws * cfg.T / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": 2 * nbytes, "d2h_bytes_per_step": 2 * nbytes,

@@ -118,7 +118,7 @@ usaf_status usaf_route_topk(const usaf_moe_shape* shape, const void* x, usaf_dty
  * be given (the logits are never kept in scratch).
  * Scratch: a fixed device array of USAF_NOALLOC_SCRATCH_BYTES inside the library, which every
  * GPU that loads the library holds until the process exits. It needs
- * ceil(T*k/1024)*E*4 bytes (rounded up to 256) + 6*E*H bytes; a layer needing more is refused
+ * ceil(T*k/256)*E*4 bytes (rounded up to 256) + 6*E*H bytes; a layer needing more is refused
  * with USAF_ERR_WORKSPACE before anything is enqueued. The first call on each device looks up
  * the array's device address (cudaGetSymbolAddress) with that device current; make that first
  * call before any stream capture. All calls share the one array and leave their scratch in it;
@@ -148,7 +148,9 @@ usaf_status usaf_route_topk_noalloc(const usaf_moe_shape* shape, const void* x,
  *                feature j (gate for j < I, up for j >= I) of permuted row `row`
  *   wa_save      [I,R_cap]  out: w * A per permuted row, feature-major (0 in padding rows)
  *   y            [T,H]      out
- * Errors: INVALID_ARG, UNSUPPORTED (bf16 shape limits), WORKSPACE, CUDA.
+ * Errors: INVALID_ARG, UNSUPPORTED (bf16 shape limits; also any dtype with
+ * max(2I,H) * R_cap >= 2^31 * (16 / element size), the range of the 32-bit vector indices into the
+ * feature-major rows), WORKSPACE, CUDA.
  * ------------------------------------------------------------------------------------------- */
 size_t usaf_moe_fwd_workspace_size(const usaf_moe_shape* shape, usaf_dtype dtype);
 usaf_status usaf_moe_fwd(const usaf_moe_shape* shape, usaf_dtype dtype, const void* x,

@@ -197,6 +197,10 @@ static usaf_status fill_args(MoeArgs& a, const usaf_moe_shape* s, usaf_dtype dt,
   if (!shape_ok(s) || !dtype_ok(dt) || !routing_ok(rt) || !x || !wgu || !wd)
     return USAF_ERR_INVALID_ARG;
   if (dt == USAF_BF16 && !tc_shape_ok(*s)) return USAF_ERR_UNSUPPORTED;
+  // feature-major rows are addressed by 32-bit 16-byte-vector indices
+  const int64_t vw = dt == USAF_BF16 ? 8 : 4;
+  if (std::max<int64_t>(2 * s->I, s->H) * usaf_routed_rows_capacity(s) / vw >= INT32_MAX)
+    return USAF_ERR_UNSUPPORTED;
   a.s = *s;
   a.dt = dt;
   a.R_cap = usaf_routed_rows_capacity(s);

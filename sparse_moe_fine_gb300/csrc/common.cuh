@@ -81,6 +81,22 @@ __device__ __forceinline__ void flag_status_warp(uint32_t* st, bool cond, uint32
 
 __device__ __forceinline__ bool finite_f(float v) { return isfinite(v); }
 
+// Butterfly transpose-reduce across a warp: lane l returns the warp-wide sum of x[l] (31 shuffles
+// for 32 sums). x is clobbered.
+__device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int j = 0; j < off; ++j) {
+      const float send = upper ? x[j] : x[j + off];
+      const float keep = upper ? x[j + off] : x[j];
+      x[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  return x[0];
+}
+
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 __device__ __forceinline__ float silu_grad_f(float z) {
   float s = 1.0f / (1.0f + expf(-z));

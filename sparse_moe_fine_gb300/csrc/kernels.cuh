@@ -31,7 +31,6 @@ struct BwdWs {
   void* dh;           // dh^T [2I, R_cap] of dtype
   float* dx_acc;      // [T,H]
   float* gvec;        // [R_cap, I] (fp32 path only)
-  int32_t* row_ptr;   // [E*2I + E*H + 1] first active entry of each weight row
   int32_t* plan;      // [E+1] prefix of token tiles per expert (tensor-core path)
   void* dy_perm;      // dy^T [H, R_cap]: dy in permuted order, feature-major
 };

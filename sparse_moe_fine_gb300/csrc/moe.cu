@@ -219,22 +219,25 @@ __global__ void swiglu_bwd_rows_kernel(const float* __restrict__ gvec, const T* 
 // ================================================================================================
 
 // Gather-transpose: xT[h, row] = x[perm_tok[row], h] for routed rows, 0 for padding and tail
-// rows. A block moves a 32-row x 64-feature tile through shared memory with 16-byte accesses.
+// rows. A block moves a 128-row x 64-feature tile through shared memory with 16-byte accesses, so
+// each feature row of xT receives 256 contiguous bytes (bf16).
+constexpr int GT_ROWS = 128;
 template <typename T>
 __global__ void __launch_bounds__(256) gather_transpose_kernel(
     const T* __restrict__ x, const int32_t* __restrict__ ptok, const int32_t* __restrict__ pslot,
     const int32_t* __restrict__ off_end, int64_t R_cap, int H, T* __restrict__ xT) {
   constexpr int VW = 16 / sizeof(T);  // elements per 16-byte vector
-  __shared__ T tile[64][32 + VW];
-  const int64_t r0 = (int64_t)blockIdx.x * 32;
+  // feature f's row of the tile is rotated by (f / VW) * VW columns: the column writes of the
+  // load phase then fall in distinct banks, and the 16-byte reads of the store phase stay aligned
+  __shared__ __align__(16) T tile[64 * GT_ROWS];
+  const int64_t r0 = (int64_t)blockIdx.x * GT_ROWS;
   const int h0 = blockIdx.y * 64;
   const int64_t end = *off_end;
   const bool vec = (H % VW) == 0;
-  // load: 32 rows x (64 / VW) vectors
-  for (int v = threadIdx.x; v < 32 * (64 / VW); v += blockDim.x) {
+  for (int v = threadIdx.x; v < GT_ROWS * (64 / VW); v += blockDim.x) {
     const int r = v / (64 / VW), f = (v % (64 / VW)) * VW;
     const int64_t row = r0 + r;
-    const bool live = row < end && pslot[row] >= 0;
+    const bool live = row < R_cap && row < end && pslot[row] >= 0;
     const int64_t src = live ? (int64_t)ptok[row] * H : 0;
     alignas(16) T buf[VW];
     if (vec && h0 + f + VW <= H) {
@@ -247,18 +250,17 @@ __global__ void __launch_bounds__(256) gather_transpose_kernel(
         buf[q] = (live && h0 + f + q < H) ? x[src + h0 + f + q] : from_f32<T>(0.f);
     }
 #pragma unroll
-    for (int q = 0; q < VW; ++q) tile[f + q][r] = buf[q];
+    for (int q = 0; q < VW; ++q) {
+      const int ff = f + q;
+      tile[ff * GT_ROWS + (r + (ff / VW) * VW) % GT_ROWS] = buf[q];
+    }
   }
   __syncthreads();
-  // store: 64 features x (32 / VW) vectors of consecutive rows
-  for (int v = threadIdx.x; v < 64 * (32 / VW); v += blockDim.x) {
-    const int f = v / (32 / VW), r = (v % (32 / VW)) * VW;
-    if (h0 + f >= H) continue;
-    alignas(16) T buf[VW];
-#pragma unroll
-    for (int q = 0; q < VW; ++q) buf[q] = tile[f][r + q];
+  for (int v = threadIdx.x; v < 64 * (GT_ROWS / VW); v += blockDim.x) {
+    const int f = v / (GT_ROWS / VW), r = (v % (GT_ROWS / VW)) * VW;
+    if (h0 + f >= H || r0 + r >= R_cap) continue;
     *reinterpret_cast<uint4*>(xT + (int64_t)(h0 + f) * R_cap + r0 + r) =
-        *reinterpret_cast<const uint4*>(buf);
+        *reinterpret_cast<const uint4*>(&tile[f * GT_ROWS + (r + (f / VW) * VW) % GT_ROWS]);
   }
 }
 
@@ -283,88 +285,95 @@ __device__ __forceinline__ float dot_vec<float>(const uint4& a, const uint4& b) 
                         __uint_as_float(a.w) * __uint_as_float(b.w))));
 }
 
-// S9/S10 masked weight gradient (sampled dense-dense product). One warp per weight row; its four
-// groups of eight lanes take the row's active entries four at a time, each group a dot product
-// over the expert's tokens (16-byte vectors, then a 3-step shuffle reduction):
-//   gate_up row (e, j), column c:  g = sum_t dh^T[j, t] * x^T[c, t]
-//   down row (e, h), column c:     g = sum_t dy^T[h, t] * (wA)^T[c, t]
+// S9/S10 masked weight gradient as a sampled dense-dense product on CUDA cores. A warp takes 32
+// consecutive active entries at a time, and lane l decodes entry l into the two feature-major rows
+// whose dot product over the expert's routed tokens is that entry's gradient:
+//   gate_up entry (e, j, c):  g = sum_t dh^T[j, o_e + t] * x^T[c, o_e + t]
+//   down entry (e, h, c):     g = sum_t dy^T[h, o_e + t] * (wA)^T[c, o_e + t]
+// The warp then walks the 32 entries together, lane l reading 16-byte vector l of both rows with
+// the loads of four entries in flight before their FMAs; a butterfly transpose of the 32 per-lane
+// partial sums leaves entry l's total in lane l, stored with one coalesced write. Experts with more
+// tokens than 32 vectors take further passes over the batch.
+constexpr int SD_WARPS = 8;
 template <typename T>
-__global__ void __launch_bounds__(256) sddmm_kernel(
-    const int64_t* __restrict__ act, const int32_t* __restrict__ rp, int64_t n_rows,
-    int64_t n_gu_rows, const int32_t* __restrict__ cnt, const int32_t* __restrict__ off, int H,
-    int I, int64_t Ngu, int64_t rcap, const T* __restrict__ dhT, const T* __restrict__ xT,
-    const T* __restrict__ dyT, const T* __restrict__ waT, float* __restrict__ g_act,
-    uint32_t* dev_status) {
+__global__ void __launch_bounds__(SD_WARPS * 32, 2) sddmm_kernel(
+    const int64_t* __restrict__ act, int64_t K, const int32_t* __restrict__ cnt,
+    const int32_t* __restrict__ off, int H, int I, int64_t Ngu, int64_t rcap,
+    const T* __restrict__ dhT, const T* __restrict__ xT, const T* __restrict__ dyT,
+    const T* __restrict__ waT, float* __restrict__ g_act, uint32_t* dev_status) {
   constexpr int VW = 16 / sizeof(T);
-  const int lane = threadIdx.x & 31, grp = lane >> 3, gl = lane & 7;
-  const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  constexpr int U = 4;  // entries whose loads are in flight together
+  constexpr uint32_t GU = 0x80000000u;
+  __shared__ int4 meta[SD_WARPS][32];  // per entry: a-row vector, b-row vector, vectors | GU
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int64_t stride = (int64_t)gridDim.x * SD_WARPS * 32;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
   bool bad = false;
-  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < n_rows;
-       r += warps) {
-    const int64_t a0 = rp[r], a1 = rp[r + 1];
-    if (a0 >= a1) continue;
-    const T* av;
-    const T* bbase;
-    int64_t base;
-    int e;
-    if (r < n_gu_rows) {
-      e = (int)(r / (2 * I));
-      av = dhT + (r % (2 * I)) * rcap;
-      bbase = xT;
-      base = r * H;
-    } else {
-      const int64_t rd = r - n_gu_rows;
-      e = (int)(rd / H);
-      av = dyT + (rd % H) * rcap;
-      bbase = waT;
-      base = Ngu + rd * I;
-    }
-    const int o = off[e];
-    const int n = (cnt[e] + VW - 1) / VW * VW;  // padding rows hold zeros in every operand
-    av += o;
-    for (int64_t q0 = a0; q0 < a1; q0 += 4) {
-      const int64_t q = q0 + grp;
-      float acc = 0.f;
-      if (q < a1) {
-        const T* bv = bbase + (act[q] - base) * rcap + o;
-        for (int t = gl * VW; t < n; t += 8 * VW)
-          acc += dot_vec<T>(__ldg(reinterpret_cast<const uint4*>(av + t)),
-                            __ldg(reinterpret_cast<const uint4*>(bv + t)));
+  for (int64_t b0 = ((int64_t)blockIdx.x * SD_WARPS + wid) * 32; b0 < K; b0 += stride) {
+    const int64_t q = b0 + lane;
+    int4 md = make_int4(0, 0, 0, 0);
+    if (q < K) {
+      const int64_t f = act[q];
+      int64_t arow, col;
+      int e;
+      uint32_t gu = 0;
+      if (f < Ngu) {
+        const int64_t row = f / H;
+        col = f - row * H;
+        e = (int)(row / (2 * I));
+        arow = row - (int64_t)e * 2 * I;
+        gu = GU;
+      } else {
+        const int64_t row = (f - Ngu) / I;
+        col = (f - Ngu) - row * I;
+        e = (int)(row / H);
+        arow = row - (int64_t)e * H;
       }
-      acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      if (gl == 0 && q < a1) {
-        g_act[q] = acc;
-        bad |= !finite_f(acc);
+      const int64_t o = off[e];
+      md.x = (int)((arow * rcap + o) / VW);
+      md.y = (int)((col * rcap + o) / VW);
+      md.z = (int)(((uint32_t)(cnt[e] + VW - 1) / VW) | gu);
+    }
+    meta[wid][lane] = md;
+    const unsigned passes = __reduce_max_sync(
+        0xffffffffu, (((uint32_t)md.z & ~GU) + 31u) / 32u);
+    __syncwarp();
+    float part[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) part[i] = 0.f;
+#pragma unroll
+    for (int i0 = 0; i0 < 32; i0 += U) {
+      const uint4* A[U];
+      const uint4* Bm[U];
+      uint32_t nv[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int4 m = meta[wid][i0 + u];
+        const uint32_t z = (uint32_t)m.z;
+        A[u] = reinterpret_cast<const uint4*>((z & GU) ? dhT : dyT) + (uint32_t)m.x;
+        Bm[u] = reinterpret_cast<const uint4*>((z & GU) ? xT : waT) + (uint32_t)m.y;
+        nv[u] = z & ~GU;
+      }
+      for (unsigned p = 0; p < passes; ++p) {
+        const uint32_t v = p * 32u + (uint32_t)lane;
+        uint4 av[U], bv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          av[u] = v < nv[u] ? __ldg(A[u] + v) : zero;
+          bv[u] = v < nv[u] ? __ldg(Bm[u] + v) : zero;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) part[i0 + u] += dot_vec<T>(av[u], bv[u]);
       }
     }
+    const float g = transpose_reduce32(part, lane);
+    if (q < K) {
+      g_act[q] = g;
+      bad |= !finite_f(g);
+    }
+    __syncwarp();  // the next batch rewrites meta
   }
   flag_status_warp(dev_status, bad, USAF_DEV_NONFINITE);
-}
-
-// First active entry of every weight row (gate_up rows, then down rows); entry n_rows = K. The
-// actives are sorted, so their rows are too: active a fills the entries between its
-// predecessor's row and its own, and the entries after the last active's row get K.
-__device__ __forceinline__ int64_t weight_row(int64_t f, int64_t Ngu, int64_t n_gu_rows, int H,
-                                              int I) {
-  return f < Ngu ? f / H : n_gu_rows + (f - Ngu) / I;
-}
-
-__global__ void row_ptr_kernel(const int64_t* __restrict__ act, int64_t K, int64_t n_gu_rows,
-                               int64_t n_rows, int H, int I, int64_t Ngu,
-                               int32_t* __restrict__ rp) {
-  const int64_t tail = K > 0 ? weight_row(act[K - 1], Ngu, n_gu_rows, H, I) + 1 : 0;
-  const int64_t n = K > n_rows + 1 ? K : n_rows + 1;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    if (i < K) {
-      const int64_t pos = weight_row(act[i], Ngu, n_gu_rows, H, I);
-      const int64_t prev = i > 0 ? weight_row(act[i - 1], Ngu, n_gu_rows, H, I) : -1;
-      for (int64_t x = prev + 1; x <= pos; ++x) rp[x] = (int32_t)i;
-    }
-    if (i >= tail && i <= n_rows) rp[i] = (int32_t)K;
-  }
 }
 
 // g_router[e, h] = sum over the rows routed to e of dl[row] * x^T[h, row] (renormalised routing):
@@ -573,14 +582,13 @@ void bwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, int64_t K, Carver& c,
   w.dh = c.take<char>(R_cap * 2 * s.I * (int64_t)es);
   w.dx_acc = c.take<float>(s.T * s.H);
   w.gvec = dt == USAF_F32 ? c.take<float>(R_cap * s.I) : nullptr;
-  w.row_ptr = c.take<int32_t>(s.E * 2 * s.I + s.E * s.H + 1);
   w.plan = dt == USAF_BF16 ? c.take<int32_t>(s.E + 1) : nullptr;
   w.dy_perm = c.take<char>(R_cap * s.H * (int64_t)es);
 }
 
 template <typename T>
 static usaf_status gather_t(const MoeArgs& a, const T* src, T* dstT, cudaStream_t st) {
-  const dim3 grid((unsigned)ceil_div(a.R_cap, 32), (unsigned)ceil_div(a.s.H, 64));
+  const dim3 grid((unsigned)ceil_div(a.R_cap, GT_ROWS), (unsigned)ceil_div(a.s.H, 64));
   gather_transpose_kernel<T><<<grid, 256, 0, st>>>(src, a.rt.perm_tok, a.rt.perm_slot,
                                                    a.rt.expert_offset + a.s.E, a.R_cap,
                                                    (int)a.s.H, dstT);
@@ -728,17 +736,11 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
   }
   // S9, S10: expert weight gradients at the active set
   if (K > 0) {
-    const int64_t n_gu_rows = s.E * 2 * s.I, n_rows = n_gu_rows + s.E * s.H;
-    {
-      USAF_TRACE("wgrad_row_ptr", st);
-      row_ptr_kernel<<<grid_dim_for(std::max<int64_t>(K, n_rows + 1)), 256, 0, st>>>(
-          act_idx, K, n_gu_rows, n_rows, H, I, Ngu, w.row_ptr);
-      USAF_CHECK_LAUNCH();
-    }
     USAF_TRACE("wgrad_sddmm", st);
-    const unsigned blocks = (unsigned)std::min<int64_t>(ceil_div(n_rows, 8), device_sm_count() * 16);
-    sddmm_kernel<T><<<blocks, 256, 0, st>>>(act_idx, w.row_ptr, n_rows, n_gu_rows, cnt, off, H, I,
-                                            Ngu, a.R_cap, dhT, xT, dyT, waT, g_act, dev_status);
+    const unsigned blocks = (unsigned)std::min<int64_t>(ceil_div(K, SD_WARPS * 32),
+                                                        device_sm_count() * 2);
+    sddmm_kernel<T><<<blocks, SD_WARPS * 32, 0, st>>>(act_idx, K, cnt, off, H, I, Ngu, a.R_cap,
+                                                      dhT, xT, dyT, waT, g_act, dev_status);
     USAF_CHECK_LAUNCH();
   }
   return USAF_OK;

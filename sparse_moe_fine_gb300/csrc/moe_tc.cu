@@ -228,20 +228,6 @@ __device__ __forceinline__ int total_tiles(const Params& p, const int32_t* s_pla
 // ---------------------------------------------------------------------------- epilogues
 // Column sums of a 32x32 block held one column per register: after 31 shuffles lane l holds the
 // sum over the warp's lanes of column l.
-__device__ __forceinline__ float transpose_reduce32(float (&x)[32], int lane) {
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    const bool upper = (lane & off) != 0;
-#pragma unroll
-    for (int j = 0; j < off; ++j) {
-      const float send = upper ? x[j] : x[j + off];
-      const float keep = upper ? x[j + off] : x[j];
-      x[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-    }
-  }
-  return x[0];
-}
-
 __device__ __forceinline__ float sigmoid_fast(float z) { return __fdividef(1.f, 1.f + __expf(-z)); }
 
 // 16 bytes = 8 bf16 of a feature-major row; `cnt` of the 8 tokens are valid (0 elsewhere)
