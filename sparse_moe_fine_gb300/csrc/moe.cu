@@ -264,12 +264,12 @@ __global__ void __launch_bounds__(256) gather_transpose_kernel(
   }
 }
 
+// s + the dot product of two 16-byte vectors (8 bf16 or 4 fp32), accumulated in fp32
 template <typename T>
-__device__ __forceinline__ float dot_vec(const uint4& a, const uint4& b);
+__device__ __forceinline__ float dot_acc(const uint4& a, const uint4& b, float s);
 template <>
-__device__ __forceinline__ float dot_vec<__nv_bfloat16>(const uint4& a, const uint4& b) {
+__device__ __forceinline__ float dot_acc<__nv_bfloat16>(const uint4& a, const uint4& b, float s) {
   const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-  float s = 0.f;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     s = fmaf(__uint_as_float(aw[q] << 16), __uint_as_float(bw[q] << 16), s);
@@ -278,11 +278,11 @@ __device__ __forceinline__ float dot_vec<__nv_bfloat16>(const uint4& a, const ui
   return s;
 }
 template <>
-__device__ __forceinline__ float dot_vec<float>(const uint4& a, const uint4& b) {
-  return fmaf(__uint_as_float(a.x), __uint_as_float(b.x),
-              fmaf(__uint_as_float(a.y), __uint_as_float(b.y),
-                   fmaf(__uint_as_float(a.z), __uint_as_float(b.z),
-                        __uint_as_float(a.w) * __uint_as_float(b.w))));
+__device__ __forceinline__ float dot_acc<float>(const uint4& a, const uint4& b, float s) {
+  s = fmaf(__uint_as_float(a.x), __uint_as_float(b.x), s);
+  s = fmaf(__uint_as_float(a.y), __uint_as_float(b.y), s);
+  s = fmaf(__uint_as_float(a.z), __uint_as_float(b.z), s);
+  return fmaf(__uint_as_float(a.w), __uint_as_float(b.w), s);
 }
 
 // S9/S10 masked weight gradient as a sampled dense-dense product on CUDA cores. A warp takes 32
@@ -290,10 +290,12 @@ __device__ __forceinline__ float dot_vec<float>(const uint4& a, const uint4& b) 
 // whose dot product over the expert's routed tokens is that entry's gradient:
 //   gate_up entry (e, j, c):  g = sum_t dh^T[j, o_e + t] * x^T[c, o_e + t]
 //   down entry (e, h, c):     g = sum_t dy^T[h, o_e + t] * (wA)^T[c, o_e + t]
-// The warp then walks the 32 entries together, lane l reading 16-byte vector l of both rows with
-// the loads of four entries in flight before their FMAs; a butterfly transpose of the 32 per-lane
-// partial sums leaves entry l's total in lane l, stored with one coalesced write. Experts with more
-// tokens than 32 vectors take further passes over the batch.
+// Full passes: the warp walks the 32 entries together, lane l reading 16-byte vector l of both
+// rows (a pass covers 32 vectors, 256 bf16 tokens), the loads of four entries in flight before
+// their FMAs. The number of full passes is the batch's smallest vector count rounded to the
+// nearest multiple of 32; vectors beyond them are taken by groups of eight lanes, four entries at
+// a time. A butterfly transpose of the 32 per-lane partial sums then leaves entry l's total in
+// lane l for one coalesced store.
 constexpr int SD_WARPS = 8;
 template <typename T>
 __global__ void __launch_bounds__(SD_WARPS * 32, 2) sddmm_kernel(
@@ -302,10 +304,11 @@ __global__ void __launch_bounds__(SD_WARPS * 32, 2) sddmm_kernel(
     const T* __restrict__ dhT, const T* __restrict__ xT, const T* __restrict__ dyT,
     const T* __restrict__ waT, float* __restrict__ g_act, uint32_t* dev_status) {
   constexpr int VW = 16 / sizeof(T);
-  constexpr int U = 4;  // entries whose loads are in flight together
+  constexpr int U = 4;   // entries whose loads are in flight together in a full pass
+  constexpr int RU = 2;  // rounds whose first loads are in flight together after them
   constexpr uint32_t GU = 0x80000000u;
   __shared__ int4 meta[SD_WARPS][32];  // per entry: a-row vector, b-row vector, vectors | GU
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, grp = lane >> 3, gl = lane & 7;
   const int64_t stride = (int64_t)gridDim.x * SD_WARPS * 32;
   const uint4 zero = make_uint4(0, 0, 0, 0);
   bool bad = false;
@@ -335,35 +338,67 @@ __global__ void __launch_bounds__(SD_WARPS * 32, 2) sddmm_kernel(
       md.z = (int)(((uint32_t)(cnt[e] + VW - 1) / VW) | gu);
     }
     meta[wid][lane] = md;
-    const unsigned passes = __reduce_max_sync(
-        0xffffffffu, (((uint32_t)md.z & ~GU) + 31u) / 32u);
+    const uint32_t nvl = (uint32_t)md.z & ~GU;
+    const uint32_t passes = (__reduce_min_sync(0xffffffffu, nvl) + 16u) / 32u;
+    const uint32_t vrest = 32u * passes;  // first vector left to the eight-lane groups
+    const bool rest = __any_sync(0xffffffffu, nvl > vrest);
     __syncwarp();
     float part[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) part[i] = 0.f;
+    if (passes > 0) {
 #pragma unroll
-    for (int i0 = 0; i0 < 32; i0 += U) {
-      const uint4* A[U];
-      const uint4* Bm[U];
-      uint32_t nv[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int4 m = meta[wid][i0 + u];
-        const uint32_t z = (uint32_t)m.z;
-        A[u] = reinterpret_cast<const uint4*>((z & GU) ? dhT : dyT) + (uint32_t)m.x;
-        Bm[u] = reinterpret_cast<const uint4*>((z & GU) ? xT : waT) + (uint32_t)m.y;
-        nv[u] = z & ~GU;
-      }
-      for (unsigned p = 0; p < passes; ++p) {
-        const uint32_t v = p * 32u + (uint32_t)lane;
-        uint4 av[U], bv[U];
+      for (int i0 = 0; i0 < 32; i0 += U) {
+        const uint4* A[U];
+        const uint4* Bm[U];
+        uint32_t nv[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-          av[u] = v < nv[u] ? __ldg(A[u] + v) : zero;
-          bv[u] = v < nv[u] ? __ldg(Bm[u] + v) : zero;
+          const int4 m = meta[wid][i0 + u];
+          const uint32_t z = (uint32_t)m.z;
+          A[u] = reinterpret_cast<const uint4*>((z & GU) ? dhT : dyT) + (uint32_t)m.x;
+          Bm[u] = reinterpret_cast<const uint4*>((z & GU) ? xT : waT) + (uint32_t)m.y;
+          nv[u] = z & ~GU;
+        }
+        for (uint32_t p = 0; p < passes; ++p) {
+          const uint32_t v = p * 32u + (uint32_t)lane;
+          uint4 av[U], bv[U];
+#pragma unroll
+          for (int u = 0; u < U; ++u) {
+            av[u] = v < nv[u] ? __ldg(A[u] + v) : zero;
+            bv[u] = v < nv[u] ? __ldg(Bm[u] + v) : zero;
+          }
+#pragma unroll
+          for (int u = 0; u < U; ++u) part[i0 + u] = dot_acc<T>(av[u], bv[u], part[i0 + u]);
+        }
+      }
+    }
+    if (rest) {
+      // entry 4r + grp in round r; the first vector of every round is loaded up front
+#pragma unroll
+      for (int h = 0; h < 8; h += RU) {
+        const uint4* A[RU];
+        const uint4* Bm[RU];
+        uint32_t nv[RU];
+        uint4 av[RU], bv[RU];
+        const uint32_t v0 = vrest + (uint32_t)gl;
+#pragma unroll
+        for (int r = 0; r < RU; ++r) {
+          const int4 m = meta[wid][4 * (h + r) + grp];
+          const uint32_t z = (uint32_t)m.z;
+          A[r] = reinterpret_cast<const uint4*>((z & GU) ? dhT : dyT) + (uint32_t)m.x;
+          Bm[r] = reinterpret_cast<const uint4*>((z & GU) ? xT : waT) + (uint32_t)m.y;
+          nv[r] = z & ~GU;
+          av[r] = v0 < nv[r] ? __ldg(A[r] + v0) : zero;
+          bv[r] = v0 < nv[r] ? __ldg(Bm[r] + v0) : zero;
         }
 #pragma unroll
-        for (int u = 0; u < U; ++u) part[i0 + u] += dot_vec<T>(av[u], bv[u]);
+        for (int r = 0; r < RU; ++r) {
+          float s = dot_acc<T>(av[r], bv[r], 0.f);
+          for (uint32_t v = v0 + 8; v < nv[r]; v += 8) s = dot_acc<T>(__ldg(A[r] + v), __ldg(Bm[r] + v), s);
+#pragma unroll
+          for (int g = 0; g < 4; ++g) part[4 * (h + r) + g] += grp == g ? s : 0.f;
+        }
       }
     }
     const float g = transpose_reduce32(part, lane);

@@ -164,10 +164,19 @@ __global__ void __launch_bounds__(1024) perm_scan_kernel(int32_t* __restrict__ c
   const int e = threadIdx.x;
   int32_t total = 0;
   if (e < E) {
-    for (int b = 0; b < nchunks; ++b) {
-      int32_t c = chunk_hist[(int64_t)b * E + e];
-      chunk_hist[(int64_t)b * E + e] = total;  // exclusive base of chunk b within expert e
-      total += c;
+    // 16 chunks' counts are loaded before any base is written back, so the column costs
+    // nchunks / 16 load latencies instead of nchunks
+    constexpr int UNR = 16;
+    for (int b0 = 0; b0 < nchunks; b0 += UNR) {
+      int32_t c[UNR];
+#pragma unroll
+      for (int j = 0; j < UNR; ++j)
+        c[j] = b0 + j < nchunks ? chunk_hist[(int64_t)(b0 + j) * E + e] : 0;
+#pragma unroll
+      for (int j = 0; j < UNR; ++j) {
+        if (b0 + j < nchunks) chunk_hist[(int64_t)(b0 + j) * E + e] = total;  // exclusive base
+        total += c[j];
+      }
     }
     expert_count[e] = total;
   }

@@ -122,6 +122,23 @@ def test_bf16_empty_and_crowded_experts():
     assert (got["g_act"][e_ == 5] == 0).all()
 
 
+def test_bf16_skewed_routing():
+    """Zipf-skewed expert loads (a few experts far above one 256-token tile, many below it, four
+    never routed): the masked gradient then mixes full passes and remainders within one batch of
+    active entries, and token tiles of every size occur."""
+    dev = device()
+    cfg = synth.small_config("zipf", T=1536, H=128, E=32, k=4, I=64, bf16=True, frac=0.05)
+    inp = synth.moe_inputs(cfg, seed=8)
+    synth.apply_skew(inp, synth.skew_bias(cfg.E, 0.2, 4, seed=8))
+    logits = oracle.router_logits(inp["x"], inp["w_router"])
+    act = synth.uniform_mask(cfg.N, cfg.K, seed=8)
+    got = run_layer(cfg, inp, act, logits, dev)
+    counts = np.asarray(got["count"])
+    assert (counts == 0).sum() >= 4 and counts.max() > 512 and ((counts > 0) & (counts < 128)).any()
+    idx, b, g = oracle_layer(cfg, inp, act, logits)
+    compare(cfg, got, idx, b, g, 1e-2)
+
+
 def test_qwen3_shaped_layer_sampled():
     """Full Qwen3-30B-A3B-shaped layer (T=4096, H=2048, E=128, top-8, I=768, 0.5% active) in the
     launch configuration the benchmark times; the oracle checks every output of the forward and
