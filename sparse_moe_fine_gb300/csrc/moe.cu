@@ -285,17 +285,57 @@ __device__ __forceinline__ float dot_acc<float>(const uint4& a, const uint4& b, 
   return fmaf(__uint_as_float(a.w), __uint_as_float(b.w), s);
 }
 
-// S9/S10 masked weight gradient as a sampled dense-dense product on CUDA cores. A warp takes 32
-// consecutive active entries at a time, and lane l decodes entry l into the two feature-major rows
-// whose dot product over the expert's routed tokens is that entry's gradient:
+// Butterfly transpose-reduce of 16 values across a warp: lanes l and l + 16 both return the
+// warp-wide sum of x[l & 15] (16 shuffles for 16 sums). x is clobbered.
+__device__ __forceinline__ float transpose_reduce16(float (&x)[16], int lane) {
+#pragma unroll
+  for (int off = 8; off >= 1; off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int j = 0; j < off; ++j) {
+      const float send = upper ? x[j] : x[j + off];
+      const float keep = upper ? x[j + off] : x[j];
+      x[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  return x[0] + __shfl_xor_sync(0xffffffffu, x[0], 16);
+}
+
+// Number of sorted active entries below flat index n (the gate_up entries): a 32-way search by
+// one warp, about five dependent loads for millions of entries.
+__device__ __forceinline__ int64_t count_below(const int64_t* __restrict__ act, int64_t K,
+                                               int64_t n, int lane) {
+  int64_t lo = 0, hi = K;  // act[i] < n for i < lo, act[i] >= n for i >= hi
+  while (hi - lo > 32) {
+    const int64_t step = (hi - lo + 31) / 32;
+    const int64_t i = lo + (int64_t)lane * step;
+    const int c = __popc(__ballot_sync(0xffffffffu, i < hi && act[i] < n));
+    if (c == 0) {  // act[lo] >= n
+      hi = lo;
+      break;
+    }
+    // probes j < c are below n; probe c is not (or lies past hi)
+    const int64_t nhi = lo + (int64_t)c * step;
+    lo += (int64_t)(c - 1) * step + 1;
+    hi = nhi < hi ? nhi : hi;
+  }
+  const int64_t i = lo + lane;
+  return lo + __popc(__ballot_sync(0xffffffffu, i < hi && act[i] < n));
+}
+
+// S9/S10 masked weight gradient as a sampled dense-dense product on CUDA cores. The gate_up and
+// the down entries are cut separately into batches of 32 consecutive active entries; for a batch
+// the warp's lane l decodes entry l into the two feature-major rows whose dot product over the
+// expert's routed tokens is that entry's gradient:
 //   gate_up entry (e, j, c):  g = sum_t dh^T[j, o_e + t] * x^T[c, o_e + t]
 //   down entry (e, h, c):     g = sum_t dy^T[h, o_e + t] * (wA)^T[c, o_e + t]
-// Full passes: the warp walks the 32 entries together, lane l reading 16-byte vector l of both
-// rows (a pass covers 32 vectors, 256 bf16 tokens), the loads of four entries in flight before
-// their FMAs. The number of full passes is the batch's smallest vector count rounded to the
-// nearest multiple of 32; vectors beyond them are taken by groups of eight lanes, four entries at
-// a time. A butterfly transpose of the 32 per-lane partial sums then leaves entry l's total in
-// lane l for one coalesced store.
+// The 32 entries are then taken in two halves of 16. Full passes: the warp walks the half's
+// entries together, lane l reading 16-byte vector l of both rows (a pass covers 32 vectors, 256
+// bf16 tokens), the loads of eight entries in flight before their FMAs; an entry in the same
+// weight row as the one before it reuses that entry's row vector instead of loading it again. The
+// number of full passes is the half's smallest vector count rounded to the nearest multiple of 32;
+// vectors beyond them are taken by groups of eight lanes, four entries at a time. A butterfly
+// transpose of the 16 per-lane partial sums then leaves entry i's total in lane i.
 constexpr int SD_WARPS = 8;
 template <typename T>
 __global__ void __launch_bounds__(SD_WARPS * 32, 2) sddmm_kernel(
@@ -304,107 +344,104 @@ __global__ void __launch_bounds__(SD_WARPS * 32, 2) sddmm_kernel(
     const T* __restrict__ dhT, const T* __restrict__ xT, const T* __restrict__ dyT,
     const T* __restrict__ waT, float* __restrict__ g_act, uint32_t* dev_status) {
   constexpr int VW = 16 / sizeof(T);
-  constexpr int U = 4;   // entries whose loads are in flight together in a full pass
-  constexpr int RU = 2;  // rounds whose first loads are in flight together after them
-  constexpr uint32_t GU = 0x80000000u;
-  __shared__ int4 meta[SD_WARPS][32];  // per entry: a-row vector, b-row vector, vectors | GU
+  constexpr int U = 8;   // entries whose loads are in flight together in a full pass
+  constexpr int RU = 2;  // remainder rounds whose first loads are in flight together
+  __shared__ int4 meta[SD_WARPS][32];  // per entry: a-row vector, b-row vector, vector count
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, grp = lane >> 3, gl = lane & 7;
-  const int64_t stride = (int64_t)gridDim.x * SD_WARPS * 32;
   const uint4 zero = make_uint4(0, 0, 0, 0);
+  const int64_t kgu = count_below(act, K, Ngu, lane);
+  const int64_t nb_gu = (kgu + 31) / 32, nb = nb_gu + (K - kgu + 31) / 32;
   bool bad = false;
-  for (int64_t b0 = ((int64_t)blockIdx.x * SD_WARPS + wid) * 32; b0 < K; b0 += stride) {
-    const int64_t q = b0 + lane;
-    int4 md = make_int4(0, 0, 0, 0);
-    if (q < K) {
-      const int64_t f = act[q];
-      int64_t arow, col;
-      int e;
-      uint32_t gu = 0;
-      if (f < Ngu) {
-        const int64_t row = f / H;
-        col = f - row * H;
-        e = (int)(row / (2 * I));
-        arow = row - (int64_t)e * 2 * I;
-        gu = GU;
-      } else {
-        const int64_t row = (f - Ngu) / I;
-        col = (f - Ngu) - row * I;
-        e = (int)(row / H);
-        arow = row - (int64_t)e * H;
+  for (int64_t bt = (int64_t)blockIdx.x * SD_WARPS + wid; bt < nb;
+       bt += (int64_t)gridDim.x * SD_WARPS) {
+    const bool gu = bt < nb_gu;
+    const int64_t b0 = gu ? 32 * bt : kgu + 32 * (bt - nb_gu);
+    const int64_t lim = gu ? kgu : K;
+    const uint4* A = reinterpret_cast<const uint4*>(gu ? dhT : dyT);
+    const uint4* Bm = reinterpret_cast<const uint4*>(gu ? xT : waT);
+    {
+      const int64_t q = b0 + lane;
+      int4 md = make_int4(0, 0, 0, 0);
+      if (q < lim) {
+        const int64_t f = gu ? act[q] : act[q] - Ngu;
+        const int64_t wcols = gu ? H : I, wrows = gu ? 2 * I : H;
+        const int64_t row = f / wcols;
+        const int64_t col = f - row * wcols;
+        const int e = (int)(row / wrows);
+        const int64_t arow = row - (int64_t)e * wrows;
+        const int64_t o = off[e];
+        md.x = (int)((arow * rcap + o) / VW);
+        md.y = (int)((col * rcap + o) / VW);
+        md.z = (cnt[e] + VW - 1) / VW;
       }
-      const int64_t o = off[e];
-      md.x = (int)((arow * rcap + o) / VW);
-      md.y = (int)((col * rcap + o) / VW);
-      md.z = (int)(((uint32_t)(cnt[e] + VW - 1) / VW) | gu);
+      meta[wid][lane] = md;
     }
-    meta[wid][lane] = md;
-    const uint32_t nvl = (uint32_t)md.z & ~GU;
-    const uint32_t passes = (__reduce_min_sync(0xffffffffu, nvl) + 16u) / 32u;
-    const uint32_t vrest = 32u * passes;  // first vector left to the eight-lane groups
-    const bool rest = __any_sync(0xffffffffu, nvl > vrest);
     __syncwarp();
-    float part[32];
+    for (int hf = 0; hf < 2; ++hf) {
+      const int4* mh = &meta[wid][16 * hf];
+      const uint32_t nvl = (uint32_t)mh[lane & 15].z;
+      const uint32_t passes = (__reduce_min_sync(0xffffffffu, nvl) + 16u) / 32u;
+      const uint32_t vrest = 32u * passes;  // first vector left to the eight-lane groups
+      const bool rest = __any_sync(0xffffffffu, nvl > vrest);
+      float part[16];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) part[i] = 0.f;
-    if (passes > 0) {
+      for (int i = 0; i < 16; ++i) part[i] = 0.f;
+      if (passes > 0) {
 #pragma unroll
-      for (int i0 = 0; i0 < 32; i0 += U) {
-        const uint4* A[U];
-        const uint4* Bm[U];
-        uint32_t nv[U];
+        for (int i0 = 0; i0 < 16; i0 += U) {
+          for (uint32_t p = 0; p < passes; ++p) {
+            const uint32_t v = p * 32u + (uint32_t)lane;
+            uint4 av[U], bv[U];
+            uint32_t ax[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int4 m = meta[wid][i0 + u];
-          const uint32_t z = (uint32_t)m.z;
-          A[u] = reinterpret_cast<const uint4*>((z & GU) ? dhT : dyT) + (uint32_t)m.x;
-          Bm[u] = reinterpret_cast<const uint4*>((z & GU) ? xT : waT) + (uint32_t)m.y;
-          nv[u] = z & ~GU;
+            for (int u = 0; u < U; ++u) {
+              const int4 m = mh[i0 + u];
+              ax[u] = (uint32_t)m.x;
+              const uint32_t bx = (uint32_t)m.y, nv = (uint32_t)m.z;
+              const bool ok = v < nv;
+              const bool reuse = u > 0 && ax[u] == ax[u > 0 ? u - 1 : 0];
+              const uint4 ld = ok && !reuse ? __ldg(A + ((size_t)ax[u] + v)) : zero;
+              av[u] = reuse ? av[u > 0 ? u - 1 : 0] : ld;
+              bv[u] = ok ? __ldg(Bm + ((size_t)bx + v)) : zero;
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) part[i0 + u] = dot_acc<T>(av[u], bv[u], part[i0 + u]);
+          }
         }
-        for (uint32_t p = 0; p < passes; ++p) {
-          const uint32_t v = p * 32u + (uint32_t)lane;
-          uint4 av[U], bv[U];
+      }
+      if (rest) {
+        // entry 4r + grp of the half in round r; the first vector of every round is loaded up front
 #pragma unroll
-          for (int u = 0; u < U; ++u) {
-            av[u] = v < nv[u] ? __ldg(A[u] + v) : zero;
-            bv[u] = v < nv[u] ? __ldg(Bm[u] + v) : zero;
+        for (int h = 0; h < 4; h += RU) {
+          uint32_t ax[RU], bx[RU], nv[RU];
+          uint4 av[RU], bv[RU];
+          const uint32_t v0 = vrest + (uint32_t)gl;
+#pragma unroll
+          for (int r = 0; r < RU; ++r) {
+            const int4 m = mh[4 * (h + r) + grp];
+            ax[r] = (uint32_t)m.x;
+            bx[r] = (uint32_t)m.y;
+            nv[r] = (uint32_t)m.z;
+            av[r] = v0 < nv[r] ? __ldg(A + ((size_t)ax[r] + v0)) : zero;
+            bv[r] = v0 < nv[r] ? __ldg(Bm + ((size_t)bx[r] + v0)) : zero;
           }
 #pragma unroll
-          for (int u = 0; u < U; ++u) part[i0 + u] = dot_acc<T>(av[u], bv[u], part[i0 + u]);
+          for (int r = 0; r < RU; ++r) {
+            float sacc = dot_acc<T>(av[r], bv[r], 0.f);
+            for (uint32_t v = v0 + 8; v < nv[r]; v += 8)
+              sacc = dot_acc<T>(__ldg(A + ((size_t)ax[r] + v)), __ldg(Bm + ((size_t)bx[r] + v)),
+                                sacc);
+#pragma unroll
+            for (int g = 0; g < 4; ++g) part[4 * (h + r) + g] += grp == g ? sacc : 0.f;
+          }
         }
       }
-    }
-    if (rest) {
-      // entry 4r + grp in round r; the first vector of every round is loaded up front
-#pragma unroll
-      for (int h = 0; h < 8; h += RU) {
-        const uint4* A[RU];
-        const uint4* Bm[RU];
-        uint32_t nv[RU];
-        uint4 av[RU], bv[RU];
-        const uint32_t v0 = vrest + (uint32_t)gl;
-#pragma unroll
-        for (int r = 0; r < RU; ++r) {
-          const int4 m = meta[wid][4 * (h + r) + grp];
-          const uint32_t z = (uint32_t)m.z;
-          A[r] = reinterpret_cast<const uint4*>((z & GU) ? dhT : dyT) + (uint32_t)m.x;
-          Bm[r] = reinterpret_cast<const uint4*>((z & GU) ? xT : waT) + (uint32_t)m.y;
-          nv[r] = z & ~GU;
-          av[r] = v0 < nv[r] ? __ldg(A[r] + v0) : zero;
-          bv[r] = v0 < nv[r] ? __ldg(Bm[r] + v0) : zero;
-        }
-#pragma unroll
-        for (int r = 0; r < RU; ++r) {
-          float s = dot_acc<T>(av[r], bv[r], 0.f);
-          for (uint32_t v = v0 + 8; v < nv[r]; v += 8) s = dot_acc<T>(__ldg(A[r] + v), __ldg(Bm[r] + v), s);
-#pragma unroll
-          for (int g = 0; g < 4; ++g) part[4 * (h + r) + g] += grp == g ? s : 0.f;
-        }
+      const float gsum = transpose_reduce16(part, lane);
+      const int64_t q = b0 + 16 * hf + lane;
+      if (lane < 16 && q < lim) {
+        g_act[q] = gsum;
+        bad |= !finite_f(gsum);
       }
-    }
-    const float g = transpose_reduce32(part, lane);
-    if (q < K) {
-      g_act[q] = g;
-      bad |= !finite_f(g);
     }
     __syncwarp();  // the next batch rewrites meta
   }

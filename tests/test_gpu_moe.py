@@ -139,6 +139,19 @@ def test_bf16_skewed_routing():
     compare(cfg, got, idx, b, g, 1e-2)
 
 
+def test_bf16_empty_active_set():
+    """K = 0: no expert weight is trained; the router gradient, dx and dw are still produced."""
+    dev = device()
+    cfg = synth.small_config("k0", T=200, H=128, E=8, k=2, I=128, bf16=True, frac=0.05)
+    inp = synth.moe_inputs(cfg, seed=9)
+    logits = oracle.router_logits(inp["x"], inp["w_router"])
+    act = np.zeros(0, dtype=np.int64)
+    got = run_layer(cfg, inp, act, logits, dev)
+    idx, b, g = oracle_layer(cfg, inp, act, logits)
+    assert got["g_act"].size == 0 and g.size == 0
+    compare(cfg, got, idx, b, g, 1e-2)
+
+
 def test_qwen3_shaped_layer_sampled():
     """Full Qwen3-30B-A3B-shaped layer (T=4096, H=2048, E=128, top-8, I=768, 0.5% active) in the
     launch configuration the benchmark times; the oracle checks every output of the forward and
