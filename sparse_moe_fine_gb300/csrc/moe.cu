@@ -264,18 +264,27 @@ __global__ void __launch_bounds__(256) gather_transpose_kernel(
   }
 }
 
+// bf16 pair -> (lo, hi) fp32 pair in one 64-bit register, and the packed fp32 FMA on such pairs
+__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(w << 16), "r"(w & 0xFFFF0000u));
+  return r;
+}
+__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
 // s + the dot product of two 16-byte vectors (8 bf16 or 4 fp32), accumulated in fp32
 template <typename T>
 __device__ __forceinline__ float dot_acc(const uint4& a, const uint4& b, float s);
 template <>
 __device__ __forceinline__ float dot_acc<__nv_bfloat16>(const uint4& a, const uint4& b, float s) {
-  const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    s = fmaf(__uint_as_float(aw[q] << 16), __uint_as_float(bw[q] << 16), s);
-    s = fmaf(__uint_as_float(aw[q] & 0xFFFF0000u), __uint_as_float(bw[q] & 0xFFFF0000u), s);
-  }
-  return s;
+  uint64_t acc = ffma2(bf16x2_to_f32x2(a.x), bf16x2_to_f32x2(b.x), (uint64_t)__float_as_uint(s));
+  acc = ffma2(bf16x2_to_f32x2(a.y), bf16x2_to_f32x2(b.y), acc);
+  acc = ffma2(bf16x2_to_f32x2(a.z), bf16x2_to_f32x2(b.z), acc);
+  acc = ffma2(bf16x2_to_f32x2(a.w), bf16x2_to_f32x2(b.w), acc);
+  return __uint_as_float((uint32_t)acc) + __uint_as_float((uint32_t)(acc >> 32));
 }
 template <>
 __device__ __forceinline__ float dot_acc<float>(const uint4& a, const uint4& b, float s) {
@@ -300,6 +309,34 @@ __device__ __forceinline__ float transpose_reduce16(float (&x)[16], int lane) {
   }
   return x[0] + __shfl_xor_sync(0xffffffffu, x[0], 16);
 }
+
+// One 16-byte vector of a row operand held in fp32 for repeated dot products against other
+// vectors: bf16 pairs unpacked once into (lo, hi) fp32 pairs and multiplied with packed fp32 FMAs.
+template <typename T>
+struct RowVec;
+template <>
+struct RowVec<__nv_bfloat16> {
+  uint64_t f2[4];
+  __device__ __forceinline__ void set(const uint4& a) {
+    f2[0] = bf16x2_to_f32x2(a.x);
+    f2[1] = bf16x2_to_f32x2(a.y);
+    f2[2] = bf16x2_to_f32x2(a.z);
+    f2[3] = bf16x2_to_f32x2(a.w);
+  }
+  __device__ __forceinline__ float dot(const uint4& b) const {
+    uint64_t acc = ffma2(f2[0], bf16x2_to_f32x2(b.x), 0ull);
+    acc = ffma2(f2[1], bf16x2_to_f32x2(b.y), acc);
+    acc = ffma2(f2[2], bf16x2_to_f32x2(b.z), acc);
+    acc = ffma2(f2[3], bf16x2_to_f32x2(b.w), acc);
+    return __uint_as_float((uint32_t)acc) + __uint_as_float((uint32_t)(acc >> 32));
+  }
+};
+template <>
+struct RowVec<float> {
+  uint4 f;
+  __device__ __forceinline__ void set(const uint4& a) { f = a; }
+  __device__ __forceinline__ float dot(const uint4& b) const { return dot_acc<float>(f, b, 0.f); }
+};
 
 // Number of sorted active entries below flat index n (the gate_up entries): a 32-way search by
 // one warp, about five dependent loads for millions of entries.
@@ -331,8 +368,8 @@ __device__ __forceinline__ int64_t count_below(const int64_t* __restrict__ act, 
 //   down entry (e, h, c):     g = sum_t dy^T[h, o_e + t] * (wA)^T[c, o_e + t]
 // The 32 entries are then taken in two halves of 16. Full passes: the warp walks the half's
 // entries together, lane l reading 16-byte vector l of both rows (a pass covers 32 vectors, 256
-// bf16 tokens), the loads of eight entries in flight before their FMAs; an entry in the same
-// weight row as the one before it reuses that entry's row vector instead of loading it again. The
+// bf16 tokens), the loads of eight entries in flight before their FMAs; the row vector is loaded
+// and unpacked to fp32 pairs only where the weight row changes (packed fp32 FMAs). The
 // number of full passes is the half's smallest vector count rounded to the nearest multiple of 32;
 // vectors beyond them are taken by groups of eight lanes, four entries at a time. A butterfly
 // transpose of the 16 per-lane partial sums then leaves entry i's total in lane i.
@@ -387,25 +424,29 @@ __global__ void __launch_bounds__(SD_WARPS * 32, 2) sddmm_kernel(
 #pragma unroll
       for (int i = 0; i < 16; ++i) part[i] = 0.f;
       if (passes > 0) {
+        RowVec<T> rowv;
 #pragma unroll
         for (int i0 = 0; i0 < 16; i0 += U) {
           for (uint32_t p = 0; p < passes; ++p) {
             const uint32_t v = p * 32u + (uint32_t)lane;
             uint4 av[U], bv[U];
-            uint32_t ax[U];
+            bool fresh[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
               const int4 m = mh[i0 + u];
-              ax[u] = (uint32_t)m.x;
-              const uint32_t bx = (uint32_t)m.y, nv = (uint32_t)m.z;
+              const uint32_t nv = (uint32_t)m.z;
+              // the row operand is loaded and unpacked only where the weight row changes
+              fresh[u] = i0 + u == 0 ? true
+                                     : passes > 1 || m.x != mh[i0 + u == 0 ? 0 : i0 + u - 1].x;
               const bool ok = v < nv;
-              const bool reuse = u > 0 && ax[u] == ax[u > 0 ? u - 1 : 0];
-              const uint4 ld = ok && !reuse ? __ldg(A + ((size_t)ax[u] + v)) : zero;
-              av[u] = reuse ? av[u > 0 ? u - 1 : 0] : ld;
-              bv[u] = ok ? __ldg(Bm + ((size_t)bx + v)) : zero;
+              av[u] = ok && fresh[u] ? __ldg(A + ((size_t)(uint32_t)m.x + v)) : zero;
+              bv[u] = ok ? __ldg(Bm + ((size_t)(uint32_t)m.y + v)) : zero;
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u) part[i0 + u] = dot_acc<T>(av[u], bv[u], part[i0 + u]);
+            for (int u = 0; u < U; ++u) {
+              if (fresh[u]) rowv.set(av[u]);
+              part[i0 + u] += rowv.dot(bv[u]);
+            }
           }
         }
       }
