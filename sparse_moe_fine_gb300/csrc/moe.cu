@@ -323,19 +323,28 @@ struct RowVec<__nv_bfloat16> {
     f2[2] = bf16x2_to_f32x2(a.z);
     f2[3] = bf16x2_to_f32x2(a.w);
   }
-  __device__ __forceinline__ float dot(const uint4& b) const {
-    uint64_t acc = ffma2(f2[0], bf16x2_to_f32x2(b.x), 0ull);
-    acc = ffma2(f2[1], bf16x2_to_f32x2(b.y), acc);
-    acc = ffma2(f2[2], bf16x2_to_f32x2(b.z), acc);
-    acc = ffma2(f2[3], bf16x2_to_f32x2(b.w), acc);
+  // `m16` is 65536 passed at run time: the low half is unpacked by an integer multiply, which the
+  // compiler cannot turn into a shift, so half of the unpacking runs on the FMA pipe
+  __device__ __forceinline__ float dot(const uint4& b, uint32_t m16) const {
+    uint64_t acc = ffma2(f2[0], unpack_m(b.x, m16), 0ull);
+    acc = ffma2(f2[1], unpack_m(b.y, m16), acc);
+    acc = ffma2(f2[2], unpack_m(b.z, m16), acc);
+    acc = ffma2(f2[3], unpack_m(b.w, m16), acc);
     return __uint_as_float((uint32_t)acc) + __uint_as_float((uint32_t)(acc >> 32));
+  }
+  __device__ __forceinline__ static uint64_t unpack_m(uint32_t w, uint32_t m16) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(w * m16), "r"(w & 0xFFFF0000u));
+    return r;
   }
 };
 template <>
 struct RowVec<float> {
   uint4 f;
   __device__ __forceinline__ void set(const uint4& a) { f = a; }
-  __device__ __forceinline__ float dot(const uint4& b) const { return dot_acc<float>(f, b, 0.f); }
+  __device__ __forceinline__ float dot(const uint4& b, uint32_t) const {
+    return dot_acc<float>(f, b, 0.f);
+  }
 };
 
 // Number of sorted active entries below flat index n (the gate_up entries): a 32-way search by
@@ -369,8 +378,9 @@ __device__ __forceinline__ int64_t count_below(const int64_t* __restrict__ act, 
 // The 32 entries are then taken in two halves of 16. Full passes: the warp walks the half's
 // entries together, lane l reading 16-byte vector l of both rows (a pass covers 32 vectors, 256
 // bf16 tokens), the loads of eight entries in flight before their FMAs; the row vector is loaded
-// and unpacked to fp32 pairs only where the weight row changes (packed fp32 FMAs). The
-// number of full passes is the half's smallest vector count rounded to the nearest multiple of 32;
+// and unpacked to fp32 pairs only where the weight row changes (packed fp32 FMAs). Lanes past an
+// entry's last vector re-read that vector (an in-bounds address) and drop the product. The number
+// of full passes is the half's smallest vector count rounded to the nearest multiple of 32;
 // vectors beyond them are taken by groups of eight lanes, four entries at a time. A butterfly
 // transpose of the 16 per-lane partial sums then leaves entry i's total in lane i.
 constexpr int SD_WARPS = 8;
@@ -379,13 +389,13 @@ __global__ void __launch_bounds__(SD_WARPS * 32, 2) sddmm_kernel(
     const int64_t* __restrict__ act, int64_t K, const int32_t* __restrict__ cnt,
     const int32_t* __restrict__ off, int H, int I, int64_t Ngu, int64_t rcap,
     const T* __restrict__ dhT, const T* __restrict__ xT, const T* __restrict__ dyT,
-    const T* __restrict__ waT, float* __restrict__ g_act, uint32_t* dev_status) {
+    const T* __restrict__ waT, float* __restrict__ g_act, uint32_t m16, uint32_t* dev_status) {
   constexpr int VW = 16 / sizeof(T);
   constexpr int U = 8;   // entries whose loads are in flight together in a full pass
   constexpr int RU = 2;  // remainder rounds whose first loads are in flight together
-  __shared__ int4 meta[SD_WARPS][32];  // per entry: a-row vector, b-row vector, vector count
+  // per entry: a-row vector, b-row vector, vector count, last vector (0 when there is none)
+  __shared__ int4 meta[SD_WARPS][32];
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, grp = lane >> 3, gl = lane & 7;
-  const uint4 zero = make_uint4(0, 0, 0, 0);
   const int64_t kgu = count_below(act, K, Ngu, lane);
   const int64_t nb_gu = (kgu + 31) / 32, nb = nb_gu + (K - kgu + 31) / 32;
   bool bad = false;
@@ -407,9 +417,13 @@ __global__ void __launch_bounds__(SD_WARPS * 32, 2) sddmm_kernel(
         const int e = (int)(row / wrows);
         const int64_t arow = row - (int64_t)e * wrows;
         const int64_t o = off[e];
-        md.x = (int)((arow * rcap + o) / VW);
-        md.y = (int)((col * rcap + o) / VW);
-        md.z = (cnt[e] + VW - 1) / VW;
+        const int nv = (cnt[e] + VW - 1) / VW;
+        if (nv > 0) {
+          md.x = (int)((arow * rcap + o) / VW);
+          md.y = (int)((col * rcap + o) / VW);
+          md.z = nv;
+          md.w = nv - 1;
+        }
       }
       meta[wid][lane] = md;
     }
@@ -430,52 +444,57 @@ __global__ void __launch_bounds__(SD_WARPS * 32, 2) sddmm_kernel(
           for (uint32_t p = 0; p < passes; ++p) {
             const uint32_t v = p * 32u + (uint32_t)lane;
             uint4 av[U], bv[U];
-            bool fresh[U];
+            uint32_t fresh = 0, ok = 0;  // bit u: entry i0 + u starts a new weight row / has vector v
 #pragma unroll
             for (int u = 0; u < U; ++u) {
               const int4 m = mh[i0 + u];
-              const uint32_t nv = (uint32_t)m.z;
               // the row operand is loaded and unpacked only where the weight row changes
-              fresh[u] = i0 + u == 0 ? true
-                                     : passes > 1 || m.x != mh[i0 + u == 0 ? 0 : i0 + u - 1].x;
-              const bool ok = v < nv;
-              av[u] = ok && fresh[u] ? __ldg(A + ((size_t)(uint32_t)m.x + v)) : zero;
-              bv[u] = ok ? __ldg(Bm + ((size_t)(uint32_t)m.y + v)) : zero;
+              const bool f = i0 + u == 0 ? true
+                                         : passes > 1 || m.x != mh[i0 + u == 0 ? 0 : i0 + u - 1].x;
+              fresh |= (uint32_t)f << u;
+              ok |= (uint32_t)(v < (uint32_t)m.z) << u;
+              const uint32_t vv = min(v, (uint32_t)m.w);
+              if (f) av[u] = __ldg(A + ((uint32_t)m.x + vv));
+              bv[u] = __ldg(Bm + ((uint32_t)m.y + vv));
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-              if (fresh[u]) rowv.set(av[u]);
-              part[i0 + u] += rowv.dot(bv[u]);
+              if (fresh & (1u << u)) rowv.set(av[u]);
+              const float d = rowv.dot(bv[u], m16);
+              if (ok & (1u << u)) part[i0 + u] += d;
             }
           }
         }
       }
       if (rest) {
         // entry 4r + grp of the half in round r; the first vector of every round is loaded up front
+        float rem[4];
 #pragma unroll
         for (int h = 0; h < 4; h += RU) {
-          uint32_t ax[RU], bx[RU], nv[RU];
+          int4 m[RU];
           uint4 av[RU], bv[RU];
           const uint32_t v0 = vrest + (uint32_t)gl;
 #pragma unroll
           for (int r = 0; r < RU; ++r) {
-            const int4 m = mh[4 * (h + r) + grp];
-            ax[r] = (uint32_t)m.x;
-            bx[r] = (uint32_t)m.y;
-            nv[r] = (uint32_t)m.z;
-            av[r] = v0 < nv[r] ? __ldg(A + ((size_t)ax[r] + v0)) : zero;
-            bv[r] = v0 < nv[r] ? __ldg(Bm + ((size_t)bx[r] + v0)) : zero;
+            m[r] = mh[4 * (h + r) + grp];
+            const uint32_t vv = min(v0, (uint32_t)m[r].w);
+            av[r] = __ldg(A + ((uint32_t)m[r].x + vv));
+            bv[r] = __ldg(Bm + ((uint32_t)m[r].y + vv));
           }
 #pragma unroll
           for (int r = 0; r < RU; ++r) {
             float sacc = dot_acc<T>(av[r], bv[r], 0.f);
-            for (uint32_t v = v0 + 8; v < nv[r]; v += 8)
-              sacc = dot_acc<T>(__ldg(A + ((size_t)ax[r] + v)), __ldg(Bm + ((size_t)bx[r] + v)),
-                                sacc);
-#pragma unroll
-            for (int g = 0; g < 4; ++g) part[4 * (h + r) + g] += grp == g ? sacc : 0.f;
+            if (v0 >= (uint32_t)m[r].z) sacc = 0.f;
+            for (uint32_t v = v0 + 8; v < (uint32_t)m[r].z; v += 8)
+              sacc = dot_acc<T>(__ldg(A + ((uint32_t)m[r].x + v)),
+                                __ldg(Bm + ((uint32_t)m[r].y + v)), sacc);
+            rem[h + r] = sacc;
           }
         }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int g = 0; g < 4; ++g) part[4 * r + g] += grp == g ? rem[r] : 0.f;
       }
       const float gsum = transpose_reduce16(part, lane);
       const int64_t q = b0 + 16 * hf + lane;
@@ -853,7 +872,8 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
     const unsigned blocks = (unsigned)std::min<int64_t>(ceil_div(K, SD_WARPS * 32),
                                                         device_sm_count() * 2);
     sddmm_kernel<T><<<blocks, SD_WARPS * 32, 0, st>>>(act_idx, K, cnt, off, H, I, Ngu, a.R_cap,
-                                                      dhT, xT, dyT, waT, g_act, dev_status);
+                                                      dhT, xT, dyT, waT, g_act, 65536u,
+                                                      dev_status);
     USAF_CHECK_LAUNCH();
   }
   return USAF_OK;

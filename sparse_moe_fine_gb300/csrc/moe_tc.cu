@@ -1,13 +1,11 @@
 // bf16 grouped expert GEMMs on 5th-generation tensor cores (tcgen05.mma, accumulators in TMEM),
-// fed by TMA (cp.async.bulk.tensor) through an mbarrier ring of shared-memory stages. One
-// persistent CTA per SM with three roles: warp 0 issues TMA loads, warp 1 issues MMAs (one thread)
-// and owns the TMEM allocation, eight epilogue warps run the fused epilogue out of the TMEM
+// fed by TMA (cp.async.bulk.tensor) through a 4-stage mbarrier pipeline. One persistent CTA per SM
+// with three roles: warp 0 issues TMA loads, warp 1 issues MMAs (one thread) and owns the TMEM
+// allocation, eight epilogue warps run the fused epilogue out of a double-buffered TMEM
 // accumulator (two warps per TMEM lane quarter, alternating 32-column chunks).
 //
-// Every GEMM puts the weight dimension on M and the routed tokens on N (16..256 per tile), so an
-// expert's ragged token count only pads to 16. An expert GEMM tile covers 256 weight rows as two
-// 128-row MMAs that share each stage's token operand (three 64 KB stages); the router keeps
-// 128-row tiles (four 48 KB stages, double-buffered accumulator). The token operand is
+// Every GEMM puts the weight dimension on M (128 rows per tile) and the routed tokens on N
+// (16..256 per tile), so an expert's ragged token count only pads to 16. The token operand is
 // feature-major (one row per feature, the expert's permuted tokens contiguous) and is loaded as
 // the MN-major B operand in boxes of 64 tokens.
 //   S4 gate_up: h^T = gate_up[e] x^T     A = gate/up rows interleaved (K-major), B = x^T
@@ -28,35 +26,23 @@ namespace usaf {
 
 namespace {
 
-constexpr int BM = 128;  // rows of one MMA (M) and of one A sub-tile
+constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int BN = 256;
-constexpr int MAX_STAGES = 4;
+constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int B_BOX = 64 * BK * 2;  // one MN-major box: 64 tokens x 64 k
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_E = 1024;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + 2 * (MAX_E + 1) * 4;
+static_assert(SMEM_BYTES <= 232448, "shared memory of the tensor-core kernel");
 constexpr long long TIMEOUT_CYCLES = 1ll << 32;  // about two seconds
 
 enum Var { V_GATEUP = 0, V_DOWN = 1, V_GVEC = 2, V_DX = 3, V_ROUTER = 4 };
-
-// Per variant: an expert GEMM tile holds UM = 2 sub-tiles of 128 weight rows that share the
-// token operand of every stage (two MMAs per k step, 256 x N accumulators filling TMEM, so one
-// accumulator buffer); the router keeps 128-row tiles with a double-buffered accumulator.
-template <int VAR>
-struct Cfg {
-  static constexpr int UM = VAR == V_ROUTER ? 1 : 2;
-  static constexpr int STAGES = UM == 2 ? 3 : 4;
-  static constexpr int NBUF = UM == 2 ? 1 : 2;
-  static constexpr int STAGE_BYTES = UM * A_BYTES + B_BYTES;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + 256 + 2 * (MAX_E + 1) * 4;
-  static_assert(STAGES <= MAX_STAGES, "barrier slots");
-  static_assert(SMEM <= 232448, "shared memory of the tensor-core kernel");
-  static_assert(UM * NBUF * BN <= TMEM_COLS, "tensor memory columns");
-};
 
 struct Params {
   const int32_t* off;
@@ -186,7 +172,6 @@ struct Tile {
   int row0;   // first permuted row (token) of the tile
   int nrows;  // tokens in the tile (multiple of 16)
   int klen;   // K extent
-  int nsub;   // 128-row sub-tiles inside the weight range (1 or 2)
 };
 
 template <int VAR>
@@ -218,7 +203,6 @@ __device__ __forceinline__ Tile get_tile(const Params& p, const int32_t* s_plan,
     ti.row0 = nt * ROUTER_BN;
     ti.nrows = min(ROUTER_BN, (p.T - ti.row0 + 15) / 16 * 16);
     ti.klen = 3 * p.H;
-    ti.nsub = 1;
   } else {
     const int e = upper_bound_i32(s_plan, p.E + 1, t / p.MT) - 1;
     const int nts = s_plan[e + 1] - s_plan[e];
@@ -227,11 +211,7 @@ __device__ __forceinline__ Tile get_tile(const Params& p, const int32_t* s_plan,
     const int npad = s_off[e + 1] - s_off[e];
     const int base = ((npad + nts - 1) / nts + 15) / 16 * 16;
     ti.e = e;
-    // M units of a sub-tile: gate_up counts features (64 gate + 64 up rows), the others rows
-    constexpr int SUB = VAR == V_GATEUP ? 64 : BM;
-    const int mtot = (VAR == V_GATEUP || VAR == V_GVEC) ? p.I : p.H;
-    ti.m0 = mt * SUB * Cfg<VAR>::UM;
-    ti.nsub = min(Cfg<VAR>::UM, (mtot - ti.m0 + SUB - 1) / SUB);
+    ti.m0 = mt * (VAR == V_GATEUP ? 64 : BM);
     ti.row0 = s_off[e] + nt * base;
     ti.nrows = min(base, npad - nt * base);
     ti.klen = (VAR == V_GATEUP || VAR == V_GVEC) ? p.H : (VAR == V_DOWN ? p.I : 2 * p.I);
@@ -286,13 +266,13 @@ __device__ __forceinline__ float bf_at(const uint32_t (&a)[16], int j) {
 }
 
 template <int VAR>
-__device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, int m0, uint32_t taddr,
-                                         int row, int lane, int half) {
+__device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32_t taddr, int row,
+                                         int lane, int half) {
   constexpr unsigned FULL = 0xffffffffu;
   const int H = p.H, I = p.I;
   const int nch = (ti.nrows + 31) / 32;
   if constexpr (VarTraits<VAR>::router) {
-    const int e = m0 + row;
+    const int e = ti.m0 + row;
     for (int ch = half; ch < nch; ch += 2) {
       float v[32];
       tmem_ld32(taddr + ch * 32, v);
@@ -306,7 +286,7 @@ __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, int m0
   }
   uint32_t hg[16], hu[16];  // V_GVEC: gate and up of the chunk being processed
   if constexpr (VAR == V_GVEC) {
-    const int i = m0 + row;
+    const int i = ti.m0 + row;
     const int ncol = min(32, ti.nrows - half * 32);
     load_row32(p.hin + (int64_t)i * p.R_cap + ti.row0 + half * 32, i < I && half < nch, ncol, hg);
     load_row32(p.hin + (int64_t)(I + i) * p.R_cap + ti.row0 + half * 32, i < I && half < nch,
@@ -325,7 +305,7 @@ __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, int m0
     if constexpr (VAR == V_GATEUP) {
       float v[32];
       tmem_ld32(taddr + ch * 32, v);
-      const int i = m0 + (row >> 1);
+      const int i = ti.m0 + (row >> 1);
       const int g = row & 1;  // rows alternate gate (even lane) and up (odd lane) of feature i
       store_row32(p.h + (int64_t)(g * I + i) * p.R_cap + ti.row0 + cbase, v, ncol);
       float wa[32];
@@ -340,7 +320,7 @@ __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, int m0
     } else if constexpr (VAR == V_DOWN || VAR == V_DX) {
       float v[32];
       tmem_ld32(taddr + ch * 32, v);
-      const int hh = m0 + row;
+      const int hh = ti.m0 + row;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         if (j >= ncol) break;
@@ -349,7 +329,7 @@ __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, int m0
         if (sj >= 0 && hh < H) atomicAdd(&p.acc_out[(int64_t)tj * H + hh], v[j]);
       }
     } else {  // V_GVEC: SwiGLU backward, dh^T and the routing-weight gradient dw
-      const int i = m0 + row;
+      const int i = ti.m0 + row;
       const bool iv = i < I;
       uint32_t ng[16], nu[16];
       if (ch + 2 < nch) {  // next chunk of gate/up in flight during this one
@@ -410,18 +390,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  constexpr int STAGES = Cfg<VAR>::STAGES, STAGE_BYTES = Cfg<VAR>::STAGE_BYTES;
-  constexpr int UM = Cfg<VAR>::UM, NBUF = Cfg<VAR>::NBUF;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  // bars: full[MAX_STAGES], empty[MAX_STAGES], tfull[2], tempty[2], drain[1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * MAX_STAGES + 5);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain[1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int32_t* s_plan = reinterpret_cast<int32_t*>(smem + STAGES * STAGE_BYTES + 256);
   int32_t* s_off = s_plan + (MAX_E + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * MAX_STAGES;
-  const uint32_t tfull0 = empty0 + 8 * MAX_STAGES, tempty0 = tfull0 + 16, drain = tempty0 + 16;
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES;
+  const uint32_t tfull0 = empty0 + 8 * STAGES, tempty0 = tfull0 + 16, drain = tempty0 + 16;
 
   if constexpr (!VarTraits<VAR>::router) {
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
@@ -434,7 +412,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
-    for (int a = 0; a < NBUF; ++a) {
+    for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
       mbar_init(tempty0 + 8 * a, EPI_WARPS);
     }
@@ -473,7 +451,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           const uint32_t a_dst = smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t b_dst = a_dst + UM * A_BYTES;
+          const uint32_t b_dst = a_dst + A_BYTES;
           const uint32_t fb = full0 + 8 * stage;
           const int k0 = kb * BK;
           if constexpr (VarTraits<VAR>::router) {
@@ -481,20 +459,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tma_2d(a_dst, &tmA, fb, k0, ti.m0);
             tma_2d(b_dst, &tmB, fb, k0 % p.H, ti.row0);  // x, once for each part of Wr
           } else {
-            mbar_expect_tx(fb, ti.nsub * A_BYTES + nbox * B_BOX);
-            for (int h = 0; h < ti.nsub; ++h) {
-              const uint32_t ad = a_dst + h * A_BYTES;
-              if constexpr (VAR == V_GATEUP) {
-                tma_4d(ad, &tmA, fb, k0, 0, ti.m0 + 64 * h, ti.e);
-              } else if constexpr (VAR == V_DOWN) {
-                tma_2d(ad, &tmA, fb, k0, ti.e * p.H + ti.m0 + BM * h);
-              } else if constexpr (VAR == V_GVEC) {
-                tma_2d(ad, &tmA, fb, ti.m0 + BM * h, ti.e * p.H + k0);
-                tma_2d(ad + 8192, &tmA, fb, ti.m0 + BM * h + 64, ti.e * p.H + k0);
-              } else {  // V_DX
-                tma_2d(ad, &tmA, fb, ti.m0 + BM * h, ti.e * 2 * p.I + k0);
-                tma_2d(ad + 8192, &tmA, fb, ti.m0 + BM * h + 64, ti.e * 2 * p.I + k0);
-              }
+            mbar_expect_tx(fb, A_BYTES + nbox * B_BOX);
+            if constexpr (VAR == V_GATEUP) {
+              tma_4d(a_dst, &tmA, fb, k0, 0, ti.m0, ti.e);
+            } else if constexpr (VAR == V_DOWN) {
+              tma_2d(a_dst, &tmA, fb, k0, ti.e * p.H + ti.m0);
+            } else if constexpr (VAR == V_GVEC) {
+              tma_2d(a_dst, &tmA, fb, ti.m0, ti.e * p.H + k0);
+              tma_2d(a_dst + 8192, &tmA, fb, ti.m0 + 64, ti.e * p.H + k0);
+            } else {  // V_DX
+              tma_2d(a_dst, &tmA, fb, ti.m0, ti.e * 2 * p.I + k0);
+              tma_2d(a_dst + 8192, &tmA, fb, ti.m0 + 64, ti.e * 2 * p.I + k0);
             }
             // B: feature-major tokens, boxes of 64 tokens x 64 k (MN-major, 8 KB apart)
             for (int q = 0; q < nbox; ++q) tma_2d(b_dst + q * B_BOX, &tmB, fb, ti.row0 + 64 * q, k0);
@@ -534,7 +509,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t d = tmem_base + acc * UM * BN;
+        const uint32_t d = tmem_base + acc * BN;
         const uint32_t idesc = idesc_bf16(ti.nrows, a_mn, b_mn);
         const int nkb = (ti.klen + BK - 1) / BK;
         for (int kb = 0; kb < nkb; ++kb) {
@@ -544,14 +519,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after();
           const uint32_t a_base = smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t b_base = a_base + UM * A_BYTES;
-          for (int h = 0; h < ti.nsub; ++h) {
+          const uint32_t b_base = a_base + A_BYTES;
 #pragma unroll
-            for (int ks = 0; ks < BK / 16; ++ks) {
-              const uint64_t ad = sdesc(a_base + h * A_BYTES + ks * a_step, a_lbo, 1024);
-              const uint64_t bd = sdesc(b_base + ks * b_step, b_lbo, 1024);
-              umma_bf16(d + h * BN, ad, bd, idesc, (kb | ks) != 0 ? 1u : 0u);
-            }
+          for (int ks = 0; ks < BK / 16; ++ks) {
+            const uint64_t ad = sdesc(a_base + ks * a_step, a_lbo, 1024);
+            const uint64_t bd = sdesc(b_base + ks * b_step, b_lbo, 1024);
+            umma_bf16(d, ad, bd, idesc, (kb | ks) != 0 ? 1u : 0u);
           }
           umma_commit(empty0 + 8 * stage);
           if (++stage == STAGES) {
@@ -561,7 +534,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (failed) break;
         umma_commit(tfull0 + 8 * acc);
-        if (++acc == NBUF) {
+        if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1;
         }
@@ -588,15 +561,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-#pragma unroll 1
-      for (int h = 0; h < ti.nsub; ++h)
-        epilogue<VAR>(p, ti, ti.m0 + h * (VAR == V_GATEUP ? 64 : BM),
-                      tmem_base + ((uint32_t)(q * 32) << 16) + (acc * UM + h) * BN, row, lane,
-                      half);
+      epilogue<VAR>(p, ti, tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN, row, lane, half);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
-      if (++acc == NBUF) {
+      if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1;
       }
@@ -716,11 +685,11 @@ usaf_status launch(const CUtensorMap& a, const CUtensorMap& b, const Params& p, 
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(tc_gemm_kernel<VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg<VAR>::SMEM) != cudaSuccess)
+                             SMEM_BYTES) != cudaSuccess)
       return USAF_ERR_CUDA;
     attr_done = true;
   }
-  tc_gemm_kernel<VAR><<<device_sm_count(), NUM_THREADS, Cfg<VAR>::SMEM, st>>>(a, b, p);
+  tc_gemm_kernel<VAR><<<device_sm_count(), NUM_THREADS, SMEM_BYTES, st>>>(a, b, p);
   USAF_CHECK_LAUNCH();
   return USAF_OK;
 }
@@ -783,7 +752,7 @@ usaf_status tc_fwd_gate_up(const MoeArgs& a, const void* xT, void* hT, void* waT
       !map_tokens(&mb, xT, a.s.H, a.R_cap))
     return USAF_ERR_CUDA;
   Params p = base_params(a);
-  p.MT = (int)ceil_div(a.s.I, 64 * Cfg<V_GATEUP>::UM);
+  p.MT = (int)(a.s.I / 64);
   p.h = static_cast<__nv_bfloat16*>(hT);
   p.wa = static_cast<__nv_bfloat16*>(waT);
   return launch<V_GATEUP>(ma, mb, p, st);
@@ -794,7 +763,7 @@ usaf_status tc_fwd_down(const MoeArgs& a, const void* waT, float* y_acc, cudaStr
   if (!map_2d(&ma, a.w_down, a.s.I, a.s.E * a.s.H, 64, 128) || !map_tokens(&mb, waT, a.s.I, a.R_cap))
     return USAF_ERR_CUDA;
   Params p = base_params(a);
-  p.MT = (int)ceil_div(a.s.H, BM * Cfg<V_DOWN>::UM);
+  p.MT = (int)ceil_div(a.s.H, BM);
   p.acc_out = y_acc;
   return launch<V_DOWN>(ma, mb, p, st);
 }
@@ -805,7 +774,7 @@ usaf_status tc_bwd_gvec(const MoeArgs& a, const void* dyT, const void* hT, void*
   if (!map_2d(&ma, a.w_down, a.s.I, a.s.E * a.s.H, 64, 64) || !map_tokens(&mb, dyT, a.s.H, a.R_cap))
     return USAF_ERR_CUDA;
   Params p = base_params(a);
-  p.MT = (int)ceil_div(a.s.I, BM * Cfg<V_GVEC>::UM);
+  p.MT = (int)ceil_div(a.s.I, BM);
   p.hin = static_cast<const __nv_bfloat16*>(hT);
   p.dh = static_cast<__nv_bfloat16*>(dhT);
   p.dw = dw;
@@ -818,7 +787,7 @@ usaf_status tc_bwd_dx(const MoeArgs& a, const void* dhT, float* dx_acc, cudaStre
       !map_tokens(&mb, dhT, 2 * a.s.I, a.R_cap))
     return USAF_ERR_CUDA;
   Params p = base_params(a);
-  p.MT = (int)ceil_div(a.s.H, BM * Cfg<V_DX>::UM);
+  p.MT = (int)ceil_div(a.s.H, BM);
   p.acc_out = dx_acc;
   return launch<V_DX>(ma, mb, p, st);
 }

@@ -7,8 +7,8 @@
 //
 // Fast path, one read of g: a strided sample gives a candidate threshold tau0 a safe margin below
 // the K-th largest key; one coalesced pass compacts every (key, index) with key >= tau0 into
-// per-block regions in index order; an exact radix select (4 digit rounds) and an ordered
-// compaction then run on the candidates only. If a region overflows or fewer than K candidates
+// per-warp regions in index order; an exact radix select (4 digit rounds) and an ordered
+// compaction then run on the candidates only, one block per region. If a region overflows or fewer than K candidates
 // exist, the same kernels run on the full array instead (exact multi-pass path); the choice is
 // taken on the device, so the launch sequence is fixed and needs no host synchronisation.
 #include "common.cuh"
@@ -19,6 +19,7 @@ namespace usaf {
 namespace {
 
 constexpr int SEL_THREADS = 256;
+constexpr int COMPACT_WARPS = 8;  // warps per block of the compacting pass, one region each
 constexpr int SAMPLE_S = 32768;
 // radix rounds over the 31-bit key, most significant digit first: bits 30..23, 22..15, 14..7, 6..0
 __host__ __device__ constexpr int round_shift(int r) { return r == 0 ? 23 : r == 1 ? 15 : r == 2 ? 7 : 0; }
@@ -72,21 +73,27 @@ struct SelWs {
 SelPlan make_plan(int64_t N, int64_t K) {
   SelPlan p{};
   const int64_t sms = device_sm_count();
-  int64_t G = ceil_div(N, 16384);
-  if (G > sms * 4) G = sms * 4;
-  if (G < 1) G = 1;
-  p.G = (int)G;
-  p.L = round_up(ceil_div(N, G), 1024);
   p.sampling = N >= (int64_t)4 * 1024 * 1024 && K * 16 <= N;
   if (p.sampling) {
     const double q = std::ceil((double)SAMPLE_S * (double)K / (double)N);
     const double qq = q + 8.0 * std::sqrt(q) + 32.0;
     p.q = (int)std::min<double>(qq, SAMPLE_S);
-    const double frac = (double)p.q / SAMPLE_S;
-    p.cap = round_up((int64_t)((double)p.L * frac * 1.5) + 2048, 256);
     if (p.q >= SAMPLE_S / 8) p.sampling = false;
   }
-  if (!p.sampling) {
+  if (p.sampling) {
+    // one candidate region per warp of the compacting pass (COMPACT_WARPS per block)
+    int64_t G = std::min<int64_t>(ceil_div(N, 65536), sms * 32);
+    G = round_up(G < 1 ? 1 : G, COMPACT_WARPS);
+    p.G = (int)G;
+    p.L = round_up(ceil_div(N, G), 1024);
+    const double mean = (double)p.L * (double)p.q / SAMPLE_S;
+    p.cap = round_up((int64_t)(mean * 1.5 + 8.0 * std::sqrt(mean)) + 256, 256);
+  } else {
+    int64_t G = ceil_div(N, 16384);
+    if (G > sms * 4) G = sms * 4;
+    if (G < 1) G = 1;
+    p.G = (int)G;
+    p.L = round_up(ceil_div(N, G), 1024);
     p.q = 0;
     p.cap = 0;
   }
@@ -235,64 +242,75 @@ __global__ void __launch_bounds__(1024) sel_sample_tau_kernel(const uint32_t* __
   if (threadIdx.x == 0) c->tau0 = s_prefix;
 }
 
-// The one pass over g: compact (key, index) with key >= tau0 (and not excluded) per block region.
-__global__ void __launch_bounds__(SEL_THREADS) sel_compact_kernel(
+// The one pass over g: every warp compacts the (key, index) pairs with key >= tau0 (and not
+// excluded) of its own contiguous part of g into its own region, in index order. Four float4
+// loads per lane are in flight; a warp scan places the candidates only when some lane has one.
+__global__ void __launch_bounds__(COMPACT_WARPS * 32) sel_compact_kernel(
     const float* __restrict__ g, int64_t N, int64_t L, const uint32_t* __restrict__ excl,
     int64_t cap, uint32_t* __restrict__ ckeys, uint32_t* __restrict__ cids,
     uint32_t* __restrict__ ccnt, SelCtrl* c, int vec_ok, uint32_t* dev_status) {
+  constexpr int UN = 4;
   const uint32_t tau0 = c->tau0;
-  const int b = blockIdx.x;
-  const int64_t lo = (int64_t)b * L;
+  const int lane = threadIdx.x & 31;
+  const int64_t r = (int64_t)blockIdx.x * COMPACT_WARPS + (threadIdx.x >> 5);
+  const int64_t lo = r * L;
   const int64_t hi = min(N, lo + L);
-  uint32_t* rk = ckeys + (int64_t)b * cap;
-  uint32_t* ri = cids + (int64_t)b * cap;
+  uint32_t* rk = ckeys + r * cap;
+  uint32_t* ri = cids + r * cap;
   uint32_t count = 0;
   bool over = false, bad = false;
-  constexpr int TILE = SEL_THREADS * 4;
-  for (int64_t t0 = lo; t0 < hi; t0 += TILE) {
-    uint32_t key[4];
-    bool ok[4];
-    const int64_t i0 = t0 + (int64_t)threadIdx.x * 4;
-    if (vec_ok && i0 + 3 < hi) {
-      const float4 v = __ldcs(reinterpret_cast<const float4*>(g + i0));
-      key[0] = abs_key(v.x);
-      key[1] = abs_key(v.y);
-      key[2] = abs_key(v.z);
-      key[3] = abs_key(v.w);
+  for (int64_t t0 = lo; t0 < hi; t0 += 128 * UN) {
+    uint32_t key[UN][4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) ok[j] = true;
-    } else {
+    for (int u = 0; u < UN; ++u) {
+      const int64_t i0 = t0 + u * 128 + lane * 4;
+      if (vec_ok && i0 + 3 < hi) {
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(g + i0));
+        key[u][0] = abs_key(v.x);
+        key[u][1] = abs_key(v.y);
+        key[u][2] = abs_key(v.z);
+        key[u][3] = abs_key(v.w);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) key[u][j] = i0 + j < hi ? abs_key(g[i0 + j]) : 0u;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < UN; ++u) {
+      const int64_t i0 = t0 + u * 128 + lane * 4;
+      uint32_t okm = 0;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        ok[j] = i0 + j < hi;
-        key[j] = ok[j] ? abs_key(g[i0 + j]) : 0u;
+        const bool in = i0 + j < hi;
+        bad |= in && key[u][j] >= 0x7F800000u;
+        if (in && key[u][j] >= tau0 && !excluded(excl, i0 + j)) okm |= 1u << j;
       }
-    }
-    uint32_t mine = 0;
+      if (!__any_sync(0xffffffffu, okm != 0)) continue;
+      const uint32_t mine = __popc(okm);
+      uint32_t x = mine;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      bad |= ok[j] && key[j] >= 0x7F800000u;
-      ok[j] = ok[j] && key[j] >= tau0 && !excluded(excl, i0 + j);
-      mine += ok[j];
-    }
-    uint32_t tot;
-    uint32_t pos = count + block_excl_scan(mine, &tot);
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      uint32_t pos = count + x - mine;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      if (ok[j]) {
-        if (pos < cap) {
-          rk[pos] = key[j];
-          ri[pos] = (uint32_t)(i0 + j);
-        } else {
-          over = true;
+      for (int j = 0; j < 4; ++j) {
+        if (okm & (1u << j)) {
+          if (pos < cap) {
+            rk[pos] = key[u][j];
+            ri[pos] = (uint32_t)(i0 + j);
+          } else {
+            over = true;
+          }
+          ++pos;
         }
-        ++pos;
       }
+      count += __shfl_sync(0xffffffffu, x, 31);
     }
-    count += tot;
   }
-  if (threadIdx.x == 0) {
-    ccnt[b] = count < cap ? count : (uint32_t)cap;
+  if (lane == 0 && lo < N) {
+    ccnt[r] = count < cap ? count : (uint32_t)cap;
     atomicAdd(&c->total, (unsigned long long)count);
   }
   if (over) c->overflow = 1;
@@ -438,8 +456,8 @@ usaf_status run_select(const SelPlan& p, const SelWs& w, Src s, int64_t K, int64
     sel_sample_tau_kernel<<<1, 1024, 0, st>>>(w.samples, p.q, w.ctrl);
     USAF_CHECK_LAUNCH();
     const int vec_ok = (reinterpret_cast<uintptr_t>(s.g) & 15) == 0;
-    sel_compact_kernel<<<p.G, SEL_THREADS, 0, st>>>(s.g, s.n, p.L, s.excl, p.cap, w.ckeys,
-                                                    w.cids, w.ccnt, w.ctrl, vec_ok, dev_status);
+    sel_compact_kernel<<<p.G / COMPACT_WARPS, COMPACT_WARPS * 32, 0, st>>>(
+        s.g, s.n, p.L, s.excl, p.cap, w.ckeys, w.cids, w.ccnt, w.ctrl, vec_ok, dev_status);
     USAF_CHECK_LAUNCH();
   }
   USAF_TRACE("select_exact", st);
