@@ -216,7 +216,7 @@ usaf_status usaf_moe_fwd(const usaf_moe_shape* s, usaf_dtype dt, const void* x,
                          const void* w_gate_up, const void* w_down, const usaf_routing* rt,
                          void* x_perm_save, void* h_save, void* wa_save, void* y, void* ws,
                          size_t ws_bytes, void* stream) {
-  MoeArgs a;
+  MoeArgs a{};
   USAF_TRY(fill_args(a, s, dt, x, nullptr, w_gate_up, w_down, rt));
   if (!x_perm_save || !h_save || !wa_save || !y) return USAF_ERR_INVALID_ARG;
   if (!ws || ws_bytes < usaf_moe_fwd_workspace_size(s, dt)) return USAF_ERR_WORKSPACE;
@@ -242,7 +242,7 @@ usaf_status usaf_moe_bwd_sparse(const usaf_moe_shape* s, usaf_dtype dt, int reno
                                 const void* dy, const int64_t* act_idx, int64_t K, float* g_act,
                                 float* g_router, void* dx, float* dw_slot, uint32_t* dev_status,
                                 void* ws, size_t ws_bytes, void* stream) {
-  MoeArgs a;
+  MoeArgs a{};
   USAF_TRY(fill_args(a, s, dt, x, w_router, w_gate_up, w_down, rt));
   if (renorm != 0 && renorm != 1) return USAF_ERR_INVALID_ARG;
   if (!w_router || !x_perm_save || !h_save || !wa_save || !dy || !g_router)

@@ -22,6 +22,7 @@ usaf_status route_launch(const usaf_moe_shape& s, const void* x, usaf_dtype xdt,
 struct FwdWs {
   float* y_acc;  // [T,H] fp32 accumulator of the routing-weighted combine
   int32_t* plan; // [E+1] prefix of token tiles per expert (tensor-core path)
+  float* wperm;  // [R_cap] routing weight per permuted row
 };
 struct BwdWs {
   float* dw;          // [T*k] when the caller gives no dw_slot
@@ -32,6 +33,7 @@ struct BwdWs {
   float* dx_acc;      // [T,H]
   float* gvec;        // [R_cap, I] (fp32 path only)
   int32_t* plan;      // [E+1] prefix of token tiles per expert (tensor-core path)
+  float* wperm;       // [R_cap] routing weight per permuted row
   void* dy_perm;      // dy^T [H, R_cap]: dy in permuted order, feature-major
 };
 void fwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, Carver& c, FwdWs& w);
@@ -47,6 +49,7 @@ struct MoeArgs {
   const void* w_down;
   usaf_routing rt;
   int32_t* plan;  // token-tile prefix written by tc_plan (tensor-core path)
+  float* wperm;   // [R_cap] routing weight of each permuted row (0 in padding), by the gather
 };
 
 usaf_status moe_fwd_launch(const MoeArgs& a, void* x_perm, void* h, void* wa, void* y, FwdWs& w,

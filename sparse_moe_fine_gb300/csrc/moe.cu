@@ -225,7 +225,8 @@ constexpr int GT_ROWS = 128;
 template <typename T>
 __global__ void __launch_bounds__(256) gather_transpose_kernel(
     const T* __restrict__ x, const int32_t* __restrict__ ptok, const int32_t* __restrict__ pslot,
-    const int32_t* __restrict__ off_end, int64_t R_cap, int H, T* __restrict__ xT) {
+    const int32_t* __restrict__ off_end, int64_t R_cap, int H, T* __restrict__ xT,
+    const float* __restrict__ topk_w, float* __restrict__ wperm) {
   constexpr int VW = 16 / sizeof(T);  // elements per 16-byte vector
   // feature f's row of the tile is rotated by (f / VW) * VW columns: the column writes of the
   // load phase then fall in distinct banks, and the 16-byte reads of the store phase stay aligned
@@ -253,6 +254,14 @@ __global__ void __launch_bounds__(256) gather_transpose_kernel(
     for (int q = 0; q < VW; ++q) {
       const int ff = f + q;
       tile[ff * GT_ROWS + (r + (ff / VW) * VW) % GT_ROWS] = buf[q];
+    }
+  }
+  if (wperm && blockIdx.y == 0) {
+    for (int r = threadIdx.x; r < GT_ROWS; r += blockDim.x) {
+      const int64_t row = r0 + r;
+      if (row >= R_cap) break;
+      const int sl = row < end ? pslot[row] : -1;
+      wperm[row] = sl >= 0 ? topk_w[sl] : 0.f;
     }
   }
   __syncthreads();
@@ -701,6 +710,7 @@ __global__ void __launch_bounds__(256) dx_finalize_kernel(
 void fwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, Carver& c, FwdWs& w) {
   w.y_acc = c.take<float>(s.T * s.H);
   w.plan = dt == USAF_BF16 ? c.take<int32_t>(s.E + 1) : nullptr;
+  w.wperm = c.take<float>(usaf_routed_rows_capacity(&s));
 }
 
 void bwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, int64_t K, Carver& c, BwdWs& w) {
@@ -715,6 +725,7 @@ void bwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, int64_t K, Carver& c,
   w.dx_acc = c.take<float>(s.T * s.H);
   w.gvec = dt == USAF_F32 ? c.take<float>(R_cap * s.I) : nullptr;
   w.plan = dt == USAF_BF16 ? c.take<int32_t>(s.E + 1) : nullptr;
+  w.wperm = c.take<float>(R_cap);
   w.dy_perm = c.take<char>(R_cap * s.H * (int64_t)es);
 }
 
@@ -723,7 +734,7 @@ static usaf_status gather_t(const MoeArgs& a, const T* src, T* dstT, cudaStream_
   const dim3 grid((unsigned)ceil_div(a.R_cap, GT_ROWS), (unsigned)ceil_div(a.s.H, 64));
   gather_transpose_kernel<T><<<grid, 256, 0, st>>>(src, a.rt.perm_tok, a.rt.perm_slot,
                                                    a.rt.expert_offset + a.s.E, a.R_cap,
-                                                   (int)a.s.H, dstT);
+                                                   (int)a.s.H, dstT, a.rt.topk_w, a.wperm);
   USAF_CHECK_LAUNCH();
   return USAF_OK;
 }
@@ -755,14 +766,16 @@ static usaf_status moe_fwd_t(const MoeArgs& a, T* xT, T* hT, T* waT, T* y, FwdWs
                              cudaStream_t st) {
   const auto& s = a.s;
   const int64_t TH = s.T * s.H;
+  MoeArgs aw = a;
+  aw.wperm = w.wperm;
   {
     USAF_TRACE("gather_x", st);
-    USAF_TRY(gather_t<T>(a, static_cast<const T*>(a.x), xT, st));
+    USAF_TRY(gather_t<T>(aw, static_cast<const T*>(a.x), xT, st));
     zero_f32_kernel<<<grid_dim_for(TH), 256, 0, st>>>(w.y_acc, TH);
     USAF_CHECK_LAUNCH();
   }
   if (a.dt == USAF_BF16) {
-    MoeArgs b = a;
+    MoeArgs b = aw;
     b.plan = w.plan;
     USAF_TRY(tc_plan(b, st));
     USAF_TRY(tc_fwd_gate_up(b, xT, hT, waT, st));
@@ -794,6 +807,7 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
                              uint32_t* dev_status, BwdWs& w, cudaStream_t st) {
   MoeArgs a = a0;
   a.plan = w.plan;
+  a.wperm = w.wperm;
   const auto& s = a.s;
   const int H = (int)s.H, I = (int)s.I, E = (int)s.E, Tn = (int)s.T, k = (int)s.k;
   const int32_t* cnt = a.rt.expert_count;

@@ -59,6 +59,7 @@ struct Params {
   float* dw;              // S6
   __nv_bfloat16* dh;      // dh^T out (S6)
   const __nv_bfloat16* hin;  // h^T in (S6)
+  const float* wperm;        // routing weight per permuted row (0 in padding)
   uint32_t* status;
 };
 
@@ -265,9 +266,44 @@ __device__ __forceinline__ float bf_at(const uint32_t (&a)[16], int j) {
   return (j & 1) ? __uint_as_float(a[j >> 1] & 0xFFFF0000u) : __uint_as_float(a[j >> 1] << 16);
 }
 
+// Per-warp inputs of a tile's epilogue that do not depend on the accumulator, loaded before the
+// warp waits for it: for the warp's chunks c = 0..3 (columns (half + 2c) * 32 + lane) the slot,
+// token and routing weight of the column, and for S6 the gate/up values of the first chunk.
+struct EpiPre {
+  int slot[4];
+  int tok[4];
+  float w[4];
+  uint32_t hg[16], hu[16];
+};
+
+template <int VAR>
+__device__ __forceinline__ void epi_prefetch(const Params& p, const Tile& ti, int row, int lane,
+                                             int half, EpiPre& pre) {
+  if constexpr (!VarTraits<VAR>::router) {
+    const int nch = (ti.nrows + 31) / 32;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const int ch = half + 2 * c;
+      const int col = ch * 32 + lane;
+      const bool in = ch < nch && col < ti.nrows;
+      pre.slot[c] = in ? p.pslot[ti.row0 + col] : -1;
+      pre.tok[c] = in && (VAR == V_DOWN || VAR == V_DX) ? p.ptok[ti.row0 + col] : 0;
+      pre.w[c] = in && (VAR == V_GATEUP || VAR == V_GVEC) ? p.wperm[ti.row0 + col] : 0.f;
+    }
+    if constexpr (VAR == V_GVEC) {
+      const int i = ti.m0 + row;
+      const int ncol = min(32, ti.nrows - half * 32);
+      load_row32(p.hin + (int64_t)i * p.R_cap + ti.row0 + half * 32, i < p.I && half < nch, ncol,
+                 pre.hg);
+      load_row32(p.hin + (int64_t)(p.I + i) * p.R_cap + ti.row0 + half * 32,
+                 i < p.I && half < nch, ncol, pre.hu);
+    }
+  }
+}
+
 template <int VAR>
 __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32_t taddr, int row,
-                                         int lane, int half) {
+                                         int lane, int half, EpiPre& pre) {
   constexpr unsigned FULL = 0xffffffffu;
   const int H = p.H, I = p.I;
   const int nch = (ti.nrows + 31) / 32;
@@ -284,23 +320,19 @@ __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32
     }
     return;
   }
-  uint32_t hg[16], hu[16];  // V_GVEC: gate and up of the chunk being processed
-  if constexpr (VAR == V_GVEC) {
-    const int i = ti.m0 + row;
-    const int ncol = min(32, ti.nrows - half * 32);
-    load_row32(p.hin + (int64_t)i * p.R_cap + ti.row0 + half * 32, i < I && half < nch, ncol, hg);
-    load_row32(p.hin + (int64_t)(I + i) * p.R_cap + ti.row0 + half * 32, i < I && half < nch,
-               ncol, hu);
-  }
+  uint32_t (&hg)[16] = pre.hg;  // V_GVEC: gate and up of the chunk being processed
+  uint32_t (&hu)[16] = pre.hu;
   for (int ch = half; ch < nch; ch += 2) {
     const int cbase = ch * 32;
-    const int col = cbase + lane;
-    int slot = -1, tok = 0;
-    if (col < ti.nrows) {
-      slot = p.pslot[ti.row0 + col];
-      tok = p.ptok[ti.row0 + col];
+    // this chunk's column inputs, then the next chunk's moved up
+    const int slot = pre.slot[0], tok = pre.tok[0];
+    const float wl = pre.w[0];
+#pragma unroll
+    for (int c = 0; c < 3; ++c) {
+      pre.slot[c] = pre.slot[c + 1];
+      pre.tok[c] = pre.tok[c + 1];
+      pre.w[c] = pre.w[c + 1];
     }
-    const float wl = slot >= 0 ? p.topk_w[slot] : 0.f;
     const int ncol = min(32, ti.nrows - cbase);
     if constexpr (VAR == V_GATEUP) {
       float v[32];
@@ -556,12 +588,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
       const Tile ti = get_tile<VAR>(p, s_plan, s_off, t);
+      EpiPre pre;
+      epi_prefetch<VAR>(p, ti, row, lane, half, pre);
       int ok = 1;
       if (lane == 0) ok = mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
-      epilogue<VAR>(p, ti, tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN, row, lane, half);
+      epilogue<VAR>(p, ti, tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN, row, lane, half,
+                    pre);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
@@ -701,6 +736,7 @@ Params base_params(const MoeArgs& a) {
   p.pslot = a.rt.perm_slot;
   p.topk_w = a.rt.topk_w;
   p.plan = a.plan;
+  p.wperm = a.wperm;
   p.E = (int)a.s.E;
   p.H = (int)a.s.H;
   p.I = (int)a.s.I;
