@@ -180,7 +180,7 @@ struct VarTraits {
   static constexpr bool router = VAR == V_ROUTER;
   static constexpr bool a_mn = VAR == V_GVEC || VAR == V_DX;
 };
-constexpr int ROUTER_BN = 128;
+constexpr int ROUTER_BN = 32;  // tokens per router tile: T / 32 tiles keep most SMs busy
 
 __device__ __forceinline__ int upper_bound_i32(const int32_t* a, int n, int v) {
   int lo = 0, hi = n;
@@ -647,20 +647,23 @@ __global__ void __launch_bounds__(1024) token_plan_kernel(const int32_t* __restr
 
 // Router weight split for the tensor-core logits: w = hi + mid + lo, each part bf16 and each
 // residual exact in fp32, so x . w is carried by three bf16 products with fp32 accumulation.
-__global__ void router_split_kernel(const float* __restrict__ wr, int64_t E, int64_t H,
+__global__ void router_split_kernel(const float* __restrict__ wr, int H,
                                     __nv_bfloat16* __restrict__ wr3) {
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < E * H;
-       i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t e = i / H, k = i % H;
-    const float w = wr[i];
-    const __nv_bfloat16 hi = __float2bfloat16_rn(w);
-    const float r1 = w - __bfloat162float(hi);
-    const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
-    const float r2 = r1 - __bfloat162float(mid);
-    __nv_bfloat16* row = wr3 + e * 3 * H;
-    row[k] = hi;
-    row[H + k] = mid;
-    row[2 * H + k] = __float2bfloat16_rn(r2);
+  // block row e of Wr, two columns per thread (H is a multiple of 64 on this path)
+  const int e = blockIdx.y;
+  const float* src = wr + (int64_t)e * H;
+  __nv_bfloat16* row = wr3 + (int64_t)e * 3 * H;
+  for (int k = (blockIdx.x * blockDim.x + threadIdx.x) * 2; k < H; k += gridDim.x * blockDim.x * 2) {
+    const float2 w = *reinterpret_cast<const float2*>(src + k);
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(w.x, w.y);
+    const float2 hf = __bfloat1622float2(hi);
+    const float2 r1 = make_float2(w.x - hf.x, w.y - hf.y);
+    const __nv_bfloat162 mid = __floats2bfloat162_rn(r1.x, r1.y);
+    const float2 mf = __bfloat1622float2(mid);
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(r1.x - mf.x, r1.y - mf.y);
+    *reinterpret_cast<__nv_bfloat162*>(row + k) = hi;
+    *reinterpret_cast<__nv_bfloat162*>(row + H + k) = mid;
+    *reinterpret_cast<__nv_bfloat162*>(row + 2 * H + k) = lo;
   }
 }
 
@@ -763,12 +766,12 @@ usaf_status tc_router_logits(const usaf_moe_shape& s, const void* x, const float
                              void* wr3, float* logits, cudaStream_t st) {
   {
     USAF_TRACE("router_split", st);
-    router_split_kernel<<<grid_dim_for(s.E * s.H), 256, 0, st>>>(
-        wr, s.E, s.H, static_cast<__nv_bfloat16*>(wr3));
+    const dim3 grid((unsigned)ceil_div(s.H, 512), (unsigned)s.E);
+    router_split_kernel<<<grid, 256, 0, st>>>(wr, (int)s.H, static_cast<__nv_bfloat16*>(wr3));
     USAF_CHECK_LAUNCH();
   }
   CUtensorMap ma, mb;
-  if (!map_2d(&ma, wr3, 3 * s.H, s.E, 64, 128) || !map_2d(&mb, x, s.H, s.T, 64, 128))
+  if (!map_2d(&ma, wr3, 3 * s.H, s.E, 64, 128) || !map_2d(&mb, x, s.H, s.T, 64, ROUTER_BN))
     return USAF_ERR_CUDA;
   Params p{};
   p.E = (int)s.E;

@@ -20,6 +20,7 @@ namespace {
 
 constexpr int SEL_THREADS = 256;
 constexpr int COMPACT_WARPS = 8;  // warps per block of the compacting pass, one region each
+constexpr int ROUND_THREADS = 256;  // radix rounds: eight blocks per SM, parts taken in turn
 constexpr int SAMPLE_S = 32768;
 // radix rounds over the 31-bit key, most significant digit first: bits 30..23, 22..15, 14..7, 6..0
 __host__ __device__ constexpr int round_shift(int r) { return r == 0 ? 23 : r == 1 ? 15 : r == 2 ? 7 : 0; }
@@ -48,6 +49,7 @@ struct Src {
   const uint32_t* ccnt;
   int64_t cap;
   int drop;                // 1: keys are complemented |p| (mode 2 source)
+  int G;                   // parts (regions)
 };
 
 struct SelPlan {
@@ -202,11 +204,18 @@ __global__ void sel_sample_kernel(const float* __restrict__ g, int64_t N,
   samples[i] = excluded(excl, pos) ? 0u : abs_key(g[pos]);
 }
 
-// One block: the q-th largest sample (1-based) by 4 digit rounds; tau0 := that key.
+// One block: the q-th largest sample (1-based) by 4 digit rounds; tau0 := that key. Each thread
+// keeps its 32 samples in registers; every warp counts digits into its own shared histogram.
 __global__ void __launch_bounds__(1024) sel_sample_tau_kernel(const uint32_t* __restrict__ samples,
                                                               int q, SelCtrl* c) {
+  constexpr int PER = SAMPLE_S / 1024;
+  __shared__ uint32_t wh[32][257];
   __shared__ uint32_t hist[256];
   __shared__ uint32_t s_prefix, s_krem;
+  const int wid = threadIdx.x >> 5;
+  uint32_t key[PER];
+#pragma unroll
+  for (int j = 0; j < PER; ++j) key[j] = samples[j * 1024 + threadIdx.x];
   if (threadIdx.x == 0) {
     s_prefix = 0;
     s_krem = (uint32_t)q;
@@ -214,17 +223,20 @@ __global__ void __launch_bounds__(1024) sel_sample_tau_kernel(const uint32_t* __
   for (int r = 0; r < 4; ++r) {
     const int shift = round_shift(r), bits = round_bits(r);
     const uint32_t dmask = (1u << bits) - 1;
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+    for (int i = threadIdx.x; i < 32 * 257; i += blockDim.x) (&wh[0][0])[i] = 0;
     __syncthreads();
     const uint32_t prefix = s_prefix;
     const int hs = shift + bits;
-    for (int i0 = 0; i0 < SAMPLE_S; i0 += blockDim.x) {
-      const int i = i0 + threadIdx.x;
-      const uint32_t key = samples[i];
-      const bool m = hs >= 32 || (key >> hs) == (prefix >> hs);
-      const int d = m ? (int)((key >> shift) & dmask) : -1 - (int)(threadIdx.x & 31);
-      const unsigned peers = __match_any_sync(0xffffffffu, d);
-      if (m && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[d], __popc(peers));
+#pragma unroll
+    for (int j = 0; j < PER; ++j)
+      if (hs >= 32 || (key[j] >> hs) == (prefix >> hs))
+        atomicAdd(&wh[wid][(key[j] >> shift) & dmask], 1u);
+    __syncthreads();
+    if (threadIdx.x < 256) {
+      uint32_t t = 0;
+#pragma unroll 8
+      for (int w = 0; w < 32; ++w) t += wh[w][threadIdx.x];
+      hist[threadIdx.x] = t;
     }
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -242,14 +254,28 @@ __global__ void __launch_bounds__(1024) sel_sample_tau_kernel(const uint32_t* __
   if (threadIdx.x == 0) c->tau0 = s_prefix;
 }
 
+// Four consecutive elements of g from i0 (zeros past hi), one 16-byte load when possible.
+__device__ __forceinline__ float4 load4(const float* __restrict__ g, int64_t i0, int64_t hi,
+                                        int vec_ok) {
+  if (vec_ok && i0 + 3 < hi) return __ldcs(reinterpret_cast<const float4*>(g + i0));
+  float4 v;
+  v.x = i0 < hi ? g[i0] : 0.f;
+  v.y = i0 + 1 < hi ? g[i0 + 1] : 0.f;
+  v.z = i0 + 2 < hi ? g[i0 + 2] : 0.f;
+  v.w = i0 + 3 < hi ? g[i0 + 3] : 0.f;
+  return v;
+}
+
 // The one pass over g: every warp compacts the (key, index) pairs with key >= tau0 (and not
-// excluded) of its own contiguous part of g into its own region, in index order. Four float4
-// loads per lane are in flight; a warp scan places the candidates only when some lane has one.
+// excluded) of its own contiguous part of g into its own region, in index order. The loads of the
+// next 512 elements are issued before the current 512 are examined; a warp scan places the
+// candidates only when some lane has one.
 __global__ void __launch_bounds__(COMPACT_WARPS * 32) sel_compact_kernel(
     const float* __restrict__ g, int64_t N, int64_t L, const uint32_t* __restrict__ excl,
     int64_t cap, uint32_t* __restrict__ ckeys, uint32_t* __restrict__ cids,
     uint32_t* __restrict__ ccnt, SelCtrl* c, int vec_ok, uint32_t* dev_status) {
   constexpr int UN = 4;
+  constexpr int STEP = 128 * UN;
   const uint32_t tau0 = c->tau0;
   const int lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * COMPACT_WARPS + (threadIdx.x >> 5);
@@ -257,35 +283,41 @@ __global__ void __launch_bounds__(COMPACT_WARPS * 32) sel_compact_kernel(
   const int64_t hi = min(N, lo + L);
   uint32_t* rk = ckeys + r * cap;
   uint32_t* ri = cids + r * cap;
-  uint32_t count = 0;
-  bool over = false, bad = false;
-  for (int64_t t0 = lo; t0 < hi; t0 += 128 * UN) {
-    uint32_t key[UN][4];
+  uint32_t count = 0, kmax = 0;  // kmax: largest key seen, for the non-finite check
+  bool over = false;
+  float4 nxt[UN];
+#pragma unroll
+  for (int u = 0; u < UN; ++u) nxt[u] = load4(g, lo + u * 128 + lane * 4, hi, vec_ok);
+  for (int64_t t0 = lo; t0 < hi; t0 += STEP) {
+    float4 cur[UN];
+#pragma unroll
+    for (int u = 0; u < UN; ++u) cur[u] = nxt[u];
+    if (t0 + STEP < hi) {
+#pragma unroll
+      for (int u = 0; u < UN; ++u) nxt[u] = load4(g, t0 + STEP + u * 128 + lane * 4, hi, vec_ok);
+    }
+    const bool full = t0 + STEP <= hi && excl == nullptr;  // no range or exclusion tests
 #pragma unroll
     for (int u = 0; u < UN; ++u) {
       const int64_t i0 = t0 + u * 128 + lane * 4;
-      if (vec_ok && i0 + 3 < hi) {
-        const float4 v = __ldcs(reinterpret_cast<const float4*>(g + i0));
-        key[u][0] = abs_key(v.x);
-        key[u][1] = abs_key(v.y);
-        key[u][2] = abs_key(v.z);
-        key[u][3] = abs_key(v.w);
+      const uint32_t key[4] = {abs_key(cur[u].x), abs_key(cur[u].y), abs_key(cur[u].z),
+                               abs_key(cur[u].w)};
+      uint32_t okm = 0;
+      if (full) {
+        const uint32_t m4 = max(max(key[0], key[1]), max(key[2], key[3]));
+        kmax = max(kmax, m4);
+        if (!__any_sync(0xffffffffu, m4 >= tau0)) continue;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) okm |= (uint32_t)(key[j] >= tau0) << j;
       } else {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) key[u][j] = i0 + j < hi ? abs_key(g[i0 + j]) : 0u;
+        for (int j = 0; j < 4; ++j) {
+          const bool in = i0 + j < hi;
+          if (in) kmax = max(kmax, key[j]);
+          if (in && key[j] >= tau0 && !excluded(excl, i0 + j)) okm |= 1u << j;
+        }
+        if (!__any_sync(0xffffffffu, okm != 0)) continue;
       }
-    }
-#pragma unroll
-    for (int u = 0; u < UN; ++u) {
-      const int64_t i0 = t0 + u * 128 + lane * 4;
-      uint32_t okm = 0;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const bool in = i0 + j < hi;
-        bad |= in && key[u][j] >= 0x7F800000u;
-        if (in && key[u][j] >= tau0 && !excluded(excl, i0 + j)) okm |= 1u << j;
-      }
-      if (!__any_sync(0xffffffffu, okm != 0)) continue;
       const uint32_t mine = __popc(okm);
       uint32_t x = mine;
 #pragma unroll
@@ -298,7 +330,7 @@ __global__ void __launch_bounds__(COMPACT_WARPS * 32) sel_compact_kernel(
       for (int j = 0; j < 4; ++j) {
         if (okm & (1u << j)) {
           if (pos < cap) {
-            rk[pos] = key[u][j];
+            rk[pos] = key[j];
             ri[pos] = (uint32_t)(i0 + j);
           } else {
             over = true;
@@ -314,7 +346,7 @@ __global__ void __launch_bounds__(COMPACT_WARPS * 32) sel_compact_kernel(
     atomicAdd(&c->total, (unsigned long long)count);
   }
   if (over) c->overflow = 1;
-  flag_status_warp(dev_status, bad, USAF_DEV_NONFINITE);
+  flag_status_warp(dev_status, kmax >= 0x7F800000u, USAF_DEV_NONFINITE);
 }
 
 __global__ void sel_decide_kernel(SelCtrl* c, int64_t K, int sampling, uint32_t* dev_status) {
@@ -325,7 +357,7 @@ __global__ void sel_decide_kernel(SelCtrl* c, int64_t K, int sampling, uint32_t*
 }
 
 // One radix round over the source. The last block to finish picks the digit.
-__global__ void __launch_bounds__(SEL_THREADS) sel_round_kernel(Src s, SelCtrl* c, int shift,
+__global__ void __launch_bounds__(ROUND_THREADS) sel_round_kernel(Src s, SelCtrl* c, int shift,
                                                                 int bits, int fixed_mode) {
   __shared__ uint32_t hist[256];
   __shared__ bool last;
@@ -335,7 +367,8 @@ __global__ void __launch_bounds__(SEL_THREADS) sel_round_kernel(Src s, SelCtrl* 
   const uint32_t prefix = c->prefix;
   for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
   __syncthreads();
-  for_part(s, mode, blockIdx.x, [&](uint32_t key, int64_t, bool ok) {
+  for (int b = blockIdx.x; b < s.G; b += gridDim.x)
+  for_part(s, mode, b, [&](uint32_t key, int64_t, bool ok) {
     const bool m = ok && (hs >= 32 || (key >> hs) == (prefix >> hs));
     const int d = m ? (int)((key >> shift) & dmask) : -1 - (int)(threadIdx.x & 31);
     const unsigned peers = __match_any_sync(0xffffffffu, d);
@@ -450,17 +483,19 @@ usaf_status run_select(const SelPlan& p, const SelWs& w, Src s, int64_t K, int64
     USAF_CHECK_LAUNCH();
   }
   if (p.sampling && !fixed_drop) {
-    USAF_TRACE("select_sample_compact", st);
-    sel_sample_kernel<<<SAMPLE_S / 256, 256, 0, st>>>(s.g, s.n, s.excl, w.samples);
-    USAF_CHECK_LAUNCH();
-    sel_sample_tau_kernel<<<1, 1024, 0, st>>>(w.samples, p.q, w.ctrl);
-    USAF_CHECK_LAUNCH();
+    {
+      USAF_TRACE("select_sample", st);
+      sel_sample_kernel<<<SAMPLE_S / 256, 256, 0, st>>>(s.g, s.n, s.excl, w.samples);
+      USAF_CHECK_LAUNCH();
+      sel_sample_tau_kernel<<<1, 1024, 0, st>>>(w.samples, p.q, w.ctrl);
+      USAF_CHECK_LAUNCH();
+    }
+    USAF_TRACE("select_compact", st);
     const int vec_ok = (reinterpret_cast<uintptr_t>(s.g) & 15) == 0;
     sel_compact_kernel<<<p.G / COMPACT_WARPS, COMPACT_WARPS * 32, 0, st>>>(
         s.g, s.n, p.L, s.excl, p.cap, w.ckeys, w.cids, w.ccnt, w.ctrl, vec_ok, dev_status);
     USAF_CHECK_LAUNCH();
   }
-  USAF_TRACE("select_exact", st);
   sel_decide_kernel<<<1, 32, 0, st>>>(w.ctrl, K, p.sampling && !fixed_drop ? 1 : 0, dev_status);
   USAF_CHECK_LAUNCH();
   s.ckeys = w.ckeys;
@@ -468,10 +503,17 @@ usaf_status run_select(const SelPlan& p, const SelWs& w, Src s, int64_t K, int64
   s.ccnt = w.ccnt;
   s.cap = p.cap;
   const int fm = fixed_drop ? 2 : -1;
-  for (int r = 0; r < 4; ++r) {
-    sel_round_kernel<<<p.G, SEL_THREADS, 0, st>>>(s, w.ctrl, round_shift(r), round_bits(r), fm);
-    USAF_CHECK_LAUNCH();
+  s.G = p.G;
+  const int rgrid = (int)std::min<int64_t>(p.G, device_sm_count() * 8);
+  {
+    USAF_TRACE("select_radix", st);
+    for (int r = 0; r < 4; ++r) {
+      sel_round_kernel<<<rgrid, ROUND_THREADS, 0, st>>>(s, w.ctrl, round_shift(r), round_bits(r),
+                                                        fm);
+      USAF_CHECK_LAUNCH();
+    }
   }
+  USAF_TRACE("select_write", st);
   sel_count_kernel<<<p.G, SEL_THREADS, 0, st>>>(s, w.ctrl, w.blk_gt, w.blk_eq, fm);
   USAF_CHECK_LAUNCH();
   sel_scan_kernel<<<1, 1024, 0, st>>>(w.blk_gt, w.blk_eq, p.G, w.base_gt, w.base_eq);
