@@ -316,7 +316,11 @@ def run(args):
 
 def run_steps(args, B, MoELayer, dist, ws, rank, local, dev, cfg, inp, x, dy, wgu, wd, wr, act,
               importance, hbm, tf_burst, tf_sus, peak_src, stream):
-    layer = MoELayer(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, wgu, wd, wr, act, lr=cfg.lr, device=dev)
+    # data parallel over ranks: each rank steps on its own T tokens; the compact gradients are
+    # summed over the ranks before SparseAdam (one all-reduce per step)
+    group = dist.group.WORLD if dist is not None else None
+    layer = MoELayer(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, wgu, wd, wr, act, lr=cfg.lr, device=dev,
+                     group=group)
     # ---- train steps
     for _ in range(args.warmup):
         layer.status.zero_()
@@ -433,7 +437,8 @@ def make_line(args, cfg, ws, ms, value, step_roof_ms, fl, by, roof, trace, tot, 
         "config": {"workload": f"{WORKLOAD} layer step", "T": cfg.T, "H": cfg.H, "E": cfg.E,
                    "k": cfg.k, "I": cfg.I, "active": cfg.K, "router": "fp32",
                    "optimizer": "SparseAdam (experts at the active set, router dense)",
-                   "parallelism": f"replicas x{ws}",
+                   "parallelism": f"dp{ws}" + (" (all-reduce of the compact gradients)"
+                                               if ws > 1 else ""),
                    "l2": "inputs larger than L2 (1.2 GB of expert weights per step)"},
         "step_roofline": {"ms": step_roof_ms, "frac": step_roof_ms / ms,
                           "algorithmic_gflop": fl / 1e9, "algorithmic_gb": by / 1e9},

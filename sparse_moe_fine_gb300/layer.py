@@ -6,6 +6,11 @@ A train step is: route (router logits, top-k, permutation) -> grouped SwiGLU for
 backward (router gradient, input gradient, expert gradients at the active set) -> SparseAdam on
 the active expert entries -> SparseAdam on the router (USAF README: the router is trained in
 full, expert weights at a 0.5% active set, both under SparseAdam).
+
+Data parallel (the README's DataParallel mode): every rank holds the same weights and active set
+and runs the step on its own tokens; before the optimizer, one all-reduce sums the compact
+gradients (K active expert entries and the E*H router entries) and one takes the maximum of the
+status words, so every replica applies the same update or skips the same step.
 """
 from __future__ import annotations
 
@@ -16,9 +21,25 @@ import torch
 from . import binding as B
 
 
+STATUS_BITS = 3  # USAF_DEV_NONFINITE, USAF_DEV_SELECT_EXACT_PATH, USAF_DEV_TIMEOUT
+
+
+def allreduce_grads(g_act, g_router, status, group=None):
+    """Sum the compact gradients over the ranks of `group` and OR their status words, in place, on
+    the current stream. The loss is a sum over tokens, so the sum of the ranks' gradients is the
+    gradient of the whole batch; the OR makes a non-finite value seen by any rank skip the step on
+    every rank. (The OR is taken bit by bit as a maximum, which every backend reduces.)"""
+    import torch.distributed as dist
+    dist.all_reduce(g_act, op=dist.ReduceOp.SUM, group=group)
+    dist.all_reduce(g_router, op=dist.ReduceOp.SUM, group=group)
+    bits = torch.stack([(status >> b) & 1 for b in range(STATUS_BITS)])
+    dist.all_reduce(bits, op=dist.ReduceOp.MAX, group=group)
+    status.copy_(sum(bits[b] << b for b in range(STATUS_BITS)))
+
+
 class MoELayer:
     def __init__(self, T, H, E, k, I, w_gate_up, w_down, w_router, act_idx, lr=1e-4,
-                 betas=(0.9, 0.999), eps=1e-8, renorm=1, device="cuda"):
+                 betas=(0.9, 0.999), eps=1e-8, renorm=1, device="cuda", group=None):
         self.dev = torch.device(device)
         self.s = B.shape(T, H, E, k, I)
         self.T, self.H, self.E, self.k, self.I = T, H, E, k, I
@@ -30,6 +51,7 @@ class MoELayer:
         self.N_gu = E * 2 * I * H
         self.N = E * 3 * I * H
         self.lr, self.betas, self.eps, self.renorm = lr, betas, eps, renorm
+        self.group = group  # data-parallel process group (None: one replica)
         self.step_count = 0
         d = self.dev
         cap = B.routed_rows_capacity(self.s)
@@ -114,6 +136,9 @@ class MoELayer:
         self.step_count += 1
         b1, b2 = self.betas
         main = self._main(stream)
+        if self.group is not None:
+            with torch.cuda.stream(main):
+                allreduce_grads(self.g_act, self.g_router, self.status, self.group)
         self.ev_bwd.record(main)
         self.side.wait_event(self.ev_bwd)
         B.sparse_adam_step(self.act, self.g_act, self.p, self.m, self.v, self.w_gate_up,
