@@ -90,6 +90,30 @@ def kernel_units(cfg, sddmm_pairs=None):
     }
 
 
+# DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of one ncu capture of the
+# kernel on this workload (profiles/), with the SHA-256 of the source file at capture time; a
+# kernel whose source has changed since reports traffic null.
+NCU_TRAFFIC = {
+    "wgrad_sddmm": (452837120 + 13896448, "sparse_moe_fine_gb300/csrc/moe.cu",
+                    "2c5c5d31bc4b873a5c59e0d85d1b12eb52ea50329544c334bcc3baa480ca983c"),
+    "tc_gate_up_swiglu": (946959616 + 138687744, "sparse_moe_fine_gb300/csrc/moe_tc.cu",
+                          "13c915398fc197dfc1f8f6d2063a5ea33b5af04137efec1a5e5273c94aa0a3a2"),
+}
+
+
+def ncu_traffic(name):
+    if name not in NCU_TRAFFIC:
+        return None
+    nbytes, src, sha = NCU_TRAFFIC[name]
+    import hashlib
+    try:
+        with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), src), "rb") as f:
+            cur = hashlib.sha256(f.read()).hexdigest()
+    except OSError:
+        return None
+    return nbytes if cur == sha else None
+
+
 def sddmm_pairs(layer, cfg):
     """Sum over active entries of the routed-token count of the entry's expert."""
     cnt = layer.rt.expert_count.to(torch.int64)
@@ -368,7 +392,7 @@ def run_steps(args, B, MoELayer, dist, ws, rank, local, dev, cfg, inp, x, dy, wg
     else:
         roof = {"bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"] if roof["achieved"] else None
-    roof.update({"kernel": name, "kernel_ms": avg_ms, "traffic": None,
+    roof.update({"kernel": name, "kernel_ms": avg_ms, "traffic": ncu_traffic(name),
                  "peak_source": peak_src, "share": tms / tot if tot else None})
     fl, by = algorithmic(cfg)
     step_roof_ms = max(fl / (tf_sus * 1e12), by / (hbm * 1e9)) * 1e3
@@ -417,6 +441,9 @@ def e2e_time(args, layer, x, dy, e0, e1, stream, dist, dev):
 
 def kernel_entry(n, l, t, tot, units, hbm, tf_burst):
     e = {"name": n, "launches": l, "ms": t, "share": t / tot}
+    tr = ncu_traffic(n)
+    if tr is not None:
+        e["traffic"] = tr
     if n in units:
         fl, by = units[n]
         avg_s = t / l / 1e3
