@@ -38,7 +38,11 @@ constexpr int EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr int TMEM_COLS = 512;
 constexpr int MAX_E = 1024;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256 + 2 * (MAX_E + 1) * 4;
+constexpr int PLAN_BYTES = 8704;  // barriers, TMEM slot, abort flag, plan and offsets (E <= 1024)
+constexpr int STAGE_PITCH = 80;   // bytes per row of an epilogue warp's store staging (64 + 16)
+constexpr int EPI_STAGE_BYTES = 32 * STAGE_PITCH;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + PLAN_BYTES + EPI_WARPS * EPI_STAGE_BYTES;
+static_assert(256 + 2 * (MAX_E + 1) * 4 <= PLAN_BYTES, "plan area");
 static_assert(SMEM_BYTES <= 232448, "shared memory of the tensor-core kernel");
 constexpr long long TIMEOUT_CYCLES = 1ll << 32;  // about two seconds
 
@@ -262,6 +266,35 @@ __device__ __forceinline__ void load_row32(const __nv_bfloat16* row, bool ok, in
   }
 }
 
+// Writes up to 32 rows of 32 bf16 tokens (16 words per row, the row held by one lane) with whole
+// 32-byte sectors: each lane puts its row (staging row `srow`, or none when srow < 0) into the
+// warp's shared staging area, then lane 4r + q writes the q-th 16 bytes of staging rows r, r + 8,
+// ... to row_addr(row) (skipped when it returns null). The first `ncol` tokens are written (ncol a
+// multiple of 8). The 80-byte pitch keeps both phases free of bank conflicts.
+template <class RowAddr>
+__device__ __forceinline__ void store_rows_staged(uint8_t* stage, int lane, int srow,
+                                                  const uint32_t (&w)[16], int nrows, int ncol,
+                                                  RowAddr row_addr) {
+  if (srow >= 0) {
+    uint4* d = reinterpret_cast<uint4*>(stage + srow * STAGE_PITCH);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) d[q] = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+  }
+  __syncwarp();
+  const int r = lane >> 2, q = lane & 3;
+#pragma unroll 1
+  for (int r0 = 0; r0 < nrows; r0 += 8) {
+    const int rr = r0 + r;
+    if (rr < nrows && q * 8 < ncol) {
+      __nv_bfloat16* dst = row_addr(rr);
+      if (dst)
+        *reinterpret_cast<uint4*>(dst + q * 8) =
+            *reinterpret_cast<const uint4*>(stage + rr * STAGE_PITCH + q * 16);
+    }
+  }
+  __syncwarp();
+}
+
 __device__ __forceinline__ float bf_at(const uint32_t (&a)[16], int j) {
   return (j & 1) ? __uint_as_float(a[j >> 1] & 0xFFFF0000u) : __uint_as_float(a[j >> 1] << 16);
 }
@@ -303,7 +336,7 @@ __device__ __forceinline__ void epi_prefetch(const Params& p, const Tile& ti, in
 
 template <int VAR>
 __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32_t taddr, int row,
-                                         int lane, int half, EpiPre& pre) {
+                                         int lane, int half, EpiPre& pre, uint8_t* stage) {
   constexpr unsigned FULL = 0xffffffffu;
   const int H = p.H, I = p.I;
   const int nch = (ti.nrows + 31) / 32;
@@ -339,7 +372,14 @@ __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32
       tmem_ld32(taddr + ch * 32, v);
       const int i = ti.m0 + (row >> 1);
       const int g = row & 1;  // rows alternate gate (even lane) and up (odd lane) of feature i
-      store_row32(p.h + (int64_t)(g * I + i) * p.R_cap + ti.row0 + cbase, v, ncol);
+      const int i0 = ti.m0 + ((row - lane) >> 1);  // feature of the warp's first row pair
+      __nv_bfloat16* hbase = p.h + ti.row0 + cbase;
+      uint32_t w16[16];
+#pragma unroll
+      for (int t = 0; t < 16; ++t) w16[t] = pack_bf16x2(v[2 * t], v[2 * t + 1]);
+      store_rows_staged(stage, lane, lane, w16, 32, ncol, [&](int rr) {
+        return hbase + (int64_t)((rr & 1) * I + i0 + (rr >> 1)) * p.R_cap;
+      });
       float wa[32];
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -347,18 +387,24 @@ __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32
         const float gate = g ? other : v[j], up = g ? v[j] : other;
         wa[j] = __shfl_sync(FULL, wl, j) * gate * sigmoid_fast(gate) * up;
       }
-      // both lanes of the pair hold w*A of feature i; the even lane stores it
-      if (g == 0) store_row32(p.wa + (int64_t)i * p.R_cap + ti.row0 + cbase, wa, ncol);
+      // both lanes of the pair hold w*A of feature i; the even lane's row is stored
+#pragma unroll
+      for (int t = 0; t < 16; ++t) w16[t] = pack_bf16x2(wa[2 * t], wa[2 * t + 1]);
+      __nv_bfloat16* wbase = p.wa + ti.row0 + cbase;
+      store_rows_staged(stage, lane, g == 0 ? (lane >> 1) : -1, w16, 16, ncol, [&](int rr) {
+        return wbase + (int64_t)(i0 + rr) * p.R_cap;
+      });
+      (void)i;
     } else if constexpr (VAR == V_DOWN || VAR == V_DX) {
       float v[32];
       tmem_ld32(taddr + ch * 32, v);
       const int hh = ti.m0 + row;
+      const int tokv = slot >= 0 ? tok : -1;  // the column's token, -1 for a padding row
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         if (j >= ncol) break;
-        const int sj = __shfl_sync(FULL, slot, j);
-        const int tj = __shfl_sync(FULL, tok, j);
-        if (sj >= 0 && hh < H) atomicAdd(&p.acc_out[(int64_t)tj * H + hh], v[j]);
+        const int tj = __shfl_sync(FULL, tokv, j);
+        if (tj >= 0 && hh < H) atomicAdd(&p.acc_out[(int64_t)tj * H + hh], v[j]);
       }
     } else {  // V_GVEC: SwiGLU backward, dh^T and the routing-weight gradient dw
       const int i = ti.m0 + row;
@@ -390,16 +436,15 @@ __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32
         pg[j2] = pack_bf16x2(dgv[0], dgv[1]);
         pu[j2] = pack_bf16x2(duv[0], duv[1]);
       }
-      if (iv) {
-        uint4* dg4 = reinterpret_cast<uint4*>(p.dh + (int64_t)i * p.R_cap + ti.row0 + cbase);
-        uint4* du4 = reinterpret_cast<uint4*>(p.dh + (int64_t)(I + i) * p.R_cap + ti.row0 + cbase);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (q * 8 < ncol) {
-            dg4[q] = make_uint4(pg[4 * q], pg[4 * q + 1], pg[4 * q + 2], pg[4 * q + 3]);
-            du4[q] = make_uint4(pu[4 * q], pu[4 * q + 1], pu[4 * q + 2], pu[4 * q + 3]);
-          }
-        }
+      {
+        const int ib = ti.m0 + row - lane;  // feature of the warp's first row
+        __nv_bfloat16* dbase = p.dh + ti.row0 + cbase;
+        store_rows_staged(stage, lane, lane, pg, 32, ncol, [&](int rr) -> __nv_bfloat16* {
+          return ib + rr < I ? dbase + (int64_t)(ib + rr) * p.R_cap : nullptr;
+        });
+        store_rows_staged(stage, lane, lane, pu, 32, ncol, [&](int rr) -> __nv_bfloat16* {
+          return ib + rr < I ? dbase + (int64_t)(I + ib + rr) * p.R_cap : nullptr;
+        });
       }
       const float dwsum = transpose_reduce32(v, lane);
       if (slot >= 0) atomicAdd(&p.dw[slot], dwsum);
@@ -428,6 +473,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int32_t* s_plan = reinterpret_cast<int32_t*>(smem + STAGES * STAGE_BYTES + 256);
   int32_t* s_off = s_plan + (MAX_E + 1);
+  uint8_t* epi_stage = smem + STAGES * STAGE_BYTES + PLAN_BYTES;  // EPI_WARPS x EPI_STAGE_BYTES
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES;
@@ -596,7 +642,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       epilogue<VAR>(p, ti, tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN, row, lane, half,
-                    pre);
+                    pre, epi_stage + (warp - 2) * EPI_STAGE_BYTES);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
