@@ -349,3 +349,32 @@ def rigl_swap(act_idx, p, m, v, g, D, dense_weight_at):
     n_swapped = int(K - np.intersect1d(act_idx, new_idx).size)
     del pos
     return new_idx[order], p_new[order], m_new[order], v_new[order], n_swapped
+
+
+def reselect_full(act_idx, p, m, v, g, K_new, dense_weight_at):
+    """Full reselection by re-ranking (USAF README, "Sparsity adapts": the active set is chosen
+    again from fresh gradient magnitudes; the README reports about 92% turnover at the first
+    reselections, which a full re-rank allows and a fixed-fraction swap does not):
+
+    S' = the K_new entries with the largest |g| (ties: lower flat index first), sorted. Entries in
+    both S and S' keep (p, m, v); entries new to S' get p = dense weight value, m = v = 0.
+    Returns (new_idx, p', m', v', n_kept)."""
+    act_idx = np.asarray(act_idx, np.int64)
+    new_idx = importance_select(g, K_new)
+    p = np.asarray(p, np.float32)
+    m = np.asarray(m, np.float32)
+    v = np.asarray(v, np.float32)
+    old_pos = {int(f): i for i, f in enumerate(act_idx)}
+    p_new = np.empty(K_new, np.float32)
+    m_new = np.zeros(K_new, np.float32)
+    v_new = np.zeros(K_new, np.float32)
+    fresh = [t for t, f in enumerate(new_idx) if int(f) not in old_pos]
+    kept = [t for t, f in enumerate(new_idx) if int(f) in old_pos]
+    for t in kept:
+        i = old_pos[int(new_idx[t])]
+        p_new[t], m_new[t], v_new[t] = p[i], m[i], v[i]
+    if fresh:
+        fresh = np.asarray(fresh, np.int64)
+        p_new[fresh] = np.asarray(dense_weight_at(new_idx[fresh]), np.float32)
+    return new_idx, p_new, m_new, v_new, len(kept)
+

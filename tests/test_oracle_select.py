@@ -121,3 +121,59 @@ def test_rigl_brute_force_and_invariants():
                 assert (p2[i], m2[i], v2[i]) == (p[j], m[j], v[j])
             else:
                 assert (p2[i], m2[i], v2[i]) == (wd[f], 0, 0)
+
+
+def test_reselect_full_hand_case():
+    # |g| ranks: idx 7 (9.0), 2 (-8.0), 5 and 9 tie at 5.0 (lower index first), then 0 (4.0)
+    g = np.array([4.0, 0.5, -8.0, 1.0, 0.0, 5.0, -0.25, 9.0, 3.0, -5.0], np.float32)
+    act = np.array([0, 2, 3, 8], np.int64)
+    p = np.array([10.0, 20.0, 30.0, 80.0], np.float32)
+    m = np.array([1.0, 2.0, 3.0, 8.0], np.float32)
+    v = np.array([0.1, 0.2, 0.3, 0.8], np.float32)
+    w = np.arange(10, dtype=np.float32) * 100.0
+    new, p2, m2, v2, kept = oracle.reselect_full(act, p, m, v, g, 4, lambda i: w[i])
+    assert new.tolist() == [2, 5, 7, 9]
+    assert p2.tolist() == [20.0, 500.0, 700.0, 900.0]
+    assert m2.tolist() == [2.0, 0.0, 0.0, 0.0] and v2.tolist() == [np.float32(0.2), 0.0, 0.0, 0.0]
+    assert kept == 1
+
+
+def test_reselect_full_brute_force():
+    rng = np.random.default_rng(11)
+    for trial in range(30):
+        N = int(rng.integers(5, 60))
+        K_old = int(rng.integers(0, N + 1))
+        K_new = int(rng.integers(0, N + 1))
+        g = rng.integers(-4, 5, N).astype(np.float32)  # many ties, signed zeros below
+        g[rng.random(N) < 0.2] = -0.0
+        act = np.sort(rng.choice(N, K_old, replace=False)).astype(np.int64)
+        p = rng.standard_normal(K_old).astype(np.float32)
+        m = rng.standard_normal(K_old).astype(np.float32)
+        v = rng.random(K_old).astype(np.float32)
+        w = rng.standard_normal(N).astype(np.float32)
+        new, p2, m2, v2, kept = oracle.reselect_full(act, p, m, v, g, K_new, lambda i: w[i])
+        # brute force: rank by (|g| descending, index ascending) with plain Python
+        ranked = sorted(range(N), key=lambda i: (-abs(float(g[i])), i))
+        want = sorted(ranked[:K_new])
+        assert new.tolist() == want
+        old = {int(f): t for t, f in enumerate(act)}
+        n_k = 0
+        for t, f in enumerate(want):
+            if f in old:
+                n_k += 1
+                assert (p2[t], m2[t], v2[t]) == (p[old[f]], m[old[f]], v[old[f]])
+            else:
+                assert (p2[t], m2[t], v2[t]) == (w[f], 0.0, 0.0)
+        assert kept == n_k
+
+
+def test_reselect_full_keeps_a_set_that_still_ranks_first():
+    rng = np.random.default_rng(12)
+    N, K = 1000, 50
+    act = np.sort(rng.choice(N, K, replace=False)).astype(np.int64)
+    g = rng.standard_normal(N).astype(np.float32) * 0.1
+    g[act] = 10.0 + rng.random(K).astype(np.float32)
+    p, m, v = (rng.standard_normal(K).astype(np.float32) for _ in range(3))
+    new, p2, m2, v2, kept = oracle.reselect_full(act, p, m, v, g, K, lambda i: np.zeros(len(i)))
+    assert kept == K and (new == act).all()
+    assert (p2 == p).all() and (m2 == m).all() and (v2 == v).all()
