@@ -247,6 +247,27 @@ usaf_status usaf_rigl_swap(const float* g, int64_t N, const int64_t* act_idx, in
                            size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * usaf_reselect_full - reselection by re-ranking (USAF README, "Sparsity adapts": the active set
+ * is chosen again from fresh gradient magnitudes, with the large turnover the README reports at
+ * the first reselections): new_idx = the K entries with the largest |g| (ties: lower flat index
+ * first), sorted, exactly as usaf_importance_select. Entries that were in old_idx carry their
+ * p, m, v; entries new to the set start with p = the dense weight value and m = v = 0.
+ *   g            [N] fp32 dense gradient
+ *   old_idx      [K_old] sorted previous active set; p_in, m_in, v_in [K_old] aligned with it
+ *   w_seg0/n_seg0/w_seg1/w_dtype   dense weights, as for usaf_sparse_adam_step
+ *   new_idx, p_out, m_out, v_out   [K] out; must not overlap the inputs
+ *   n_kept       [1] int64 out: entries of new_idx that were in old_idx
+ * Limits: 0 <= K, K_old <= N < 2^32. Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
+ * ------------------------------------------------------------------------------------------- */
+size_t usaf_reselect_full_workspace_size(int64_t N, int64_t K);
+usaf_status usaf_reselect_full(const float* g, int64_t N, int64_t K, const int64_t* old_idx,
+                               int64_t K_old, const float* p_in, const float* m_in,
+                               const float* v_in, const void* w_seg0, int64_t n_seg0,
+                               const void* w_seg1, usaf_dtype w_dtype, int64_t* new_idx,
+                               float* p_out, float* m_out, float* v_out, int64_t* n_kept,
+                               uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
  * Kernel timing trace (host side, off by default). While enabled, every kernel launch of the hot
  * path is bracketed by two CUDA events recorded on its stream, so per-kernel device time can be
  * read without a profiler. usaf_trace_enable(1) clears earlier records; usaf_trace_summary

@@ -76,6 +76,9 @@ _SIGS = {
     "usaf_trace_summary": (_INT, [_P, _INT]),
     "usaf_rigl_swap": (_INT, [_P, _I64, _P, _I64, _I64, _P, _P, _P, _P, _I64, _P, _INT, _P, _P, _P,
                               _P, _P, _P, _P, _SZ, _P]),
+    "usaf_reselect_full_workspace_size": (_SZ, [_I64, _I64]),
+    "usaf_reselect_full": (_INT, [_P, _I64, _I64, _P, _I64, _P, _P, _P, _P, _I64, _P, _INT, _P,
+                                  _P, _P, _P, _P, _P, _P, _SZ, _P]),
 }
 
 
@@ -262,6 +265,22 @@ def rigl_swap(g, act_idx, D, p_in, m_in, v_in, w_seg0, n_seg0, w_seg1, new_idx, 
         _ptr(g), N, _ptr(act_idx), K, int(D), _ptr(p_in), _ptr(m_in), _ptr(v_in), _ptr(w_seg0),
         int(n_seg0), _ptr(w_seg1), _dt(w_seg0), _ptr(new_idx), _ptr(p_out), _ptr(m_out),
         _ptr(v_out), _ptr(n_swapped), _ptr(dev_status), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def reselect_full_workspace_size(N: int, K: int) -> int:
+    return int(lib().usaf_reselect_full_workspace_size(int(N), int(K)))
+
+
+def reselect_full(g, K, old_idx, p_in, m_in, v_in, w_seg0, n_seg0, w_seg1, new_idx, p_out, m_out,
+                  v_out, n_kept, dev_status=None, ws=None, stream=None):
+    N, K_old = g.numel(), old_idx.numel()
+    if ws is None:
+        ws = _ws(reselect_full_workspace_size(N, K), g.device)
+    _check("usaf_reselect_full", lib().usaf_reselect_full(
+        _ptr(g), N, int(K), _ptr(old_idx), K_old, _ptr(p_in), _ptr(m_in), _ptr(v_in),
+        _ptr(w_seg0), int(n_seg0), _ptr(w_seg1), _dt(w_seg0), _ptr(new_idx), _ptr(p_out),
+        _ptr(m_out), _ptr(v_out), _ptr(n_kept), _ptr(dev_status), _ptr(ws), ws.numel(),
+        _stream(stream)))
 
 
 def trace_enable(on: bool) -> None:

@@ -328,4 +328,36 @@ usaf_status usaf_rigl_swap(const float* g, int64_t N, const int64_t* act_idx, in
                      static_cast<cudaStream_t>(stream));
 }
 
+size_t usaf_reselect_full_workspace_size(int64_t N, int64_t K) {
+  if (N < 1 || K < 0 || K > N || N >= (int64_t(1) << 32)) return 0;
+  return reselect_ws_bytes(N, K);
+}
+
+usaf_status usaf_reselect_full(const float* g, int64_t N, int64_t K, const int64_t* old_idx,
+                               int64_t K_old, const float* p_in, const float* m_in,
+                               const float* v_in, const void* w_seg0, int64_t n_seg0,
+                               const void* w_seg1, usaf_dtype w_dtype, int64_t* new_idx,
+                               float* p_out, float* m_out, float* v_out, int64_t* n_kept,
+                               uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
+  if (!g || N < 1 || K < 0 || K > N || K_old < 0 || K_old > N || !n_kept)
+    return USAF_ERR_INVALID_ARG;
+  if (!dtype_ok(w_dtype) || n_seg0 < 0) return USAF_ERR_INVALID_ARG;
+  if (K_old > 0 && (!old_idx || !p_in || !m_in || !v_in)) return USAF_ERR_INVALID_ARG;
+  if (K > 0 && (!new_idx || !p_out || !m_out || !v_out || !w_seg0 || (N > n_seg0 && !w_seg1)))
+    return USAF_ERR_INVALID_ARG;
+  if (N >= (int64_t(1) << 32)) return USAF_ERR_UNSUPPORTED;
+  const void* ins[4] = {p_in, m_in, v_in, old_idx};
+  const size_t insz[4] = {size_t(K_old) * 4, size_t(K_old) * 4, size_t(K_old) * 4,
+                          size_t(K_old) * 8};
+  const void* outs[4] = {p_out, m_out, v_out, new_idx};
+  const size_t outsz[4] = {size_t(K) * 4, size_t(K) * 4, size_t(K) * 4, size_t(K) * 8};
+  for (int i = 0; i < 4; ++i)
+    for (int j = 0; j < 4; ++j)
+      if (overlaps(ins[i], insz[i], outs[j], outsz[j])) return USAF_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < usaf_reselect_full_workspace_size(N, K)) return USAF_ERR_WORKSPACE;
+  return reselect_launch(g, N, K, old_idx, K_old, p_in, m_in, v_in, w_seg0, n_seg0, w_seg1,
+                         w_dtype, new_idx, p_out, m_out, v_out, n_kept, dev_status, ws,
+                         static_cast<cudaStream_t>(stream));
+}
+
 }  // extern "C"

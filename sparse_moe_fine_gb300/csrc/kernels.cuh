@@ -82,6 +82,13 @@ usaf_status adam_launch(int64_t n, const int64_t* idx, const float* g, float* p,
 size_t select_ws_bytes(int64_t N, int64_t K, bool with_bitmap);
 usaf_status importance_select_launch(const float* g, int64_t N, int64_t K, int64_t* out_idx,
                                      uint32_t* dev_status, void* ws, cudaStream_t st);
+size_t reselect_ws_bytes(int64_t N, int64_t K);
+usaf_status reselect_launch(const float* g, int64_t N, int64_t K, const int64_t* old_idx,
+                            int64_t K_old, const float* p_in, const float* m_in,
+                            const float* v_in, const void* w0, int64_t n0, const void* w1,
+                            usaf_dtype wdt, int64_t* new_idx, float* p_out, float* m_out,
+                            float* v_out, int64_t* n_kept, uint32_t* dev_status, void* ws,
+                            cudaStream_t st);
 size_t rigl_ws_bytes(int64_t N, int64_t K, int64_t D);
 usaf_status rigl_launch(const float* g, int64_t N, const int64_t* act_idx, int64_t K, int64_t D,
                         const float* p_in, const float* m_in, const float* v_in, const void* w0,

@@ -581,6 +581,36 @@ __global__ void rigl_merge_kernel(const int64_t* __restrict__ act, int64_t K,
   }
 }
 
+// Full reselection: entry t of the new set carries (p, m, v) from the old set when its flat index
+// is there (binary search), else starts from the dense weight with zero moments.
+template <typename W>
+__global__ void reselect_carry_kernel(const int64_t* __restrict__ new_idx, int64_t K,
+                                      const int64_t* __restrict__ old_idx, int64_t K_old,
+                                      const float* __restrict__ p_in, const float* __restrict__ m_in,
+                                      const float* __restrict__ v_in, const W* __restrict__ w0,
+                                      int64_t n0, const W* __restrict__ w1, float* __restrict__ p_out,
+                                      float* __restrict__ m_out, float* __restrict__ v_out,
+                                      SelCtrl* c) {
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  bool kept = false;
+  if (t < K) {
+    const int64_t f = new_idx[t];
+    const int64_t s = lower_bound_i64(old_idx, K_old, f);
+    kept = s < K_old && old_idx[s] == f;
+    if (kept) {
+      p_out[t] = p_in[s];
+      m_out[t] = m_in[s];
+      v_out[t] = v_in[s];
+    } else {
+      p_out[t] = to_f32(f < n0 ? w0[f] : w1[f - n0]);
+      m_out[t] = 0.f;
+      v_out[t] = 0.f;
+    }
+  }
+  const unsigned n = __popc(__ballot_sync(0xffffffffu, kept));
+  if ((threadIdx.x & 31) == 0 && n) atomicAdd(&c->n_swapped, (unsigned long long)n);
+}
+
 __global__ void rigl_finish_kernel(const SelCtrl* c, int64_t* n_swapped) {
   if (threadIdx.x == 0) *n_swapped = (int64_t)c->n_swapped;
 }
@@ -682,6 +712,46 @@ usaf_status rigl_launch(const float* g, int64_t N, const int64_t* act_idx, int64
     USAF_CHECK_LAUNCH();
   }
   rigl_finish_kernel<<<1, 32, 0, st>>>(wd.ctrl, n_swapped);
+  USAF_CHECK_LAUNCH();
+  return USAF_OK;
+}
+
+size_t reselect_ws_bytes(int64_t N, int64_t K) { return select_ws_bytes(N, K > 0 ? K : 1, false); }
+
+usaf_status reselect_launch(const float* g, int64_t N, int64_t K, const int64_t* old_idx,
+                            int64_t K_old, const float* p_in, const float* m_in,
+                            const float* v_in, const void* w0, int64_t n0, const void* w1,
+                            usaf_dtype wdt, int64_t* new_idx, float* p_out, float* m_out,
+                            float* v_out, int64_t* n_kept, uint32_t* dev_status, void* ws,
+                            cudaStream_t st) {
+  const int64_t Ks = K > 0 ? K : 1;
+  const SelPlan p = make_plan(N, Ks);
+  Carver c(ws);
+  SelWs w;
+  sel_layout(p, c, w);
+  if (K > 0) {
+    Src s{};
+    s.g = g;
+    s.n = N;
+    s.L = p.L;
+    s.excl = nullptr;
+    s.drop = 0;
+    USAF_TRY(run_select(p, w, s, K, new_idx, dev_status, false, st));
+    USAF_TRACE("reselect_carry", st);
+    if (wdt == USAF_BF16)
+      reselect_carry_kernel<__nv_bfloat16><<<(unsigned)ceil_div(K, 256), 256, 0, st>>>(
+          new_idx, K, old_idx, K_old, p_in, m_in, v_in, static_cast<const __nv_bfloat16*>(w0),
+          n0, static_cast<const __nv_bfloat16*>(w1), p_out, m_out, v_out, w.ctrl);
+    else
+      reselect_carry_kernel<float><<<(unsigned)ceil_div(K, 256), 256, 0, st>>>(
+          new_idx, K, old_idx, K_old, p_in, m_in, v_in, static_cast<const float*>(w0), n0,
+          static_cast<const float*>(w1), p_out, m_out, v_out, w.ctrl);
+    USAF_CHECK_LAUNCH();
+  } else {
+    sel_init_kernel<<<1, 256, 0, st>>>(w.ctrl, 0, w.ccnt, p.G);
+    USAF_CHECK_LAUNCH();
+  }
+  rigl_finish_kernel<<<1, 32, 0, st>>>(w.ctrl, n_kept);
   USAF_CHECK_LAUNCH();
   return USAF_OK;
 }

@@ -12,7 +12,7 @@ from sparse_moe_fine_gb300 import binding as B
 def test_library_exports_every_header_symbol():
     L = B.lib()
     syms = B.header_symbols()
-    assert len(syms) == 18
+    assert len(syms) == 20
     for s in syms:
         assert hasattr(L, s), s
     assert L.usaf_abi_version() == 1
@@ -76,3 +76,29 @@ def test_host_argument_checks_return_codes():
     s3 = B.shape(8, 96, 4, 2, 64)
     assert _call("usaf_moe_fwd", ctypes.byref(s3), 1, 1, 1, 1, ctypes.byref(B._Routing(*[1] * 7)),
                  1, 1, 1, 1, 1, 1 << 30, None) == 2
+
+
+def test_reselect_full_host_checks():
+    L = B.lib()
+    N, K = 1 << 20, 5000
+    assert L.usaf_reselect_full_workspace_size(N, K) > 0
+    assert L.usaf_reselect_full_workspace_size(N, N + 1) == 0
+    assert L.usaf_reselect_full_workspace_size(1 << 32, K) == 0
+    fake = ctypes.c_void_p(256)  # never dereferenced: every call below fails on the host
+    one = ctypes.c_void_p(512)
+    # null gradient / null count
+    assert L.usaf_reselect_full(None, N, K, fake, K, fake, fake, fake, fake, N, None, 1, fake,
+                                fake, fake, fake, fake, None, fake, 1 << 30, None) == 1
+    assert L.usaf_reselect_full(fake, N, K, fake, K, fake, fake, fake, fake, N, None, 1, fake,
+                                fake, fake, fake, None, None, fake, 1 << 30, None) == 1
+    # an output aliasing an input
+    assert L.usaf_reselect_full(fake, N, K, fake, K, one, fake, fake, fake, N, None, 1, fake,
+                                one, fake, fake, fake, None, fake, 1 << 30, None) == 1
+    # workspace too small
+    assert L.usaf_reselect_full(fake, N, K, ctypes.c_void_p(1 << 20), K,
+                                ctypes.c_void_p(2 << 20), ctypes.c_void_p(3 << 20),
+                                ctypes.c_void_p(4 << 20), fake, N, None, 1,
+                                ctypes.c_void_p(5 << 20), ctypes.c_void_p(6 << 20),
+                                ctypes.c_void_p(7 << 20), ctypes.c_void_p(8 << 20), fake, None,
+                                fake, 16, None) == 3
+

@@ -161,3 +161,44 @@ def test_rigl_full_qwen3_layer():
     kept = (pos < K) & (act[np.minimum(pos, K - 1)] == new)
     assert (p2[kept] == p[pos[kept]]).all() and (m2[kept] == m[pos[kept]]).all()
     assert (p2[~kept] == w[new[~kept]]).all() and (m2[~kept] == 0).all() and (v2[~kept] == 0).all()
+
+
+def gpu_reselect(g_np, K, act, p, m, v, w_np, n0, dev):
+    g = to_dev(g_np, dev)
+    w = to_dev(w_np, dev, True)
+    outs = [torch.empty(K, dtype=torch.int64, device=dev)] + [torch.empty(K, device=dev)
+                                                              for _ in range(3)]
+    nk = torch.zeros(1, dtype=torch.int64, device=dev)
+    B.reselect_full(g, K, to_dev(act, dev), to_dev(p, dev), to_dev(m, dev), to_dev(v, dev),
+                    w[:n0], n0, w[n0:], *outs, nk)
+    torch.cuda.synchronize()
+    return [o.cpu().numpy() for o in outs] + [int(nk.item())]
+
+
+@pytest.mark.parametrize("N,K_old,K", [(40, 12, 9), (6000, 800, 900), (1 << 23, 41944, 41944)])
+def test_reselect_full_against_oracle(N, K_old, K):
+    """Full re-ranking reselection: new set bit-exact; state carried for kept entries, weights
+    and zero moments for new ones; kept count. The large case takes the sampled path."""
+    dev = device()
+    rng = np.random.default_rng(N + 1)
+    act = synth.uniform_mask(N, K_old, seed=N % 89)
+    if N < 10000:
+        g = (rng.integers(-4, 5, N) * 0.5).astype(np.float32)
+    else:
+        g = synth.student_t3(N, seed=5)
+        # the previous set overlaps the new one: half of it from the top of this gradient
+        top = oracle.importance_select_threshold(g, K_old // 2)
+        act = np.union1d(top, act)[:K_old]
+        act = np.sort(act)
+    p = rng.standard_normal(act.size).astype(np.float32)
+    m = rng.standard_normal(act.size).astype(np.float32)
+    v = np.abs(rng.standard_normal(act.size)).astype(np.float32)
+    w = synth.to_bf16_values(rng.standard_normal(N).astype(np.float32))
+    n0 = N // 3 * 2
+    got = gpu_reselect(g, K, act, p, m, v, w, n0, dev)
+    ref = oracle.reselect_full(act, p, m, v, g, K, lambda i: w[i])
+    for a, b in zip(got[:4], ref[:4]):
+        assert np.array_equal(a, b)
+    assert got[4] == ref[4]
+    if N >= 10000:
+        assert 0 < got[4] < K
