@@ -324,12 +324,26 @@ def run(args):
     ev[1].record()
     torch.cuda.synchronize()
     rigl_ms = ev[0].elapsed_time(ev[1]) / reps
-    del ws_rigl, ws_sel, outs
+    # full reselection: re-rank by |g|, carry the state of entries that stay
+    nk = torch.zeros(1, dtype=torch.int64, device=dev)
+    ws_res = torch.empty(B.reselect_full_workspace_size(cfg.N, cfg.K), dtype=torch.uint8,
+                         device=dev)
+    resel = lambda: B.reselect_full(g_dense, cfg.K, act, layer.p, layer.m, layer.v, wgu, cfg.N_gu,
+                                    wd, *outs, nk, ws=ws_res)
+    resel()
+    ev[0].record()
+    for _ in range(reps):
+        resel()
+    ev[1].record()
+    torch.cuda.synchronize()
+    resel_ms = ev[0].elapsed_time(ev[1]) / reps
+    del ws_rigl, ws_sel, outs, ws_res
     g_bytes = cfg.N * 4
     importance = {
         "select_ms": sel_ms, "select_gbs": g_bytes / sel_ms / 1e6,
         "select_frac": g_bytes / sel_ms / 1e6 / hbm,
         "rigl_ms": rigl_ms, "rigl_gbs": (g_bytes + cfg.N / 8 + cfg.K * 40) / rigl_ms / 1e6,
+        "reselect_full_ms": resel_ms, "reselect_full_kept": int(nk.item()),
         "select_exact_path": bool(int(st.item()) & B.DEV_SELECT_EXACT_PATH),
         "N": cfg.N, "K": cfg.K, "D": D}
     del g_dense, layer
