@@ -324,6 +324,26 @@ def run(args):
     ev[1].record()
     torch.cuda.synchronize()
     rigl_ms = ev[0].elapsed_time(ev[1]) / reps
+    # dense gradient pass of the importance phase: one micro-batch's dense expert gradient added
+    # into the accumulated g (route, forward, dense backward)
+    st_d = torch.zeros(1, dtype=torch.int32, device=dev)
+    ws_dense = torch.empty(B.moe_bwd_workspace_size(layer.s, layer.dt, 0), dtype=torch.uint8,
+                           device=dev)
+    layer.route(x)
+    layer.forward(x)
+    dense = lambda: B.moe_bwd_dense(layer.s, x, layer.w_router, layer.w_gate_up, layer.w_down,
+                                    layer.rt, layer.x_perm, layer.h, layer.wa, dy, g_dense,
+                                    layer.g_router, accumulate=1, dx=layer.dx,
+                                    logits=layer.logits, renorm=layer.renorm, dev_status=st_d,
+                                    ws=ws_dense)
+    dense()
+    ev[0].record()
+    for _ in range(reps):
+        dense()
+    ev[1].record()
+    torch.cuda.synchronize()
+    dense_ms = ev[0].elapsed_time(ev[1]) / reps
+    del ws_dense
     # full reselection: re-rank by |g|, carry the state of entries that stay
     nk = torch.zeros(1, dtype=torch.int64, device=dev)
     ws_res = torch.empty(B.reselect_full_workspace_size(cfg.N, cfg.K), dtype=torch.uint8,
@@ -344,6 +364,7 @@ def run(args):
         "select_frac": g_bytes / sel_ms / 1e6 / hbm,
         "rigl_ms": rigl_ms, "rigl_gbs": (g_bytes + cfg.N / 8 + cfg.K * 40) / rigl_ms / 1e6,
         "reselect_full_ms": resel_ms, "reselect_full_kept": int(nk.item()),
+        "dense_grad_bwd_ms": dense_ms,
         "select_exact_path": bool(int(st.item()) & B.DEV_SELECT_EXACT_PATH),
         "N": cfg.N, "K": cfg.K, "D": D}
     del g_dense, layer

@@ -189,6 +189,30 @@ usaf_status usaf_moe_bwd_sparse(const usaf_moe_shape* shape, usaf_dtype dtype, i
                                 void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * usaf_moe_bwd_dense - the same backward as usaf_moe_bwd_sparse (dh, dw, router gradient, dx),
+ * with the expert weight gradient formed densely for the importance phase (USAF README: the
+ * weights to train are the 0.5% with the largest gradient magnitude, found by a dense gradient
+ * pass; A100 operations table: "RigL dense pass ~60 s" over the accumulated gradient):
+ *   g_dense[f] = dL/dW at every flat index f (gate_up [E,2I,H] row-major, then down [E,H,I])
+ *   gate_up entry (e, r, c) = sum over rows of expert e of dh[row, r] * x[tok, c];
+ *   down entry (e, r, c)    = sum over rows of expert e of dy[tok, r] * w * A[row, c];
+ * experts without tokens give 0.
+ *   g_dense     [N] fp32, 16-byte aligned; accumulate = 1 adds into it (micro-batch
+ *               accumulation), 0 overwrites it
+ *   the other arguments and the workspace (usaf_moe_bwd_workspace_size with K = 0) as for
+ *   usaf_moe_bwd_sparse
+ * bf16 layers form g_dense on tensor cores (fp32 accumulation; stores or adds by TMA); fp32
+ * layers on CUDA cores. Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
+ * ------------------------------------------------------------------------------------------- */
+usaf_status usaf_moe_bwd_dense(const usaf_moe_shape* shape, usaf_dtype dtype, int renorm,
+                               const void* x, const float* w_router, const void* w_gate_up,
+                               const void* w_down, const usaf_routing* rt, const float* logits,
+                               const void* x_perm_save, const void* h_save, const void* wa_save,
+                               const void* dy, float* g_dense, int accumulate, float* g_router,
+                               void* dx, float* dw_slot, uint32_t* dev_status, void* ws,
+                               size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
  * usaf_sparse_adam_step - fused gather / Adam update / scatter over n entries (the README's
  * "SparseAdam (26M)" optimizer, torch.optim.SparseAdam semantics, no weight decay):
  *   m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*g^2;

@@ -76,6 +76,8 @@ _SIGS = {
     "usaf_trace_summary": (_INT, [_P, _INT]),
     "usaf_rigl_swap": (_INT, [_P, _I64, _P, _I64, _I64, _P, _P, _P, _P, _I64, _P, _INT, _P, _P, _P,
                               _P, _P, _P, _P, _SZ, _P]),
+    "usaf_moe_bwd_dense": (_INT, [_P, _INT, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                  _INT, _P, _P, _P, _P, _P, _SZ, _P]),
     "usaf_reselect_full_workspace_size": (_SZ, [_I64, _I64]),
     "usaf_reselect_full": (_INT, [_P, _I64, _I64, _P, _I64, _P, _P, _P, _P, _I64, _P, _INT, _P,
                                   _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -227,6 +229,20 @@ def moe_bwd_sparse(s: Shape, x, w_router, w_gate_up, w_down, rt: Routing, x_perm
         ctypes.byref(s), dt, int(renorm), _ptr(x), _ptr(w_router), _ptr(w_gate_up), _ptr(w_down),
         ctypes.byref(r), _ptr(logits), _ptr(x_perm), _ptr(h), _ptr(wa), _ptr(dy), _ptr(act_idx),
         K, _ptr(g_act), _ptr(g_router), _ptr(dx), _ptr(dw_slot), _ptr(dev_status), _ptr(ws),
+        ws.numel(), _stream(stream)))
+
+
+def moe_bwd_dense(s: Shape, x, w_router, w_gate_up, w_down, rt: Routing, x_perm, h, wa, dy,
+                  g_dense, g_router, accumulate=0, dx=None, dw_slot=None, logits=None, renorm=1,
+                  dev_status=None, ws=None, stream=None):
+    dt = _dt(x)
+    if ws is None:
+        ws = _ws(moe_bwd_workspace_size(s, dt, 0), x.device)
+    r = rt.c()
+    _check("usaf_moe_bwd_dense", lib().usaf_moe_bwd_dense(
+        ctypes.byref(s), dt, int(renorm), _ptr(x), _ptr(w_router), _ptr(w_gate_up), _ptr(w_down),
+        ctypes.byref(r), _ptr(logits), _ptr(x_perm), _ptr(h), _ptr(wa), _ptr(dy), _ptr(g_dense),
+        int(accumulate), _ptr(g_router), _ptr(dx), _ptr(dw_slot), _ptr(dev_status), _ptr(ws),
         ws.numel(), _stream(stream)))
 
 

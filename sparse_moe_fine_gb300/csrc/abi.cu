@@ -255,7 +255,32 @@ usaf_status usaf_moe_bwd_sparse(const usaf_moe_shape* s, usaf_dtype dt, int reno
   BwdWs w;
   bwd_ws_layout(*s, dt, K, c, w);
   return moe_bwd_launch(a, renorm, logits, x_perm_save, h_save, wa_save, dy, act_idx, K, g_act,
-                        g_router, dx, dw_slot, dev_status, w, static_cast<cudaStream_t>(stream));
+                        g_router, dx, dw_slot, nullptr, 0, dev_status, w,
+                        static_cast<cudaStream_t>(stream));
+}
+
+usaf_status usaf_moe_bwd_dense(const usaf_moe_shape* s, usaf_dtype dt, int renorm, const void* x,
+                               const float* w_router, const void* w_gate_up, const void* w_down,
+                               const usaf_routing* rt, const float* logits,
+                               const void* x_perm_save, const void* h_save, const void* wa_save,
+                               const void* dy, float* g_dense, int accumulate, float* g_router,
+                               void* dx, float* dw_slot, uint32_t* dev_status, void* ws,
+                               size_t ws_bytes, void* stream) {
+  MoeArgs a{};
+  USAF_TRY(fill_args(a, s, dt, x, w_router, w_gate_up, w_down, rt));
+  if (renorm != 0 && renorm != 1) return USAF_ERR_INVALID_ARG;
+  if (accumulate != 0 && accumulate != 1) return USAF_ERR_INVALID_ARG;
+  if (!w_router || !x_perm_save || !h_save || !wa_save || !dy || !g_router || !g_dense)
+    return USAF_ERR_INVALID_ARG;
+  if (renorm == 0 && !logits) return USAF_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(g_dense) & 15) != 0) return USAF_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < usaf_moe_bwd_workspace_size(s, dt, 0)) return USAF_ERR_WORKSPACE;
+  Carver c(ws);
+  BwdWs w;
+  bwd_ws_layout(*s, dt, 0, c, w);
+  return moe_bwd_launch(a, renorm, logits, x_perm_save, h_save, wa_save, dy, nullptr, 0, nullptr,
+                        g_router, dx, dw_slot, g_dense, accumulate, dev_status, w,
+                        static_cast<cudaStream_t>(stream));
 }
 
 usaf_status usaf_sparse_adam_step(int64_t n, const int64_t* idx, const float* g, float* p,

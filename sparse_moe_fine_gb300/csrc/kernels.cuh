@@ -57,7 +57,8 @@ usaf_status moe_fwd_launch(const MoeArgs& a, void* x_perm, void* h, void* wa, vo
 usaf_status moe_bwd_launch(const MoeArgs& a, int renorm, const float* logits, const void* x_perm,
                            const void* h, const void* wa, const void* dy, const int64_t* act_idx,
                            int64_t K, float* g_act, float* g_router, void* dx, float* dw_slot,
-                           uint32_t* dev_status, BwdWs& w, cudaStream_t st);
+                           float* g_dense, int accumulate, uint32_t* dev_status, BwdWs& w,
+                           cudaStream_t st);
 
 // tensor-core (tcgen05) grouped GEMM stages, bf16 only
 bool tc_shape_ok(const usaf_moe_shape& s);
@@ -70,6 +71,9 @@ usaf_status tc_fwd_down(const MoeArgs& a, const void* wa, float* y_acc, cudaStre
 usaf_status tc_bwd_gvec(const MoeArgs& a, const void* dyT, const void* hT, void* dhT, float* dw,
                         cudaStream_t st);
 usaf_status tc_bwd_dx(const MoeArgs& a, const void* dh, float* dx_acc, cudaStream_t st);
+// dense expert weight gradient g[e] (a_rows x b_rows, fp32) = aT . bT^T over each expert's tokens
+usaf_status tc_wgrad_dense(const MoeArgs& a, const void* aT, int64_t a_rows, const void* bT,
+                           int64_t b_rows, float* g, int accumulate, cudaStream_t st);
 
 
 // ---------------------------------------------------------------- optimizer

@@ -800,11 +800,33 @@ usaf_status moe_fwd_launch(const MoeArgs& a, void* x_perm, void* h, void* wa, vo
                           static_cast<float*>(wa), static_cast<float*>(y), w, st);
 }
 
+// Dense expert weight gradient on CUDA cores (fp32 layers): one thread per entry of
+// g[e] (a_rows x b_rows), summing over the expert's routed tokens.
+template <typename T>
+__global__ void dense_wgrad_simt_kernel(const T* __restrict__ aT, int64_t a_rows,
+                                        const T* __restrict__ bT, int64_t b_rows,
+                                        const int32_t* __restrict__ off, int E, int64_t rcap,
+                                        float* __restrict__ g, int accumulate) {
+  const int64_t per = a_rows * b_rows, n = (int64_t)E * per;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int e = (int)(i / per);
+    const int64_t rc = i - (int64_t)e * per, r = rc / b_rows, c = rc - r * b_rows;
+    const int o = off[e], np = off[e + 1] - o;
+    const T* ar = aT + r * rcap + o;
+    const T* br = bT + c * rcap + o;
+    float acc = 0.f;
+    for (int t = 0; t < np; ++t) acc = fmaf(to_f32(ar[t]), to_f32(br[t]), acc);
+    g[i] = accumulate ? g[i] + acc : acc;
+  }
+}
+
 template <typename T>
 static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits, const T* xT,
                              const T* hT, const T* waT, const T* dy, const int64_t* act_idx,
                              int64_t K, float* g_act, float* g_router, T* dx, float* dw_out,
-                             uint32_t* dev_status, BwdWs& w, cudaStream_t st) {
+                             float* g_dense, int accumulate, uint32_t* dev_status, BwdWs& w,
+                             cudaStream_t st) {
   MoeArgs a = a0;
   a.plan = w.plan;
   a.wperm = w.wperm;
@@ -890,23 +912,40 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
                                                       dev_status);
     USAF_CHECK_LAUNCH();
   }
+  // dense expert weight gradients (importance phase)
+  if (g_dense) {
+    if (a.dt == USAF_BF16) {
+      USAF_TRY(tc_wgrad_dense(a, dhT, 2 * I, xT, H, g_dense, accumulate, st));
+      USAF_TRY(tc_wgrad_dense(a, dyT, H, waT, I, g_dense + Ngu, accumulate, st));
+    } else {
+      USAF_TRACE("simt_wgrad_dense", st);
+      dense_wgrad_simt_kernel<T><<<grid_dim_for(Ngu), 256, 0, st>>>(
+          dhT, 2 * I, xT, H, off, E, a.R_cap, g_dense, accumulate);
+      USAF_CHECK_LAUNCH();
+      dense_wgrad_simt_kernel<T><<<grid_dim_for(Ngu / 2), 256, 0, st>>>(
+          dyT, H, waT, I, off, E, a.R_cap, g_dense + Ngu, accumulate);
+      USAF_CHECK_LAUNCH();
+    }
+  }
   return USAF_OK;
 }
 
 usaf_status moe_bwd_launch(const MoeArgs& a, int renorm, const float* logits, const void* x_perm,
                            const void* h, const void* wa, const void* dy, const int64_t* act_idx,
                            int64_t K, float* g_act, float* g_router, void* dx, float* dw_slot,
-                           uint32_t* dev_status, BwdWs& w, cudaStream_t st) {
+                           float* g_dense, int accumulate, uint32_t* dev_status, BwdWs& w,
+                           cudaStream_t st) {
   using B = __nv_bfloat16;
   if (a.dt == USAF_BF16)
     return moe_bwd_t<B>(a, renorm, logits, static_cast<const B*>(x_perm),
                         static_cast<const B*>(h), static_cast<const B*>(wa),
                         static_cast<const B*>(dy), act_idx, K, g_act, g_router,
-                        static_cast<B*>(dx), dw_slot, dev_status, w, st);
+                        static_cast<B*>(dx), dw_slot, g_dense, accumulate, dev_status, w, st);
   return moe_bwd_t<float>(a, renorm, logits, static_cast<const float*>(x_perm),
                           static_cast<const float*>(h), static_cast<const float*>(wa),
                           static_cast<const float*>(dy), act_idx, K, g_act, g_router,
-                          static_cast<float*>(dx), dw_slot, dev_status, w, st);
+                          static_cast<float*>(dx), dw_slot, g_dense, accumulate, dev_status, w,
+                          st);
 }
 
 }  // namespace usaf

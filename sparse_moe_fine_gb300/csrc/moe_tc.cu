@@ -662,6 +662,238 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------- dense weight gradient
+// Dense expert weight gradient for the importance phase (the whole |g| is ranked there):
+//   gate_up[e]:  G[j, c] = sum over the expert's tokens of dh^T[j, t] x^T[c, t]      (2I x H)
+//   down[e]:     G[h, c] = sum over the expert's tokens of dy^T[h, t] (wA)^T[c, t]   (H x I)
+// Both operands are feature-major rows with the tokens contiguous, so both are K-major with
+// K = the expert's padded token count (its last k-block issues only the 16-token steps inside
+// the expert). A tile is (expert, 128 rows, 256 columns); the fp32 accumulator goes out through a
+// per-warp swizzled shared staging buffer and a TMA tensor store, or a TMA add-reduction when the
+// gradient accumulates over micro-batches. Padding tokens hold zeros in both operands.
+namespace wg {
+constexpr int STAGES = 3;
+constexpr int A_BYTES = 128 * BK * 2;
+constexpr int B_BYTES = 256 * BK * 2;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int OUT_BYTES = 32 * 128;  // one 32 x 32 fp32 box, 128-byte swizzled rows
+constexpr int SMEM = STAGES * STAGE_BYTES + EPI_WARPS * 2 * OUT_BYTES + 1024 + 256;
+static_assert(SMEM <= 232448, "shared memory of the dense gradient kernel");
+}  // namespace wg
+
+struct WgParams {
+  const int32_t* off;  // expert offsets of the permuted rows
+  int E, M, N;         // rows and columns of one expert's gradient
+  int MT, NT;          // tiles per expert along M (128) and N (256)
+  int accumulate;      // 1: add into the output (TMA reduce), 0: overwrite (TMA store)
+  uint32_t* status;
+};
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                             int c2, int add) {
+  if (add)
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group"
+        " [%0, {%2, %3, %4}], [%1];" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+  else
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::
+            "l"(reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmO, const WgParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* outbuf = smem + wg::STAGES * wg::STAGE_BYTES;  // 1024-aligned: 64 KB, 8 warps x 2
+  uint64_t* bars = reinterpret_cast<uint64_t*>(outbuf + EPI_WARPS * 2 * wg::OUT_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * wg::STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * wg::STAGES;
+  const uint32_t tfull0 = empty0 + 8 * wg::STAGES, tempty0 = tfull0 + 16, drain = tempty0 + 16;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < wg::STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, EPI_WARPS);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int per_e = p.MT * p.NT;
+  const int total = p.E * per_e;
+  bool failed = false;
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      int stage = 0;
+      uint32_t phase = 0, issued = 0;
+      for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
+        const int e = t / per_e, r = t % per_e, mt = r / p.NT, nt = r % p.NT;
+        const int o = p.off[e], npad = p.off[e + 1] - o;
+        const int nkb = (npad + BK - 1) / BK;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) {
+            failed = true;
+            break;
+          }
+          const uint32_t a_dst = smem_u32(smem + stage * wg::STAGE_BYTES);
+          const uint32_t fb = full0 + 8 * stage;
+          mbar_expect_tx(fb, wg::STAGE_BYTES);
+          tma_2d(a_dst, &tmA, fb, o + kb * BK, mt * 128);
+          tma_2d(a_dst + wg::A_BYTES, &tmB, fb, o + kb * BK, nt * 256);
+          ++issued;
+          if (++stage == wg::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (failed) {
+        *abort_flag = 1;
+        flag_status(p.status, USAF_DEV_TIMEOUT);
+      }
+      for (int s = 0; s < wg::STAGES && (uint32_t)s < issued; ++s) {
+        const uint32_t last = issued - 1 - ((issued - 1 - s) % wg::STAGES);
+        mbar_wait(full0 + 8 * s, (last / wg::STAGES) & 1, abort_flag);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      const uint32_t idesc = idesc_bf16(256, false, false);
+      for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
+        const int e = t / per_e;
+        const int npad = p.off[e + 1] - p.off[e];
+        const int nkb = (npad + BK - 1) / BK;
+        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * 256;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + stage * wg::STAGE_BYTES);
+          const uint32_t b_base = a_base + wg::A_BYTES;
+          const int nks = min(BK, npad - kb * BK) / 16;  // 16-token steps inside the expert
+          for (int ks = 0; ks < nks; ++ks)
+            umma_bf16(d, sdesc(a_base + ks * 32, 16, 1024), sdesc(b_base + ks * 32, 16, 1024),
+                      idesc, (kb | ks) != 0 ? 1u : 0u);
+          umma_commit(empty0 + 8 * stage);
+          if (++stage == wg::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (failed) break;
+        umma_commit(tfull0 + 8 * acc);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      if (failed) {
+        *abort_flag = 1;
+        flag_status(p.status, USAF_DEV_TIMEOUT);
+      }
+      umma_commit(drain);
+      mbar_wait(drain, 0, abort_flag);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue warps 2..9
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    uint8_t* ob = outbuf + (warp - 2) * 2 * wg::OUT_BYTES;
+    int acc = 0, nstore = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x) {
+      const int e = t / per_e, r = t % per_e, mt = r / p.NT, nt = r % p.NT;
+      const bool empty = p.off[e + 1] == p.off[e];
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256;
+      for (int ch = half; ch < 8; ch += 2) {
+        const int c0 = nt * 256 + ch * 32;
+        if (c0 >= p.N || (empty && p.accumulate)) continue;
+        float v[32];
+        if (!empty) {
+          tmem_ld32(taddr + ch * 32, v);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0.f;
+        }
+        uint8_t* buf = ob + (nstore & 1) * wg::OUT_BYTES;
+        // the store issued from this buffer two chunks ago must have read it
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        __syncwarp();
+        uint4* row = reinterpret_cast<uint4*>(buf + lane * 128);
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          row[c ^ (lane & 7)] = make_uint4(__float_as_uint(v[4 * c]), __float_as_uint(v[4 * c + 1]),
+                                           __float_as_uint(v[4 * c + 2]),
+                                           __float_as_uint(v[4 * c + 3]));
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tmO, smem_u32(buf), c0, mt * 128 + q * 32, e, p.accumulate);
+          asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+        }
+        ++nstore;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
 // ---------------------------------------------------------------------------- plan kernel
 // Token tiles per expert: ceil(padded rows / 256), exclusive prefix over experts (E <= 1024).
 __global__ void __launch_bounds__(1024) token_plan_kernel(const int32_t* __restrict__ off, int E,
@@ -875,6 +1107,45 @@ usaf_status tc_bwd_dx(const MoeArgs& a, const void* dhT, float* dx_acc, cudaStre
   p.MT = (int)ceil_div(a.s.H, BM);
   p.acc_out = dx_acc;
   return launch<V_DX>(ma, mb, p, st);
+}
+
+usaf_status tc_wgrad_dense(const MoeArgs& a, const void* aT, int64_t a_rows, const void* bT,
+                           int64_t b_rows, float* g, int accumulate, cudaStream_t st) {
+  USAF_TRACE(accumulate ? "tc_wgrad_dense_add" : "tc_wgrad_dense", st);
+  auto fn = encode_fn();
+  if (!fn) return USAF_ERR_CUDA;
+  CUtensorMap ma, mb, mo;
+  if (!map_2d(&ma, aT, a.R_cap, a_rows, 64, 128) || !map_2d(&mb, bT, a.R_cap, b_rows, 64, 256))
+    return USAF_ERR_CUDA;
+  {
+    // g as [E][a_rows][b_rows] fp32, stored in 32 x 32 boxes with 128-byte swizzle
+    cuuint64_t dims[3] = {(cuuint64_t)b_rows, (cuuint64_t)a_rows, (cuuint64_t)a.s.E};
+    cuuint64_t strides[2] = {(cuuint64_t)b_rows * 4, (cuuint64_t)(a_rows * b_rows * 4)};
+    cuuint32_t box[3] = {32, 32, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    if (fn(&mo, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, g, dims, strides, box, es,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return USAF_ERR_CUDA;
+  }
+  WgParams p{};
+  p.off = a.rt.expert_offset;
+  p.E = (int)a.s.E;
+  p.M = (int)a_rows;
+  p.N = (int)b_rows;
+  p.MT = (int)ceil_div(a_rows, 128);
+  p.NT = (int)ceil_div(b_rows, 256);
+  p.accumulate = accumulate;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(tc_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             wg::SMEM) != cudaSuccess)
+      return USAF_ERR_CUDA;
+    attr_done = true;
+  }
+  tc_wgrad_kernel<<<device_sm_count(), NUM_THREADS, wg::SMEM, st>>>(ma, mb, mo, p);
+  USAF_CHECK_LAUNCH();
+  return USAF_OK;
 }
 
 }  // namespace usaf

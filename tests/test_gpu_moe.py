@@ -178,3 +178,118 @@ def test_qwen3_shaped_layer_sampled():
     assert sel.sum() > 1000
     assert rel_l2(got["g_act"][sel], g[sel]) <= 1e-2
     assert np.isfinite(got["g_act"]).all()
+
+
+def run_dense(cfg, inp, logits, dev, twice=False):
+    """Route, forward and the dense backward; with twice=True a second call accumulates."""
+    s = B.shape(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I)
+    bf = cfg.bf16
+    dt = torch.bfloat16 if bf else torch.float32
+    x = to_dev(inp["x"], dev, bf)
+    wr = to_dev(inp["w_router"], dev)
+    wgu = to_dev(inp["w_gate_up"], dev, bf)
+    wd = to_dev(inp["w_down"], dev, bf)
+    dy = to_dev(inp["dy"], dev, bf)
+    li = to_dev(logits, dev)
+    rt = B.Routing.empty(s, dev)
+    B.route_topk(s, x, wr, rt, logits_in=li)
+    cap = B.routed_rows_capacity(s)
+    xp = torch.empty(cfg.H, cap, dtype=dt, device=dev)
+    h = torch.empty(2 * cfg.I, cap, dtype=dt, device=dev)
+    wa = torch.empty(cfg.I, cap, dtype=dt, device=dev)
+    y = torch.empty(cfg.T, cfg.H, dtype=dt, device=dev)
+    B.moe_fwd(s, x, wgu, wd, rt, xp, h, wa, y)
+    g = torch.full((cfg.N,), float("nan"), device=dev)
+    g_r = torch.empty(cfg.E, cfg.H, device=dev)
+    dx = torch.empty(cfg.T, cfg.H, dtype=dt, device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    B.moe_bwd_dense(s, x, wr, wgu, wd, rt, xp, h, wa, dy, g, g_r, accumulate=0, dx=dx,
+                    logits=li, dev_status=st)
+    if twice:
+        B.moe_bwd_dense(s, x, wr, wgu, wd, rt, xp, h, wa, dy, g, g_r, accumulate=1, dx=dx,
+                        logits=li, dev_status=st)
+    torch.cuda.synchronize()
+    return (g.cpu().numpy(), g_r.cpu().numpy(), dx.float().cpu().numpy(), int(st.item()),
+            rt.expert_count.cpu().numpy())
+
+
+def oracle_dense(cfg, inp, logits):
+    idx, w = oracle.route_topk(logits, cfg.k)
+    b = oracle.moe_backward(inp["x"], inp["w_router"], inp["w_gate_up"], inp["w_down"], idx, w,
+                            logits, inp["dy"], dense_wgrad=True)
+    return np.concatenate([b["dW_gate_up"].reshape(-1), b["dW_down"].reshape(-1)]), b
+
+
+def test_dense_wgrad_tiny_fp32():
+    dev = device()
+    cfg = synth.CONFIGS["tiny_fp32"]
+    inp = synth.moe_inputs(cfg, seed=0)
+    logits = oracle.router_logits(inp["x"], inp["w_router"])
+    g, g_r, dx, st, _ = run_dense(cfg, inp, logits, dev)
+    ref, b = oracle_dense(cfg, inp, logits)
+    assert st == 0
+    assert rel_l2(g, ref) <= 1e-5
+    assert rel_l2(g_r, b["g_router"]) <= 1e-5 and rel_l2(dx, b["dx"]) <= 1e-5
+
+
+DENSE_BF16 = [
+    # H = 192: the down gradient's second 128-row tile is half outside H; I = 192: its columns
+    # end inside the first 256-column tile
+    dict(T=1000, H=192, E=4, k=2, I=192),
+    # several row and column tiles, experts above 256 tokens (several k-blocks, a partial last)
+    dict(T=1200, H=512, E=4, k=2, I=320),
+]
+
+
+@pytest.mark.parametrize("dims", DENSE_BF16)
+def test_dense_wgrad_bf16(dims):
+    dev = device()
+    cfg = synth.small_config("dense", bf16=True, **dims)
+    inp = synth.moe_inputs(cfg, seed=7)
+    logits = oracle.router_logits(inp["x"], inp["w_router"])
+    g, g_r, dx, st, _ = run_dense(cfg, inp, logits, dev)
+    ref, b = oracle_dense(cfg, inp, logits)
+    assert st == 0 and np.isfinite(g).all()
+    assert rel_l2(g, ref) <= 1e-2
+    assert rel_l2(g_r, b["g_router"]) <= 1e-2 and rel_l2(dx, b["dx"]) <= 1e-2
+
+
+def test_dense_wgrad_accumulates_and_zeroes_empty_experts():
+    dev = device()
+    cfg = synth.small_config("dense_skew", T=600, H=128, E=6, k=2, I=128, bf16=True)
+    inp = synth.moe_inputs(cfg, seed=8)
+    logits = oracle.router_logits(inp["x"], inp["w_router"])
+    logits[:, 3] = -1e3  # expert 3 gets no token
+    g1, _, _, _, cnt = run_dense(cfg, inp, logits, dev)
+    g2, _, _, _, _ = run_dense(cfg, inp, logits, dev, twice=True)
+    ref, _ = oracle_dense(cfg, inp, logits)
+    assert cnt[3] == 0
+    gu = (np.arange(cfg.N) < cfg.N_gu)
+    e_of = np.where(gu, np.arange(cfg.N) // (2 * cfg.I * cfg.H),
+                    (np.arange(cfg.N) - cfg.N_gu) // (cfg.H * cfg.I))
+    assert (g1[e_of == 3] == 0).all() and (g2[e_of == 3] == 0).all()
+    assert rel_l2(g1, ref) <= 1e-2
+    assert rel_l2(g2, 2 * g1) <= 1e-6
+
+
+def test_dense_wgrad_qwen3_shaped_sampled():
+    """Full Qwen3-30B-A3B-shaped layer: the dense gradient of a sample of experts."""
+    dev = device()
+    cfg = synth.CONFIGS["qwen3_30b_a3b"]
+    inp = synth.moe_inputs(cfg, seed=0)
+    logits = oracle.router_logits(inp["x"], inp["w_router"])
+    g, _, _, st, cnt = run_dense(cfg, inp, logits, dev)
+    assert st == 0 and np.isfinite(g).all()
+    idx, w = oracle.route_topk(logits, cfg.k)
+    experts = sorted({0, int(np.argmax(cnt)), int(np.argmin(cnt)), cfg.E - 1})
+    G, H, I = cfg.N_gu, cfg.H, cfg.I
+    for e in experts:
+        # dense rows of this expert through the masked oracle: every entry of a few rows
+        rows_gu = np.array([0, 1, I, 2 * I - 1])
+        rows_d = np.array([0, H // 2, H - 1])
+        act = np.concatenate([
+            (e * 2 * I * H + r * H + np.arange(H)) for r in rows_gu] + [
+            (G + e * H * I + r * I + np.arange(I)) for r in rows_d]).astype(np.int64)
+        ref = oracle.masked_expert_grad(act, inp["x"], inp["w_gate_up"], inp["w_down"], idx, w,
+                                        inp["dy"], experts=[e])
+        assert rel_l2(g[act], ref) <= 1e-2
