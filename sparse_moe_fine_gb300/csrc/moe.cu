@@ -219,24 +219,26 @@ __global__ void swiglu_bwd_rows_kernel(const float* __restrict__ gvec, const T* 
 // ================================================================================================
 
 // Gather-transpose: xT[h, row] = x[perm_tok[row], h] for routed rows, 0 for padding and tail
-// rows. A block moves a 128-row x 64-feature tile through shared memory with 16-byte accesses, so
-// each feature row of xT receives 256 contiguous bytes (bf16).
-constexpr int GT_ROWS = 128;
+// rows. A block moves a 512-row x 16-feature tile through shared memory: each warp instruction of
+// the gather reads one 16-byte piece of 32 consecutive rows, and each warp instruction of the
+// store writes 512 contiguous bytes of one feature row, so every feature row of xT is written in
+// 1 KB runs (bf16).
+constexpr int GT_ROWS = 512;
+constexpr int GT_FEAT = 16;
 template <typename T>
 __global__ void __launch_bounds__(256) gather_transpose_kernel(
     const T* __restrict__ x, const int32_t* __restrict__ ptok, const int32_t* __restrict__ pslot,
     const int32_t* __restrict__ off_end, int64_t R_cap, int H, T* __restrict__ xT,
     const float* __restrict__ topk_w, float* __restrict__ wperm) {
-  constexpr int VW = 16 / sizeof(T);  // elements per 16-byte vector
-  // feature f's row of the tile is rotated by (f / VW) * VW columns: the column writes of the
-  // load phase then fall in distinct banks, and the 16-byte reads of the store phase stay aligned
-  __shared__ __align__(16) T tile[64 * GT_ROWS];
+  constexpr int VW = 16 / sizeof(T);        // elements per 16-byte vector
+  constexpr int NV = GT_FEAT / VW;          // vectors per row piece
+  __shared__ __align__(16) T tile[GT_FEAT * GT_ROWS];
   const int64_t r0 = (int64_t)blockIdx.x * GT_ROWS;
-  const int h0 = blockIdx.y * 64;
+  const int h0 = blockIdx.y * GT_FEAT;
   const int64_t end = *off_end;
   const bool vec = (H % VW) == 0;
-  for (int v = threadIdx.x; v < GT_ROWS * (64 / VW); v += blockDim.x) {
-    const int r = v / (64 / VW), f = (v % (64 / VW)) * VW;
+  for (int v = threadIdx.x; v < GT_ROWS * NV; v += blockDim.x) {
+    const int r = v % GT_ROWS, f = (v / GT_ROWS) * VW;  // 32 consecutive rows per warp
     const int64_t row = r0 + r;
     const bool live = row < R_cap && row < end && pslot[row] >= 0;
     const int64_t src = live ? (int64_t)ptok[row] * H : 0;
@@ -251,10 +253,7 @@ __global__ void __launch_bounds__(256) gather_transpose_kernel(
         buf[q] = (live && h0 + f + q < H) ? x[src + h0 + f + q] : from_f32<T>(0.f);
     }
 #pragma unroll
-    for (int q = 0; q < VW; ++q) {
-      const int ff = f + q;
-      tile[ff * GT_ROWS + (r + (ff / VW) * VW) % GT_ROWS] = buf[q];
-    }
+    for (int q = 0; q < VW; ++q) tile[(f + q) * GT_ROWS + r] = buf[q];
   }
   if (wperm && blockIdx.y == 0) {
     for (int r = threadIdx.x; r < GT_ROWS; r += blockDim.x) {
@@ -265,11 +264,12 @@ __global__ void __launch_bounds__(256) gather_transpose_kernel(
     }
   }
   __syncthreads();
-  for (int v = threadIdx.x; v < 64 * (GT_ROWS / VW); v += blockDim.x) {
-    const int f = v / (GT_ROWS / VW), r = (v % (GT_ROWS / VW)) * VW;
+  constexpr int RV = GT_ROWS / VW;  // vectors per feature row of the tile
+  for (int v = threadIdx.x; v < GT_FEAT * RV; v += blockDim.x) {
+    const int f = v / RV, r = (v % RV) * VW;
     if (h0 + f >= H || r0 + r >= R_cap) continue;
     *reinterpret_cast<uint4*>(xT + (int64_t)(h0 + f) * R_cap + r0 + r) =
-        *reinterpret_cast<const uint4*>(&tile[f * GT_ROWS + (r + (f / VW) * VW) % GT_ROWS]);
+        *reinterpret_cast<const uint4*>(&tile[f * GT_ROWS + r]);
   }
 }
 
@@ -731,7 +731,7 @@ void bwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, int64_t K, Carver& c,
 
 template <typename T>
 static usaf_status gather_t(const MoeArgs& a, const T* src, T* dstT, cudaStream_t st) {
-  const dim3 grid((unsigned)ceil_div(a.R_cap, GT_ROWS), (unsigned)ceil_div(a.s.H, 64));
+  const dim3 grid((unsigned)ceil_div(a.R_cap, GT_ROWS), (unsigned)ceil_div(a.s.H, GT_FEAT));
   gather_transpose_kernel<T><<<grid, 256, 0, st>>>(src, a.rt.perm_tok, a.rt.perm_slot,
                                                    a.rt.expert_offset + a.s.E, a.R_cap,
                                                    (int)a.s.H, dstT, a.rt.topk_w, a.wperm);

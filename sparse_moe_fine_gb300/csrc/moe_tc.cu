@@ -847,7 +847,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256;
       for (int ch = half; ch < 8; ch += 2) {
         const int c0 = nt * 256 + ch * 32;
-        if (c0 >= p.N || (empty && p.accumulate)) continue;
+        const int r0 = mt * 128 + q * 32;
+        // boxes starting past the gradient's last row or column are not issued at all
+        if (c0 >= p.N || r0 >= p.M || (empty && p.accumulate)) continue;
         float v[32];
         if (!empty) {
           tmem_ld32(taddr + ch * 32, v);
@@ -868,7 +870,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) {
-          tma_store_3d(&tmO, smem_u32(buf), c0, mt * 128 + q * 32, e, p.accumulate);
+          tma_store_3d(&tmO, smem_u32(buf), c0, r0, e, p.accumulate);
           asm volatile("cp.async.bulk.commit_group;" ::: "memory");
         }
         ++nstore;
