@@ -219,26 +219,24 @@ __global__ void swiglu_bwd_rows_kernel(const float* __restrict__ gvec, const T* 
 // ================================================================================================
 
 // Gather-transpose: xT[h, row] = x[perm_tok[row], h] for routed rows, 0 for padding and tail
-// rows. A block moves a 512-row x 16-feature tile through shared memory: each warp instruction of
-// the gather reads one 16-byte piece of 32 consecutive rows, and each warp instruction of the
-// store writes 512 contiguous bytes of one feature row, so every feature row of xT is written in
-// 1 KB runs (bf16).
-constexpr int GT_ROWS = 512;
-constexpr int GT_FEAT = 16;
+// rows. A block moves a 128-row x 64-feature tile through shared memory with 16-byte accesses, so
+// each feature row of xT receives 256 contiguous bytes (bf16).
+constexpr int GT_ROWS = 128;
 template <typename T>
 __global__ void __launch_bounds__(256) gather_transpose_kernel(
     const T* __restrict__ x, const int32_t* __restrict__ ptok, const int32_t* __restrict__ pslot,
     const int32_t* __restrict__ off_end, int64_t R_cap, int H, T* __restrict__ xT,
     const float* __restrict__ topk_w, float* __restrict__ wperm) {
-  constexpr int VW = 16 / sizeof(T);        // elements per 16-byte vector
-  constexpr int NV = GT_FEAT / VW;          // vectors per row piece
-  __shared__ __align__(16) T tile[GT_FEAT * GT_ROWS];
+  constexpr int VW = 16 / sizeof(T);  // elements per 16-byte vector
+  // feature f's row of the tile is rotated by (f / VW) * VW columns: the column writes of the
+  // load phase then fall in distinct banks, and the 16-byte reads of the store phase stay aligned
+  __shared__ __align__(16) T tile[64 * GT_ROWS];
   const int64_t r0 = (int64_t)blockIdx.x * GT_ROWS;
-  const int h0 = blockIdx.y * GT_FEAT;
+  const int h0 = blockIdx.y * 64;
   const int64_t end = *off_end;
   const bool vec = (H % VW) == 0;
-  for (int v = threadIdx.x; v < GT_ROWS * NV; v += blockDim.x) {
-    const int r = v % GT_ROWS, f = (v / GT_ROWS) * VW;  // 32 consecutive rows per warp
+  for (int v = threadIdx.x; v < GT_ROWS * (64 / VW); v += blockDim.x) {
+    const int r = v / (64 / VW), f = (v % (64 / VW)) * VW;
     const int64_t row = r0 + r;
     const bool live = row < R_cap && row < end && pslot[row] >= 0;
     const int64_t src = live ? (int64_t)ptok[row] * H : 0;
@@ -253,7 +251,10 @@ __global__ void __launch_bounds__(256) gather_transpose_kernel(
         buf[q] = (live && h0 + f + q < H) ? x[src + h0 + f + q] : from_f32<T>(0.f);
     }
 #pragma unroll
-    for (int q = 0; q < VW; ++q) tile[(f + q) * GT_ROWS + r] = buf[q];
+    for (int q = 0; q < VW; ++q) {
+      const int ff = f + q;
+      tile[ff * GT_ROWS + (r + (ff / VW) * VW) % GT_ROWS] = buf[q];
+    }
   }
   if (wperm && blockIdx.y == 0) {
     for (int r = threadIdx.x; r < GT_ROWS; r += blockDim.x) {
@@ -264,12 +265,11 @@ __global__ void __launch_bounds__(256) gather_transpose_kernel(
     }
   }
   __syncthreads();
-  constexpr int RV = GT_ROWS / VW;  // vectors per feature row of the tile
-  for (int v = threadIdx.x; v < GT_FEAT * RV; v += blockDim.x) {
-    const int f = v / RV, r = (v % RV) * VW;
+  for (int v = threadIdx.x; v < 64 * (GT_ROWS / VW); v += blockDim.x) {
+    const int f = v / (GT_ROWS / VW), r = (v % (GT_ROWS / VW)) * VW;
     if (h0 + f >= H || r0 + r >= R_cap) continue;
     *reinterpret_cast<uint4*>(xT + (int64_t)(h0 + f) * R_cap + r0 + r) =
-        *reinterpret_cast<const uint4*>(&tile[f * GT_ROWS + r]);
+        *reinterpret_cast<const uint4*>(&tile[f * GT_ROWS + (r + (f / VW) * VW) % GT_ROWS]);
   }
 }
 
@@ -517,42 +517,58 @@ __global__ void __launch_bounds__(SD_WARPS * 32, 2) sddmm_kernel(
   flag_status_warp(dev_status, bad, USAF_DEV_NONFINITE);
 }
 
-// g_router[e, h] = sum over the rows routed to e of dl[row] * x^T[h, row] (renormalised routing):
-// one group of eight lanes per (e, h), 16-byte vectors of x^T.
+// g_router[e, h] = sum over the rows routed to e of dl[row] * x^T[h, row] (renormalised routing).
+// A warp takes one expert and 32 consecutive h: lane l holds dl of tokens [VW l, VW l + VW) of
+// the pass, reads the same 16-byte token vector of each of the 32 x^T rows (eight in flight),
+// and a butterfly transpose of its 32 partial sums leaves g_router[e, h0 + l] in lane l.
 template <typename T>
 __global__ void __launch_bounds__(256) g_router_sel_kernel(
     const T* __restrict__ xT, const float* __restrict__ dl_perm, const int32_t* __restrict__ cnt,
     const int32_t* __restrict__ off, int E, int H, int64_t rcap, float* __restrict__ g_router,
     uint32_t* dev_status) {
   constexpr int VW = 16 / sizeof(T);
-  const int lane = threadIdx.x & 31, grp = lane >> 3, gl = lane & 7;
-  const int64_t groups = (int64_t)gridDim.x * (blockDim.x >> 3);
+  constexpr int U = 8;
+  const int lane = threadIdx.x & 31;
+  const int hb = (H + 31) / 32;
+  const int64_t tasks = (int64_t)E * hb;
   bool bad = false;
-  for (int64_t u0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 4;
-       u0 < (int64_t)E * H; u0 += groups) {
-    const int64_t u = u0 + grp;
-    float acc = 0.f;
-    if (u < (int64_t)E * H) {
-      const int e = (int)(u / H), h = (int)(u % H);
-      const int o = off[e];
-      const int n = (cnt[e] + VW - 1) / VW * VW;
-      const T* xr = xT + (int64_t)h * rcap + o;
-      const float* d = dl_perm + o;
-      const int cn = cnt[e];  // dl_perm holds no value past the expert's routed rows
-      for (int t = gl * VW; t < n; t += 8 * VW) {
-        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xr + t));
-        const T* xe = reinterpret_cast<const T*>(&xv);
+  for (int64_t task = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); task < tasks;
+       task += (int64_t)gridDim.x * (blockDim.x >> 5)) {
+    const int e = (int)(task / hb), h0 = (int)(task % hb) * 32;
+    const int o = off[e], cn = cnt[e];
+    float part[32];
 #pragma unroll
-        for (int q = 0; q < VW; ++q)
-          if (t + q < cn) acc = fmaf(d[t + q], to_f32(xe[q]), acc);
+    for (int i = 0; i < 32; ++i) part[i] = 0.f;
+    for (int t0 = 0; t0 < cn; t0 += 32 * VW) {
+      const int t = t0 + lane * VW;
+      float dv[VW];
+#pragma unroll
+      for (int q = 0; q < VW; ++q) dv[q] = t + q < cn ? dl_perm[o + t + q] : 0.f;
+      const bool any = t < cn;
+#pragma unroll
+      for (int i0 = 0; i0 < 32; i0 += U) {
+        uint4 xv[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int h = h0 + i0 + u;
+          xv[u] = any && h < H
+                      ? __ldg(reinterpret_cast<const uint4*>(xT + (int64_t)h * rcap + o + t))
+                      : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const T* xe = reinterpret_cast<const T*>(&xv[u]);
+          float acc = part[i0 + u];
+#pragma unroll
+          for (int q = 0; q < VW; ++q) acc = fmaf(dv[q], to_f32(xe[q]), acc);
+          part[i0 + u] = acc;
+        }
       }
     }
-    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-    if (gl == 0 && u < (int64_t)E * H) {
-      g_router[u] = acc;
-      bad |= !finite_f(acc);
+    const float gsum = transpose_reduce32(part, lane);
+    if (h0 + lane < H) {
+      g_router[(int64_t)e * H + h0 + lane] = gsum;
+      bad |= !finite_f(gsum);
     }
   }
   flag_status_warp(dev_status, bad, USAF_DEV_NONFINITE);
@@ -731,7 +747,7 @@ void bwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, int64_t K, Carver& c,
 
 template <typename T>
 static usaf_status gather_t(const MoeArgs& a, const T* src, T* dstT, cudaStream_t st) {
-  const dim3 grid((unsigned)ceil_div(a.R_cap, GT_ROWS), (unsigned)ceil_div(a.s.H, GT_FEAT));
+  const dim3 grid((unsigned)ceil_div(a.R_cap, GT_ROWS), (unsigned)ceil_div(a.s.H, 64));
   gather_transpose_kernel<T><<<grid, 256, 0, st>>>(src, a.rt.perm_tok, a.rt.perm_slot,
                                                    a.rt.expert_offset + a.s.E, a.R_cap,
                                                    (int)a.s.H, dstT, a.rt.topk_w, a.wperm);
@@ -867,7 +883,7 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
       dlogit_sel_kernel<<<(unsigned)ceil_div(Tn, 128), 128, 0, st>>>(
           a.rt.topk_w, dw, a.rt.slot_row, Tn, k, w.dl, w.dl_perm);
       USAF_CHECK_LAUNCH();
-      g_router_sel_kernel<T><<<(unsigned)ceil_div(s.E * s.H, 32), 256, 0, st>>>(
+      g_router_sel_kernel<T><<<(unsigned)ceil_div(s.E * ceil_div(s.H, 32), 8), 256, 0, st>>>(
           xT, w.dl_perm, cnt, off, E, H, a.R_cap, g_router, dev_status);
       USAF_CHECK_LAUNCH();
     } else {
