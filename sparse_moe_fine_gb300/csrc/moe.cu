@@ -517,58 +517,42 @@ __global__ void __launch_bounds__(SD_WARPS * 32, 2) sddmm_kernel(
   flag_status_warp(dev_status, bad, USAF_DEV_NONFINITE);
 }
 
-// g_router[e, h] = sum over the rows routed to e of dl[row] * x^T[h, row] (renormalised routing).
-// A warp takes one expert and 32 consecutive h: lane l holds dl of tokens [VW l, VW l + VW) of
-// the pass, reads the same 16-byte token vector of each of the 32 x^T rows (eight in flight),
-// and a butterfly transpose of its 32 partial sums leaves g_router[e, h0 + l] in lane l.
+// g_router[e, h] = sum over the rows routed to e of dl[row] * x^T[h, row] (renormalised routing):
+// one group of eight lanes per (e, h), 16-byte vectors of x^T.
 template <typename T>
 __global__ void __launch_bounds__(256) g_router_sel_kernel(
     const T* __restrict__ xT, const float* __restrict__ dl_perm, const int32_t* __restrict__ cnt,
     const int32_t* __restrict__ off, int E, int H, int64_t rcap, float* __restrict__ g_router,
     uint32_t* dev_status) {
   constexpr int VW = 16 / sizeof(T);
-  constexpr int U = 8;
-  const int lane = threadIdx.x & 31;
-  const int hb = (H + 31) / 32;
-  const int64_t tasks = (int64_t)E * hb;
+  const int lane = threadIdx.x & 31, grp = lane >> 3, gl = lane & 7;
+  const int64_t groups = (int64_t)gridDim.x * (blockDim.x >> 3);
   bool bad = false;
-  for (int64_t task = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); task < tasks;
-       task += (int64_t)gridDim.x * (blockDim.x >> 5)) {
-    const int e = (int)(task / hb), h0 = (int)(task % hb) * 32;
-    const int o = off[e], cn = cnt[e];
-    float part[32];
+  for (int64_t u0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 4;
+       u0 < (int64_t)E * H; u0 += groups) {
+    const int64_t u = u0 + grp;
+    float acc = 0.f;
+    if (u < (int64_t)E * H) {
+      const int e = (int)(u / H), h = (int)(u % H);
+      const int o = off[e];
+      const int n = (cnt[e] + VW - 1) / VW * VW;
+      const T* xr = xT + (int64_t)h * rcap + o;
+      const float* d = dl_perm + o;
+      const int cn = cnt[e];  // dl_perm holds no value past the expert's routed rows
+      for (int t = gl * VW; t < n; t += 8 * VW) {
+        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xr + t));
+        const T* xe = reinterpret_cast<const T*>(&xv);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) part[i] = 0.f;
-    for (int t0 = 0; t0 < cn; t0 += 32 * VW) {
-      const int t = t0 + lane * VW;
-      float dv[VW];
-#pragma unroll
-      for (int q = 0; q < VW; ++q) dv[q] = t + q < cn ? dl_perm[o + t + q] : 0.f;
-      const bool any = t < cn;
-#pragma unroll
-      for (int i0 = 0; i0 < 32; i0 += U) {
-        uint4 xv[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const int h = h0 + i0 + u;
-          xv[u] = any && h < H
-                      ? __ldg(reinterpret_cast<const uint4*>(xT + (int64_t)h * rcap + o + t))
-                      : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-          const T* xe = reinterpret_cast<const T*>(&xv[u]);
-          float acc = part[i0 + u];
-#pragma unroll
-          for (int q = 0; q < VW; ++q) acc = fmaf(dv[q], to_f32(xe[q]), acc);
-          part[i0 + u] = acc;
-        }
+        for (int q = 0; q < VW; ++q)
+          if (t + q < cn) acc = fmaf(d[t + q], to_f32(xe[q]), acc);
       }
     }
-    const float gsum = transpose_reduce32(part, lane);
-    if (h0 + lane < H) {
-      g_router[(int64_t)e * H + h0 + lane] = gsum;
-      bad |= !finite_f(gsum);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    if (gl == 0 && u < (int64_t)E * H) {
+      g_router[u] = acc;
+      bad |= !finite_f(acc);
     }
   }
   flag_status_warp(dev_status, bad, USAF_DEV_NONFINITE);
@@ -883,7 +867,7 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
       dlogit_sel_kernel<<<(unsigned)ceil_div(Tn, 128), 128, 0, st>>>(
           a.rt.topk_w, dw, a.rt.slot_row, Tn, k, w.dl, w.dl_perm);
       USAF_CHECK_LAUNCH();
-      g_router_sel_kernel<T><<<(unsigned)ceil_div(s.E * ceil_div(s.H, 32), 8), 256, 0, st>>>(
+      g_router_sel_kernel<T><<<(unsigned)ceil_div(s.E * s.H, 32), 256, 0, st>>>(
           xT, w.dl_perm, cnt, off, E, H, a.R_cap, g_router, dev_status);
       USAF_CHECK_LAUNCH();
     } else {

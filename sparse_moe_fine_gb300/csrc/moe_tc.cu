@@ -29,15 +29,11 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int BN = 256;
+constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
 constexpr int B_BOX = 64 * BK * 2;  // one MN-major box: 64 tokens x 64 k
-// Two rings: the weight operand (streamed from DRAM once) runs SA k-blocks ahead, the token
-// operand (mostly L2 hits) SB; the MMA of a k-block waits for both.
-constexpr int SA = 6;
-constexpr int SB = 3;
-constexpr int RING_BYTES = SA * A_BYTES + SB * B_BYTES;
-constexpr int NBARS = 2 * SA + 2 * SB + 5;
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPI_WARPS = 8;
 constexpr int NUM_THREADS = 64 + 32 * EPI_WARPS;
 constexpr int TMEM_COLS = 512;
@@ -45,9 +41,8 @@ constexpr int MAX_E = 1024;
 constexpr int PLAN_BYTES = 8704;  // barriers, TMEM slot, abort flag, plan and offsets (E <= 1024)
 constexpr int STAGE_PITCH = 80;   // bytes per row of an epilogue warp's store staging (64 + 16)
 constexpr int EPI_STAGE_BYTES = 32 * STAGE_PITCH;
-constexpr int SMEM_BYTES = RING_BYTES + 1024 + PLAN_BYTES + EPI_WARPS * EPI_STAGE_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + PLAN_BYTES + EPI_WARPS * EPI_STAGE_BYTES;
 static_assert(256 + 2 * (MAX_E + 1) * 4 <= PLAN_BYTES, "plan area");
-static_assert(NBARS * 8 + 8 <= 256, "barrier area");
 static_assert(SMEM_BYTES <= 232448, "shared memory of the tensor-core kernel");
 constexpr long long TIMEOUT_CYCLES = 1ll << 32;  // about two seconds
 
@@ -472,20 +467,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* ringA = smem;                      // SA x A_BYTES
-  uint8_t* ringB = smem + SA * A_BYTES;       // SB x B_BYTES
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RING_BYTES);
-  // bars: fullA[SA], emptyA[SA], fullB[SB], emptyB[SB], tfull[2], tempty[2], drain[1]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBARS);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain[1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int32_t* s_plan = reinterpret_cast<int32_t*>(smem + RING_BYTES + 256);
+  int32_t* s_plan = reinterpret_cast<int32_t*>(smem + STAGES * STAGE_BYTES + 256);
   int32_t* s_off = s_plan + (MAX_E + 1);
-  uint8_t* epi_stage = smem + RING_BYTES + PLAN_BYTES;  // EPI_WARPS x EPI_STAGE_BYTES
+  uint8_t* epi_stage = smem + STAGES * STAGE_BYTES + PLAN_BYTES;  // EPI_WARPS x EPI_STAGE_BYTES
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const uint32_t fullA0 = smem_u32(bars), emptyA0 = fullA0 + 8 * SA;
-  const uint32_t fullB0 = emptyA0 + 8 * SA, emptyB0 = fullB0 + 8 * SB;
-  const uint32_t tfull0 = emptyB0 + 8 * SB, tempty0 = tfull0 + 16, drain = tempty0 + 16;
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * STAGES;
+  const uint32_t tfull0 = empty0 + 8 * STAGES, tempty0 = tfull0 + 16, drain = tempty0 + 16;
 
   if constexpr (!VarTraits<VAR>::router) {
     for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
@@ -494,13 +486,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
   if (threadIdx.x == 0) {
-    for (int s = 0; s < SA; ++s) {
-      mbar_init(fullA0 + 8 * s, 1);
-      mbar_init(emptyA0 + 8 * s, 1);
-    }
-    for (int s = 0; s < SB; ++s) {
-      mbar_init(fullB0 + 8 * s, 1);
-      mbar_init(emptyB0 + 8 * s, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull0 + 8 * a, 1);
@@ -528,80 +516,47 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer
-      // The A (weight) and B (token) loads of the k-block sequence are issued by two cursors,
-      // each as soon as its ring slot is free, so the weight stream runs up to SA k-blocks ahead.
-      struct Cur {
-        int t, kb, nkb;
-        Tile ti;
-      };
-      auto start = [&](Cur& c, int t) {
-        c.t = t;
-        c.kb = 0;
-        if (t < total) {
-          c.ti = get_tile<VAR>(p, s_plan, s_off, t);
-          c.nkb = (c.ti.klen + BK - 1) / BK;
-        }
-      };
-      auto next = [&](Cur& c) {
-        if (++c.kb == c.nkb) start(c, c.t + gridDim.x);
-      };
-      Cur ca, cb;
-      start(ca, blockIdx.x);
-      start(cb, blockIdx.x);
-      uint32_t ga = 0, gb = 0;  // k-blocks issued on each ring
-      long long t_last = clock64();
-      while (cb.t < total) {
-        bool moved = false;
-        if (ca.t < total) {
-          const uint32_t s = ga % SA, ph = (ga / SA) & 1;
-          if (mbar_try_wait(emptyA0 + 8 * s, ph ^ 1)) {
-            const uint32_t dst = smem_u32(ringA + s * A_BYTES), fb = fullA0 + 8 * s;
-            const Tile& ti = ca.ti;
-            const int k0 = ca.kb * BK;
-            mbar_expect_tx(fb, A_BYTES);
-            if constexpr (VarTraits<VAR>::router) {
-              tma_2d(dst, &tmA, fb, k0, ti.m0);
-            } else if constexpr (VAR == V_GATEUP) {
-              tma_4d(dst, &tmA, fb, k0, 0, ti.m0, ti.e);
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0;
+      for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
+        const Tile ti = get_tile<VAR>(p, s_plan, s_off, t);
+        const int nkb = (ti.klen + BK - 1) / BK;
+        const int nbox = VarTraits<VAR>::router ? 0 : (ti.nrows + 63) / 64;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) {
+            failed = true;
+            break;
+          }
+          const uint32_t a_dst = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t b_dst = a_dst + A_BYTES;
+          const uint32_t fb = full0 + 8 * stage;
+          const int k0 = kb * BK;
+          if constexpr (VarTraits<VAR>::router) {
+            mbar_expect_tx(fb, A_BYTES + ROUTER_BN * BK * 2);
+            tma_2d(a_dst, &tmA, fb, k0, ti.m0);
+            tma_2d(b_dst, &tmB, fb, k0 % p.H, ti.row0);  // x, once for each part of Wr
+          } else {
+            mbar_expect_tx(fb, A_BYTES + nbox * B_BOX);
+            if constexpr (VAR == V_GATEUP) {
+              tma_4d(a_dst, &tmA, fb, k0, 0, ti.m0, ti.e);
             } else if constexpr (VAR == V_DOWN) {
-              tma_2d(dst, &tmA, fb, k0, ti.e * p.H + ti.m0);
+              tma_2d(a_dst, &tmA, fb, k0, ti.e * p.H + ti.m0);
             } else if constexpr (VAR == V_GVEC) {
-              tma_2d(dst, &tmA, fb, ti.m0, ti.e * p.H + k0);
-              tma_2d(dst + 8192, &tmA, fb, ti.m0 + 64, ti.e * p.H + k0);
+              tma_2d(a_dst, &tmA, fb, ti.m0, ti.e * p.H + k0);
+              tma_2d(a_dst + 8192, &tmA, fb, ti.m0 + 64, ti.e * p.H + k0);
             } else {  // V_DX
-              tma_2d(dst, &tmA, fb, ti.m0, ti.e * 2 * p.I + k0);
-              tma_2d(dst + 8192, &tmA, fb, ti.m0 + 64, ti.e * 2 * p.I + k0);
+              tma_2d(a_dst, &tmA, fb, ti.m0, ti.e * 2 * p.I + k0);
+              tma_2d(a_dst + 8192, &tmA, fb, ti.m0 + 64, ti.e * 2 * p.I + k0);
             }
-            ++ga;
-            next(ca);
-            moved = true;
+            // B: feature-major tokens, boxes of 64 tokens x 64 k (MN-major, 8 KB apart)
+            for (int q = 0; q < nbox; ++q) tma_2d(b_dst + q * B_BOX, &tmB, fb, ti.row0 + 64 * q, k0);
           }
-        }
-        if (gb < ga) {
-          const uint32_t s = gb % SB, ph = (gb / SB) & 1;
-          if (mbar_try_wait(emptyB0 + 8 * s, ph ^ 1)) {
-            const uint32_t dst = smem_u32(ringB + s * B_BYTES), fb = fullB0 + 8 * s;
-            const Tile& ti = cb.ti;
-            const int k0 = cb.kb * BK;
-            if constexpr (VarTraits<VAR>::router) {
-              mbar_expect_tx(fb, ROUTER_BN * BK * 2);
-              tma_2d(dst, &tmB, fb, k0 % p.H, ti.row0);  // x, once for each part of Wr
-            } else {
-              // feature-major tokens, boxes of 64 tokens x 64 k (MN-major, 8 KB apart)
-              const int nbox = (ti.nrows + 63) / 64;
-              mbar_expect_tx(fb, nbox * B_BOX);
-              for (int q = 0; q < nbox; ++q) tma_2d(dst + q * B_BOX, &tmB, fb, ti.row0 + 64 * q, k0);
-            }
-            ++gb;
-            next(cb);
-            moved = true;
+          ++issued;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
           }
-        }
-        if (moved) {
-          t_last = clock64();
-        } else if (*abort_flag || clock64() - t_last > TIMEOUT_CYCLES) {
-          failed = true;
-          break;
         }
       }
       if (failed) {
@@ -609,19 +564,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         flag_status(p.status, USAF_DEV_TIMEOUT);
       }
       // let every issued copy land before the CTA can exit
-      for (uint32_t s = 0; s < SA && s < ga; ++s) {
-        const uint32_t last = ga - 1 - ((ga - 1 - s) % SA);
-        mbar_wait(fullA0 + 8 * s, (last / SA) & 1, abort_flag);
-      }
-      for (uint32_t s = 0; s < SB && s < gb; ++s) {
-        const uint32_t last = gb - 1 - ((gb - 1 - s) % SB);
-        mbar_wait(fullB0 + 8 * s, (last / SB) & 1, abort_flag);
+      for (int s = 0; s < STAGES && (uint32_t)s < issued; ++s) {
+        const uint32_t last = issued - 1 - ((issued - 1 - s) % STAGES);
+        mbar_wait(full0 + 8 * s, (last / STAGES) & 1, abort_flag);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
-      uint32_t g = 0;  // k-blocks consumed
+      int stage = 0;
+      uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
       constexpr bool a_mn = VarTraits<VAR>::a_mn;
@@ -638,24 +590,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t d = tmem_base + acc * BN;
         const uint32_t idesc = idesc_bf16(ti.nrows, a_mn, b_mn);
         const int nkb = (ti.klen + BK - 1) / BK;
-        for (int kb = 0; kb < nkb; ++kb, ++g) {
-          const uint32_t sa = g % SA, sb = g % SB;
-          if (!mbar_wait(fullA0 + 8 * sa, (g / SA) & 1, abort_flag) ||
-              !mbar_wait(fullB0 + 8 * sb, (g / SB) & 1, abort_flag)) {
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) {
             failed = true;
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(ringA + sa * A_BYTES);
-          const uint32_t b_base = smem_u32(ringB + sb * B_BYTES);
+          const uint32_t a_base = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t b_base = a_base + A_BYTES;
 #pragma unroll
           for (int ks = 0; ks < BK / 16; ++ks) {
             const uint64_t ad = sdesc(a_base + ks * a_step, a_lbo, 1024);
             const uint64_t bd = sdesc(b_base + ks * b_step, b_lbo, 1024);
             umma_bf16(d, ad, bd, idesc, (kb | ks) != 0 ? 1u : 0u);
           }
-          umma_commit(emptyA0 + 8 * sa);
-          umma_commit(emptyB0 + 8 * sb);
+          umma_commit(empty0 + 8 * stage);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
         }
         if (failed) break;
         umma_commit(tfull0 + 8 * acc);
