@@ -117,16 +117,18 @@ class MoELayer:
             self._main(stream).wait_event(self.ev_opt)
             self.pending_opt = False
 
-    def forward(self, x, stream=None):
+    def forward(self, x, stream=None, y=None):
         self.wait_optimizer(stream)
+        y = self.y if y is None else y
         B.moe_fwd(self.s, x, self.w_gate_up, self.w_down, self.rt, self.x_perm, self.h, self.wa,
-                  self.y, ws=self.ws_fwd, stream=stream)
-        return self.y
+                  y, ws=self.ws_fwd, stream=stream)
+        return y
 
-    def backward(self, x, dy, want_dx=True, stream=None):
+    def backward(self, x, dy, want_dx=True, stream=None, dx=None):
+        dx = self.dx if dx is None else dx
         B.moe_bwd_sparse(self.s, x, self.w_router, self.w_gate_up, self.w_down, self.rt,
                          self.x_perm, self.h, self.wa, dy, self.act, self.g_act, self.g_router,
-                         dx=self.dx if want_dx else None, logits=self.logits,
+                         dx=dx if want_dx else None, logits=self.logits,
                          renorm=self.renorm, dev_status=self.status, ws=self.ws_bwd,
                          stream=stream)
 
@@ -150,16 +152,17 @@ class MoELayer:
                            self.E * self.H, None, self.lr, b1, b2, self.eps, self.step_count,
                            skip_if_nonfinite, self.status, stream=main)
 
-    def train_step(self, x, dy, stream=None):
-        """route -> forward -> sparse backward -> SparseAdam (experts, router)."""
+    def train_step(self, x, dy, stream=None, y=None, dx=None):
+        """route -> forward -> sparse backward -> SparseAdam (experts, router). y and dx may name
+        other output buffers than the layer's own."""
         # per-step non-finite flag (a non-finite gradient skips this step), alternating words
         self.status = self.status2[self.step_count % 2:self.step_count % 2 + 1]
         self.status.zero_()
         self.route(x, stream)
-        self.forward(x, stream)
-        self.backward(x, dy, stream=stream)
+        y = self.forward(x, stream, y=y)
+        self.backward(x, dy, stream=stream, dx=dx)
         self.optimizer_step(stream)
-        return self.y, self.dx
+        return y, (self.dx if dx is None else dx)
 
     def train_step_host(self, x_host, dy_host, y_host, dx_host, x_dev, dy_dev, stream=None):
         """The same step fed from (pinned) host memory: copy x and dy in, run, copy y and dx out."""
@@ -168,6 +171,56 @@ class MoELayer:
         self.train_step(x_dev, dy_dev, stream)
         y_host.copy_(self.y, non_blocking=True)
         dx_host.copy_(self.dx, non_blocking=True)
+
+
+class HostStepper:
+    """Train steps fed from pinned host memory with the copies overlapped with compute: a step's
+    x and dY are copied in on one copy stream while the previous step computes, and its y and dx
+    are copied out on another while the next step computes. Two sets of device buffers alternate;
+    every step still moves its own inputs in and its own outputs out."""
+
+    def __init__(self, layer):
+        self.L = layer
+        d = layer.dev
+        shape = (layer.T, layer.H)
+        mk = lambda: [torch.empty(shape, dtype=layer.dtype, device=d) for _ in range(2)]
+        self.xd, self.dyd, self.yd, self.dxd = mk(), mk(), mk(), mk()
+        self.h2d = torch.cuda.Stream(device=d)
+        self.d2h = torch.cuda.Stream(device=d)
+        ev = lambda: [torch.cuda.Event() for _ in range(2)]
+        self.in_ready, self.computed, self.out_done = ev(), ev(), ev()
+        self.used = [False, False]
+        self.i = 0
+
+    def step(self, x_host, dy_host, y_host, dx_host, stream=None):
+        L = self.L
+        main = L._main(stream)
+        b = self.i % 2
+        if self.used[b]:
+            self.h2d.wait_event(self.computed[b])  # the step two back has read this input pair
+        with torch.cuda.stream(self.h2d):
+            self.xd[b].copy_(x_host, non_blocking=True)
+            self.dyd[b].copy_(dy_host, non_blocking=True)
+            self.in_ready[b].record(self.h2d)
+        main.wait_event(self.in_ready[b])
+        if self.used[b]:
+            main.wait_event(self.out_done[b])  # its outputs are out before they are overwritten
+        L.train_step(self.xd[b], self.dyd[b], stream=main, y=self.yd[b], dx=self.dxd[b])
+        self.computed[b].record(main)
+        self.d2h.wait_event(self.computed[b])
+        with torch.cuda.stream(self.d2h):
+            y_host.copy_(self.yd[b], non_blocking=True)
+            dx_host.copy_(self.dxd[b], non_blocking=True)
+            self.out_done[b].record(self.d2h)
+        self.used[b] = True
+        self.i += 1
+
+    def finish(self, stream=None):
+        """Make `stream` wait for the last outputs on the host and the last optimizer update."""
+        main = self.L._main(stream)
+        if self.i:
+            main.wait_event(self.out_done[(self.i - 1) % 2])
+        self.L.wait_optimizer(main)
 
 
 def active_count(N: int, frac: float = 0.005) -> int:

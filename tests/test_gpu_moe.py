@@ -293,3 +293,44 @@ def test_dense_wgrad_qwen3_shaped_sampled():
         ref = oracle.masked_expert_grad(act, inp["x"], inp["w_gate_up"], inp["w_down"], idx, w,
                                         inp["dy"], experts=[e])
         assert rel_l2(g[act], ref) <= 1e-2
+
+
+def test_host_stepper_matches_device_steps():
+    """Overlapped host-fed steps (copies on their own streams, double-buffered) give the outputs
+    and weights of the same steps fed from device memory."""
+    from sparse_moe_fine_gb300.layer import HostStepper, MoELayer
+    dev = device()
+    cfg = synth.small_config("host", T=256, H=256, E=8, k=2, I=128, bf16=True, frac=0.05)
+    inp = synth.moe_inputs(cfg, seed=4)
+    act = torch.from_numpy(synth.uniform_mask(cfg.N, cfg.K, seed=4)).to(dev)
+
+    def make():
+        bf = lambda a: torch.from_numpy(a).to(dev).to(torch.bfloat16)
+        return MoELayer(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, bf(inp["w_gate_up"]),
+                        bf(inp["w_down"]), torch.from_numpy(inp["w_router"]).to(dev), act,
+                        lr=1e-3, device=dev)
+    xs = [torch.from_numpy(synth.moe_inputs(cfg, seed=10 + i)["x"]).to(torch.bfloat16)
+          for i in range(3)]
+    dys = [torch.from_numpy(synth.moe_inputs(cfg, seed=20 + i)["dy"]).to(torch.bfloat16)
+           for i in range(3)]
+    a = make()
+    ref = []
+    for x, dy in zip(xs, dys):
+        y, dx = a.train_step(x.to(dev), dy.to(dev))
+        ref.append((y.float().cpu().clone(), dx.float().cpu().clone()))
+    a.wait_optimizer()
+    b = make()
+    hs = HostStepper(b)
+    outs = []
+    for x, dy in zip(xs, dys):
+        yh = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory()
+        dxh = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16).pin_memory()
+        hs.step(x.pin_memory(), dy.pin_memory(), yh, dxh)
+        outs.append((yh, dxh))
+    hs.finish()
+    torch.cuda.synchronize()
+    for (ry, rdx), (yh, dxh) in zip(ref, outs):
+        assert rel_l2(yh.float().numpy(), ry.numpy()) <= 1e-6
+        assert rel_l2(dxh.float().numpy(), rdx.numpy()) <= 1e-6
+    assert rel_l2(b.w_gate_up.float().cpu().numpy(), a.w_gate_up.float().cpu().numpy()) <= 1e-6
+    assert rel_l2(b.w_router.cpu().numpy(), a.w_router.cpu().numpy()) <= 1e-6
