@@ -383,12 +383,17 @@ __global__ void __launch_bounds__(ROUND_THREADS) sel_round_kernel(Src s, SelCtrl
   __syncthreads();
   if (!last) return;
   __threadfence();
+  // the whole block reads the global histogram at once (one load each), then one thread scans it
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+    hist[i] = i <= (int)dmask ? reinterpret_cast<volatile uint32_t*>(c->hist)[i] : 0u;
+    c->hist[i] = 0;
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
-    volatile uint32_t* gh = c->hist;
     uint32_t krem = c->k_rem, cum = 0;
     int d = (int)dmask;
     for (; d > 0; --d) {
-      const uint32_t h = gh[d];
+      const uint32_t h = hist[d];
       if (cum + h >= krem) break;
       cum += h;
     }
@@ -396,8 +401,6 @@ __global__ void __launch_bounds__(ROUND_THREADS) sel_round_kernel(Src s, SelCtrl
     c->prefix = prefix | ((uint32_t)d << shift);
     c->ticket = 0;
   }
-  __syncthreads();
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) c->hist[i] = 0;
 }
 
 // Per block: elements strictly above tau and equal to tau.
