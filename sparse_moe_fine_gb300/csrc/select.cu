@@ -25,6 +25,11 @@ constexpr int SAMPLE_S = 32768;
 // radix rounds over the 31-bit key, most significant digit first: bits 30..23, 22..15, 14..7, 6..0
 __host__ __device__ constexpr int round_shift(int r) { return r == 0 ? 23 : r == 1 ? 15 : r == 2 ? 7 : 0; }
 __host__ __device__ constexpr int round_bits(int r) { return r == 3 ? 7 : 8; }
+// the selection's own radix rounds: 8 bits (the exponent), then 12 and 11 bits
+constexpr int SEL_ROUNDS = 3;
+constexpr int MAX_BINS = 4096;
+__host__ __device__ constexpr int sel_shift(int r) { return r == 0 ? 23 : r == 1 ? 11 : 0; }
+__host__ __device__ constexpr int sel_bits(int r) { return r == 0 ? 8 : r == 1 ? 12 : 11; }
 
 struct SelCtrl {
   uint32_t tau0;
@@ -34,8 +39,9 @@ struct SelCtrl {
   unsigned long long total;
   uint32_t prefix;  // radix state: the K-th key's bits found so far
   uint32_t k_rem;   // rank still to find among keys matching prefix
-  uint32_t hist[256];
+  uint32_t hist[MAX_BINS];
   unsigned long long n_swapped;
+  uint32_t r0_done;  // the first radix digit was taken from the compacting pass's histogram
 };
 
 // Where block b's part of the source lives.
@@ -181,7 +187,7 @@ __device__ __forceinline__ void for_part(const Src& s, int mode, int b, F f) {
 // kernels
 // ------------------------------------------------------------------------------------------------
 __global__ void sel_init_kernel(SelCtrl* c, int64_t K, uint32_t* ccnt, int G) {
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) c->hist[i] = 0;
+  for (int i = threadIdx.x; i < MAX_BINS; i += blockDim.x) c->hist[i] = 0;
   for (int i = threadIdx.x; i < G; i += blockDim.x) ccnt[i] = 0;
   if (threadIdx.x == 0) {
     c->tau0 = 0;
@@ -192,6 +198,7 @@ __global__ void sel_init_kernel(SelCtrl* c, int64_t K, uint32_t* ccnt, int G) {
     c->prefix = 0;
     c->k_rem = (uint32_t)K;
     c->n_swapped = 0;
+    c->r0_done = 0;
   }
 }
 
@@ -276,6 +283,9 @@ __global__ void __launch_bounds__(COMPACT_WARPS * 32) sel_compact_kernel(
     uint32_t* __restrict__ ccnt, SelCtrl* c, int vec_ok, uint32_t* dev_status) {
   constexpr int UN = 4;
   constexpr int STEP = 128 * UN;
+  __shared__ uint32_t dhist[256];  // first radix digit (bits 30..23) of this block's candidates
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) dhist[i] = 0;
+  __syncthreads();
   const uint32_t tau0 = c->tau0;
   const int lane = threadIdx.x & 31;
   const int64_t r = (int64_t)blockIdx.x * COMPACT_WARPS + (threadIdx.x >> 5);
@@ -336,11 +346,15 @@ __global__ void __launch_bounds__(COMPACT_WARPS * 32) sel_compact_kernel(
             over = true;
           }
           ++pos;
+          atomicAdd(&dhist[key[j] >> sel_shift(0)], 1u);
         }
       }
       count += __shfl_sync(0xffffffffu, x, 31);
     }
   }
+  __syncthreads();
+  for (int i = threadIdx.x; i < 256; i += blockDim.x)
+    if (dhist[i]) atomicAdd(&c->hist[i], dhist[i]);
   if (lane == 0 && lo < N) {
     ccnt[r] = count < cap ? count : (uint32_t)cap;
     atomicAdd(&c->total, (unsigned long long)count);
@@ -349,33 +363,67 @@ __global__ void __launch_bounds__(COMPACT_WARPS * 32) sel_compact_kernel(
   flag_status_warp(dev_status, kmax >= 0x7F800000u, USAF_DEV_NONFINITE);
 }
 
+// One block of 256 threads: the candidate path or the exact path, and on the candidate path the
+// first radix digit from the histogram the compacting pass built (so the first round is skipped).
 __global__ void sel_decide_kernel(SelCtrl* c, int64_t K, int sampling, uint32_t* dev_status) {
-  if (threadIdx.x != 0) return;
-  const bool ok = sampling && !c->overflow && c->total >= (unsigned long long)K;
-  c->mode = ok ? 1u : 0u;
-  if (sampling && !ok) flag_status(dev_status, USAF_DEV_SELECT_EXACT_PATH);
+  __shared__ uint32_t h[256];
+  __shared__ bool ok;
+  if (threadIdx.x == 0) {
+    ok = sampling && !c->overflow && c->total >= (unsigned long long)K;
+    c->mode = ok ? 1u : 0u;
+    if (sampling && !ok) flag_status(dev_status, USAF_DEV_SELECT_EXACT_PATH);
+  }
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+    h[i] = reinterpret_cast<volatile uint32_t*>(c->hist)[i];
+    c->hist[i] = 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && ok) {
+    const uint32_t dmask = (1u << sel_bits(0)) - 1;
+    uint32_t krem = c->k_rem, cum = 0;
+    int d = (int)dmask;
+    for (; d > 0; --d) {
+      if (cum + h[d] >= krem) break;
+      cum += h[d];
+    }
+    c->k_rem = krem - cum;
+    c->prefix = (uint32_t)d << sel_shift(0);
+    c->r0_done = 1;
+  }
 }
 
-// One radix round over the source. The last block to finish picks the digit.
+// One radix round over the source (digits of up to 12 bits). Each block counts the digits of the
+// keys that match the prefix found so far into a shared histogram and adds it to the global one;
+// the last block to finish picks the digit with a block-wide scan from the top. The first round's
+// digits (the exponent) fall in few bins, so a warp adds equal digits once; later rounds' digits
+// are spread out and each key adds its own.
 __global__ void __launch_bounds__(ROUND_THREADS) sel_round_kernel(Src s, SelCtrl* c, int shift,
                                                                 int bits, int fixed_mode) {
-  __shared__ uint32_t hist[256];
+  __shared__ uint32_t hist[MAX_BINS];
   __shared__ bool last;
+  __shared__ int pick;
+  if (shift == sel_shift(0) && c->r0_done) return;  // taken during the compacting pass
   const int mode = fixed_mode >= 0 ? fixed_mode : (int)c->mode;
-  const uint32_t dmask = (1u << bits) - 1;
+  const int nb = 1 << bits;
+  const uint32_t dmask = (uint32_t)nb - 1;
   const int hs = shift + bits;
   const uint32_t prefix = c->prefix;
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+  for (int i = threadIdx.x; i < nb; i += blockDim.x) hist[i] = 0;
   __syncthreads();
+  const bool first = shift == sel_shift(0);  // exponent digits: few bins, aggregate per warp
   for (int b = blockIdx.x; b < s.G; b += gridDim.x)
   for_part(s, mode, b, [&](uint32_t key, int64_t, bool ok) {
     const bool m = ok && (hs >= 32 || (key >> hs) == (prefix >> hs));
-    const int d = m ? (int)((key >> shift) & dmask) : -1 - (int)(threadIdx.x & 31);
-    const unsigned peers = __match_any_sync(0xffffffffu, d);
-    if (m && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[d], __popc(peers));
+    const int d = (int)((key >> shift) & dmask);
+    if (first) {
+      const unsigned peers = __match_any_sync(0xffffffffu, m ? d : -1 - (int)(threadIdx.x & 31));
+      if (m && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[d], __popc(peers));
+    } else if (m) {
+      atomicAdd(&hist[d], 1u);
+    }
   });
   __syncthreads();
-  for (int i = threadIdx.x; i <= (int)dmask; i += blockDim.x)
+  for (int i = threadIdx.x; i < nb; i += blockDim.x)
     if (hist[i]) atomicAdd(&c->hist[i], hist[i]);
   __threadfence();
   __syncthreads();
@@ -383,22 +431,34 @@ __global__ void __launch_bounds__(ROUND_THREADS) sel_round_kernel(Src s, SelCtrl
   __syncthreads();
   if (!last) return;
   __threadfence();
-  // the whole block reads the global histogram at once (one load each), then one thread scans it
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) {
-    hist[i] = i <= (int)dmask ? reinterpret_cast<volatile uint32_t*>(c->hist)[i] : 0u;
+  for (int i = threadIdx.x; i < nb; i += blockDim.x) {
+    hist[i] = reinterpret_cast<volatile uint32_t*>(c->hist)[i];
     c->hist[i] = 0;
+  }
+  if (threadIdx.x == 0) pick = 0;
+  __syncthreads();
+  // thread t owns the per = nb / blockDim bins just below the (t)-th slice from the top
+  const int per = (nb + blockDim.x - 1) / blockDim.x;
+  const int hi = nb - 1 - threadIdx.x * per;  // highest digit of this thread's slice
+  uint32_t mine = 0;
+  for (int j = 0; j < per && hi - j >= 0; ++j) mine += hist[hi - j];
+  uint32_t tot;
+  const uint32_t above = block_excl_scan(mine, &tot);  // keys in the slices above this one
+  const uint32_t krem = c->k_rem;
+  if (above < krem && krem <= above + mine) {
+    uint32_t cum = above;
+    int d = hi;
+    for (int j = 0; j < per && hi - j >= 0; ++j) {
+      d = hi - j;
+      if (cum + hist[d] >= krem) break;
+      cum += hist[d];
+    }
+    pick = d;
+    c->k_rem = krem - cum;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    uint32_t krem = c->k_rem, cum = 0;
-    int d = (int)dmask;
-    for (; d > 0; --d) {
-      const uint32_t h = hist[d];
-      if (cum + h >= krem) break;
-      cum += h;
-    }
-    c->k_rem = krem - cum;
-    c->prefix = prefix | ((uint32_t)d << shift);
+    c->prefix = prefix | ((uint32_t)pick << shift);
     c->ticket = 0;
   }
 }
@@ -499,7 +559,7 @@ usaf_status run_select(const SelPlan& p, const SelWs& w, Src s, int64_t K, int64
         s.g, s.n, p.L, s.excl, p.cap, w.ckeys, w.cids, w.ccnt, w.ctrl, vec_ok, dev_status);
     USAF_CHECK_LAUNCH();
   }
-  sel_decide_kernel<<<1, 32, 0, st>>>(w.ctrl, K, p.sampling && !fixed_drop ? 1 : 0, dev_status);
+  sel_decide_kernel<<<1, 256, 0, st>>>(w.ctrl, K, p.sampling && !fixed_drop ? 1 : 0, dev_status);
   USAF_CHECK_LAUNCH();
   s.ckeys = w.ckeys;
   s.cids = w.cids;
@@ -510,9 +570,8 @@ usaf_status run_select(const SelPlan& p, const SelWs& w, Src s, int64_t K, int64
   const int rgrid = (int)std::min<int64_t>(p.G, device_sm_count() * 8);
   {
     USAF_TRACE("select_radix", st);
-    for (int r = 0; r < 4; ++r) {
-      sel_round_kernel<<<rgrid, ROUND_THREADS, 0, st>>>(s, w.ctrl, round_shift(r), round_bits(r),
-                                                        fm);
+    for (int r = 0; r < SEL_ROUNDS; ++r) {
+      sel_round_kernel<<<rgrid, ROUND_THREADS, 0, st>>>(s, w.ctrl, sel_shift(r), sel_bits(r), fm);
       USAF_CHECK_LAUNCH();
     }
   }
