@@ -84,7 +84,7 @@ SelPlan make_plan(int64_t N, int64_t K) {
   p.sampling = N >= (int64_t)4 * 1024 * 1024 && K * 16 <= N;
   if (p.sampling) {
     const double q = std::ceil((double)SAMPLE_S * (double)K / (double)N);
-    const double qq = q + 8.0 * std::sqrt(q) + 32.0;
+    const double qq = q + 5.0 * std::sqrt(q) + 16.0;  // 5 sigma above the expected rank
     p.q = (int)std::min<double>(qq, SAMPLE_S);
     if (p.q >= SAMPLE_S / 8) p.sampling = false;
   }
