@@ -20,27 +20,53 @@ __global__ void nonfinite_scan_kernel(const float* __restrict__ g, int64_t n,
 }
 
 template <typename W>
+__device__ __forceinline__ void adam_one(int64_t i, float gi, float& pi, float& mi, float& vi,
+                                         const int64_t* __restrict__ idx, W* __restrict__ w0,
+                                         int64_t n0, W* __restrict__ w1, float b1, float b2,
+                                         float om_b1, float om_b2, float eps, float step_size) {
+  mi = fmaf(b1, mi, om_b1 * gi);
+  vi = fmaf(b2, vi, om_b2 * gi * gi);
+  pi = pi - step_size * (mi / (sqrtf(vi) + eps));
+  const int64_t f = idx ? idx[i] : i;
+  if (f < n0) w0[f] = from_f32<W>(pi);
+  else w1[f - n0] = from_f32<W>(pi);
+}
+
+// Four consecutive entries per thread with 16-byte loads and stores of g, p, m, v (all four
+// arrays 16-byte aligned), the rest one by one.
+template <typename W>
 __global__ void __launch_bounds__(256) adam_kernel(int64_t n, const int64_t* __restrict__ idx,
                                                    const float* __restrict__ g,
                                                    float* __restrict__ p, float* __restrict__ m,
                                                    float* __restrict__ v, W* __restrict__ w0,
                                                    int64_t n0, W* __restrict__ w1, float b1,
                                                    float b2, float om_b1, float om_b2, float eps,
-                                                   float step_size, int skip,
+                                                   float step_size, int skip, int vec,
                                                    const uint32_t* dev_status) {
   if (skip && dev_status && (*(volatile const uint32_t*)dev_status & USAF_DEV_NONFINITE)) return;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+  const int64_t n4 = vec ? n / 4 : 0;
+  for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n4;
+       q += (int64_t)gridDim.x * blockDim.x) {
+    const float4 g4 = reinterpret_cast<const float4*>(g)[q];
+    float4 p4 = reinterpret_cast<const float4*>(p)[q];
+    float4 m4 = reinterpret_cast<const float4*>(m)[q];
+    float4 v4 = reinterpret_cast<const float4*>(v)[q];
+    const int64_t i = 4 * q;
+    adam_one(i, g4.x, p4.x, m4.x, v4.x, idx, w0, n0, w1, b1, b2, om_b1, om_b2, eps, step_size);
+    adam_one(i + 1, g4.y, p4.y, m4.y, v4.y, idx, w0, n0, w1, b1, b2, om_b1, om_b2, eps, step_size);
+    adam_one(i + 2, g4.z, p4.z, m4.z, v4.z, idx, w0, n0, w1, b1, b2, om_b1, om_b2, eps, step_size);
+    adam_one(i + 3, g4.w, p4.w, m4.w, v4.w, idx, w0, n0, w1, b1, b2, om_b1, om_b2, eps, step_size);
+    reinterpret_cast<float4*>(p)[q] = p4;
+    reinterpret_cast<float4*>(m)[q] = m4;
+    reinterpret_cast<float4*>(v)[q] = v4;
+  }
+  for (int64_t i = 4 * n4 + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const float gi = g[i];
-    const float mi = fmaf(b1, m[i], om_b1 * gi);
-    const float vi = fmaf(b2, v[i], om_b2 * gi * gi);
-    const float pi = p[i] - step_size * (mi / (sqrtf(vi) + eps));
+    float pi = p[i], mi = m[i], vi = v[i];
+    adam_one(i, g[i], pi, mi, vi, idx, w0, n0, w1, b1, b2, om_b1, om_b2, eps, step_size);
+    p[i] = pi;
     m[i] = mi;
     v[i] = vi;
-    p[i] = pi;
-    const int64_t f = idx ? idx[i] : i;
-    if (f < n0) w0[f] = from_f32<W>(pi);
-    else w1[f - n0] = from_f32<W>(pi);
   }
 }
 
@@ -54,6 +80,9 @@ usaf_status adam_launch(int64_t n, const int64_t* idx, const float* g, float* p,
   int64_t blocks = ceil_div(n, threads);
   const int cap = device_sm_count() * 8;
   if (blocks > cap) blocks = cap;
+  const auto al = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
+  const int vec = al(g) && al(p) && al(m) && al(v) ? 1 : 0;
+  const int64_t ublocks = std::max<int64_t>(1, ceil_div(vec ? ceil_div(n, 4) : n, threads));
   if (skip) {
     nonfinite_scan_kernel<<<(unsigned)blocks, threads, 0, st>>>(g, n, dev_status);
     USAF_CHECK_LAUNCH();
@@ -65,13 +94,14 @@ usaf_status adam_launch(int64_t n, const int64_t* idx, const float* g, float* p,
   const float om_b1 = (float)(1.0 - b1), om_b2 = (float)(1.0 - b2);
   const float b1f = (float)b1, b2f = (float)b2, epsf = (float)eps;
   if (wdt == USAF_BF16)
-    adam_kernel<__nv_bfloat16><<<(unsigned)blocks, threads, 0, st>>>(
+    adam_kernel<__nv_bfloat16><<<(unsigned)ublocks, threads, 0, st>>>(
         n, idx, g, p, m, v, static_cast<__nv_bfloat16*>(w0), n0,
-        static_cast<__nv_bfloat16*>(w1), b1f, b2f, om_b1, om_b2, epsf, step_size, skip, dev_status);
+        static_cast<__nv_bfloat16*>(w1), b1f, b2f, om_b1, om_b2, epsf, step_size, skip, vec,
+        dev_status);
   else
-    adam_kernel<float><<<(unsigned)blocks, threads, 0, st>>>(
+    adam_kernel<float><<<(unsigned)ublocks, threads, 0, st>>>(
         n, idx, g, p, m, v, static_cast<float*>(w0), n0, static_cast<float*>(w1), b1f, b2f, om_b1,
-        om_b2, epsf, step_size, skip, dev_status);
+        om_b2, epsf, step_size, skip, vec, dev_status);
   USAF_CHECK_LAUNCH();
   return USAF_OK;
 }

@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(1024) sel_sample_tau_kernel(const uint32_t* __
 // Four consecutive elements of g from i0 (zeros past hi), one 16-byte load when possible.
 __device__ __forceinline__ float4 load4(const float* __restrict__ g, int64_t i0, int64_t hi,
                                         int vec_ok) {
-  if (vec_ok && i0 + 3 < hi) return __ldcs(reinterpret_cast<const float4*>(g + i0));
+  if (vec_ok && i0 + 3 < hi) return __ldg(reinterpret_cast<const float4*>(g + i0));
   float4 v;
   v.x = i0 < hi ? g[i0] : 0.f;
   v.y = i0 + 1 < hi ? g[i0 + 1] : 0.f;
