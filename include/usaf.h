@@ -189,6 +189,19 @@ usaf_status usaf_moe_bwd_sparse(const usaf_moe_shape* shape, usaf_dtype dtype, i
                                 void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * usaf_moe_bwd_sparse_accumulate - usaf_moe_bwd_sparse for one micro-batch of a step that
+ * accumulates gradients over several (USAF README environment table: MICROBATCH): g_act and
+ * g_router are added to instead of overwritten; dx and dw_slot are this micro-batch's own, as
+ * in usaf_moe_bwd_sparse. Same arguments, workspace and errors as usaf_moe_bwd_sparse.
+ * ------------------------------------------------------------------------------------------- */
+usaf_status usaf_moe_bwd_sparse_accumulate(
+    const usaf_moe_shape* shape, usaf_dtype dtype, int renorm, const void* x,
+    const float* w_router, const void* w_gate_up, const void* w_down, const usaf_routing* rt,
+    const float* logits, const void* x_perm_save, const void* h_save, const void* wa_save,
+    const void* dy, const int64_t* act_idx, int64_t K, float* g_act, float* g_router, void* dx,
+    float* dw_slot, uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
  * usaf_moe_bwd_dense - the same backward as usaf_moe_bwd_sparse (dh, dw, router gradient, dx),
  * with the expert weight gradient formed densely for the importance phase (USAF README: the
  * weights to train are the 0.5% with the largest gradient magnitude, found by a dense gradient
@@ -197,8 +210,8 @@ usaf_status usaf_moe_bwd_sparse(const usaf_moe_shape* shape, usaf_dtype dtype, i
  *   gate_up entry (e, r, c) = sum over rows of expert e of dh[row, r] * x[tok, c];
  *   down entry (e, r, c)    = sum over rows of expert e of dy[tok, r] * w * A[row, c];
  * experts without tokens give 0.
- *   g_dense     [N] fp32, 16-byte aligned; accumulate = 1 adds into it (micro-batch
- *               accumulation), 0 overwrites it
+ *   g_dense     [N] fp32, 16-byte aligned; accumulate = 1 adds into it and into g_router
+ *               (micro-batch accumulation), 0 overwrites both
  *   the other arguments and the workspace (usaf_moe_bwd_workspace_size with K = 0) as for
  *   usaf_moe_bwd_sparse
  * bf16 layers form g_dense on tensor cores (fp32 accumulation; stores or adds by TMA); fp32

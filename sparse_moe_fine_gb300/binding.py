@@ -76,6 +76,9 @@ _SIGS = {
     "usaf_trace_summary": (_INT, [_P, _INT]),
     "usaf_rigl_swap": (_INT, [_P, _I64, _P, _I64, _I64, _P, _P, _P, _P, _I64, _P, _INT, _P, _P, _P,
                               _P, _P, _P, _P, _SZ, _P]),
+    "usaf_moe_bwd_sparse_accumulate": (_INT, [_P, _INT, _INT, _P, _P, _P, _P, _P, _P, _P, _P,
+                                              _P, _P, _P, _I64, _P, _P, _P, _P, _P, _P, _SZ,
+                                              _P]),
     "usaf_moe_bwd_dense": (_INT, [_P, _INT, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                   _INT, _P, _P, _P, _P, _P, _SZ, _P]),
     "usaf_reselect_full_workspace_size": (_SZ, [_I64, _I64]),
@@ -226,6 +229,22 @@ def moe_bwd_sparse(s: Shape, x, w_router, w_gate_up, w_down, rt: Routing, x_perm
         ws = _ws(moe_bwd_workspace_size(s, dt, K), x.device)
     r = rt.c()
     _check("usaf_moe_bwd_sparse", lib().usaf_moe_bwd_sparse(
+        ctypes.byref(s), dt, int(renorm), _ptr(x), _ptr(w_router), _ptr(w_gate_up), _ptr(w_down),
+        ctypes.byref(r), _ptr(logits), _ptr(x_perm), _ptr(h), _ptr(wa), _ptr(dy), _ptr(act_idx),
+        K, _ptr(g_act), _ptr(g_router), _ptr(dx), _ptr(dw_slot), _ptr(dev_status), _ptr(ws),
+        ws.numel(), _stream(stream)))
+
+
+def moe_bwd_sparse_accumulate(s: Shape, x, w_router, w_gate_up, w_down, rt: Routing, x_perm,
+                              h, wa, dy, act_idx, g_act, g_router, dx=None, dw_slot=None,
+                              logits=None, renorm=1, dev_status=None, ws=None, stream=None):
+    """moe_bwd_sparse that adds this micro-batch's g_act and g_router to the buffers."""
+    dt = _dt(x)
+    K = 0 if act_idx is None else act_idx.numel()
+    if ws is None:
+        ws = _ws(moe_bwd_workspace_size(s, dt, K), x.device)
+    r = rt.c()
+    _check("usaf_moe_bwd_sparse_accumulate", lib().usaf_moe_bwd_sparse_accumulate(
         ctypes.byref(s), dt, int(renorm), _ptr(x), _ptr(w_router), _ptr(w_gate_up), _ptr(w_down),
         ctypes.byref(r), _ptr(logits), _ptr(x_perm), _ptr(h), _ptr(wa), _ptr(dy), _ptr(act_idx),
         K, _ptr(g_act), _ptr(g_router), _ptr(dx), _ptr(dw_slot), _ptr(dev_status), _ptr(ws),

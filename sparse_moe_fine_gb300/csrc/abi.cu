@@ -259,6 +259,29 @@ usaf_status usaf_moe_bwd_sparse(const usaf_moe_shape* s, usaf_dtype dt, int reno
                         static_cast<cudaStream_t>(stream));
 }
 
+usaf_status usaf_moe_bwd_sparse_accumulate(
+    const usaf_moe_shape* s, usaf_dtype dt, int renorm, const void* x, const float* w_router,
+    const void* w_gate_up, const void* w_down, const usaf_routing* rt, const float* logits,
+    const void* x_perm_save, const void* h_save, const void* wa_save, const void* dy,
+    const int64_t* act_idx, int64_t K, float* g_act, float* g_router, void* dx, float* dw_slot,
+    uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
+  MoeArgs a{};
+  USAF_TRY(fill_args(a, s, dt, x, w_router, w_gate_up, w_down, rt));
+  if (renorm != 0 && renorm != 1) return USAF_ERR_INVALID_ARG;
+  if (!w_router || !x_perm_save || !h_save || !wa_save || !dy || !g_router)
+    return USAF_ERR_INVALID_ARG;
+  if (renorm == 0 && !logits) return USAF_ERR_INVALID_ARG;
+  const int64_t N = s->E * 3 * s->I * s->H;
+  if (K < 0 || K > N || (K > 0 && (!act_idx || !g_act))) return USAF_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < usaf_moe_bwd_workspace_size(s, dt, K)) return USAF_ERR_WORKSPACE;
+  Carver c(ws);
+  BwdWs w;
+  bwd_ws_layout(*s, dt, K, c, w);
+  return moe_bwd_launch(a, renorm, logits, x_perm_save, h_save, wa_save, dy, act_idx, K, g_act,
+                        g_router, dx, dw_slot, nullptr, 1, dev_status, w,
+                        static_cast<cudaStream_t>(stream));
+}
+
 usaf_status usaf_moe_bwd_dense(const usaf_moe_shape* s, usaf_dtype dt, int renorm, const void* x,
                                const float* w_router, const void* w_gate_up, const void* w_down,
                                const usaf_routing* rt, const float* logits,

@@ -398,7 +398,8 @@ __global__ void __launch_bounds__(SD_WARPS * 32, 2) sddmm_kernel(
     const int64_t* __restrict__ act, int64_t K, const int32_t* __restrict__ cnt,
     const int32_t* __restrict__ off, int H, int I, int64_t Ngu, int64_t rcap,
     const T* __restrict__ dhT, const T* __restrict__ xT, const T* __restrict__ dyT,
-    const T* __restrict__ waT, float* __restrict__ g_act, uint32_t m16, uint32_t* dev_status) {
+    const T* __restrict__ waT, float* __restrict__ g_act, uint32_t m16, int accumulate,
+    uint32_t* dev_status) {
   constexpr int VW = 16 / sizeof(T);
   constexpr int U = 8;   // entries whose loads are in flight together in a full pass
   constexpr int RU = 2;  // remainder rounds whose first loads are in flight together
@@ -508,8 +509,9 @@ __global__ void __launch_bounds__(SD_WARPS * 32, 2) sddmm_kernel(
       const float gsum = transpose_reduce16(part, lane);
       const int64_t q = b0 + 16 * hf + lane;
       if (lane < 16 && q < lim) {
-        g_act[q] = gsum;
-        bad |= !finite_f(gsum);
+        const float gv = accumulate ? g_act[q] + gsum : gsum;
+        g_act[q] = gv;
+        bad |= !finite_f(gv);
       }
     }
     __syncwarp();  // the next batch rewrites meta
@@ -523,7 +525,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) g_router_sel_kernel(
     const T* __restrict__ xT, const float* __restrict__ dl_perm, const int32_t* __restrict__ cnt,
     const int32_t* __restrict__ off, int E, int H, int64_t rcap, float* __restrict__ g_router,
-    uint32_t* dev_status) {
+    int accumulate, uint32_t* dev_status) {
   constexpr int VW = 16 / sizeof(T);
   const int lane = threadIdx.x & 31, grp = lane >> 3, gl = lane & 7;
   const int64_t groups = (int64_t)gridDim.x * (blockDim.x >> 3);
@@ -551,8 +553,9 @@ __global__ void __launch_bounds__(256) g_router_sel_kernel(
     acc += __shfl_xor_sync(0xffffffffu, acc, 2);
     acc += __shfl_xor_sync(0xffffffffu, acc, 1);
     if (gl == 0 && u < (int64_t)E * H) {
-      g_router[u] = acc;
-      bad |= !finite_f(acc);
+      const float gv = accumulate ? g_router[u] + acc : acc;
+      g_router[u] = gv;
+      bad |= !finite_f(gv);
     }
   }
   flag_status_warp(dev_status, bad, USAF_DEV_NONFINITE);
@@ -636,13 +639,14 @@ __global__ void dlogit_dense_kernel(const float* __restrict__ logits,
 template <typename T>
 __global__ void g_router_dense_kernel(const T* __restrict__ x, const float* __restrict__ dlogit,
                                       int Tn, int E, int H, float* __restrict__ g_router,
-                                      uint32_t* dev_status) {
+                                      int accumulate, uint32_t* dev_status) {
   const int e = blockIdx.y;
   const int h = blockIdx.x * blockDim.x + threadIdx.x;
   float acc = 0.f;
   if (h < H) {
     for (int t = 0; t < Tn; ++t)
       acc = fmaf(dlogit[(int64_t)t * E + e], to_f32(x[(int64_t)t * H + h]), acc);
+    if (accumulate) acc += g_router[(int64_t)e * H + h];
     g_router[(int64_t)e * H + h] = acc;
   }
   flag_status_warp(dev_status, h < H && !finite_f(acc), USAF_DEV_NONFINITE);
@@ -868,14 +872,14 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
           a.rt.topk_w, dw, a.rt.slot_row, Tn, k, w.dl, w.dl_perm);
       USAF_CHECK_LAUNCH();
       g_router_sel_kernel<T><<<(unsigned)ceil_div(s.E * s.H, 32), 256, 0, st>>>(
-          xT, w.dl_perm, cnt, off, E, H, a.R_cap, g_router, dev_status);
+          xT, w.dl_perm, cnt, off, E, H, a.R_cap, g_router, accumulate, dev_status);
       USAF_CHECK_LAUNCH();
     } else {
       dlogit_dense_kernel<<<(unsigned)Tn, 128, 0, st>>>(logits, a.rt.topk_idx, a.rt.topk_w, dw,
                                                         Tn, E, k, w.dlogit);
       USAF_CHECK_LAUNCH();
       g_router_dense_kernel<T><<<dim3((unsigned)ceil_div(H, 128), (unsigned)E), 128, 0, st>>>(
-          static_cast<const T*>(a.x), w.dlogit, Tn, E, H, g_router, dev_status);
+          static_cast<const T*>(a.x), w.dlogit, Tn, E, H, g_router, accumulate, dev_status);
       USAF_CHECK_LAUNCH();
     }
   }
@@ -909,7 +913,7 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
                                                         device_sm_count() * 2);
     sddmm_kernel<T><<<blocks, SD_WARPS * 32, 0, st>>>(act_idx, K, cnt, off, H, I, Ngu, a.R_cap,
                                                       dhT, xT, dyT, waT, g_act, 65536u,
-                                                      dev_status);
+                                                      accumulate, dev_status);
     USAF_CHECK_LAUNCH();
   }
   // dense expert weight gradients (importance phase)
