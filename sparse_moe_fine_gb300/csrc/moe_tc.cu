@@ -398,13 +398,43 @@ __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32
     } else if constexpr (VAR == V_DOWN || VAR == V_DX) {
       float v[32];
       tmem_ld32(taddr + ch * 32, v);
-      const int hh = ti.m0 + row;
+      // 4x4 transposes inside each group of four lanes: lane 4a + c then holds column j0 + c for
+      // rows 4a .. 4a + 3 and adds them with one 16-byte vector atomic
       const int tokv = slot >= 0 ? tok : -1;  // the column's token, -1 for a padding row
+      const int pc = lane & 3;
+      const int hq = ti.m0 + row - lane + (lane & ~3);  // first of this lane's four rows
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        if (j >= ncol) break;
-        const int tj = __shfl_sync(FULL, tokv, j);
-        if (tj >= 0 && hh < H) atomicAdd(&p.acc_out[(int64_t)tj * H + hh], v[j]);
+      for (int j0 = 0; j0 < 32; j0 += 4) {
+        if (j0 >= ncol) break;
+        float x0 = v[j0], x1 = v[j0 + 1], x2 = v[j0 + 2], x3 = v[j0 + 3];
+        {
+          const bool h2 = (pc & 2) != 0;
+          const float b0 = __shfl_xor_sync(FULL, h2 ? x0 : x2, 2);
+          const float b1 = __shfl_xor_sync(FULL, h2 ? x1 : x3, 2);
+          if (h2) {
+            x0 = b0;
+            x1 = b1;
+          } else {
+            x2 = b0;
+            x3 = b1;
+          }
+        }
+        {
+          const bool h1 = (pc & 1) != 0;
+          const float d0 = __shfl_xor_sync(FULL, h1 ? x0 : x1, 1);
+          const float d1 = __shfl_xor_sync(FULL, h1 ? x2 : x3, 1);
+          if (h1) {
+            x0 = d0;
+            x2 = d1;
+          } else {
+            x1 = d0;
+            x3 = d1;
+          }
+        }
+        const int tj = __shfl_sync(FULL, tokv, j0 + pc);
+        if (tj >= 0 && hq < H)
+          atomicAdd(reinterpret_cast<float4*>(&p.acc_out[(int64_t)tj * H + hq]),
+                    make_float4(x0, x1, x2, x3));
       }
     } else {  // V_GVEC: SwiGLU backward, dh^T and the routing-weight gradient dw
       const int i = ti.m0 + row;
