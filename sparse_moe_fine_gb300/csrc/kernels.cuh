@@ -39,6 +39,10 @@ struct BwdWs {
 void fwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, Carver& c, FwdWs& w);
 void bwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, int64_t K, Carver& c, BwdWs& w);
 
+// Tokens per tensor-core tile at most; the per-expert tile plan (written by the gathers) counts
+// ceil(padded rows / TC_TOKEN_TILE) tiles per expert.
+constexpr int TC_TOKEN_TILE = 256;
+
 struct MoeArgs {
   usaf_moe_shape s;
   usaf_dtype dt;
@@ -64,7 +68,6 @@ usaf_status moe_bwd_launch(const MoeArgs& a, int renorm, const float* logits, co
 bool tc_shape_ok(const usaf_moe_shape& s);
 usaf_status tc_router_logits(const usaf_moe_shape& s, const void* x, const float* wr, void* wr3,
                              float* logits, cudaStream_t st);
-usaf_status tc_plan(const MoeArgs& a, cudaStream_t st);
 usaf_status tc_fwd_gate_up(const MoeArgs& a, const void* xT, void* hT, void* waT,
                            cudaStream_t st);
 usaf_status tc_fwd_down(const MoeArgs& a, const void* wa, float* y_acc, cudaStream_t st);

@@ -218,6 +218,71 @@ __global__ void swiglu_bwd_rows_kernel(const float* __restrict__ gvec, const T* 
 // Gathers, masked gradient, router
 // ================================================================================================
 
+// Side duties of a gather launch, so that they need no launch of their own: zero up to two fp32
+// buffers (16-byte aligned), and in block (0, 0) write the tensor-core tile plan (per expert
+// ceil(padded rows / TC_TOKEN_TILE), exclusive prefix over experts, E <= 1024).
+struct GatherExtra {
+  float* z0;
+  int64_t n0;
+  float* z1;
+  int64_t n1;
+  const int32_t* off;
+  int E;
+  int32_t* plan;
+};
+
+__device__ void zero_slice(float* z, int64_t n) {
+  if (!z || n == 0) return;
+  const int64_t nb = (int64_t)gridDim.x * gridDim.y, b = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;
+  if ((reinterpret_cast<uintptr_t>(z) & 15) != 0) {  // a caller buffer off a 16-byte boundary
+    for (int64_t i = b * blockDim.x + threadIdx.x; i < n; i += nb * blockDim.x) z[i] = 0.f;
+    return;
+  }
+  const int64_t n4 = n & ~int64_t(3);
+  const int64_t per = ((n4 / 4 + nb - 1) / nb) * 4;
+  const int64_t lo = b * per, hi = min(n4, lo + per);
+  for (int64_t i = lo + 4 * threadIdx.x; i < hi; i += 4 * blockDim.x)
+    *reinterpret_cast<float4*>(z + i) = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (b == 0 && threadIdx.x < n - n4) z[n4 + threadIdx.x] = 0.f;
+}
+
+__device__ void tile_plan(const int32_t* __restrict__ off, int E, int32_t* __restrict__ plan) {
+  __shared__ int32_t wsum[32];
+  constexpr int PER = 4;  // experts per thread (256 threads, E <= 1024)
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int32_t n[PER], tot = 0;
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int e = threadIdx.x * PER + j;
+    n[j] = e < E ? (off[e + 1] - off[e] + TC_TOKEN_TILE - 1) / TC_TOKEN_TILE : 0;
+    tot += n[j];
+  }
+  int32_t v = tot;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += y;
+  }
+  if (lane == 31) wsum[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    int32_t w = lane < (int)(blockDim.x >> 5) ? wsum[lane] : 0;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    wsum[lane] = w;
+  }
+  __syncthreads();
+  int32_t run = v - tot + (wid > 0 ? wsum[wid - 1] : 0);
+#pragma unroll
+  for (int j = 0; j < PER; ++j) {
+    const int e = threadIdx.x * PER + j;
+    if (e < E) plan[e] = run;
+    run += n[j];
+    if (e == E - 1) plan[E] = run;
+  }
+}
+
 // Gather-transpose: xT[h, row] = x[perm_tok[row], h] for routed rows, 0 for padding and tail
 // rows. A block moves a 128-row x 64-feature tile through shared memory with 16-byte accesses, so
 // each feature row of xT receives 256 contiguous bytes (bf16).
@@ -226,7 +291,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) gather_transpose_kernel(
     const T* __restrict__ x, const int32_t* __restrict__ ptok, const int32_t* __restrict__ pslot,
     const int32_t* __restrict__ off_end, int64_t R_cap, int H, T* __restrict__ xT,
-    const float* __restrict__ topk_w, float* __restrict__ wperm) {
+    const float* __restrict__ topk_w, float* __restrict__ wperm, GatherExtra ex) {
   constexpr int VW = 16 / sizeof(T);  // elements per 16-byte vector
   // feature f's row of the tile is rotated by (f / VW) * VW columns: the column writes of the
   // load phase then fall in distinct banks, and the 16-byte reads of the store phase stay aligned
@@ -256,6 +321,9 @@ __global__ void __launch_bounds__(256) gather_transpose_kernel(
       tile[ff * GT_ROWS + (r + (ff / VW) * VW) % GT_ROWS] = buf[q];
     }
   }
+  zero_slice(ex.z0, ex.n0);
+  zero_slice(ex.z1, ex.n1);
+  if (ex.plan && blockIdx.x == 0 && blockIdx.y == 0) tile_plan(ex.off, ex.E, ex.plan);
   if (wperm && blockIdx.y == 0) {
     for (int r = threadIdx.x; r < GT_ROWS; r += blockDim.x) {
       const int64_t row = r0 + r;
@@ -561,11 +629,6 @@ __global__ void __launch_bounds__(256) g_router_sel_kernel(
   flag_status_warp(dev_status, bad, USAF_DEV_NONFINITE);
 }
 
-__global__ void zero_f32_kernel(float* __restrict__ p, int64_t n) {
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
-       i += (int64_t)gridDim.x * blockDim.x)
-    p[i] = 0.f;
-}
 
 template <typename T>
 __global__ void f32_to_kernel(const float* __restrict__ src, T* __restrict__ dst, int64_t n) {
@@ -734,11 +797,12 @@ void bwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, int64_t K, Carver& c,
 }
 
 template <typename T>
-static usaf_status gather_t(const MoeArgs& a, const T* src, T* dstT, cudaStream_t st) {
+static usaf_status gather_t(const MoeArgs& a, const T* src, T* dstT, cudaStream_t st,
+                           GatherExtra ex) {
   const dim3 grid((unsigned)ceil_div(a.R_cap, GT_ROWS), (unsigned)ceil_div(a.s.H, 64));
   gather_transpose_kernel<T><<<grid, 256, 0, st>>>(src, a.rt.perm_tok, a.rt.perm_slot,
                                                    a.rt.expert_offset + a.s.E, a.R_cap,
-                                                   (int)a.s.H, dstT, a.rt.topk_w, a.wperm);
+                                                   (int)a.s.H, dstT, a.rt.topk_w, a.wperm, ex);
   USAF_CHECK_LAUNCH();
   return USAF_OK;
 }
@@ -774,14 +838,14 @@ static usaf_status moe_fwd_t(const MoeArgs& a, T* xT, T* hT, T* waT, T* y, FwdWs
   aw.wperm = w.wperm;
   {
     USAF_TRACE("gather_x", st);
-    USAF_TRY(gather_t<T>(aw, static_cast<const T*>(a.x), xT, st));
-    zero_f32_kernel<<<grid_dim_for(TH), 256, 0, st>>>(w.y_acc, TH);
-    USAF_CHECK_LAUNCH();
+    // also zeroes the combine accumulator and writes the tile plan
+    const GatherExtra ex{w.y_acc, TH, nullptr, 0, a.rt.expert_offset, (int)s.E,
+                         a.dt == USAF_BF16 ? w.plan : nullptr};
+    USAF_TRY(gather_t<T>(aw, static_cast<const T*>(a.x), xT, st, ex));
   }
   if (a.dt == USAF_BF16) {
     MoeArgs b = aw;
     b.plan = w.plan;
-    USAF_TRY(tc_plan(b, st));
     USAF_TRY(tc_fwd_gate_up(b, xT, hT, waT, st));
     USAF_TRY(tc_fwd_down(b, waT, w.y_acc, st));
   } else {
@@ -847,12 +911,12 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
   // S6: gvec, dw, dh
   {
     USAF_TRACE("gather_dy", st);
-    USAF_TRY(gather_t<T>(a, dy, dyT, st));
-    zero_f32_kernel<<<grid_dim_for(s.T * s.k), 256, 0, st>>>(dw, s.T * s.k);
-    USAF_CHECK_LAUNCH();
+    // also zeroes dw and the dx accumulator and writes the tile plan
+    const GatherExtra ex{dw, s.T * s.k, dx ? w.dx_acc : nullptr, dx ? s.T * s.H : 0,
+                         a.rt.expert_offset, (int)s.E, a.dt == USAF_BF16 ? w.plan : nullptr};
+    USAF_TRY(gather_t<T>(a, dy, dyT, st, ex));
   }
   if (a.dt == USAF_BF16) {
-    USAF_TRY(tc_plan(a, st));
     USAF_TRY(tc_bwd_gvec(a, dyT, hT, dhT, dw, st));
   } else {
     USAF_TRACE("simt_gvec", st);
@@ -885,11 +949,6 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
   }
   // S8: dx
   if (dx) {
-    {
-      USAF_TRACE("dx_zero", st);
-      zero_f32_kernel<<<grid_dim_for(s.T * s.H), 256, 0, st>>>(w.dx_acc, s.T * s.H);
-      USAF_CHECK_LAUNCH();
-    }
     if (a.dt == USAF_BF16) {
       USAF_TRY(tc_bwd_dx(a, dhT, w.dx_acc, st));
     } else {

@@ -28,7 +28,7 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int BN = 256;
+constexpr int BN = TC_TOKEN_TILE;
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;
 constexpr int B_BYTES = BN * BK * 2;
@@ -926,35 +926,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
-// ---------------------------------------------------------------------------- plan kernel
-// Token tiles per expert: ceil(padded rows / 256), exclusive prefix over experts (E <= 1024).
-__global__ void __launch_bounds__(1024) token_plan_kernel(const int32_t* __restrict__ off, int E,
-                                                          int32_t* __restrict__ plan) {
-  __shared__ int32_t wsum[32];
-  const int e = threadIdx.x, lane = e & 31, wid = e >> 5;
-  int32_t n = 0;
-  if (e < E) n = (off[e + 1] - off[e] + BN - 1) / BN;
-  int32_t v = n;
-  for (int o = 1; o < 32; o <<= 1) {
-    int32_t y = __shfl_up_sync(0xffffffffu, v, o);
-    if (lane >= o) v += y;
-  }
-  if (lane == 31) wsum[wid] = v;
-  __syncthreads();
-  if (wid == 0) {
-    int32_t w = wsum[lane];
-    for (int o = 1; o < 32; o <<= 1) {
-      int32_t y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
-    }
-    wsum[lane] = w;
-  }
-  __syncthreads();
-  const int32_t incl = v + (wid > 0 ? wsum[wid - 1] : 0);
-  if (e < E) plan[e] = incl - n;
-  if (e == E - 1) plan[E] = incl;
-}
-
 // Router weight split for the tensor-core logits: w = hi + mid + lo, each part bf16 and each
 // residual exact in fp32, so x . w is carried by three bf16 products with fp32 accumulation.
 __global__ void router_split_kernel(const float* __restrict__ wr, int H,
@@ -1063,13 +1034,6 @@ Params base_params(const MoeArgs& a) {
 bool tc_shape_ok(const usaf_moe_shape& s) {
   return s.H % 64 == 0 && s.I % 64 == 0 && s.E <= MAX_E && s.H <= (1 << 20) &&
          s.I <= (1 << 20) && s.E * s.H < (int64_t(1) << 31) && s.E * 2 * s.I < (int64_t(1) << 31);
-}
-
-usaf_status tc_plan(const MoeArgs& a, cudaStream_t st) {
-  USAF_TRACE("tc_plan", st);
-  token_plan_kernel<<<1, 1024, 0, st>>>(a.rt.expert_offset, (int)a.s.E, a.plan);
-  USAF_CHECK_LAUNCH();
-  return USAF_OK;
 }
 
 usaf_status tc_router_logits(const usaf_moe_shape& s, const void* x, const float* wr,
