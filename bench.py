@@ -94,10 +94,12 @@ def kernel_units(cfg, sddmm_pairs=None):
 # kernel on this workload (profiles/), with the SHA-256 of the source file at capture time; a
 # kernel whose source has changed since reports traffic null.
 NCU_TRAFFIC = {
-    "wgrad_sddmm": (452837120 + 13896448, "sparse_moe_fine_gb300/csrc/moe.cu",
-                    "2c5c5d31bc4b873a5c59e0d85d1b12eb52ea50329544c334bcc3baa480ca983c"),
-    "tc_gate_up_swiglu": (946959616 + 138687744, "sparse_moe_fine_gb300/csrc/moe_tc.cu",
-                          "13c915398fc197dfc1f8f6d2063a5ea33b5af04137efec1a5e5273c94aa0a3a2"),
+    "wgrad_sddmm": (452632320 + 13817344, "sparse_moe_fine_gb300/csrc/moe.cu",
+                    "7af6f3f2d475f54db8162835914e7a527c7c0b6f9cd8c5c344522c7fc7a802b6"),
+    "tc_gate_up_swiglu": (947226368 + 139350784, "sparse_moe_fine_gb300/csrc/moe_tc.cu",
+                          "27f5d83d3a9fa26e4e11d8146b42d19b0113565e7e00027f385f2b23fb819220"),
+    "tc_dx": (1057620480 + 139103744, "sparse_moe_fine_gb300/csrc/moe_tc.cu",
+              "27f5d83d3a9fa26e4e11d8146b42d19b0113565e7e00027f385f2b23fb819220"),
 }
 
 
