@@ -94,8 +94,8 @@ def kernel_units(cfg, sddmm_pairs=None):
 # kernel on this workload (profiles/), with the SHA-256 of the source file at capture time; a
 # kernel whose source has changed since reports traffic null.
 NCU_TRAFFIC = {
-    "wgrad_sddmm": (452632320 + 13817344, "sparse_moe_fine_gb300/csrc/moe.cu",
-                    "7af6f3f2d475f54db8162835914e7a527c7c0b6f9cd8c5c344522c7fc7a802b6"),
+    "wgrad_sddmm": (452660736 + 13634560, "sparse_moe_fine_gb300/csrc/moe.cu",
+                    "cb9242436d596106f2e9e14ada4989bb304ed4ef06f8654df35ae4b0189d26f2"),
     "tc_gate_up_swiglu": (947226368 + 139350784, "sparse_moe_fine_gb300/csrc/moe_tc.cu",
                           "27f5d83d3a9fa26e4e11d8146b42d19b0113565e7e00027f385f2b23fb819220"),
     "tc_dx": (1057620480 + 139103744, "sparse_moe_fine_gb300/csrc/moe_tc.cu",

@@ -341,27 +341,27 @@ __global__ void __launch_bounds__(256) gather_transpose_kernel(
   }
 }
 
-// bf16 pair -> (lo, hi) fp32 pair in one 64-bit register, and the packed fp32 FMA on such pairs
-__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(w << 16), "r"(w & 0xFFFF0000u));
-  return r;
-}
-__device__ __forceinline__ uint64_t ffma2(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t d;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-  return d;
+// The masked-gradient dot products. The bf16 products use the mixed-precision FMA (bf16 sources,
+// fp32 addend and result, sm_100 and later): the product of two bf16 values is exact in fp32, so
+// each step equals an fp32 FMA of the widened values and no unpacking is needed.
+// c + a.lo * b.lo, then + a.hi * b.hi, for two bf16 pairs a and b
+__device__ __forceinline__ float fma_bf16_pair(uint32_t a, uint32_t b, float c) {
+  unsigned short al, ah, bl, bh;
+  asm("mov.b32 {%0, %1}, %2;" : "=h"(al), "=h"(ah) : "r"(a));
+  asm("mov.b32 {%0, %1}, %2;" : "=h"(bl), "=h"(bh) : "r"(b));
+  asm("fma.rn.f32.bf16 %0, %1, %2, %0;" : "+f"(c) : "h"(al), "h"(bl));
+  asm("fma.rn.f32.bf16 %0, %1, %2, %0;" : "+f"(c) : "h"(ah), "h"(bh));
+  return c;
 }
 // s + the dot product of two 16-byte vectors (8 bf16 or 4 fp32), accumulated in fp32
 template <typename T>
 __device__ __forceinline__ float dot_acc(const uint4& a, const uint4& b, float s);
 template <>
 __device__ __forceinline__ float dot_acc<__nv_bfloat16>(const uint4& a, const uint4& b, float s) {
-  uint64_t acc = ffma2(bf16x2_to_f32x2(a.x), bf16x2_to_f32x2(b.x), (uint64_t)__float_as_uint(s));
-  acc = ffma2(bf16x2_to_f32x2(a.y), bf16x2_to_f32x2(b.y), acc);
-  acc = ffma2(bf16x2_to_f32x2(a.z), bf16x2_to_f32x2(b.z), acc);
-  acc = ffma2(bf16x2_to_f32x2(a.w), bf16x2_to_f32x2(b.w), acc);
-  return __uint_as_float((uint32_t)acc) + __uint_as_float((uint32_t)(acc >> 32));
+  s = fma_bf16_pair(a.x, b.x, s);
+  s = fma_bf16_pair(a.y, b.y, s);
+  s = fma_bf16_pair(a.z, b.z, s);
+  return fma_bf16_pair(a.w, b.w, s);
 }
 template <>
 __device__ __forceinline__ float dot_acc<float>(const uint4& a, const uint4& b, float s) {
@@ -371,11 +371,12 @@ __device__ __forceinline__ float dot_acc<float>(const uint4& a, const uint4& b, 
   return fmaf(__uint_as_float(a.w), __uint_as_float(b.w), s);
 }
 
-// Butterfly transpose-reduce of 16 values across a warp: lanes l and l + 16 both return the
-// warp-wide sum of x[l & 15] (16 shuffles for 16 sums). x is clobbered.
-__device__ __forceinline__ float transpose_reduce16(float (&x)[16], int lane) {
+// Butterfly transpose-reduce of G values across a warp (G = 2, 4, 8 or 16): every lane l returns
+// the warp-wide sum of x[l % G] (G - 1 + log2(32 / G) shuffles). x is clobbered.
+template <int G>
+__device__ __forceinline__ float transpose_reduce(float (&x)[G], int lane) {
 #pragma unroll
-  for (int off = 8; off >= 1; off >>= 1) {
+  for (int off = G / 2; off >= 1; off >>= 1) {
     const bool upper = (lane & off) != 0;
 #pragma unroll
     for (int j = 0; j < off; ++j) {
@@ -384,43 +385,19 @@ __device__ __forceinline__ float transpose_reduce16(float (&x)[16], int lane) {
       x[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
     }
   }
-  return x[0] + __shfl_xor_sync(0xffffffffu, x[0], 16);
+  float r = x[0];
+#pragma unroll
+  for (int o = G; o < 32; o <<= 1) r += __shfl_xor_sync(0xffffffffu, r, o);
+  return r;
 }
 
-// One 16-byte vector of a row operand held in fp32 for repeated dot products against other
-// vectors: bf16 pairs unpacked once into (lo, hi) fp32 pairs and multiplied with packed fp32 FMAs.
+// One 16-byte vector of a row operand held for repeated dot products against other vectors.
 template <typename T>
-struct RowVec;
-template <>
-struct RowVec<__nv_bfloat16> {
-  uint64_t f2[4];
-  __device__ __forceinline__ void set(const uint4& a) {
-    f2[0] = bf16x2_to_f32x2(a.x);
-    f2[1] = bf16x2_to_f32x2(a.y);
-    f2[2] = bf16x2_to_f32x2(a.z);
-    f2[3] = bf16x2_to_f32x2(a.w);
-  }
-  // `m16` is 65536 passed at run time: the low half is unpacked by an integer multiply, which the
-  // compiler cannot turn into a shift, so half of the unpacking runs on the FMA pipe
-  __device__ __forceinline__ float dot(const uint4& b, uint32_t m16) const {
-    uint64_t acc = ffma2(f2[0], unpack_m(b.x, m16), 0ull);
-    acc = ffma2(f2[1], unpack_m(b.y, m16), acc);
-    acc = ffma2(f2[2], unpack_m(b.z, m16), acc);
-    acc = ffma2(f2[3], unpack_m(b.w, m16), acc);
-    return __uint_as_float((uint32_t)acc) + __uint_as_float((uint32_t)(acc >> 32));
-  }
-  __device__ __forceinline__ static uint64_t unpack_m(uint32_t w, uint32_t m16) {
-    uint64_t r;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(w * m16), "r"(w & 0xFFFF0000u));
-    return r;
-  }
-};
-template <>
-struct RowVec<float> {
-  uint4 f;
-  __device__ __forceinline__ void set(const uint4& a) { f = a; }
-  __device__ __forceinline__ float dot(const uint4& b, uint32_t) const {
-    return dot_acc<float>(f, b, 0.f);
+struct RowVec {
+  uint4 r;
+  __device__ __forceinline__ void set(const uint4& a) { r = a; }
+  __device__ __forceinline__ float dot_acc(const uint4& b, float s) const {
+    return ::usaf::dot_acc<T>(r, b, s);
   }
 };
 
@@ -452,28 +429,31 @@ __device__ __forceinline__ int64_t count_below(const int64_t* __restrict__ act, 
 // expert's routed tokens is that entry's gradient:
 //   gate_up entry (e, j, c):  g = sum_t dh^T[j, o_e + t] * x^T[c, o_e + t]
 //   down entry (e, h, c):     g = sum_t dy^T[h, o_e + t] * (wA)^T[c, o_e + t]
-// The 32 entries are then taken in two halves of 16. Full passes: the warp walks the half's
-// entries together, lane l reading 16-byte vector l of both rows (a pass covers 32 vectors, 256
-// bf16 tokens), the loads of eight entries in flight before their FMAs; the row vector is loaded
-// and unpacked to fp32 pairs only where the weight row changes (packed fp32 FMAs). Lanes past an
-// entry's last vector re-read that vector (an in-bounds address) and drop the product. The number
-// of full passes is the half's smallest vector count rounded to the nearest multiple of 32;
-// vectors beyond them are taken by groups of eight lanes, four entries at a time. A butterfly
-// transpose of the 16 per-lane partial sums then leaves entry i's total in lane i.
+// The 32 entries are then taken in groups of SD_G.
+// - Full passes: the warp walks the group's entries together, lane l reading 16-byte vector l of
+//   both rows (a pass covers 32 vectors, 256 bf16 tokens), four entries' loads in flight before
+//   their FMAs. The row vector is loaded only where the weight row changes. The number of passes
+//   is the group's smallest vector count rounded to the nearest multiple of 32. When every entry
+//   has a vector for every lane the pass runs unguarded; otherwise lanes past an entry's last
+//   vector re-read that vector (an in-bounds address) and keep their partial sum unchanged.
+// - Vectors past the full passes go to 32 / SD_G lanes per entry, which take entry i's remaining
+//   vectors in turn and combine with shuffles.
+// A butterfly transpose of the SD_G per-lane partial sums then leaves entry i's total in lane i.
 constexpr int SD_WARPS = 8;
+constexpr int SD_BLOCKS_PER_SM = 4;
+constexpr int SD_G = 16;  // entries per group
 template <typename T>
-__global__ void __launch_bounds__(SD_WARPS * 32, 2) sddmm_kernel(
+__global__ void __launch_bounds__(SD_WARPS * 32, SD_BLOCKS_PER_SM) sddmm_kernel(
     const int64_t* __restrict__ act, int64_t K, const int32_t* __restrict__ cnt,
     const int32_t* __restrict__ off, int H, int I, int64_t Ngu, int64_t rcap,
     const T* __restrict__ dhT, const T* __restrict__ xT, const T* __restrict__ dyT,
-    const T* __restrict__ waT, float* __restrict__ g_act, uint32_t m16, int accumulate,
-    uint32_t* dev_status) {
+    const T* __restrict__ waT, float* __restrict__ g_act, int accumulate, uint32_t* dev_status) {
   constexpr int VW = 16 / sizeof(T);
-  constexpr int U = 8;   // entries whose loads are in flight together in a full pass
-  constexpr int RU = 2;  // remainder rounds whose first loads are in flight together
+  constexpr int U = 2;  // entries whose loads are in flight together in a full pass
+  constexpr uint32_t FULL = 0xffffffffu;
   // per entry: a-row vector, b-row vector, vector count, last vector (0 when there is none)
   __shared__ int4 meta[SD_WARPS][32];
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, grp = lane >> 3, gl = lane & 7;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, il = lane % SD_G;
   const int64_t kgu = count_below(act, K, Ngu, lane);
   const int64_t nb_gu = (kgu + 31) / 32, nb = nb_gu + (K - kgu + 31) / 32;
   bool bad = false;
@@ -490,10 +470,20 @@ __global__ void __launch_bounds__(SD_WARPS * 32, 2) sddmm_kernel(
       if (q < lim) {
         const int64_t f = gu ? act[q] : act[q] - Ngu;
         const int64_t wcols = gu ? H : I, wrows = gu ? 2 * I : H;
-        const int64_t row = f / wcols;
-        const int64_t col = f - row * wcols;
-        const int e = (int)(row / wrows);
-        const int64_t arow = row - (int64_t)e * wrows;
+        int64_t col, arow;
+        int e;
+        if ((uint64_t)f <= 0xFFFFFFFFull) {  // 32-bit divisions where the flat index allows
+          const uint32_t r32 = (uint32_t)f / (uint32_t)wcols;
+          const uint32_t e32 = r32 / (uint32_t)wrows;
+          col = (int64_t)((uint32_t)f - r32 * (uint32_t)wcols);
+          e = (int)e32;
+          arow = (int64_t)(r32 - e32 * (uint32_t)wrows);
+        } else {
+          const int64_t row = f / wcols;
+          col = f - row * wcols;
+          e = (int)(row / wrows);
+          arow = row - (int64_t)e * wrows;
+        }
         const int64_t o = off[e];
         const int nv = (cnt[e] + VW - 1) / VW;
         if (nv > 0) {
@@ -506,77 +496,79 @@ __global__ void __launch_bounds__(SD_WARPS * 32, 2) sddmm_kernel(
       meta[wid][lane] = md;
     }
     __syncwarp();
-    for (int hf = 0; hf < 2; ++hf) {
-      const int4* mh = &meta[wid][16 * hf];
-      const uint32_t nvl = (uint32_t)mh[lane & 15].z;
-      const uint32_t passes = (__reduce_min_sync(0xffffffffu, nvl) + 16u) / 32u;
-      const uint32_t vrest = 32u * passes;  // first vector left to the eight-lane groups
-      const bool rest = __any_sync(0xffffffffu, nvl > vrest);
-      float part[16];
+    for (int hf = 0; hf < 32 / SD_G; ++hf) {
+      const int4* mh = &meta[wid][SD_G * hf];
+      const int4 mine = mh[il];
+      const uint32_t nvl = (uint32_t)mine.z;
+      const uint32_t nmin = __reduce_min_sync(FULL, nvl);
+      const uint32_t passes = (nmin + 16u) / 32u;
+      const uint32_t vrest = 32u * passes;  // first vector left to the lane pairs
+      const bool filled = nmin >= vrest;    // every entry has a vector for every lane of a pass
+      // bit i: entry i loads its row vector (a new weight row, or a new vector on every pass)
+      const bool fl = il == 0 || passes > 1 || mine.x != mh[il == 0 ? 0 : il - 1].x;
+      const uint32_t fresh = __ballot_sync(FULL, fl) & ((1u << SD_G) - 1u);
+      float part[SD_G];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) part[i] = 0.f;
+      for (int i = 0; i < SD_G; ++i) part[i] = 0.f;
       if (passes > 0) {
         RowVec<T> rowv;
 #pragma unroll
-        for (int i0 = 0; i0 < 16; i0 += U) {
+        for (int i0 = 0; i0 < SD_G; i0 += U) {
           for (uint32_t p = 0; p < passes; ++p) {
             const uint32_t v = p * 32u + (uint32_t)lane;
             uint4 av[U], bv[U];
-            uint32_t fresh = 0, ok = 0;  // bit u: entry i0 + u starts a new weight row / has vector v
+            if (filled) {
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-              const int4 m = mh[i0 + u];
-              // the row operand is loaded and unpacked only where the weight row changes
-              const bool f = i0 + u == 0 ? true
-                                         : passes > 1 || m.x != mh[i0 + u == 0 ? 0 : i0 + u - 1].x;
-              fresh |= (uint32_t)f << u;
-              ok |= (uint32_t)(v < (uint32_t)m.z) << u;
-              const uint32_t vv = min(v, (uint32_t)m.w);
-              if (f) av[u] = __ldg(A + ((uint32_t)m.x + vv));
-              bv[u] = __ldg(Bm + ((uint32_t)m.y + vv));
-            }
+              for (int u = 0; u < U; ++u) {
+                const int4 m = mh[i0 + u];
+                if (fresh & (1u << (i0 + u))) av[u] = __ldg(A + ((uint32_t)m.x + v));
+                bv[u] = __ldg(Bm + ((uint32_t)m.y + v));
+              }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-              if (fresh & (1u << u)) rowv.set(av[u]);
-              const float d = rowv.dot(bv[u], m16);
-              if (ok & (1u << u)) part[i0 + u] += d;
+              for (int u = 0; u < U; ++u) {
+                if (fresh & (1u << (i0 + u))) rowv.set(av[u]);
+                part[i0 + u] = rowv.dot_acc(bv[u], part[i0 + u]);
+              }
+            } else {
+              uint32_t ok = 0;  // bit u: entry i0 + u has vector v
+#pragma unroll
+              for (int u = 0; u < U; ++u) {
+                const int4 m = mh[i0 + u];
+                ok |= (uint32_t)(v < (uint32_t)m.z) << u;
+                const uint32_t vv = min(v, (uint32_t)m.w);
+                if (fresh & (1u << (i0 + u))) av[u] = __ldg(A + ((uint32_t)m.x + vv));
+                bv[u] = __ldg(Bm + ((uint32_t)m.y + vv));
+              }
+#pragma unroll
+              for (int u = 0; u < U; ++u) {
+                if (fresh & (1u << (i0 + u))) rowv.set(av[u]);
+                const float d = rowv.dot_acc(bv[u], part[i0 + u]);
+                if (ok & (1u << u)) part[i0 + u] = d;
+              }
             }
           }
         }
       }
-      if (rest) {
-        // entry 4r + grp of the half in round r; the first vector of every round is loaded up front
-        float rem[4];
-#pragma unroll
-        for (int h = 0; h < 4; h += RU) {
-          int4 m[RU];
-          uint4 av[RU], bv[RU];
-          const uint32_t v0 = vrest + (uint32_t)gl;
-#pragma unroll
-          for (int r = 0; r < RU; ++r) {
-            m[r] = mh[4 * (h + r) + grp];
-            const uint32_t vv = min(v0, (uint32_t)m[r].w);
-            av[r] = __ldg(A + ((uint32_t)m[r].x + vv));
-            bv[r] = __ldg(Bm + ((uint32_t)m[r].y + vv));
-          }
-#pragma unroll
-          for (int r = 0; r < RU; ++r) {
-            float sacc = dot_acc<T>(av[r], bv[r], 0.f);
-            if (v0 >= (uint32_t)m[r].z) sacc = 0.f;
-            for (uint32_t v = v0 + 8; v < (uint32_t)m[r].z; v += 8)
-              sacc = dot_acc<T>(__ldg(A + ((uint32_t)m[r].x + v)),
-                                __ldg(Bm + ((uint32_t)m[r].y + v)), sacc);
-            rem[h + r] = sacc;
-          }
+      float rem = 0.f;
+      if (__any_sync(FULL, nvl > vrest)) {
+        constexpr int LP = 32 / SD_G;  // lanes per entry
+        const int4 m = mh[lane / LP];
+        const uint32_t nr = (uint32_t)m.z > vrest ? (uint32_t)m.z - vrest : 0u;
+        const uint32_t vend = vrest + __reduce_max_sync(FULL, nr);
+        float s = 0.f;
+        for (uint32_t v = vrest + (uint32_t)(lane % LP); v < vend; v += LP) {
+          const uint32_t vv = min(v, (uint32_t)m.w);
+          const float d = dot_acc<T>(__ldg(A + ((uint32_t)m.x + vv)),
+                                     __ldg(Bm + ((uint32_t)m.y + vv)), s);
+          if (v < (uint32_t)m.z) s = d;
         }
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
-#pragma unroll
-          for (int g = 0; g < 4; ++g) part[4 * r + g] += grp == g ? rem[r] : 0.f;
+        for (int o = 1; o < LP; o <<= 1) s += __shfl_xor_sync(FULL, s, o);
+        rem = __shfl_sync(FULL, s, LP * il);  // entry il's remainder, from lane LP il
       }
-      const float gsum = transpose_reduce16(part, lane);
-      const int64_t q = b0 + 16 * hf + lane;
-      if (lane < 16 && q < lim) {
+      const float gsum = transpose_reduce<SD_G>(part, lane) + rem;
+      const int64_t q = b0 + SD_G * hf + lane;
+      if (lane < SD_G && q < lim) {
         const float gv = accumulate ? g_act[q] + gsum : gsum;
         g_act[q] = gv;
         bad |= !finite_f(gv);
@@ -969,10 +961,10 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
   if (K > 0) {
     USAF_TRACE("wgrad_sddmm", st);
     const unsigned blocks = (unsigned)std::min<int64_t>(ceil_div(K, SD_WARPS * 32),
-                                                        device_sm_count() * 2);
+                                                        device_sm_count() * SD_BLOCKS_PER_SM);
     sddmm_kernel<T><<<blocks, SD_WARPS * 32, 0, st>>>(act_idx, K, cnt, off, H, I, Ngu, a.R_cap,
-                                                      dhT, xT, dyT, waT, g_act, 65536u,
-                                                      accumulate, dev_status);
+                                                      dhT, xT, dyT, waT, g_act, accumulate,
+                                                      dev_status);
     USAF_CHECK_LAUNCH();
   }
   // dense expert weight gradients (importance phase)
