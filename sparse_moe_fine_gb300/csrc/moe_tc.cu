@@ -235,21 +235,10 @@ __device__ __forceinline__ int total_tiles(const Params& p, const int32_t* s_pla
 // sum over the warp's lanes of column l.
 __device__ __forceinline__ float sigmoid_fast(float z) { return __fdividef(1.f, 1.f + __expf(-z)); }
 
-// 16 bytes = 8 bf16 of a feature-major row; `cnt` of the 8 tokens are valid (0 elsewhere)
+// two floats as a bf16 pair, rounded to nearest even
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   const __nv_bfloat162 pr = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&pr);
-}
-
-// store v[0..31] as bf16 to row[0..ncol) (ncol a multiple of 8; row 16-byte aligned)
-__device__ __forceinline__ void store_row32(__nv_bfloat16* row, const float (&v)[32], int ncol) {
-  uint4* dst = reinterpret_cast<uint4*>(row);
-#pragma unroll
-  for (int q = 0; q < 4; ++q)
-    if (q * 8 < ncol)
-      dst[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                          pack_bf16x2(v[8 * q + 4], v[8 * q + 5]),
-                          pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
 }
 
 // load row[0..32) bf16 as 16 words (two tokens each); 0 beyond ncol or when !ok
@@ -610,6 +599,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       constexpr bool b_mn = !VarTraits<VAR>::router;
       const uint32_t a_step = a_mn ? 2048 : 32, b_step = b_mn ? 2048 : 32;
       const uint32_t a_lbo = a_mn ? 8192 : 16, b_lbo = b_mn ? B_BOX : 16;
+      // the operand descriptors of stage 0: a stage or k-step moves only their start-address
+      // field (16-byte units, no carry within the CTA's shared memory)
+      const uint64_t ad0 = sdesc(smem_u32(smem), a_lbo, 1024);
+      const uint64_t bd0 = sdesc(smem_u32(smem) + A_BYTES, b_lbo, 1024);
       for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
         const Tile ti = get_tile<VAR>(p, s_plan, s_off, t);
         if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag)) {
@@ -626,14 +619,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a_base = smem_u32(smem + stage * STAGE_BYTES);
-          const uint32_t b_base = a_base + A_BYTES;
+          const uint64_t so = (uint64_t)((stage * STAGE_BYTES) >> 4);
 #pragma unroll
-          for (int ks = 0; ks < BK / 16; ++ks) {
-            const uint64_t ad = sdesc(a_base + ks * a_step, a_lbo, 1024);
-            const uint64_t bd = sdesc(b_base + ks * b_step, b_lbo, 1024);
-            umma_bf16(d, ad, bd, idesc, (kb | ks) != 0 ? 1u : 0u);
-          }
+          for (int ks = 0; ks < BK / 16; ++ks)
+            umma_bf16(d, ad0 + so + ((ks * a_step) >> 4), bd0 + so + ((ks * b_step) >> 4), idesc,
+                      (kb | ks) != 0 ? 1u : 0u);
           umma_commit(empty0 + 8 * stage);
           if (++stage == STAGES) {
             stage = 0;
