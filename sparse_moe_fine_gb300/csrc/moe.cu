@@ -231,19 +231,20 @@ struct GatherExtra {
   int32_t* plan;
 };
 
+// z[0..n) = 0, shared by all blocks of the grid: grid-stride float4 stores (scalar ones when z is
+// off a 16-byte boundary)
 __device__ void zero_slice(float* z, int64_t n) {
   if (!z || n == 0) return;
   const int64_t nb = (int64_t)gridDim.x * gridDim.y, b = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;
-  if ((reinterpret_cast<uintptr_t>(z) & 15) != 0) {  // a caller buffer off a 16-byte boundary
-    for (int64_t i = b * blockDim.x + threadIdx.x; i < n; i += nb * blockDim.x) z[i] = 0.f;
+  const int64_t stride = nb * blockDim.x, i0 = b * blockDim.x + threadIdx.x;
+  if ((reinterpret_cast<uintptr_t>(z) & 15) != 0) {
+    for (int64_t i = i0; i < n; i += stride) z[i] = 0.f;
     return;
   }
-  const int64_t n4 = n & ~int64_t(3);
-  const int64_t per = ((n4 / 4 + nb - 1) / nb) * 4;
-  const int64_t lo = b * per, hi = min(n4, lo + per);
-  for (int64_t i = lo + 4 * threadIdx.x; i < hi; i += 4 * blockDim.x)
-    *reinterpret_cast<float4*>(z + i) = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (b == 0 && threadIdx.x < n - n4) z[n4 + threadIdx.x] = 0.f;
+  const int64_t n4 = n >> 2;
+  float4* z4 = reinterpret_cast<float4*>(z);
+  for (int64_t i = i0; i < n4; i += stride) z4[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (b == 0 && threadIdx.x < (n & 3)) z[(n4 << 2) + threadIdx.x] = 0.f;
 }
 
 __device__ void tile_plan(const int32_t* __restrict__ off, int E, int32_t* __restrict__ plan) {
@@ -288,7 +289,7 @@ __device__ void tile_plan(const int32_t* __restrict__ off, int E, int32_t* __res
 // each feature row of xT receives 256 contiguous bytes (bf16).
 constexpr int GT_ROWS = 128;
 template <typename T>
-__global__ void __launch_bounds__(256) gather_transpose_kernel(
+__global__ void __launch_bounds__(256, 8) gather_transpose_kernel(
     const T* __restrict__ x, const int32_t* __restrict__ ptok, const int32_t* __restrict__ pslot,
     const int32_t* __restrict__ off_end, int64_t R_cap, int H, T* __restrict__ xT,
     const float* __restrict__ topk_w, float* __restrict__ wperm, GatherExtra ex) {
@@ -315,11 +316,10 @@ __global__ void __launch_bounds__(256) gather_transpose_kernel(
       for (int q = 0; q < VW; ++q)
         buf[q] = (live && h0 + f + q < H) ? x[src + h0 + f + q] : from_f32<T>(0.f);
     }
+    // feature f + q goes to row f + q of the tile, rotated by f columns (f is a multiple of VW)
+    T* dst = &tile[f * GT_ROWS + ((r + f) & (GT_ROWS - 1))];
 #pragma unroll
-    for (int q = 0; q < VW; ++q) {
-      const int ff = f + q;
-      tile[ff * GT_ROWS + (r + (ff / VW) * VW) % GT_ROWS] = buf[q];
-    }
+    for (int q = 0; q < VW; ++q) dst[q * GT_ROWS] = buf[q];
   }
   zero_slice(ex.z0, ex.n0);
   zero_slice(ex.z1, ex.n1);
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(256) gather_transpose_kernel(
     const int f = v / (GT_ROWS / VW), r = (v % (GT_ROWS / VW)) * VW;
     if (h0 + f >= H || r0 + r >= R_cap) continue;
     *reinterpret_cast<uint4*>(xT + (int64_t)(h0 + f) * R_cap + r0 + r) =
-        *reinterpret_cast<const uint4*>(&tile[f * GT_ROWS + (r + (f / VW) * VW) % GT_ROWS]);
+        *reinterpret_cast<const uint4*>(&tile[f * GT_ROWS + ((r + (f / VW) * VW) & (GT_ROWS - 1))]);
   }
 }
 

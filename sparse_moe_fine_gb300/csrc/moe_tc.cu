@@ -938,6 +938,203 @@ __global__ void router_split_kernel(const float* __restrict__ wr, int H,
   }
 }
 
+// ---------------------------------------------------------------------------- router, K split
+// logits^T tile (128 experts x RK_N tokens) with the 3H / 64 k-blocks cut among the RK_SPLIT CTAs of
+// a cluster. A tcgen05 MMA costs about the same at N = 32 as at N = 256, so a long K loop over
+// narrow token tiles leaves the tensor pipe mostly idle; here every CTA runs 256-token MMAs over a
+// twelfth-sized K range. Each CTA leaves its partial tile in its shared memory (the ring, free
+// once the MMAs are done); after a cluster barrier CTA r adds the RK_SPLIT partials of tokens
+// [32 r, 32 r + 32) in split order through distributed shared memory and writes those logits.
+// The sum order is fixed, so the logits do not depend on timing.
+constexpr int RK_SPLIT = 8;                  // CTAs per cluster = K splits
+constexpr int RK_N = 256;                    // tokens per tile
+constexpr int RK_STAGES = 4;
+constexpr int RK_B_BYTES = RK_N * BK * 2;    // x box: 256 tokens x 64 k (K-major)
+constexpr int RK_STAGE_BYTES = A_BYTES + RK_B_BYTES;
+constexpr int RK_EPI_WARPS = 4;
+constexpr int RK_THREADS = 64 + 32 * RK_EPI_WARPS;
+constexpr int RK_PART_PITCH = BM + 4;        // floats per token row of a partial tile
+constexpr int RK_SMEM_BYTES = RK_STAGES * RK_STAGE_BYTES + 1024 + 256;
+static_assert(RK_N * RK_PART_PITCH * 4 <= RK_STAGES * RK_STAGE_BYTES, "partial tile in the ring");
+static_assert(RK_N % RK_SPLIT == 0 && (RK_N / RK_SPLIT) % 4 == 0, "token slices of the reduction");
+
+__device__ __forceinline__ uint32_t peer_smem(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_peer_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+// grid (RK_SPLIT * token tiles, expert tiles), clusters of RK_SPLIT along x
+__global__ void __launch_bounds__(RK_THREADS, 1)
+    tc_router_split_kernel(const __grid_constant__ CUtensorMap tmA,
+                           const __grid_constant__ CUtensorMap tmB, int T, int E, int H,
+                           float* __restrict__ logits) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RK_STAGES * RK_STAGE_BYTES);
+  // bars: full[RK_STAGES], empty[RK_STAGES], tfull
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * RK_STAGES + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* part = reinterpret_cast<float*>(smem);  // [RK_N][RK_PART_PITCH] after the MMAs
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * RK_STAGES;
+  const uint32_t tfull = empty0 + 8 * RK_STAGES;
+  const uint32_t rank = cluster_rank();
+  const int n0 = (blockIdx.x / RK_SPLIT) * RK_N, m0 = blockIdx.y * BM;
+  const int nrows = min(RK_N, (T - n0 + 15) / 16 * 16);
+  const int nkb_all = 3 * H / BK;
+  const int kb0 = (int)rank * nkb_all / RK_SPLIT, kb1 = ((int)rank + 1) * nkb_all / RK_SPLIT;
+  const int nkb = kb1 - kb0;  // may be 0 for a short K: the partial is then zero
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < RK_STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_init(tfull, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(RK_N)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  bool failed = false;
+
+  if (warp == 0) {
+    if (lane == 0) {  // ------------------------------------------------ TMA producer
+      uint32_t issued = 0;
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % RK_STAGES;
+        if (!mbar_wait(empty0 + 8 * s, ((kb / RK_STAGES) & 1) ^ 1, abort_flag)) {
+          failed = true;
+          break;
+        }
+        const uint32_t a_dst = smem_u32(smem + s * RK_STAGE_BYTES);
+        const uint32_t fb = full0 + 8 * s;
+        const int k0 = (kb0 + kb) * BK;
+        mbar_expect_tx(fb, RK_STAGE_BYTES);
+        tma_2d(a_dst, &tmA, fb, k0, m0);
+        tma_2d(a_dst + A_BYTES, &tmB, fb, k0 % H, n0);  // x, once for each part of Wr
+        ++issued;
+      }
+      if (failed) *abort_flag = 1;
+      // let every issued copy land before the CTA can move on
+      for (int s = 0; s < RK_STAGES && (uint32_t)s < issued; ++s) {
+        const uint32_t last = issued - 1 - ((issued - 1 - s) % RK_STAGES);
+        mbar_wait(full0 + 8 * s, (last / RK_STAGES) & 1, abort_flag);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {  // ------------------------------------------------ MMA issuer
+      const uint64_t ad0 = sdesc(smem_u32(smem), 16, 1024);
+      const uint64_t bd0 = sdesc(smem_u32(smem) + A_BYTES, 16, 1024);
+      const uint32_t idesc = idesc_bf16(nrows, false, false);
+      for (int kb = 0; kb < nkb; ++kb) {
+        const int s = kb % RK_STAGES;
+        if (!mbar_wait(full0 + 8 * s, (kb / RK_STAGES) & 1, abort_flag)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        const uint64_t so = (uint64_t)((s * RK_STAGE_BYTES) >> 4);
+#pragma unroll
+        for (int ks = 0; ks < BK / 16; ++ks)
+          umma_bf16(tmem_base, ad0 + so + ((ks * 32) >> 4), bd0 + so + ((ks * 32) >> 4), idesc,
+                    (kb | ks) != 0 ? 1u : 0u);
+        umma_commit(empty0 + 8 * s);
+      }
+      if (failed) *abort_flag = 1;
+      umma_commit(tfull);  // after every MMA above (at once when there were none)
+      mbar_wait(tfull, 0, abort_flag);  // no MMA in flight when TMEM and the ring are reused
+    }
+  } else {  // ---------------------------------------------------- epilogue warps 2..5
+    const int q = warp & 3;  // TMEM lane quarter: experts m0 + 32 q + lane
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(tfull, 0, abort_flag) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) {
+      tc_fence_after();
+      const int e = q * 32 + lane;
+      for (int ch = 0; ch * 32 < nrows; ++ch) {
+        float v[32];
+        if (nkb > 0) {
+          tmem_ld32(tmem_base + ((uint32_t)(q * 32) << 16) + ch * 32, v);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) part[(ch * 32 + j) * RK_PART_PITCH + e] = v[j];
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_barrier();  // every CTA's partial is in its shared memory
+  {
+    // this CTA's tokens: [n0 + 32 rank, + 32), all experts of the tile, float4 at a time
+    constexpr int TOK = RK_N / RK_SPLIT;
+    const uint32_t base = smem_u32(part);
+    const bool vec = (E & 3) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
+    for (int i = threadIdx.x; i < TOK * (BM / 4); i += RK_THREADS) {
+      const int t = (int)rank * TOK + i / (BM / 4), e4 = (i % (BM / 4)) * 4;
+      const int tok = n0 + t;
+      if (tok >= T || t >= nrows) continue;
+      const uint32_t off = (uint32_t)((t * RK_PART_PITCH + e4) * 4);
+      float4 acc = ld_peer_f4(peer_smem(base + off, 0));
+#pragma unroll
+      for (int r = 1; r < RK_SPLIT; ++r) {
+        const float4 w = ld_peer_f4(peer_smem(base + off, (uint32_t)r));
+        acc.x += w.x;
+        acc.y += w.y;
+        acc.z += w.z;
+        acc.w += w.w;
+      }
+      float* dst = logits + (int64_t)tok * E + m0 + e4;
+      if (vec && m0 + e4 + 3 < E) {
+        *reinterpret_cast<float4*>(dst) = acc;
+      } else {
+        const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+        for (int j = 0; j < 4 && m0 + e4 + j < E; ++j) dst[j] = a4[j];
+      }
+    }
+  }
+  cluster_barrier();  // no peer reads this CTA's shared memory any more
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(RK_N)
+                 : "memory");
+  }
+}
+
 // ---------------------------------------------------------------------------- host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -1026,6 +1223,33 @@ bool tc_shape_ok(const usaf_moe_shape& s) {
          s.I <= (1 << 20) && s.E * s.H < (int64_t(1) << 31) && s.E * 2 * s.I < (int64_t(1) << 31);
 }
 
+// Whether clusters of RK_SPLIT CTAs of the split-K router kernel fit on this device (checked once).
+static bool router_split_ok() {
+  static int ok = -1;
+  if (ok < 0) {
+    ok = 0;
+    if (cudaFuncSetAttribute(tc_router_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             RK_SMEM_BYTES) == cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = RK_SPLIT;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(RK_SPLIT);
+      cfg.blockDim = dim3(RK_THREADS);
+      cfg.dynamicSmemBytes = RK_SMEM_BYTES;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, tc_router_split_kernel, &cfg) == cudaSuccess && n > 0)
+        ok = 1;
+    }
+    cudaGetLastError();  // a refused query leaves no error behind
+  }
+  return ok == 1;
+}
+
 usaf_status tc_router_logits(const usaf_moe_shape& s, const void* x, const float* wr,
                              void* wr3, float* logits, cudaStream_t st) {
   {
@@ -1033,6 +1257,30 @@ usaf_status tc_router_logits(const usaf_moe_shape& s, const void* x, const float
     const dim3 grid((unsigned)ceil_div(s.H, 512), (unsigned)s.E);
     router_split_kernel<<<grid, 256, 0, st>>>(wr, (int)s.H, static_cast<__nv_bfloat16*>(wr3));
     USAF_CHECK_LAUNCH();
+  }
+  if (router_split_ok()) {
+    // K split over clusters of RK_SPLIT CTAs, 256-token tiles
+    USAF_TRACE("tc_router_logits", st);
+    CUtensorMap ma, mb;
+    if (!map_2d(&ma, wr3, 3 * s.H, s.E, 64, 128) || !map_2d(&mb, x, s.H, s.T, 64, RK_N))
+      return USAF_ERR_CUDA;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = RK_SPLIT;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3((unsigned)(RK_SPLIT * ceil_div(s.T, RK_N)), (unsigned)ceil_div(s.E, BM));
+    cfg.blockDim = dim3(RK_THREADS);
+    cfg.dynamicSmemBytes = RK_SMEM_BYTES;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, tc_router_split_kernel, ma, mb, (int)s.T, (int)s.E, (int)s.H,
+                           logits) != cudaSuccess)
+      return USAF_ERR_CUDA;
+    USAF_CHECK_LAUNCH();
+    return USAF_OK;
   }
   CUtensorMap ma, mb;
   if (!map_2d(&ma, wr3, 3 * s.H, s.E, 64, 128) || !map_2d(&mb, x, s.H, s.T, 64, ROUTER_BN))
