@@ -941,16 +941,19 @@ __global__ void router_split_kernel(const float* __restrict__ wr, int H,
 // ---------------------------------------------------------------------------- router, K split
 // logits^T tile (128 experts x RK_N tokens) with the 3H / 64 k-blocks cut among the RK_SPLIT CTAs of
 // a cluster. A tcgen05 MMA costs about the same at N = 32 as at N = 256, so a long K loop over
-// narrow token tiles leaves the tensor pipe mostly idle; here every CTA runs 256-token MMAs over a
-// twelfth-sized K range. Each CTA leaves its partial tile in its shared memory (the ring, free
+// narrow token tiles leaves the tensor pipe mostly idle; here every CTA runs wide MMAs over a
+// fraction of the K range. (Clusters of four fit 36 times on a 152-SM part at this shared-memory
+// size, clusters of eight only 15 times.) Each CTA leaves its partial tile in its shared memory (the ring, free
 // once the MMAs are done); after a cluster barrier CTA r adds the RK_SPLIT partials of tokens
-// [32 r, 32 r + 32) in split order through distributed shared memory and writes those logits.
+// [r RK_N / RK_SPLIT, (r + 1) RK_N / RK_SPLIT) in split order through distributed shared memory
+// and writes those logits.
 // The sum order is fixed, so the logits do not depend on timing.
-constexpr int RK_SPLIT = 8;                  // CTAs per cluster = K splits
-constexpr int RK_N = 256;                    // tokens per tile
-constexpr int RK_STAGES = 4;
-constexpr int RK_B_BYTES = RK_N * BK * 2;    // x box: 256 tokens x 64 k (K-major)
+constexpr int RK_SPLIT = 4;                  // CTAs per cluster = K splits
+constexpr int RK_N = 128;                    // tokens per tile
+constexpr int RK_B_BYTES = RK_N * BK * 2;    // x box: RK_N tokens x 64 k (K-major)
 constexpr int RK_STAGE_BYTES = A_BYTES + RK_B_BYTES;
+constexpr int RK_STAGES = STAGES * STAGE_BYTES / RK_STAGE_BYTES;  // the ring of the expert GEMMs
+static_assert(RK_STAGES >= 2 && (2 * RK_STAGES + 1) * 8 + 8 <= 256, "router ring barriers");
 constexpr int RK_EPI_WARPS = 4;
 constexpr int RK_THREADS = 64 + 32 * RK_EPI_WARPS;
 constexpr int RK_PART_PITCH = BM + 4;        // floats per token row of a partial tile
@@ -1099,7 +1102,7 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
   __syncthreads();
   cluster_barrier();  // every CTA's partial is in its shared memory
   {
-    // this CTA's tokens: [n0 + 32 rank, + 32), all experts of the tile, float4 at a time
+    // this CTA's tokens of the tile, all experts of the tile, float4 at a time
     constexpr int TOK = RK_N / RK_SPLIT;
     const uint32_t base = smem_u32(part);
     const bool vec = (E & 3) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
