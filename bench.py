@@ -94,12 +94,12 @@ def kernel_units(cfg, sddmm_pairs=None):
 # kernel on this workload (profiles/), with the SHA-256 of the source file at capture time; a
 # kernel whose source has changed since reports traffic null.
 NCU_TRAFFIC = {
-    "wgrad_sddmm": (452660736 + 13634560, "sparse_moe_fine_gb300/csrc/moe.cu",
-                    "cb9242436d596106f2e9e14ada4989bb304ed4ef06f8654df35ae4b0189d26f2"),
-    "tc_gate_up_swiglu": (947226368 + 139350784, "sparse_moe_fine_gb300/csrc/moe_tc.cu",
-                          "27f5d83d3a9fa26e4e11d8146b42d19b0113565e7e00027f385f2b23fb819220"),
-    "tc_dx": (1057620480 + 139103744, "sparse_moe_fine_gb300/csrc/moe_tc.cu",
-              "27f5d83d3a9fa26e4e11d8146b42d19b0113565e7e00027f385f2b23fb819220"),
+    "wgrad_sddmm": (452653568 + 14011904, "sparse_moe_fine_gb300/csrc/moe.cu",
+                    "0f3dd5f8893a392c9b3c0e9ccf074ccab5753ac924ea76f716bcedc8857f1235"),
+    "tc_gate_up_swiglu": (945693696 + 139366144, "sparse_moe_fine_gb300/csrc/moe_tc.cu",
+                          "453c743e8e9281e3666d42b9251fba1d76ece5e5662ece45bdd94ad6bc2266b6"),
+    "tc_dx": (1056654848 + 139791360, "sparse_moe_fine_gb300/csrc/moe_tc.cu",
+              "453c743e8e9281e3666d42b9251fba1d76ece5e5662ece45bdd94ad6bc2266b6"),
 }
 
 
