@@ -222,13 +222,22 @@ __global__ void __launch_bounds__(32) perm_fill_kernel(const int32_t* __restrict
   __syncwarp();
   const int64_t s0 = (int64_t)blockIdx.x * PERM_CHUNK;
   const int64_t s1 = min(R, s0 + PERM_CHUNK);
-  for (int64_t base = s0; base < s1; base += 32) {
-    int64_t s = base + lane;
-    bool ok = s < s1;
-    int e = ok ? topk_idx[s] : -1 - lane;  // unique dummies for idle lanes
-    unsigned peers = __match_any_sync(0xffffffffu, e);
-    int rank = __popc(peers & ((1u << lane) - 1));
-    int pos = ok ? cnt[e] + rank : 0;
+  // the chunk's experts, all loaded before the ranking walk (unique dummies for idle lanes)
+  constexpr int NPASS = PERM_CHUNK / 32;
+  int ev[NPASS];
+#pragma unroll
+  for (int i = 0; i < NPASS; ++i) {
+    const int64_t s = s0 + 32 * i + lane;
+    ev[i] = s < s1 ? topk_idx[s] : -1 - lane;
+  }
+#pragma unroll
+  for (int i = 0; i < NPASS; ++i) {
+    const int64_t s = s0 + 32 * i + lane;
+    const bool ok = s < s1;
+    const int e = ev[i];
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1));
+    const int pos = ok ? cnt[e] + rank : 0;
     __syncwarp();
     if (ok && rank == 0) cnt[e] += __popc(peers);
     __syncwarp();

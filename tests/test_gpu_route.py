@@ -65,11 +65,13 @@ def test_topk_bit_exact_given_logits(name, renorm):
 
 
 SMALL = {"bf16_ragged": dict(T=300, H=256, E=8, k=2, I=64),
-         "bf16_two_m_tiles": dict(T=1000, H=128, E=160, k=4, I=64)}
+         "bf16_two_m_tiles": dict(T=1000, H=128, E=160, k=4, I=64),
+         # 3 k-blocks for 4 K splits (one split empty), E not a multiple of 4, one short tile
+         "bf16_short_k_odd_e": dict(T=70, H=64, E=6, k=2, I=64)}
 
 
 @pytest.mark.parametrize("name", ["tiny_fp32", "qwen3_30b_a3b", "bf16_ragged",
-                                  "bf16_two_m_tiles"])
+                                  "bf16_two_m_tiles", "bf16_short_k_odd_e"])
 def test_router_logits_and_routing_from_x(name):
     """fp32 tokens: CUDA-core FFMA logits; bf16 tokens: three bf16 tensor-core products of the
     split fp32 router weight. Both within the fp32 dot-product error bound of the oracle."""
