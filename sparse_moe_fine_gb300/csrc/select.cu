@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(COMPACT_WARPS * 32) sel_compact_kernel(
 #pragma unroll
       for (int u = 0; u < UN; ++u) nxt[u] = load4(g, t0 + STEP + u * 128 + lane * 4, hi, vec_ok);
     }
-    const bool full = t0 + STEP <= hi && excl == nullptr;  // no range or exclusion tests
+    const bool full = t0 + STEP <= hi;  // no range tests
 #pragma unroll
     for (int u = 0; u < UN; ++u) {
       const int64_t i0 = t0 + u * 128 + lane * 4;
@@ -317,8 +317,11 @@ __global__ void __launch_bounds__(COMPACT_WARPS * 32) sel_compact_kernel(
         const uint32_t m4 = max(max(key[0], key[1]), max(key[2], key[3]));
         kmax = max(kmax, m4);
         if (!__any_sync(0xffffffffu, m4 >= tau0)) continue;
+        // the exclusion set is looked up only for keys above the threshold
 #pragma unroll
-        for (int j = 0; j < 4; ++j) okm |= (uint32_t)(key[j] >= tau0) << j;
+        for (int j = 0; j < 4; ++j)
+          okm |= (uint32_t)(key[j] >= tau0 && !excluded(excl, i0 + j)) << j;
+        if (excl && !__any_sync(0xffffffffu, okm != 0)) continue;
       } else {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
