@@ -66,48 +66,51 @@ __global__ void __launch_bounds__(256) router_logits_kernel(const T* __restrict_
 
 // ------------------------------------------------------------------------------------------------
 // S2: one warp per token. k rounds of a warp argmax over the logits not yet taken; order is
-// (logit descending, expert ascending) with floating-point comparison (so -0 == +0).
+// (logit descending, expert ascending) with floating-point comparison (so -0 == +0). Lane l
+// holds the token's logits l, l + 32, ... in registers (NL of them), with a bit mask of the ones
+// taken; lane j keeps the j-th selection.
 // ------------------------------------------------------------------------------------------------
 __device__ __forceinline__ bool better(float v, int e, float bv, int be) {
   return v > bv || (v == bv && e < be);
 }
 
+template <int NL>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int Tn,
                                                    int E, int k, int renorm,
                                                    int32_t* __restrict__ topk_idx,
                                                    float* __restrict__ topk_w) {
-  extern __shared__ unsigned char smem_raw[];
-  const int warps = blockDim.x / 32;
-  const int wid = threadIdx.x / 32, lane = threadIdx.x % 32;
-  float* lw = reinterpret_cast<float*>(smem_raw) + wid * E;
-  unsigned char* taken = smem_raw + sizeof(float) * warps * E + wid * E;
-  const int t = blockIdx.x * warps + wid;
+  constexpr unsigned FULL = 0xffffffffu;
+  const int lane = threadIdx.x % 32;
+  const int t = blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
   if (t >= Tn) return;
   const float* row = logits + (int64_t)t * E;
+  float v[NL];
   float mx = -INFINITY;
-  for (int e = lane; e < E; e += 32) {
-    float v = row[e];
-    lw[e] = v;
-    taken[e] = 0;
-    mx = fmaxf(mx, v);
+#pragma unroll
+  for (int i = 0; i < NL; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = e < E ? row[e] : -INFINITY;
+    if (e < E) mx = fmaxf(mx, v[i]);
   }
-  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  __syncwarp();
-  float sel_l[32];
-  int sel_e[32];
+  for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, o));
+  uint32_t taken = 0;  // bit i: logit lane + 32 i is selected
+  float my_l = 0.f;    // lane j < k: the j-th selected logit and its expert
+  int my_e = 0;
 #pragma unroll 1
   for (int j = 0; j < k; ++j) {
     float bv = -INFINITY;
     int be = 0x7fffffff;
-    for (int e = lane; e < E; e += 32) {
-      if (!taken[e] && better(lw[e], e, bv, be)) {
-        bv = lw[e];
+#pragma unroll
+    for (int i = 0; i < NL; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !((taken >> i) & 1u) && better(v[i], e, bv, be)) {
+        bv = v[i];
         be = e;
       }
     }
     for (int o = 16; o; o >>= 1) {
-      float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      const float ov = __shfl_xor_sync(FULL, bv, o);
+      const int oe = __shfl_xor_sync(FULL, be, o);
       if (better(ov, oe, bv, be)) {
         bv = ov;
         be = oe;
@@ -115,25 +118,26 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
     }
     // every lane holds the same winner now
     if (be == 0x7fffffff) be = 0;  // only if all remaining logits are NaN
-    if (lane == 0) taken[be] = 1;
-    __syncwarp();
-    sel_l[j & 31] = bv;
-    sel_e[j & 31] = be;
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if (lane == j) {
+      my_l = bv;
+      my_e = be;
+    }
   }
+  const float ref = __shfl_sync(FULL, my_l, 0);
   float denom = 0.f;
-  const float ref = sel_l[0];
   if (renorm) {
-    for (int j = 0; j < k; ++j) denom += expf(sel_l[j] - ref);
+    for (int j = 0; j < k; ++j) denom += expf(__shfl_sync(FULL, my_l, j) - ref);
   } else {
-    float s = 0.f;
-    for (int e = lane; e < E; e += 32) s += expf(lw[e] - mx);
-    for (int o = 16; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-    denom = s;
+#pragma unroll
+    for (int i = 0; i < NL; ++i)
+      if (lane + 32 * i < E) denom += expf(v[i] - mx);
+    for (int o = 16; o; o >>= 1) denom += __shfl_xor_sync(FULL, denom, o);
   }
-  for (int j = lane; j < k; j += 32) {
-    float num = renorm ? expf(sel_l[j] - ref) : expf(sel_l[j] - mx);
-    topk_idx[(int64_t)t * k + j] = sel_e[j];
-    topk_w[(int64_t)t * k + j] = num / denom;
+  if (lane < k) {
+    const float num = renorm ? expf(my_l - ref) : expf(my_l - mx);
+    topk_idx[(int64_t)t * k + lane] = my_e;
+    topk_w[(int64_t)t * k + lane] = num / denom;
   }
 }
 
@@ -295,9 +299,22 @@ usaf_status route_launch(const usaf_moe_shape& s, const void* x, usaf_dtype xdt,
   {
     USAF_TRACE("route_topk", st);
     const int warps = 8;
-    size_t sm = (size_t)warps * E * (sizeof(float) + 1);
-    topk_kernel<<<(unsigned)ceil_div(Tn, warps), warps * 32, sm, st>>>(logits, Tn, E, k, renorm,
-                                                                       rt.topk_idx, rt.topk_w);
+    const dim3 grid((unsigned)ceil_div(Tn, warps));
+    const int nl = (E + 31) / 32;  // logits per lane (E <= 1024)
+    if (nl <= 1)
+      topk_kernel<1><<<grid, warps * 32, 0, st>>>(logits, Tn, E, k, renorm, rt.topk_idx, rt.topk_w);
+    else if (nl <= 2)
+      topk_kernel<2><<<grid, warps * 32, 0, st>>>(logits, Tn, E, k, renorm, rt.topk_idx, rt.topk_w);
+    else if (nl <= 4)
+      topk_kernel<4><<<grid, warps * 32, 0, st>>>(logits, Tn, E, k, renorm, rt.topk_idx, rt.topk_w);
+    else if (nl <= 8)
+      topk_kernel<8><<<grid, warps * 32, 0, st>>>(logits, Tn, E, k, renorm, rt.topk_idx, rt.topk_w);
+    else if (nl <= 16)
+      topk_kernel<16><<<grid, warps * 32, 0, st>>>(logits, Tn, E, k, renorm, rt.topk_idx,
+                                                    rt.topk_w);
+    else
+      topk_kernel<32><<<grid, warps * 32, 0, st>>>(logits, Tn, E, k, renorm, rt.topk_idx,
+                                                    rt.topk_w);
     USAF_CHECK_LAUNCH();
   }
   USAF_TRACE("route_permute", st);
