@@ -110,7 +110,8 @@ def test_rigl_hand_case():
     assert new.tolist() == c["new_idx"] and ns == c["D"]
 
 
-@pytest.mark.parametrize("N,K,D", [(50, 20, 6), (5000, 700, 200), (1 << 23, 41944, 12583)])
+@pytest.mark.parametrize("N,K,D", [(50, 20, 6), (5000, 700, 200), (5000, 700, 0),
+                                   (1 << 23, 41944, 12583)])
 def test_rigl_against_oracle(N, K, D):
     dev = device()
     rng = np.random.default_rng(N)
