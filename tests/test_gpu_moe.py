@@ -180,6 +180,72 @@ def test_qwen3_shaped_layer_sampled():
     assert np.isfinite(got["g_act"]).all()
 
 
+def _union_sample(ranges, n, rng):
+    """n distinct flat indices drawn uniformly from a union of disjoint [lo, hi) ranges."""
+    sizes = np.array([hi - lo for lo, hi in ranges], dtype=np.int64)
+    starts = np.concatenate([[0], np.cumsum(sizes)[:-1]])
+    got = np.empty(0, dtype=np.int64)
+    while got.size < n:
+        got = np.unique(np.concatenate([got, rng.integers(0, sizes.sum(), n - got.size + 64)]))
+    got = got[np.sort(rng.permutation(got.size)[:n])]
+    r = np.searchsorted(starts, got, side="right") - 1
+    return np.array([lo for lo, _ in ranges], dtype=np.int64)[r] + (got - starts[r])
+
+
+def skewed_mask(cfg, counts, seed):
+    """The skewed workload's active set: 80% of K uniformly over the weights of the 16 most
+    loaded experts, the rest over the others' (both tensors of each expert)."""
+    rng = np.random.default_rng(seed)
+    hot = set(np.argsort(-counts, kind="stable")[:16].tolist())
+    pgu, pd = 2 * cfg.I * cfg.H, cfg.H * cfg.I
+
+    def ranges(es):
+        return ([(e * pgu, (e + 1) * pgu) for e in es] +
+                [(cfg.N_gu + e * pd, cfg.N_gu + (e + 1) * pd) for e in es])
+    n_hot = int(0.8 * cfg.K)
+    a = _union_sample(ranges(sorted(hot)), n_hot, rng)
+    b = _union_sample(ranges([e for e in range(cfg.E) if e not in hot]), cfg.K - n_hot, rng)
+    return np.sort(np.concatenate([a, b]))
+
+
+@pytest.mark.parametrize("name,ntok", [("qwen3_skewed", 256), ("mixtral_8x7b", 48)])
+def test_large_layers_sampled(name, ntok):
+    """The skewed Qwen3-shaped layer (T=16384, Zipf loads with ten dead experts, 80% of the active
+    set on the 16 most loaded experts) and the Mixtral-8x7B-shaped layer (H=4096, E=8, top-2,
+    I=14336, T=8192), whole on the GPU. The oracle checks the routing of every token, Y, dx and
+    dw of a token sample, and the masked gradients of a sample of experts."""
+    dev = device()
+    cfg = synth.CONFIGS[name]
+    inp = synth.moe_inputs(cfg, seed=0)
+    if "zipf_s" in cfg.extra:
+        synth.apply_skew(inp, synth.skew_bias(cfg.E, cfg.extra["zipf_s"],
+                                              cfg.extra["dead_experts"], seed=0))
+    logits = oracle.router_logits(inp["x"], inp["w_router"])
+    idx, w = oracle.route_topk(logits, cfg.k)
+    counts = np.bincount(idx.reshape(-1), minlength=cfg.E)
+    act = (skewed_mask(cfg, counts, seed=5) if "zipf_s" in cfg.extra
+           else synth.uniform_mask(cfg.N, cfg.K, seed=0))
+    got = run_layer(cfg, inp, act, logits, dev)
+    assert (got["idx"] == idx).all() and got["status"] == 0
+    assert (got["count"] == counts).all()
+    if "dead_experts" in cfg.extra:  # the dead ones, and any of the lowest Zipf ranks
+        assert (counts == 0).sum() >= cfg.extra["dead_experts"]
+    toks = np.sort(np.random.default_rng(1).choice(cfg.T, ntok, replace=False))
+    b = oracle.moe_backward(inp["x"][toks], inp["w_router"], inp["w_gate_up"], inp["w_down"],
+                            idx[toks], w[toks], logits[toks], inp["dy"][toks])
+    for key in ("Y", "dx", "dw"):
+        assert rel_l2(got[key][toks], b[key]) <= 1e-2, key
+    live = np.nonzero(counts)[0]
+    experts = sorted({int(live[np.argmin(counts[live])]), int(live[len(live) // 2]),
+                      int(np.argmax(counts))})
+    g = oracle.masked_expert_grad(act, inp["x"], inp["w_gate_up"], inp["w_down"], idx, w,
+                                  inp["dy"], experts=experts)
+    sel = ~np.isnan(g)
+    assert sel.sum() > 1000
+    assert rel_l2(got["g_act"][sel], g[sel]) <= 1e-2
+    assert np.isfinite(got["g_act"]).all() and np.isfinite(got["g_router"]).all()
+
+
 def run_dense(cfg, inp, logits, dev, twice=False):
     """Route, forward and the dense backward; with twice=True a second call accumulates."""
     s = B.shape(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I)
