@@ -158,6 +158,17 @@ usaf_status usaf_moe_fwd(const usaf_moe_shape* shape, usaf_dtype dtype, const vo
                          void* x_perm_save, void* h_save, void* wa_save, void* y, void* ws,
                          size_t ws_bytes, void* stream);
 
+/* usaf_moe_fwd_wait - usaf_moe_fwd whose reads of the expert weights wait for a CUDA event.
+ * weights_ready is a cudaEvent_t (NULL: no wait, the same as usaf_moe_fwd), typically recorded
+ * by the caller on another stream after an optimizer update of w_gate_up / w_down. The token
+ * gather into x_perm_save, which reads only x and the routing tables, is enqueued before the
+ * wait and so overlaps that update; everything after it on `stream` is ordered after the event.
+ * Same results and errors as usaf_moe_fwd. */
+usaf_status usaf_moe_fwd_wait(const usaf_moe_shape* shape, usaf_dtype dtype, const void* x,
+                              const void* w_gate_up, const void* w_down, const usaf_routing* rt,
+                              void* x_perm_save, void* h_save, void* wa_save, void* y,
+                              void* weights_ready, void* ws, size_t ws_bytes, void* stream);
+
 /* ---------------------------------------------------------------------------------------------
  * usaf_moe_bwd_sparse - sparse backward of the layer for upstream gradient dy = dL/dY.
  * Per slot: gvec = down_proj[e]^T dy[t], dw = <gvec, A>, dA = w*gvec, dgate = dA*up*silu'(gate),

@@ -63,6 +63,7 @@ _SIGS = {
     "usaf_route_topk_noalloc": (_INT, [_P, _P, _INT, _P, _P, _P, _INT, _P, _P]),
     "usaf_moe_fwd_workspace_size": (_SZ, [_P, _INT]),
     "usaf_moe_fwd": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "usaf_moe_fwd_wait": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "usaf_moe_bwd_workspace_size": (_SZ, [_P, _INT, _I64]),
     "usaf_moe_bwd_sparse": (_INT, [_P, _INT, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    _I64, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -206,14 +207,18 @@ def moe_fwd_workspace_size(s: Shape, dt: int) -> int:
     return int(lib().usaf_moe_fwd_workspace_size(ctypes.byref(s), dt))
 
 
-def moe_fwd(s: Shape, x, w_gate_up, w_down, rt: Routing, x_perm, h, wa, y, ws=None, stream=None):
+def moe_fwd(s: Shape, x, w_gate_up, w_down, rt: Routing, x_perm, h, wa, y, ws=None, stream=None,
+            weights_ready=None):
+    """weights_ready: a recorded torch.cuda.Event that the reads of the expert weights wait for
+    (the token gather before them does not)."""
     dt = _dt(x)
     if ws is None:
         ws = _ws(moe_fwd_workspace_size(s, dt), x.device)
     r = rt.c()
-    _check("usaf_moe_fwd", lib().usaf_moe_fwd(
+    ev = None if weights_ready is None else ctypes.c_void_p(weights_ready.cuda_event)
+    _check("usaf_moe_fwd_wait", lib().usaf_moe_fwd_wait(
         ctypes.byref(s), dt, _ptr(x), _ptr(w_gate_up), _ptr(w_down), ctypes.byref(r),
-        _ptr(x_perm), _ptr(h), _ptr(wa), _ptr(y), _ptr(ws), ws.numel(), _stream(stream)))
+        _ptr(x_perm), _ptr(h), _ptr(wa), _ptr(y), ev, _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def moe_bwd_workspace_size(s: Shape, dt: int, K: int) -> int:

@@ -212,10 +212,10 @@ static usaf_status fill_args(MoeArgs& a, const usaf_moe_shape* s, usaf_dtype dt,
   return USAF_OK;
 }
 
-usaf_status usaf_moe_fwd(const usaf_moe_shape* s, usaf_dtype dt, const void* x,
-                         const void* w_gate_up, const void* w_down, const usaf_routing* rt,
-                         void* x_perm_save, void* h_save, void* wa_save, void* y, void* ws,
-                         size_t ws_bytes, void* stream) {
+usaf_status usaf_moe_fwd_wait(const usaf_moe_shape* s, usaf_dtype dt, const void* x,
+                              const void* w_gate_up, const void* w_down, const usaf_routing* rt,
+                              void* x_perm_save, void* h_save, void* wa_save, void* y,
+                              void* weights_ready, void* ws, size_t ws_bytes, void* stream) {
   MoeArgs a{};
   USAF_TRY(fill_args(a, s, dt, x, nullptr, w_gate_up, w_down, rt));
   if (!x_perm_save || !h_save || !wa_save || !y) return USAF_ERR_INVALID_ARG;
@@ -224,7 +224,16 @@ usaf_status usaf_moe_fwd(const usaf_moe_shape* s, usaf_dtype dt, const void* x,
   FwdWs w;
   fwd_ws_layout(*s, dt, c, w);
   return moe_fwd_launch(a, x_perm_save, h_save, wa_save, y, w,
+                        static_cast<cudaEvent_t>(weights_ready),
                         static_cast<cudaStream_t>(stream));
+}
+
+usaf_status usaf_moe_fwd(const usaf_moe_shape* s, usaf_dtype dt, const void* x,
+                         const void* w_gate_up, const void* w_down, const usaf_routing* rt,
+                         void* x_perm_save, void* h_save, void* wa_save, void* y, void* ws,
+                         size_t ws_bytes, void* stream) {
+  return usaf_moe_fwd_wait(s, dt, x, w_gate_up, w_down, rt, x_perm_save, h_save, wa_save, y,
+                           nullptr, ws, ws_bytes, stream);
 }
 
 size_t usaf_moe_bwd_workspace_size(const usaf_moe_shape* s, usaf_dtype dt, int64_t K) {

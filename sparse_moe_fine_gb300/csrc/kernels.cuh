@@ -56,8 +56,10 @@ struct MoeArgs {
   float* wperm;   // [R_cap] routing weight of each permuted row (0 in padding), by the gather
 };
 
+// weights_ready (may be null): the kernels that read the expert weights wait for it; the token
+// gather before them does not
 usaf_status moe_fwd_launch(const MoeArgs& a, void* x_perm, void* h, void* wa, void* y, FwdWs& w,
-                           cudaStream_t st);
+                           cudaEvent_t weights_ready, cudaStream_t st);
 usaf_status moe_bwd_launch(const MoeArgs& a, int renorm, const float* logits, const void* x_perm,
                            const void* h, const void* wa, const void* dy, const int64_t* act_idx,
                            int64_t K, float* g_act, float* g_router, void* dx, float* dw_slot,

@@ -823,7 +823,7 @@ static usaf_status fwd_simt(const MoeArgs& a, T* xT, T* hT, T* waT, float* yacc,
 
 template <typename T>
 static usaf_status moe_fwd_t(const MoeArgs& a, T* xT, T* hT, T* waT, T* y, FwdWs& w,
-                             cudaStream_t st) {
+                             cudaEvent_t weights_ready, cudaStream_t st) {
   const auto& s = a.s;
   const int64_t TH = s.T * s.H;
   MoeArgs aw = a;
@@ -835,6 +835,9 @@ static usaf_status moe_fwd_t(const MoeArgs& a, T* xT, T* hT, T* waT, T* y, FwdWs
                          a.dt == USAF_BF16 ? w.plan : nullptr};
     USAF_TRY(gather_t<T>(aw, static_cast<const T*>(a.x), xT, st, ex));
   }
+  // the expert weights are read from here on: wait for their last update only now
+  if (weights_ready && cudaStreamWaitEvent(st, weights_ready, 0) != cudaSuccess)
+    return USAF_ERR_CUDA;
   if (a.dt == USAF_BF16) {
     MoeArgs b = aw;
     b.plan = w.plan;
@@ -850,14 +853,14 @@ static usaf_status moe_fwd_t(const MoeArgs& a, T* xT, T* hT, T* waT, T* y, FwdWs
 }
 
 usaf_status moe_fwd_launch(const MoeArgs& a, void* x_perm, void* h, void* wa, void* y, FwdWs& w,
-                           cudaStream_t st) {
+                           cudaEvent_t weights_ready, cudaStream_t st) {
   if (a.dt == USAF_BF16)
     return moe_fwd_t<__nv_bfloat16>(a, static_cast<__nv_bfloat16*>(x_perm),
                                     static_cast<__nv_bfloat16*>(h),
                                     static_cast<__nv_bfloat16*>(wa),
-                                    static_cast<__nv_bfloat16*>(y), w, st);
+                                    static_cast<__nv_bfloat16*>(y), w, weights_ready, st);
   return moe_fwd_t<float>(a, static_cast<float*>(x_perm), static_cast<float*>(h),
-                          static_cast<float*>(wa), static_cast<float*>(y), w, st);
+                          static_cast<float*>(wa), static_cast<float*>(y), w, weights_ready, st);
 }
 
 // Dense expert weight gradient on CUDA cores (fp32 layers): one thread per entry of

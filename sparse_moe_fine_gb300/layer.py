@@ -118,10 +118,12 @@ class MoELayer:
             self.pending_opt = False
 
     def forward(self, x, stream=None, y=None):
-        self.wait_optimizer(stream)
+        """The token gather overlaps the last expert update; the GEMMs wait for it."""
         y = self.y if y is None else y
+        ready = self.ev_opt if self.pending_opt else None
         B.moe_fwd(self.s, x, self.w_gate_up, self.w_down, self.rt, self.x_perm, self.h, self.wa,
-                  y, ws=self.ws_fwd, stream=stream)
+                  y, ws=self.ws_fwd, stream=stream, weights_ready=ready)
+        self.pending_opt = False  # the stream is ordered after the update from here on
         return y
 
     def backward(self, x, dy, want_dx=True, stream=None, dx=None):

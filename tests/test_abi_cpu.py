@@ -12,7 +12,7 @@ from sparse_moe_fine_gb300 import binding as B
 def test_library_exports_every_header_symbol():
     L = B.lib()
     syms = B.header_symbols()
-    assert len(syms) == 22
+    assert len(syms) == 23
     for s in syms:
         assert hasattr(L, s), s
     assert L.usaf_abi_version() == 1

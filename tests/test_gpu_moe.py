@@ -246,6 +246,45 @@ def test_large_layers_sampled(name, ntok):
     assert np.isfinite(got["g_act"]).all() and np.isfinite(got["g_router"]).all()
 
 
+def test_fwd_waits_for_weights_ready():
+    """usaf_moe_fwd_wait: the GEMMs read the expert weights only after the given event, here
+    recorded behind a delayed update of w_gate_up on another stream; the result is the forward of
+    the updated weights, not of the ones in memory when the call was enqueued."""
+    dev = device()
+    cfg = synth.small_config("wait", T=256, H=128, E=8, k=2, I=64, bf16=True)
+    inp = synth.moe_inputs(cfg, seed=6)
+    s = B.shape(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I)
+    x = to_dev(inp["x"], dev, True)
+    wr = to_dev(inp["w_router"], dev)
+    wgu = to_dev(inp["w_gate_up"], dev, True)
+    wd = to_dev(inp["w_down"], dev, True)
+    w_new = wgu * 2
+    rt = B.Routing.empty(s, dev)
+    B.route_topk(s, x, wr, rt)
+    cap = B.routed_rows_capacity(s)
+    bufs = lambda: (torch.empty(cfg.H, cap, dtype=torch.bfloat16, device=dev),
+                    torch.empty(2 * cfg.I, cap, dtype=torch.bfloat16, device=dev),
+                    torch.empty(cfg.I, cap, dtype=torch.bfloat16, device=dev),
+                    torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev))
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream(device=dev)
+    ev = torch.cuda.Event()
+    with torch.cuda.stream(side):
+        torch.cuda._sleep(100_000_000)  # tens of milliseconds: the update lands late
+        wgu.copy_(w_new)
+        ev.record(side)
+    xp, h, wa, y = bufs()
+    B.moe_fwd(s, x, wgu, wd, rt, xp, h, wa, y, weights_ready=ev)
+    torch.cuda.synchronize()
+    xp2, h2, wa2, y_new = bufs()
+    B.moe_fwd(s, x, w_new, wd, rt, xp2, h2, wa2, y_new)
+    xp3, h3, wa3, y_old = bufs()
+    B.moe_fwd(s, x, w_new / 2, wd, rt, xp3, h3, wa3, y_old)
+    torch.cuda.synchronize()
+    assert rel_l2(y.float().cpu().numpy(), y_new.float().cpu().numpy()) <= 1e-4
+    assert rel_l2(y_old.float().cpu().numpy(), y_new.float().cpu().numpy()) > 1e-2
+
+
 def run_dense(cfg, inp, logits, dev, twice=False):
     """Route, forward and the dense backward; with twice=True a second call accumulates."""
     s = B.shape(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I)
