@@ -73,6 +73,7 @@ class MoELayer:
         self.ev_bwd = torch.cuda.Event()
         self.ev_opt = torch.cuda.Event()
         self.pending_opt = False
+        self.replayed_kernels = 0  # library kernels run by graph replays (graphed_train_step)
         self.ws_route = torch.empty(B.route_topk_workspace_size(self.s), dtype=torch.uint8,
                                     device=d)
         self.ws_fwd = torch.empty(B.moe_fwd_workspace_size(self.s, self.dt), dtype=torch.uint8,
@@ -102,6 +103,7 @@ class MoELayer:
         self.g_act = torch.empty(K, device=self.dev)
         self.ws_bwd = torch.empty(B.moe_bwd_workspace_size(self.s, self.dt, K),
                                   dtype=torch.uint8, device=self.dev)
+        self._graphs = {}  # captured steps hold the old active set's pointers
 
     # ------------------------------------------------------------------ the step
     def route(self, x, stream=None):
@@ -165,6 +167,48 @@ class MoELayer:
         self.backward(x, dy, stream=stream, dx=dx)
         self.optimizer_step(stream)
         return y, (self.dx if dx is None else dx)
+
+    def graphed_train_step(self, x, dy, stream=None):
+        """train_step with the routing and the forward + sparse backward replayed from CUDA graphs,
+        captured on first use for these x and dy buffers (one pair per status-word parity), so
+        their dependent launches run without per-launch gaps. The expert update of the previous
+        step overlaps the routing graph; the forward graph starts after it. The two SparseAdam
+        updates stay ordinary launches, since their step sizes change every step. Outputs are
+        the layer's own y and dx buffers."""
+        main = self._main(stream)
+        par = self.step_count % 2
+        key = (x.data_ptr(), dy.data_ptr(), par)
+        if key not in self._graphs:
+            self._graphs[key] = self._capture(x, dy, par, main)
+        g_route, g_body, n_kernels = self._graphs[key]
+        self.status = self.status2[par:par + 1]
+        with torch.cuda.stream(main):
+            g_route.replay()
+            self.wait_optimizer(main)
+            g_body.replay()
+        self.replayed_kernels += n_kernels
+        self.optimizer_step(main)
+        return self.y, self.dx
+
+    def _capture(self, x, dy, par, main):
+        status = self.status2[par:par + 1]
+        cs = torch.cuda.Stream(device=self.dev)
+        cs.wait_stream(main)
+        g_route, g_body = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        n0 = B.launch_count()
+        with torch.cuda.graph(g_route, stream=cs):
+            status.zero_()
+            B.route_topk(self.s, x, self.w_router, self.rt, logits_out=self.logits,
+                         renorm=self.renorm, ws=self.ws_route, stream=cs)
+        with torch.cuda.graph(g_body, stream=cs):
+            B.moe_fwd(self.s, x, self.w_gate_up, self.w_down, self.rt, self.x_perm, self.h,
+                      self.wa, self.y, ws=self.ws_fwd, stream=cs)
+            B.moe_bwd_sparse(self.s, x, self.w_router, self.w_gate_up, self.w_down, self.rt,
+                             self.x_perm, self.h, self.wa, dy, self.act, self.g_act,
+                             self.g_router, dx=self.dx, logits=self.logits, renorm=self.renorm,
+                             dev_status=status, ws=self.ws_bwd, stream=cs)
+        main.wait_stream(cs)
+        return g_route, g_body, B.launch_count() - n0  # library kernels in the two graphs
 
     def train_step_host(self, x_host, dy_host, y_host, dx_host, x_dev, dy_dev, stream=None):
         """The same step fed from (pinned) host memory: copy x and dy in, run, copy y and dx out."""
