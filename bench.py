@@ -438,7 +438,7 @@ def run_steps(args, B, MoELayer, dist, ws, rank, local, dev, cfg, inp, x, dy, wg
 
     # ---- end to end: x, dy from pinned host memory, y and dx back, through the layer API
     if args.no_e2e:
-        e2e_ms = float("nan")
+        e2e_ms = None
     else:
         e2e_ms = e2e_time(args, layer, x, dy, e0, e1, stream, dist, dev)
     nbytes = x.numel() * 2
@@ -516,9 +516,10 @@ def make_line(args, cfg, ws, ms, value, step_roof_ms, fl, by, roof, trace, tot, 
         "roofline": roof,
         "kernels": [kernel_entry(n, l, t, tot, units, hbm, tf_burst) for n, l, t in trace],
         "importance_pass": importance,
-        "e2e": {"value": ws * cfg.T / (e2e_ms / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": 2 * nbytes, "d2h_bytes_per_step": 2 * nbytes,
-                "ms_per_step": e2e_ms},
+        "e2e": None if e2e_ms is None else {
+            "value": ws * cfg.T / (e2e_ms / 1e3), "unit": "tokens/s",
+            "h2d_bytes_per_step": 2 * nbytes, "d2h_bytes_per_step": 2 * nbytes,
+            "ms_per_step": e2e_ms},
         "gpu_launches": int(launches) * args.steps,
         "clocks": clk.summary(),
     }
