@@ -106,7 +106,20 @@ class MoELayer:
         self._graphs = {}  # captured steps hold the old active set's pointers
 
     # ------------------------------------------------------------------ the step
+    def _check_tokens(self, **ts):
+        """The library reads and writes [T, H] token tensors through bare pointers, so their
+        shape, dtype and layout are checked here, before any launch."""
+        for name, t in ts.items():
+            if t is None:
+                continue
+            if tuple(t.shape) != (self.T, self.H) or t.dtype != self.dtype:
+                raise ValueError(f"{name}: expected a [{self.T}, {self.H}] {self.dtype} tensor, "
+                                 f"got {list(t.shape)} {t.dtype}")
+            if not (t.is_cuda and t.is_contiguous()):
+                raise ValueError(f"{name}: expected a contiguous CUDA tensor")
+
     def route(self, x, stream=None):
+        self._check_tokens(x=x)
         B.route_topk(self.s, x, self.w_router, self.rt, logits_out=self.logits,
                      renorm=self.renorm, ws=self.ws_route, stream=stream)
 
@@ -122,6 +135,7 @@ class MoELayer:
     def forward(self, x, stream=None, y=None):
         """The token gather overlaps the last expert update; the GEMMs wait for it."""
         y = self.y if y is None else y
+        self._check_tokens(x=x, y=y)
         ready = self.ev_opt if self.pending_opt else None
         B.moe_fwd(self.s, x, self.w_gate_up, self.w_down, self.rt, self.x_perm, self.h, self.wa,
                   y, ws=self.ws_fwd, stream=stream, weights_ready=ready)
@@ -130,6 +144,7 @@ class MoELayer:
 
     def backward(self, x, dy, want_dx=True, stream=None, dx=None):
         dx = self.dx if dx is None else dx
+        self._check_tokens(x=x, dy=dy, dx=dx)
         B.moe_bwd_sparse(self.s, x, self.w_router, self.w_gate_up, self.w_down, self.rt,
                          self.x_perm, self.h, self.wa, dy, self.act, self.g_act, self.g_router,
                          dx=dx if want_dx else None, logits=self.logits,
@@ -174,7 +189,9 @@ class MoELayer:
         their dependent launches run without per-launch gaps. The expert update of the previous
         step overlaps the routing graph; the forward graph starts after it. The two SparseAdam
         updates stay ordinary launches, since their step sizes change every step. Outputs are
-        the layer's own y and dx buffers."""
+        the layer's own y and dx buffers. One graph pair is kept per distinct (x, dy) buffer pair
+        and parity, so a caller cycles through a fixed set of input buffers."""
+        self._check_tokens(x=x, dy=dy)
         main = self._main(stream)
         par = self.step_count % 2
         key = (x.data_ptr(), dy.data_ptr(), par)
