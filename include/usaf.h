@@ -175,8 +175,8 @@ usaf_status usaf_moe_fwd_wait(const usaf_moe_shape* shape, usaf_dtype dtype, con
  * dup = dA*silu(gate). Router: dlogit[t,e_j] = w_j*(dw_j - sum_i w_i dw_i) (renorm=1; renorm=0
  * uses the all-E softmax form), g_router = dlogit^T x. dx = sum_j gate_up_proj[e_j]^T dh_j +
  * dlogit . w_router. Expert weight gradients are formed only at the active set
- * (the news article's "updates only a subset of weights within each activated expert";
- * the README's "Backward ~30ms/layer (26M params)"):
+ * (news article, key differences: inside each expert that fires, only part of its weights is
+ * trained; README, A100 operations table: the backward row, counted over the trained 26M):
  *   g_act[a] = sum over rows of expert e of dh[row, r] * x[tok, c]         (gate_up entry e,r,c)
  *   g_act[a] = sum over rows of expert e of dy[tok, r] * w * A[row, c]      (down entry e,r,c)
  * Experts that received no token get zero gradient.

@@ -17,8 +17,8 @@ Sources (page title and section):
     reselection every 50 steps), the A100 operations table (SparseAdam over the trained 26M),
     the results table (steps with NaN are skipped).
   * "USAF Open Source: 12G VRAM Fine-Tuning Qwen3-30B MoE", section on the key differences
-    (a subset of weights within each activated expert is updated; optimizer state only for it;
-    only routed experts receive gradients).
+    (only part of the weights of each routed expert is trained, and only that part has optimizer
+    state; experts that receive no token get no gradient).
   * experts4bit-qlora page, "The abstraction that fails, and what replaces it" (fused layouts
     gate_up_proj [E,2I,H], down_proj [E,H,I]) and its epilogue-contract bullet (act(gate)*up).
 

@@ -1,8 +1,8 @@
 // Exact top-K selection by magnitude (the importance phase) and RigL drop/grow.
 //
 // USAF README: "Not all weights matter" (the importance phase keeps the 0.5% of weights with the
-// highest gradient magnitude) and "Sparsity adapts" (RigL reselection replaces underperforming
-// weights every 50 steps). Order: key descending, flat index ascending among equal keys; the key
+// highest gradient magnitude) and "Sparsity adapts" (every 50 steps RigL swaps active weights
+// that contribute little for inactive ones with large gradients). Order: key descending, flat index ascending among equal keys; the key
 // of |g| is its fp32 bit pattern with the sign cleared.
 //
 // Fast path, one read of g: a strided sample gives a candidate threshold tau0 a safe margin below
