@@ -1,0 +1,85 @@
+"""The benchmark's roofline arithmetic, checked on the host: the per-step algorithmic FLOPs and
+bytes, and each main kernel's per-launch bytes, against the same quantities summed term by term
+from the tensor sizes of the Qwen3-30B-A3B-shaped layer (T 4096, H 2048, E 128, top-8, I 768,
+K = 3,019,899 active entries)."""
+import importlib.util
+import os
+
+import pytest
+
+from sparse_moe_fine_gb300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def bench():
+    spec = importlib.util.spec_from_file_location("bench", os.path.join(ROOT, "bench.py"))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)  # defines functions only; main() is not run
+    return mod
+
+
+CFG = synth.CONFIGS["qwen3_30b_a3b"]
+MB = 1e6
+
+
+def test_workload_sizes():
+    assert (CFG.T, CFG.H, CFG.E, CFG.k, CFG.I) == (4096, 2048, 128, 8, 768)
+    assert CFG.N == 603_979_776 and CFG.K == 3_019_899
+
+
+def test_step_flops_by_term(bench):
+    fl, _ = bench.algorithmic(CFG)
+    R = 32_768  # routed rows, T * k
+    terms_gf = {
+        "forward: gate_up 2*R*2I*H + down 2*R*I*H": 206.158 + 103.079,
+        "dgrad through down": 103.079,
+        "dx through gate_up": 206.158,
+        "router: logits, its gradient, the dx term": 3 * 2 * 4096 * 128 * 2048 / 1e9,
+        "masked dW: 2 flops per (entry, routed token), R/E tokens per expert":
+            2 * 3_019_899 * (R / 128) / 1e9,
+    }
+    assert fl / 1e9 == pytest.approx(sum(terms_gf.values()), rel=1e-4)
+    assert fl / 1e9 == pytest.approx(626.46, abs=0.01)
+
+
+def test_step_bytes_by_term(bench):
+    _, by = bench.algorithmic(CFG)
+    terms_mb = {
+        "expert weights read in the forward and again in the backward": 2 * 1207.96,
+        "x read twice (router, gather)": 33.55,
+        "h written and read (bf16 [R, 2I])": 201.33,
+        "A written and read (bf16 [R, I])": 100.66,
+        "y, dy, dx once each": 50.33,
+        "dh written and read": 201.33,
+        "logits written and read (fp32 [T, E])": 4.19,
+        "gradients written and read (K + E*H fp32)": 26.26,
+        "SparseAdam: 8 idx + 4 g + 3 x 4 read + 3 x 4 written + 2 weight per entry":
+            34 * (3_019_899 + 262_144) / MB,
+    }
+    assert by / MB == pytest.approx(sum(terms_mb.values()), rel=2e-4)
+    assert by / 1e9 == pytest.approx(3.145, abs=0.001)
+
+
+def test_kernel_bytes_match_the_operands(bench):
+    u = bench.kernel_units(CFG)
+    w_gu, w_d = 805.31, 402.65  # bf16 [E, 2I, H] and [E, H, I]
+    x_perm, h, wa = 134.22, 100.66, 50.33  # bf16 [R, H], [R, 2I], [R, I]
+    expect = {
+        "tc_gate_up_swiglu": w_gu + x_perm + h + wa,
+        "tc_down_combine": w_d + wa,
+        "tc_gvec_swiglu_bwd": w_d + x_perm + h + h,  # dy_perm [R, H], h read, dh written
+        "tc_dx": w_gu + h,                           # dh [R, 2I]
+        "gather_x": 16.78 + x_perm,
+        "wgrad_sddmm": h + x_perm + x_perm + wa + 3_019_899 * 12 / MB,
+    }
+    for name, mb in expect.items():
+        assert u[name][1] / MB == pytest.approx(mb, rel=2e-4), name
+    assert u["tc_gate_up_swiglu"][0] == u["tc_dx"][0] == 2 * 32_768 * 1536 * 2048
+    assert u["tc_down_combine"][0] == u["tc_gvec_swiglu_bwd"][0] == 2 * 32_768 * 768 * 2048
+
+
+def test_traffic_is_reported_only_for_captured_kernels(bench):
+    assert bench.ncu_traffic("gather_x") is None
+    assert set(bench.NCU_TRAFFIC) <= set(bench.kernel_units(CFG))
