@@ -5,8 +5,14 @@ import ctypes
 import math
 
 import pytest
+import torch
 
 from sparse_moe_fine_gb300 import binding as B
+
+# The argument-check tests pass fake device addresses that a launch would dereference. They are
+# meant for a machine without a GPU, where a check that failed to refuse could not reach a device.
+fake_addresses = pytest.mark.skipif(torch.cuda.is_available(),
+                                    reason="fake device addresses; run where no GPU is visible")
 
 
 def test_library_exports_every_header_symbol():
@@ -42,6 +48,7 @@ def _call(name, *args):
     return getattr(B.lib(), name)(*args)
 
 
+@fake_addresses
 def test_host_argument_checks_return_codes():
     s = B.shape(8, 64, 4, 2, 64)
     r = B._Routing()
@@ -78,6 +85,7 @@ def test_host_argument_checks_return_codes():
                  1, 1, 1, 1, 1, 1 << 30, None) == 2
 
 
+@fake_addresses
 def test_reselect_full_host_checks():
     L = B.lib()
     N, K = 1 << 20, 5000
@@ -102,3 +110,41 @@ def test_reselect_full_host_checks():
                                 ctypes.c_void_p(7 << 20), ctypes.c_void_p(8 << 20), fake, None,
                                 fake, 16, None) == 3
 
+
+
+@fake_addresses
+def test_layer_call_host_checks():
+    """The forward and backward entry points refuse bad arguments on the host, before any launch:
+    every pointer below is a fake address that a launch would fault on."""
+    s = B.shape(64, 64, 4, 2, 64)
+    rt = ctypes.byref(B._Routing(*[4096] * 7))
+    f = 8192  # fake device address, 16-byte aligned
+    big = 1 << 30
+    fwd_ws = B.moe_fwd_workspace_size(s, B.BF16)
+    bwd_ws = B.moe_bwd_workspace_size(s, B.BF16, 100)
+    assert fwd_ws > 0 and bwd_ws > 0
+    fwd = lambda y, ev, ws: _call("usaf_moe_fwd_wait", ctypes.byref(s), B.BF16, f, f, f, rt, f, f,
+                                  f, y, ev, f, ws, None)
+    assert fwd(None, None, big) == 1           # no output buffer
+    assert fwd(f, None, fwd_ws - 1) == 3       # workspace one byte short
+    assert fwd(f, f, fwd_ws - 1) == 3          # the same with an event to wait for
+    assert _call("usaf_moe_fwd_wait", ctypes.byref(s), 7, f, f, f, rt, f, f, f, f, None, f, big,
+                 None) == 1                    # unknown dtype
+
+    def bwd(name, renorm=1, logits=f, K=100, ws=big):
+        return _call(name, ctypes.byref(s), B.BF16, renorm, f, f, f, f, rt, logits, f, f, f, f,
+                     f, K, f, f, f, None, None, f, ws, None)
+    for name in ("usaf_moe_bwd_sparse", "usaf_moe_bwd_sparse_accumulate"):
+        assert bwd(name, renorm=2) == 1                 # renorm must be 0 or 1
+        assert bwd(name, renorm=0, logits=None) == 1    # the all-E softmax form needs the logits
+        assert bwd(name, K=-1) == 1
+        assert bwd(name, K=64 * 3 * 64 * 4 + 1) == 1    # K > N
+        assert bwd(name, ws=bwd_ws - 1) == 3
+
+    def dense(g, acc=0, ws=big):
+        return _call("usaf_moe_bwd_dense", ctypes.byref(s), B.BF16, 1, f, f, f, f, rt, f, f, f,
+                     f, f, g, acc, f, f, None, None, f, ws, None)
+    assert dense(f + 4) == 1          # the dense gradient must be 16-byte aligned
+    assert dense(f, acc=2) == 1       # accumulate must be 0 or 1
+    assert dense(None) == 1
+    assert dense(f, ws=B.moe_bwd_workspace_size(s, B.BF16, 0) - 1) == 3
