@@ -320,7 +320,9 @@ usaf_status usaf_reselect_full(const float* g, int64_t N, int64_t K, const int64
  * path is bracketed by two CUDA events recorded on its stream, so per-kernel device time can be
  * read without a profiler. usaf_trace_enable(1) clears earlier records; usaf_trace_summary
  * waits for the recorded events, then fills up to `cap` entries (one per kernel name, in order
- * of first launch) and returns how many names were seen, or -1 on a CUDA error.
+ * of first launch) and returns how many names were seen, or -1 on a CUDA error. The trace times
+ * launches issued directly; keep it off while capturing calls into a CUDA graph, since events
+ * recorded during a capture mark graph dependencies and are never timed.
  * ------------------------------------------------------------------------------------------- */
 typedef struct {
   char name[48];
@@ -332,7 +334,9 @@ usaf_status usaf_trace_enable(int on);
 int usaf_trace_summary(usaf_trace_entry* out, int cap);
 
 /* Number of kernel launches the library has issued since it was loaded (all threads). A caller
- * can difference two readings to count the device work behind a sequence of calls. */
+ * can difference two readings to count the device work behind a sequence of calls. A call
+ * captured into a CUDA graph counts its launches once, at capture; replays of the graph add
+ * nothing, so a caller that replays graphs counts their kernels itself. */
 int64_t usaf_launch_count(void);
 
 #ifdef __cplusplus
