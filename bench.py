@@ -261,12 +261,11 @@ def run_reference(args):
             "ms_per_step": 1e3 * sec / len(times) * (cfg.T / tokens),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": f"{WORKLOAD} layer step, oracle on a {tokens}-token sample",
-                       "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I,
-                       "active": cfg.K},
+            "config": workload_config(cfg, ws),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads(),
                              "kind": "oracle",
-                             "sample": f"first {tokens} of {cfg.T} tokens per step"},
+                             "sample": f"one step on the first {tokens} of {cfg.T} tokens, "
+                                       "per timed step"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -499,18 +498,23 @@ def kernel_entry(n, l, t, tot, units, hbm, tf_burst):
     return e
 
 
+def workload_config(cfg, ws):
+    """The `config` object of the JSON line; both arms report the same one."""
+    return {"workload": f"{WORKLOAD} layer step", "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k,
+            "I": cfg.I, "active": cfg.K, "router": "fp32",
+            "optimizer": "SparseAdam (experts at the active set, router dense)",
+            "parallelism": f"dp{ws}" + (" (all-reduce of the compact gradients)"
+                                        if ws > 1 else ""),
+            "l2": "inputs larger than L2 (1.2 GB of expert weights per step)"}
+
+
 def make_line(args, cfg, ws, ms, value, step_roof_ms, fl, by, roof, trace, tot, importance,
               e2e_ms, nbytes, launches, clk, units, hbm, tf_burst):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD} layer step", "T": cfg.T, "H": cfg.H, "E": cfg.E,
-                   "k": cfg.k, "I": cfg.I, "active": cfg.K, "router": "fp32",
-                   "optimizer": "SparseAdam (experts at the active set, router dense)",
-                   "parallelism": f"dp{ws}" + (" (all-reduce of the compact gradients)"
-                                               if ws > 1 else ""),
-                   "l2": "inputs larger than L2 (1.2 GB of expert weights per step)"},
+        "config": workload_config(cfg, ws),
         "step_roofline": {"ms": step_roof_ms, "frac": step_roof_ms / ms,
                           "algorithmic_gflop": fl / 1e9, "algorithmic_gb": by / 1e9},
         "roofline": roof,

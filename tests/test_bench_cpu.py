@@ -83,3 +83,45 @@ def test_kernel_bytes_match_the_operands(bench):
 def test_traffic_is_reported_only_for_captured_kernels(bench):
     assert bench.ncu_traffic("gather_x") is None
     assert set(bench.NCU_TRAFFIC) <= set(bench.kernel_units(CFG))
+
+
+def test_clock_summary_parses_throttle_reasons(bench):
+    clk = bench.ClockSampler(0)
+    clk.lines = ["2070, 2070, 900.5, 0x4, Not Active, Not Active, Not Active, Active",
+                 "2055, 2070, 910.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+                 "[N/A], 2070, 0, 0x0, Not Active, Not Active, Not Active, Not Active",
+                 "2070, 2070, 905.0, 0x0, Not Active, Not Active, Not Active, Not Active"]
+    s = clk.summary()
+    assert s == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": ["sw_power_cap"],
+                 "samples": 3}
+
+
+def test_json_line_carries_every_contract_key(bench):
+    import argparse
+    args = argparse.Namespace(steps=200, warmup=5)
+    clk = bench.ClockSampler(0)
+    clk.lines = ["2070, 2070, 900, 0x0, Not Active, Not Active, Not Active, Not Active"]
+    fl, by = bench.algorithmic(CFG)
+    units = bench.kernel_units(CFG)
+    trace = [("tc_dx", 200, 48.7), ("wgrad_sddmm", 200, 41.1), ("route_topk", 200, 2.4)]
+    nbytes = CFG.T * CFG.H * 2
+    roof = {"bound": "hbm", "achieved": 3700.0, "peak": 6779.0, "unit": "GB/s", "frac": 0.55,
+            "traffic": None}
+    line = bench.make_line(args, CFG, 1, 1.31, 3.1e6, 0.464, fl, by, roof, trace, 92.2, None,
+                           1.36, nbytes, 22, clk, units, 6779.0, 1918.6)
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "roofline", "e2e", "gpu_launches", "clocks"):
+        assert key in line, key
+    assert line["config"] == bench.workload_config(CFG, 1)
+    assert line["config"]["workload"] == "qwen3_30b_a3b layer step"
+    assert line["gpu_launches"] == 22 * 200
+    assert line["e2e"]["h2d_bytes_per_step"] == 2 * nbytes  # x and dy in
+    assert line["e2e"]["d2h_bytes_per_step"] == 2 * nbytes  # y and dx out
+    assert line["e2e"]["value"] == pytest.approx(CFG.T / 1.36e-3)
+    dx = next(k for k in line["kernels"] if k["name"] == "tc_dx")
+    assert dx["gbs"] == pytest.approx(units["tc_dx"][1] / (48.7 / 200 / 1e3) / 1e9)
+    assert "gbs" not in next(k for k in line["kernels"] if k["name"] == "route_topk")
+    skipped = bench.make_line(args, CFG, 1, 1.31, 3.1e6, 0.464, fl, by, roof, trace, 92.2, None,
+                              None, nbytes, 22, clk, units, 6779.0, 1918.6)
+    assert skipped["e2e"] is None
