@@ -99,3 +99,26 @@ def test_sharded_gradients_sum_to_whole_batch():
         np.testing.assert_allclose(g_r, b["g_router"], rtol=1e-12, atol=1e-15)
         np.testing.assert_allclose(p, p1, rtol=1e-6, atol=1e-9)  # fp32 master values
     np.testing.assert_array_equal(res[0][2], res[1][2])  # identical replicas
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="the GPU arm would use NCCL; CPU check")
+def test_reference_arm_under_torchrun_prints_once():
+    """`bench.py --impl reference` launched as two ranks: rank 0 alone runs the oracle and prints
+    one JSON line; the other rank exits 0 without output."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+           os.path.join(root, "bench.py"), "--impl", "reference", "--gpus", "2", "--steps", "1",
+           "--warmup", "0", "--cpu-tokens", "8"]
+    r = subprocess.run(cmd, cwd=root, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "tokens/s" and d["value"] > 0
+    assert d["n_gpus"] == 2 and d["config"]["parallelism"].startswith("dp2")
+    assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}
