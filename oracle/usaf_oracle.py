@@ -316,13 +316,16 @@ def importance_select_threshold(g, K):
     return np.sort(np.concatenate([above, eq[:need]])).astype(np.int64)
 
 
-def rigl_swap(act_idx, p, m, v, g, D, dense_weight_at):
+def rigl_swap(act_idx, p, m, v, g, D, dense_weight_at, grow_by="sort"):
     """RigL drop/grow with a fixed count D:
 
     drop = the D entries of the active set S with the smallest |p| (ties: lower flat index first);
     grow = the D entries outside S with the largest |g| (ties: lower flat index first);
     S' = (S minus drop) union grow, sorted. Kept entries keep (p, m, v); grown entries get
     p = dense weight value (dense_weight_at(idx) -> float32 array), m = v = 0.
+    grow_by="threshold" finds the same grow set by its threshold form (for large N): with tau the
+    D-th largest key outside S, every outside entry with key > tau plus the lowest-index outside
+    entries with key == tau.
     Returns (new_idx, p', m', v', n_swapped)."""
     act_idx = np.asarray(act_idx, np.int64)
     K = act_idx.size
@@ -336,9 +339,16 @@ def rigl_swap(act_idx, p, m, v, g, D, dense_weight_at):
     N = gk.size
     inactive = np.ones(N, dtype=bool)
     inactive[act_idx] = False
-    cand = np.nonzero(inactive)[0]
-    grow_order = np.lexsort((cand, -gk[cand]))
-    grow = np.sort(cand[grow_order[:D]])
+    if grow_by == "sort":
+        cand = np.nonzero(inactive)[0]
+        grow_order = np.lexsort((cand, -gk[cand]))
+        grow = np.sort(cand[grow_order[:D]])
+    else:
+        outk = np.where(inactive, gk, -1)  # entries of S can never be grown
+        tau = np.partition(outk, N - D)[N - D] if D > 0 else np.iinfo(np.int64).max
+        above = np.nonzero(outk > tau)[0]
+        eq = np.nonzero(outk == tau)[0]
+        grow = np.sort(np.concatenate([above, eq[:D - above.size]])).astype(np.int64)
     kept = act_idx[keep_mask]
     new_idx = np.concatenate([kept, grow])
     p_new = np.concatenate([np.asarray(p, np.float32)[keep_mask],

@@ -123,6 +123,30 @@ def test_rigl_brute_force_and_invariants():
                 assert (p2[i], m2[i], v2[i]) == (wd[f], 0, 0)
 
 
+def test_rigl_threshold_form_equals_sort_form():
+    """The threshold form of the grow set (used for full-size layers) gives the sort form's result,
+    also when the threshold key is shared by entries inside and outside the active set and when
+    many outside entries tie at it; brute force on the small cases too."""
+    rng = np.random.default_rng(7)
+    for N, K, D in ((60, 20, 7), (500, 120, 0), (500, 120, 120), (2_000_000, 10_000, 3_000)):
+        act = np.sort(rng.choice(N, K, replace=False)).astype(np.int64)
+        g = (rng.integers(-40, 41, N) * 0.25).astype(np.float32)
+        if N > 1000:
+            g[::13] = 20.0          # a tied group larger than D: the threshold key
+            g[act[::2]] = 20.0      # the same key inside the set, never grown
+        p = (rng.integers(-3, 4, K) * 0.5).astype(np.float32)
+        m = rng.standard_normal(K).astype(np.float32)
+        v = np.abs(rng.standard_normal(K)).astype(np.float32)
+        wd = rng.standard_normal(N).astype(np.float32)
+        a = oracle.rigl_swap(act, p, m, v, g, D, lambda i: wd[i])
+        b = oracle.rigl_swap(act, p, m, v, g, D, lambda i: wd[i], grow_by="threshold")
+        for x, y in zip(a[:4], b[:4]):
+            assert np.array_equal(x, y)
+        assert a[4] == b[4] == D
+        if N < 1000:
+            assert a[0].tolist() == _brute_rigl(act, p, g, D)[0]
+
+
 def test_reselect_full_hand_case():
     # |g| ranks: idx 7 (9.0), 2 (-8.0), 5 and 9 tie at 5.0 (lower index first), then 0 (4.0)
     g = np.array([4.0, 0.5, -8.0, 1.0, 0.0, 5.0, -0.25, 9.0, 3.0, -5.0], np.float32)
