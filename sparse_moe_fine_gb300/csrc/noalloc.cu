@@ -29,7 +29,12 @@ size_t hist_bytes(const usaf_moe_shape& s) {
   return (size_t)round_up(ceil_div(s.T * s.k, PERM_CHUNK) * s.E * (int64_t)sizeof(int32_t), 256);
 }
 
-size_t split_bytes(const usaf_moe_shape& s) { return (size_t)(s.E * 3 * s.H * 2); }
+// The bf16 split of the router weight exists only on the tensor-core logits path, the same
+// condition route_launch takes it under.
+size_t split_bytes(const usaf_moe_shape& s, const float* logits_in, usaf_dtype x_dtype) {
+  const bool tc = !logits_in && x_dtype == USAF_BF16 && tc_shape_ok(s);
+  return tc ? (size_t)(s.E * 3 * s.H * 2) : 0;
+}
 
 // Device address of the scratch array on the current device, looked up once per device.
 usaf_status scratch_address(void** out) {
@@ -58,7 +63,7 @@ extern "C" usaf_status usaf_route_topk_noalloc(const usaf_moe_shape* s, const vo
                                                usaf_dtype x_dtype, const float* w_router,
                                                const float* logits_in, float* logits_out,
                                                int renorm, const usaf_routing* rt,
-                                               void* stream) {
+                                               uint32_t* dev_status, void* stream) {
   if (!s || usaf_routed_rows_capacity(s) < 0) return USAF_ERR_INVALID_ARG;
   if (!rt || !rt->topk_idx || !rt->topk_w || !rt->expert_count || !rt->expert_offset ||
       !rt->perm_tok || !rt->perm_slot || !rt->slot_row)
@@ -67,7 +72,7 @@ extern "C" usaf_status usaf_route_topk_noalloc(const usaf_moe_shape* s, const vo
   if (!logits_in && (!x || !w_router || (x_dtype != USAF_F32 && x_dtype != USAF_BF16)))
     return USAF_ERR_INVALID_ARG;
   if (renorm != 0 && renorm != 1) return USAF_ERR_INVALID_ARG;
-  if (hist_bytes(*s) + split_bytes(*s) > (size_t)USAF_NOALLOC_SCRATCH_BYTES)
+  if (hist_bytes(*s) + split_bytes(*s, logits_in, x_dtype) > (size_t)USAF_NOALLOC_SCRATCH_BYTES)
     return USAF_ERR_WORKSPACE;  // the layer needs more scratch than the fixed array holds
   void* base = nullptr;
   USAF_TRY(scratch_address(&base));
@@ -76,5 +81,5 @@ extern "C" usaf_status usaf_route_topk_noalloc(const usaf_moe_shape* s, const vo
   w.chunk_hist = static_cast<int32_t*>(base);
   w.wr3 = static_cast<char*>(base) + hist_bytes(*s);
   return route_launch(*s, x, x_dtype, w_router, logits_in, logits_out, renorm, *rt, w,
-                      static_cast<cudaStream_t>(stream));
+                      dev_status, static_cast<cudaStream_t>(stream));
 }

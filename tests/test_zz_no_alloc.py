@@ -74,5 +74,24 @@ def test_noalloc_fp32_layer_and_size_limit():
     big = B.shape(16, 4096, 1024, 2, 64)
     r = B._Routing(*[1] * 7)
     code = B.lib().usaf_route_topk_noalloc(ctypes.byref(big), 1, B.BF16, 1, None, 1, 1,
-                                           ctypes.byref(r), None)
+                                           ctypes.byref(r), None, None)
     assert code == 3
+    # the same layer routed from given logits, or with fp32 tokens, needs no split weights and
+    # fits: both calls run and agree with the workspace entry point
+    E, H, T = 1024, 4096, 16
+    bs = B.shape(T, H, E, 2, 64)
+    gen = torch.Generator().manual_seed(3)
+    xb = torch.randn(T, H, generator=gen).to(dev)
+    wrb = (0.02 * torch.randn(E, H, generator=gen)).to(dev)
+    got, want = B.Routing.empty(bs, dev), B.Routing.empty(bs, dev)
+    lg, lw = torch.empty(T, E, device=dev), torch.empty(T, E, device=dev)
+    B.route_topk_noalloc(bs, xb, wrb, got, logits_out=lg)
+    B.route_topk(bs, xb, wrb, want, logits_out=lw)
+    torch.cuda.synchronize()
+    assert torch.equal(lg, lw)
+    assert torch.equal(got.topk_idx, want.topk_idx)
+    got2 = B.Routing.empty(bs, dev)
+    B.route_topk_noalloc(bs, None, None, got2, logits_in=lw)
+    torch.cuda.synchronize()
+    assert torch.equal(got2.topk_idx, want.topk_idx)
+    assert torch.equal(got2.perm_slot, want.perm_slot)
