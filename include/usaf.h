@@ -20,8 +20,11 @@
  *  - Host-side argument checks run before anything is enqueued; a failed check returns
  *    USAF_ERR_INVALID_ARG (or USAF_ERR_UNSUPPORTED / USAF_ERR_WORKSPACE) and enqueues nothing.
  *    A failed kernel launch returns USAF_ERR_CUDA. Conditions that only the device can see
- *    (non-finite gradients, a selection that had to take the exact multi-pass path) are OR-ed
- *    as bits into the caller's `dev_status` word (device memory, may be NULL); no kernel traps.
+ *    (non-finite gradients, a selection that had to take the exact multi-pass path, a bounded
+ *    wait that gave up, an active-set index out of range) are OR-ed as bits into the caller's
+ *    `dev_status` word (device memory, may be NULL); no kernel traps.
+ *  - With the environment variable USAF_DEBUG=1 set when a call is made, every call that reads
+ *    an active set first runs usaf_validate_active on it (one extra kernel per call).
  *  - Flat expert-weight index f (int64): f < N_gu = E*2I*H addresses gate_up_proj row-major,
  *    N_gu <= f < N = E*3*I*H addresses down_proj row-major at f - N_gu. Active sets are sorted
  *    ascending and free of duplicates.
@@ -36,7 +39,7 @@
 extern "C" {
 #endif
 
-#define USAF_ABI_VERSION 1
+#define USAF_ABI_VERSION 2
 
 /* Each expert's rows in the permuted (expert-sorted) order start at a multiple of this. */
 #define USAF_ROW_ALIGN 16
@@ -47,7 +50,7 @@ typedef enum {
   USAF_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels handle (see each call) */
   USAF_ERR_WORKSPACE = 3,   /* workspace pointer NULL or smaller than the query says */
   USAF_ERR_CUDA = 4,        /* a CUDA runtime/driver call or a kernel launch failed */
-  USAF_ERR_TIMEOUT = 5      /* reserved: a bounded device wait gave up */
+  USAF_ERR_TIMEOUT = 5      /* not returned by any call: timeouts are device status bits */
 } usaf_status;
 
 typedef enum { USAF_F32 = 0, USAF_BF16 = 1 } usaf_dtype;
@@ -56,7 +59,13 @@ typedef enum { USAF_F32 = 0, USAF_BF16 = 1 } usaf_dtype;
 #define USAF_DEV_NONFINITE 1u       /* a gradient (or selection key) was NaN or Inf */
 #define USAF_DEV_SELECT_EXACT_PATH 2u /* informational: the sampled one-pass selection fell back
                                        * to the exact multi-pass radix select */
-#define USAF_DEV_TIMEOUT 4u         /* reserved for bounded device waits */
+#define USAF_DEV_TIMEOUT 4u         /* a tensor-core kernel's pipeline wait gave up after about
+                                     * two seconds; that kernel's outputs are incomplete (the
+                                     * router kernel then writes none of the affected logits) */
+#define USAF_DEV_BAD_INDEX 8u       /* an active-set index was out of range, out of order or
+                                     * repeated; kernels skip such entries, never address them */
+/* The bits after which usaf_sparse_adam_step with skip_if_nonfinite updates nothing. */
+#define USAF_DEV_SKIP_MASK (USAF_DEV_NONFINITE | USAF_DEV_TIMEOUT | USAF_DEV_BAD_INDEX)
 
 /* MoE layer dimensions: T tokens, H hidden size, E experts, k experts per token, I expert
  * intermediate size. */
@@ -99,13 +108,16 @@ int64_t usaf_routed_rows_capacity(const usaf_moe_shape* shape);
  *   logits_in  [T,E] fp32 or NULL: use these logits instead of computing them
  *   logits_out [T,E] fp32 or NULL: where computed logits are written
  *   rt         routing tables (all seven arrays required)
+ *   dev_status gets USAF_DEV_TIMEOUT if the tensor-core logits kernel gave up a wait (its logits
+ *              are then not written and the routing of the affected tokens is meaningless); may
+ *              be NULL
  * Limits: 1 <= k <= E <= 1024, k <= 32, T*k < 2^31. Errors: INVALID_ARG, WORKSPACE, CUDA.
  * ------------------------------------------------------------------------------------------- */
 size_t usaf_route_topk_workspace_size(const usaf_moe_shape* shape);
 usaf_status usaf_route_topk(const usaf_moe_shape* shape, const void* x, usaf_dtype x_dtype,
                             const float* w_router, const float* logits_in, float* logits_out,
-                            int renorm, const usaf_routing* rt, void* ws, size_t ws_bytes,
-                            void* stream);
+                            int renorm, const usaf_routing* rt, uint32_t* dev_status, void* ws,
+                            size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
  * usaf_route_topk_noalloc - usaf_route_topk for callers that cannot allocate device memory.
@@ -117,9 +129,10 @@ usaf_status usaf_route_topk(const usaf_moe_shape* shape, const void* x, usaf_dty
  * Same inputs, outputs and results as usaf_route_topk, except that logits_in or logits_out must
  * be given (the logits are never kept in scratch).
  * Scratch: a fixed device array of USAF_NOALLOC_SCRATCH_BYTES inside the library, which every
- * GPU that loads the library holds until the process exits. It needs
- * ceil(T*k/256)*E*4 bytes (rounded up to 256) + 6*E*H bytes; a layer needing more is refused
- * with USAF_ERR_WORKSPACE before anything is enqueued. The first call on each device looks up
+ * GPU that loads the library holds until the process exits. It needs ceil(T*k/256)*E*4 bytes
+ * (rounded up to 256), plus 6*E*H bytes for the bf16 split of the router weight when the
+ * tensor-core logits path runs (logits_in NULL, x bf16, H and I multiples of 64); a call needing
+ * more is refused with USAF_ERR_WORKSPACE before anything is enqueued. The first call on each device looks up
  * the array's device address (cudaGetSymbolAddress) with that device current; make that first
  * call before any stream capture. All calls share the one array and leave their scratch in it;
  * every byte a call reads from it was written earlier by the same call, so nothing needs
@@ -131,7 +144,7 @@ usaf_status usaf_route_topk(const usaf_moe_shape* shape, const void* x, usaf_dty
 usaf_status usaf_route_topk_noalloc(const usaf_moe_shape* shape, const void* x,
                                     usaf_dtype x_dtype, const float* w_router,
                                     const float* logits_in, float* logits_out, int renorm,
-                                    const usaf_routing* rt, void* stream);
+                                    const usaf_routing* rt, uint32_t* dev_status, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
  * usaf_moe_fwd - grouped SwiGLU expert forward over the permuted rows.
@@ -148,6 +161,7 @@ usaf_status usaf_route_topk_noalloc(const usaf_moe_shape* shape, const void* x,
  *                feature j (gate for j < I, up for j >= I) of permuted row `row`
  *   wa_save      [I,R_cap]  out: w * A per permuted row, feature-major (0 in padding rows)
  *   y            [T,H]      out
+ *   dev_status   gets USAF_DEV_TIMEOUT if a tensor-core kernel gave up a wait (may be NULL)
  * Errors: INVALID_ARG, UNSUPPORTED (bf16 shape limits; also any dtype with
  * max(2I,H) * R_cap >= 2^31 * (16 / element size), the range of the 32-bit vector indices into the
  * feature-major rows), WORKSPACE, CUDA.
@@ -155,8 +169,8 @@ usaf_status usaf_route_topk_noalloc(const usaf_moe_shape* shape, const void* x,
 size_t usaf_moe_fwd_workspace_size(const usaf_moe_shape* shape, usaf_dtype dtype);
 usaf_status usaf_moe_fwd(const usaf_moe_shape* shape, usaf_dtype dtype, const void* x,
                          const void* w_gate_up, const void* w_down, const usaf_routing* rt,
-                         void* x_perm_save, void* h_save, void* wa_save, void* y, void* ws,
-                         size_t ws_bytes, void* stream);
+                         void* x_perm_save, void* h_save, void* wa_save, void* y,
+                         uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
 
 /* usaf_moe_fwd_wait - usaf_moe_fwd whose reads of the expert weights wait for a CUDA event.
  * weights_ready is a cudaEvent_t (NULL: no wait, the same as usaf_moe_fwd), typically recorded
@@ -167,7 +181,8 @@ usaf_status usaf_moe_fwd(const usaf_moe_shape* shape, usaf_dtype dtype, const vo
 usaf_status usaf_moe_fwd_wait(const usaf_moe_shape* shape, usaf_dtype dtype, const void* x,
                               const void* w_gate_up, const void* w_down, const usaf_routing* rt,
                               void* x_perm_save, void* h_save, void* wa_save, void* y,
-                              void* weights_ready, void* ws, size_t ws_bytes, void* stream);
+                              void* weights_ready, uint32_t* dev_status, void* ws,
+                              size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
  * usaf_moe_bwd_sparse - sparse backward of the layer for upstream gradient dy = dL/dY.
@@ -187,7 +202,9 @@ usaf_status usaf_moe_fwd_wait(const usaf_moe_shape* shape, usaf_dtype dtype, con
  *   g_act        [K] fp32 out;  g_router [E,H] fp32 out
  *   dx           [T,H] of dtype out, or NULL to skip the input gradient
  *   dw_slot      [T*k] fp32 out (dL/dw per slot), or NULL
- *   dev_status   gets USAF_DEV_NONFINITE if any produced gradient is NaN/Inf (may be NULL)
+ *   dev_status   gets USAF_DEV_NONFINITE if any produced gradient is NaN/Inf, USAF_DEV_TIMEOUT if
+ *                a tensor-core kernel gave up a wait, USAF_DEV_BAD_INDEX if an active index does
+ *                not address an expert weight (that entry's g_act is left 0) (may be NULL)
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
  * ------------------------------------------------------------------------------------------- */
 size_t usaf_moe_bwd_workspace_size(const usaf_moe_shape* shape, usaf_dtype dtype, int64_t K);
@@ -198,6 +215,12 @@ usaf_status usaf_moe_bwd_sparse(const usaf_moe_shape* shape, usaf_dtype dtype, i
                                 const void* dy, const int64_t* act_idx, int64_t K, float* g_act,
                                 float* g_router, void* dx, float* dw_slot, uint32_t* dev_status,
                                 void* ws, size_t ws_bytes, void* stream);
+
+/* Byte offset inside the backward workspace of dlogit at the selected experts: after a
+ * usaf_moe_bwd_sparse* call with renorm = 1, ws + offset holds [T*k] fp32 values in slot order
+ * (slot t*k + j: dL/dlogit[t, topk_idx[t*k + j]]; every other expert's dlogit is 0). A read-only
+ * view for checking the router backward; -1 for an invalid shape. Host only. */
+int64_t usaf_moe_bwd_dlogit_offset(const usaf_moe_shape* shape, usaf_dtype dtype, int64_t K);
 
 /* ---------------------------------------------------------------------------------------------
  * usaf_moe_bwd_sparse_accumulate - usaf_moe_bwd_sparse for one micro-batch of a step that
@@ -250,8 +273,11 @@ usaf_status usaf_moe_bwd_dense(const usaf_moe_shape* shape, usaf_dtype dtype, in
  *                in double on the host and passed to the kernel as fp32
  *   step         1-based step count
  *   skip_if_nonfinite  if nonzero, the entry point first scans g, and no entry is updated when
- *                this scan or an earlier call (a bit already set in *dev_status, e.g. by
- *                usaf_moe_bwd_sparse) found a non-finite gradient (the README's NaN step skip)
+ *                this scan or an earlier call found a non-finite gradient, or an earlier call
+ *                timed out or saw a bad active index (any bit of USAF_DEV_SKIP_MASK already set
+ *                in *dev_status, e.g. by usaf_moe_bwd_sparse) (the README's NaN step skip)
+ *   dev_status   with USAF_DEV_BAD_INDEX already set, no entry is updated whatever
+ *                skip_if_nonfinite says (the indices would address memory outside the weights)
  * Errors: INVALID_ARG, CUDA.
  * ------------------------------------------------------------------------------------------- */
 usaf_status usaf_sparse_adam_step(int64_t n, const int64_t* idx, const float* g, float* p,
@@ -314,6 +340,29 @@ usaf_status usaf_reselect_full(const float* g, int64_t N, int64_t K, const int64
                                const void* w_seg1, usaf_dtype w_dtype, int64_t* new_idx,
                                float* p_out, float* m_out, float* v_out, int64_t* n_kept,
                                uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * usaf_validate_active - checks an active set against the contract every call above assumes
+ * (USAF README, "Not all weights matter": the trained subset is a set of expert weights, here a
+ * sorted list of flat indices): 0 <= idx[i] < N, and idx[i-1] < idx[i] (ascending, no repeats).
+ * One kernel reads idx[0..K) and nothing else; any violation sets USAF_DEV_BAD_INDEX in
+ * *dev_status (required). The host learns of it by reading the word after the stream has run it.
+ * Limits: 0 <= K, 1 <= N. Errors: INVALID_ARG, CUDA.
+ * ------------------------------------------------------------------------------------------- */
+usaf_status usaf_validate_active(const int64_t* idx, int64_t K, int64_t N, uint32_t* dev_status,
+                                 void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * usaf_diag_bounded_wait - exercises the failure path of the tensor-core kernels' bounded waits
+ * without any GPU fault. The pages have no counterpart; it exists so a test can show that a wait
+ * that runs out is reported and leaves the context usable. One CTA allocates tensor memory,
+ * initialises an mbarrier that nothing ever arrives on, and waits on it with the same bounded
+ * wait the GEMM kernels use, limited to limit_cycles SM clock cycles; when the wait gives up it
+ * sets USAF_DEV_TIMEOUT in *dev_status (required), drains its (empty) MMA pipeline with the same
+ * deadline-bounded drain, frees the tensor memory and returns.
+ * Limits: 1 <= limit_cycles <= 2^32 (about two seconds). Errors: INVALID_ARG, CUDA.
+ * ------------------------------------------------------------------------------------------- */
+usaf_status usaf_diag_bounded_wait(int64_t limit_cycles, uint32_t* dev_status, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
  * Kernel timing trace (host side, off by default). While enabled, every kernel launch of the hot

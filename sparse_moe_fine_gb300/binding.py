@@ -22,7 +22,8 @@ F32, BF16 = 0, 1
 ROW_ALIGN = 16
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace", 4: "CUDA error",
           5: "timeout"}
-DEV_NONFINITE, DEV_SELECT_EXACT_PATH, DEV_TIMEOUT = 1, 2, 4
+DEV_NONFINITE, DEV_SELECT_EXACT_PATH, DEV_TIMEOUT, DEV_BAD_INDEX = 1, 2, 4, 8
+DEV_SKIP_MASK = DEV_NONFINITE | DEV_TIMEOUT | DEV_BAD_INDEX
 
 
 class UsafError(RuntimeError):
@@ -59,11 +60,12 @@ _SIGS = {
     "usaf_status_string": (ctypes.c_char_p, [_INT]),
     "usaf_routed_rows_capacity": (_I64, [_P]),
     "usaf_route_topk_workspace_size": (_SZ, [_P]),
-    "usaf_route_topk": (_INT, [_P, _P, _INT, _P, _P, _P, _INT, _P, _P, _SZ, _P]),
-    "usaf_route_topk_noalloc": (_INT, [_P, _P, _INT, _P, _P, _P, _INT, _P, _P]),
+    "usaf_route_topk": (_INT, [_P, _P, _INT, _P, _P, _P, _INT, _P, _P, _P, _SZ, _P]),
+    "usaf_route_topk_noalloc": (_INT, [_P, _P, _INT, _P, _P, _P, _INT, _P, _P, _P]),
     "usaf_moe_fwd_workspace_size": (_SZ, [_P, _INT]),
-    "usaf_moe_fwd": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
-    "usaf_moe_fwd_wait": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "usaf_moe_fwd": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "usaf_moe_fwd_wait": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                                 _P]),
     "usaf_moe_bwd_workspace_size": (_SZ, [_P, _INT, _I64]),
     "usaf_moe_bwd_sparse": (_INT, [_P, _INT, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                    _I64, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -82,6 +84,9 @@ _SIGS = {
                                               _P]),
     "usaf_moe_bwd_dense": (_INT, [_P, _INT, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                   _INT, _P, _P, _P, _P, _P, _SZ, _P]),
+    "usaf_validate_active": (_INT, [_P, _I64, _I64, _P, _P]),
+    "usaf_moe_bwd_dlogit_offset": (_I64, [_P, _INT, _I64]),
+    "usaf_diag_bounded_wait": (_INT, [_I64, _P, _P]),
     "usaf_reselect_full_workspace_size": (_SZ, [_I64, _I64]),
     "usaf_reselect_full": (_INT, [_P, _I64, _I64, _P, _I64, _P, _P, _P, _P, _I64, _P, _INT, _P,
                                   _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -182,7 +187,7 @@ def route_topk_workspace_size(s: Shape) -> int:
 
 
 def route_topk(s: Shape, x, w_router, rt: Routing, logits_in=None, logits_out=None, renorm=1,
-               ws=None, stream=None):
+               dev_status=None, ws=None, stream=None):
     dev = rt.topk_idx.device
     if ws is None:
         ws = _ws(route_topk_workspace_size(s), dev)
@@ -190,17 +195,17 @@ def route_topk(s: Shape, x, w_router, rt: Routing, logits_in=None, logits_out=No
     r = rt.c()
     _check("usaf_route_topk", lib().usaf_route_topk(
         ctypes.byref(s), _ptr(x), xdt, _ptr(w_router), _ptr(logits_in), _ptr(logits_out),
-        int(renorm), ctypes.byref(r), _ptr(ws), ws.numel(), _stream(stream)))
+        int(renorm), ctypes.byref(r), _ptr(dev_status), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def route_topk_noalloc(s: Shape, x, w_router, rt: Routing, logits_in=None, logits_out=None,
-                       renorm=1, stream=None):
+                       renorm=1, dev_status=None, stream=None):
     """usaf_route_topk_noalloc: no workspace argument; scratch is the library's fixed array."""
     xdt = _dt(x) if x is not None else F32
     r = rt.c()
     _check("usaf_route_topk_noalloc", lib().usaf_route_topk_noalloc(
         ctypes.byref(s), _ptr(x), xdt, _ptr(w_router), _ptr(logits_in), _ptr(logits_out),
-        int(renorm), ctypes.byref(r), _stream(stream)))
+        int(renorm), ctypes.byref(r), _ptr(dev_status), _stream(stream)))
 
 
 def moe_fwd_workspace_size(s: Shape, dt: int) -> int:
@@ -208,7 +213,7 @@ def moe_fwd_workspace_size(s: Shape, dt: int) -> int:
 
 
 def moe_fwd(s: Shape, x, w_gate_up, w_down, rt: Routing, x_perm, h, wa, y, ws=None, stream=None,
-            weights_ready=None):
+            weights_ready=None, dev_status=None):
     """weights_ready: a recorded torch.cuda.Event that the reads of the expert weights wait for
     (the token gather before them does not)."""
     dt = _dt(x)
@@ -218,11 +223,17 @@ def moe_fwd(s: Shape, x, w_gate_up, w_down, rt: Routing, x_perm, h, wa, y, ws=No
     ev = None if weights_ready is None else ctypes.c_void_p(weights_ready.cuda_event)
     _check("usaf_moe_fwd_wait", lib().usaf_moe_fwd_wait(
         ctypes.byref(s), dt, _ptr(x), _ptr(w_gate_up), _ptr(w_down), ctypes.byref(r),
-        _ptr(x_perm), _ptr(h), _ptr(wa), _ptr(y), ev, _ptr(ws), ws.numel(), _stream(stream)))
+        _ptr(x_perm), _ptr(h), _ptr(wa), _ptr(y), ev, _ptr(dev_status), _ptr(ws), ws.numel(),
+        _stream(stream)))
 
 
 def moe_bwd_workspace_size(s: Shape, dt: int, K: int) -> int:
     return int(lib().usaf_moe_bwd_workspace_size(ctypes.byref(s), dt, int(K)))
+
+
+def moe_bwd_dlogit_offset(s: Shape, dt: int, K: int) -> int:
+    """Byte offset in the backward workspace of dlogit at the selected experts ([T*k] fp32)."""
+    return int(lib().usaf_moe_bwd_dlogit_offset(ctypes.byref(s), dt, int(K)))
 
 
 def moe_bwd_sparse(s: Shape, x, w_router, w_gate_up, w_down, rt: Routing, x_perm, h, wa, dy,
@@ -321,6 +332,20 @@ def reselect_full(g, K, old_idx, p_in, m_in, v_in, w_seg0, n_seg0, w_seg1, new_i
         _ptr(w_seg0), int(n_seg0), _ptr(w_seg1), _dt(w_seg0), _ptr(new_idx), _ptr(p_out),
         _ptr(m_out), _ptr(v_out), _ptr(n_kept), _ptr(dev_status), _ptr(ws), ws.numel(),
         _stream(stream)))
+
+
+def validate_active(idx, N, dev_status, stream=None):
+    """usaf_validate_active: sets DEV_BAD_INDEX in dev_status unless idx is strictly ascending in
+    [0, N)."""
+    K = 0 if idx is None else idx.numel()
+    _check("usaf_validate_active", lib().usaf_validate_active(
+        _ptr(idx), K, int(N), _ptr(dev_status), _stream(stream)))
+
+
+def diag_bounded_wait(limit_cycles, dev_status, stream=None):
+    """usaf_diag_bounded_wait: one CTA whose bounded mbarrier wait runs out after limit_cycles."""
+    _check("usaf_diag_bounded_wait", lib().usaf_diag_bounded_wait(
+        int(limit_cycles), _ptr(dev_status), _stream(stream)))
 
 
 def trace_enable(on: bool) -> None:

@@ -2,6 +2,7 @@
 // and the launch sequence of each call. Everything here is host code; the arithmetic is in the
 // kernel files.
 #include <atomic>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -96,6 +97,17 @@ static bool routing_ok(const usaf_routing* r) {
 
 static bool dtype_ok(usaf_dtype d) { return d == USAF_F32 || d == USAF_BF16; }
 
+// USAF_DEBUG=1 in the environment: calls that read an active set validate it first.
+static bool debug_on() {
+  const char* v = std::getenv("USAF_DEBUG");
+  return v && v[0] == '1';
+}
+static usaf_status debug_validate(const int64_t* idx, int64_t K, int64_t N, uint32_t* dev_status,
+                                  void* stream) {
+  if (!debug_on() || !idx || K <= 0 || !dev_status) return USAF_OK;
+  return validate_launch(idx, K, N, dev_status, static_cast<cudaStream_t>(stream));
+}
+
 }  // namespace usaf
 
 using namespace usaf;
@@ -169,8 +181,8 @@ size_t usaf_route_topk_workspace_size(const usaf_moe_shape* s) {
 
 usaf_status usaf_route_topk(const usaf_moe_shape* s, const void* x, usaf_dtype x_dtype,
                             const float* w_router, const float* logits_in, float* logits_out,
-                            int renorm, const usaf_routing* rt, void* ws, size_t ws_bytes,
-                            void* stream) {
+                            int renorm, const usaf_routing* rt, uint32_t* dev_status, void* ws,
+                            size_t ws_bytes, void* stream) {
   if (!shape_ok(s) || !routing_ok(rt)) return USAF_ERR_INVALID_ARG;
   if (!logits_in && (!x || !w_router || !dtype_ok(x_dtype))) return USAF_ERR_INVALID_ARG;
   if (renorm != 0 && renorm != 1) return USAF_ERR_INVALID_ARG;
@@ -180,7 +192,7 @@ usaf_status usaf_route_topk(const usaf_moe_shape* s, const void* x, usaf_dtype x
   RouteWs w;
   route_ws_layout(*s, c, w);
   return route_launch(*s, x, x_dtype, w_router, logits_in, logits_out, renorm, *rt, w,
-                      static_cast<cudaStream_t>(stream));
+                      dev_status, static_cast<cudaStream_t>(stream));
 }
 
 size_t usaf_moe_fwd_workspace_size(const usaf_moe_shape* s, usaf_dtype dt) {
@@ -215,9 +227,11 @@ static usaf_status fill_args(MoeArgs& a, const usaf_moe_shape* s, usaf_dtype dt,
 usaf_status usaf_moe_fwd_wait(const usaf_moe_shape* s, usaf_dtype dt, const void* x,
                               const void* w_gate_up, const void* w_down, const usaf_routing* rt,
                               void* x_perm_save, void* h_save, void* wa_save, void* y,
-                              void* weights_ready, void* ws, size_t ws_bytes, void* stream) {
+                              void* weights_ready, uint32_t* dev_status, void* ws,
+                              size_t ws_bytes, void* stream) {
   MoeArgs a{};
   USAF_TRY(fill_args(a, s, dt, x, nullptr, w_gate_up, w_down, rt));
+  a.status = dev_status;
   if (!x_perm_save || !h_save || !wa_save || !y) return USAF_ERR_INVALID_ARG;
   if (!ws || ws_bytes < usaf_moe_fwd_workspace_size(s, dt)) return USAF_ERR_WORKSPACE;
   Carver c(ws);
@@ -230,10 +244,10 @@ usaf_status usaf_moe_fwd_wait(const usaf_moe_shape* s, usaf_dtype dt, const void
 
 usaf_status usaf_moe_fwd(const usaf_moe_shape* s, usaf_dtype dt, const void* x,
                          const void* w_gate_up, const void* w_down, const usaf_routing* rt,
-                         void* x_perm_save, void* h_save, void* wa_save, void* y, void* ws,
-                         size_t ws_bytes, void* stream) {
+                         void* x_perm_save, void* h_save, void* wa_save, void* y,
+                         uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
   return usaf_moe_fwd_wait(s, dt, x, w_gate_up, w_down, rt, x_perm_save, h_save, wa_save, y,
-                           nullptr, ws, ws_bytes, stream);
+                           nullptr, dev_status, ws, ws_bytes, stream);
 }
 
 size_t usaf_moe_bwd_workspace_size(const usaf_moe_shape* s, usaf_dtype dt, int64_t K) {
@@ -242,6 +256,14 @@ size_t usaf_moe_bwd_workspace_size(const usaf_moe_shape* s, usaf_dtype dt, int64
   BwdWs w;
   bwd_ws_layout(*s, dt, K, c, w);
   return c.size();
+}
+
+int64_t usaf_moe_bwd_dlogit_offset(const usaf_moe_shape* s, usaf_dtype dt, int64_t K) {
+  if (!shape_ok(s) || !dtype_ok(dt) || K < 0) return -1;
+  Carver c(reinterpret_cast<void*>(uintptr_t(256)));  // a nonzero base: offsets, not sizes
+  BwdWs w;
+  bwd_ws_layout(*s, dt, K, c, w);
+  return (int64_t)(reinterpret_cast<char*>(w.dl) - reinterpret_cast<char*>(uintptr_t(256)));
 }
 
 usaf_status usaf_moe_bwd_sparse(const usaf_moe_shape* s, usaf_dtype dt, int renorm,
@@ -253,6 +275,7 @@ usaf_status usaf_moe_bwd_sparse(const usaf_moe_shape* s, usaf_dtype dt, int reno
                                 void* ws, size_t ws_bytes, void* stream) {
   MoeArgs a{};
   USAF_TRY(fill_args(a, s, dt, x, w_router, w_gate_up, w_down, rt));
+  a.status = dev_status;
   if (renorm != 0 && renorm != 1) return USAF_ERR_INVALID_ARG;
   if (!w_router || !x_perm_save || !h_save || !wa_save || !dy || !g_router)
     return USAF_ERR_INVALID_ARG;
@@ -260,6 +283,7 @@ usaf_status usaf_moe_bwd_sparse(const usaf_moe_shape* s, usaf_dtype dt, int reno
   const int64_t N = s->E * 3 * s->I * s->H;
   if (K < 0 || K > N || (K > 0 && (!act_idx || !g_act))) return USAF_ERR_INVALID_ARG;
   if (!ws || ws_bytes < usaf_moe_bwd_workspace_size(s, dt, K)) return USAF_ERR_WORKSPACE;
+  USAF_TRY(debug_validate(act_idx, K, N, dev_status, stream));
   Carver c(ws);
   BwdWs w;
   bwd_ws_layout(*s, dt, K, c, w);
@@ -276,6 +300,7 @@ usaf_status usaf_moe_bwd_sparse_accumulate(
     uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
   MoeArgs a{};
   USAF_TRY(fill_args(a, s, dt, x, w_router, w_gate_up, w_down, rt));
+  a.status = dev_status;
   if (renorm != 0 && renorm != 1) return USAF_ERR_INVALID_ARG;
   if (!w_router || !x_perm_save || !h_save || !wa_save || !dy || !g_router)
     return USAF_ERR_INVALID_ARG;
@@ -283,6 +308,7 @@ usaf_status usaf_moe_bwd_sparse_accumulate(
   const int64_t N = s->E * 3 * s->I * s->H;
   if (K < 0 || K > N || (K > 0 && (!act_idx || !g_act))) return USAF_ERR_INVALID_ARG;
   if (!ws || ws_bytes < usaf_moe_bwd_workspace_size(s, dt, K)) return USAF_ERR_WORKSPACE;
+  USAF_TRY(debug_validate(act_idx, K, N, dev_status, stream));
   Carver c(ws);
   BwdWs w;
   bwd_ws_layout(*s, dt, K, c, w);
@@ -300,6 +326,7 @@ usaf_status usaf_moe_bwd_dense(const usaf_moe_shape* s, usaf_dtype dt, int renor
                                size_t ws_bytes, void* stream) {
   MoeArgs a{};
   USAF_TRY(fill_args(a, s, dt, x, w_router, w_gate_up, w_down, rt));
+  a.status = dev_status;
   if (renorm != 0 && renorm != 1) return USAF_ERR_INVALID_ARG;
   if (accumulate != 0 && accumulate != 1) return USAF_ERR_INVALID_ARG;
   if (!w_router || !x_perm_save || !h_save || !wa_save || !dy || !g_router || !g_dense)
@@ -326,6 +353,8 @@ usaf_status usaf_sparse_adam_step(int64_t n, const int64_t* idx, const float* g,
   if (skip_if_nonfinite && !dev_status) return USAF_ERR_INVALID_ARG;
   if (!(beta1 >= 0.0 && beta1 < 1.0 && beta2 >= 0.0 && beta2 < 1.0 && eps >= 0.0))
     return USAF_ERR_INVALID_ARG;
+  // the set's bound is not known here: only order and sign are checked (N = INT64_MAX)
+  USAF_TRY(debug_validate(idx, n, INT64_MAX, dev_status, stream));
   return adam_launch(n, idx, g, p, m, v, w_seg0, n_seg0, w_seg1, w_dtype, lr, beta1, beta2, eps,
                      step, skip_if_nonfinite, dev_status, static_cast<cudaStream_t>(stream));
 }
@@ -380,6 +409,7 @@ usaf_status usaf_rigl_swap(const float* g, int64_t N, const int64_t* act_idx, in
     for (int j = 0; j < 4; ++j)
       if (overlaps(ins[i], insz[i], outs[j], outsz[j])) return USAF_ERR_INVALID_ARG;
   if (!ws || ws_bytes < usaf_rigl_swap_workspace_size(N, K, D)) return USAF_ERR_WORKSPACE;
+  USAF_TRY(debug_validate(act_idx, K, N, dev_status, stream));
   return rigl_launch(g, N, act_idx, K, D, p_in, m_in, v_in, w_seg0, n_seg0, w_seg1, w_dtype,
                      new_idx, p_out, m_out, v_out, n_swapped, dev_status, ws,
                      static_cast<cudaStream_t>(stream));
@@ -412,9 +442,22 @@ usaf_status usaf_reselect_full(const float* g, int64_t N, int64_t K, const int64
     for (int j = 0; j < 4; ++j)
       if (overlaps(ins[i], insz[i], outs[j], outsz[j])) return USAF_ERR_INVALID_ARG;
   if (!ws || ws_bytes < usaf_reselect_full_workspace_size(N, K)) return USAF_ERR_WORKSPACE;
+  USAF_TRY(debug_validate(old_idx, K_old, N, dev_status, stream));
   return reselect_launch(g, N, K, old_idx, K_old, p_in, m_in, v_in, w_seg0, n_seg0, w_seg1,
                          w_dtype, new_idx, p_out, m_out, v_out, n_kept, dev_status, ws,
                          static_cast<cudaStream_t>(stream));
+}
+
+usaf_status usaf_validate_active(const int64_t* idx, int64_t K, int64_t N, uint32_t* dev_status,
+                                 void* stream) {
+  if (K < 0 || N < 1 || !dev_status || (K > 0 && !idx)) return USAF_ERR_INVALID_ARG;
+  return validate_launch(idx, K, N, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+usaf_status usaf_diag_bounded_wait(int64_t limit_cycles, uint32_t* dev_status, void* stream) {
+  if (limit_cycles < 1 || limit_cycles > (int64_t(1) << 32) || !dev_status)
+    return USAF_ERR_INVALID_ARG;
+  return diag_wait_launch(limit_cycles, dev_status, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

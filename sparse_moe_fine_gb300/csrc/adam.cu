@@ -43,7 +43,10 @@ __global__ void __launch_bounds__(256) adam_kernel(int64_t n, const int64_t* __r
                                                    float b2, float om_b1, float om_b2, float eps,
                                                    float step_size, int skip, int vec,
                                                    const uint32_t* dev_status) {
-  if (skip && dev_status && (*(volatile const uint32_t*)dev_status & USAF_DEV_NONFINITE)) return;
+  if (dev_status) {
+    const uint32_t st = *(volatile const uint32_t*)dev_status;
+    if ((st & USAF_DEV_BAD_INDEX) || (skip && (st & USAF_DEV_SKIP_MASK))) return;
+  }
   const int64_t n4 = vec ? n / 4 : 0;
   for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n4;
        q += (int64_t)gridDim.x * blockDim.x) {
@@ -68,6 +71,27 @@ __global__ void __launch_bounds__(256) adam_kernel(int64_t n, const int64_t* __r
     m[i] = mi;
     v[i] = vi;
   }
+}
+
+// Active-set contract: 0 <= idx[i] < N and idx[i - 1] < idx[i]. Reads idx only.
+__global__ void validate_active_kernel(const int64_t* __restrict__ idx, int64_t K, int64_t N,
+                                       uint32_t* dev_status) {
+  bool bad = false;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < K;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t f = idx[i];
+    bad |= f < 0 || f >= N || (i > 0 && idx[i - 1] >= f);
+  }
+  flag_status_warp(dev_status, bad, USAF_DEV_BAD_INDEX);
+}
+
+usaf_status validate_launch(const int64_t* idx, int64_t K, int64_t N, uint32_t* dev_status,
+                            cudaStream_t st) {
+  if (K == 0) return USAF_OK;
+  USAF_TRACE("validate_active", st);
+  validate_active_kernel<<<grid_dim_for(K), 256, 0, st>>>(idx, K, N, dev_status);
+  USAF_CHECK_LAUNCH();
+  return USAF_OK;
 }
 
 usaf_status adam_launch(int64_t n, const int64_t* idx, const float* g, float* p, float* m,

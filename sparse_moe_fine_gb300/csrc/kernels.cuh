@@ -16,7 +16,8 @@ struct RouteWs {
 void route_ws_layout(const usaf_moe_shape& s, Carver& c, RouteWs& w);
 usaf_status route_launch(const usaf_moe_shape& s, const void* x, usaf_dtype xdt, const float* wr,
                          const float* logits_in, float* logits_out, int renorm,
-                         const usaf_routing& rt, RouteWs& w, cudaStream_t st);
+                         const usaf_routing& rt, RouteWs& w, uint32_t* dev_status,
+                         cudaStream_t st);
 
 // ---------------------------------------------------------------- expert forward / backward
 struct FwdWs {
@@ -54,6 +55,7 @@ struct MoeArgs {
   usaf_routing rt;
   int32_t* plan;  // token-tile prefix written by tc_plan (tensor-core path)
   float* wperm;   // [R_cap] routing weight of each permuted row (0 in padding), by the gather
+  uint32_t* status;  // device status word of the call (may be null): bounded waits that give up
 };
 
 // weights_ready (may be null): the kernels that read the expert weights wait for it; the token
@@ -69,7 +71,7 @@ usaf_status moe_bwd_launch(const MoeArgs& a, int renorm, const float* logits, co
 // tensor-core (tcgen05) grouped GEMM stages, bf16 only
 bool tc_shape_ok(const usaf_moe_shape& s);
 usaf_status tc_router_logits(const usaf_moe_shape& s, const void* x, const float* wr, void* wr3,
-                             float* logits, cudaStream_t st);
+                             float* logits, uint32_t* status, cudaStream_t st);
 usaf_status tc_fwd_gate_up(const MoeArgs& a, const void* xT, void* hT, void* waT,
                            cudaStream_t st);
 usaf_status tc_fwd_down(const MoeArgs& a, const void* wa, float* y_acc, cudaStream_t st);
@@ -79,6 +81,8 @@ usaf_status tc_bwd_dx(const MoeArgs& a, const void* dh, float* dx_acc, cudaStrea
 // dense expert weight gradient g[e] (a_rows x b_rows, fp32) = aT . bT^T over each expert's tokens
 usaf_status tc_wgrad_dense(const MoeArgs& a, const void* aT, int64_t a_rows, const void* bT,
                            int64_t b_rows, float* g, int accumulate, cudaStream_t st);
+// one CTA whose bounded wait runs out on purpose (see usaf_diag_bounded_wait)
+usaf_status diag_wait_launch(int64_t limit_cycles, uint32_t* status, cudaStream_t st);
 
 
 // ---------------------------------------------------------------- optimizer
@@ -86,6 +90,9 @@ usaf_status adam_launch(int64_t n, const int64_t* idx, const float* g, float* p,
                         float* v, void* w0, int64_t n0, void* w1, usaf_dtype wdt, double lr,
                         double b1, double b2, double eps, int64_t step, int skip,
                         uint32_t* dev_status, cudaStream_t st);
+// USAF_DEV_BAD_INDEX when idx[0..K) is not strictly ascending inside [0, N)
+usaf_status validate_launch(const int64_t* idx, int64_t K, int64_t N, uint32_t* dev_status,
+                            cudaStream_t st);
 
 // ---------------------------------------------------------------- selection / RigL
 size_t select_ws_bytes(int64_t N, int64_t K, bool with_bitmap);

@@ -445,7 +445,7 @@ constexpr int SD_G = 16;  // entries per group
 template <typename T>
 __global__ void __launch_bounds__(SD_WARPS * 32, SD_BLOCKS_PER_SM) sddmm_kernel(
     const int64_t* __restrict__ act, int64_t K, const int32_t* __restrict__ cnt,
-    const int32_t* __restrict__ off, int H, int I, int64_t Ngu, int64_t rcap,
+    const int32_t* __restrict__ off, int E, int H, int I, int64_t Ngu, int64_t rcap,
     const T* __restrict__ dhT, const T* __restrict__ xT, const T* __restrict__ dyT,
     const T* __restrict__ waT, float* __restrict__ g_act, int accumulate, uint32_t* dev_status) {
   constexpr int VW = 16 / sizeof(T);
@@ -456,7 +456,7 @@ __global__ void __launch_bounds__(SD_WARPS * 32, SD_BLOCKS_PER_SM) sddmm_kernel(
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, il = lane % SD_G;
   const int64_t kgu = count_below(act, K, Ngu, lane);
   const int64_t nb_gu = (kgu + 31) / 32, nb = nb_gu + (K - kgu + 31) / 32;
-  bool bad = false;
+  bool bad = false, badidx = false;
   for (int64_t bt = (int64_t)blockIdx.x * SD_WARPS + wid; bt < nb;
        bt += (int64_t)gridDim.x * SD_WARPS) {
     const bool gu = bt < nb_gu;
@@ -467,8 +467,12 @@ __global__ void __launch_bounds__(SD_WARPS * 32, SD_BLOCKS_PER_SM) sddmm_kernel(
     {
       const int64_t q = b0 + lane;
       int4 md = make_int4(0, 0, 0, 0);
-      if (q < lim) {
-        const int64_t f = gu ? act[q] : act[q] - Ngu;
+      const int64_t f = q < lim ? (gu ? act[q] : act[q] - Ngu) : 0;
+      // an index outside its tensor (out of range, or an unsorted set split at the wrong place)
+      // is flagged and gets a zero gradient; it is never decoded into addresses
+      const bool inr = f >= 0 && f < (gu ? Ngu : (int64_t)E * H * I);
+      badidx |= q < lim && !inr;
+      if (q < lim && inr) {
         const int64_t wcols = gu ? H : I, wrows = gu ? 2 * I : H;
         int64_t col, arow;
         int e;
@@ -577,6 +581,7 @@ __global__ void __launch_bounds__(SD_WARPS * 32, SD_BLOCKS_PER_SM) sddmm_kernel(
     __syncwarp();  // the next batch rewrites meta
   }
   flag_status_warp(dev_status, bad, USAF_DEV_NONFINITE);
+  flag_status_warp(dev_status, badidx, USAF_DEV_BAD_INDEX);
 }
 
 // g_router[e, h] = sum over the rows routed to e of dl[row] * x^T[h, row] (renormalised routing):
@@ -965,7 +970,7 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
     USAF_TRACE("wgrad_sddmm", st);
     const unsigned blocks = (unsigned)std::min<int64_t>(ceil_div(K, SD_WARPS * 32),
                                                         device_sm_count() * SD_BLOCKS_PER_SM);
-    sddmm_kernel<T><<<blocks, SD_WARPS * 32, 0, st>>>(act_idx, K, cnt, off, H, I, Ngu, a.R_cap,
+    sddmm_kernel<T><<<blocks, SD_WARPS * 32, 0, st>>>(act_idx, K, cnt, off, E, H, I, Ngu, a.R_cap,
                                                       dhT, xT, dyT, waT, g_act, accumulate,
                                                       dev_status);
     USAF_CHECK_LAUNCH();

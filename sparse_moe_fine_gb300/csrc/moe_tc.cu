@@ -92,14 +92,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait: false when the phase did not complete within the limit or another role gave up.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          long long limit = TIMEOUT_CYCLES) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > TIMEOUT_CYCLES) return false;
+    if (clock64() - t0 > limit) return false;
   }
+}
+// Drain wait, for work this thread has already issued (TMA copies, MMAs): such work completes
+// whatever the other roles do, so the abort flag is not consulted; only the deadline (a clock64
+// value shared by all of a role's drain waits) bounds it.
+__device__ __forceinline__ bool mbar_drain(uint32_t bar, uint32_t parity, long long deadline) {
+  while (!mbar_try_wait(bar, parity))
+    if (clock64() > deadline) return false;
+  return true;
 }
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0,
                                        int c1) {
@@ -582,10 +591,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         *abort_flag = 1;
         flag_status(p.status, USAF_DEV_TIMEOUT);
       }
-      // let every issued copy land before the CTA can exit
+      // let every issued copy land before the CTA can exit or reuse its shared memory
+      const long long deadline = clock64() + TIMEOUT_CYCLES;
       for (int s = 0; s < STAGES && (uint32_t)s < issued; ++s) {
         const uint32_t last = issued - 1 - ((issued - 1 - s) % STAGES);
-        mbar_wait(full0 + 8 * s, (last / STAGES) & 1, abort_flag);
+        mbar_drain(full0 + 8 * s, (last / STAGES) & 1, deadline);
       }
     }
   } else if (warp == 1) {
@@ -643,7 +653,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       // wait for every MMA this thread issued before TMEM is released
       umma_commit(drain);
-      mbar_wait(drain, 0, abort_flag);
+      mbar_drain(drain, 0, clock64() + TIMEOUT_CYCLES);
     }
   } else {
     // -------------------------------------------------------------- epilogue warps 2..9
@@ -657,7 +667,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       EpiPre pre;
       epi_prefetch<VAR>(p, ti, row, lane, half, pre);
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag) ? 1 : 0;
+      if (lane == 0) {
+        ok = mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag) ? 1 : 0;
+        if (!ok) {
+          *abort_flag = 1;
+          flag_status(p.status, USAF_DEV_TIMEOUT);
+        }
+      }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
@@ -796,9 +812,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         *abort_flag = 1;
         flag_status(p.status, USAF_DEV_TIMEOUT);
       }
+      const long long deadline = clock64() + TIMEOUT_CYCLES;
       for (int s = 0; s < wg::STAGES && (uint32_t)s < issued; ++s) {
         const uint32_t last = issued - 1 - ((issued - 1 - s) % wg::STAGES);
-        mbar_wait(full0 + 8 * s, (last / wg::STAGES) & 1, abort_flag);
+        mbar_drain(full0 + 8 * s, (last / wg::STAGES) & 1, deadline);
       }
     }
   } else if (warp == 1) {
@@ -847,7 +864,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         flag_status(p.status, USAF_DEV_TIMEOUT);
       }
       umma_commit(drain);
-      mbar_wait(drain, 0, abort_flag);
+      mbar_drain(drain, 0, clock64() + TIMEOUT_CYCLES);
     }
   } else {
     // -------------------------------------------------------------- epilogue warps 2..9
@@ -860,7 +877,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int e = t / per_e, r = t % per_e, mt = r / p.NT, nt = r % p.NT;
       const bool empty = p.off[e + 1] == p.off[e];
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag) ? 1 : 0;
+      if (lane == 0) {
+        ok = mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag) ? 1 : 0;
+        if (!ok) {
+          *abort_flag = 1;
+          flag_status(p.status, USAF_DEV_TIMEOUT);
+        }
+      }
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
@@ -974,6 +997,11 @@ __device__ __forceinline__ float4 ld_peer_f4(uint32_t addr) {
                : "memory");
   return v;
 }
+__device__ __forceinline__ uint32_t ld_peer_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -988,7 +1016,7 @@ __device__ __forceinline__ void cluster_barrier() {
 __global__ void __launch_bounds__(RK_THREADS, 1)
     tc_router_split_kernel(const __grid_constant__ CUtensorMap tmA,
                            const __grid_constant__ CUtensorMap tmB, int T, int E, int H,
-                           float* __restrict__ logits) {
+                           float* __restrict__ logits, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -1049,9 +1077,10 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
       }
       if (failed) *abort_flag = 1;
       // let every issued copy land before the CTA can move on
+      const long long deadline = clock64() + TIMEOUT_CYCLES;
       for (int s = 0; s < RK_STAGES && (uint32_t)s < issued; ++s) {
         const uint32_t last = issued - 1 - ((issued - 1 - s) % RK_STAGES);
-        mbar_wait(full0 + 8 * s, (last / RK_STAGES) & 1, abort_flag);
+        mbar_drain(full0 + 8 * s, (last / RK_STAGES) & 1, deadline);
       }
     }
   } else if (warp == 1) {
@@ -1075,12 +1104,16 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
       }
       if (failed) *abort_flag = 1;
       umma_commit(tfull);  // after every MMA above (at once when there were none)
-      mbar_wait(tfull, 0, abort_flag);  // no MMA in flight when TMEM and the ring are reused
+      // no MMA in flight when TMEM and the ring are reused
+      mbar_drain(tfull, 0, clock64() + TIMEOUT_CYCLES);
     }
   } else {  // ---------------------------------------------------- epilogue warps 2..5
     const int q = warp & 3;  // TMEM lane quarter: experts m0 + 32 q + lane
     int ok = 1;
-    if (lane == 0) ok = mbar_wait(tfull, 0, abort_flag) ? 1 : 0;
+    if (lane == 0) {
+      ok = mbar_wait(tfull, 0, abort_flag) ? 1 : 0;
+      if (!ok) *abort_flag = 1;
+    }
     ok = __shfl_sync(0xffffffffu, ok, 0);
     if (ok) {
       tc_fence_after();
@@ -1100,8 +1133,13 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_barrier();  // every CTA's partial is in its shared memory
-  {
+  if (threadIdx.x == 0 && *abort_flag) flag_status(status, USAF_DEV_TIMEOUT);
+  cluster_barrier();  // every CTA's partial (or its failure flag) is in its shared memory
+  // a CTA that gave up left no partial: the cluster then writes none of the tile's logits
+  uint32_t peer_failed = 0;
+  for (uint32_t r = 0; r < RK_SPLIT; ++r)
+    peer_failed |= ld_peer_u32(peer_smem(smem_u32((const void*)abort_flag), r));
+  if (!peer_failed) {
     // this CTA's tokens of the tile, all experts of the tile, float4 at a time
     constexpr int TOK = RK_N / RK_SPLIT;
     const uint32_t base = smem_u32(part);
@@ -1134,6 +1172,53 @@ __global__ void __launch_bounds__(RK_THREADS, 1)
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
                  "r"(RK_N)
+                 : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------- bounded-wait check
+// The failure path of the kernels above, run on purpose and without any fault: one CTA takes
+// tensor memory, waits on an mbarrier that nothing arrives on through the same bounded wait
+// (limited to `limit` cycles instead of about two seconds), records the timeout, drains its MMA
+// pipeline (nothing was issued, so the commit completes at once) and frees the tensor memory.
+__global__ void __launch_bounds__(64, 1) diag_wait_kernel(long long limit, uint32_t* status) {
+  __shared__ __align__(8) uint64_t bars[2];  // never-arriving barrier, drain
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_word;
+  volatile int* abort_flag = &abort_word;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t never = smem_u32(&bars[0]), drain = smem_u32(&bars[1]);
+  if (threadIdx.x == 0) {
+    mbar_init(never, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(&tmem_slot)),
+                 "r"(32)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_slot;
+  if (warp == 0 && lane == 0) {
+    if (!mbar_wait(never, 0, abort_flag, limit)) {
+      *abort_flag = 1;
+      flag_status(status, USAF_DEV_TIMEOUT);
+    }
+  } else if (warp == 1 && lane == 0) {
+    umma_commit(drain);
+    mbar_drain(drain, 0, clock64() + limit);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(32)
                  : "memory");
   }
 }
@@ -1216,6 +1301,7 @@ Params base_params(const MoeArgs& a) {
   p.I = (int)a.s.I;
   p.T = (int)a.s.T;
   p.R_cap = a.R_cap;
+  p.status = a.status;
   return p;
 }
 
@@ -1254,7 +1340,7 @@ static bool router_split_ok() {
 }
 
 usaf_status tc_router_logits(const usaf_moe_shape& s, const void* x, const float* wr,
-                             void* wr3, float* logits, cudaStream_t st) {
+                             void* wr3, float* logits, uint32_t* status, cudaStream_t st) {
   {
     USAF_TRACE("router_split", st);
     const dim3 grid((unsigned)ceil_div(s.H, 512), (unsigned)s.E);
@@ -1280,7 +1366,7 @@ usaf_status tc_router_logits(const usaf_moe_shape& s, const void* x, const float
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, tc_router_split_kernel, ma, mb, (int)s.T, (int)s.E, (int)s.H,
-                           logits) != cudaSuccess)
+                           logits, status) != cudaSuccess)
       return USAF_ERR_CUDA;
     USAF_CHECK_LAUNCH();
     return USAF_OK;
@@ -1296,6 +1382,7 @@ usaf_status tc_router_logits(const usaf_moe_shape& s, const void* x, const float
   p.MT = (int)ceil_div(s.E, BM);
   p.NT = (int)ceil_div(s.T, ROUTER_BN);
   p.acc_out = logits;
+  p.status = status;
   return launch<V_ROUTER>(ma, mb, p, st);
 }
 
@@ -1346,6 +1433,13 @@ usaf_status tc_bwd_dx(const MoeArgs& a, const void* dhT, float* dx_acc, cudaStre
   return launch<V_DX>(ma, mb, p, st);
 }
 
+usaf_status diag_wait_launch(int64_t limit_cycles, uint32_t* status, cudaStream_t st) {
+  USAF_TRACE("diag_bounded_wait", st);
+  diag_wait_kernel<<<1, 64, 0, st>>>((long long)limit_cycles, status);
+  USAF_CHECK_LAUNCH();
+  return USAF_OK;
+}
+
 usaf_status tc_wgrad_dense(const MoeArgs& a, const void* aT, int64_t a_rows, const void* bT,
                            int64_t b_rows, float* g, int accumulate, cudaStream_t st) {
   USAF_TRACE(accumulate ? "tc_wgrad_dense_add" : "tc_wgrad_dense", st);
@@ -1373,6 +1467,7 @@ usaf_status tc_wgrad_dense(const MoeArgs& a, const void* aT, int64_t a_rows, con
   p.MT = (int)ceil_div(a_rows, 128);
   p.NT = (int)ceil_div(b_rows, 256);
   p.accumulate = accumulate;
+  p.status = a.status;
   static bool attr_done = false;
   if (!attr_done) {
     if (cudaFuncSetAttribute(tc_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

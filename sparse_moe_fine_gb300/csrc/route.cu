@@ -274,14 +274,15 @@ __global__ void perm_pad_kernel(const int32_t* __restrict__ expert_count,
 
 usaf_status route_launch(const usaf_moe_shape& s, const void* x, usaf_dtype xdt,
                          const float* wr, const float* logits_in, float* logits_out, int renorm,
-                         const usaf_routing& rt, RouteWs& w, cudaStream_t st) {
+                         const usaf_routing& rt, RouteWs& w, uint32_t* dev_status,
+                         cudaStream_t st) {
   const int Tn = (int)s.T, H = (int)s.H, E = (int)s.E, k = (int)s.k;
   const int64_t R = s.T * s.k;
   const float* logits = logits_in;
   if (!logits_in && xdt == USAF_BF16 && tc_shape_ok(s)) {
     // bf16 tokens: three bf16 tensor-core products of the split fp32 router weight
     float* out = logits_out ? logits_out : w.logits;
-    USAF_TRY(tc_router_logits(s, x, wr, w.wr3, out, st));
+    USAF_TRY(tc_router_logits(s, x, wr, w.wr3, out, dev_status, st));
     logits = out;
   } else if (!logits_in) {
     USAF_TRACE("route_logits", st);

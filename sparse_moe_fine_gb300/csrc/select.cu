@@ -532,12 +532,20 @@ __global__ void bitmap_zero_kernel(uint32_t* bm, int64_t words) {
     bm[i] = 0;
 }
 
-__global__ void bitmap_set_kernel(const int64_t* __restrict__ idx, int64_t K, uint32_t* bm) {
+// Indices outside [0, N) are skipped and flagged (the set violates its contract).
+__global__ void bitmap_set_kernel(const int64_t* __restrict__ idx, int64_t K, int64_t N,
+                                  uint32_t* bm, uint32_t* dev_status) {
+  bool bad = false;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < K;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t f = idx[i];
+    if (f < 0 || f >= N) {
+      bad = true;
+      continue;
+    }
     atomicOr(&bm[f >> 5], 1u << (f & 31));
   }
+  flag_status_warp(dev_status, bad, USAF_DEV_BAD_INDEX);
 }
 
 // The fixed sequence of launches that selects the top-K of `s` (see file comment).
@@ -629,6 +637,7 @@ __global__ void rigl_merge_kernel(const int64_t* __restrict__ act, int64_t K,
     } else {
       const int64_t f = act[t];
       const int64_t pos = (t - nd) + lower_bound_i64(grown, D, f);
+      if (pos >= K) return;  // only an unsorted act_idx gets here
       new_idx[pos] = f;
       p_out[pos] = p_in[t];
       m_out[pos] = m_in[t];
@@ -639,6 +648,7 @@ __global__ void rigl_merge_kernel(const int64_t* __restrict__ act, int64_t K,
     const int64_t f = grown[j];
     const int64_t kept_before = lower_bound_i64(act, K, f) - dropped_below(act, dpos, D, f);
     const int64_t pos = j + kept_before;
+    if (pos < 0 || pos >= K) return;  // only an unsorted act_idx gets here
     new_idx[pos] = f;
     p_out[pos] = to_f32(f < n0 ? w0[f] : w1[f - n0]);
     m_out[pos] = 0.f;
@@ -749,7 +759,7 @@ usaf_status rigl_launch(const float* g, int64_t N, const int64_t* act_idx, int64
       USAF_TRACE("rigl_bitmap", st);
       bitmap_zero_kernel<<<grid_dim_for(words), 256, 0, st>>>(bitmap, words);
       USAF_CHECK_LAUNCH();
-      bitmap_set_kernel<<<grid_dim_for(K), 256, 0, st>>>(act_idx, K, bitmap);
+      bitmap_set_kernel<<<grid_dim_for(K), 256, 0, st>>>(act_idx, K, N, bitmap, dev_status);
       USAF_CHECK_LAUNCH();
     }
     Src sg{};

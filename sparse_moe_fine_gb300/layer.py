@@ -21,7 +21,7 @@ import torch
 from . import binding as B
 
 
-STATUS_BITS = 3  # USAF_DEV_NONFINITE, USAF_DEV_SELECT_EXACT_PATH, USAF_DEV_TIMEOUT
+STATUS_BITS = 4  # NONFINITE, SELECT_EXACT_PATH, TIMEOUT, BAD_INDEX (usaf.h USAF_DEV_*)
 
 
 def allreduce_grads(g_act, g_router, status, group=None):
@@ -86,8 +86,15 @@ class MoELayer:
 
     # ------------------------------------------------------------------ active set
     def set_active(self, act_idx, p=None, m=None, v=None):
-        """Install a sorted active set; fresh state starts from the weight values."""
-        self.act = act_idx.to(self.dev, torch.int64).contiguous()
+        """Install a sorted active set; fresh state starts from the weight values. The set is
+        checked on the device (usaf_validate_active: ascending, no repeats, inside [0, N)) and
+        refused with ValueError before anything reads it; this waits for the device once."""
+        act = act_idx.to(self.dev, torch.int64).contiguous()
+        chk = torch.zeros(1, dtype=torch.int32, device=self.dev)
+        B.validate_active(act, self.N, chk)
+        if int(chk.item()) & B.DEV_BAD_INDEX:
+            raise ValueError("active set is not strictly ascending inside [0, N)")
+        self.act = act
         K = self.act.numel()
         self.K = K
         if p is None:
@@ -121,7 +128,7 @@ class MoELayer:
     def route(self, x, stream=None):
         self._check_tokens(x=x)
         B.route_topk(self.s, x, self.w_router, self.rt, logits_out=self.logits,
-                     renorm=self.renorm, ws=self.ws_route, stream=stream)
+                     renorm=self.renorm, dev_status=self.status, ws=self.ws_route, stream=stream)
 
     def _main(self, stream):
         return torch.cuda.current_stream(self.dev) if stream is None else stream
@@ -138,7 +145,7 @@ class MoELayer:
         self._check_tokens(x=x, y=y)
         ready = self.ev_opt if self.pending_opt else None
         B.moe_fwd(self.s, x, self.w_gate_up, self.w_down, self.rt, self.x_perm, self.h, self.wa,
-                  y, ws=self.ws_fwd, stream=stream, weights_ready=ready)
+                  y, ws=self.ws_fwd, stream=stream, weights_ready=ready, dev_status=self.status)
         self.pending_opt = False  # the stream is ordered after the update from here on
         return y
 
@@ -174,9 +181,11 @@ class MoELayer:
     def train_step(self, x, dy, stream=None, y=None, dx=None):
         """route -> forward -> sparse backward -> SparseAdam (experts, router). y and dx may name
         other output buffers than the layer's own."""
-        # per-step non-finite flag (a non-finite gradient skips this step), alternating words
+        # per-step non-finite flag (a non-finite gradient skips this step), alternating words;
+        # cleared on the step's own stream, ahead of the kernels that set its bits
         self.status = self.status2[self.step_count % 2:self.step_count % 2 + 1]
-        self.status.zero_()
+        with torch.cuda.stream(self._main(stream)):
+            self.status.zero_()
         self.route(x, stream)
         y = self.forward(x, stream, y=y)
         self.backward(x, dy, stream=stream, dx=dx)
@@ -216,10 +225,10 @@ class MoELayer:
         with torch.cuda.graph(g_route, stream=cs):
             status.zero_()
             B.route_topk(self.s, x, self.w_router, self.rt, logits_out=self.logits,
-                         renorm=self.renorm, ws=self.ws_route, stream=cs)
+                         renorm=self.renorm, dev_status=status, ws=self.ws_route, stream=cs)
         with torch.cuda.graph(g_body, stream=cs):
             B.moe_fwd(self.s, x, self.w_gate_up, self.w_down, self.rt, self.x_perm, self.h,
-                      self.wa, self.y, ws=self.ws_fwd, stream=cs)
+                      self.wa, self.y, ws=self.ws_fwd, stream=cs, dev_status=status)
             B.moe_bwd_sparse(self.s, x, self.w_router, self.w_gate_up, self.w_down, self.rt,
                              self.x_perm, self.h, self.wa, dy, self.act, self.g_act,
                              self.g_router, dx=self.dx, logits=self.logits, renorm=self.renorm,
@@ -228,12 +237,16 @@ class MoELayer:
         return g_route, g_body, B.launch_count() - n0  # library kernels in the two graphs
 
     def train_step_host(self, x_host, dy_host, y_host, dx_host, x_dev, dy_dev, stream=None):
-        """The same step fed from (pinned) host memory: copy x and dy in, run, copy y and dx out."""
-        x_dev.copy_(x_host, non_blocking=True)
-        dy_dev.copy_(dy_host, non_blocking=True)
-        self.train_step(x_dev, dy_dev, stream)
-        y_host.copy_(self.y, non_blocking=True)
-        dx_host.copy_(self.dx, non_blocking=True)
+        """The same step fed from (pinned) host memory: copy x and dy in, run, copy y and dx out,
+        every copy on the step's stream."""
+        main = self._main(stream)
+        with torch.cuda.stream(main):
+            x_dev.copy_(x_host, non_blocking=True)
+            dy_dev.copy_(dy_host, non_blocking=True)
+        self.train_step(x_dev, dy_dev, main)
+        with torch.cuda.stream(main):
+            y_host.copy_(self.y, non_blocking=True)
+            dx_host.copy_(self.dx, non_blocking=True)
 
 
 class HostStepper:

@@ -33,3 +33,15 @@ def max_rel(got, ref, floor_frac=1e-4):
         return 0.0
     floor = max(floor_frac * float(np.max(np.abs(ref))), 1e-300)
     return float(np.max(np.abs(got - ref) / np.maximum(np.abs(ref), floor)))
+
+
+def max_rel_terms(got, ref, *terms):
+    """max |got - ref| / max(|ref|, |each term|): the relative error of a sum or difference
+    measured against the size of its terms, so a result that cancels to near zero (an updated
+    weight crossing zero) is held to the rounding of the terms that formed it."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    scale = np.abs(ref)
+    for t in terms:
+        scale = np.maximum(scale, np.abs(np.asarray(t, np.float64)))
+    return float(np.max(np.abs(got - ref) / np.maximum(scale, 1e-300))) if ref.size else 0.0

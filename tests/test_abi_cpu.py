@@ -18,10 +18,10 @@ fake_addresses = pytest.mark.skipif(torch.cuda.is_available(),
 def test_library_exports_every_header_symbol():
     L = B.lib()
     syms = B.header_symbols()
-    assert len(syms) == 23
+    assert len(syms) == 26
     for s in syms:
         assert hasattr(L, s), s
-    assert L.usaf_abi_version() == 1
+    assert L.usaf_abi_version() == 2
     assert L.usaf_status_string(0) == b"ok"
     assert L.usaf_status_string(3) == b"workspace missing or too small"
 
@@ -33,6 +33,8 @@ def test_capacity_and_workspace_queries():
     assert B.route_topk_workspace_size(s) > 4096 * 128 * 4
     assert B.moe_fwd_workspace_size(s, B.BF16) >= 4096 * 2048 * 4
     assert B.moe_bwd_workspace_size(s, B.BF16, 3019899) > 0
+    off = B.moe_bwd_dlogit_offset(s, B.BF16, 3019899)
+    assert off % 256 == 0 and off + 4096 * 8 * 4 <= B.moe_bwd_workspace_size(s, B.BF16, 3019899)
     N = 603979776
     K = math.ceil(0.005 * N)
     ws = B.importance_select_workspace_size(N, K)
@@ -54,7 +56,7 @@ def test_host_argument_checks_return_codes():
     r = B._Routing()
     # null routing arrays
     assert _call("usaf_route_topk", ctypes.byref(s), 1, 0, 1, None, None, 1, ctypes.byref(r),
-                 1, 1 << 20, None) == 1
+                 None, 1, 1 << 20, None) == 1
     # k > E
     s2 = B.shape(8, 64, 4, 5, 64)
     assert _call("usaf_routed_rows_capacity", ctypes.byref(s2)) == -1
@@ -82,7 +84,15 @@ def test_host_argument_checks_return_codes():
     # bf16 layers need H and I multiples of 64
     s3 = B.shape(8, 96, 4, 2, 64)
     assert _call("usaf_moe_fwd", ctypes.byref(s3), 1, 1, 1, 1, ctypes.byref(B._Routing(*[1] * 7)),
-                 1, 1, 1, 1, 1, 1 << 30, None) == 2
+                 1, 1, 1, 1, None, 1, 1 << 30, None) == 2
+    # active-set validation needs a status word and a positive bound
+    assert _call("usaf_validate_active", 1, 4, 10, None, None) == 1
+    assert _call("usaf_validate_active", 1, 4, 0, 1, None) == 1
+    assert _call("usaf_validate_active", None, 4, 10, 1, None) == 1
+    # the bounded-wait check: limit in [1, 2^32], status word required
+    assert _call("usaf_diag_bounded_wait", 0, 1, None) == 1
+    assert _call("usaf_diag_bounded_wait", (1 << 32) + 1, 1, None) == 1
+    assert _call("usaf_diag_bounded_wait", 1000, None, None) == 1
 
 
 @fake_addresses
@@ -124,12 +134,12 @@ def test_layer_call_host_checks():
     bwd_ws = B.moe_bwd_workspace_size(s, B.BF16, 100)
     assert fwd_ws > 0 and bwd_ws > 0
     fwd = lambda y, ev, ws: _call("usaf_moe_fwd_wait", ctypes.byref(s), B.BF16, f, f, f, rt, f, f,
-                                  f, y, ev, f, ws, None)
+                                  f, y, ev, None, f, ws, None)
     assert fwd(None, None, big) == 1           # no output buffer
     assert fwd(f, None, fwd_ws - 1) == 3       # workspace one byte short
     assert fwd(f, f, fwd_ws - 1) == 3          # the same with an event to wait for
-    assert _call("usaf_moe_fwd_wait", ctypes.byref(s), 7, f, f, f, rt, f, f, f, f, None, f, big,
-                 None) == 1                    # unknown dtype
+    assert _call("usaf_moe_fwd_wait", ctypes.byref(s), 7, f, f, f, rt, f, f, f, f, None, None, f,
+                 big, None) == 1               # unknown dtype
 
     def bwd(name, renorm=1, logits=f, K=100, ws=big):
         return _call(name, ctypes.byref(s), B.BF16, renorm, f, f, f, f, rt, logits, f, f, f, f,

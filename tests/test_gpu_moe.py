@@ -11,7 +11,7 @@ import oracle
 from sparse_moe_fine_gb300 import binding as B
 from sparse_moe_fine_gb300 import synth
 
-from _gpu import device, rel_l2, to_dev
+from _gpu import device, max_rel, max_rel_terms, rel_l2, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -41,13 +41,19 @@ def run_layer(cfg, inp, act_idx, logits, dev, renorm=1, want_dx=True):
     dx = torch.empty(cfg.T, cfg.H, dtype=dt, device=dev) if want_dx else None
     dw = torch.empty(cfg.T * cfg.k, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
+    dtc = B.BF16 if bf else B.F32
+    ws = torch.empty(B.moe_bwd_workspace_size(s, dtc, K), dtype=torch.uint8, device=dev)
     B.moe_bwd_sparse(s, x, wr, wgu, wd, rt, xp, h, wa, dy, act, g_act, g_r, dx=dx, dw_slot=dw,
-                     logits=li, renorm=renorm, dev_status=st)
+                     logits=li, renorm=renorm, dev_status=st, ws=ws)
     torch.cuda.synchronize()
     out = {"Y": y.float().cpu().numpy(), "g_act": g_act.cpu().numpy(),
            "g_router": g_r.cpu().numpy(), "dw": dw.cpu().numpy().reshape(cfg.T, cfg.k),
            "status": int(st.item()), "idx": rt.topk_idx.cpu().numpy().reshape(cfg.T, cfg.k),
            "count": rt.expert_count.cpu().numpy()}
+    if renorm:  # the device's dlogit at the selected experts, slot order
+        off = B.moe_bwd_dlogit_offset(s, dtc, K)
+        dl = ws[off:off + 4 * cfg.T * cfg.k].view(torch.float32)
+        out["dl_sel"] = dl.cpu().numpy().reshape(cfg.T, cfg.k)
     if want_dx:
         out["dx"] = dx.float().cpu().numpy()
     return out
@@ -244,6 +250,22 @@ def test_large_layers_sampled(name, ntok):
     assert sel.sum() > 1000
     assert rel_l2(got["g_act"][sel], g[sel]) <= 1e-2
     assert np.isfinite(got["g_act"]).all() and np.isfinite(got["g_router"]).all()
+    # router backward: dlogit of the sampled tokens against the oracle (bf16 bound) ...
+    dl_dense = np.zeros((ntok, cfg.E))
+    np.put_along_axis(dl_dense, idx[toks], got["dl_sel"][toks], axis=1)
+    assert rel_l2(dl_dense, b["dlogit"]) <= 1e-2
+    # ... and g_router = dlogit^T x from the device's own dlogit, in fp64 on the host: this
+    # isolates the reduction kernel (fp32 sums of the same products, so a far tighter bound)
+    dl_all = np.zeros((cfg.T, cfg.E))
+    np.put_along_axis(dl_all, idx, got["dl_sel"].astype(np.float64), axis=1)
+    assert rel_l2(got["g_router"], dl_all.T @ inp["x"].astype(np.float64)) <= 1e-4
+    if name == "qwen3_skewed":
+        # the whole-batch router gradient against the oracle (every token, dead experts included)
+        full = oracle.moe_backward(inp["x"], inp["w_router"], inp["w_gate_up"], inp["w_down"],
+                                   idx, w, logits, inp["dy"])
+        assert rel_l2(got["g_router"], full["g_router"]) <= 1e-2
+        dead = counts == 0
+        assert (got["g_router"][dead] == 0).all() and (full["g_router"][dead] == 0).all()
 
 
 def test_fwd_waits_for_weights_ready():
@@ -472,3 +494,65 @@ def test_graphed_steps_match_eager_steps():
     for ta, tb in ((a.p, b.p), (a.m, b.m), (a.v, b.v), (a.r_p, b.r_p)):
         assert rel_l2(tb.cpu().numpy(), ta.cpu().numpy()) <= 1e-5
     assert b.replayed_kernels > 0 and len(b._graphs) == 2
+
+
+def test_graphed_steps_match_oracle():
+    """The benchmarked step (MoELayer.graphed_train_step: routing and forward + backward replayed
+    from CUDA graphs, SparseAdam on a side stream) against the oracle composition over two
+    steps: routing -> moe_backward -> masked_expert_grad -> sparse_adam. Each step's oracle reads
+    the weights, router and optimizer state the device held before that step, and routes on the
+    device's logits (the same scores; the logits themselves are pinned by the routing tests)."""
+    from sparse_moe_fine_gb300.layer import MoELayer
+    dev = device()
+    cfg = synth.small_config("graph_oracle", T=512, H=256, E=16, k=4, I=128, bf16=True,
+                             frac=0.05)
+    inp = synth.moe_inputs(cfg, seed=13)
+    act_np = synth.uniform_mask(cfg.N, cfg.K, seed=13)
+    act = torch.from_numpy(act_np).to(dev)
+    bf = lambda a: torch.from_numpy(a).to(dev).to(torch.bfloat16)
+    L = MoELayer(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, bf(inp["w_gate_up"]), bf(inp["w_down"]),
+                 torch.from_numpy(inp["w_router"]).to(dev), act, lr=1e-3, device=dev)
+    x, dy = bf(inp["x"]), bf(inp["dy"])
+    b1, b2 = L.betas
+    for step in (1, 2):
+        L.wait_optimizer()
+        torch.cuda.synchronize()
+        wgu0 = L.w_gate_up.float().cpu().numpy()
+        wd0 = L.w_down.float().cpu().numpy()
+        wr0 = L.w_router.cpu().numpy().copy()
+        p0, m0, v0 = (t.cpu().numpy().copy() for t in (L.p, L.m, L.v))
+        rp0, rm0, rv0 = (t.cpu().numpy().copy() for t in (L.r_p, L.r_m, L.r_v))
+        y, dx = L.graphed_train_step(x, dy)
+        L.wait_optimizer()
+        torch.cuda.synchronize()
+        assert int(L.status.item()) == 0
+        logits = L.logits.cpu().numpy()
+        idx, w = oracle.route_topk(logits, cfg.k)
+        assert (L.rt.topk_idx.cpu().numpy().reshape(cfg.T, cfg.k) == idx).all()
+        b = oracle.moe_backward(inp["x"], wr0, wgu0, wd0, idx, w, logits, inp["dy"])
+        g = oracle.masked_expert_grad(act_np, inp["x"], wgu0, wd0, idx, w, inp["dy"])
+        assert rel_l2(y.float().cpu().numpy(), b["Y"]) <= 1e-2
+        assert rel_l2(dx.float().cpu().numpy(), b["dx"]) <= 1e-2
+        g_dev = L.g_act.cpu().numpy()
+        assert rel_l2(g_dev, g) <= 1e-2
+        assert rel_l2(L.g_router.cpu().numpy(), b["g_router"]) <= 1e-2
+        # the optimizer on the device's own gradients (the SparseAdam bound: max-rel 1e-5, with
+        # m measured against the size of its two terms, as in the optimizer's own tests)
+        op, om, ov = oracle.sparse_adam(g_dev, p0, m0, v0, 1e-3, b1, b2, L.eps, step)
+        # p = p0 - update: against the size of p0 and of the update (a weight crossing zero)
+        assert max_rel_terms(L.p.cpu().numpy(), op, p0, op - p0.astype(np.float64)) <= 1e-5
+        assert max_rel(L.v.cpu().numpy(), ov) <= 1e-5
+        m_scale = np.maximum(np.abs(om), b1 * np.abs(m0) + (1 - b1) * np.abs(g_dev))
+        assert np.max(np.abs(L.m.cpu().numpy() - om) / np.maximum(m_scale, 1e-30)) <= 1e-5
+        rp, rm, rv = oracle.sparse_adam(L.g_router.cpu().numpy().reshape(-1), rp0, rm0, rv0,
+                                        1e-3, b1, b2, L.eps, step)
+        assert max_rel_terms(L.r_p.cpu().numpy(), rp, rp0, rp - rp0.astype(np.float64)) <= 1e-5
+        assert np.array_equal(L.w_router.cpu().numpy().reshape(-1), L.r_p.cpu().numpy())
+        # the bf16 weights: RNE of the master copy at the active set, unchanged elsewhere
+        w_all = np.concatenate([L.w_gate_up.float().cpu().numpy().reshape(-1),
+                                L.w_down.float().cpu().numpy().reshape(-1)])
+        w_before = np.concatenate([wgu0.reshape(-1), wd0.reshape(-1)])
+        assert np.array_equal(w_all[act_np], oracle.bf16_round(L.p.cpu().numpy()))
+        keep = np.ones(cfg.N, bool)
+        keep[act_np] = False
+        assert np.array_equal(w_all[keep], w_before[keep])

@@ -134,7 +134,9 @@ def test_rigl_against_oracle(N, K, D):
 
 
 def test_rigl_full_qwen3_layer():
-    """N = 603,979,776, K = 3,019,899, D = floor(0.3 K) = 905,969: drop and grow sets exact."""
+    """N = 603,979,776, K = 3,019,899, D = floor(0.3 K) = 905,969: the oracle's RigL swap (grow
+    set by its threshold form, pinned to the sort form on the CPU) and the device's agree on the
+    new set and on every carried or reset state entry."""
     dev = device()
     cfg = synth.CONFIGS["qwen3_30b_a3b"]
     N, K = cfg.N, cfg.K
@@ -146,22 +148,11 @@ def test_rigl_full_qwen3_layer():
     w = np.concatenate([wgu, wd])
     p = w[act].copy()
     m, v = synth.adam_state(K, seed=0)
-    new, p2, m2, v2, ns = gpu_rigl(g, act, p, m, v, w, cfg.N_gu, D, dev)
-    assert ns == D and new.size == K and (np.diff(new) > 0).all()
-    # drop: the D smallest |p| (ties to the lower index), from the oracle's rule on the K entries
-    key = oracle.abs_key(p).astype(np.int64)
-    drop = np.sort(act[np.lexsort((act, key))[:D]])
-    # grow: the D largest |g| outside the old set (threshold form, actives masked to key 0)
-    gm = g.copy()
-    gm[act] = 0.0
-    grow = oracle.importance_select_threshold(gm, D)
-    assert np.abs(g[grow]).min() > 0
-    ref_new = np.sort(np.concatenate([np.setdiff1d(act, drop), grow]))
-    assert np.array_equal(new, ref_new)
-    pos = np.searchsorted(act, new)
-    kept = (pos < K) & (act[np.minimum(pos, K - 1)] == new)
-    assert (p2[kept] == p[pos[kept]]).all() and (m2[kept] == m[pos[kept]]).all()
-    assert (p2[~kept] == w[new[~kept]]).all() and (m2[~kept] == 0).all() and (v2[~kept] == 0).all()
+    got = gpu_rigl(g, act, p, m, v, w, cfg.N_gu, D, dev)
+    ref = oracle.rigl_swap(act, p, m, v, g, D, lambda i: w[i], grow_by="threshold")
+    for a, b in zip(got[:4], ref[:4]):
+        assert np.array_equal(a, b)
+    assert got[4] == ref[4] == D
 
 
 def gpu_reselect(g_np, K, act, p, m, v, w_np, n0, dev):
