@@ -3,12 +3,15 @@
 A step is one pass of the whole hot path over one batch: route (router logits, top-k,
 permutation) -> grouped SwiGLU forward -> sparse backward (router gradient, dx, expert gradients
 at the 0.5% active set) -> SparseAdam on the active expert entries and on the router.
-Workload: the Qwen3-30B-A3B-shaped layer (T=4096 tokens, H=2048, E=128, top-8, I=768, bf16,
-router fp32, K = ceil(0.005 * 603,979,776) = 3,019,899 active entries chosen by the importance
-selection of a seeded Student-t(3) dense gradient). Inputs are seeded synthetic data; the
-weights (1.2 GB) are larger than L2, so no flush is needed between steps.
+Default workload: the Qwen3-30B-A3B-shaped layer (T=4096 tokens, H=2048, E=128, top-8, I=768,
+bf16, router fp32, K = ceil(0.005 * 603,979,776) = 3,019,899 active entries chosen by the
+importance selection of a seeded Student-t(3) dense gradient). --workload qwen3_skewed times the
+same layer at T=16384 under Zipf(1.2) expert loads with ten dead experts and 80% of the active
+set on the 16 most loaded experts; --workload mixtral_8x7b the Mixtral-8x7B-shaped layer (H=4096,
+E=8, top-2, I=14336, T=8192, uniform 0.5% active set). Inputs are seeded synthetic data; the
+expert weights (1.2 GB and more) are larger than L2, so no flush is needed between steps.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference] [--workload NAME]
 
 Prints one JSON line. Under torchrun each rank runs its own replica (weak scaling, no
 collective on the data path); rank 0 prints.
@@ -34,7 +37,41 @@ sys.path.insert(0, ROOT)
 from sparse_moe_fine_gb300 import synth  # noqa: E402
 
 METRIC = "MoE-layer train-step tokens/s (fwd+sparse bwd+SparseAdam); % of roofline"
-WORKLOAD = "qwen3_30b_a3b"
+WORKLOADS = ("qwen3_30b_a3b", "qwen3_skewed", "mixtral_8x7b")
+HOT_EXPERTS, HOT_FRAC = 16, 0.8  # the skewed workload's active-set concentration
+
+
+def workload_inputs(name):
+    """The workload's configuration and its seeded inputs (skewed routing realised through
+    x[:, 0] = 1 and the router's first column)."""
+    cfg = synth.CONFIGS[name]
+    inp = synth.moe_inputs(cfg, seed=0)
+    if "zipf_s" in cfg.extra:
+        synth.apply_skew(inp, skew_bias(cfg))
+    return cfg, inp
+
+
+def skew_bias(cfg):
+    return synth.skew_bias(cfg.E, cfg.extra["zipf_s"], cfg.extra["dead_experts"], seed=0)
+
+
+def fixed_active_set(name, cfg):
+    """The active set of the workloads whose set is drawn rather than selected: the skewed
+    layer's concentrated set (hot experts = the largest logit offsets) or a uniform set."""
+    if name == "qwen3_skewed":
+        hot = np.argsort(-skew_bias(cfg), kind="stable")[:HOT_EXPERTS]
+        return synth.concentrated_mask(cfg, hot, HOT_FRAC, seed=0)
+    return synth.uniform_mask(cfg.N, cfg.K, seed=0)
+
+
+def oracle_active_set(name, cfg):
+    """The active set the CPU baseline uses, formed on the host only: for the default workload
+    the oracle's importance selection of the same seeded Student-t(3) gradient the device selects
+    from (the two are the same set; the GPU tests check it bit for bit)."""
+    if name == "qwen3_30b_a3b":
+        import oracle
+        return oracle.importance_select_threshold(synth.student_t3(cfg.N, seed=0), cfg.K)
+    return fixed_active_set(name, cfg)
 
 
 def peaks():
@@ -47,14 +84,16 @@ def peaks():
         return 6800.0, 1900.0, 1700.0, "fallback"
 
 
-def algorithmic(cfg):
-    """Algorithmic FLOPs and HBM bytes of one step (unpadded, SDDMM-counted masked dW)."""
+def algorithmic(cfg, sddmm_pairs=None):
+    """Algorithmic FLOPs and HBM bytes of one step (unpadded, SDDMM-counted masked dW: 2 flops per
+    (active entry, token routed to its expert) pair, from the live routing when given)."""
     T, H, E, k, I, K = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.K
     R = T * k
+    pairs = sddmm_pairs if sddmm_pairs is not None else K * (R / E)
     fl = (2 * R * 2 * I * H + 2 * R * I * H          # forward GEMMs
           + 2 * R * I * H + 2 * R * 2 * I * H        # dgrad through down, dx
           + 2 * T * E * H * 3                        # router logits, g_router, dx router term
-          + 2 * K * (R / E))                         # masked dW at the active set
+          + 2 * pairs)                               # masked dW at the active set
     by = (2 * cfg.N * 2                             # expert weights, read in fwd and in bwd
           + 2 * T * H * 2                            # x
           + 2 * R * 2 * I * 2 + 2 * R * I * 2        # h, A (write + read)
@@ -239,33 +278,47 @@ def cpu_threads():
         return os.cpu_count()
 
 
+def oracle_steps(name, tokens, steps, warmup):
+    """The one CPU baseline both arms report: the oracle's step (oracle_step_sample) on the first
+    `tokens` tokens of the workload, with the workload's weights and an active set formed on the
+    host; `warmup` untimed steps, then `steps` timed ones. Returns (seconds per step, cfg)."""
+    cfg, inp = workload_inputs(name)
+    act = oracle_active_set(name, cfg)
+    p0 = master_values(inp, act, cfg.N_gu)
+    inp = {k: v.astype(np.float64) for k, v in inp.items()}  # exact upcast of the bf16 inputs
+    for _ in range(warmup):
+        oracle_step_sample(cfg, inp, act, p0, tokens)
+    times = [oracle_step_sample(cfg, inp, act, p0, tokens) for _ in range(max(1, steps))]
+    return sum(times) / len(times), cfg
+
+
+def cpu_baseline_entry(sec_per_step, tokens, cfg, steps):
+    return {"value": tokens / sec_per_step, "unit": "tokens/s", "cores": cpu_threads(),
+            "kind": "oracle",
+            "sample": f"oracle step on the first {tokens} of {cfg.T} tokens (whole router, "
+                      f"every expert those tokens reach, SparseAdam over all {cfg.K} active "
+                      f"entries and the router), mean of {steps} steps",
+            "ms_per_step": 1e3 * sec_per_step}
+
+
 def run_reference(args):
-    """The oracle on the host cores: the same metric on bounded samples of the workload."""
+    """The oracle on the host cores: the same metric on bounded samples of the workload. Every
+    timed step is one oracle step on the same token sample the GPU arm's cpu_baseline uses."""
     dist, ws, rank, local = dist_setup()
     if rank != 0:
         return
-    cfg = synth.CONFIGS[WORKLOAD]
-    inp = synth.moe_inputs(cfg, seed=0)
-    act = synth.uniform_mask(cfg.N, cfg.K, seed=0)
-    p0 = master_values(inp, act, cfg.N_gu)
-    inp = {k: v.astype(np.float64) for k, v in inp.items()}  # exact upcast of the bf16 inputs
-    # per-step sample: fewer tokens when more steps are asked for, so the run stays in minutes
-    tokens = args.cpu_tokens if args.steps <= 10 else (64 if args.steps <= 100 else 16)
-    for _ in range(min(args.warmup, 1)):
-        oracle_step_sample(cfg, inp, act, p0, tokens)
-    times = [oracle_step_sample(cfg, inp, act, p0, tokens) for _ in range(max(1, args.steps))]
-    sec = sum(times)
-    value = tokens * len(times) / sec
+    tokens = args.cpu_tokens
+    sec, cfg = oracle_steps(args.workload, tokens, args.steps, args.warmup)
+    value = tokens / sec
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
-            "n_gpus": ws, "steps": len(times), "warmup": args.warmup,
-            "ms_per_step": 1e3 * sec / len(times) * (cfg.T / tokens),
+            "n_gpus": ws, "steps": max(1, args.steps), "warmup": args.warmup,
+            "ms_per_step": 1e3 * sec,
+            "ms_per_step_note": f"time of the {tokens}-token step that ran",
+            "est_ms_per_full_batch": 1e3 * sec * cfg.T / tokens,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": workload_config(cfg, ws),
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_threads(),
-                             "kind": "oracle",
-                             "sample": f"one step on the first {tokens} of {cfg.T} tokens, "
-                                       "per timed step"},
+            "config": workload_config(args.workload, cfg, ws),
+            "cpu_baseline": cpu_baseline_entry(sec, tokens, cfg, max(1, args.steps)),
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -280,19 +333,20 @@ def run(args):
     torch.cuda.set_device(dev)
     B.lib()
     hbm, tf_burst, tf_sus, peak_src = peaks()
-    cfg = synth.CONFIGS[WORKLOAD]
-    inp = synth.moe_inputs(cfg, seed=0)
+    cfg, inp = workload_inputs(args.workload)
     bf = lambda a: torch.from_numpy(a).to(dev).to(torch.bfloat16)
     x, dy = bf(inp["x"]), bf(inp["dy"])
     wgu, wd = bf(inp["w_gate_up"]), bf(inp["w_down"])
     wr = torch.from_numpy(inp["w_router"]).to(dev)
     stream = torch.cuda.current_stream()
 
-    # ---- importance pass: the active set is the top 0.5% |g| of a dense gradient
-    if args.no_importance:
+    # ---- importance pass: the active set is the top 0.5% |g| of a dense gradient (default
+    # workload); the other workloads' sets are drawn
+    if args.no_importance or args.workload != "qwen3_30b_a3b":
+        act = fixed_active_set(args.workload, cfg)
         return run_steps(args, B, MoELayer, dist, ws, rank, local, dev, cfg, inp, x, dy, wgu, wd,
-                         wr, torch.from_numpy(synth.uniform_mask(cfg.N, cfg.K, 0)).to(dev),
-                         None, hbm, tf_burst, tf_sus, peak_src, stream)
+                         wr, torch.from_numpy(act).to(dev), None, hbm, tf_burst, tf_sus,
+                         peak_src, stream)
     g_dense = torch.from_numpy(synth.student_t3(cfg.N, seed=0)).to(dev)
     act = torch.empty(cfg.K, dtype=torch.int64, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -414,7 +468,8 @@ def run_steps(args, B, MoELayer, dist, ws, rank, local, dev, cfg, inp, x, dy, wg
     trace = B.trace_summary()
     B.trace_enable(False)
     tot = sum(t for _, _, t in trace)
-    units = kernel_units(cfg, sddmm_pairs(layer, cfg))
+    pairs = sddmm_pairs(layer, cfg)
+    units = kernel_units(cfg, pairs)
     dominant = max(trace, key=lambda r: r[2])
     name, nl, tms = dominant
     avg_ms = tms / nl
@@ -432,7 +487,7 @@ def run_steps(args, B, MoELayer, dist, ws, rank, local, dev, cfg, inp, x, dy, wg
     roof["frac"] = roof["achieved"] / roof["peak"] if roof["achieved"] else None
     roof.update({"kernel": name, "kernel_ms": avg_ms, "traffic": ncu_traffic(name),
                  "peak_source": peak_src, "share": tms / tot if tot else None})
-    fl, by = algorithmic(cfg)
+    fl, by = algorithmic(cfg, pairs)
     step_roof_ms = max(fl / (tf_sus * 1e12), by / (hbm * 1e9)) * 1e3
 
     # ---- end to end: x, dy from pinned host memory, y and dx back, through the layer API
@@ -444,15 +499,10 @@ def run_steps(args, B, MoELayer, dist, ws, rank, local, dev, cfg, inp, x, dy, wg
     line = make_line(args, cfg, ws, ms, value, step_roof_ms, fl, by, roof, trace, tot,
                      importance, e2e_ms, nbytes, launches, clk, units, hbm, tf_burst)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        tokens = args.cpu_tokens
-        a = act.cpu().numpy()
-        p0 = master_values(inp, a, cfg.N_gu)
-        del layer, wgu, wd
-        inp = {k: v.astype(np.float64) for k, v in inp.items()}  # exact upcast of bf16 values
-        t = oracle_step_sample(cfg, inp, a, p0, tokens)
-        line["cpu_baseline"] = {"value": tokens / t, "unit": "tokens/s", "cores": cpu_threads(),
-                                "kind": "oracle",
-                                "sample": f"one step on the first {tokens} of {cfg.T} tokens"}
+        del layer, wgu, wd, inp
+        # the reference arm's measurement on the same sample (about 10 s of CPU work)
+        sec, _ = oracle_steps(args.workload, args.cpu_tokens, args.cpu_steps, 1)
+        line["cpu_baseline"] = cpu_baseline_entry(sec, args.cpu_tokens, cfg, args.cpu_steps)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist is not None:
@@ -498,14 +548,24 @@ def kernel_entry(n, l, t, tot, units, hbm, tf_burst):
     return e
 
 
-def workload_config(cfg, ws):
+def workload_config(name, cfg, ws):
     """The `config` object of the JSON line; both arms report the same one."""
-    return {"workload": f"{WORKLOAD} layer step", "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k,
-            "I": cfg.I, "active": cfg.K, "router": "fp32",
-            "optimizer": "SparseAdam (experts at the active set, router dense)",
-            "parallelism": f"dp{ws}" + (" (all-reduce of the compact gradients)"
-                                        if ws > 1 else ""),
-            "l2": "inputs larger than L2 (1.2 GB of expert weights per step)"}
+    c = {"workload": f"{name} layer step", "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k,
+         "I": cfg.I, "active": cfg.K, "router": "fp32",
+         "optimizer": "SparseAdam (experts at the active set, router dense)",
+         "parallelism": f"dp{ws}" + (" (all-reduce of the compact gradients)"
+                                     if ws > 1 else ""),
+         "l2": f"inputs larger than L2 ({cfg.N * 2 / 1e9:.1f} GB of expert weights per step)"}
+    if name == "qwen3_30b_a3b":
+        c["active_set"] = "importance selection of a seeded Student-t(3) dense gradient"
+    elif name == "qwen3_skewed":
+        c["routing"] = (f"Zipf({cfg.extra['zipf_s']}) expert loads, "
+                        f"{cfg.extra['dead_experts']} experts never routed")
+        c["active_set"] = (f"{int(HOT_FRAC * 100)}% on the {HOT_EXPERTS} most loaded experts, "
+                           "the rest uniform")
+    else:
+        c["active_set"] = "uniform"
+    return c
 
 
 def make_line(args, cfg, ws, ms, value, step_roof_ms, fl, by, roof, trace, tot, importance,
@@ -514,7 +574,7 @@ def make_line(args, cfg, ws, ms, value, step_roof_ms, fl, by, roof, trace, tot, 
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(cfg, ws),
+        "config": workload_config(args.workload, cfg, ws),
         "step_roofline": {"ms": step_roof_ms, "frac": step_roof_ms / ms,
                           "algorithmic_gflop": fl / 1e9, "algorithmic_gb": by / 1e9},
         "roofline": roof,
@@ -536,7 +596,10 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen3_30b_a3b", choices=WORKLOADS)
     ap.add_argument("--cpu-tokens", type=int, default=512)
+    ap.add_argument("--cpu-steps", type=int, default=8,
+                    help="oracle steps timed for the GPU arm's cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-importance", action="store_true",
                     help="skip the importance/RigL timing; use a seeded uniform 0.5%% mask")

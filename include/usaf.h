@@ -260,6 +260,24 @@ usaf_status usaf_moe_bwd_dense(const usaf_moe_shape* shape, usaf_dtype dtype, in
                                size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * usaf_moe_wgrad_dense - the dense expert weight gradient of usaf_moe_bwd_dense alone, for a
+ * micro-batch whose backward already ran (the importance phase's dense pass on a step that also
+ * trains: README, "Sparsity adapts"; A100 operations table, "RigL dense pass"). It reads the dh
+ * and the permuted dy that the preceding usaf_moe_bwd_sparse* or usaf_moe_bwd_dense call left in
+ * its workspace: pass that same workspace, with the same shape, dtype and routing, on the same
+ * stream and with no other backward call in between; gvec, the router gradient and dx are not
+ * recomputed.
+ *   x_perm_save, wa_save   as written by usaf_moe_fwd with that routing
+ *   g_dense     [N] fp32, 16-byte aligned; accumulate = 1 adds into it, 0 overwrites
+ *   dev_status  gets USAF_DEV_TIMEOUT if a tensor-core kernel gave up a wait (may be NULL)
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
+ * ------------------------------------------------------------------------------------------- */
+usaf_status usaf_moe_wgrad_dense(const usaf_moe_shape* shape, usaf_dtype dtype,
+                                 const usaf_routing* rt, const void* x_perm_save,
+                                 const void* wa_save, float* g_dense, int accumulate,
+                                 uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
  * usaf_sparse_adam_step - fused gather / Adam update / scatter over n entries (the README's
  * "SparseAdam (26M)" optimizer, torch.optim.SparseAdam semantics, no weight decay):
  *   m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*g^2;

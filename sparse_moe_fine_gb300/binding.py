@@ -85,6 +85,7 @@ _SIGS = {
     "usaf_moe_bwd_dense": (_INT, [_P, _INT, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                   _INT, _P, _P, _P, _P, _P, _SZ, _P]),
     "usaf_validate_active": (_INT, [_P, _I64, _I64, _P, _P]),
+    "usaf_moe_wgrad_dense": (_INT, [_P, _INT, _P, _P, _P, _P, _INT, _P, _P, _SZ, _P]),
     "usaf_moe_bwd_dlogit_offset": (_I64, [_P, _INT, _I64]),
     "usaf_diag_bounded_wait": (_INT, [_I64, _P, _P]),
     "usaf_reselect_full_workspace_size": (_SZ, [_I64, _I64]),
@@ -279,6 +280,16 @@ def moe_bwd_dense(s: Shape, x, w_router, w_gate_up, w_down, rt: Routing, x_perm,
         ctypes.byref(r), _ptr(logits), _ptr(x_perm), _ptr(h), _ptr(wa), _ptr(dy), _ptr(g_dense),
         int(accumulate), _ptr(g_router), _ptr(dx), _ptr(dw_slot), _ptr(dev_status), _ptr(ws),
         ws.numel(), _stream(stream)))
+
+
+def moe_wgrad_dense(s: Shape, rt: Routing, x_perm, wa, g_dense, ws, accumulate=0,
+                    dev_status=None, stream=None):
+    """usaf_moe_wgrad_dense: the dense expert gradient from the dh and permuted dy that the last
+    backward call left in `ws` (that call's workspace)."""
+    r = rt.c()
+    _check("usaf_moe_wgrad_dense", lib().usaf_moe_wgrad_dense(
+        ctypes.byref(s), _dt(x_perm), ctypes.byref(r), _ptr(x_perm), _ptr(wa), _ptr(g_dense),
+        int(accumulate), _ptr(dev_status), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def sparse_adam_step(idx, g, p, m, v, w_seg0, n_seg0, w_seg1, lr, beta1, beta2, eps, step,

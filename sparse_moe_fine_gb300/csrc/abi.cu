@@ -342,6 +342,29 @@ usaf_status usaf_moe_bwd_dense(const usaf_moe_shape* s, usaf_dtype dt, int renor
                         static_cast<cudaStream_t>(stream));
 }
 
+usaf_status usaf_moe_wgrad_dense(const usaf_moe_shape* s, usaf_dtype dt, const usaf_routing* rt,
+                                 const void* x_perm_save, const void* wa_save, float* g_dense,
+                                 int accumulate, uint32_t* dev_status, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  if (!shape_ok(s) || !dtype_ok(dt) || !routing_ok(rt)) return USAF_ERR_INVALID_ARG;
+  if (dt == USAF_BF16 && !tc_shape_ok(*s)) return USAF_ERR_UNSUPPORTED;
+  if (!x_perm_save || !wa_save || !g_dense) return USAF_ERR_INVALID_ARG;
+  if (accumulate != 0 && accumulate != 1) return USAF_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(g_dense) & 15) != 0) return USAF_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < usaf_moe_bwd_workspace_size(s, dt, 0)) return USAF_ERR_WORKSPACE;
+  MoeArgs a{};
+  a.s = *s;
+  a.dt = dt;
+  a.R_cap = usaf_routed_rows_capacity(s);
+  a.rt = *rt;
+  a.status = dev_status;
+  Carver c(ws);
+  BwdWs w;
+  bwd_ws_layout(*s, dt, 0, c, w);
+  return moe_wgrad_dense_launch(a, x_perm_save, wa_save, g_dense, accumulate, w,
+                                static_cast<cudaStream_t>(stream));
+}
+
 usaf_status usaf_sparse_adam_step(int64_t n, const int64_t* idx, const float* g, float* p,
                                   float* m, float* v, void* w_seg0, int64_t n_seg0, void* w_seg1,
                                   usaf_dtype w_dtype, double lr, double beta1, double beta2,

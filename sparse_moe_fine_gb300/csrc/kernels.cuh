@@ -27,6 +27,7 @@ struct FwdWs {
 };
 struct BwdWs {
   float* dw;          // [T*k] when the caller gives no dw_slot
+  float* dw_part;     // [4 * ceil(I / 128)][T*k] per-tile partial sums of dw (tensor-core path)
   float* dl;          // [T*k] dlogit at the selected experts (renorm = 1)
   float* dl_perm;     // [R_cap] the same in permuted row order
   float* dlogit;      // [T,E] dense dlogit (renorm = 0)
@@ -67,6 +68,8 @@ usaf_status moe_bwd_launch(const MoeArgs& a, int renorm, const float* logits, co
                            int64_t K, float* g_act, float* g_router, void* dx, float* dw_slot,
                            float* g_dense, int accumulate, uint32_t* dev_status, BwdWs& w,
                            cudaStream_t st);
+usaf_status moe_wgrad_dense_launch(const MoeArgs& a, const void* x_perm, const void* wa,
+                                   float* g_dense, int accumulate, BwdWs& w, cudaStream_t st);
 
 // tensor-core (tcgen05) grouped GEMM stages, bf16 only
 bool tc_shape_ok(const usaf_moe_shape& s);
@@ -75,8 +78,9 @@ usaf_status tc_router_logits(const usaf_moe_shape& s, const void* x, const float
 usaf_status tc_fwd_gate_up(const MoeArgs& a, const void* xT, void* hT, void* waT,
                            cudaStream_t st);
 usaf_status tc_fwd_down(const MoeArgs& a, const void* wa, float* y_acc, cudaStream_t st);
-usaf_status tc_bwd_gvec(const MoeArgs& a, const void* dyT, const void* hT, void* dhT, float* dw,
-                        cudaStream_t st);
+// dw_part [4 * ceil(I / 128)][T*k]: one partial of dw per (M tile, row quarter, slot)
+usaf_status tc_bwd_gvec(const MoeArgs& a, const void* dyT, const void* hT, void* dhT,
+                        float* dw_part, cudaStream_t st);
 usaf_status tc_bwd_dx(const MoeArgs& a, const void* dh, float* dx_acc, cudaStream_t st);
 // dense expert weight gradient g[e] (a_rows x b_rows, fp32) = aT . bT^T over each expert's tokens
 usaf_status tc_wgrad_dense(const MoeArgs& a, const void* aT, int64_t a_rows, const void* bT,

@@ -634,17 +634,34 @@ __global__ void f32_to_kernel(const float* __restrict__ src, T* __restrict__ dst
     dst[i] = from_f32<T>(src[i]);
 }
 
+// dw of slot q: the sum of its nparts partials in order (tensor-core path), else dw[q] as written;
+// the summed value is stored to dw[q]
+__device__ __forceinline__ float slot_dw(float* __restrict__ dw, const float* __restrict__ part,
+                                         int nparts, int64_t n_slots, int64_t q) {
+  if (nparts == 0) return dw[q];
+  float d = 0.f;
+  for (int i = 0; i < nparts; ++i) d += part[(int64_t)i * n_slots + q];
+  dw[q] = d;
+  return d;
+}
+
 // dlogit at the selected experts, renormalised routing: w_j (dw_j - sum_i w_i dw_i).
-__global__ void dlogit_sel_kernel(const float* __restrict__ w, const float* __restrict__ dw,
+__global__ void dlogit_sel_kernel(const float* __restrict__ w, float* __restrict__ dw,
+                                  const float* __restrict__ dw_part, int nparts,
                                   const int32_t* __restrict__ slot_row, int Tn, int k,
                                   float* __restrict__ dl, float* __restrict__ dl_perm) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= Tn) return;
+  const int64_t n_slots = (int64_t)Tn * k;
+  float dws[32];
   float s = 0.f;
-  for (int j = 0; j < k; ++j) s = fmaf(w[(int64_t)t * k + j], dw[(int64_t)t * k + j], s);
+  for (int j = 0; j < k; ++j) {
+    dws[j] = slot_dw(dw, dw_part, nparts, n_slots, (int64_t)t * k + j);
+    s = fmaf(w[(int64_t)t * k + j], dws[j], s);
+  }
   for (int j = 0; j < k; ++j) {
     const int64_t q = (int64_t)t * k + j;
-    const float d = w[q] * (dw[q] - s);
+    const float d = w[q] * (dws[j] - s);
     dl[q] = d;
     dl_perm[slot_row[q]] = d;  // the same value at the slot's permuted row
   }
@@ -653,12 +670,17 @@ __global__ void dlogit_sel_kernel(const float* __restrict__ w, const float* __re
 // dense dlogit for softmax-over-all-E routing: p_e (dw_e [e selected] - sum_i p_{e_i} dw_i).
 __global__ void dlogit_dense_kernel(const float* __restrict__ logits,
                                     const int32_t* __restrict__ idx,
-                                    const float* __restrict__ w, const float* __restrict__ dw,
-                                    int Tn, int E, int k, float* __restrict__ dlogit) {
+                                    const float* __restrict__ w, float* __restrict__ dw,
+                                    const float* __restrict__ dw_part, int nparts, int Tn, int E,
+                                    int k, float* __restrict__ dlogit) {
   const int t = blockIdx.x;
   const float* l = logits + (int64_t)t * E;
   __shared__ float red[32];
   __shared__ float sh_mx, sh_sum, sh_s;
+  __shared__ float s_dw[32];
+  if (threadIdx.x < k)
+    s_dw[threadIdx.x] =
+        slot_dw(dw, dw_part, nparts, (int64_t)Tn * k, (int64_t)t * k + threadIdx.x);
   float mx = -INFINITY;
   for (int e = threadIdx.x; e < E; e += blockDim.x) mx = fmaxf(mx, l[e]);
   for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -681,7 +703,7 @@ __global__ void dlogit_dense_kernel(const float* __restrict__ logits,
     for (int i = 0; i < (int)(blockDim.x >> 5); ++i) s2 += red[i];
     sh_sum = s2;
     float s = 0.f;
-    for (int j = 0; j < k; ++j) s = fmaf(w[(int64_t)t * k + j], dw[(int64_t)t * k + j], s);
+    for (int j = 0; j < k; ++j) s = fmaf(w[(int64_t)t * k + j], s_dw[j], s);
     sh_s = s;
   }
   __syncthreads();
@@ -689,7 +711,7 @@ __global__ void dlogit_dense_kernel(const float* __restrict__ logits,
     float p = expf(l[e] - sh_mx) / sh_sum;
     float d = 0.f;
     for (int j = 0; j < k; ++j)
-      if (idx[(int64_t)t * k + j] == e) d = dw[(int64_t)t * k + j];
+      if (idx[(int64_t)t * k + j] == e) d = s_dw[j];
     dlogit[(int64_t)t * E + e] = p * (d - sh_s);
   }
 }
@@ -782,6 +804,7 @@ void bwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, int64_t K, Carver& c,
   const int64_t R_cap = usaf_routed_rows_capacity(&s);
   const size_t es = dt == USAF_BF16 ? 2 : 4;
   w.dw = c.take<float>(s.T * s.k);
+  w.dw_part = dt == USAF_BF16 ? c.take<float>(4 * ceil_div(s.I, 128) * s.T * s.k) : nullptr;
   w.dl = c.take<float>(s.T * s.k);
   w.dl_perm = c.take<float>(R_cap);
   w.dlogit = c.take<float>(s.T * s.E);
@@ -911,13 +934,13 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
   // S6: gvec, dw, dh
   {
     USAF_TRACE("gather_dy", st);
-    // also zeroes dw and the dx accumulator and writes the tile plan
-    const GatherExtra ex{dw, s.T * s.k, dx ? w.dx_acc : nullptr, dx ? s.T * s.H : 0,
+    // also zeroes the dx accumulator and writes the tile plan
+    const GatherExtra ex{dx ? w.dx_acc : nullptr, dx ? s.T * s.H : 0, nullptr, 0,
                          a.rt.expert_offset, (int)s.E, a.dt == USAF_BF16 ? w.plan : nullptr};
     USAF_TRY(gather_t<T>(a, dy, dyT, st, ex));
   }
   if (a.dt == USAF_BF16) {
-    USAF_TRY(tc_bwd_gvec(a, dyT, hT, dhT, dw, st));
+    USAF_TRY(tc_bwd_gvec(a, dyT, hT, dhT, w.dw_part, st));
   } else {
     USAF_TRACE("simt_gvec", st);
     ProbGvec<T> p{dyT, static_cast<const T*>(a.w_down), w.gvec, cnt, off, H, I, a.R_cap};
@@ -928,19 +951,20 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
                                                                  off + E, I, a.R_cap, dhT, dw);
     USAF_CHECK_LAUNCH();
   }
-  // S7: router gradient
+  // S7: router gradient (on the tensor-core path dw is first summed from its tile partials)
+  const int nparts = a.dt == USAF_BF16 ? 4 * (int)ceil_div(s.I, 128) : 0;
   {
     USAF_TRACE("router_bwd", st);
     if (renorm) {
       dlogit_sel_kernel<<<(unsigned)ceil_div(Tn, 128), 128, 0, st>>>(
-          a.rt.topk_w, dw, a.rt.slot_row, Tn, k, w.dl, w.dl_perm);
+          a.rt.topk_w, dw, w.dw_part, nparts, a.rt.slot_row, Tn, k, w.dl, w.dl_perm);
       USAF_CHECK_LAUNCH();
       g_router_sel_kernel<T><<<(unsigned)ceil_div(s.E * s.H, 32), 256, 0, st>>>(
           xT, w.dl_perm, cnt, off, E, H, a.R_cap, g_router, accumulate, dev_status);
       USAF_CHECK_LAUNCH();
     } else {
       dlogit_dense_kernel<<<(unsigned)Tn, 128, 0, st>>>(logits, a.rt.topk_idx, a.rt.topk_w, dw,
-                                                        Tn, E, k, w.dlogit);
+                                                        w.dw_part, nparts, Tn, E, k, w.dlogit);
       USAF_CHECK_LAUNCH();
       g_router_dense_kernel<T><<<dim3((unsigned)ceil_div(H, 128), (unsigned)E), 128, 0, st>>>(
           static_cast<const T*>(a.x), w.dlogit, Tn, E, H, g_router, accumulate, dev_status);
@@ -990,6 +1014,37 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
       USAF_CHECK_LAUNCH();
     }
   }
+  return USAF_OK;
+}
+
+// The dense expert weight gradient alone, from the dh^T and dy^T that the preceding backward call
+// left in the same workspace (the importance phase's dense pass after a sparse backward).
+usaf_status moe_wgrad_dense_launch(const MoeArgs& a0, const void* x_perm, const void* wa,
+                                   float* g_dense, int accumulate, BwdWs& w, cudaStream_t st) {
+  MoeArgs a = a0;
+  a.plan = w.plan;
+  a.wperm = w.wperm;
+  const auto& s = a.s;
+  const int H = (int)s.H, I = (int)s.I, E = (int)s.E;
+  const int64_t Ngu = s.E * 2 * s.I * s.H;
+  if (a.dt == USAF_BF16) {
+    using T = __nv_bfloat16;
+    const T* dhT = static_cast<const T*>(w.dh);
+    const T* dyT = static_cast<const T*>(w.dy_perm);
+    USAF_TRY(tc_wgrad_dense(a, dhT, 2 * I, x_perm, H, g_dense, accumulate, st));
+    USAF_TRY(tc_wgrad_dense(a, dyT, H, wa, I, g_dense + Ngu, accumulate, st));
+    return USAF_OK;
+  }
+  USAF_TRACE("simt_wgrad_dense", st);
+  const float* dhT = static_cast<const float*>(w.dh);
+  const float* dyT = static_cast<const float*>(w.dy_perm);
+  const int32_t* off = a.rt.expert_offset;
+  dense_wgrad_simt_kernel<float><<<grid_dim_for(Ngu), 256, 0, st>>>(
+      dhT, 2 * I, static_cast<const float*>(x_perm), H, off, E, a.R_cap, g_dense, accumulate);
+  USAF_CHECK_LAUNCH();
+  dense_wgrad_simt_kernel<float><<<grid_dim_for(Ngu / 2), 256, 0, st>>>(
+      dyT, H, static_cast<const float*>(wa), I, off, E, a.R_cap, g_dense + Ngu, accumulate);
+  USAF_CHECK_LAUNCH();
   return USAF_OK;
 }
 

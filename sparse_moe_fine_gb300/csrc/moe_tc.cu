@@ -60,7 +60,8 @@ struct Params {
   __nv_bfloat16* h;       // h^T out (S4)
   __nv_bfloat16* wa;      // (w*A)^T out (S4)
   float* acc_out;         // y_acc (S5), dx_acc (S8) or the router logits
-  float* dw;              // S6
+  float* dw_part;         // S6: dw partial sums [4 * MT][n_slots] (row quarter of an M tile)
+  int64_t n_slots;        // T * k
   __nv_bfloat16* dh;      // dh^T out (S6)
   const __nv_bfloat16* hin;  // h^T in (S6)
   const float* wperm;        // routing weight per permuted row (0 in padding)
@@ -474,8 +475,11 @@ __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32
           return ib + rr < I ? dbase + (int64_t)(I + ib + rr) * p.R_cap : nullptr;
         });
       }
+      // this warp's 32 rows of the tile: one partial per (M tile, row quarter, slot), summed
+      // in a fixed order later, so dw does not depend on which tile finished first
       const float dwsum = transpose_reduce32(v, lane);
-      if (slot >= 0) atomicAdd(&p.dw[slot], dwsum);
+      if (slot >= 0)
+        p.dw_part[((int64_t)(ti.m0 / BM) * 4 + (row >> 5)) * p.n_slots + slot] = dwsum;
       if (ch + 2 < nch) {
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -1409,7 +1413,8 @@ usaf_status tc_fwd_down(const MoeArgs& a, const void* waT, float* y_acc, cudaStr
   return launch<V_DOWN>(ma, mb, p, st);
 }
 
-usaf_status tc_bwd_gvec(const MoeArgs& a, const void* dyT, const void* hT, void* dhT, float* dw,
+usaf_status tc_bwd_gvec(const MoeArgs& a, const void* dyT, const void* hT, void* dhT,
+                        float* dw_part,
                         cudaStream_t st) {
   CUtensorMap ma, mb;
   if (!map_2d(&ma, a.w_down, a.s.I, a.s.E * a.s.H, 64, 64) || !map_tokens(&mb, dyT, a.s.H, a.R_cap))
@@ -1418,7 +1423,8 @@ usaf_status tc_bwd_gvec(const MoeArgs& a, const void* dyT, const void* hT, void*
   p.MT = (int)ceil_div(a.s.I, BM);
   p.hin = static_cast<const __nv_bfloat16*>(hT);
   p.dh = static_cast<__nv_bfloat16*>(dhT);
-  p.dw = dw;
+  p.dw_part = dw_part;
+  p.n_slots = a.s.T * a.s.k;
   return launch<V_GVEC>(ma, mb, p, st);
 }
 

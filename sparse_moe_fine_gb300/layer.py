@@ -112,6 +112,36 @@ class MoELayer:
                                   dtype=torch.uint8, device=self.dev)
         self._graphs = {}  # captured steps hold the old active set's pointers
 
+    # ------------------------------------------------------------------ checkpoint / resume
+    def checkpoint(self) -> dict:
+        """The layer's whole training state as CPU tensors and host scalars: expert and router
+        weights, the active set with its fp32 master copy and Adam moments, the router's Adam
+        state, the step count and the optimizer settings. Waits for the last update. A layer
+        rebuilt from it (from_checkpoint) continues exactly as this one would."""
+        self.wait_optimizer()
+        torch.cuda.current_stream(self.dev).synchronize()
+        cpu = lambda t: t.detach().to("cpu", copy=True)
+        return {"shape": (self.T, self.H, self.E, self.k, self.I),
+                "w_gate_up": cpu(self.w_gate_up), "w_down": cpu(self.w_down),
+                "w_router": cpu(self.w_router), "act": cpu(self.act), "p": cpu(self.p),
+                "m": cpu(self.m), "v": cpu(self.v), "r_p": cpu(self.r_p), "r_m": cpu(self.r_m),
+                "r_v": cpu(self.r_v), "step_count": self.step_count, "lr": self.lr,
+                "betas": tuple(self.betas), "eps": self.eps, "renorm": self.renorm}
+
+    @classmethod
+    def from_checkpoint(cls, ck: dict, device="cuda", group=None) -> "MoELayer":
+        T, H, E, k, I = ck["shape"]
+        d = torch.device(device)
+        L = cls(T, H, E, k, I, ck["w_gate_up"].to(d), ck["w_down"].to(d), ck["w_router"].to(d),
+                ck["act"].to(d), lr=ck["lr"], betas=ck["betas"], eps=ck["eps"],
+                renorm=ck["renorm"], device=d, group=group)
+        L.set_active(ck["act"].to(d), ck["p"].to(d), ck["m"].to(d), ck["v"].to(d))
+        L.r_p.copy_(ck["r_p"])
+        L.r_m.copy_(ck["r_m"])
+        L.r_v.copy_(ck["r_v"])
+        L.step_count = int(ck["step_count"])
+        return L
+
     # ------------------------------------------------------------------ the step
     def _check_tokens(self, **ts):
         """The library reads and writes [T, H] token tensors through bare pointers, so their

@@ -174,6 +174,35 @@ def skew_bias(E: int, zipf_s: float, dead: int, seed: int) -> np.ndarray:
     return b
 
 
+def _union_sample(ranges, n: int, rng) -> np.ndarray:
+    """n distinct indices drawn uniformly from a union of disjoint [lo, hi) ranges, sorted."""
+    sizes = np.array([hi - lo for lo, hi in ranges], dtype=np.int64)
+    starts = np.concatenate([[0], np.cumsum(sizes)[:-1]])
+    got = np.empty(0, dtype=np.int64)
+    while got.size < n:
+        got = np.unique(np.concatenate([got, rng.integers(0, sizes.sum(), n - got.size + 64)]))
+    got = got[np.sort(rng.permutation(got.size)[:n])]
+    r = np.searchsorted(starts, got, side="right") - 1
+    return np.array([lo for lo, _ in ranges], dtype=np.int64)[r] + (got - starts[r])
+
+
+def concentrated_mask(cfg: "MoEConfig", hot_experts, hot_frac: float, seed: int) -> np.ndarray:
+    """The skewed workload's active set: hot_frac of K uniformly over the weights (both tensors)
+    of the given experts, the rest uniformly over the other experts' weights; sorted."""
+    rng = np.random.default_rng([seed + STREAM["mask"], 2])
+    hot = sorted(set(int(e) for e in hot_experts))
+    cold = [e for e in range(cfg.E) if e not in set(hot)]
+    pgu, pd = 2 * cfg.I * cfg.H, cfg.H * cfg.I
+
+    def ranges(es):
+        return ([(e * pgu, (e + 1) * pgu) for e in es] +
+                [(cfg.N_gu + e * pd, cfg.N_gu + (e + 1) * pd) for e in es])
+    n_hot = int(hot_frac * cfg.K)
+    a = _union_sample(ranges(hot), n_hot, rng)
+    b = _union_sample(ranges(cold), cfg.K - n_hot, rng)
+    return np.sort(np.concatenate([a, b]))
+
+
 def apply_skew(inputs: dict, bias: np.ndarray) -> None:
     """Realise a router logit bias without a bias term: x[:,0] := 1 and w_router[:,0] := bias."""
     inputs["x"][:, 0] = 1.0

@@ -49,7 +49,6 @@ class StackTrainer:
         self.step_no = 0
         self.history = []  # per step: lr, status words, turnover (device tensors until read)
         self._g_dense = [None] * len(self.layers)
-        self._g_r_scratch = [torch.zeros_like(L.g_router) for L in self.layers]
 
     # ------------------------------------------------------------------ one micro-batch
     def _forward(self, x):
@@ -70,14 +69,12 @@ class StackTrainer:
                L.g_act, L.g_router, dx=dx, logits=L.logits, renorm=L.renorm,
                dev_status=L.status, ws=L.ws_bwd)
             if dense:
-                # the importance phase's dense gradient of this micro-batch, accumulated; its
-                # router gradient goes to a scratch buffer (the sparse call above owns g_router)
+                # the importance phase's dense gradient of this micro-batch, accumulated, from
+                # the dh and permuted dy the sparse call just left in the layer's workspace
                 if self._g_dense[i] is None:
                     self._g_dense[i] = torch.zeros(L.N, device=L.dev)
-                B.moe_bwd_dense(L.s, x, L.w_router, L.w_gate_up, L.w_down, L.rt, L.x_perm, L.h,
-                                L.wa, dy, self._g_dense[i], self._g_r_scratch[i], accumulate=1,
-                                dx=dx, logits=L.logits, renorm=L.renorm, dev_status=L.status,
-                                ws=L.ws_bwd)
+                B.moe_wgrad_dense(L.s, L.rt, L.x_perm, L.wa, self._g_dense[i], L.ws_bwd,
+                                  accumulate=1, dev_status=L.status)
             dy = L.dx
 
     # ------------------------------------------------------------------ one optimizer step
@@ -93,8 +90,6 @@ class StackTrainer:
         for i, L in enumerate(self.layers):
             L.status = L.status2[L.step_count % 2:L.step_count % 2 + 1]
             L.status.zero_()
-            if dense:
-                self._g_r_scratch[i].zero_()
         for j, (x, dy) in enumerate(zip(x_micro, dy_micro)):
             inputs = self._forward(x)
             self._backward(inputs, dy, first=(j == 0), dense=dense)

@@ -98,7 +98,7 @@ def test_clock_summary_parses_throttle_reasons(bench):
 
 def test_json_line_carries_every_contract_key(bench):
     import argparse
-    args = argparse.Namespace(steps=200, warmup=5)
+    args = argparse.Namespace(steps=200, warmup=5, workload="qwen3_30b_a3b")
     clk = bench.ClockSampler(0)
     clk.lines = ["2070, 2070, 900, 0x0, Not Active, Not Active, Not Active, Not Active"]
     fl, by = bench.algorithmic(CFG)
@@ -113,7 +113,7 @@ def test_json_line_carries_every_contract_key(bench):
                 "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
                 "roofline", "e2e", "gpu_launches", "clocks"):
         assert key in line, key
-    assert line["config"] == bench.workload_config(CFG, 1)
+    assert line["config"] == bench.workload_config("qwen3_30b_a3b", CFG, 1)
     assert line["config"]["workload"] == "qwen3_30b_a3b layer step"
     assert line["gpu_launches"] == 22 * 200
     assert line["e2e"]["h2d_bytes_per_step"] == 2 * nbytes  # x and dy in
@@ -125,3 +125,26 @@ def test_json_line_carries_every_contract_key(bench):
     skipped = bench.make_line(args, CFG, 1, 1.31, 3.1e6, 0.464, fl, by, roof, trace, 92.2, None,
                               None, nbytes, 22, clk, units, 6779.0, 1918.6)
     assert skipped["e2e"] is None
+
+
+def test_other_workloads_configs_and_active_sets(bench):
+    """The skewed and Mixtral-shaped workloads: their JSON config names them, and the skewed
+    layer's drawn active set puts 80% of K on the 16 experts with the largest logit offsets."""
+    import numpy as np
+    sk = synth.CONFIGS["qwen3_skewed"]
+    c = bench.workload_config("qwen3_skewed", sk, 1)
+    assert c["workload"] == "qwen3_skewed layer step" and c["T"] == 16384
+    assert "Zipf" in c["routing"] and "16 most loaded" in c["active_set"]
+    act = bench.fixed_active_set("qwen3_skewed", sk)
+    assert act.size == sk.K and (np.diff(act) > 0).all()
+    hot = set(np.argsort(-bench.skew_bias(sk), kind="stable")[:16].tolist())
+    gu = act < sk.N_gu
+    e = np.where(gu, act // (2 * sk.I * sk.H), (act - sk.N_gu) // (sk.H * sk.I))
+    assert np.isin(e, list(hot)).sum() == int(0.8 * sk.K)
+    mx = synth.CONFIGS["mixtral_8x7b"]
+    assert bench.workload_config("mixtral_8x7b", mx, 1)["active_set"] == "uniform"
+    assert mx.K == 7_046_431
+    # the masked-gradient term of the step counts the live routing when given
+    fl_u, _ = bench.algorithmic(sk)
+    fl_l, _ = bench.algorithmic(sk, sddmm_pairs=10**10)
+    assert fl_l - fl_u == pytest.approx(2 * (10**10 - sk.K * sk.T * sk.k / sk.E))

@@ -122,3 +122,7 @@ def test_reference_arm_under_torchrun_prints_once():
     assert d["n_gpus"] == 2 and d["config"]["parallelism"].startswith("dp2")
     assert d["e2e"] == {"value": d["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}
+    # the time of what ran: one 8-token step, its own rate; the full-batch figure apart
+    assert d["ms_per_step"] == pytest.approx(1e3 * 8 / d["value"], rel=1e-9)
+    assert d["est_ms_per_full_batch"] == pytest.approx(d["ms_per_step"] * 4096 / 8, rel=1e-9)
+    assert d["cpu_baseline"]["value"] == d["value"]

@@ -186,32 +186,11 @@ def test_qwen3_shaped_layer_sampled():
     assert np.isfinite(got["g_act"]).all()
 
 
-def _union_sample(ranges, n, rng):
-    """n distinct flat indices drawn uniformly from a union of disjoint [lo, hi) ranges."""
-    sizes = np.array([hi - lo for lo, hi in ranges], dtype=np.int64)
-    starts = np.concatenate([[0], np.cumsum(sizes)[:-1]])
-    got = np.empty(0, dtype=np.int64)
-    while got.size < n:
-        got = np.unique(np.concatenate([got, rng.integers(0, sizes.sum(), n - got.size + 64)]))
-    got = got[np.sort(rng.permutation(got.size)[:n])]
-    r = np.searchsorted(starts, got, side="right") - 1
-    return np.array([lo for lo, _ in ranges], dtype=np.int64)[r] + (got - starts[r])
-
-
 def skewed_mask(cfg, counts, seed):
     """The skewed workload's active set: 80% of K uniformly over the weights of the 16 most
     loaded experts, the rest over the others' (both tensors of each expert)."""
-    rng = np.random.default_rng(seed)
-    hot = set(np.argsort(-counts, kind="stable")[:16].tolist())
-    pgu, pd = 2 * cfg.I * cfg.H, cfg.H * cfg.I
-
-    def ranges(es):
-        return ([(e * pgu, (e + 1) * pgu) for e in es] +
-                [(cfg.N_gu + e * pd, cfg.N_gu + (e + 1) * pd) for e in es])
-    n_hot = int(0.8 * cfg.K)
-    a = _union_sample(ranges(sorted(hot)), n_hot, rng)
-    b = _union_sample(ranges([e for e in range(cfg.E) if e not in hot]), cfg.K - n_hot, rng)
-    return np.sort(np.concatenate([a, b]))
+    hot = np.argsort(-counts, kind="stable")[:16]
+    return synth.concentrated_mask(cfg, hot, 0.8, seed)
 
 
 @pytest.mark.parametrize("name,ntok", [("qwen3_skewed", 256), ("mixtral_8x7b", 48)])
@@ -556,3 +535,52 @@ def test_graphed_steps_match_oracle():
         keep = np.ones(cfg.N, bool)
         keep[act_np] = False
         assert np.array_equal(w_all[keep], w_before[keep])
+
+
+@pytest.mark.parametrize("bf16", [True, False])
+def test_wgrad_dense_from_the_sparse_backward_workspace(bf16):
+    """usaf_moe_wgrad_dense after usaf_moe_bwd_sparse (same workspace) gives the dense gradient
+    usaf_moe_bwd_dense forms, bit for bit (the same kernels on the same dh and dy), and the
+    oracle's within the layer's bound."""
+    dev = device()
+    if bf16:
+        cfg = synth.small_config("wg_reuse", T=600, H=192, E=4, k=2, I=192, bf16=True)
+    else:
+        cfg = synth.CONFIGS["tiny_fp32"]
+    inp = synth.moe_inputs(cfg, seed=31)
+    logits = oracle.router_logits(inp["x"], inp["w_router"])
+    s = B.shape(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I)
+    dt = torch.bfloat16 if bf16 else torch.float32
+    x, wr = to_dev(inp["x"], dev, bf16), to_dev(inp["w_router"], dev)
+    wgu, wd = to_dev(inp["w_gate_up"], dev, bf16), to_dev(inp["w_down"], dev, bf16)
+    dy, li = to_dev(inp["dy"], dev, bf16), to_dev(logits, dev)
+    rt = B.Routing.empty(s, dev)
+    B.route_topk(s, x, wr, rt, logits_in=li)
+    cap = B.routed_rows_capacity(s)
+    xp = torch.empty(cfg.H, cap, dtype=dt, device=dev)
+    h = torch.empty(2 * cfg.I, cap, dtype=dt, device=dev)
+    wa = torch.empty(cfg.I, cap, dtype=dt, device=dev)
+    y = torch.empty(cfg.T, cfg.H, dtype=dt, device=dev)
+    B.moe_fwd(s, x, wgu, wd, rt, xp, h, wa, y)
+    act = to_dev(synth.uniform_mask(cfg.N, cfg.K, seed=31), dev)
+    g_act = torch.empty(act.numel(), device=dev)
+    g_r = torch.empty(cfg.E, cfg.H, device=dev)
+    dtc = B.BF16 if bf16 else B.F32
+    ws = torch.empty(B.moe_bwd_workspace_size(s, dtc, act.numel()), dtype=torch.uint8,
+                     device=dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    B.moe_bwd_sparse(s, x, wr, wgu, wd, rt, xp, h, wa, dy, act, g_act, g_r, logits=li,
+                     dev_status=st, ws=ws)
+    g1 = torch.full((cfg.N,), float("nan"), device=dev)
+    B.moe_wgrad_dense(s, rt, xp, wa, g1, ws, accumulate=0, dev_status=st)
+    g2 = torch.full((cfg.N,), float("nan"), device=dev)
+    g_r2 = torch.empty(cfg.E, cfg.H, device=dev)
+    B.moe_bwd_dense(s, x, wr, wgu, wd, rt, xp, h, wa, dy, g2, g_r2, accumulate=0, logits=li,
+                    dev_status=st)
+    B.moe_wgrad_dense(s, rt, xp, wa, g1, ws, accumulate=1, dev_status=st)  # adds a second copy
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    g1n, g2n = g1.cpu().numpy(), g2.cpu().numpy()
+    assert np.array_equal(g1n, 2 * g2n) or rel_l2(g1n, 2 * g2n) <= 1e-6
+    ref, _ = oracle_dense(cfg, inp, logits)
+    assert rel_l2(g2n, ref) <= (1e-2 if bf16 else 1e-5)

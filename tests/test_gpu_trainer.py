@@ -111,3 +111,33 @@ def test_reselection_every_two_steps(mode):
         assert 0.0 < met[1]["turnover"][0] <= 1.0
         assert np.setdiff1d(new, act).size > 0
     assert met[1]["load_balance"][0] >= 1.0
+
+
+def test_checkpoint_resume_continues_bit_exactly():
+    """Save after one step, rebuild the layer from the saved state (through torch.save and
+    torch.load), run two more steps: every piece of training state equals, bit for bit, that of a
+    layer that ran the three steps without interruption. (The state evolves without
+    order-dependent sums: dw is summed from per-tile partials in a fixed order; only y and dx,
+    which are outputs, are summed by atomics.)"""
+    import io
+    dev = device()
+    xs, dys = zip(*[micro(40 + i) for i in range(3)])
+    bf = lambda a: torch.from_numpy(a).to(dev).to(torch.bfloat16)
+    a, _, _ = make_layer(dev, 41)
+    b, _, _ = make_layer(dev, 41)
+    for i in range(3):
+        ya, _ = a.train_step(bf(xs[i]), bf(dys[i]))
+    b.train_step(bf(xs[0]), bf(dys[0]))
+    buf = io.BytesIO()
+    torch.save(b.checkpoint(), buf)
+    del b
+    buf.seek(0)
+    c = MoELayer.from_checkpoint(torch.load(buf), device=dev)
+    assert c.step_count == 1
+    for i in (1, 2):
+        yc, _ = c.train_step(bf(xs[i]), bf(dys[i]))
+    ka, kc = a.checkpoint(), c.checkpoint()
+    for key in ("w_gate_up", "w_down", "w_router", "act", "p", "m", "v", "r_p", "r_m", "r_v"):
+        assert torch.equal(ka[key], kc[key]), key
+    assert ka["step_count"] == kc["step_count"] == 3
+    assert rel_l2(yc.float().cpu().numpy(), ya.float().cpu().numpy()) <= 1e-3

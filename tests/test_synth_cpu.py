@@ -73,3 +73,17 @@ def test_workload_sizes_follow_the_recipe():
     assert (q.N_gu, q.N, q.K) == (402_653_184, 603_979_776, 3_019_899)
     mx = synth.CONFIGS["mixtral_8x7b"]
     assert (mx.N_gu, mx.N, mx.K) == (939_524_096, 1_409_286_144, 7_046_431)
+
+
+def test_concentrated_mask():
+    """hot_frac of K on the given experts' weights (both tensors), the rest on the others; sorted,
+    distinct, inside [0, N), and the same draw for the same seed."""
+    cfg = synth.small_config("conc", T=64, H=64, E=16, k=2, I=32, frac=0.05)
+    hot = [3, 7, 11]
+    a = synth.concentrated_mask(cfg, hot, 0.8, seed=4)
+    assert a.size == cfg.K and (np.diff(a) > 0).all() and a[0] >= 0 and a[-1] < cfg.N
+    gu = a < cfg.N_gu
+    e = np.where(gu, a // (2 * cfg.I * cfg.H), (a - cfg.N_gu) // (cfg.H * cfg.I))
+    assert np.isin(e, hot).sum() == int(0.8 * cfg.K)
+    assert gu[np.isin(e, hot)].any() and (~gu[np.isin(e, hot)]).any()
+    assert np.array_equal(a, synth.concentrated_mask(cfg, hot, 0.8, seed=4))
