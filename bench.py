@@ -412,6 +412,16 @@ def run(args):
     ev[1].record()
     torch.cuda.synchronize()
     resel_ms = ev[0].elapsed_time(ev[1]) / reps
+    # per-stage device times of one more selection and one more RigL swap (event trace)
+    B.trace_enable(True)
+    B.importance_select(g_dense, cfg.K, act, dev_status=st, ws=ws_sel)
+    torch.cuda.synchronize()
+    sel_stages = {n: 1e3 * t / max(1, c) for n, c, t in B.trace_summary()}
+    B.trace_enable(True)
+    rigl()
+    torch.cuda.synchronize()
+    rigl_stages = {n: 1e3 * t for n, c, t in B.trace_summary()}
+    B.trace_enable(False)
     del ws_rigl, ws_sel, outs, ws_res
     g_bytes = cfg.N * 4
     importance = {
@@ -421,6 +431,7 @@ def run(args):
         "reselect_full_ms": resel_ms, "reselect_full_kept": int(nk.item()),
         "dense_grad_bwd_ms": dense_ms,
         "select_exact_path": bool(int(st.item()) & B.DEV_SELECT_EXACT_PATH),
+        "select_stages_us": sel_stages, "rigl_stages_us": rigl_stages,
         "N": cfg.N, "K": cfg.K, "D": D}
     del g_dense, layer
     torch.cuda.empty_cache()

@@ -328,6 +328,9 @@ usaf_status usaf_importance_select(const float* g, int64_t N, int64_t K, int64_t
  *   w_seg0/n_seg0/w_seg1/w_dtype   dense weights, as for usaf_sparse_adam_step
  *   new_idx, p_out, m_out, v_out   [K] out; must not overlap the inputs
  *   n_swapped  [1] int64 out: number of entries of act_idx not in new_idx (= D)
+ * The drop selection runs on a private stream forked from and joined back to `stream` (created
+ * and released inside the call), so it overlaps the pass over g; the call's work as a whole is
+ * still ordered on `stream`.
  * Limits: 0 <= D <= K, D <= N - K, N < 2^32. Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
  * ------------------------------------------------------------------------------------------- */
 size_t usaf_rigl_swap_workspace_size(int64_t N, int64_t K, int64_t D);

@@ -105,10 +105,21 @@ def _expert_rows(topk_idx, e):
     return rows, slots
 
 
-def moe_forward(x, w_gate_up, w_down, topk_idx, topk_w):
+def _keep(a):
+    return a
+
+
+def moe_forward(x, w_gate_up, w_down, topk_idx, topk_w, rnd=None):
     """Y[t] = sum_j w[t,j] * down[e_j] . (silu(gate) * up), [gate; up] = gate_up[e_j] . x[t].
 
-    Returns dict(Y [T,H], h [T,k,2I], A [T,k,I]) in float64."""
+    rnd (bf16-emulating mode, for narrowing a failing comparison): None keeps every value in
+    fp64; bf16_round rounds where the bf16 device path stores an intermediate: h (gate|up, from
+    which the backward works) and w * A (what the down projection reads; A itself is formed from
+    the unrounded h). Then Y[t] = sum_j down[e_j] . rnd(w[t,j] * A_j), the same sum with the
+    routing weight moved inside the linear map.
+
+    Returns dict(Y [T,H], h [T,k,2I], A [T,k,I], wA [T,k,I]) in float64 (h and wA as rounded)."""
+    rnd = _keep if rnd is None else rnd
     x = np.asarray(x, F64)
     Wgu = np.asarray(w_gate_up, F64)
     Wd = np.asarray(w_down, F64)
@@ -120,6 +131,7 @@ def moe_forward(x, w_gate_up, w_down, topk_idx, topk_w):
     Y = np.zeros((T, H))
     h = np.zeros((T, k, I2))
     A = np.zeros((T, k, I))
+    wA = np.zeros((T, k, I))
     for e in range(E):
         rows, slots = _expert_rows(topk_idx, e)
         if rows.size == 0:
@@ -127,15 +139,21 @@ def moe_forward(x, w_gate_up, w_down, topk_idx, topk_w):
         he = x[rows] @ Wgu[e].T
         gate, up = he[:, :I], he[:, I:]
         Ae = silu(gate) * up
-        ye = Ae @ Wd[e].T
-        Y[rows] += w[rows, slots][:, None] * ye
-        h[rows, slots] = he
+        we = w[rows, slots][:, None]
+        if rnd is _keep:
+            Y[rows] += we * (Ae @ Wd[e].T)
+            wAe = we * Ae
+        else:
+            wAe = np.asarray(rnd(we * Ae), F64)
+            Y[rows] += wAe @ Wd[e].T
+        h[rows, slots] = rnd(he)
         A[rows, slots] = Ae
-    return {"Y": Y, "h": h, "A": A}
+        wA[rows, slots] = wAe
+    return {"Y": Y, "h": h, "A": A, "wA": wA}
 
 
 def moe_backward(x, w_router, w_gate_up, w_down, topk_idx, topk_w, logits, dY, renorm=1,
-                 dense_wgrad=False):
+                 dense_wgrad=False, rnd=None):
     """Gradients of L = sum(dY * Y) with the expert selection held fixed.
 
     gvec = down[e]^T dY[t]; dw_j = <gvec, A_j>; dA = w_j gvec;
@@ -144,6 +162,9 @@ def moe_backward(x, w_router, w_gate_up, w_down, topk_idx, topk_w, logits, dY, r
             renorm=0 -> p_e (dw_e [e selected] - sum_i p_{e_i} dw_i) for every e;
     g_router = dlogit^T x; dx = sum_j gate_up[e_j]^T dh_j + dlogit . Wr.
     Only routed experts receive gradient (the news article's key differences).
+    rnd (bf16-emulating mode, see moe_forward): the backward reads the rounded h (for A in dw and
+    for the SwiGLU derivative), rounds dh where the device stores it (dx and the gate_up weight
+    gradient read the rounded dh), and the down weight gradient reads the rounded w * A.
     Returns dict(dw, dh, dlogit, g_router, dx [, dW_gate_up, dW_down])."""
     x = np.asarray(x, F64)
     Wr = np.asarray(w_router, F64)
@@ -155,7 +176,8 @@ def moe_backward(x, w_router, w_gate_up, w_down, topk_idx, topk_w, logits, dY, r
     E, I2, _ = Wgu.shape
     I = I2 // 2
     k = topk_idx.shape[1]
-    fwd = moe_forward(x, Wgu, Wd, topk_idx, w)
+    fwd = moe_forward(x, Wgu, Wd, topk_idx, w, rnd=rnd)
+    rnd = _keep if rnd is None else rnd
     dw = np.zeros((T, k))
     dh = np.zeros((T, k, I2))
     dx = np.zeros((T, H))
@@ -166,17 +188,22 @@ def moe_backward(x, w_router, w_gate_up, w_down, topk_idx, topk_w, logits, dY, r
         if rows.size == 0:
             continue
         he = fwd["h"][rows, slots]
-        Ae = fwd["A"][rows, slots]
         gate, up = he[:, :I], he[:, I:]
+        # A from the h the backward reads (the rounded one in bf16-emulating mode)
+        Ae = fwd["A"][rows, slots] if rnd is _keep else silu(gate) * up
         gvec = dY[rows] @ Wd[e]
         dw[rows, slots] = np.sum(gvec * Ae, axis=1)
         dA = w[rows, slots][:, None] * gvec
-        dge = np.concatenate([dA * up * silu_grad(gate), dA * silu(gate)], axis=1)
+        dge = np.asarray(rnd(np.concatenate([dA * up * silu_grad(gate), dA * silu(gate)],
+                                            axis=1)), F64)
         dh[rows, slots] = dge
         dx[rows] += dge @ Wgu[e]
         if dense_wgrad:
             dWgu[e] = dge.T @ x[rows]
-            dWd[e] = (w[rows, slots][:, None] * dY[rows]).T @ Ae
+            if rnd is _keep:
+                dWd[e] = (w[rows, slots][:, None] * dY[rows]).T @ Ae
+            else:
+                dWd[e] = dY[rows].T @ fwd["wA"][rows, slots]
     dlogit = np.zeros((T, E))
     if renorm:
         s = np.sum(w * dw, axis=1, keepdims=True)
@@ -215,13 +242,17 @@ def split_flat_index(f, E, I, H):
     return out_t, e, r, c
 
 
-def masked_expert_grad(act_idx, x, w_gate_up, w_down, topk_idx, topk_w, dY, experts=None):
+def masked_expert_grad(act_idx, x, w_gate_up, w_down, topk_idx, topk_w, dY, experts=None,
+                       rnd=None):
     """Expert weight gradients at the active flat indices only (the USAF sparse backward):
 
     gate_up entry (e, r, c): sum over tokens routed to e of dh[t, r] * x[t, c]
     down entry (e, r, c):    sum over tokens routed to e of w[t] * dY[t, r] * A[t, c]
     Experts with no routed token give 0. If `experts` is given, only actives of those experts are
-    computed and the others are returned as NaN (for sampled checks of large layers)."""
+    computed and the others are returned as NaN (for sampled checks of large layers).
+    rnd (bf16-emulating mode, see moe_forward and moe_backward): dh from the rounded h, then
+    rounded; the down entries read the rounded w * A."""
+    rnd = _keep if rnd is None else rnd
     x = np.asarray(x, F64)
     Wgu = np.asarray(w_gate_up, F64)
     Wd = np.asarray(w_down, F64)
@@ -241,19 +272,28 @@ def masked_expert_grad(act_idx, x, w_gate_up, w_down, topk_idx, topk_w, dY, expe
         if rows.size == 0:
             g[sel] = 0.0
             continue
-        he = x[rows] @ Wgu[e].T
+        he_exact = x[rows] @ Wgu[e].T
+        we = w[rows, slots][:, None]
+        he = np.asarray(rnd(he_exact), F64)
         gate, up = he[:, :I], he[:, I:]
         Ae = silu(gate) * up
         gvec = dY[rows] @ Wd[e]
-        dA = w[rows, slots][:, None] * gvec
-        dge = np.concatenate([dA * up * silu_grad(gate), dA * silu(gate)], axis=1)
-        wdy = w[rows, slots][:, None] * dY[rows]
+        dA = we * gvec
+        dge = np.asarray(rnd(np.concatenate([dA * up * silu_grad(gate), dA * silu(gate)],
+                                            axis=1)), F64)
         gu = sel[tens[sel] == 0]
         dn = sel[tens[sel] == 1]
         if gu.size:
             g[gu] = np.einsum("ta,ta->a", dge[:, rr[gu]], x[rows][:, cc[gu]])
         if dn.size:
-            g[dn] = np.einsum("ta,ta->a", wdy[:, rr[dn]], Ae[:, cc[dn]])
+            if rnd is _keep:
+                wdy = we * dY[rows]
+                g[dn] = np.einsum("ta,ta->a", wdy[:, rr[dn]], Ae[:, cc[dn]])
+            else:
+                # w * A from the unrounded h, rounded where the forward stores it
+                ge, ue = he_exact[:, :I], he_exact[:, I:]
+                wAe = np.asarray(rnd(we * silu(ge) * ue), F64)
+                g[dn] = np.einsum("ta,ta->a", dY[rows][:, rr[dn]], wAe[:, cc[dn]])
     return g
 
 

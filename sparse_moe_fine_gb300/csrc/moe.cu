@@ -634,34 +634,36 @@ __global__ void f32_to_kernel(const float* __restrict__ src, T* __restrict__ dst
     dst[i] = from_f32<T>(src[i]);
 }
 
-// dw of slot q: the sum of its nparts partials in order (tensor-core path), else dw[q] as written;
-// the summed value is stored to dw[q]
-__device__ __forceinline__ float slot_dw(float* __restrict__ dw, const float* __restrict__ part,
-                                         int nparts, int64_t n_slots, int64_t q) {
-  if (nparts == 0) return dw[q];
-  float d = 0.f;
-  for (int i = 0; i < nparts; ++i) d += part[(int64_t)i * n_slots + q];
-  dw[q] = d;
-  return d;
+// dw[q] = the sum of slot q's nparts partials (one per M tile and row quarter of the gvec GEMM),
+// in a fixed order with four loads in flight: dw does not depend on which tile finished first.
+__global__ void __launch_bounds__(256) dw_reduce_kernel(const float* __restrict__ part, int nparts,
+                                                        int64_t n_slots, float* __restrict__ dw) {
+  for (int64_t q = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; q < n_slots;
+       q += (int64_t)gridDim.x * blockDim.x) {
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    int i = 0;
+    for (; i + 4 <= nparts; i += 4) {
+      a0 += part[(int64_t)i * n_slots + q];
+      a1 += part[(int64_t)(i + 1) * n_slots + q];
+      a2 += part[(int64_t)(i + 2) * n_slots + q];
+      a3 += part[(int64_t)(i + 3) * n_slots + q];
+    }
+    for (; i < nparts; ++i) a0 += part[(int64_t)i * n_slots + q];
+    dw[q] = (a0 + a1) + (a2 + a3);
+  }
 }
 
 // dlogit at the selected experts, renormalised routing: w_j (dw_j - sum_i w_i dw_i).
-__global__ void dlogit_sel_kernel(const float* __restrict__ w, float* __restrict__ dw,
-                                  const float* __restrict__ dw_part, int nparts,
+__global__ void dlogit_sel_kernel(const float* __restrict__ w, const float* __restrict__ dw,
                                   const int32_t* __restrict__ slot_row, int Tn, int k,
                                   float* __restrict__ dl, float* __restrict__ dl_perm) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= Tn) return;
-  const int64_t n_slots = (int64_t)Tn * k;
-  float dws[32];
   float s = 0.f;
-  for (int j = 0; j < k; ++j) {
-    dws[j] = slot_dw(dw, dw_part, nparts, n_slots, (int64_t)t * k + j);
-    s = fmaf(w[(int64_t)t * k + j], dws[j], s);
-  }
+  for (int j = 0; j < k; ++j) s = fmaf(w[(int64_t)t * k + j], dw[(int64_t)t * k + j], s);
   for (int j = 0; j < k; ++j) {
     const int64_t q = (int64_t)t * k + j;
-    const float d = w[q] * (dws[j] - s);
+    const float d = w[q] * (dw[q] - s);
     dl[q] = d;
     dl_perm[slot_row[q]] = d;  // the same value at the slot's permuted row
   }
@@ -670,17 +672,14 @@ __global__ void dlogit_sel_kernel(const float* __restrict__ w, float* __restrict
 // dense dlogit for softmax-over-all-E routing: p_e (dw_e [e selected] - sum_i p_{e_i} dw_i).
 __global__ void dlogit_dense_kernel(const float* __restrict__ logits,
                                     const int32_t* __restrict__ idx,
-                                    const float* __restrict__ w, float* __restrict__ dw,
-                                    const float* __restrict__ dw_part, int nparts, int Tn, int E,
-                                    int k, float* __restrict__ dlogit) {
+                                    const float* __restrict__ w, const float* __restrict__ dw,
+                                    int Tn, int E, int k, float* __restrict__ dlogit) {
   const int t = blockIdx.x;
   const float* l = logits + (int64_t)t * E;
   __shared__ float red[32];
   __shared__ float sh_mx, sh_sum, sh_s;
   __shared__ float s_dw[32];
-  if (threadIdx.x < k)
-    s_dw[threadIdx.x] =
-        slot_dw(dw, dw_part, nparts, (int64_t)Tn * k, (int64_t)t * k + threadIdx.x);
+  if (threadIdx.x < k) s_dw[threadIdx.x] = dw[(int64_t)t * k + threadIdx.x];
   float mx = -INFINITY;
   for (int e = threadIdx.x; e < E; e += blockDim.x) mx = fmaxf(mx, l[e]);
   for (int o = 16; o; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -952,19 +951,24 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
     USAF_CHECK_LAUNCH();
   }
   // S7: router gradient (on the tensor-core path dw is first summed from its tile partials)
-  const int nparts = a.dt == USAF_BF16 ? 4 * (int)ceil_div(s.I, 128) : 0;
   {
     USAF_TRACE("router_bwd", st);
+    if (a.dt == USAF_BF16) {
+      const int nparts = 4 * (int)ceil_div(s.I, 128);
+      dw_reduce_kernel<<<grid_dim_for(s.T * s.k), 256, 0, st>>>(w.dw_part, nparts, s.T * s.k,
+                                                               dw);
+      USAF_CHECK_LAUNCH();
+    }
     if (renorm) {
       dlogit_sel_kernel<<<(unsigned)ceil_div(Tn, 128), 128, 0, st>>>(
-          a.rt.topk_w, dw, w.dw_part, nparts, a.rt.slot_row, Tn, k, w.dl, w.dl_perm);
+          a.rt.topk_w, dw, a.rt.slot_row, Tn, k, w.dl, w.dl_perm);
       USAF_CHECK_LAUNCH();
       g_router_sel_kernel<T><<<(unsigned)ceil_div(s.E * s.H, 32), 256, 0, st>>>(
           xT, w.dl_perm, cnt, off, E, H, a.R_cap, g_router, accumulate, dev_status);
       USAF_CHECK_LAUNCH();
     } else {
       dlogit_dense_kernel<<<(unsigned)Tn, 128, 0, st>>>(logits, a.rt.topk_idx, a.rt.topk_w, dw,
-                                                        w.dw_part, nparts, Tn, E, k, w.dlogit);
+                                                        Tn, E, k, w.dlogit);
       USAF_CHECK_LAUNCH();
       g_router_dense_kernel<T><<<dim3((unsigned)ceil_div(H, 128), (unsigned)E), 128, 0, st>>>(
           static_cast<const T*>(a.x), w.dlogit, Tn, E, H, g_router, accumulate, dev_status);

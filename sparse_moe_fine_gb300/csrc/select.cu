@@ -68,7 +68,6 @@ struct SelPlan {
 
 struct SelWs {
   SelCtrl* ctrl;
-  uint32_t* samples;
   uint32_t* ckeys;
   uint32_t* cids;
   uint32_t* ccnt;
@@ -110,7 +109,6 @@ SelPlan make_plan(int64_t N, int64_t K) {
 
 void sel_layout(const SelPlan& p, Carver& c, SelWs& w) {
   w.ctrl = c.take<SelCtrl>(1);
-  w.samples = c.take<uint32_t>(p.sampling ? SAMPLE_S : 0);
   w.ckeys = c.take<uint32_t>(p.G * p.cap);
   w.cids = c.take<uint32_t>(p.G * p.cap);
   w.ccnt = c.take<uint32_t>(p.G);
@@ -202,19 +200,63 @@ __global__ void sel_init_kernel(SelCtrl* c, int64_t K, uint32_t* ccnt, int G) {
   }
 }
 
-__global__ void sel_sample_kernel(const float* __restrict__ g, int64_t N,
-                                  const uint32_t* __restrict__ excl,
-                                  uint32_t* __restrict__ samples) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= SAMPLE_S) return;
-  const int64_t pos = (int64_t)(((unsigned long long)i * (unsigned long long)N) / SAMPLE_S);
-  samples[i] = excluded(excl, pos) ? 0u : abs_key(g[pos]);
+// The digit of one radix round from a 256-bin histogram (digits above dmask empty), by warp 0:
+// the largest d whose bins above d hold fewer than *krem keys and whose bins from d up hold at
+// least *krem; *krem becomes the rank still to find among the keys with digit d. Lane l owns
+// bins 255 - 8l .. 248 - 8l; a warp scan gives each lane the keys above its bins.
+__device__ __forceinline__ void pick_digit_warp(const uint32_t* hist, uint32_t* krem_io,
+                                                uint32_t* prefix_io, int shift) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t krem = *krem_io;
+  uint32_t bins[8], mine = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    bins[j] = hist[255 - 8 * lane - j];
+    mine += bins[j];
+  }
+  uint32_t incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const uint32_t above = incl - mine;
+  const unsigned hit = __ballot_sync(0xffffffffu, above < krem && krem <= incl);
+  int d = 0;
+  uint32_t cum = 0;
+  if (hit) {
+    const int src = __ffs(hit) - 1;
+    if (lane == src) {
+      cum = above;
+      d = 255 - 8 * lane - 7;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        if (cum + bins[j] >= krem) {
+          d = 255 - 8 * lane - j;
+          break;
+        }
+        cum += bins[j];
+      }
+    }
+    d = __shfl_sync(0xffffffffu, d, src);
+    cum = __shfl_sync(0xffffffffu, cum, src);
+  } else {
+    // krem above the total (cannot happen for a rank inside the sample): digit 0
+    cum = __shfl_sync(0xffffffffu, incl, 31) - hist[0];
+  }
+  if (lane == 0) {
+    *krem_io = krem - cum;
+    *prefix_io |= (uint32_t)d << shift;
+  }
 }
 
-// One block: the q-th largest sample (1-based) by 4 digit rounds; tau0 := that key. Each thread
-// keeps its 32 samples in registers; every warp counts digits into its own shared histogram.
-__global__ void __launch_bounds__(1024) sel_sample_tau_kernel(const uint32_t* __restrict__ samples,
-                                                              int q, SelCtrl* c) {
+// Set-up and threshold of the sampled path in one block of 1024 threads: the control block and
+// the region counts are cleared (as sel_init_kernel does), each thread reads 32 strided samples
+// of the keys straight from g (0 where excluded), and the q-th largest sample (1-based) is found
+// by 4 digit rounds over per-warp shared histograms; tau0 := that key.
+__global__ void __launch_bounds__(1024) sel_sample_tau_kernel(
+    const float* __restrict__ g, int64_t N, const uint32_t* __restrict__ excl, int q, SelCtrl* c,
+    int64_t K, uint32_t* ccnt, int G) {
   constexpr int PER = SAMPLE_S / 1024;
   __shared__ uint32_t wh[32][257];
   __shared__ uint32_t hist[256];
@@ -222,8 +264,23 @@ __global__ void __launch_bounds__(1024) sel_sample_tau_kernel(const uint32_t* __
   const int wid = threadIdx.x >> 5;
   uint32_t key[PER];
 #pragma unroll
-  for (int j = 0; j < PER; ++j) key[j] = samples[j * 1024 + threadIdx.x];
+  for (int j = 0; j < PER; ++j) {
+    const int i = j * 1024 + threadIdx.x;
+    const int64_t pos = (int64_t)(((unsigned long long)i * (unsigned long long)N) / SAMPLE_S);
+    key[j] = excluded(excl, pos) ? 0u : abs_key(g[pos]);
+  }
+  for (int i = threadIdx.x; i < MAX_BINS; i += blockDim.x) c->hist[i] = 0;
+  for (int i = threadIdx.x; i < G; i += blockDim.x) ccnt[i] = 0;
   if (threadIdx.x == 0) {
+    c->tau0 = 0;
+    c->mode = 0;
+    c->overflow = 0;
+    c->ticket = 0;
+    c->total = 0;
+    c->prefix = 0;
+    c->k_rem = (uint32_t)K;
+    c->n_swapped = 0;
+    c->r0_done = 0;
     s_prefix = 0;
     s_krem = (uint32_t)q;
   }
@@ -246,16 +303,7 @@ __global__ void __launch_bounds__(1024) sel_sample_tau_kernel(const uint32_t* __
       hist[threadIdx.x] = t;
     }
     __syncthreads();
-    if (threadIdx.x == 0) {
-      uint32_t krem = s_krem, cum = 0;
-      int d = (int)dmask;
-      for (; d > 0; --d) {
-        if (cum + hist[d] >= krem) break;
-        cum += hist[d];
-      }
-      s_krem = krem - cum;
-      s_prefix = prefix | ((uint32_t)d << shift);
-    }
+    if (wid == 0) pick_digit_warp(hist, &s_krem, &s_prefix, shift);
     __syncthreads();
   }
   if (threadIdx.x == 0) c->tau0 = s_prefix;
@@ -381,17 +429,20 @@ __global__ void sel_decide_kernel(SelCtrl* c, int64_t K, int sampling, uint32_t*
     c->hist[i] = 0;
   }
   __syncthreads();
-  if (threadIdx.x == 0 && ok) {
-    const uint32_t dmask = (1u << sel_bits(0)) - 1;
-    uint32_t krem = c->k_rem, cum = 0;
-    int d = (int)dmask;
-    for (; d > 0; --d) {
-      if (cum + h[d] >= krem) break;
-      cum += h[d];
+  if (ok && threadIdx.x < 32) {
+    __shared__ uint32_t s_krem, s_prefix;
+    if (threadIdx.x == 0) {
+      s_krem = c->k_rem;
+      s_prefix = 0;
     }
-    c->k_rem = krem - cum;
-    c->prefix = (uint32_t)d << sel_shift(0);
-    c->r0_done = 1;
+    __syncwarp();
+    pick_digit_warp(h, &s_krem, &s_prefix, sel_shift(0));
+    __syncwarp();
+    if (threadIdx.x == 0) {
+      c->k_rem = s_krem;
+      c->prefix = s_prefix;
+      c->r0_done = 1;
+    }
   }
 }
 
@@ -551,23 +602,20 @@ __global__ void bitmap_set_kernel(const int64_t* __restrict__ idx, int64_t K, in
 // The fixed sequence of launches that selects the top-K of `s` (see file comment).
 usaf_status run_select(const SelPlan& p, const SelWs& w, Src s, int64_t K, int64_t* out,
                        uint32_t* dev_status, bool fixed_drop, cudaStream_t st) {
-  {
-    USAF_TRACE("select_init", st);
-    sel_init_kernel<<<1, 256, 0, st>>>(w.ctrl, K, w.ccnt, p.G);
-    USAF_CHECK_LAUNCH();
-  }
   if (p.sampling && !fixed_drop) {
     {
       USAF_TRACE("select_sample", st);
-      sel_sample_kernel<<<SAMPLE_S / 256, 256, 0, st>>>(s.g, s.n, s.excl, w.samples);
-      USAF_CHECK_LAUNCH();
-      sel_sample_tau_kernel<<<1, 1024, 0, st>>>(w.samples, p.q, w.ctrl);
+      sel_sample_tau_kernel<<<1, 1024, 0, st>>>(s.g, s.n, s.excl, p.q, w.ctrl, K, w.ccnt, p.G);
       USAF_CHECK_LAUNCH();
     }
     USAF_TRACE("select_compact", st);
     const int vec_ok = (reinterpret_cast<uintptr_t>(s.g) & 15) == 0;
     sel_compact_kernel<<<p.G / COMPACT_WARPS, COMPACT_WARPS * 32, 0, st>>>(
         s.g, s.n, p.L, s.excl, p.cap, w.ckeys, w.cids, w.ccnt, w.ctrl, vec_ok, dev_status);
+    USAF_CHECK_LAUNCH();
+  } else {
+    USAF_TRACE("select_init", st);
+    sel_init_kernel<<<1, 256, 0, st>>>(w.ctrl, K, w.ccnt, p.G);
     USAF_CHECK_LAUNCH();
   }
   sel_decide_kernel<<<1, 256, 0, st>>>(w.ctrl, K, p.sampling && !fixed_drop ? 1 : 0, dev_status);
@@ -596,6 +644,27 @@ usaf_status run_select(const SelPlan& p, const SelWs& w, Src s, int64_t K, int64
   return USAF_OK;
 }
 
+// Entries of the sorted a[0, n) below key, found by one warp with 32 probes per step (about four
+// dependent loads for a million entries instead of twenty); every lane gets the result.
+__device__ __forceinline__ int64_t lower_bound_warp(const int64_t* a, int64_t n, int64_t key) {
+  const int lane = threadIdx.x & 31;
+  int64_t lo = 0, hi = n;  // a[i] < key for i < lo, a[i] >= key for i >= hi
+  while (hi - lo > 32) {
+    const int64_t step = (hi - lo + 31) / 32;
+    const int64_t i = lo + (int64_t)lane * step;
+    const int c = __popc(__ballot_sync(0xffffffffu, i < hi && a[i] < key));
+    if (c == 0) {
+      hi = lo;
+      break;
+    }
+    const int64_t nhi = lo + (int64_t)c * step;
+    lo += (int64_t)(c - 1) * step + 1;
+    hi = nhi < hi ? nhi : hi;
+  }
+  const int64_t i = lo + lane;
+  return lo + __popc(__ballot_sync(0xffffffffu, i < hi && a[i] < key));
+}
+
 __device__ __forceinline__ int64_t lower_bound_i64(const int64_t* a, int64_t n, int64_t key) {
   int64_t lo = 0, hi = n;
   while (lo < hi) {
@@ -606,54 +675,114 @@ __device__ __forceinline__ int64_t lower_bound_i64(const int64_t* a, int64_t n, 
   return lo;
 }
 
-// dropped flat indices below f: count q with act_idx[drop_pos[q]] < f (sorted in q)
-__device__ __forceinline__ int64_t dropped_below(const int64_t* act, const int64_t* dpos,
-                                                 int64_t D, int64_t f) {
-  int64_t lo = 0, hi = D;
-  while (lo < hi) {
-    const int64_t mid = (lo + hi) >> 1;
-    if (act[dpos[mid]] < f) lo = mid + 1;
-    else hi = mid;
-  }
-  return lo;
-}
-
+// Merge of the kept and grown entries by tiles of the old set: block b takes act[s0, s1) (MG_TILE
+// entries). One search each gives the dropped positions inside the tile and the grown entries that
+// fall between act[s0] and act[s1] (block 0 also takes those below act[0], the last block those
+// above act[K-1]). A kept entry's new position is (kept entries before it) + (grown entries below
+// it); a grown entry's is (its index among the grown) + (kept entries below it). Inside the tile
+// the kept ranks come from a block scan and the searches run over the tile in shared memory or
+// over the tile's own range of the grown list, so no per-entry search crosses the whole set.
+constexpr int MG_TILE = 2048;
+constexpr int MG_THREADS = 256;
+constexpr int MG_GROWN = 2048;  // grown entries of a tile's range kept in shared memory
 template <typename W>
-__global__ void rigl_merge_kernel(const int64_t* __restrict__ act, int64_t K,
-                                  const int64_t* __restrict__ dpos,
-                                  const int64_t* __restrict__ grown, int64_t D,
-                                  const float* __restrict__ p_in, const float* __restrict__ m_in,
-                                  const float* __restrict__ v_in, const W* __restrict__ w0,
-                                  int64_t n0, const W* __restrict__ w1,
-                                  int64_t* __restrict__ new_idx, float* __restrict__ p_out,
-                                  float* __restrict__ m_out, float* __restrict__ v_out,
-                                  SelCtrl* c) {
-  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (t < K) {
-    const int64_t nd = lower_bound_i64(dpos, D, t);
-    const bool dropped = nd < D && dpos[nd] == t;
-    if (dropped) {
-      atomicAdd(&c->n_swapped, 1ull);
+__global__ void __launch_bounds__(MG_THREADS) rigl_merge_tile_kernel(
+    const int64_t* __restrict__ act, int64_t K, const int64_t* __restrict__ dpos,
+    const int64_t* __restrict__ grown, int64_t D, const float* __restrict__ p_in,
+    const float* __restrict__ m_in, const float* __restrict__ v_in, const W* __restrict__ w0,
+    int64_t n0, const W* __restrict__ w1, int64_t* __restrict__ new_idx,
+    float* __restrict__ p_out, float* __restrict__ m_out, float* __restrict__ v_out, SelCtrl* c) {
+  constexpr int PER = MG_TILE / MG_THREADS;
+  __shared__ int64_t sh_act[MG_TILE];
+  __shared__ uint32_t sh_keep[MG_TILE + 1];  // exclusive kept ranks inside the tile
+  __shared__ int64_t sh_grown[MG_GROWN];      // the tile's range of the grown list, if it fits
+  __shared__ int64_t sh_rng[4];               // d0, d1, g0, g1
+  const int64_t s0 = (int64_t)blockIdx.x * MG_TILE;
+  const int64_t s1 = min(K, s0 + MG_TILE);
+  const int n = (int)(s1 - s0);
+  const bool last = s1 == K;
+  const int wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the four boundary searches, one warp each
+  if (wid < 4) {
+    int64_t r;
+    if (wid == 0) r = lower_bound_warp(dpos, D, s0);
+    else if (wid == 1) r = lower_bound_warp(dpos, D, s1);
+    else if (wid == 2) r = blockIdx.x == 0 ? 0 : lower_bound_warp(grown, D, act[s0]);
+    else r = last ? D : lower_bound_warp(grown, D, act[s1]);
+    if (lane == 0) sh_rng[wid] = r;
+  }
+  for (int i = threadIdx.x; i < n; i += MG_THREADS) {
+    sh_act[i] = act[s0 + i];
+    sh_keep[i] = 1;
+  }
+  __syncthreads();
+  const int64_t d0 = sh_rng[0], d1 = sh_rng[1], g0 = sh_rng[2], g1 = sh_rng[3];
+  const bool g_in_smem = g1 - g0 <= MG_GROWN;
+  if (g_in_smem)
+    for (int64_t j = g0 + threadIdx.x; j < g1; j += MG_THREADS) sh_grown[j - g0] = grown[j];
+  for (int64_t j = d0 + threadIdx.x; j < d1; j += MG_THREADS) sh_keep[dpos[j] - s0] = 0;
+  __syncthreads();
+  // exclusive scan of the keep flags: thread t owns entries PER t .. PER t + PER - 1
+  uint32_t f[PER], mine = 0;
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int i = threadIdx.x * PER + u;
+    f[u] = i < n ? sh_keep[i] : 0u;
+    mine += f[u];
+  }
+  uint32_t tot;
+  uint32_t run = block_excl_scan(mine, &tot);
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int i = threadIdx.x * PER + u;
+    if (i < n) sh_keep[i] = run;  // flags are in f[] now
+    run += f[u];
+  }
+  if (threadIdx.x == 0) sh_keep[n] = tot;
+  __syncthreads();
+  const int64_t kept_before = s0 - d0;
+  // kept entries
+#pragma unroll
+  for (int u = 0; u < PER; ++u) {
+    const int i = threadIdx.x * PER + u;
+    if (i >= n || !f[u]) continue;
+    const int64_t fi = sh_act[i];
+    int64_t below;  // grown entries of the tile's range below fi
+    if (g_in_smem) {
+      int lo = 0, hi = (int)(g1 - g0);
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (sh_grown[mid] < fi) lo = mid + 1;
+        else hi = mid;
+      }
+      below = lo;
     } else {
-      const int64_t f = act[t];
-      const int64_t pos = (t - nd) + lower_bound_i64(grown, D, f);
-      if (pos >= K) return;  // only an unsorted act_idx gets here
-      new_idx[pos] = f;
-      p_out[pos] = p_in[t];
-      m_out[pos] = m_in[t];
-      v_out[pos] = v_in[t];
+      below = lower_bound_i64(grown + g0, g1 - g0, fi);
     }
-  } else if (t < K + D) {
-    const int64_t j = t - K;
-    const int64_t f = grown[j];
-    const int64_t kept_before = lower_bound_i64(act, K, f) - dropped_below(act, dpos, D, f);
-    const int64_t pos = j + kept_before;
-    if (pos < 0 || pos >= K) return;  // only an unsorted act_idx gets here
-    new_idx[pos] = f;
-    p_out[pos] = to_f32(f < n0 ? w0[f] : w1[f - n0]);
+    const int64_t pos = kept_before + sh_keep[i] + g0 + below;
+    if (pos >= K) continue;  // only an unsorted act_idx gets here
+    new_idx[pos] = fi;
+    p_out[pos] = p_in[s0 + i];
+    m_out[pos] = m_in[s0 + i];
+    v_out[pos] = v_in[s0 + i];
+  }
+  // grown entries of the tile's range
+  for (int64_t j = g0 + threadIdx.x; j < g1; j += MG_THREADS) {
+    const int64_t fj = g_in_smem ? sh_grown[j - g0] : grown[j];
+    int lo = 0, hi = n;  // kept-or-dropped tile entries below fj
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (sh_act[mid] < fj) lo = mid + 1;
+      else hi = mid;
+    }
+    const int64_t pos = kept_before + sh_keep[lo] + j;
+    if (pos < 0 || pos >= K) continue;  // only an unsorted act_idx gets here
+    new_idx[pos] = fj;
+    p_out[pos] = to_f32(fj < n0 ? w0[fj] : w1[fj - n0]);
     m_out[pos] = 0.f;
     v_out[pos] = 0.f;
   }
+  if (threadIdx.x == 0 && d1 > d0) atomicAdd(&c->n_swapped, (unsigned long long)(d1 - d0));
 }
 
 // Full reselection: entry t of the new set carries (p, m, v) from the old set when its flat index
@@ -747,20 +876,45 @@ usaf_status rigl_launch(const float* g, int64_t N, const int64_t* act_idx, int64
   SelWs wg;
   sel_layout(pg, cg, wg);
   uint32_t* bitmap = cg.take<uint32_t>(ceil_div(N, 32));
+  // the drop selection (over the K values of |p|, a chain of small launches) runs on a stream of
+  // its own, forked from and joined back to `st`, so it overlaps the pass over g
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  auto release = [&]() {
+    if (fork) cudaEventDestroy(fork);
+    if (join) cudaEventDestroy(join);
+    if (side) cudaStreamDestroy(side);  // its work still completes
+  };
   if (D > 0) {
+    if (cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventRecord(fork, st) != cudaSuccess || cudaStreamWaitEvent(side, fork, 0) != cudaSuccess) {
+      release();
+      return USAF_ERR_CUDA;
+    }
     Src sd{};
     sd.g = p_in;
     sd.n = K;
     sd.L = pd.L;
     sd.drop = 1;
-    USAF_TRY(run_select(pd, wd, sd, D, dpos, dev_status, true, st));
+    const usaf_status sdrop = run_select(pd, wd, sd, D, dpos, dev_status, true, side);
+    if (sdrop != USAF_OK || cudaEventRecord(join, side) != cudaSuccess) {
+      release();
+      return sdrop != USAF_OK ? sdrop : USAF_ERR_CUDA;
+    }
     const int64_t words = ceil_div(N, 32);
     {
       USAF_TRACE("rigl_bitmap", st);
       bitmap_zero_kernel<<<grid_dim_for(words), 256, 0, st>>>(bitmap, words);
-      USAF_CHECK_LAUNCH();
+      count_launch();
       bitmap_set_kernel<<<grid_dim_for(K), 256, 0, st>>>(act_idx, K, N, bitmap, dev_status);
-      USAF_CHECK_LAUNCH();
+      count_launch();
+      if (cudaGetLastError() != cudaSuccess) {
+        cudaStreamWaitEvent(st, join, 0);
+        release();
+        return USAF_ERR_CUDA;
+      }
     }
     Src sg{};
     sg.g = g;
@@ -768,20 +922,24 @@ usaf_status rigl_launch(const float* g, int64_t N, const int64_t* act_idx, int64
     sg.L = pg.L;
     sg.excl = bitmap;
     sg.drop = 0;
-    USAF_TRY(run_select(pg, wg, sg, D, grown, dev_status, false, st));
+    const usaf_status sgrow = run_select(pg, wg, sg, D, grown, dev_status, false, st);
+    const bool joined = cudaStreamWaitEvent(st, join, 0) == cudaSuccess;
+    release();
+    if (sgrow != USAF_OK) return sgrow;
+    if (!joined) return USAF_ERR_CUDA;
   } else {
     sel_init_kernel<<<1, 256, 0, st>>>(wd.ctrl, 0, wd.ccnt, pd.G);
     USAF_CHECK_LAUNCH();
   }
-  const int64_t n = K + D;
   USAF_TRACE("rigl_merge", st);
-  if (n > 0) {
+  if (K > 0) {
+    const unsigned nb = (unsigned)ceil_div(K, MG_TILE);
     if (wdt == USAF_BF16)
-      rigl_merge_kernel<__nv_bfloat16><<<(unsigned)ceil_div(n, 256), 256, 0, st>>>(
+      rigl_merge_tile_kernel<__nv_bfloat16><<<nb, MG_THREADS, 0, st>>>(
           act_idx, K, dpos, grown, D, p_in, m_in, v_in, static_cast<const __nv_bfloat16*>(w0),
           n0, static_cast<const __nv_bfloat16*>(w1), new_idx, p_out, m_out, v_out, wd.ctrl);
     else
-      rigl_merge_kernel<float><<<(unsigned)ceil_div(n, 256), 256, 0, st>>>(
+      rigl_merge_tile_kernel<float><<<nb, MG_THREADS, 0, st>>>(
           act_idx, K, dpos, grown, D, p_in, m_in, v_in, static_cast<const float*>(w0), n0,
           static_cast<const float*>(w1), new_idx, p_out, m_out, v_out, wd.ctrl);
     USAF_CHECK_LAUNCH();

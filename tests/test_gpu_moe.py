@@ -112,6 +112,32 @@ def test_small_bf16_layers(dims):
     compare(cfg, got, idx, b, g, 1e-2)
 
 
+@pytest.mark.parametrize("dims", SMALL_BF16)
+def test_small_bf16_layers_against_the_bf16_emulating_oracle(dims):
+    """The same layers against the oracle's bf16-emulating mode (h, w*A and dh rounded to bf16
+    where the device stores them): what is left is the device's fp32 accumulation and the final
+    bf16 rounding of y and dx, so the bounds are far below the 1e-2 of the fp64 comparison --
+    y and dx 3e-3 (one bf16 rounding: 2^-9 relative at most), the fp32 results 1e-3."""
+    dev = device()
+    cfg = synth.small_config("small", bf16=True, frac=0.05, dy_std=1e-2, **dims)
+    inp = synth.moe_inputs(cfg, seed=5)
+    logits = oracle.router_logits(inp["x"], inp["w_router"])
+    act = synth.uniform_mask(cfg.N, cfg.K, seed=5)
+    got = run_layer(cfg, inp, act, logits, dev)
+    idx, w = oracle.route_topk(logits, cfg.k)
+    r = oracle.bf16_round
+    b = oracle.moe_backward(inp["x"], inp["w_router"], inp["w_gate_up"], inp["w_down"], idx, w,
+                            logits, inp["dy"], rnd=r)
+    g = oracle.masked_expert_grad(act, inp["x"], inp["w_gate_up"], inp["w_down"], idx, w,
+                                  inp["dy"], rnd=r)
+    assert (got["idx"] == idx).all() and got["status"] == 0
+    assert rel_l2(got["Y"], b["Y"]) <= 3e-3
+    assert rel_l2(got["dx"], b["dx"]) <= 3e-3
+    for key in ("dw", "g_router"):
+        assert rel_l2(got[key], b[key]) <= 1e-3, key
+    assert rel_l2(got["g_act"], g) <= 1e-3
+
+
 def test_bf16_empty_and_crowded_experts():
     dev = device()
     cfg = synth.small_config("skew", T=700, H=128, E=6, k=2, I=128, bf16=True, frac=0.05)

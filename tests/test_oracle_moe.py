@@ -174,3 +174,57 @@ def test_router_grad_invariants():
     mask = np.zeros_like(b["dlogit"], dtype=bool)
     np.put_along_axis(mask, idx.astype(np.int64), True, axis=1)
     assert (b["dlogit"][~mask] == 0).all()
+
+
+def _bf16_inputs(seed=3):
+    cfg = synth.small_config("bf", T=96, H=32, E=6, k=2, I=16, bf16=True, dy_std=1.0)
+    inp = synth.moe_inputs(cfg, seed=seed)
+    for key in ("w_gate_up", "w_down"):
+        inp[key] = synth.to_bf16_values(inp[key] * 20)
+    logits = oracle.router_logits(inp["x"], inp["w_router"])
+    idx, w = oracle.route_topk(logits, cfg.k)
+    act = synth.uniform_mask(cfg.N, cfg.K, seed=seed)
+    return cfg, inp, logits, idx, w, act
+
+
+def _all_outputs(cfg, inp, logits, idx, w, act, rnd):
+    b = oracle.moe_backward(inp["x"], inp["w_router"], inp["w_gate_up"], inp["w_down"], idx, w,
+                            logits, inp["dy"], dense_wgrad=True, rnd=rnd)
+    g = oracle.masked_expert_grad(act, inp["x"], inp["w_gate_up"], inp["w_down"], idx, w,
+                                  inp["dy"], rnd=rnd)
+    return b, g
+
+
+def test_bf16_emulating_mode_with_identity_rounding_is_the_fp64_oracle():
+    """With a rounding function that changes nothing, the bf16-emulating code path gives the fp64
+    oracle's results (up to the order of the routing-weight product), so the mode adds nothing but
+    its rounding points."""
+    cfg, inp, logits, idx, w, act = _bf16_inputs()
+    ref_b, ref_g = _all_outputs(cfg, inp, logits, idx, w, act, None)
+    got_b, got_g = _all_outputs(cfg, inp, logits, idx, w, act, lambda a: np.array(a, np.float64))
+    for key in ("Y", "dx", "dw", "dh", "dlogit", "g_router", "dW_gate_up", "dW_down"):
+        np.testing.assert_allclose(got_b[key], ref_b[key], rtol=1e-11, atol=1e-13, err_msg=key)
+    np.testing.assert_allclose(got_g, ref_g, rtol=1e-11, atol=1e-13)
+
+
+def test_bf16_emulating_mode_rounds_at_the_storage_points():
+    """With bf16 rounding (pinned against torch's cast): the stored h is the nearest bf16 of the
+    fp64 h, w*A is the nearest bf16 of the fp64 w*A, every stored dh is a bf16 value, and each
+    result stays within a few bf16 half-ulps (2^-9 relative) of the fp64 oracle."""
+    cfg, inp, logits, idx, w, act = _bf16_inputs()
+    ref_b, ref_g = _all_outputs(cfg, inp, logits, idx, w, act, None)
+    rb, rg = _all_outputs(cfg, inp, logits, idx, w, act, oracle.bf16_round)
+    f64 = oracle.moe_forward(inp["x"], inp["w_gate_up"], inp["w_down"], idx, w)
+    f16 = oracle.moe_forward(inp["x"], inp["w_gate_up"], inp["w_down"], idx, w,
+                             rnd=oracle.bf16_round)
+    assert np.array_equal(f16["h"], oracle.bf16_round(f64["h"]))
+    assert np.array_equal(f16["wA"], oracle.bf16_round(f64["wA"]))
+    assert np.array_equal(rb["dh"], oracle.bf16_round(rb["dh"]))
+    rel = lambda a, b: np.linalg.norm(a - b) / np.linalg.norm(b)
+    for key in ("Y", "dx", "dw", "g_router", "dW_gate_up", "dW_down"):
+        e = rel(rb[key], ref_b[key])
+        assert 1e-5 < e < 2e-2, (key, e)  # rounded somewhere, and only by bf16 steps
+    assert 1e-5 < rel(rg, ref_g) < 2e-2
+    # the masked gradient is the dense one gathered at the mask in this mode too
+    dense = np.concatenate([rb["dW_gate_up"].reshape(-1), rb["dW_down"].reshape(-1)])
+    np.testing.assert_allclose(rg, dense[act], rtol=1e-10, atol=1e-12)
