@@ -37,6 +37,16 @@ def allreduce_grads(g_act, g_router, status, group=None):
     status.copy_(sum(bits[b] << b for b in range(STATUS_BITS)))
 
 
+def allreduce_dense_grad(g_dense, group=None):
+    """Sum the accumulated dense expert gradient of the importance phase over the ranks of
+    `group`, in place, on the current stream. Each rank accumulated the gradient of its own
+    tokens; the sum is the whole batch's gradient, so every replica then ranks the same |g| and
+    installs the same active set (the compact gradients of later steps index the same weights
+    on every rank)."""
+    import torch.distributed as dist
+    dist.all_reduce(g_dense, op=dist.ReduceOp.SUM, group=group)
+
+
 class MoELayer:
     def __init__(self, T, H, E, k, I, w_gate_up, w_down, w_router, act_idx, lr=1e-4,
                  betas=(0.9, 0.999), eps=1e-8, renorm=1, device="cuda", group=None):

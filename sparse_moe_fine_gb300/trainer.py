@@ -14,6 +14,7 @@ import math
 import torch
 
 from . import binding as B
+from .layer import allreduce_dense_grad
 
 
 def cosine_lr(step: int, total_steps: int, peak: float, warmup_steps: int = 0,
@@ -112,6 +113,9 @@ class StackTrainer:
         for i, L in enumerate(self.layers):
             L.wait_optimizer()
             g = self._g_dense[i]
+            if L.group is not None:
+                # data parallel: rank the whole batch's gradient, so the replicas' sets agree
+                allreduce_dense_grad(g, L.group)
             K = L.K
             new = torch.empty(K, dtype=torch.int64, device=L.dev)
             p, m, v = (torch.empty(K, device=L.dev) for _ in range(3))

@@ -12,7 +12,7 @@ import torch.multiprocessing as mp
 
 import oracle
 from sparse_moe_fine_gb300 import synth
-from sparse_moe_fine_gb300.layer import allreduce_grads
+from sparse_moe_fine_gb300.layer import allreduce_dense_grad, allreduce_grads
 
 WORLD = 2
 
@@ -99,6 +99,66 @@ def test_sharded_gradients_sum_to_whole_batch():
         np.testing.assert_allclose(g_r, b["g_router"], rtol=1e-12, atol=1e-15)
         np.testing.assert_allclose(p, p1, rtol=1e-6, atol=1e-9)  # fp32 master values
     np.testing.assert_array_equal(res[0][2], res[1][2])  # identical replicas
+
+
+def _dense_grad(inp, x, dy):
+    logits = oracle.router_logits(x, inp["w_router"])
+    idx, w = oracle.route_topk(logits, CFG.k)
+    b = oracle.moe_backward(x, inp["w_router"], inp["w_gate_up"], inp["w_down"], idx, w, logits,
+                            dy, dense_wgrad=True)
+    return np.concatenate([b["dW_gate_up"].reshape(-1), b["dW_down"].reshape(-1)])
+
+
+def _shard_reselect(rank):
+    """One rank: the dense gradient of its half of the tokens, exchanged with the trainer's
+    reduction, then both reselection rules (RigL drop/grow and the full re-rank)."""
+    inp = synth.moe_inputs(CFG, seed=4)
+    act = synth.uniform_mask(CFG.N, CFG.K, seed=4)
+    sl = slice(rank * CFG.T // WORLD, (rank + 1) * CFG.T // WORLD)
+    # fp64 shards: their sum is the whole batch's gradient up to fp64 rounding, so after the
+    # fp32 cast the ranking is the whole batch's
+    g64 = torch.from_numpy(np.ascontiguousarray(_dense_grad(inp, inp["x"][sl], inp["dy"][sl])))
+    local = g64.numpy().astype(np.float32)
+    allreduce_dense_grad(g64)
+    g = g64.float()
+    w = np.concatenate([inp["w_gate_up"].reshape(-1), inp["w_down"].reshape(-1)])
+    p = w[act].copy()
+    m, v = synth.adam_state(act.size, seed=4)
+    D = int(0.3 * act.size)
+    rig = oracle.rigl_swap(act, p, m, v, g.numpy(), D, lambda i: w[i])
+    full = oracle.reselect_full(act, p, m, v, g.numpy(), act.size, lambda i: w[i])
+    # without the exchange the replicas would rank different gradients
+    alone = oracle.rigl_swap(act, p, m, v, local, D, lambda i: w[i])[0]
+    return rig[0].copy(), rig[1].copy(), full[0].copy(), alone.copy(), g.numpy().copy()
+
+
+def test_reselection_after_the_dense_exchange_agrees_across_ranks():
+    res = _spawn(_shard_reselect)
+    inp = synth.moe_inputs(CFG, seed=4)
+    act = synth.uniform_mask(CFG.N, CFG.K, seed=4)
+    g_all = _dense_grad(inp, inp["x"], inp["dy"])
+    w = np.concatenate([inp["w_gate_up"].reshape(-1), inp["w_down"].reshape(-1)])
+    p = w[act].copy()
+    m, v = synth.adam_state(act.size, seed=4)
+    D = int(0.3 * act.size)
+    # the exchanged gradient is the whole batch's
+    for *_, g in res:
+        np.testing.assert_array_equal(g, g_all.astype(np.float32))
+    np.testing.assert_array_equal(res[0][4], res[1][4])
+    ref_rig = oracle.rigl_swap(act, p, m, v, res[0][4], D, lambda i: w[i])
+    ref_full = oracle.reselect_full(act, p, m, v, res[0][4], act.size, lambda i: w[i])
+    for rig_idx, rig_p, full_idx, _, _ in res:
+        np.testing.assert_array_equal(rig_idx, ref_rig[0])
+        np.testing.assert_array_equal(rig_p, ref_rig[1])
+        np.testing.assert_array_equal(full_idx, ref_full[0])
+    # the sets from the exchanged gradient are the whole batch's
+    g32 = g_all.astype(np.float32)
+    np.testing.assert_array_equal(
+        ref_rig[0], oracle.rigl_swap(act, p, m, v, g32, D, lambda i: w[i])[0])
+    np.testing.assert_array_equal(
+        ref_full[0], oracle.reselect_full(act, p, m, v, g32, act.size, lambda i: w[i])[0])
+    # and each rank alone would have installed a different set
+    assert not np.array_equal(res[0][3], res[1][3])
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="the GPU arm would use NCCL; CPU check")
