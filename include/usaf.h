@@ -236,6 +236,42 @@ usaf_status usaf_moe_bwd_sparse_accumulate(
     float* dw_slot, uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * Masked-gradient plan of an active set. The sparse backward forms each active entry's gradient
+ * as a dot product over its expert's routed tokens (usaf_moe_bwd_sparse). Where the active set
+ * is dense inside an expert (importance selection concentrates on some experts; the skewed
+ * workload puts 80% of the set on 16 of 128 experts), a dense tensor-core tile of that expert's
+ * gradient, read out at the active entries only, costs less. The plan lists those experts and,
+ * for each, the first active entry of every weight row. It depends only on the active set and
+ * the shape: build it when the set changes (README, "Sparsity adapts": every 50 steps).
+ *   usaf_masked_plan_size   bytes of the plan buffer for this shape (host only)
+ *   usaf_masked_plan_build  dense_density: an expert is listed when its active entries (both
+ *                           tensors) are at least dense_density * 3*I*H (> 0; 1 lists none).
+ *                           plan [usaf_masked_plan_size] device buffer, 256-byte aligned.
+ *                           After the stream has run the build, the plan's first 8 bytes hold
+ *                           the number of listed experts as an int64, for the caller to read.
+ * Errors: INVALID_ARG, CUDA.
+ * ------------------------------------------------------------------------------------------- */
+size_t usaf_masked_plan_size(const usaf_moe_shape* shape);
+usaf_status usaf_masked_plan_build(const usaf_moe_shape* shape, const int64_t* act_idx, int64_t K,
+                                   double dense_density, void* plan, size_t plan_bytes,
+                                   void* stream);
+
+/* usaf_moe_bwd_sparse_planned - usaf_moe_bwd_sparse (accumulate = 0) or
+ * usaf_moe_bwd_sparse_accumulate (accumulate = 1) with a masked-gradient plan of act_idx: the
+ * listed experts' active entries are read out of dense bf16 tensor-core tiles (fp32
+ * accumulation), every other entry as before. n_dense is the count the caller read from the
+ * plan's first 8 bytes; with n_dense = 0 the plan is not read (may be NULL) and the call is the
+ * plain sparse backward. fp32 layers ignore the plan. Same results (within the bf16 bound),
+ * workspace and errors as usaf_moe_bwd_sparse. */
+usaf_status usaf_moe_bwd_sparse_planned(
+    const usaf_moe_shape* shape, usaf_dtype dtype, int renorm, const void* x,
+    const float* w_router, const void* w_gate_up, const void* w_down, const usaf_routing* rt,
+    const float* logits, const void* x_perm_save, const void* h_save, const void* wa_save,
+    const void* dy, const int64_t* act_idx, int64_t K, float* g_act, float* g_router, void* dx,
+    float* dw_slot, int accumulate, const void* plan, int64_t n_dense, uint32_t* dev_status,
+    void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
  * usaf_moe_bwd_dense - the same backward as usaf_moe_bwd_sparse (dh, dw, router gradient, dx),
  * with the expert weight gradient formed densely for the importance phase (USAF README: the
  * weights to train are the 0.5% with the largest gradient magnitude, found by a dense gradient

@@ -85,6 +85,11 @@ _SIGS = {
     "usaf_moe_bwd_dense": (_INT, [_P, _INT, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                   _INT, _P, _P, _P, _P, _P, _SZ, _P]),
     "usaf_validate_active": (_INT, [_P, _I64, _I64, _P, _P]),
+    "usaf_masked_plan_size": (_SZ, [_P]),
+    "usaf_masked_plan_build": (_INT, [_P, _P, _I64, _D, _P, _SZ, _P]),
+    "usaf_moe_bwd_sparse_planned": (_INT, [_P, _INT, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                           _P, _P, _I64, _P, _P, _P, _P, _INT, _P, _I64, _P, _P,
+                                           _SZ, _P]),
     "usaf_moe_wgrad_dense": (_INT, [_P, _INT, _P, _P, _P, _P, _INT, _P, _P, _SZ, _P]),
     "usaf_moe_bwd_dlogit_offset": (_I64, [_P, _INT, _I64]),
     "usaf_diag_bounded_wait": (_INT, [_I64, _P, _P]),
@@ -250,6 +255,40 @@ def moe_bwd_sparse(s: Shape, x, w_router, w_gate_up, w_down, rt: Routing, x_perm
         ctypes.byref(r), _ptr(logits), _ptr(x_perm), _ptr(h), _ptr(wa), _ptr(dy), _ptr(act_idx),
         K, _ptr(g_act), _ptr(g_router), _ptr(dx), _ptr(dw_slot), _ptr(dev_status), _ptr(ws),
         ws.numel(), _stream(stream)))
+
+
+def masked_plan_size(s: Shape) -> int:
+    return int(lib().usaf_masked_plan_size(ctypes.byref(s)))
+
+
+def masked_plan_build(s: Shape, act_idx, dense_density, plan, stream=None):
+    """usaf_masked_plan_build; after the stream has run it, masked_plan_count(plan) reads the
+    number of listed experts."""
+    K = 0 if act_idx is None else act_idx.numel()
+    _check("usaf_masked_plan_build", lib().usaf_masked_plan_build(
+        ctypes.byref(s), _ptr(act_idx), K, float(dense_density), _ptr(plan), plan.numel(),
+        _stream(stream)))
+
+
+def masked_plan_count(plan) -> int:
+    """The plan's first 8 bytes: the number of experts it lists (reads device memory)."""
+    return int(plan[:8].view(torch.int64).item())
+
+
+def moe_bwd_sparse_planned(s: Shape, x, w_router, w_gate_up, w_down, rt: Routing, x_perm, h, wa,
+                           dy, act_idx, g_act, g_router, plan=None, n_dense=0, accumulate=0,
+                           dx=None, dw_slot=None, logits=None, renorm=1, dev_status=None,
+                           ws=None, stream=None):
+    dt = _dt(x)
+    K = 0 if act_idx is None else act_idx.numel()
+    if ws is None:
+        ws = _ws(moe_bwd_workspace_size(s, dt, K), x.device)
+    r = rt.c()
+    _check("usaf_moe_bwd_sparse_planned", lib().usaf_moe_bwd_sparse_planned(
+        ctypes.byref(s), dt, int(renorm), _ptr(x), _ptr(w_router), _ptr(w_gate_up), _ptr(w_down),
+        ctypes.byref(r), _ptr(logits), _ptr(x_perm), _ptr(h), _ptr(wa), _ptr(dy), _ptr(act_idx),
+        K, _ptr(g_act), _ptr(g_router), _ptr(dx), _ptr(dw_slot), int(accumulate), _ptr(plan),
+        int(n_dense), _ptr(dev_status), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def moe_bwd_sparse_accumulate(s: Shape, x, w_router, w_gate_up, w_down, rt: Routing, x_perm,

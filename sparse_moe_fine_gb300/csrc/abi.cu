@@ -1,7 +1,9 @@
 // The extern "C" entry points declared in include/usaf.h: argument checks, workspace carving,
 // and the launch sequence of each call. Everything here is host code; the arithmetic is in the
 // kernel files.
+#include <algorithm>
 #include <atomic>
+#include <cmath>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -315,6 +317,57 @@ usaf_status usaf_moe_bwd_sparse_accumulate(
   return moe_bwd_launch(a, renorm, logits, x_perm_save, h_save, wa_save, dy, act_idx, K, g_act,
                         g_router, dx, dw_slot, nullptr, 1, dev_status, w,
                         static_cast<cudaStream_t>(stream));
+}
+
+size_t usaf_masked_plan_size(const usaf_moe_shape* s) {
+  if (!shape_ok(s)) return 0;
+  return masked_plan_bytes(*s);
+}
+
+usaf_status usaf_masked_plan_build(const usaf_moe_shape* s, const int64_t* act_idx, int64_t K,
+                                   double dense_density, void* plan, size_t plan_bytes,
+                                   void* stream) {
+  if (!shape_ok(s) || !plan || K < 0 || (K > 0 && !act_idx)) return USAF_ERR_INVALID_ARG;
+  if (!(dense_density > 0.0)) return USAF_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(plan) & 255) != 0) return USAF_ERR_INVALID_ARG;
+  if (K > s->E * 3 * s->I * s->H) return USAF_ERR_INVALID_ARG;
+  if (plan_bytes < masked_plan_bytes(*s)) return USAF_ERR_WORKSPACE;
+  const double thr = std::ceil(dense_density * (double)(3 * s->I * s->H));
+  const int64_t thr_count = thr > 9.0e18 ? INT64_MAX : std::max<int64_t>(1, (int64_t)thr);
+  return masked_plan_build_launch(*s, act_idx, K, thr_count, plan,
+                                  static_cast<cudaStream_t>(stream));
+}
+
+usaf_status usaf_moe_bwd_sparse_planned(
+    const usaf_moe_shape* s, usaf_dtype dt, int renorm, const void* x, const float* w_router,
+    const void* w_gate_up, const void* w_down, const usaf_routing* rt, const float* logits,
+    const void* x_perm_save, const void* h_save, const void* wa_save, const void* dy,
+    const int64_t* act_idx, int64_t K, float* g_act, float* g_router, void* dx, float* dw_slot,
+    int accumulate, const void* plan, int64_t n_dense, uint32_t* dev_status, void* ws,
+    size_t ws_bytes, void* stream) {
+  MoeArgs a{};
+  USAF_TRY(fill_args(a, s, dt, x, w_router, w_gate_up, w_down, rt));
+  a.status = dev_status;
+  if (renorm != 0 && renorm != 1) return USAF_ERR_INVALID_ARG;
+  if (accumulate != 0 && accumulate != 1) return USAF_ERR_INVALID_ARG;
+  if (!w_router || !x_perm_save || !h_save || !wa_save || !dy || !g_router)
+    return USAF_ERR_INVALID_ARG;
+  if (renorm == 0 && !logits) return USAF_ERR_INVALID_ARG;
+  const int64_t N = s->E * 3 * s->I * s->H;
+  if (K < 0 || K > N || (K > 0 && (!act_idx || !g_act))) return USAF_ERR_INVALID_ARG;
+  if (n_dense < 0 || n_dense > s->E || (n_dense > 0 && !plan)) return USAF_ERR_INVALID_ARG;
+  if (plan && (reinterpret_cast<uintptr_t>(plan) & 255) != 0) return USAF_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < usaf_moe_bwd_workspace_size(s, dt, K)) return USAF_ERR_WORKSPACE;
+  USAF_TRY(debug_validate(act_idx, K, N, dev_status, stream));
+  Carver c(ws);
+  BwdWs w;
+  bwd_ws_layout(*s, dt, K, c, w);
+  MaskedPlan mp{};
+  if (n_dense > 0) mp = masked_plan_layout(*s, const_cast<void*>(plan));
+  return moe_bwd_launch(a, renorm, logits, x_perm_save, h_save, wa_save, dy, act_idx, K, g_act,
+                        g_router, dx, dw_slot, nullptr, accumulate, dev_status, w,
+                        static_cast<cudaStream_t>(stream), n_dense > 0 ? &mp : nullptr,
+                        n_dense);
 }
 
 usaf_status usaf_moe_bwd_dense(const usaf_moe_shape* s, usaf_dtype dt, int renorm, const void* x,

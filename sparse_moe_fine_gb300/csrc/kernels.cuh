@@ -59,15 +59,33 @@ struct MoeArgs {
   uint32_t* status;  // device status word of the call (may be null): bounded waits that give up
 };
 
+// The masked-gradient plan of an active set (built by usaf_masked_plan_build): the experts whose
+// active density makes a dense tensor-core tile cheaper than per-entry dot products, and for
+// those the first active entry of every row. row_ptr per expert: gate_up rows 0 .. 2I (2I + 1
+// values, the last the end of the expert's gate_up entries), then down rows 0 .. H.
+struct MaskedPlan {
+  const int32_t* n_dense;     // device: number of listed experts
+  const int32_t* dense_list;  // [E]
+  const int32_t* dense_flag;  // [E] 1 for listed experts
+  const int64_t* row_ptr;     // [E][rp_stride]
+  int64_t rp_stride;          // 2I + H + 2
+};
+size_t masked_plan_bytes(const usaf_moe_shape& s);
+MaskedPlan masked_plan_layout(const usaf_moe_shape& s, void* base);
+usaf_status masked_plan_build_launch(const usaf_moe_shape& s, const int64_t* act, int64_t K,
+                                     int64_t thr_count, void* plan, cudaStream_t st);
+
 // weights_ready (may be null): the kernels that read the expert weights wait for it; the token
 // gather before them does not
 usaf_status moe_fwd_launch(const MoeArgs& a, void* x_perm, void* h, void* wa, void* y, FwdWs& w,
                            cudaEvent_t weights_ready, cudaStream_t st);
+// plan / n_dense: the masked-gradient plan of act_idx and its number of dense experts as the
+// host read it (0: every entry by the sparse kernel, plan unused)
 usaf_status moe_bwd_launch(const MoeArgs& a, int renorm, const float* logits, const void* x_perm,
                            const void* h, const void* wa, const void* dy, const int64_t* act_idx,
                            int64_t K, float* g_act, float* g_router, void* dx, float* dw_slot,
                            float* g_dense, int accumulate, uint32_t* dev_status, BwdWs& w,
-                           cudaStream_t st);
+                           cudaStream_t st, const MaskedPlan* plan = nullptr, int64_t n_dense = 0);
 usaf_status moe_wgrad_dense_launch(const MoeArgs& a, const void* x_perm, const void* wa,
                                    float* g_dense, int accumulate, BwdWs& w, cudaStream_t st);
 
@@ -85,6 +103,10 @@ usaf_status tc_bwd_dx(const MoeArgs& a, const void* dh, float* dx_acc, cudaStrea
 // dense expert weight gradient g[e] (a_rows x b_rows, fp32) = aT . bT^T over each expert's tokens
 usaf_status tc_wgrad_dense(const MoeArgs& a, const void* aT, int64_t a_rows, const void* bT,
                            int64_t b_rows, float* g, int accumulate, cudaStream_t st);
+// the gradient at the active entries of the plan's dense experts: tensor 0 gate_up, 1 down
+usaf_status tc_wgrad_gather(const MoeArgs& a, const void* aT, int64_t a_rows, const void* bT,
+                            int64_t b_rows, const MaskedPlan& plan, int tensor, const int64_t* act,
+                            float* g_act, int accumulate, cudaStream_t st);
 // one CTA whose bounded wait runs out on purpose (see usaf_diag_bounded_wait)
 usaf_status diag_wait_launch(int64_t limit_cycles, uint32_t* status, cudaStream_t st);
 

@@ -447,7 +447,8 @@ __global__ void __launch_bounds__(SD_WARPS * 32, SD_BLOCKS_PER_SM) sddmm_kernel(
     const int64_t* __restrict__ act, int64_t K, const int32_t* __restrict__ cnt,
     const int32_t* __restrict__ off, int E, int H, int I, int64_t Ngu, int64_t rcap,
     const T* __restrict__ dhT, const T* __restrict__ xT, const T* __restrict__ dyT,
-    const T* __restrict__ waT, float* __restrict__ g_act, int accumulate, uint32_t* dev_status) {
+    const T* __restrict__ waT, float* __restrict__ g_act, int accumulate, uint32_t* dev_status,
+    const int32_t* __restrict__ dense_flag) {
   constexpr int VW = 16 / sizeof(T);
   constexpr int U = 2;  // entries whose loads are in flight together in a full pass
   constexpr uint32_t FULL = 0xffffffffu;
@@ -457,6 +458,7 @@ __global__ void __launch_bounds__(SD_WARPS * 32, SD_BLOCKS_PER_SM) sddmm_kernel(
   const int64_t kgu = count_below(act, K, Ngu, lane);
   const int64_t nb_gu = (kgu + 31) / 32, nb = nb_gu + (K - kgu + 31) / 32;
   bool bad = false, badidx = false;
+  uint32_t skipm = 0;  // entries of the batch left to the dense tile kernel (not stored here)
   for (int64_t bt = (int64_t)blockIdx.x * SD_WARPS + wid; bt < nb;
        bt += (int64_t)gridDim.x * SD_WARPS) {
     const bool gu = bt < nb_gu;
@@ -472,7 +474,13 @@ __global__ void __launch_bounds__(SD_WARPS * 32, SD_BLOCKS_PER_SM) sddmm_kernel(
       // is flagged and gets a zero gradient; it is never decoded into addresses
       const bool inr = f >= 0 && f < (gu ? Ngu : (int64_t)E * H * I);
       badidx |= q < lim && !inr;
-      if (q < lim && inr) {
+      bool mine_dense = false;  // the entry's expert is formed by the dense tile kernel
+      if (q < lim && inr && dense_flag) {
+        const int64_t per = gu ? (int64_t)2 * I * H : (int64_t)H * I;
+        mine_dense = dense_flag[(int)(f / per)] != 0;
+      }
+      skipm = __ballot_sync(FULL, mine_dense);
+      if (q < lim && inr && !mine_dense) {
         const int64_t wcols = gu ? H : I, wrows = gu ? 2 * I : H;
         int64_t col, arow;
         int e;
@@ -572,7 +580,7 @@ __global__ void __launch_bounds__(SD_WARPS * 32, SD_BLOCKS_PER_SM) sddmm_kernel(
       }
       const float gsum = transpose_reduce<SD_G>(part, lane) + rem;
       const int64_t q = b0 + SD_G * hf + lane;
-      if (lane < SD_G && q < lim) {
+      if (lane < SD_G && q < lim && !((skipm >> (SD_G * hf + lane)) & 1u)) {
         const float gv = accumulate ? g_act[q] + gsum : gsum;
         g_act[q] = gv;
         bad |= !finite_f(gv);
@@ -916,7 +924,7 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
                              const T* hT, const T* waT, const T* dy, const int64_t* act_idx,
                              int64_t K, float* g_act, float* g_router, T* dx, float* dw_out,
                              float* g_dense, int accumulate, uint32_t* dev_status, BwdWs& w,
-                             cudaStream_t st) {
+                             cudaStream_t st, const MaskedPlan* plan, int64_t n_dense) {
   MoeArgs a = a0;
   a.plan = w.plan;
   a.wperm = w.wperm;
@@ -995,13 +1003,22 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
   }
   // S9, S10: expert weight gradients at the active set
   if (K > 0) {
-    USAF_TRACE("wgrad_sddmm", st);
-    const unsigned blocks = (unsigned)std::min<int64_t>(ceil_div(K, SD_WARPS * 32),
-                                                        device_sm_count() * SD_BLOCKS_PER_SM);
-    sddmm_kernel<T><<<blocks, SD_WARPS * 32, 0, st>>>(act_idx, K, cnt, off, E, H, I, Ngu, a.R_cap,
-                                                      dhT, xT, dyT, waT, g_act, accumulate,
-                                                      dev_status);
-    USAF_CHECK_LAUNCH();
+    const bool use_plan = plan && n_dense > 0 && a.dt == USAF_BF16;
+    {
+      USAF_TRACE("wgrad_sddmm", st);
+      const unsigned blocks = (unsigned)std::min<int64_t>(ceil_div(K, SD_WARPS * 32),
+                                                          device_sm_count() * SD_BLOCKS_PER_SM);
+      sddmm_kernel<T><<<blocks, SD_WARPS * 32, 0, st>>>(
+          act_idx, K, cnt, off, E, H, I, Ngu, a.R_cap, dhT, xT, dyT, waT, g_act, accumulate,
+          dev_status, use_plan ? plan->dense_flag : nullptr);
+      USAF_CHECK_LAUNCH();
+    }
+    if (use_plan) {
+      // the experts whose active density makes a dense tile cheaper: tensor-core tiles, the
+      // accumulator written at the active entries only
+      USAF_TRY(tc_wgrad_gather(a, dhT, 2 * I, xT, H, *plan, 0, act_idx, g_act, accumulate, st));
+      USAF_TRY(tc_wgrad_gather(a, dyT, H, waT, I, *plan, 1, act_idx, g_act, accumulate, st));
+    }
   }
   // dense expert weight gradients (importance phase)
   if (g_dense) {
@@ -1056,18 +1073,127 @@ usaf_status moe_bwd_launch(const MoeArgs& a, int renorm, const float* logits, co
                            const void* h, const void* wa, const void* dy, const int64_t* act_idx,
                            int64_t K, float* g_act, float* g_router, void* dx, float* dw_slot,
                            float* g_dense, int accumulate, uint32_t* dev_status, BwdWs& w,
-                           cudaStream_t st) {
+                           cudaStream_t st, const MaskedPlan* plan, int64_t n_dense) {
   using B = __nv_bfloat16;
   if (a.dt == USAF_BF16)
     return moe_bwd_t<B>(a, renorm, logits, static_cast<const B*>(x_perm),
                         static_cast<const B*>(h), static_cast<const B*>(wa),
                         static_cast<const B*>(dy), act_idx, K, g_act, g_router,
-                        static_cast<B*>(dx), dw_slot, g_dense, accumulate, dev_status, w, st);
+                        static_cast<B*>(dx), dw_slot, g_dense, accumulate, dev_status, w, st,
+                        plan, n_dense);
   return moe_bwd_t<float>(a, renorm, logits, static_cast<const float*>(x_perm),
                           static_cast<const float*>(h), static_cast<const float*>(wa),
                           static_cast<const float*>(dy), act_idx, K, g_act, g_router,
                           static_cast<float*>(dx), dw_slot, g_dense, accumulate, dev_status, w,
-                          st);
+                          st, nullptr, 0);
+}
+
+// ================================================================================================
+// Masked-gradient plan of an active set
+// ================================================================================================
+size_t masked_plan_bytes(const usaf_moe_shape& s) {
+  Carver c(nullptr);
+  c.take<int64_t>(4);
+  c.take<int32_t>(s.E);
+  c.take<int32_t>(s.E);
+  c.take<int64_t>(s.E * (2 * s.I + s.H + 2));
+  return c.size();
+}
+
+MaskedPlan masked_plan_layout(const usaf_moe_shape& s, void* base) {
+  Carver c(base);
+  MaskedPlan p{};
+  int64_t* head = c.take<int64_t>(4);
+  p.dense_list = c.take<int32_t>(s.E);
+  p.dense_flag = c.take<int32_t>(s.E);
+  p.row_ptr = c.take<int64_t>(s.E * (2 * s.I + s.H + 2));
+  p.n_dense = reinterpret_cast<const int32_t*>(head + 1);  // head[0]: the same count as int64
+  p.rp_stride = 2 * s.I + s.H + 2;
+  return p;
+}
+
+__device__ __forceinline__ int64_t lower_bound_act(const int64_t* a, int64_t lo, int64_t hi,
+                                                   int64_t key) {
+  while (lo < hi) {
+    const int64_t mid = (lo + hi) >> 1;
+    if (a[mid] < key) lo = mid + 1;
+    else hi = mid;
+  }
+  return lo;
+}
+
+// One block, one thread per expert (E <= 1024): the expert's active entries in both tensors; an
+// expert with at least thr_count of them is listed (in expert order) for the dense tile kernel.
+__global__ void __launch_bounds__(1024) plan_experts_kernel(const int64_t* __restrict__ act,
+                                                            int64_t K, int E, int H, int I,
+                                                            int64_t thr_count, int64_t* head,
+                                                            int32_t* dense_list,
+                                                            int32_t* dense_flag) {
+  __shared__ int32_t wsum[32];
+  const int e = threadIdx.x, lane = e & 31, wid = e >> 5;
+  int32_t dense = 0;
+  if (e < E) {
+    const int64_t pgu = (int64_t)2 * I * H, pd = (int64_t)H * I, Ngu = (int64_t)E * pgu;
+    const int64_t a0 = lower_bound_act(act, 0, K, (int64_t)e * pgu);
+    const int64_t a1 = lower_bound_act(act, a0, K, (int64_t)(e + 1) * pgu);
+    const int64_t b0 = lower_bound_act(act, 0, K, Ngu + (int64_t)e * pd);
+    const int64_t b1 = lower_bound_act(act, b0, K, Ngu + (int64_t)(e + 1) * pd);
+    dense = (a1 - a0) + (b1 - b0) >= thr_count ? 1 : 0;
+    dense_flag[e] = dense;
+  }
+  int32_t x = dense;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int32_t v = lane < (int)(blockDim.x >> 5) ? wsum[lane] : 0;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    wsum[lane] = v;
+  }
+  __syncthreads();
+  const int32_t before = x - dense + (wid > 0 ? wsum[wid - 1] : 0);
+  if (dense) dense_list[before] = e;
+  if (e == (int)blockDim.x - 1) {
+    const int32_t total = wsum[(blockDim.x >> 5) - 1];
+    head[0] = total;
+    reinterpret_cast<int32_t*>(head + 1)[0] = total;
+  }
+}
+
+// First active entry of every row of the listed experts (gate_up rows 0 .. 2I, down rows 0 .. H).
+__global__ void plan_rows_kernel(const int64_t* __restrict__ act, int64_t K, int E, int H, int I,
+                                 const int32_t* __restrict__ dense_flag, int64_t stride,
+                                 int64_t* __restrict__ row_ptr) {
+  const int e = blockIdx.y;
+  if (!dense_flag[e]) return;
+  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= stride) return;
+  const int64_t pgu = (int64_t)2 * I * H, pd = (int64_t)H * I, Ngu = (int64_t)E * pgu;
+  const int64_t f = r <= 2 * I ? (int64_t)e * pgu + r * H
+                               : Ngu + (int64_t)e * pd + (r - (2 * I + 1)) * I;
+  row_ptr[(int64_t)e * stride + r] = lower_bound_act(act, 0, K, f);
+}
+
+usaf_status masked_plan_build_launch(const usaf_moe_shape& s, const int64_t* act, int64_t K,
+                                     int64_t thr_count, void* plan, cudaStream_t st) {
+  USAF_TRACE("masked_plan", st);
+  const MaskedPlan p = masked_plan_layout(s, plan);
+  int64_t* head = static_cast<int64_t*>(plan);
+  plan_experts_kernel<<<1, 1024, 0, st>>>(act, K, (int)s.E, (int)s.H, (int)s.I, thr_count, head,
+                                          const_cast<int32_t*>(p.dense_list),
+                                          const_cast<int32_t*>(p.dense_flag));
+  USAF_CHECK_LAUNCH();
+  const dim3 grid((unsigned)ceil_div(p.rp_stride, 256), (unsigned)s.E);
+  plan_rows_kernel<<<grid, 256, 0, st>>>(act, K, (int)s.E, (int)s.H, (int)s.I, p.dense_flag,
+                                         p.rp_stride, const_cast<int64_t*>(p.row_ptr));
+  USAF_CHECK_LAUNCH();
+  return USAF_OK;
 }
 
 }  // namespace usaf

@@ -727,6 +727,15 @@ struct WgParams {
   int MT, NT;          // tiles per expert along M (128) and N (256)
   int accumulate;      // 1: add into the output (TMA reduce), 0: overwrite (TMA store)
   uint32_t* status;
+  // gather form (the gradient is wanted only at the active entries of some experts):
+  const int32_t* dlist;   // the experts to form, dlist[0 .. *n_list)
+  const int32_t* n_list;
+  const int64_t* row_ptr;  // per expert [rp_stride]: first active entry of each row
+  int64_t rp_stride;
+  int rp_off;              // this tensor's first row in row_ptr (0 gate_up, 2I down)
+  const int64_t* act;      // the sorted active set
+  int64_t flat0;           // flat index of this tensor's entry (0, 0, 0)
+  float* g_act;            // gradient at the active entries
 };
 
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1,
@@ -745,6 +754,10 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
         : "memory");
 }
 
+// GATHER = true: the tiles of the experts in p.dlist only, and the epilogue writes the
+// accumulator at the active entries (g_act) instead of storing the tile: each lane walks its
+// row's active entries from row_ptr, the entries of a 32-column chunk taken in column order.
+template <bool GATHER>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_wgrad_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmO, const WgParams p) {
@@ -784,7 +797,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const int per_e = p.MT * p.NT;
-  const int total = p.E * per_e;
+  const int total = (GATHER ? *p.n_list : p.E) * per_e;
+  auto expert_of = [&](int t) { return GATHER ? p.dlist[t / per_e] : t / per_e; };
   bool failed = false;
   if (warp == 0) {
     if (lane == 0) {
@@ -792,7 +806,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       int stage = 0;
       uint32_t phase = 0, issued = 0;
       for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
-        const int e = t / per_e, r = t % per_e, mt = r / p.NT, nt = r % p.NT;
+        const int e = expert_of(t), r = t % per_e, mt = r / p.NT, nt = r % p.NT;
         const int o = p.off[e], npad = p.off[e + 1] - o;
         const int nkb = (npad + BK - 1) / BK;
         for (int kb = 0; kb < nkb; ++kb) {
@@ -829,7 +843,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0, acc_phase = 0;
       const uint32_t idesc = idesc_bf16(256, false, false);
       for (int t = blockIdx.x; t < total && !failed; t += gridDim.x) {
-        const int e = t / per_e;
+        const int e = expert_of(t);
         const int npad = p.off[e + 1] - p.off[e];
         const int nkb = (npad + BK - 1) / BK;
         if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag)) {
@@ -878,7 +892,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int acc = 0, nstore = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
-      const int e = t / per_e, r = t % per_e, mt = r / p.NT, nt = r % p.NT;
+      const int e = expert_of(t), r = t % per_e, mt = r / p.NT, nt = r % p.NT;
       const bool empty = p.off[e + 1] == p.off[e];
       int ok = 1;
       if (lane == 0) {
@@ -892,6 +906,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) + acc * 256;
+      if constexpr (GATHER) {
+        // this lane's row of the tile and its active entries, walked chunk by chunk
+        const int row = mt * 128 + q * 32 + lane;
+        const bool live = row < p.M;
+        const int64_t* rp = p.row_ptr + (int64_t)e * p.rp_stride + p.rp_off;
+        int64_t ptr = live ? rp[row] : 0, end = live ? rp[row + 1] : 0;
+        const int64_t rbase = p.flat0 + ((int64_t)e * p.M + row) * p.N;
+        for (int ch = half; ch < 8; ch += 2) {
+          const int c0 = nt * 256 + ch * 32;
+          if (c0 >= p.N || mt * 128 + q * 32 >= p.M) continue;
+          const int64_t fb = rbase + c0;  // flat index of (row, c0)
+          while (ptr < end && p.act[ptr] < fb) ++ptr;  // entries of the other half's chunks
+          int64_t f = ptr < end ? p.act[ptr] : INT64_MAX;
+          if (!__any_sync(0xffffffffu, f < fb + 32)) continue;  // no entry in this chunk
+          float v[32];
+          if (!empty) {
+            tmem_ld32(taddr + ch * 32, v);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
+          }
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (f == fb + j) {
+              p.g_act[ptr] = p.accumulate ? p.g_act[ptr] + v[j] : v[j];
+              ++ptr;
+              f = ptr < end ? p.act[ptr] : INT64_MAX;
+            }
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty0 + 8 * acc);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+        continue;
+      }
       for (int ch = half; ch < 8; ch += 2) {
         const int c0 = nt * 256 + ch * 32;
         const int r0 = mt * 128 + q * 32;
@@ -1476,12 +1529,49 @@ usaf_status tc_wgrad_dense(const MoeArgs& a, const void* aT, int64_t a_rows, con
   p.status = a.status;
   static bool attr_done = false;
   if (!attr_done) {
-    if (cudaFuncSetAttribute(tc_wgrad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(tc_wgrad_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              wg::SMEM) != cudaSuccess)
       return USAF_ERR_CUDA;
     attr_done = true;
   }
-  tc_wgrad_kernel<<<device_sm_count(), NUM_THREADS, wg::SMEM, st>>>(ma, mb, mo, p);
+  tc_wgrad_kernel<false><<<device_sm_count(), NUM_THREADS, wg::SMEM, st>>>(ma, mb, mo, p);
+  USAF_CHECK_LAUNCH();
+  return USAF_OK;
+}
+
+usaf_status tc_wgrad_gather(const MoeArgs& a, const void* aT, int64_t a_rows, const void* bT,
+                            int64_t b_rows, const MaskedPlan& plan, int tensor, const int64_t* act,
+                            float* g_act, int accumulate, cudaStream_t st) {
+  USAF_TRACE(tensor == 0 ? "tc_wgrad_gather_gate_up" : "tc_wgrad_gather_down", st);
+  CUtensorMap ma, mb;
+  if (!map_2d(&ma, aT, a.R_cap, a_rows, 64, 128) || !map_2d(&mb, bT, a.R_cap, b_rows, 64, 256))
+    return USAF_ERR_CUDA;
+  WgParams p{};
+  p.off = a.rt.expert_offset;
+  p.E = (int)a.s.E;
+  p.M = (int)a_rows;
+  p.N = (int)b_rows;
+  p.MT = (int)ceil_div(a_rows, 128);
+  p.NT = (int)ceil_div(b_rows, 256);
+  p.accumulate = accumulate;
+  p.status = a.status;
+  p.dlist = plan.dense_list;
+  p.n_list = plan.n_dense;
+  p.row_ptr = plan.row_ptr;
+  p.rp_stride = plan.rp_stride;
+  p.rp_off = tensor == 0 ? 0 : (int)(2 * a.s.I + 1);
+  p.act = act;
+  p.flat0 = tensor == 0 ? 0 : a.s.E * 2 * a.s.I * a.s.H;
+  p.g_act = g_act;
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(tc_wgrad_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             wg::SMEM) != cudaSuccess)
+      return USAF_ERR_CUDA;
+    attr_done = true;
+  }
+  // the output map is not used by the gather form; ma is passed in its place
+  tc_wgrad_kernel<true><<<device_sm_count(), NUM_THREADS, wg::SMEM, st>>>(ma, mb, ma, p);
   USAF_CHECK_LAUNCH();
   return USAF_OK;
 }

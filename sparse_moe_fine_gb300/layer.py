@@ -49,7 +49,8 @@ def allreduce_dense_grad(g_dense, group=None):
 
 class MoELayer:
     def __init__(self, T, H, E, k, I, w_gate_up, w_down, w_router, act_idx, lr=1e-4,
-                 betas=(0.9, 0.999), eps=1e-8, renorm=1, device="cuda", group=None):
+                 betas=(0.9, 0.999), eps=1e-8, renorm=1, device="cuda", group=None,
+                 dense_density=0.015):
         self.dev = torch.device(device)
         self.s = B.shape(T, H, E, k, I)
         self.T, self.H, self.E, self.k, self.I = T, H, E, k, I
@@ -62,6 +63,9 @@ class MoELayer:
         self.N = E * 3 * I * H
         self.lr, self.betas, self.eps, self.renorm = lr, betas, eps, renorm
         self.group = group  # data-parallel process group (None: one replica)
+        # experts whose active entries are at least this fraction of their weights get their
+        # masked gradient from dense tensor-core tiles (usaf_masked_plan_build)
+        self.dense_density = dense_density
         self.step_count = 0
         d = self.dev
         cap = B.routed_rows_capacity(self.s)
@@ -117,6 +121,14 @@ class MoELayer:
             m = torch.zeros(K, device=self.dev)
             v = torch.zeros(K, device=self.dev)
         self.p, self.m, self.v = p, m, v
+        # the masked-gradient plan of this set; its expert count is read once, here
+        self.plan = torch.empty(max(1, B.masked_plan_size(self.s)), dtype=torch.uint8,
+                                device=self.dev)
+        if self.dt == B.BF16 and K > 0:
+            B.masked_plan_build(self.s, self.act, self.dense_density, self.plan)
+            self.n_dense = B.masked_plan_count(self.plan)
+        else:
+            self.n_dense = 0
         self.g_act = torch.empty(K, device=self.dev)
         self.ws_bwd = torch.empty(B.moe_bwd_workspace_size(self.s, self.dt, K),
                                   dtype=torch.uint8, device=self.dev)
@@ -136,7 +148,8 @@ class MoELayer:
                 "w_router": cpu(self.w_router), "act": cpu(self.act), "p": cpu(self.p),
                 "m": cpu(self.m), "v": cpu(self.v), "r_p": cpu(self.r_p), "r_m": cpu(self.r_m),
                 "r_v": cpu(self.r_v), "step_count": self.step_count, "lr": self.lr,
-                "betas": tuple(self.betas), "eps": self.eps, "renorm": self.renorm}
+                "betas": tuple(self.betas), "eps": self.eps, "renorm": self.renorm,
+                "dense_density": self.dense_density}
 
     @classmethod
     def from_checkpoint(cls, ck: dict, device="cuda", group=None) -> "MoELayer":
@@ -144,7 +157,8 @@ class MoELayer:
         d = torch.device(device)
         L = cls(T, H, E, k, I, ck["w_gate_up"].to(d), ck["w_down"].to(d), ck["w_router"].to(d),
                 ck["act"].to(d), lr=ck["lr"], betas=ck["betas"], eps=ck["eps"],
-                renorm=ck["renorm"], device=d, group=group)
+                renorm=ck["renorm"], device=d, group=group,
+                dense_density=ck.get("dense_density", 0.015))
         L.set_active(ck["act"].to(d), ck["p"].to(d), ck["m"].to(d), ck["v"].to(d))
         L.r_p.copy_(ck["r_p"])
         L.r_m.copy_(ck["r_m"])
@@ -192,11 +206,18 @@ class MoELayer:
     def backward(self, x, dy, want_dx=True, stream=None, dx=None):
         dx = self.dx if dx is None else dx
         self._check_tokens(x=x, dy=dy, dx=dx)
-        B.moe_bwd_sparse(self.s, x, self.w_router, self.w_gate_up, self.w_down, self.rt,
-                         self.x_perm, self.h, self.wa, dy, self.act, self.g_act, self.g_router,
-                         dx=dx if want_dx else None, logits=self.logits,
-                         renorm=self.renorm, dev_status=self.status, ws=self.ws_bwd,
-                         stream=stream)
+        self.backward_into(x, dy, accumulate=0, dx=dx if want_dx else None, stream=stream)
+
+    def backward_into(self, x, dy, accumulate=0, dx=None, stream=None, dev_status=None):
+        """The sparse backward with this set's masked-gradient plan; accumulate = 1 adds into
+        g_act and g_router (micro-batches)."""
+        B.moe_bwd_sparse_planned(self.s, x, self.w_router, self.w_gate_up, self.w_down, self.rt,
+                                 self.x_perm, self.h, self.wa, dy, self.act, self.g_act,
+                                 self.g_router, plan=self.plan, n_dense=self.n_dense,
+                                 accumulate=accumulate, dx=dx, logits=self.logits,
+                                 renorm=self.renorm,
+                                 dev_status=self.status if dev_status is None else dev_status,
+                                 ws=self.ws_bwd, stream=stream)
 
     def optimizer_step(self, stream=None, skip_if_nonfinite=1):
         """Router update on the calling stream (the next routing reads it); expert update on the
@@ -269,10 +290,7 @@ class MoELayer:
         with torch.cuda.graph(g_body, stream=cs):
             B.moe_fwd(self.s, x, self.w_gate_up, self.w_down, self.rt, self.x_perm, self.h,
                       self.wa, self.y, ws=self.ws_fwd, stream=cs, dev_status=status)
-            B.moe_bwd_sparse(self.s, x, self.w_router, self.w_gate_up, self.w_down, self.rt,
-                             self.x_perm, self.h, self.wa, dy, self.act, self.g_act,
-                             self.g_router, dx=self.dx, logits=self.logits, renorm=self.renorm,
-                             dev_status=status, ws=self.ws_bwd, stream=cs)
+            self.backward_into(x, dy, accumulate=0, dx=self.dx, stream=cs, dev_status=status)
         main.wait_stream(cs)
         return g_route, g_body, B.launch_count() - n0  # library kernels in the two graphs
 

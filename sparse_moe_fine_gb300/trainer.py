@@ -64,11 +64,8 @@ class StackTrainer:
         for i in reversed(range(len(self.layers))):
             L = self.layers[i]
             x = inputs[i]
-            fn = B.moe_bwd_sparse if first else B.moe_bwd_sparse_accumulate
             dx = L.dx if i > 0 else None  # the bottom layer's input needs no gradient
-            fn(L.s, x, L.w_router, L.w_gate_up, L.w_down, L.rt, L.x_perm, L.h, L.wa, dy, L.act,
-               L.g_act, L.g_router, dx=dx, logits=L.logits, renorm=L.renorm,
-               dev_status=L.status, ws=L.ws_bwd)
+            L.backward_into(x, dy, accumulate=0 if first else 1, dx=dx)
             if dense:
                 # the importance phase's dense gradient of this micro-batch, accumulated, from
                 # the dh and permuted dy the sparse call just left in the layer's workspace

@@ -18,7 +18,7 @@ fake_addresses = pytest.mark.skipif(torch.cuda.is_available(),
 def test_library_exports_every_header_symbol():
     L = B.lib()
     syms = B.header_symbols()
-    assert len(syms) == 27
+    assert len(syms) == 30
     for s in syms:
         assert hasattr(L, s), s
     assert L.usaf_abi_version() == 2

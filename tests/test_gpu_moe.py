@@ -16,7 +16,7 @@ from _gpu import device, max_rel, max_rel_terms, rel_l2, to_dev
 pytestmark = pytest.mark.gpu
 
 
-def run_layer(cfg, inp, act_idx, logits, dev, renorm=1, want_dx=True):
+def run_layer(cfg, inp, act_idx, logits, dev, renorm=1, want_dx=True, plan_density=None):
     s = B.shape(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I)
     bf = cfg.bf16
     dt = torch.bfloat16 if bf else torch.float32
@@ -43,13 +43,22 @@ def run_layer(cfg, inp, act_idx, logits, dev, renorm=1, want_dx=True):
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     dtc = B.BF16 if bf else B.F32
     ws = torch.empty(B.moe_bwd_workspace_size(s, dtc, K), dtype=torch.uint8, device=dev)
-    B.moe_bwd_sparse(s, x, wr, wgu, wd, rt, xp, h, wa, dy, act, g_act, g_r, dx=dx, dw_slot=dw,
-                     logits=li, renorm=renorm, dev_status=st, ws=ws)
+    n_dense = None
+    if plan_density is None:
+        B.moe_bwd_sparse(s, x, wr, wgu, wd, rt, xp, h, wa, dy, act, g_act, g_r, dx=dx,
+                         dw_slot=dw, logits=li, renorm=renorm, dev_status=st, ws=ws)
+    else:
+        plan = torch.empty(B.masked_plan_size(s), dtype=torch.uint8, device=dev)
+        B.masked_plan_build(s, act, plan_density, plan)
+        n_dense = B.masked_plan_count(plan)
+        B.moe_bwd_sparse_planned(s, x, wr, wgu, wd, rt, xp, h, wa, dy, act, g_act, g_r,
+                                 plan=plan, n_dense=n_dense, dx=dx, dw_slot=dw, logits=li,
+                                 renorm=renorm, dev_status=st, ws=ws)
     torch.cuda.synchronize()
     out = {"Y": y.float().cpu().numpy(), "g_act": g_act.cpu().numpy(),
            "g_router": g_r.cpu().numpy(), "dw": dw.cpu().numpy().reshape(cfg.T, cfg.k),
            "status": int(st.item()), "idx": rt.topk_idx.cpu().numpy().reshape(cfg.T, cfg.k),
-           "count": rt.expert_count.cpu().numpy()}
+           "count": rt.expert_count.cpu().numpy(), "n_dense": n_dense}
     if renorm:  # the device's dlogit at the selected experts, slot order
         off = B.moe_bwd_dlogit_offset(s, dtc, K)
         dl = ws[off:off + 4 * cfg.T * cfg.k].view(torch.float32)
@@ -610,3 +619,96 @@ def test_wgrad_dense_from_the_sparse_backward_workspace(bf16):
     assert np.array_equal(g1n, 2 * g2n) or rel_l2(g1n, 2 * g2n) <= 1e-6
     ref, _ = oracle_dense(cfg, inp, logits)
     assert rel_l2(g2n, ref) <= (1e-2 if bf16 else 1e-5)
+
+
+def _expert_of(act, cfg):
+    gu = act < cfg.N_gu
+    return np.where(gu, act // (2 * cfg.I * cfg.H), (act - cfg.N_gu) // (cfg.H * cfg.I))
+
+
+def test_planned_backward_reads_dense_experts_from_tiles():
+    """An active set concentrated on two experts (6% of their weights; 0.5% elsewhere) with the
+    masked-gradient plan at 1.5%: the two are read out of dense tensor-core tiles, the rest from
+    the sparse kernel. Against the oracle (bf16 bound), against the unplanned call (the same
+    products, fp32 sums in another order), and with micro-batch accumulation. One listed expert
+    receives no token (its entries get zero). H = 256 and I = 192 leave partial row and column
+    tiles in both tensors."""
+    dev = device()
+    cfg = synth.small_config("planned", T=1024, H=256, E=8, k=2, I=192, bf16=True, frac=0.02)
+    inp = synth.moe_inputs(cfg, seed=33)
+    logits = oracle.router_logits(inp["x"], inp["w_router"])
+    logits[:, 6] = -1e3  # expert 6 gets no token
+    act = synth.concentrated_mask(cfg, [1, 5, 6], 0.8, seed=33)
+    plain = run_layer(cfg, inp, act, logits, dev)
+    got = run_layer(cfg, inp, act, logits, dev, plan_density=0.015)
+    assert got["n_dense"] == 3 and got["status"] == 0 and got["count"][6] == 0
+    idx, b, g = oracle_layer(cfg, inp, act, logits)
+    assert rel_l2(got["g_act"], g) <= 1e-2
+    assert rel_l2(got["g_act"], plain["g_act"]) <= 1e-5
+    e_of = _expert_of(act, cfg)
+    assert (got["g_act"][e_of == 6] == 0).all()
+    for key in ("g_router", "dw"):
+        assert np.array_equal(got[key], plain[key]), key
+    # a density no expert reaches lists none: the plain sparse backward
+    none = run_layer(cfg, inp, act, logits, dev, plan_density=0.9)
+    assert none["n_dense"] == 0 and np.array_equal(none["g_act"], plain["g_act"])
+
+
+def test_planned_backward_accumulates():
+    dev = device()
+    cfg = synth.small_config("planned_acc", T=512, H=128, E=4, k=2, I=128, bf16=True, frac=0.02)
+    inp = synth.moe_inputs(cfg, seed=34)
+    s = B.shape(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I)
+    act_np = synth.concentrated_mask(cfg, [2], 0.9, seed=34)
+    li = to_dev(oracle.router_logits(inp["x"], inp["w_router"]), dev)
+    bf = lambda a: to_dev(a, dev, True)
+    x, wgu, wd, dy = bf(inp["x"]), bf(inp["w_gate_up"]), bf(inp["w_down"]), bf(inp["dy"])
+    wr = to_dev(inp["w_router"], dev)
+    rt = B.Routing.empty(s, dev)
+    B.route_topk(s, x, wr, rt, logits_in=li)
+    cap = B.routed_rows_capacity(s)
+    xp = torch.empty(cfg.H, cap, dtype=torch.bfloat16, device=dev)
+    h = torch.empty(2 * cfg.I, cap, dtype=torch.bfloat16, device=dev)
+    wa = torch.empty(cfg.I, cap, dtype=torch.bfloat16, device=dev)
+    y = torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev)
+    B.moe_fwd(s, x, wgu, wd, rt, xp, h, wa, y)
+    act = to_dev(act_np, dev)
+    plan = torch.empty(B.masked_plan_size(s), dtype=torch.uint8, device=dev)
+    B.masked_plan_build(s, act, 0.015, plan)
+    nd = B.masked_plan_count(plan)
+    assert nd == 1
+    g1 = torch.empty(act.numel(), device=dev)
+    g_r = torch.empty(cfg.E, cfg.H, device=dev)
+    B.moe_bwd_sparse_planned(s, x, wr, wgu, wd, rt, xp, h, wa, dy, act, g1, g_r, plan=plan,
+                             n_dense=nd, logits=li)
+    g2 = g1.clone()
+    B.moe_bwd_sparse_planned(s, x, wr, wgu, wd, rt, xp, h, wa, dy, act, g2, g_r, plan=plan,
+                             n_dense=nd, accumulate=1, logits=li)
+    torch.cuda.synchronize()
+    assert torch.equal(g2, 2 * g1)
+
+
+def test_skewed_layer_planned_sampled():
+    """The full skewed Qwen3-shaped layer (T 16384, 80% of the active set on the 16 most loaded
+    experts) with the masked-gradient plan: the hot experts are read out of dense tiles. The
+    masked gradients of the least, a middle and the most loaded expert against the oracle."""
+    dev = device()
+    cfg = synth.CONFIGS["qwen3_skewed"]
+    inp = synth.moe_inputs(cfg, seed=0)
+    synth.apply_skew(inp, synth.skew_bias(cfg.E, cfg.extra["zipf_s"], cfg.extra["dead_experts"],
+                                          seed=0))
+    logits = oracle.router_logits(inp["x"], inp["w_router"])
+    idx, w = oracle.route_topk(logits, cfg.k)
+    counts = np.bincount(idx.reshape(-1), minlength=cfg.E)
+    act = skewed_mask(cfg, counts, seed=5)
+    got = run_layer(cfg, inp, act, logits, dev, want_dx=False, plan_density=0.015)
+    assert got["status"] == 0 and got["n_dense"] == 16
+    live = np.nonzero(counts)[0]
+    experts = sorted({int(live[np.argmin(counts[live])]), int(live[len(live) // 2]),
+                      int(np.argmax(counts))})
+    g = oracle.masked_expert_grad(act, inp["x"], inp["w_gate_up"], inp["w_down"], idx, w,
+                                  inp["dy"], experts=experts)
+    sel = ~np.isnan(g)
+    assert sel.sum() > 1000
+    assert rel_l2(got["g_act"][sel], g[sel]) <= 1e-2
+    assert np.isfinite(got["g_act"]).all()
