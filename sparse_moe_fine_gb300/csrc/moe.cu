@@ -341,6 +341,77 @@ __global__ void __launch_bounds__(256, 8) gather_transpose_kernel(
   }
 }
 
+// Gather-transpose of bf16 rows without shared memory: a thread takes 8 permuted rows x 8
+// features (one 16-byte vector of each row), transposes the 8 x 8 block in registers (one byte
+// permute per output word) and writes 8 feature rows of 8 tokens (16 bytes each). Lane l of a
+// warp takes rows 8 (l / 8) .. + 8 of the warp's 32 and features 8 (l % 8) .. + 8, so each load
+// instruction reads 128 contiguous bytes of 4 rows and each store writes 64 contiguous bytes of 8
+// feature rows. A block of 8 warps covers 256 rows x 64 features (H a multiple of 64, R_cap a
+// multiple of 256). Side duties as in gather_transpose_kernel.
+constexpr int GR_ROWS = 256;
+__global__ void __launch_bounds__(256) gather_transpose_bf16_kernel(
+    const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ ptok,
+    const int32_t* __restrict__ pslot, const int32_t* __restrict__ off_end, int64_t R_cap, int H,
+    __nv_bfloat16* __restrict__ xT, const float* __restrict__ topk_w, float* __restrict__ wperm,
+    GatherExtra ex) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  // this thread's first row and first feature
+  const int64_t r0 = (int64_t)blockIdx.x * GR_ROWS + wid * 32 + (lane >> 3) * 8;
+  const int f0 = blockIdx.y * 64 + (lane & 7) * 8;
+  const int64_t end = *off_end;
+  int tok[8];
+  bool live[8];
+  {
+    const int4 t0 = *reinterpret_cast<const int4*>(ptok + r0);
+    const int4 t1 = *reinterpret_cast<const int4*>(ptok + r0 + 4);
+    const int4 s0 = *reinterpret_cast<const int4*>(pslot + r0);
+    const int4 s1 = *reinterpret_cast<const int4*>(pslot + r0 + 4);
+    const int tt[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+    const int ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      live[i] = r0 + i < end && ss[i] >= 0;
+      tok[i] = tt[i];
+    }
+  }
+  uint32_t a[8][4];  // a[i][w]: row i, features 2w and 2w+1
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint4 v = live[i]
+                        ? __ldg(reinterpret_cast<const uint4*>(x + (int64_t)tok[i] * H + f0))
+                        : make_uint4(0, 0, 0, 0);
+    a[i][0] = v.x;
+    a[i][1] = v.y;
+    a[i][2] = v.z;
+    a[i][3] = v.w;
+  }
+  zero_slice(ex.z0, ex.n0);
+  zero_slice(ex.z1, ex.n1);
+  if (ex.plan && blockIdx.x == 0 && blockIdx.y == 0) tile_plan(ex.off, ex.E, ex.plan);
+  if (wperm && blockIdx.y == 0) {
+    for (int r = threadIdx.x; r < GR_ROWS; r += blockDim.x) {
+      const int64_t row = (int64_t)blockIdx.x * GR_ROWS + r;
+      const int sl = row < end ? pslot[row] : -1;
+      wperm[row] = sl >= 0 ? topk_w[sl] : 0.f;
+    }
+  }
+  // feature 2w takes the low halves of word w of rows 2u, 2u+1; feature 2w+1 the high halves
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    uint4 lo, hi;
+    lo.x = __byte_perm(a[0][w], a[1][w], 0x5410);
+    lo.y = __byte_perm(a[2][w], a[3][w], 0x5410);
+    lo.z = __byte_perm(a[4][w], a[5][w], 0x5410);
+    lo.w = __byte_perm(a[6][w], a[7][w], 0x5410);
+    hi.x = __byte_perm(a[0][w], a[1][w], 0x7632);
+    hi.y = __byte_perm(a[2][w], a[3][w], 0x7632);
+    hi.z = __byte_perm(a[4][w], a[5][w], 0x7632);
+    hi.w = __byte_perm(a[6][w], a[7][w], 0x7632);
+    *reinterpret_cast<uint4*>(xT + (int64_t)(f0 + 2 * w) * R_cap + r0) = lo;
+    *reinterpret_cast<uint4*>(xT + (int64_t)(f0 + 2 * w + 1) * R_cap + r0) = hi;
+  }
+}
+
 // The masked-gradient dot products. The bf16 products use the mixed-precision FMA (bf16 sources,
 // fp32 addend and result, sm_100 and later): the product of two bf16 values is exact in fp32, so
 // each step equals an fp32 FMA of the widened values and no unpacking is needed.
@@ -826,6 +897,18 @@ void bwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, int64_t K, Carver& c,
 template <typename T>
 static usaf_status gather_t(const MoeArgs& a, const T* src, T* dstT, cudaStream_t st,
                            GatherExtra ex) {
+  if constexpr (sizeof(T) == 2) {
+    const auto al16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
+    if (a.s.H % 64 == 0 && a.R_cap % GR_ROWS == 0 && al16(src) && al16(dstT) &&
+        al16(a.rt.perm_tok) && al16(a.rt.perm_slot)) {
+      const dim3 grid((unsigned)(a.R_cap / GR_ROWS), (unsigned)(a.s.H / 64));
+      gather_transpose_bf16_kernel<<<grid, 256, 0, st>>>(
+          src, a.rt.perm_tok, a.rt.perm_slot, a.rt.expert_offset + a.s.E, a.R_cap, (int)a.s.H,
+          dstT, a.rt.topk_w, a.wperm, ex);
+      USAF_CHECK_LAUNCH();
+      return USAF_OK;
+    }
+  }
   const dim3 grid((unsigned)ceil_div(a.R_cap, GT_ROWS), (unsigned)ceil_div(a.s.H, 64));
   gather_transpose_kernel<T><<<grid, 256, 0, st>>>(src, a.rt.perm_tok, a.rt.perm_slot,
                                                    a.rt.expert_offset + a.s.E, a.R_cap,
