@@ -399,6 +399,66 @@ usaf_status usaf_reselect_full(const float* g, int64_t N, int64_t K, const int64
                                uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * Selection spread over data-parallel ranks (the importance pass of the README's DataParallel
+ * mode, "Multi-GPU (DataParallel)"; every rank holds the same weights and active set). After a
+ * reduce-scatter of the dense gradient each rank holds a contiguous part g[0, n) of it, at global
+ * offset `base`. The top-K of |g| over all parts (ties to the lower global index) is found by
+ * digit rounds: each rank forms the digit histogram of its part, the histograms are summed over
+ * the ranks, and every rank picks the same digit. A rank's own histograms also give its counts
+ * above and at the final threshold; the tie quota is split in rank order, and each rank emits its
+ * winners, which an all-gather concatenates into the sorted set. The exchanges and the digit
+ * picks are the caller's (see sparse_moe_fine_gb300/dist_select.py); these calls are the per-part
+ * kernels. Keys are |g| as the fp32 bit pattern with the sign cleared. excl (may be NULL): n-bit
+ * bitmap of excluded entries of the part (RigL's grow set excludes the active set), from
+ * usaf_active_bitmap.
+ *   usaf_shard_key_histogram  hist[d] += keys whose bits above shift+bits equal prefix's, by the
+ *                             digit d of `bits` bits at `shift` (1 <= bits <= 11,
+ *                             shift + bits <= 31); hist [2^bits]
+ *   usaf_shard_emit           out[0 .. gt + take_eq) = base + i for the part's keys > tau and its
+ *                             first take_eq keys == tau, ascending; count = gt + eq of the part
+ *                             (sizes the compaction; any value gives the same result: a
+ *                             compaction region that overflows sends the part to the exact
+ *                             whole-part pass and sets USAF_DEV_SELECT_EXACT_PATH)
+ *   usaf_active_bitmap        bitmap [ceil(n/32)] words: bit i set when lo + i is in idx[0, K)
+ * Limits: 0 <= n < 2^32. Errors: INVALID_ARG, WORKSPACE, CUDA.
+ * ------------------------------------------------------------------------------------------- */
+usaf_status usaf_shard_key_histogram(const float* g, int64_t n, const uint32_t* excl,
+                                     uint32_t prefix, int shift, int bits,
+                                     unsigned long long* hist, void* stream);
+size_t usaf_shard_emit_workspace_size(int64_t n, int64_t count);
+usaf_status usaf_shard_emit(const float* g, int64_t n, const uint32_t* excl, uint32_t tau,
+                            int64_t take_eq, int64_t count, int64_t base, int64_t* out,
+                            uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
+usaf_status usaf_active_bitmap(const int64_t* idx, int64_t K, int64_t lo, int64_t n,
+                               uint32_t* bitmap, void* stream);
+
+/* usaf_rigl_apply - usaf_rigl_swap with the grow set given (grown [D], sorted, disjoint from
+ * act_idx, in [0, N); chosen across ranks): the drop selection and the merge, state as
+ * usaf_rigl_swap.
+ * usaf_reselect_carry - the state carry of usaf_reselect_full for a given new set new_idx [K]
+ * (sorted, in [0, N)).
+ * N is the number of expert weight entries (w_seg1 holds N - n_seg0). A given entry outside
+ * [0, N) is not read from the weights: it gets p = 0 and sets USAF_DEV_BAD_INDEX in dev_status
+ * (may be NULL); with USAF_DEBUG=1 the given sets are validated as by usaf_validate_active.
+ * Workspace: usaf_rigl_apply_workspace_size(K, D), usaf_reselect_carry_workspace_size().
+ * Errors: INVALID_ARG, WORKSPACE, CUDA. */
+size_t usaf_rigl_apply_workspace_size(int64_t K, int64_t D);
+usaf_status usaf_rigl_apply(const int64_t* act_idx, int64_t K, int64_t N, int64_t D,
+                            const int64_t* grown,
+                            const float* p_in, const float* m_in, const float* v_in,
+                            const void* w_seg0, int64_t n_seg0, const void* w_seg1,
+                            usaf_dtype w_dtype, int64_t* new_idx, float* p_out, float* m_out,
+                            float* v_out, int64_t* n_swapped, uint32_t* dev_status, void* ws,
+                            size_t ws_bytes, void* stream);
+size_t usaf_reselect_carry_workspace_size(void);
+usaf_status usaf_reselect_carry(const int64_t* new_idx, int64_t K, int64_t N,
+                                const int64_t* old_idx, int64_t K_old, const float* p_in,
+                                const float* m_in, const float* v_in, const void* w_seg0,
+                                int64_t n_seg0, const void* w_seg1, usaf_dtype w_dtype,
+                                float* p_out, float* m_out, float* v_out, int64_t* n_kept,
+                                uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
  * usaf_validate_active - checks an active set against the contract every call above assumes
  * (USAF README, "Not all weights matter": the trained subset is a set of expert weights, here a
  * sorted list of flat indices): 0 <= idx[i] < N, and idx[i-1] < idx[i] (ascending, no repeats).

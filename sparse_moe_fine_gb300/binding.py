@@ -85,6 +85,17 @@ _SIGS = {
     "usaf_moe_bwd_dense": (_INT, [_P, _INT, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                   _INT, _P, _P, _P, _P, _P, _SZ, _P]),
     "usaf_validate_active": (_INT, [_P, _I64, _I64, _P, _P]),
+    "usaf_shard_key_histogram": (_INT, [_P, _I64, _P, ctypes.c_uint32, _INT, _INT, _P, _P]),
+    "usaf_shard_emit_workspace_size": (_SZ, [_I64, _I64]),
+    "usaf_shard_emit": (_INT, [_P, _I64, _P, ctypes.c_uint32, _I64, _I64, _I64, _P, _P, _P, _SZ,
+                               _P]),
+    "usaf_active_bitmap": (_INT, [_P, _I64, _I64, _I64, _P, _P]),
+    "usaf_rigl_apply_workspace_size": (_SZ, [_I64, _I64]),
+    "usaf_rigl_apply": (_INT, [_P, _I64, _I64, _I64, _P, _P, _P, _P, _P, _I64, _P, _INT, _P, _P,
+                               _P, _P, _P, _P, _P, _SZ, _P]),
+    "usaf_reselect_carry_workspace_size": (_SZ, []),
+    "usaf_reselect_carry": (_INT, [_P, _I64, _I64, _P, _I64, _P, _P, _P, _P, _I64, _P, _INT, _P,
+                                   _P, _P, _P, _P, _P, _SZ, _P]),
     "usaf_masked_plan_size": (_SZ, [_P]),
     "usaf_masked_plan_build": (_INT, [_P, _P, _I64, _D, _P, _SZ, _P]),
     "usaf_moe_bwd_sparse_planned": (_INT, [_P, _INT, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _P,
@@ -396,6 +407,56 @@ def diag_bounded_wait(limit_cycles, dev_status, stream=None):
     """usaf_diag_bounded_wait: one CTA whose bounded mbarrier wait runs out after limit_cycles."""
     _check("usaf_diag_bounded_wait", lib().usaf_diag_bounded_wait(
         int(limit_cycles), _ptr(dev_status), _stream(stream)))
+
+
+def shard_key_histogram(g, excl, prefix, shift, bits, hist, stream=None):
+    """hist [2^bits] uint64 (int64 tensor) += digit counts of the part's keys (usaf.h)."""
+    _check("usaf_shard_key_histogram", lib().usaf_shard_key_histogram(
+        _ptr(g), g.numel(), _ptr(excl), int(prefix) & 0xFFFFFFFF, int(shift), int(bits),
+        _ptr(hist), _stream(stream)))
+
+
+def shard_emit(g, excl, tau, take_eq, count, base, out, dev_status=None, ws=None, stream=None):
+    n = g.numel()
+    if ws is None:
+        ws = _ws(lib().usaf_shard_emit_workspace_size(n, int(count)), g.device)
+    _check("usaf_shard_emit", lib().usaf_shard_emit(
+        _ptr(g), n, _ptr(excl), int(tau) & 0xFFFFFFFF, int(take_eq), int(count), int(base),
+        _ptr(out), _ptr(dev_status), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def active_bitmap(idx, lo, n, bitmap, stream=None):
+    K = 0 if idx is None else idx.numel()
+    _check("usaf_active_bitmap", lib().usaf_active_bitmap(
+        _ptr(idx), K, int(lo), int(n), _ptr(bitmap), _stream(stream)))
+
+
+def _n_entries(n_seg0, w_seg1):
+    return int(n_seg0) + (0 if w_seg1 is None else w_seg1.numel())
+
+
+def rigl_apply(act_idx, D, grown, p_in, m_in, v_in, w_seg0, n_seg0, w_seg1, new_idx, p_out,
+               m_out, v_out, n_swapped, dev_status=None, ws=None, stream=None):
+    """usaf_rigl_apply: RigL's drop and merge with the grow set given (chosen over ranks)."""
+    K = act_idx.numel()
+    if ws is None:
+        ws = _ws(lib().usaf_rigl_apply_workspace_size(K, int(D)), act_idx.device)
+    _check("usaf_rigl_apply", lib().usaf_rigl_apply(
+        _ptr(act_idx), K, _n_entries(n_seg0, w_seg1), int(D), _ptr(grown), _ptr(p_in), _ptr(m_in), _ptr(v_in), _ptr(w_seg0),
+        int(n_seg0), _ptr(w_seg1), _dt(w_seg0), _ptr(new_idx), _ptr(p_out), _ptr(m_out),
+        _ptr(v_out), _ptr(n_swapped), _ptr(dev_status), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def reselect_carry(new_idx, old_idx, p_in, m_in, v_in, w_seg0, n_seg0, w_seg1, p_out, m_out,
+                   v_out, n_kept, dev_status=None, ws=None, stream=None):
+    """usaf_reselect_carry: the state of a full reselection for a new set chosen over ranks."""
+    if ws is None:
+        ws = _ws(lib().usaf_reselect_carry_workspace_size(), new_idx.device)
+    _check("usaf_reselect_carry", lib().usaf_reselect_carry(
+        _ptr(new_idx), new_idx.numel(), _n_entries(n_seg0, w_seg1), _ptr(old_idx),
+        old_idx.numel(), _ptr(p_in), _ptr(m_in), _ptr(v_in), _ptr(w_seg0), int(n_seg0),
+        _ptr(w_seg1), _dt(w_seg0), _ptr(p_out), _ptr(m_out), _ptr(v_out), _ptr(n_kept),
+        _ptr(dev_status), _ptr(ws), ws.numel(), _stream(stream)))
 
 
 def trace_enable(on: bool) -> None:

@@ -524,6 +524,95 @@ usaf_status usaf_reselect_full(const float* g, int64_t N, int64_t K, const int64
                          static_cast<cudaStream_t>(stream));
 }
 
+usaf_status usaf_shard_key_histogram(const float* g, int64_t n, const uint32_t* excl,
+                                     uint32_t prefix, int shift, int bits,
+                                     unsigned long long* hist, void* stream) {
+  if (n < 0 || n >= (int64_t(1) << 32) || (n > 0 && !g) || !hist) return USAF_ERR_INVALID_ARG;
+  if (bits < 1 || bits > 11 || shift < 0 || shift + bits > 31) return USAF_ERR_INVALID_ARG;
+  return shard_hist_launch(g, n, excl, prefix, shift, bits, hist,
+                           static_cast<cudaStream_t>(stream));
+}
+
+size_t usaf_shard_emit_workspace_size(int64_t n, int64_t count) {
+  if (n < 0 || n >= (int64_t(1) << 32) || count < 0) return 0;
+  return shard_emit_ws_bytes(n, count);
+}
+
+usaf_status usaf_shard_emit(const float* g, int64_t n, const uint32_t* excl, uint32_t tau,
+                            int64_t take_eq, int64_t count, int64_t base, int64_t* out,
+                            uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
+  if (n < 0 || n >= (int64_t(1) << 32) || (n > 0 && (!g || !out)) || take_eq < 0 ||
+      take_eq > n || count < 0 || base < 0)
+    return USAF_ERR_INVALID_ARG;
+  if (n > 0 && (!ws || ws_bytes < shard_emit_ws_bytes(n, count))) return USAF_ERR_WORKSPACE;
+  return shard_emit_launch(g, n, excl, tau, take_eq, count, base, out, dev_status, ws,
+                           static_cast<cudaStream_t>(stream));
+}
+
+usaf_status usaf_active_bitmap(const int64_t* idx, int64_t K, int64_t lo, int64_t n,
+                               uint32_t* bitmap, void* stream) {
+  if (K < 0 || (K > 0 && !idx) || n < 1 || !bitmap || lo < 0) return USAF_ERR_INVALID_ARG;
+  return bitmap_range_launch(idx, K, lo, n, bitmap, static_cast<cudaStream_t>(stream));
+}
+
+size_t usaf_rigl_apply_workspace_size(int64_t K, int64_t D) {
+  if (K < 0 || D < 0 || D > K) return 0;
+  Carver c(nullptr);
+  c.take<int64_t>(D);
+  c.take<int64_t>(D);
+  c.take<char>(select_ws_bytes(K > 0 ? K : 1, D > 0 ? D : 1, false));
+  return c.size();
+}
+
+usaf_status usaf_rigl_apply(const int64_t* act_idx, int64_t K, int64_t N, int64_t D,
+                            const int64_t* grown,
+                            const float* p_in, const float* m_in, const float* v_in,
+                            const void* w_seg0, int64_t n_seg0, const void* w_seg1,
+                            usaf_dtype w_dtype, int64_t* new_idx, float* p_out, float* m_out,
+                            float* v_out, int64_t* n_swapped, uint32_t* dev_status, void* ws,
+                            size_t ws_bytes, void* stream) {
+  if (K < 0 || D < 0 || D > K || K > N || !n_swapped || !dtype_ok(w_dtype) || n_seg0 < 0 ||
+      n_seg0 > N)
+    return USAF_ERR_INVALID_ARG;
+  if (K > 0 && (!act_idx || !p_in || !m_in || !v_in || !new_idx || !p_out || !m_out || !v_out))
+    return USAF_ERR_INVALID_ARG;
+  if (D > 0 && (!grown || !w_seg0 || (N > n_seg0 && !w_seg1))) return USAF_ERR_INVALID_ARG;
+  const size_t kb = size_t(K) * 4;
+  const void* ins[4] = {p_in, m_in, v_in, act_idx};
+  const size_t insz[4] = {kb, kb, kb, size_t(K) * 8};
+  const void* outs[4] = {p_out, m_out, v_out, new_idx};
+  for (int i = 0; i < 4; ++i)
+    for (int j = 0; j < 4; ++j)
+      if (overlaps(ins[i], insz[i], outs[j], insz[j])) return USAF_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < usaf_rigl_apply_workspace_size(K, D)) return USAF_ERR_WORKSPACE;
+  USAF_TRY(debug_validate(act_idx, K, N, dev_status, stream));
+  USAF_TRY(debug_validate(grown, D, N, dev_status, stream));
+  return rigl_launch(nullptr, N, act_idx, K, D, p_in, m_in, v_in, w_seg0, n_seg0, w_seg1,
+                     w_dtype, new_idx, p_out, m_out, v_out, n_swapped, dev_status, ws,
+                     static_cast<cudaStream_t>(stream), D > 0 ? grown : act_idx);
+}
+
+size_t usaf_reselect_carry_workspace_size(void) { return reselect_carry_ws_bytes(); }
+
+usaf_status usaf_reselect_carry(const int64_t* new_idx, int64_t K, int64_t N,
+                                const int64_t* old_idx, int64_t K_old, const float* p_in,
+                                const float* m_in, const float* v_in, const void* w_seg0,
+                                int64_t n_seg0, const void* w_seg1, usaf_dtype w_dtype,
+                                float* p_out, float* m_out, float* v_out, int64_t* n_kept,
+                                uint32_t* dev_status, void* ws, size_t ws_bytes, void* stream) {
+  if (K < 0 || K_old < 0 || K > N || K_old > N || !n_kept || !dtype_ok(w_dtype) || n_seg0 < 0 ||
+      n_seg0 > N)
+    return USAF_ERR_INVALID_ARG;
+  if (K > 0 && (!new_idx || !p_out || !m_out || !v_out || !w_seg0 || (N > n_seg0 && !w_seg1)))
+    return USAF_ERR_INVALID_ARG;
+  if (K_old > 0 && (!old_idx || !p_in || !m_in || !v_in)) return USAF_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < reselect_carry_ws_bytes()) return USAF_ERR_WORKSPACE;
+  USAF_TRY(debug_validate(new_idx, K, N, dev_status, stream));
+  return reselect_carry_launch(new_idx, K, N, old_idx, K_old, p_in, m_in, v_in, w_seg0, n_seg0,
+                               w_seg1, w_dtype, p_out, m_out, v_out, n_kept, dev_status, ws,
+                               static_cast<cudaStream_t>(stream));
+}
+
 usaf_status usaf_validate_active(const int64_t* idx, int64_t K, int64_t N, uint32_t* dev_status,
                                  void* stream) {
   if (K < 0 || N < 1 || !dev_status || (K > 0 && !idx)) return USAF_ERR_INVALID_ARG;

@@ -131,11 +131,28 @@ usaf_status reselect_launch(const float* g, int64_t N, int64_t K, const int64_t*
                             usaf_dtype wdt, int64_t* new_idx, float* p_out, float* m_out,
                             float* v_out, int64_t* n_kept, uint32_t* dev_status, void* ws,
                             cudaStream_t st);
+// shard primitives of a selection spread over ranks (see usaf_shard_* in usaf.h)
+usaf_status shard_hist_launch(const float* g, int64_t n, const uint32_t* excl, uint32_t prefix,
+                              int shift, int bits, unsigned long long* hist, cudaStream_t st);
+size_t shard_emit_ws_bytes(int64_t n, int64_t count);
+usaf_status shard_emit_launch(const float* g, int64_t n, const uint32_t* excl, uint32_t tau,
+                              int64_t take_eq, int64_t count, int64_t base, int64_t* out,
+                              uint32_t* dev_status, void* ws, cudaStream_t st);
+usaf_status bitmap_range_launch(const int64_t* idx, int64_t K, int64_t lo, int64_t n,
+                                uint32_t* bm, cudaStream_t st);
 size_t rigl_ws_bytes(int64_t N, int64_t K, int64_t D);
 usaf_status rigl_launch(const float* g, int64_t N, const int64_t* act_idx, int64_t K, int64_t D,
                         const float* p_in, const float* m_in, const float* v_in, const void* w0,
                         int64_t n0, const void* w1, usaf_dtype wdt, int64_t* new_idx,
                         float* p_out, float* m_out, float* v_out, int64_t* n_swapped,
-                        uint32_t* dev_status, void* ws, cudaStream_t st);
+                        uint32_t* dev_status, void* ws, cudaStream_t st,
+                        const int64_t* grown_in = nullptr);
+usaf_status reselect_carry_launch(const int64_t* new_idx, int64_t K, int64_t N,
+                                  const int64_t* old_idx, int64_t K_old, const float* p_in,
+                                  const float* m_in, const float* v_in, const void* w0, int64_t n0,
+                                  const void* w1, usaf_dtype wdt, float* p_out, float* m_out,
+                                  float* v_out, int64_t* n_kept, uint32_t* dev_status, void* ws,
+                                  cudaStream_t st);
+size_t reselect_carry_ws_bytes();
 
 }  // namespace usaf

@@ -56,6 +56,7 @@ struct Src {
   int64_t cap;
   int drop;                // 1: keys are complemented |p| (mode 2 source)
   int G;                   // parts (regions)
+  int64_t base;            // modes 0, 2: added to the element index an ordered write emits
 };
 
 struct SelPlan {
@@ -88,8 +89,10 @@ SelPlan make_plan(int64_t N, int64_t K) {
     if (p.q >= SAMPLE_S / 8) p.sampling = false;
   }
   if (p.sampling) {
-    // one candidate region per warp of the compacting pass (COMPACT_WARPS per block)
-    int64_t G = std::min<int64_t>(ceil_div(N, 65536), sms * 32);
+    // one candidate region per warp of the compacting pass (COMPACT_WARPS per block), at least
+    // 4096 entries each, up to 32 per SM: a part of a few tens of millions of entries still fills
+    // every SM with warps
+    int64_t G = std::min<int64_t>(ceil_div(N, 4096), sms * 32);
     G = round_up(G < 1 ? 1 : G, COMPACT_WARPS);
     p.G = (int)G;
     p.L = round_up(ceil_div(N, G), 1024);
@@ -168,7 +171,7 @@ __device__ __forceinline__ void for_part(const Src& s, int mode, int b, F f) {
     for (int64_t j0 = 0; j0 < n; j0 += blockDim.x) {
       const int64_t j = j0 + threadIdx.x;
       const bool ok = j < n;
-      f(ok ? kk[j] : 0u, ok ? (int64_t)ii[j] : 0, ok);
+      f(ok ? kk[j] : 0u, ok ? s.base + (int64_t)ii[j] : 0, ok);
     }
   } else {
     const int64_t lo = (int64_t)b * s.L;
@@ -176,7 +179,7 @@ __device__ __forceinline__ void for_part(const Src& s, int mode, int b, F f) {
     for (int64_t i0 = lo; i0 < hi; i0 += blockDim.x) {
       const int64_t i = i0 + threadIdx.x;
       const bool ok = i < hi && !(mode == 0 && excluded(s.excl, i));
-      f(ok ? src_key(s, i) : 0u, i, ok);
+      f(ok ? src_key(s, i) : 0u, s.base + i, ok);
     }
   }
 }
@@ -691,7 +694,8 @@ __global__ void __launch_bounds__(MG_THREADS) rigl_merge_tile_kernel(
     const int64_t* __restrict__ grown, int64_t D, const float* __restrict__ p_in,
     const float* __restrict__ m_in, const float* __restrict__ v_in, const W* __restrict__ w0,
     int64_t n0, const W* __restrict__ w1, int64_t* __restrict__ new_idx,
-    float* __restrict__ p_out, float* __restrict__ m_out, float* __restrict__ v_out, SelCtrl* c) {
+    float* __restrict__ p_out, float* __restrict__ m_out, float* __restrict__ v_out, SelCtrl* c,
+    int64_t N, uint32_t* dev_status) {
   constexpr int PER = MG_TILE / MG_THREADS;
   __shared__ int64_t sh_act[MG_TILE];
   __shared__ uint32_t sh_keep[MG_TILE + 1];  // exclusive kept ranks inside the tile
@@ -766,7 +770,9 @@ __global__ void __launch_bounds__(MG_THREADS) rigl_merge_tile_kernel(
     m_out[pos] = m_in[s0 + i];
     v_out[pos] = v_in[s0 + i];
   }
-  // grown entries of the tile's range
+  // grown entries of the tile's range (a given grow set is range-checked before its weight is
+  // read: an entry outside [0, N) gets p = 0 and sets USAF_DEV_BAD_INDEX)
+  bool bad = false;
   for (int64_t j = g0 + threadIdx.x; j < g1; j += MG_THREADS) {
     const int64_t fj = g_in_smem ? sh_grown[j - g0] : grown[j];
     int lo = 0, hi = n;  // kept-or-dropped tile entries below fj
@@ -777,11 +783,14 @@ __global__ void __launch_bounds__(MG_THREADS) rigl_merge_tile_kernel(
     }
     const int64_t pos = kept_before + sh_keep[lo] + j;
     if (pos < 0 || pos >= K) continue;  // only an unsorted act_idx gets here
+    const bool ok = fj >= 0 && fj < N;
+    bad |= !ok;
     new_idx[pos] = fj;
-    p_out[pos] = to_f32(fj < n0 ? w0[fj] : w1[fj - n0]);
+    p_out[pos] = ok ? to_f32(fj < n0 ? w0[fj] : w1[fj - n0]) : 0.f;
     m_out[pos] = 0.f;
     v_out[pos] = 0.f;
   }
+  flag_status_warp(dev_status, bad, USAF_DEV_BAD_INDEX);
   if (threadIdx.x == 0 && d1 > d0) atomicAdd(&c->n_swapped, (unsigned long long)(d1 - d0));
 }
 
@@ -794,9 +803,9 @@ __global__ void reselect_carry_kernel(const int64_t* __restrict__ new_idx, int64
                                       const float* __restrict__ v_in, const W* __restrict__ w0,
                                       int64_t n0, const W* __restrict__ w1, float* __restrict__ p_out,
                                       float* __restrict__ m_out, float* __restrict__ v_out,
-                                      SelCtrl* c) {
+                                      SelCtrl* c, int64_t N, uint32_t* dev_status) {
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  bool kept = false;
+  bool kept = false, bad = false;
   if (t < K) {
     const int64_t f = new_idx[t];
     const int64_t s = lower_bound_i64(old_idx, K_old, f);
@@ -806,11 +815,13 @@ __global__ void reselect_carry_kernel(const int64_t* __restrict__ new_idx, int64
       m_out[t] = m_in[s];
       v_out[t] = v_in[s];
     } else {
-      p_out[t] = to_f32(f < n0 ? w0[f] : w1[f - n0]);
+      bad = f < 0 || f >= N;  // a given set is range-checked before its weight is read
+      p_out[t] = bad ? 0.f : to_f32(f < n0 ? w0[f] : w1[f - n0]);
       m_out[t] = 0.f;
       v_out[t] = 0.f;
     }
   }
+  flag_status_warp(dev_status, bad, USAF_DEV_BAD_INDEX);
   const unsigned n = __popc(__ballot_sync(0xffffffffu, kept));
   if ((threadIdx.x & 31) == 0 && n) atomicAdd(&c->n_swapped, (unsigned long long)n);
 }
@@ -858,10 +869,48 @@ usaf_status rigl_launch(const float* g, int64_t N, const int64_t* act_idx, int64
                         const float* p_in, const float* m_in, const float* v_in, const void* w0,
                         int64_t n0, const void* w1, usaf_dtype wdt, int64_t* new_idx,
                         float* p_out, float* m_out, float* v_out, int64_t* n_swapped,
-                        uint32_t* dev_status, void* ws, cudaStream_t st) {
+                        uint32_t* dev_status, void* ws, cudaStream_t st,
+                        const int64_t* grown_in) {
   Carver c(ws);
   int64_t* dpos = c.take<int64_t>(D);
   int64_t* grown = c.take<int64_t>(D);
+  if (grown_in) {
+    // the grow set is given (chosen across ranks): drop selection and merge only
+    const int64_t Ks = K > 0 ? K : 1, Ds = D > 0 ? D : 1;
+    char* ws_drop = c.take<char>(select_ws_bytes(Ks, Ds, false));
+    const SelPlan pd = make_plan(Ks, Ds);
+    Carver cd(ws_drop);
+    SelWs wd;
+    sel_layout(pd, cd, wd);
+    if (D > 0) {
+      Src sd{};
+      sd.g = p_in;
+      sd.n = K;
+      sd.L = pd.L;
+      sd.drop = 1;
+      USAF_TRY(run_select(pd, wd, sd, D, dpos, dev_status, true, st));
+    } else {
+      sel_init_kernel<<<1, 256, 0, st>>>(wd.ctrl, 0, wd.ccnt, pd.G);
+      USAF_CHECK_LAUNCH();
+    }
+    USAF_TRACE("rigl_merge", st);
+    if (K > 0) {
+      const unsigned nb = (unsigned)ceil_div(K, MG_TILE);
+      if (wdt == USAF_BF16)
+        rigl_merge_tile_kernel<__nv_bfloat16><<<nb, MG_THREADS, 0, st>>>(
+            act_idx, K, dpos, grown_in, D, p_in, m_in, v_in,
+            static_cast<const __nv_bfloat16*>(w0), n0, static_cast<const __nv_bfloat16*>(w1),
+            new_idx, p_out, m_out, v_out, wd.ctrl, N, dev_status);
+      else
+        rigl_merge_tile_kernel<float><<<nb, MG_THREADS, 0, st>>>(
+            act_idx, K, dpos, grown_in, D, p_in, m_in, v_in, static_cast<const float*>(w0), n0,
+            static_cast<const float*>(w1), new_idx, p_out, m_out, v_out, wd.ctrl, N, dev_status);
+      USAF_CHECK_LAUNCH();
+    }
+    rigl_finish_kernel<<<1, 32, 0, st>>>(wd.ctrl, n_swapped);
+    USAF_CHECK_LAUNCH();
+    return USAF_OK;
+  }
   const int64_t Ks = K > 0 ? K : 1, Ds = D > 0 ? D : 1;
   char* ws_drop = c.take<char>(select_ws_bytes(Ks, Ds, false));
   char* ws_grow = c.take<char>(select_ws_bytes(N, Ds, true));
@@ -937,11 +986,12 @@ usaf_status rigl_launch(const float* g, int64_t N, const int64_t* act_idx, int64
     if (wdt == USAF_BF16)
       rigl_merge_tile_kernel<__nv_bfloat16><<<nb, MG_THREADS, 0, st>>>(
           act_idx, K, dpos, grown, D, p_in, m_in, v_in, static_cast<const __nv_bfloat16*>(w0),
-          n0, static_cast<const __nv_bfloat16*>(w1), new_idx, p_out, m_out, v_out, wd.ctrl);
+          n0, static_cast<const __nv_bfloat16*>(w1), new_idx, p_out, m_out, v_out, wd.ctrl, N,
+          dev_status);
     else
       rigl_merge_tile_kernel<float><<<nb, MG_THREADS, 0, st>>>(
           act_idx, K, dpos, grown, D, p_in, m_in, v_in, static_cast<const float*>(w0), n0,
-          static_cast<const float*>(w1), new_idx, p_out, m_out, v_out, wd.ctrl);
+          static_cast<const float*>(w1), new_idx, p_out, m_out, v_out, wd.ctrl, N, dev_status);
     USAF_CHECK_LAUNCH();
   }
   rigl_finish_kernel<<<1, 32, 0, st>>>(wd.ctrl, n_swapped);
@@ -949,7 +999,214 @@ usaf_status rigl_launch(const float* g, int64_t N, const int64_t* act_idx, int64
   return USAF_OK;
 }
 
+// ------------------------------------------------------------------------------------------------
+// Shard primitives of a selection spread over several ranks (each rank holds a contiguous part of
+// the keys): digit histograms, counts at a threshold, and the ordered emission of a part's winners.
+// The rounds, the digit picks and the exchanges between ranks run on the host.
+// ------------------------------------------------------------------------------------------------
+namespace {
+constexpr int SH_THREADS = 256;
+constexpr int SH_MAX_BITS = 11;
+
+// hist[d] += keys of g[0, n) (not excluded) whose bits above shift + bits equal prefix's, by the
+// digit of `bits` bits at `shift`. Digits of up to 8 bits go to per-warp shared histograms (the
+// first round, where every key lands in a few bins); wider digits to one per-block histogram (the
+// later rounds, where the prefix test lets few keys through). One global add per block and bin.
+template <bool PER_WARP>
+__global__ void __launch_bounds__(SH_THREADS) shard_hist_kernel(
+    const float* __restrict__ g, int64_t n, const uint32_t* __restrict__ excl, uint32_t prefix,
+    int shift, int bits, unsigned long long* hist) {
+  constexpr int WB = 257;                                      // per-warp bins, padded
+  constexpr int WORDS = PER_WARP ? (SH_THREADS / 32) * WB : (1 << SH_MAX_BITS);
+  __shared__ uint32_t sh[WORDS];
+  for (int i = threadIdx.x; i < WORDS; i += blockDim.x) sh[i] = 0;
+  __syncthreads();
+  uint32_t* hw = PER_WARP ? sh + (threadIdx.x >> 5) * WB : sh;
+  const uint32_t dmask = (1u << bits) - 1;
+  const int hs = shift + bits;
+  auto add = [&](uint32_t k, int64_t i) {
+    if (excluded(excl, i)) return;
+    if (hs >= 32 || (k >> hs) == (prefix >> hs)) atomicAdd(&hw[(k >> shift) & dmask], 1u);
+  };
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  int64_t done = 0;
+  if ((reinterpret_cast<uintptr_t>(g) & 15) == 0) {  // 16-byte loads over the aligned body
+    const int64_t n4 = n >> 2;
+    const float4* g4 = reinterpret_cast<const float4*>(g);
+    for (int64_t q = tid; q < n4; q += stride) {
+      const float4 v = __ldg(g4 + q);
+      add(abs_key(v.x), 4 * q);
+      add(abs_key(v.y), 4 * q + 1);
+      add(abs_key(v.z), 4 * q + 2);
+      add(abs_key(v.w), 4 * q + 3);
+    }
+    done = n4 << 2;
+  }
+  for (int64_t i = done + tid; i < n; i += stride) add(abs_key(g[i]), i);
+  __syncthreads();
+  for (int d = threadIdx.x; d <= (int)dmask; d += blockDim.x) {
+    uint32_t t = 0;
+    if (PER_WARP)
+      for (int w = 0; w < SH_THREADS / 32; ++w) t += sh[w * WB + d];
+    else
+      t = sh[d];
+    if (t) atomicAdd(&hist[d], (unsigned long long)t);
+  }
+}
+
+// Control block of an emission at a known threshold: candidates are the keys >= tau.
+__global__ void shard_emit_init_kernel(SelCtrl* c, uint32_t tau, uint32_t take_eq, uint32_t* ccnt,
+                                       int G) {
+  for (int i = threadIdx.x; i < MAX_BINS; i += blockDim.x) c->hist[i] = 0;
+  for (int i = threadIdx.x; i < G; i += blockDim.x) ccnt[i] = 0;
+  if (threadIdx.x == 0) {
+    c->tau0 = tau;
+    c->prefix = tau;
+    c->k_rem = take_eq;
+    c->mode = 0;
+    c->overflow = 0;
+    c->total = 0;
+    c->ticket = 0;
+  }
+}
+
+// The candidate path unless a region overflowed (then the whole part, in order, reported as
+// USAF_DEV_SELECT_EXACT_PATH)
+__global__ void shard_emit_decide_kernel(SelCtrl* c, uint32_t* dev_status) {
+  if (threadIdx.x == 0) {
+    c->mode = c->overflow ? 0u : 1u;
+    if (c->overflow) flag_status(dev_status, USAF_DEV_SELECT_EXACT_PATH);
+  }
+}
+
+__global__ void bitmap_range_kernel(const int64_t* __restrict__ idx, int64_t K, int64_t lo,
+                                    int64_t n, uint32_t* bm) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < K;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t f = idx[i] - lo;
+    if (f >= 0 && f < n) atomicOr(&bm[f >> 5], 1u << (f & 31));
+  }
+}
+}  // namespace
+
+usaf_status shard_hist_launch(const float* g, int64_t n, const uint32_t* excl, uint32_t prefix,
+                              int shift, int bits, unsigned long long* hist, cudaStream_t st) {
+  if (n == 0) return USAF_OK;
+  USAF_TRACE("shard_hist", st);
+  const unsigned grid = (unsigned)std::min<int64_t>(ceil_div(n, 4 * SH_THREADS),
+                                                    (int64_t)device_sm_count() * 8);
+  if (bits <= 8)
+    shard_hist_kernel<true><<<grid, SH_THREADS, 0, st>>>(g, n, excl, prefix, shift, bits, hist);
+  else
+    shard_hist_kernel<false><<<grid, SH_THREADS, 0, st>>>(g, n, excl, prefix, shift, bits, hist);
+  USAF_CHECK_LAUNCH();
+  return USAF_OK;
+}
+
+size_t shard_emit_ws_bytes(int64_t n, int64_t count) {
+  const int64_t ns = n > 0 ? n : 1;
+  SelPlan p = make_plan(ns, count > 0 ? count : 1);
+  Carver c(nullptr);
+  SelWs w;
+  sel_layout(p, c, w);
+  return c.size();
+}
+
+// The part's winners in index order: keys > tau, then the first take_eq keys == tau. `count` is
+// the number of keys >= tau in the part (from the count step); it sizes the candidate regions of
+// one compacting pass at threshold tau, after which the ordered write runs over the candidates
+// (over the whole part if a region overflowed).
+usaf_status shard_emit_launch(const float* g, int64_t n, const uint32_t* excl, uint32_t tau,
+                              int64_t take_eq, int64_t count, int64_t base, int64_t* out,
+                              uint32_t* dev_status, void* ws, cudaStream_t st) {
+  if (n == 0) return USAF_OK;
+  USAF_TRACE("shard_emit", st);
+  const SelPlan p = make_plan(n, count > 0 ? count : 1);
+  Carver c(ws);
+  SelWs w;
+  sel_layout(p, c, w);
+  shard_emit_init_kernel<<<1, 256, 0, st>>>(w.ctrl, tau, (uint32_t)take_eq, w.ccnt, p.G);
+  USAF_CHECK_LAUNCH();
+  Src s{};
+  s.g = g;
+  s.n = n;
+  s.L = p.L;
+  s.excl = excl;
+  s.drop = 0;
+  s.G = p.G;
+  s.base = base;
+  int fm = 0;
+  if (p.sampling) {
+    const int vec_ok = (reinterpret_cast<uintptr_t>(g) & 15) == 0;
+    sel_compact_kernel<<<p.G / COMPACT_WARPS, COMPACT_WARPS * 32, 0, st>>>(
+        g, n, p.L, excl, p.cap, w.ckeys, w.cids, w.ccnt, w.ctrl, vec_ok, dev_status);
+    USAF_CHECK_LAUNCH();
+    shard_emit_decide_kernel<<<1, 32, 0, st>>>(w.ctrl, dev_status);
+    USAF_CHECK_LAUNCH();
+    s.ckeys = w.ckeys;
+    s.cids = w.cids;
+    s.ccnt = w.ccnt;
+    s.cap = p.cap;
+    fm = -1;
+  }
+  sel_count_kernel<<<p.G, SEL_THREADS, 0, st>>>(s, w.ctrl, w.blk_gt, w.blk_eq, fm);
+  USAF_CHECK_LAUNCH();
+  sel_scan_kernel<<<1, 1024, 0, st>>>(w.blk_gt, w.blk_eq, p.G, w.base_gt, w.base_eq);
+  USAF_CHECK_LAUNCH();
+  sel_write_kernel<<<p.G, SEL_THREADS, 0, st>>>(s, w.ctrl, w.base_gt, w.base_eq, out, fm);
+  USAF_CHECK_LAUNCH();
+  return USAF_OK;
+}
+
+usaf_status bitmap_range_launch(const int64_t* idx, int64_t K, int64_t lo, int64_t n,
+                                uint32_t* bm, cudaStream_t st) {
+  const int64_t words = ceil_div(n, 32);
+  bitmap_zero_kernel<<<grid_dim_for(words), 256, 0, st>>>(bm, words);
+  USAF_CHECK_LAUNCH();
+  if (K > 0) {
+    bitmap_range_kernel<<<grid_dim_for(K), 256, 0, st>>>(idx, K, lo, n, bm);
+    USAF_CHECK_LAUNCH();
+  }
+  return USAF_OK;
+}
+
 size_t reselect_ws_bytes(int64_t N, int64_t K) { return select_ws_bytes(N, K > 0 ? K : 1, false); }
+
+// The state carry of a full reselection for a new set chosen elsewhere (across ranks).
+usaf_status reselect_carry_launch(const int64_t* new_idx, int64_t K, int64_t N,
+                                  const int64_t* old_idx, int64_t K_old, const float* p_in,
+                                  const float* m_in, const float* v_in, const void* w0, int64_t n0,
+                                  const void* w1, usaf_dtype wdt, float* p_out, float* m_out,
+                                  float* v_out, int64_t* n_kept, uint32_t* dev_status, void* ws,
+                                  cudaStream_t st) {
+  Carver c(ws);
+  SelCtrl* ctrl = c.take<SelCtrl>(1);
+  uint32_t* ccnt = c.take<uint32_t>(1);
+  sel_init_kernel<<<1, 256, 0, st>>>(ctrl, 0, ccnt, 1);
+  USAF_CHECK_LAUNCH();
+  if (K > 0) {
+    USAF_TRACE("reselect_carry", st);
+    if (wdt == USAF_BF16)
+      reselect_carry_kernel<__nv_bfloat16><<<(unsigned)ceil_div(K, 256), 256, 0, st>>>(
+          new_idx, K, old_idx, K_old, p_in, m_in, v_in, static_cast<const __nv_bfloat16*>(w0),
+          n0, static_cast<const __nv_bfloat16*>(w1), p_out, m_out, v_out, ctrl, N, dev_status);
+    else
+      reselect_carry_kernel<float><<<(unsigned)ceil_div(K, 256), 256, 0, st>>>(
+          new_idx, K, old_idx, K_old, p_in, m_in, v_in, static_cast<const float*>(w0), n0,
+          static_cast<const float*>(w1), p_out, m_out, v_out, ctrl, N, dev_status);
+    USAF_CHECK_LAUNCH();
+  }
+  rigl_finish_kernel<<<1, 32, 0, st>>>(ctrl, n_kept);
+  USAF_CHECK_LAUNCH();
+  return USAF_OK;
+}
+size_t reselect_carry_ws_bytes() {
+  Carver c(nullptr);
+  c.take<SelCtrl>(1);
+  c.take<uint32_t>(1);
+  return c.size();
+}
 
 usaf_status reselect_launch(const float* g, int64_t N, int64_t K, const int64_t* old_idx,
                             int64_t K_old, const float* p_in, const float* m_in,
@@ -974,11 +1231,12 @@ usaf_status reselect_launch(const float* g, int64_t N, int64_t K, const int64_t*
     if (wdt == USAF_BF16)
       reselect_carry_kernel<__nv_bfloat16><<<(unsigned)ceil_div(K, 256), 256, 0, st>>>(
           new_idx, K, old_idx, K_old, p_in, m_in, v_in, static_cast<const __nv_bfloat16*>(w0),
-          n0, static_cast<const __nv_bfloat16*>(w1), p_out, m_out, v_out, w.ctrl);
+          n0, static_cast<const __nv_bfloat16*>(w1), p_out, m_out, v_out, w.ctrl, N,
+          dev_status);
     else
       reselect_carry_kernel<float><<<(unsigned)ceil_div(K, 256), 256, 0, st>>>(
           new_idx, K, old_idx, K_old, p_in, m_in, v_in, static_cast<const float*>(w0), n0,
-          static_cast<const float*>(w1), p_out, m_out, v_out, w.ctrl);
+          static_cast<const float*>(w1), p_out, m_out, v_out, w.ctrl, N, dev_status);
     USAF_CHECK_LAUNCH();
   } else {
     sel_init_kernel<<<1, 256, 0, st>>>(w.ctrl, 0, w.ccnt, p.G);

@@ -14,6 +14,7 @@ import math
 import torch
 
 from . import binding as B
+from . import dist_select as DS
 from .layer import allreduce_dense_grad
 
 
@@ -38,9 +39,16 @@ class StackTrainer:
     the input gradient dx of layer i+1 is the upstream gradient dy of layer i."""
 
     def __init__(self, layers, total_steps, lr_peak=2e-4, warmup_steps=0, reselect_every=50,
-                 reselect="rigl", drop_frac=0.3, skip_nonfinite=True):
+                 reselect="rigl", drop_frac=0.3, skip_nonfinite=True, dense_exchange="allreduce"):
+        """dense_exchange (data parallel only): how the replicas agree on the importance phase's
+        gradient. "allreduce": every rank sums the whole dense gradient and selects alone;
+        "reduce_scatter": every rank sums one part and the selection runs over the parts
+        (dist_select), moving half the bytes and ranking 1/world of the entries per rank."""
         if reselect not in ("rigl", "full"):
             raise ValueError("reselect must be 'rigl' or 'full'")
+        if dense_exchange not in ("allreduce", "reduce_scatter"):
+            raise ValueError("dense_exchange must be 'allreduce' or 'reduce_scatter'")
+        self.dense_exchange = dense_exchange
         self.layers = list(layers)
         self.total_steps = total_steps
         self.lr_peak, self.warmup_steps = lr_peak, warmup_steps
@@ -110,13 +118,18 @@ class StackTrainer:
         for i, L in enumerate(self.layers):
             L.wait_optimizer()
             g = self._g_dense[i]
-            if L.group is not None:
-                # data parallel: rank the whole batch's gradient, so the replicas' sets agree
-                allreduce_dense_grad(g, L.group)
             K = L.K
             new = torch.empty(K, dtype=torch.int64, device=L.dev)
             p, m, v = (torch.empty(K, device=L.dev) for _ in range(3))
             cnt = torch.zeros(1, dtype=torch.int64, device=L.dev)
+            if L.group is not None and self.dense_exchange == "reduce_scatter":
+                turn.append(self._reselect_parts(L, g, new, p, m, v, cnt))
+                L.set_active(new, p, m, v)
+                g.zero_()
+                continue
+            if L.group is not None:
+                # data parallel: rank the whole batch's gradient, so the replicas' sets agree
+                allreduce_dense_grad(g, L.group)
             if self.reselect == "rigl":
                 D = int(self.drop_frac * K)
                 B.rigl_swap(g, L.act, D, L.p, L.m, L.v, L.w_gate_up, L.N_gu, L.w_down, new, p, m,
@@ -129,6 +142,23 @@ class StackTrainer:
             L.set_active(new, p, m, v)
             g.zero_()
         return turn
+
+    def _reselect_parts(self, L, g, new, p, m, v, cnt):
+        """Reselection with the dense gradient reduce-scattered: each rank holds the batch's sum
+        over one part of the entries; the new set (or RigL's grow set) is selected over the parts
+        of all ranks, and every rank carries its state with the library as on one GPU."""
+        part, lo = DS.reduce_scatter_part(g, L.group)
+        comm, ops = DS.TorchComm(L.group), DS.LibShardOps()
+        if self.reselect == "rigl":
+            D = int(self.drop_frac * L.K)
+            excl = DS.part_bitmap(L.act, lo, part.numel())
+            grown = DS.topk_over_parts([(part, lo, excl)], D, ops, comm)
+            B.rigl_apply(L.act, D, grown, L.p, L.m, L.v, L.w_gate_up, L.N_gu, L.w_down, new, p,
+                         m, v, cnt)
+            return cnt
+        new.copy_(DS.topk_over_parts([(part, lo, None)], L.K, ops, comm))
+        B.reselect_carry(new, L.act, L.p, L.m, L.v, L.w_gate_up, L.N_gu, L.w_down, p, m, v, cnt)
+        return L.K - cnt
 
     # ------------------------------------------------------------------ metrics
     def metrics(self):

@@ -18,12 +18,67 @@ fake_addresses = pytest.mark.skipif(torch.cuda.is_available(),
 def test_library_exports_every_header_symbol():
     L = B.lib()
     syms = B.header_symbols()
-    assert len(syms) == 30
+    assert len(syms) == 38
     for s in syms:
         assert hasattr(L, s), s
     assert L.usaf_abi_version() == 2
     assert L.usaf_status_string(0) == b"ok"
     assert L.usaf_status_string(3) == b"workspace missing or too small"
+
+
+def _header_arity():
+    """Parameter count of every function the header declares (declarations, not comments)."""
+    import os
+    import re
+    text = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                             "include", "usaf.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    out = {}
+    for name, params in re.findall(r"\b(usaf_[a-z0-9_]+)\s*\(([^)]*)\)\s*;", text):
+        params = " ".join(params.split())
+        out[name] = 0 if params in ("", "void") else params.count(",") + 1
+    return out
+
+
+def test_binding_prototypes_match_the_header():
+    """Every ctypes prototype has as many arguments as the header's declaration."""
+    arity = _header_arity()
+    assert set(arity) == set(B.header_symbols())
+    for name, (_, args) in B._SIGS.items():
+        assert name in arity, name
+        assert len(args) == arity[name], (name, len(args), arity[name])
+    assert set(B._SIGS) == set(arity)
+
+
+@fake_addresses
+def test_shard_selection_host_checks():
+    L = B.lib()
+    fake = ctypes.c_void_p(256)  # never dereferenced: every call below fails on the host
+    # digit widths outside 1..11 and digits past bit 30
+    assert L.usaf_shard_key_histogram(fake, 10, None, 0, 0, 12, fake, None) == 1
+    assert L.usaf_shard_key_histogram(fake, 10, None, 0, 21, 11, fake, None) == 1
+    assert L.usaf_shard_key_histogram(fake, 10, None, 0, 0, 0, fake, None) == 1
+    assert L.usaf_shard_key_histogram(fake, 1 << 32, None, 0, 0, 7, fake, None) == 1
+    assert L.usaf_shard_key_histogram(fake, 10, None, 0, 0, 7, None, None) == 1
+    # more ties than entries, a negative base, no workspace
+    assert L.usaf_shard_emit(fake, 10, None, 0, 11, 11, 0, fake, None, fake, 1 << 20, None) == 1
+    assert L.usaf_shard_emit(fake, 10, None, 0, 1, 1, -1, fake, None, fake, 1 << 20, None) == 1
+    assert L.usaf_shard_emit(fake, 10, None, 0, 1, 1, 0, fake, None, None, 0, None) == 3
+    assert L.usaf_shard_emit_workspace_size(1 << 32, 1) == 0
+    assert L.usaf_active_bitmap(fake, 5, 0, 0, fake, None) == 1
+    # K above the entry count, D above K, a missing grow set
+    assert L.usaf_rigl_apply(fake, 100, 50, 10, fake, fake, fake, fake, fake, 50, None, 1, fake,
+                             fake, fake, fake, fake, None, fake, 1 << 30, None) == 1
+    assert L.usaf_rigl_apply(fake, 10, 50, 11, fake, fake, fake, fake, fake, 50, None, 1, fake,
+                             fake, fake, fake, fake, None, fake, 1 << 30, None) == 1
+    assert L.usaf_rigl_apply(fake, 10, 50, 2, None, fake, fake, fake, fake, 50, None, 1, fake,
+                             fake, fake, fake, fake, None, fake, 1 << 30, None) == 1
+    # the second weight segment missing while N > n_seg0
+    assert L.usaf_reselect_carry(fake, 10, 50, fake, 10, fake, fake, fake, fake, 40, None, 1,
+                                 fake, fake, fake, fake, None, fake, 1 << 20, None) == 1
+    assert L.usaf_reselect_carry(fake, 10, 50, fake, 10, fake, fake, fake, fake, 50, None, 1,
+                                 fake, fake, fake, fake, None, None, 0, None) == 3
 
 
 def test_capacity_and_workspace_queries():
