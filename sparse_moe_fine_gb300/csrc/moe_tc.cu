@@ -702,6 +702,322 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------------- CTA pairs
+// The expert GEMMs on pairs of SMs (tcgen05 cta_group::2): a tile is 256 weight rows by up to 256
+// tokens. Each CTA of the pair loads its own 128 weight rows and half of the token tile into its
+// shared memory; the pair's MMA (issued by the even CTA) reads both CTAs' halves and leaves each
+// CTA's 128 rows x all tokens in that CTA's tensor memory, so each epilogue is the single-CTA one
+// over its own rows. A stage is 32 KB per SM instead of 48 KB (the token tile is split, not
+// copied), so six stages are in flight instead of four, and the MMA reads 8 KB of shared memory
+// per 16-deep step instead of 12 KB.
+// - full[s]: in the even CTA only, expecting both CTAs' bytes (the odd CTA's copies signal it);
+// - empty[s]: in both CTAs, arrived by the pair's MMA commit (multicast);
+// - tfull[a]: in both CTAs, arrived by the MMA commit (multicast) when accumulator a is complete;
+// - tempty[a]: in the even CTA, arrived by the 16 epilogue warps of both CTAs.
+// Every wait is bounded as in the single-CTA kernel; a role that gives up also raises the other
+// CTA's abort flag.
+namespace pr {
+constexpr int STAGES = 6;
+constexpr int A_BYTES = BM * BK * 2;        // this CTA's 128 weight rows
+constexpr int B_BYTES = (BN / 2) * BK * 2;  // this CTA's half of the token tile
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int SMEM = STAGES * STAGE_BYTES + 1024 + PLAN_BYTES + EPI_WARPS * EPI_STAGE_BYTES;
+static_assert(SMEM <= 232448, "shared memory of the CTA-pair kernel");
+static_assert(2 * STAGES + 5 <= 30, "barrier area");
+}  // namespace pr
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// address of the same shared variable in CTA 0 of the cluster
+__device__ __forceinline__ uint32_t map_to_cta0(uint32_t a) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, 0;" : "=r"(r) : "r"(a));
+  return r;
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ void tma_2d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".cta_group::2 [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
+      : "memory");
+}
+__device__ __forceinline__ void tma_4d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                            int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".cta_group::2 [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                               uint32_t acc) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+// arrive on barrier `bar` (same offset) in both CTAs when this thread's MMAs are complete
+__device__ __forceinline__ void umma_commit_both(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)3)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit_local_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+                   bar_cluster_addr)
+               : "memory");
+}
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+// the other CTA of the pair
+__device__ __forceinline__ uint32_t map_to_peer(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank ^ 1u));
+  return r;
+}
+
+// Instruction descriptor, kind::f16, for the pair's M = 256.
+__device__ __forceinline__ uint32_t idesc_bf16_m256(int n, bool a_mn, bool b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
+         ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+}
+
+// Pair tile t of CTA `rank`: the pair covers M tiles 2 mt and 2 mt + 1 of the single-CTA plan.
+template <int VAR>
+__device__ __forceinline__ Tile get_tile_pair(const Params& p, const int32_t* s_plan,
+                                              const int32_t* s_off, int t, uint32_t rank) {
+  const int MTp = p.MT / 2;
+  const int e = upper_bound_i32(s_plan, p.E + 1, t / MTp) - 1;
+  const int nts = s_plan[e + 1] - s_plan[e];
+  const int local = t - MTp * s_plan[e];
+  const int mt = 2 * (local / nts) + (int)rank, nt = local % nts;
+  return get_tile<VAR>(p, s_plan, s_off, p.MT * s_plan[e] + mt * nts + nt);
+}
+
+template <int VAR>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const Params p) {
+  static_assert(!VarTraits<VAR>::router, "the router GEMM runs on single CTAs");
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + pr::STAGES * pr::STAGE_BYTES);
+  // bars: full[STAGES], empty[STAGES], tfull[2], tempty[2], drain[1]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * pr::STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int32_t* s_plan = reinterpret_cast<int32_t*>(smem + pr::STAGES * pr::STAGE_BYTES + 256);
+  int32_t* s_off = s_plan + (MAX_E + 1);
+  uint8_t* epi_stage = smem + pr::STAGES * pr::STAGE_BYTES + PLAN_BYTES;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const uint32_t rank = cluster_rank();
+  const bool even = rank == 0;
+  const uint32_t full0 = smem_u32(bars), empty0 = full0 + 8 * pr::STAGES;
+  const uint32_t tfull0 = empty0 + 8 * pr::STAGES, tempty0 = tfull0 + 16, drain = tempty0 + 16;
+  const uint32_t peer_abort = map_to_peer(smem_u32((const void*)abort_flag), rank);
+  auto give_up = [&]() {
+    *abort_flag = 1;
+    st_cluster_u32(peer_abort, 1u);
+    flag_status(p.status, USAF_DEV_TIMEOUT);
+  };
+
+  for (int i = threadIdx.x; i <= p.E; i += blockDim.x) {
+    s_off[i] = p.off[i];
+    s_plan[i] = p.plan[i];
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < pr::STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(tfull0 + 8 * a, 1);
+      mbar_init(tempty0 + 8 * a, 2 * EPI_WARPS);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 1) {  // one warp of each CTA allocates, together, the same columns in both
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(tmem_slot)),
+                 "r"(TMEM_COLS)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_barrier();  // both CTAs' barriers and abort flags are initialised
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = (p.MT / 2) * s_plan[p.E];
+  const int npairs = (int)(gridDim.x / 2), pair0 = (int)(blockIdx.x / 2);
+  bool failed = false;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer (both CTAs)
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t issued = 0;
+      const uint32_t full_even0 = even ? full0 : map_to_cta0(full0);
+      for (int t = pair0; t < total && !failed; t += npairs) {
+        const Tile ti = get_tile_pair<VAR>(p, s_plan, s_off, t, rank);
+        const int nkb = (ti.klen + BK - 1) / BK;
+        const int half = ti.nrows / 2;  // a multiple of 8
+        const int nbox = (half + 63) / 64;
+        const int tok0 = ti.row0 + (int)rank * half;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(empty0 + 8 * stage, phase ^ 1, abort_flag)) {
+            failed = true;
+            break;
+          }
+          const uint32_t a_dst = smem_u32(smem + stage * pr::STAGE_BYTES);
+          const uint32_t b_dst = a_dst + pr::A_BYTES;
+          const uint32_t fb = full_even0 + 8 * stage;
+          const int k0 = kb * BK;
+          if (even) mbar_expect_tx(full0 + 8 * stage, 2 * (pr::A_BYTES + nbox * B_BOX));
+          if constexpr (VAR == V_GATEUP) {
+            tma_4d_pair(a_dst, &tmA, fb, k0, 0, ti.m0, ti.e);
+          } else if constexpr (VAR == V_DOWN) {
+            tma_2d_pair(a_dst, &tmA, fb, k0, ti.e * p.H + ti.m0);
+          } else if constexpr (VAR == V_GVEC) {
+            tma_2d_pair(a_dst, &tmA, fb, ti.m0, ti.e * p.H + k0);
+            tma_2d_pair(a_dst + 8192, &tmA, fb, ti.m0 + 64, ti.e * p.H + k0);
+          } else {  // V_DX
+            tma_2d_pair(a_dst, &tmA, fb, ti.m0, ti.e * 2 * p.I + k0);
+            tma_2d_pair(a_dst + 8192, &tmA, fb, ti.m0 + 64, ti.e * 2 * p.I + k0);
+          }
+          for (int q = 0; q < nbox; ++q) tma_2d_pair(b_dst + q * B_BOX, &tmB, fb, tok0 + 64 * q, k0);
+          ++issued;
+          if (++stage == pr::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (failed) give_up();
+      // the even CTA's full barriers complete when both CTAs' copies of a stage have landed
+      if (even) {
+        const long long deadline = clock64() + TIMEOUT_CYCLES;
+        for (int s = 0; s < pr::STAGES && (uint32_t)s < issued; ++s) {
+          const uint32_t last = issued - 1 - ((issued - 1 - s) % pr::STAGES);
+          mbar_drain(full0 + 8 * s, (last / pr::STAGES) & 1, deadline);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && even) {
+      // ------------------------------------------------------------ MMA issuer (even CTA)
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      constexpr bool a_mn = VarTraits<VAR>::a_mn;
+      const uint32_t a_step = a_mn ? 2048 : 32, b_step = 2048;
+      const uint32_t a_lbo = a_mn ? 8192 : 16, b_lbo = B_BOX;
+      const uint64_t ad0 = sdesc(smem_u32(smem), a_lbo, 1024);
+      const uint64_t bd0 = sdesc(smem_u32(smem) + pr::A_BYTES, b_lbo, 1024);
+      for (int t = pair0; t < total && !failed; t += npairs) {
+        const Tile ti = get_tile_pair<VAR>(p, s_plan, s_off, t, rank);
+        if (!mbar_wait(tempty0 + 8 * acc, acc_phase ^ 1, abort_flag)) {
+          failed = true;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * BN;
+        const uint32_t idesc = idesc_bf16_m256(ti.nrows, a_mn, true);
+        const int nkb = (ti.klen + BK - 1) / BK;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(full0 + 8 * stage, phase, abort_flag)) {
+            failed = true;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t so = (uint64_t)((stage * pr::STAGE_BYTES) >> 4);
+#pragma unroll
+          for (int ks = 0; ks < BK / 16; ++ks)
+            umma_bf16_pair(d, ad0 + so + ((ks * a_step) >> 4), bd0 + so + ((ks * b_step) >> 4),
+                           idesc, (kb | ks) != 0 ? 1u : 0u);
+          umma_commit_both(empty0 + 8 * stage);
+          if (++stage == pr::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (failed) break;
+        umma_commit_both(tfull0 + 8 * acc);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      if (failed) give_up();
+      // every MMA this thread issued completes before either CTA releases tensor memory
+      umma_commit_local_pair(drain);
+      mbar_drain(drain, 0, clock64() + TIMEOUT_CYCLES);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue warps 2..9
+    const int q = warp & 3;
+    const int half = (warp - 2) >> 2;
+    const int row = q * 32 + lane;
+    const uint32_t tempty_even0 = even ? tempty0 : map_to_cta0(tempty0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = pair0; t < total; t += npairs) {
+      const Tile ti = get_tile_pair<VAR>(p, s_plan, s_off, t, rank);
+      EpiPre pre;
+      epi_prefetch<VAR>(p, ti, row, lane, half, pre);
+      int ok = 1;
+      if (lane == 0) {
+        ok = mbar_wait(tfull0 + 8 * acc, acc_phase, abort_flag) ? 1 : 0;
+        if (!ok) give_up();
+      }
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      epilogue<VAR>(p, ti, tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN, row, lane, half,
+                    pre, epi_stage + (warp - 2) * EPI_STAGE_BYTES);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty_even0 + 8 * acc);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_barrier();  // the pair's MMAs are complete and neither CTA reads the other any more
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                 "r"(TMEM_COLS)
+                 : "memory");
+  }
+}
+
 // ---------------------------------------------------------------------------- dense weight gradient
 // Dense expert weight gradient for the importance phase (the whole |g| is ranked there):
 //   gate_up[e]:  G[j, c] = sum over the expert's tokens of dh^T[j, t] x^T[c, t]      (2I x H)
@@ -1059,15 +1375,6 @@ __device__ __forceinline__ uint32_t ld_peer_u32(uint32_t addr) {
   asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
   return v;
 }
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_barrier() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
-                   : "memory");
-}
 
 // grid (RK_SPLIT * token tiles, expert tiles), clusters of RK_SPLIT along x
 __global__ void __launch_bounds__(RK_THREADS, 1)
@@ -1330,8 +1637,29 @@ bool map_tokens(CUtensorMap* m, const void* base, uint64_t features, uint64_t R_
 constexpr const char* VAR_NAME[5] = {"tc_gate_up_swiglu", "tc_down_combine", "tc_gvec_swiglu_bwd",
                                      "tc_dx", "tc_router_logits"};
 
+// The CTA-pair kernel where the M tiles pair up (an even count of 128-row tiles); the
+// single-CTA kernel otherwise.
+template <int VAR>
+usaf_status launch_pair(const CUtensorMap& a, const CUtensorMap& b, const Params& p,
+                        cudaStream_t st) {
+  USAF_TRACE(VAR_NAME[VAR], st);
+  static bool attr_done = false;
+  if (!attr_done) {
+    if (cudaFuncSetAttribute(tc_gemm_pair_kernel<VAR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             pr::SMEM) != cudaSuccess)
+      return USAF_ERR_CUDA;
+    attr_done = true;
+  }
+  tc_gemm_pair_kernel<VAR><<<device_sm_count() / 2 * 2, NUM_THREADS, pr::SMEM, st>>>(a, b, p);
+  USAF_CHECK_LAUNCH();
+  return USAF_OK;
+}
+
 template <int VAR>
 usaf_status launch(const CUtensorMap& a, const CUtensorMap& b, const Params& p, cudaStream_t st) {
+  if constexpr (!VarTraits<VAR>::router) {
+    if (p.MT % 2 == 0) return launch_pair<VAR>(a, b, p, st);
+  }
   USAF_TRACE(VAR_NAME[VAR], st);
   static bool attr_done = false;
   if (!attr_done) {
