@@ -99,7 +99,10 @@ usaf_status tc_fwd_down(const MoeArgs& a, const void* wa, float* y_acc, cudaStre
 // dw_part [4 * ceil(I / 128)][T*k]: one partial of dw per (M tile, row quarter, slot)
 usaf_status tc_bwd_gvec(const MoeArgs& a, const void* dyT, const void* hT, void* dhT,
                         float* dw_part, cudaStream_t st);
-usaf_status tc_bwd_dx(const MoeArgs& a, const void* dh, float* dx_acc, cudaStream_t st);
+// dl_perm (may be null): dlogit per permuted row; with it the router's share of dx (renormalised
+// routing) is added in the epilogue
+usaf_status tc_bwd_dx(const MoeArgs& a, const void* dh, float* dx_acc, const float* dl_perm,
+                      cudaStream_t st);
 // dense expert weight gradient g[e] (a_rows x b_rows, fp32) = aT . bT^T over each expert's tokens
 usaf_status tc_wgrad_dense(const MoeArgs& a, const void* aT, int64_t a_rows, const void* bT,
                            int64_t b_rows, float* g, int accumulate, cudaStream_t st);

@@ -663,44 +663,79 @@ __global__ void __launch_bounds__(SD_WARPS * 32, SD_BLOCKS_PER_SM) sddmm_kernel(
   flag_status_warp(dev_status, badidx, USAF_DEV_BAD_INDEX);
 }
 
-// g_router[e, h] = sum over the rows routed to e of dl[row] * x^T[h, row] (renormalised routing):
-// one group of eight lanes per (e, h), 16-byte vectors of x^T.
+// g_router[e, h] = sum over the rows routed to e of dl[row] * x[tok(row), h] (renormalised
+// routing), read from the token-major x: the expert's rows gather its tokens' rows of x, which
+// stay in L2 (x is T x H) while the eight experts of each token read them. A block takes one expert
+// and 32 x VW features (one 16-byte vector per lane); its eight warps take contiguous eighths of
+// the expert's rows with four rows' loads in flight, and the eight partial sums are added in warp
+// order, so the result does not depend on scheduling.
 template <typename T>
 __global__ void __launch_bounds__(256) g_router_sel_kernel(
-    const T* __restrict__ xT, const float* __restrict__ dl_perm, const int32_t* __restrict__ cnt,
-    const int32_t* __restrict__ off, int E, int H, int64_t rcap, float* __restrict__ g_router,
-    int accumulate, uint32_t* dev_status) {
+    const T* __restrict__ x, const int32_t* __restrict__ ptok, const float* __restrict__ dl_perm,
+    const int32_t* __restrict__ cnt, const int32_t* __restrict__ off, int H,
+    float* __restrict__ g_router, int accumulate, uint32_t* dev_status) {
   constexpr int VW = 16 / sizeof(T);
-  const int lane = threadIdx.x & 31, grp = lane >> 3, gl = lane & 7;
-  const int64_t groups = (int64_t)gridDim.x * (blockDim.x >> 3);
-  bool bad = false;
-  for (int64_t u0 = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * 4;
-       u0 < (int64_t)E * H; u0 += groups) {
-    const int64_t u = u0 + grp;
-    float acc = 0.f;
-    if (u < (int64_t)E * H) {
-      const int e = (int)(u / H), h = (int)(u % H);
-      const int o = off[e];
-      const int n = (cnt[e] + VW - 1) / VW * VW;
-      const T* xr = xT + (int64_t)h * rcap + o;
-      const float* d = dl_perm + o;
-      const int cn = cnt[e];  // dl_perm holds no value past the expert's routed rows
-      for (int t = gl * VW; t < n; t += 8 * VW) {
-        const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xr + t));
-        const T* xe = reinterpret_cast<const T*>(&xv);
+  constexpr int FB = 32 * VW;  // features per block
+  __shared__ float part[8][FB];
+  const int e = blockIdx.y, lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int h = blockIdx.x * FB + lane * VW;
+  const int o = off[e], n = cnt[e];
+  const int r0 = (int)((int64_t)n * wid / 8), r1 = (int)((int64_t)n * (wid + 1) / 8);
+  const bool vec = (H % VW) == 0;
+  struct Vec {
+    float f[VW];
+  };
+  float acc[VW];
 #pragma unroll
-        for (int q = 0; q < VW; ++q)
-          if (t + q < cn) acc = fmaf(d[t + q], to_f32(xe[q]), acc);
-      }
+  for (int q = 0; q < VW; ++q) acc[q] = 0.f;
+  auto load = [&](int tk) {
+    alignas(16) T buf[VW];
+    if (vec && h < H) {
+      *reinterpret_cast<uint4*>(buf) = __ldg(reinterpret_cast<const uint4*>(x + (int64_t)tk * H + h));
+    } else {
+#pragma unroll
+      for (int q = 0; q < VW; ++q)
+        buf[q] = h + q < H ? x[(int64_t)tk * H + h + q] : from_f32<T>(0.f);
     }
-    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-    if (gl == 0 && u < (int64_t)E * H) {
-      const float gv = accumulate ? g_router[u] + acc : acc;
-      g_router[u] = gv;
-      bad |= !finite_f(gv);
+    Vec v;
+#pragma unroll
+    for (int q = 0; q < VW; ++q) v.f[q] = to_f32(buf[q]);
+    return v;
+  };
+  int r = r0;
+  for (; r + 4 <= r1; r += 4) {
+    Vec v[4];
+    float d[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      d[u] = dl_perm[o + r + u];
+      v[u] = load(ptok[o + r + u]);
     }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int q = 0; q < VW; ++q) acc[q] = fmaf(d[u], v[u].f[q], acc[q]);
+  }
+  for (; r < r1; ++r) {
+    const float d = dl_perm[o + r];
+    const Vec v = load(ptok[o + r]);
+#pragma unroll
+    for (int q = 0; q < VW; ++q) acc[q] = fmaf(d, v.f[q], acc[q]);
+  }
+#pragma unroll
+  for (int q = 0; q < VW; ++q) part[wid][lane * VW + q] = acc[q];
+  __syncthreads();
+  bool bad = false;
+  for (int c = threadIdx.x; c < FB; c += blockDim.x) {
+    const int hh = blockIdx.x * FB + c;
+    if (hh >= H) continue;
+    float sum = 0.f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) sum += part[w][c];
+    const int64_t u = (int64_t)e * H + hh;
+    const float gv = accumulate ? g_router[u] + sum : sum;
+    g_router[u] = gv;
+    bad |= !finite_f(gv);
   }
   flag_status_warp(dev_status, bad, USAF_DEV_NONFINITE);
 }
@@ -813,12 +848,13 @@ __global__ void g_router_dense_kernel(const T* __restrict__ x, const float* __re
 }
 
 // dx[t, h] = dx_acc[t, h] + router term: sum_j dl[t,j] Wr[e_j, h] (renormalised routing) or
-// sum_e dlogit[t,e] Wr[e, h]. One token per block, four h per thread.
+// sum_e dlogit[t,e] Wr[e, h]; router_term = 0 when the dx GEMM's epilogue already added it. One
+// token per block, four h per thread.
 template <typename T>
 __global__ void __launch_bounds__(256) dx_finalize_kernel(
     const float* __restrict__ dx_acc, const float* __restrict__ wr, const int32_t* __restrict__ idx,
     const float* __restrict__ dl, const float* __restrict__ dlogit, int Tn, int H, int E, int k,
-    int renorm, T* __restrict__ dx, uint32_t* dev_status) {
+    int renorm, int router_term, T* __restrict__ dx, uint32_t* dev_status) {
   __shared__ float s_d[1024];
   __shared__ int s_e[32];
   const int t = blockIdx.x;
@@ -842,7 +878,7 @@ __global__ void __launch_bounds__(256) dx_finalize_kernel(
 #pragma unroll
       for (int q = 0; q < 4; ++q) v[q] = h0 + q < H ? dx_acc[(int64_t)t * H + h0 + q] : 0.f;
     }
-    const int nterm = renorm ? k : E;
+    const int nterm = !router_term ? 0 : renorm ? k : E;
     for (int j = 0; j < nterm; ++j) {
       const float d = s_d[j];
       const float* wrow = wr + (int64_t)(renorm ? s_e[j] : j) * H + h0;
@@ -1054,8 +1090,10 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
       dlogit_sel_kernel<<<(unsigned)ceil_div(Tn, 128), 128, 0, st>>>(
           a.rt.topk_w, dw, a.rt.slot_row, Tn, k, w.dl, w.dl_perm);
       USAF_CHECK_LAUNCH();
-      g_router_sel_kernel<T><<<(unsigned)ceil_div(s.E * s.H, 32), 256, 0, st>>>(
-          xT, w.dl_perm, cnt, off, E, H, a.R_cap, g_router, accumulate, dev_status);
+      constexpr int FB = 32 * (16 / (int)sizeof(T));
+      g_router_sel_kernel<T><<<dim3((unsigned)ceil_div(H, FB), (unsigned)E), 256, 0, st>>>(
+          static_cast<const T*>(a.x), a.rt.perm_tok, w.dl_perm, cnt, off, H, g_router,
+          accumulate, dev_status);
       USAF_CHECK_LAUNCH();
     } else {
       dlogit_dense_kernel<<<(unsigned)Tn, 128, 0, st>>>(logits, a.rt.topk_idx, a.rt.topk_w, dw,
@@ -1067,9 +1105,12 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
     }
   }
   // S8: dx
+  // with renormalised routing the tensor-core dx epilogue adds the router's share itself
+  const bool rterm_in_gemm = a.dt == USAF_BF16 && renorm &&
+                             (reinterpret_cast<uintptr_t>(a.w_router) & 15) == 0;
   if (dx) {
     if (a.dt == USAF_BF16) {
-      USAF_TRY(tc_bwd_dx(a, dhT, w.dx_acc, st));
+      USAF_TRY(tc_bwd_dx(a, dhT, w.dx_acc, rterm_in_gemm ? w.dl_perm : nullptr, st));
     } else {
       USAF_TRACE("simt_dx", st);
       ProbDx<T> p{dhT, static_cast<const T*>(a.w_gate_up), w.dx_acc, cnt, off, a.rt.perm_tok,
@@ -1080,8 +1121,8 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
     }
     USAF_TRACE("dx_finalize", st);
     dx_finalize_kernel<T><<<(unsigned)Tn, 256, 0, st>>>(w.dx_acc, a.w_router, a.rt.topk_idx, w.dl,
-                                                        w.dlogit, Tn, H, E, k, renorm, dx,
-                                                        dev_status);
+                                                        w.dlogit, Tn, H, E, k, renorm,
+                                                        rterm_in_gemm ? 0 : 1, dx, dev_status);
     USAF_CHECK_LAUNCH();
   }
   // S9, S10: expert weight gradients at the active set

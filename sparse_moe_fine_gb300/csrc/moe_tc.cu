@@ -65,6 +65,8 @@ struct Params {
   __nv_bfloat16* dh;      // dh^T out (S6)
   const __nv_bfloat16* hin;  // h^T in (S6)
   const float* wperm;        // routing weight per permuted row (0 in padding)
+  const float* dl_perm;      // S8 (may be null): dlogit of each permuted row's slot, for the
+  const float* w_router;     //   router term dl * Wr[e, :] added in the dx epilogue
   uint32_t* status;
 };
 
@@ -320,7 +322,10 @@ __device__ __forceinline__ void epi_prefetch(const Params& p, const Tile& ti, in
       const bool in = ch < nch && col < ti.nrows;
       pre.slot[c] = in ? p.pslot[ti.row0 + col] : -1;
       pre.tok[c] = in && (VAR == V_DOWN || VAR == V_DX) ? p.ptok[ti.row0 + col] : 0;
-      pre.w[c] = in && (VAR == V_GATEUP || VAR == V_GVEC) ? p.wperm[ti.row0 + col] : 0.f;
+      pre.w[c] = !in ? 0.f
+                 : (VAR == V_GATEUP || VAR == V_GVEC) ? p.wperm[ti.row0 + col]
+                 : (VAR == V_DX && p.dl_perm) ? p.dl_perm[ti.row0 + col]
+                                               : 0.f;
     }
     if constexpr (VAR == V_GVEC) {
       const int i = ti.m0 + row;
@@ -402,6 +407,12 @@ __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32
       const int tokv = slot >= 0 ? tok : -1;  // the column's token, -1 for a padding row
       const int pc = lane & 3;
       const int hq = ti.m0 + row - lane + (lane & ~3);  // first of this lane's four rows
+      // S8 with renormalised routing: the router's share of dx, dl of the column's slot times
+      // Wr[e, h], joins the same atomic (rows hq .. hq + 3 of the expert's router row)
+      const bool rterm = VAR == V_DX && p.dl_perm != nullptr && hq < H;
+      const float4 wr4 = rterm ? __ldg(reinterpret_cast<const float4*>(
+                                     p.w_router + (int64_t)ti.e * H + hq))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int j0 = 0; j0 < 32; j0 += 4) {
         if (j0 >= ncol) break;
@@ -431,6 +442,13 @@ __device__ __forceinline__ void epilogue(const Params& p, const Tile& ti, uint32
           }
         }
         const int tj = __shfl_sync(FULL, tokv, j0 + pc);
+        if (rterm) {
+          const float dj = __shfl_sync(FULL, wl, j0 + pc);
+          x0 = fmaf(dj, wr4.x, x0);
+          x1 = fmaf(dj, wr4.y, x1);
+          x2 = fmaf(dj, wr4.z, x2);
+          x3 = fmaf(dj, wr4.w, x3);
+        }
         if (tj >= 0 && hq < H)
           atomicAdd(reinterpret_cast<float4*>(&p.acc_out[(int64_t)tj * H + hq]),
                     make_float4(x0, x1, x2, x3));
@@ -1809,7 +1827,8 @@ usaf_status tc_bwd_gvec(const MoeArgs& a, const void* dyT, const void* hT, void*
   return launch<V_GVEC>(ma, mb, p, st);
 }
 
-usaf_status tc_bwd_dx(const MoeArgs& a, const void* dhT, float* dx_acc, cudaStream_t st) {
+usaf_status tc_bwd_dx(const MoeArgs& a, const void* dhT, float* dx_acc, const float* dl_perm,
+                      cudaStream_t st) {
   CUtensorMap ma, mb;
   if (!map_2d(&ma, a.w_gate_up, a.s.H, a.s.E * 2 * a.s.I, 64, 64) ||
       !map_tokens(&mb, dhT, 2 * a.s.I, a.R_cap))
@@ -1817,6 +1836,8 @@ usaf_status tc_bwd_dx(const MoeArgs& a, const void* dhT, float* dx_acc, cudaStre
   Params p = base_params(a);
   p.MT = (int)ceil_div(a.s.H, BM);
   p.acc_out = dx_acc;
+  p.dl_perm = dl_perm;
+  p.w_router = a.w_router;
   return launch<V_DX>(ma, mb, p, st);
 }
 
