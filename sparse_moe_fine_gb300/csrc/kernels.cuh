@@ -1,6 +1,8 @@
 // Internal launch interfaces between the ABI layer and the kernel files.
 #pragma once
 
+#include <cuda.h>
+
 #include "common.cuh"
 
 namespace usaf {
@@ -99,6 +101,9 @@ usaf_status tc_fwd_down(const MoeArgs& a, const void* wa, float* y_acc, cudaStre
 // dw_part [4 * ceil(I / 128)][T*k]: one partial of dw per (M tile, row quarter, slot)
 usaf_status tc_bwd_gvec(const MoeArgs& a, const void* dyT, const void* hT, void* dhT,
                         float* dw_part, cudaStream_t st);
+// The tensor map of a feature-major token array [features, R_cap] (bf16) in boxes of 64 tokens x
+// 64 features, 128-byte swizzle: the GEMMs' token operand, and the gather's TMA store target.
+bool tc_token_map(CUtensorMap* m, const void* base, uint64_t features, uint64_t R_cap);
 // dl_perm (may be null): dlogit per permuted row; with it the router's share of dx (renormalised
 // routing) is added in the epilogue
 usaf_status tc_bwd_dx(const MoeArgs& a, const void* dh, float* dx_acc, const float* dl_perm,

@@ -341,23 +341,30 @@ __global__ void __launch_bounds__(256, 8) gather_transpose_kernel(
   }
 }
 
-// Gather-transpose of bf16 rows without shared memory: a thread takes 8 permuted rows x 8
-// features (one 16-byte vector of each row), transposes the 8 x 8 block in registers (one byte
-// permute per output word) and writes 8 feature rows of 8 tokens (16 bytes each). Lane l of a
-// warp takes rows 8 (l / 8) .. + 8 of the warp's 32 and features 8 (l % 8) .. + 8, so each load
-// instruction reads 128 contiguous bytes of 4 rows and each store writes 64 contiguous bytes of 8
-// feature rows. A block of 8 warps covers 256 rows x 64 features (H a multiple of 64, R_cap a
-// multiple of 256). Side duties as in gather_transpose_kernel.
+// Gather-transpose of bf16 rows: a block takes 256 permuted rows x 64 features and writes the
+// transposed tile with four TMA stores of 64 tokens x 64 features (128-byte swizzled boxes). Lane
+// l of warp w takes the eight rows 32 w + 8 (l / 8) .. + 8 and the eight features 8 (l % 8) .. + 8,
+// so each load instruction reads 128 contiguous bytes of four rows; it transposes its 8 x 8 block
+// in registers (one byte permute per output word) and puts each feature's eight tokens into the
+// box. In the box, 16-byte chunk c of feature row f sits at chunk c ^ (f % 8); lane l writes its
+// eight feature rows starting from row l % 8 of its eight, so the eight lanes that share a token
+// chunk write eight different chunk positions and every store is conflict-free. H a multiple of
+// 64, R_cap of 256. Side duties as in gather_transpose_kernel.
 constexpr int GR_ROWS = 256;
+constexpr int GR_SMEM = 4 * 8192 + 1024;  // four boxes, and room to align them to 1 KB
 __global__ void __launch_bounds__(256) gather_transpose_bf16_kernel(
-    const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ ptok,
-    const int32_t* __restrict__ pslot, const int32_t* __restrict__ off_end, int64_t R_cap, int H,
-    __nv_bfloat16* __restrict__ xT, const float* __restrict__ topk_w, float* __restrict__ wperm,
-    GatherExtra ex) {
+    const __grid_constant__ CUtensorMap tm_out, const __nv_bfloat16* __restrict__ x,
+    const int32_t* __restrict__ ptok, const int32_t* __restrict__ pslot,
+    const int32_t* __restrict__ off_end, int64_t R_cap, int H, const float* __restrict__ topk_w,
+    float* __restrict__ wperm, GatherExtra ex) {
+  extern __shared__ uint8_t gr_raw[];
+  uint8_t* tile = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gr_raw) + 1023) &
+                                             ~uintptr_t(1023));
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  // this thread's first row and first feature
-  const int64_t r0 = (int64_t)blockIdx.x * GR_ROWS + wid * 32 + (lane >> 3) * 8;
-  const int f0 = blockIdx.y * 64 + (lane & 7) * 8;
+  const int tl = wid * 32 + (lane >> 3) * 8;  // first row within the block's 256
+  const int fl = (lane & 7) * 8;              // first feature within the block's 64
+  const int64_t r0 = (int64_t)blockIdx.x * GR_ROWS + tl;
+  const int f0 = blockIdx.y * 64 + fl;
   const int64_t end = *off_end;
   int tok[8];
   bool live[8];
@@ -395,20 +402,53 @@ __global__ void __launch_bounds__(256) gather_transpose_bf16_kernel(
       wperm[row] = sl >= 0 ? topk_w[sl] : 0.f;
     }
   }
-  // feature 2w takes the low halves of word w of rows 2u, 2u+1; feature 2w+1 the high halves
+  // out[j]: feature fl + j, the eight rows' tokens; feature 2w takes the low halves of word w of
+  // rows 2u, 2u+1 and feature 2w+1 the high halves
+  uint4 out[8];
 #pragma unroll
   for (int w = 0; w < 4; ++w) {
-    uint4 lo, hi;
-    lo.x = __byte_perm(a[0][w], a[1][w], 0x5410);
-    lo.y = __byte_perm(a[2][w], a[3][w], 0x5410);
-    lo.z = __byte_perm(a[4][w], a[5][w], 0x5410);
-    lo.w = __byte_perm(a[6][w], a[7][w], 0x5410);
-    hi.x = __byte_perm(a[0][w], a[1][w], 0x7632);
-    hi.y = __byte_perm(a[2][w], a[3][w], 0x7632);
-    hi.z = __byte_perm(a[4][w], a[5][w], 0x7632);
-    hi.w = __byte_perm(a[6][w], a[7][w], 0x7632);
-    *reinterpret_cast<uint4*>(xT + (int64_t)(f0 + 2 * w) * R_cap + r0) = lo;
-    *reinterpret_cast<uint4*>(xT + (int64_t)(f0 + 2 * w + 1) * R_cap + r0) = hi;
+    out[2 * w].x = __byte_perm(a[0][w], a[1][w], 0x5410);
+    out[2 * w].y = __byte_perm(a[2][w], a[3][w], 0x5410);
+    out[2 * w].z = __byte_perm(a[4][w], a[5][w], 0x5410);
+    out[2 * w].w = __byte_perm(a[6][w], a[7][w], 0x5410);
+    out[2 * w + 1].x = __byte_perm(a[0][w], a[1][w], 0x7632);
+    out[2 * w + 1].y = __byte_perm(a[2][w], a[3][w], 0x7632);
+    out[2 * w + 1].z = __byte_perm(a[4][w], a[5][w], 0x7632);
+    out[2 * w + 1].w = __byte_perm(a[6][w], a[7][w], 0x7632);
+  }
+  // rotate by rot = lane % 8 (three conditional rotations): out[k] becomes feature fl + (k + rot) % 8
+  const int rot = lane & 7;
+#pragma unroll
+  for (int sh = 1; sh < 8; sh <<= 1) {
+    if (rot & sh) {
+      uint4 t[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) t[k] = out[(k + sh) & 7];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) out[k] = t[k];
+    }
+  }
+  uint8_t* bx = tile + (tl >> 6) * 8192;
+  const int c = (tl & 63) >> 3;  // this thread's 16-byte token chunk within the box's rows
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int fk = (k + rot) & 7;  // = f % 8
+    *reinterpret_cast<uint4*>(bx + (fl + fk) * 128 + ((c ^ fk) << 4)) = out[k];
+  }
+  // the tile is complete in shared memory: make it visible to the copy engine and store it
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const uint32_t src = static_cast<uint32_t>(__cvta_generic_to_shared(tile));
+    for (int b = 0; b < 4; ++b)
+      asm volatile(
+          "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+              reinterpret_cast<uint64_t>(&tm_out)),
+          "r"((int)(blockIdx.x * GR_ROWS + b * 64)), "r"((int)(blockIdx.y * 64)),
+          "r"(src + b * 8192)
+          : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");  // written before the block ends
   }
 }
 
@@ -935,12 +975,21 @@ static usaf_status gather_t(const MoeArgs& a, const T* src, T* dstT, cudaStream_
                            GatherExtra ex) {
   if constexpr (sizeof(T) == 2) {
     const auto al16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
+    CUtensorMap tm;
     if (a.s.H % 64 == 0 && a.R_cap % GR_ROWS == 0 && al16(src) && al16(dstT) &&
-        al16(a.rt.perm_tok) && al16(a.rt.perm_slot)) {
+        al16(a.rt.perm_tok) && al16(a.rt.perm_slot) && tc_token_map(&tm, dstT, a.s.H, a.R_cap)) {
+      static bool attr_done = false;
+      if (!attr_done) {
+        if (cudaFuncSetAttribute(gather_transpose_bf16_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 GR_SMEM) != cudaSuccess)
+          return USAF_ERR_CUDA;
+        attr_done = true;
+      }
       const dim3 grid((unsigned)(a.R_cap / GR_ROWS), (unsigned)(a.s.H / 64));
-      gather_transpose_bf16_kernel<<<grid, 256, 0, st>>>(
-          src, a.rt.perm_tok, a.rt.perm_slot, a.rt.expert_offset + a.s.E, a.R_cap, (int)a.s.H,
-          dstT, a.rt.topk_w, a.wperm, ex);
+      gather_transpose_bf16_kernel<<<grid, 256, GR_SMEM, st>>>(
+          tm, src, a.rt.perm_tok, a.rt.perm_slot, a.rt.expert_offset + a.s.E, a.R_cap,
+          (int)a.s.H, a.rt.topk_w, a.wperm, ex);
       USAF_CHECK_LAUNCH();
       return USAF_OK;
     }

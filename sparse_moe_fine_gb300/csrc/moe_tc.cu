@@ -1742,6 +1742,10 @@ static bool router_split_ok() {
   return ok == 1;
 }
 
+bool tc_token_map(CUtensorMap* m, const void* base, uint64_t features, uint64_t R_cap) {
+  return map_tokens(m, base, features, R_cap);
+}
+
 usaf_status tc_router_logits(const usaf_moe_shape& s, const void* x, const float* wr,
                              void* wr3, float* logits, uint32_t* status, cudaStream_t st) {
   {
