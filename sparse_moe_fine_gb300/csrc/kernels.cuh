@@ -39,6 +39,7 @@ struct BwdWs {
   int32_t* plan;      // [E+1] prefix of token tiles per expert (tensor-core path)
   float* wperm;       // [R_cap] routing weight per permuted row
   void* dy_perm;      // dy^T [H, R_cap]: dy in permuted order, feature-major
+  float* g_part;      // [token tiles][H] router-gradient partial sums (tensor-core path)
 };
 void fwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, Carver& c, FwdWs& w);
 void bwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, int64_t K, Carver& c, BwdWs& w);

@@ -704,23 +704,41 @@ __global__ void __launch_bounds__(SD_WARPS * 32, SD_BLOCKS_PER_SM) sddmm_kernel(
 }
 
 // g_router[e, h] = sum over the rows routed to e of dl[row] * x[tok(row), h] (renormalised
-// routing), read from the token-major x: the expert's rows gather its tokens' rows of x, which
-// stay in L2 (x is T x H) while the eight experts of each token read them. A block takes one expert
-// and 32 x VW features (one 16-byte vector per lane); its eight warps take contiguous eighths of
-// the expert's rows with four rows' loads in flight, and the eight partial sums are added in warp
-// order, so the result does not depend on scheduling.
+// routing), read from the token-major x, whose rows stay in L2 while the eight experts of each
+// token read them. On the tensor-core path (g_router_part_kernel):
+// block (features, t) takes token tile t of the tensor-core tile plan (at most 256 rows of one
+// expert, the experts' rows split in equal 16-row multiples) and 32 x VW features (one 16-byte
+// vector per lane); its eight warps take contiguous eighths of the tile's rows with four rows'
+// loads in flight, and the eight sums are added in warp order. A crowded expert is spread over as
+// many blocks as it has tiles, each writing its sums to part[t][h]; g_router_reduce_kernel then
+// adds them in tile order. An expert of one tile is written directly, one of none gets zeros from
+// the reduction. The result does not depend on scheduling.
 template <typename T>
-__global__ void __launch_bounds__(256) g_router_sel_kernel(
+__global__ void __launch_bounds__(256) g_router_part_kernel(
     const T* __restrict__ x, const int32_t* __restrict__ ptok, const float* __restrict__ dl_perm,
-    const int32_t* __restrict__ cnt, const int32_t* __restrict__ off, int H,
+    const int32_t* __restrict__ cnt, const int32_t* __restrict__ off,
+    const int32_t* __restrict__ plan, int E, int H, float* __restrict__ part,
     float* __restrict__ g_router, int accumulate, uint32_t* dev_status) {
   constexpr int VW = 16 / sizeof(T);
   constexpr int FB = 32 * VW;  // features per block
-  __shared__ float part[8][FB];
-  const int e = blockIdx.y, lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  __shared__ float sp[8][FB];
+  const int t = blockIdx.y;
+  if (t >= plan[E]) return;  // the grid covers the most tiles any routing can have
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int lo = 0, hi = E;  // the tile's expert: the last e with plan[e] <= t
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (plan[mid] <= t) lo = mid;
+    else hi = mid;
+  }
+  const int e = lo;
+  const int nts = plan[e + 1] - plan[e], npad = off[e + 1] - off[e];
+  const int base = ((npad + nts - 1) / nts + 15) / 16 * 16;
+  const int row0 = off[e] + (t - plan[e]) * base;
+  const int rend = min(row0 + base, off[e] + cnt[e]);  // routed rows only (not the padding)
+  const int n = max(0, rend - row0);
+  const int r0 = row0 + (int)((int64_t)n * wid / 8), r1 = row0 + (int)((int64_t)n * (wid + 1) / 8);
   const int h = blockIdx.x * FB + lane * VW;
-  const int o = off[e], n = cnt[e];
-  const int r0 = (int)((int64_t)n * wid / 8), r1 = (int)((int64_t)n * (wid + 1) / 8);
   const bool vec = (H % VW) == 0;
   struct Vec {
     float f[VW];
@@ -748,8 +766,8 @@ __global__ void __launch_bounds__(256) g_router_sel_kernel(
     float d[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      d[u] = dl_perm[o + r + u];
-      v[u] = load(ptok[o + r + u]);
+      d[u] = dl_perm[r + u];
+      v[u] = load(ptok[r + u]);
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u)
@@ -757,13 +775,82 @@ __global__ void __launch_bounds__(256) g_router_sel_kernel(
       for (int q = 0; q < VW; ++q) acc[q] = fmaf(d[u], v[u].f[q], acc[q]);
   }
   for (; r < r1; ++r) {
-    const float d = dl_perm[o + r];
-    const Vec v = load(ptok[o + r]);
+    const float d = dl_perm[r];
+    const Vec v = load(ptok[r]);
 #pragma unroll
     for (int q = 0; q < VW; ++q) acc[q] = fmaf(d, v.f[q], acc[q]);
   }
 #pragma unroll
-  for (int q = 0; q < VW; ++q) part[wid][lane * VW + q] = acc[q];
+  for (int q = 0; q < VW; ++q) sp[wid][lane * VW + q] = acc[q];
+  __syncthreads();
+  bool bad = false;
+  const int c = threadIdx.x;  // FB <= blockDim.x: one feature per thread
+  const int hh = blockIdx.x * FB + c;
+  float sum = 0.f;
+  if (c < FB) {
+#pragma unroll
+    for (int w = 0; w < 8; ++w) sum += sp[w][c];
+  }
+  if (nts > 1) {
+    if (c < FB && hh < H) part[(int64_t)t * H + hh] = sum;
+    return;
+  }
+  if (c < FB && hh < H) {
+    const int64_t u = (int64_t)e * H + hh;
+    const float gv = accumulate ? g_router[u] + sum : sum;
+    g_router[u] = gv;
+    bad = !finite_f(gv);
+  }
+  flag_status_warp(dev_status, bad, USAF_DEV_NONFINITE);
+}
+
+// g_router rows of the experts with several tiles (their partial sums in tile order) and of the
+// experts with none (zeros); the rows of one-tile experts are already written.
+__global__ void g_router_reduce_kernel(const float* __restrict__ part,
+                                       const int32_t* __restrict__ plan, int E, int H,
+                                       float* __restrict__ g_router, int accumulate,
+                                       uint32_t* dev_status) {
+  bool bad = false;
+  for (int64_t u = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; u < (int64_t)E * H;
+       u += (int64_t)gridDim.x * blockDim.x) {
+    const int e = (int)(u / H), h = (int)(u - (int64_t)e * H);
+    const int t0 = plan[e], t1 = plan[e + 1];
+    if (t1 - t0 == 1) continue;
+    float sum = 0.f;
+    for (int t = t0; t < t1; ++t) sum += part[(int64_t)t * H + h];
+    const float gv = accumulate ? g_router[u] + sum : sum;
+    g_router[u] = gv;
+    bad |= !finite_f(gv);
+  }
+  flag_status_warp(dev_status, bad, USAF_DEV_NONFINITE);
+}
+
+// The same sum for layers without the tile plan (fp32 layers): one block per expert and 32 x VW
+// features, its eight warps over contiguous eighths of all the expert's rows.
+template <typename T>
+__global__ void __launch_bounds__(256) g_router_sel_kernel(
+    const T* __restrict__ x, const int32_t* __restrict__ ptok, const float* __restrict__ dl_perm,
+    const int32_t* __restrict__ cnt, const int32_t* __restrict__ off, int H,
+    float* __restrict__ g_router, int accumulate, uint32_t* dev_status) {
+  constexpr int VW = 16 / sizeof(T);
+  constexpr int FB = 32 * VW;
+  __shared__ float sp[8][FB];
+  const int e = blockIdx.y, lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int h = blockIdx.x * FB + lane * VW;
+  const int o = off[e], n = cnt[e];
+  const int r0 = o + (int)((int64_t)n * wid / 8), r1 = o + (int)((int64_t)n * (wid + 1) / 8);
+  float acc[VW];
+#pragma unroll
+  for (int q = 0; q < VW; ++q) acc[q] = 0.f;
+  for (int r = r0; r < r1; ++r) {
+    const float d = dl_perm[r];
+    const int64_t xr = (int64_t)ptok[r] * H;
+#pragma unroll
+    for (int q = 0; q < VW; ++q)
+      if (h + q < H) acc[q] = fmaf(d, to_f32(x[xr + h + q]), acc[q]);
+  }
+#pragma unroll
+  for (int q = 0; q < VW; ++q) sp[wid][lane * VW + q] = acc[q];
   __syncthreads();
   bool bad = false;
   for (int c = threadIdx.x; c < FB; c += blockDim.x) {
@@ -771,7 +858,7 @@ __global__ void __launch_bounds__(256) g_router_sel_kernel(
     if (hh >= H) continue;
     float sum = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) sum += part[w][c];
+    for (int w = 0; w < 8; ++w) sum += sp[w][c];
     const int64_t u = (int64_t)e * H + hh;
     const float gv = accumulate ? g_router[u] + sum : sum;
     g_router[u] = gv;
@@ -968,6 +1055,8 @@ void bwd_ws_layout(const usaf_moe_shape& s, usaf_dtype dt, int64_t K, Carver& c,
   w.plan = dt == USAF_BF16 ? c.take<int32_t>(s.E + 1) : nullptr;
   w.wperm = c.take<float>(R_cap);
   w.dy_perm = c.take<char>(R_cap * s.H * (int64_t)es);
+  w.g_part = dt == USAF_BF16 ? c.take<float>((ceil_div(R_cap, TC_TOKEN_TILE) + s.E) * s.H)
+                             : nullptr;
 }
 
 template <typename T>
@@ -1140,9 +1229,20 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
           a.rt.topk_w, dw, a.rt.slot_row, Tn, k, w.dl, w.dl_perm);
       USAF_CHECK_LAUNCH();
       constexpr int FB = 32 * (16 / (int)sizeof(T));
-      g_router_sel_kernel<T><<<dim3((unsigned)ceil_div(H, FB), (unsigned)E), 256, 0, st>>>(
-          static_cast<const T*>(a.x), a.rt.perm_tok, w.dl_perm, cnt, off, H, g_router,
-          accumulate, dev_status);
+      if (a.dt == USAF_BF16) {
+        // token tiles of at most 256 rows: ceil(R_cap / 256) + E bounds their count
+        const unsigned ntile = (unsigned)(ceil_div(a.R_cap, TC_TOKEN_TILE) + E);
+        g_router_part_kernel<T><<<dim3((unsigned)ceil_div(H, FB), ntile), 256, 0, st>>>(
+            static_cast<const T*>(a.x), a.rt.perm_tok, w.dl_perm, cnt, off, w.plan, E, H,
+            w.g_part, g_router, accumulate, dev_status);
+        USAF_CHECK_LAUNCH();
+        g_router_reduce_kernel<<<grid_dim_for((int64_t)E * H), 256, 0, st>>>(
+            w.g_part, w.plan, E, H, g_router, accumulate, dev_status);
+      } else {
+        g_router_sel_kernel<T><<<dim3((unsigned)ceil_div(H, FB), (unsigned)E), 256, 0, st>>>(
+            static_cast<const T*>(a.x), a.rt.perm_tok, w.dl_perm, cnt, off, H, g_router,
+            accumulate, dev_status);
+      }
       USAF_CHECK_LAUNCH();
     } else {
       dlogit_dense_kernel<<<(unsigned)Tn, 128, 0, st>>>(logits, a.rt.topk_idx, a.rt.topk_w, dw,
