@@ -552,7 +552,30 @@ __device__ __forceinline__ int64_t count_below(const int64_t* __restrict__ act, 
 // A butterfly transpose of the SD_G per-lane partial sums then leaves entry i's total in lane i.
 constexpr int SD_WARPS = 8;
 constexpr int SD_BLOCKS_PER_SM = 4;
-constexpr int SD_G = 16;  // entries per group
+constexpr int SD_G = 16;    // entries per group
+constexpr int SD_RING = 6;  // entries whose vectors are in flight through a warp's ring
+constexpr int SD_RING_BYTES = SD_WARPS * SD_RING * 2 * 512;  // a slot: b vector, a vector
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+  const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(d), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+// wait until at most n of this thread's committed groups are pending (n a small constant after
+// unrolling)
+__device__ __forceinline__ void cp_async_wait_dyn(int n) {
+  switch (n) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+  }
+}
 template <typename T>
 __global__ void __launch_bounds__(SD_WARPS * 32, SD_BLOCKS_PER_SM) sddmm_kernel(
     const int64_t* __restrict__ act, int64_t K, const int32_t* __restrict__ cnt,
@@ -561,10 +584,10 @@ __global__ void __launch_bounds__(SD_WARPS * 32, SD_BLOCKS_PER_SM) sddmm_kernel(
     const T* __restrict__ waT, float* __restrict__ g_act, int accumulate, uint32_t* dev_status,
     const int32_t* __restrict__ dense_flag) {
   constexpr int VW = 16 / sizeof(T);
-  constexpr int U = 2;  // entries whose loads are in flight together in a full pass
   constexpr uint32_t FULL = 0xffffffffu;
   // per entry: a-row vector, b-row vector, vector count, last vector (0 when there is none)
   __shared__ int4 meta[SD_WARPS][32];
+  extern __shared__ __align__(16) uint8_t sd_ring[];  // SD_RING_BYTES
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, il = lane % SD_G;
   const int64_t kgu = count_below(act, K, Ngu, lane);
   const int64_t nb_gu = (kgu + 31) / 32, nb = nb_gu + (K - kgu + 31) / 32;
@@ -634,41 +657,33 @@ __global__ void __launch_bounds__(SD_WARPS * 32, SD_BLOCKS_PER_SM) sddmm_kernel(
 #pragma unroll
       for (int i = 0; i < SD_G; ++i) part[i] = 0.f;
       if (passes > 0) {
+        // Each entry's vectors come through a per-warp ring of SD_RING slots by cp.async, so the
+        // loads of the next SD_RING entries are in flight while one entry's products run (no
+        // registers are held for them). A lane copies, and reads back, only its own vector.
+        uint8_t* ring = sd_ring + (size_t)wid * SD_RING * 2 * 512 + lane * 16;
         RowVec<T> rowv;
+        for (uint32_t p = 0; p < passes; ++p) {
+          const uint32_t v = p * 32u + (uint32_t)lane;
+          auto issue = [&](int i) {
+            const int4 m = mh[i];
+            const uint32_t vv = filled ? v : min(v, (uint32_t)m.w);  // in bounds
+            uint8_t* slot = ring + (i % SD_RING) * 1024;
+            cp_async16(slot, Bm + ((uint32_t)m.y + vv));
+            if (fresh & (1u << i)) cp_async16(slot + 512, A + ((uint32_t)m.x + vv));
+            cp_async_commit();
+          };
 #pragma unroll
-        for (int i0 = 0; i0 < SD_G; i0 += U) {
-          for (uint32_t p = 0; p < passes; ++p) {
-            const uint32_t v = p * 32u + (uint32_t)lane;
-            uint4 av[U], bv[U];
-            if (filled) {
+          for (int i = 0; i < SD_RING; ++i) issue(i);
 #pragma unroll
-              for (int u = 0; u < U; ++u) {
-                const int4 m = mh[i0 + u];
-                if (fresh & (1u << (i0 + u))) av[u] = __ldg(A + ((uint32_t)m.x + v));
-                bv[u] = __ldg(Bm + ((uint32_t)m.y + v));
-              }
-#pragma unroll
-              for (int u = 0; u < U; ++u) {
-                if (fresh & (1u << (i0 + u))) rowv.set(av[u]);
-                part[i0 + u] = rowv.dot_acc(bv[u], part[i0 + u]);
-              }
-            } else {
-              uint32_t ok = 0;  // bit u: entry i0 + u has vector v
-#pragma unroll
-              for (int u = 0; u < U; ++u) {
-                const int4 m = mh[i0 + u];
-                ok |= (uint32_t)(v < (uint32_t)m.z) << u;
-                const uint32_t vv = min(v, (uint32_t)m.w);
-                if (fresh & (1u << (i0 + u))) av[u] = __ldg(A + ((uint32_t)m.x + vv));
-                bv[u] = __ldg(Bm + ((uint32_t)m.y + vv));
-              }
-#pragma unroll
-              for (int u = 0; u < U; ++u) {
-                if (fresh & (1u << (i0 + u))) rowv.set(av[u]);
-                const float d = rowv.dot_acc(bv[u], part[i0 + u]);
-                if (ok & (1u << u)) part[i0 + u] = d;
-              }
-            }
+          for (int i = 0; i < SD_G; ++i) {
+            // groups committed after entry i's: min(SD_G, i + SD_RING) - (i + 1)
+            cp_async_wait_dyn(min(SD_G, i + SD_RING) - (i + 1));
+            const uint8_t* slot = ring + (i % SD_RING) * 1024;
+            const uint4 bv = *reinterpret_cast<const uint4*>(slot);
+            if (fresh & (1u << i)) rowv.set(*reinterpret_cast<const uint4*>(slot + 512));
+            const float d = rowv.dot_acc(bv, part[i]);
+            if (filled || v < (uint32_t)mh[i].z) part[i] = d;
+            if (i + SD_RING < SD_G) issue(i + SD_RING);
           }
         }
       }
@@ -1281,7 +1296,14 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
       USAF_TRACE("wgrad_sddmm", st);
       const unsigned blocks = (unsigned)std::min<int64_t>(ceil_div(K, SD_WARPS * 32),
                                                           device_sm_count() * SD_BLOCKS_PER_SM);
-      sddmm_kernel<T><<<blocks, SD_WARPS * 32, 0, st>>>(
+      static bool ring_attr = false;  // the ring plus the static metadata exceed 48 KB
+      if (!ring_attr) {
+        if (cudaFuncSetAttribute(sddmm_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SD_RING_BYTES) != cudaSuccess)
+          return USAF_ERR_CUDA;
+        ring_attr = true;
+      }
+      sddmm_kernel<T><<<blocks, SD_WARPS * 32, SD_RING_BYTES, st>>>(
           act_idx, K, cnt, off, E, H, I, Ngu, a.R_cap, dhT, xT, dyT, waT, g_act, accumulate,
           dev_status, use_plan ? plan->dense_flag : nullptr);
       USAF_CHECK_LAUNCH();
