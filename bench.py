@@ -135,10 +135,10 @@ def kernel_units(cfg, sddmm_pairs=None):
 NCU_TRAFFIC = {
     "wgrad_sddmm": (452653568 + 14011904, "sparse_moe_fine_gb300/csrc/moe.cu",
                     "0f3dd5f8893a392c9b3c0e9ccf074ccab5753ac924ea76f716bcedc8857f1235"),
-    "tc_gate_up_swiglu": (945693696 + 139366144, "sparse_moe_fine_gb300/csrc/moe_tc.cu",
-                          "453c743e8e9281e3666d42b9251fba1d76ece5e5662ece45bdd94ad6bc2266b6"),
-    "tc_dx": (1056654848 + 139791360, "sparse_moe_fine_gb300/csrc/moe_tc.cu",
-              "453c743e8e9281e3666d42b9251fba1d76ece5e5662ece45bdd94ad6bc2266b6"),
+    "tc_gate_up_swiglu": (946807808 + 140072704, "sparse_moe_fine_gb300/csrc/moe_tc.cu",
+                          "09b3f6edd25128d85ed5df16d125b3f4c7f081890aea944cce53f1f7891ea79c"),
+    "tc_dx": (1122077000 + 156789504, "sparse_moe_fine_gb300/csrc/moe_tc.cu",
+              "09b3f6edd25128d85ed5df16d125b3f4c7f081890aea944cce53f1f7891ea79c"),
 }
 
 
