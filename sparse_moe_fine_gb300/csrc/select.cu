@@ -683,11 +683,13 @@ __device__ __forceinline__ int64_t lower_bound_i64(const int64_t* a, int64_t n, 
 // fall between act[s0] and act[s1] (block 0 also takes those below act[0], the last block those
 // above act[K-1]). A kept entry's new position is (kept entries before it) + (grown entries below
 // it); a grown entry's is (its index among the grown) + (kept entries below it). Inside the tile
-// the kept ranks come from a block scan and the searches run over the tile in shared memory or
-// over the tile's own range of the grown list, so no per-entry search crosses the whole set.
-constexpr int MG_TILE = 2048;
+// the kept ranks come from block scans over rounds of consecutive entries (thread t takes entries
+// t, t + MG_THREADS, ..., so the reads of p, m, v and the writes of the new set are coalesced),
+// and the searches run over the tile in shared memory or over the tile's own range of the grown
+// list, so no per-entry search crosses the whole set.
+constexpr int MG_TILE = 1024;
 constexpr int MG_THREADS = 256;
-constexpr int MG_GROWN = 2048;  // grown entries of a tile's range kept in shared memory
+constexpr int MG_GROWN = 1024;  // grown entries of a tile's range kept in shared memory
 template <typename W>
 __global__ void __launch_bounds__(MG_THREADS) rigl_merge_tile_kernel(
     const int64_t* __restrict__ act, int64_t K, const int64_t* __restrict__ dpos,
@@ -726,29 +728,26 @@ __global__ void __launch_bounds__(MG_THREADS) rigl_merge_tile_kernel(
     for (int64_t j = g0 + threadIdx.x; j < g1; j += MG_THREADS) sh_grown[j - g0] = grown[j];
   for (int64_t j = d0 + threadIdx.x; j < d1; j += MG_THREADS) sh_keep[dpos[j] - s0] = 0;
   __syncthreads();
-  // exclusive scan of the keep flags: thread t owns entries PER t .. PER t + PER - 1
-  uint32_t f[PER], mine = 0;
+  // exclusive ranks of the kept entries, in rounds of MG_THREADS consecutive entries (entry
+  // u MG_THREADS + t to thread t), so every global access below is coalesced
+  uint32_t f[PER];
+  uint32_t run = 0;
 #pragma unroll
   for (int u = 0; u < PER; ++u) {
-    const int i = threadIdx.x * PER + u;
+    const int i = u * MG_THREADS + threadIdx.x;
     f[u] = i < n ? sh_keep[i] : 0u;
-    mine += f[u];
+    uint32_t tot;
+    const uint32_t r = run + block_excl_scan(f[u], &tot);
+    if (i < n) sh_keep[i] = r;  // each thread rewrites only the entry it read
+    run += tot;
   }
-  uint32_t tot;
-  uint32_t run = block_excl_scan(mine, &tot);
-#pragma unroll
-  for (int u = 0; u < PER; ++u) {
-    const int i = threadIdx.x * PER + u;
-    if (i < n) sh_keep[i] = run;  // flags are in f[] now
-    run += f[u];
-  }
-  if (threadIdx.x == 0) sh_keep[n] = tot;
+  if (threadIdx.x == 0) sh_keep[n] = run;
   __syncthreads();
   const int64_t kept_before = s0 - d0;
   // kept entries
 #pragma unroll
   for (int u = 0; u < PER; ++u) {
-    const int i = threadIdx.x * PER + u;
+    const int i = u * MG_THREADS + threadIdx.x;
     if (i >= n || !f[u]) continue;
     const int64_t fi = sh_act[i];
     int64_t below;  // grown entries of the tile's range below fi
