@@ -25,11 +25,14 @@ constexpr int SAMPLE_S = 32768;
 // radix rounds over the 31-bit key, most significant digit first: bits 30..23, 22..15, 14..7, 6..0
 __host__ __device__ constexpr int round_shift(int r) { return r == 0 ? 23 : r == 1 ? 15 : r == 2 ? 7 : 0; }
 __host__ __device__ constexpr int round_bits(int r) { return r == 3 ? 7 : 8; }
-// the selection's own radix rounds: 8 bits (the exponent), then 12 and 11 bits
-constexpr int SEL_ROUNDS = 3;
-constexpr int MAX_BINS = 4096;
-__host__ __device__ constexpr int sel_shift(int r) { return r == 0 ? 23 : r == 1 ? 11 : 0; }
-__host__ __device__ constexpr int sel_bits(int r) { return r == 0 ? 8 : r == 1 ? 12 : 11; }
+// the selection's own radix rounds: 8 bits (the exponent), 8, 8 and 7 bits (256-bin histograms,
+// so each block adds at most 256 bins into the global one)
+constexpr int SEL_ROUNDS = 4;
+constexpr int MAX_BINS = 256;
+__host__ __device__ constexpr int sel_shift(int r) {
+  return r == 0 ? 23 : r == 1 ? 15 : r == 2 ? 7 : 0;
+}
+__host__ __device__ constexpr int sel_bits(int r) { return r == 3 ? 7 : 8; }
 
 struct SelCtrl {
   uint32_t tau0;
@@ -76,6 +79,7 @@ struct SelWs {
   uint32_t* blk_eq;
   uint32_t* base_gt;
   uint32_t* base_eq;
+  uint32_t* samples;  // [SAMPLE_S] sampled keys (sampled path)
 };
 
 SelPlan make_plan(int64_t N, int64_t K) {
@@ -119,6 +123,7 @@ void sel_layout(const SelPlan& p, Carver& c, SelWs& w) {
   w.blk_eq = c.take<uint32_t>(p.G);
   w.base_gt = c.take<uint32_t>(p.G);
   w.base_eq = c.take<uint32_t>(p.G);
+  w.samples = p.sampling ? c.take<uint32_t>(SAMPLE_S) : nullptr;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -253,13 +258,23 @@ __device__ __forceinline__ void pick_digit_warp(const uint32_t* hist, uint32_t* 
   }
 }
 
+// The SAMPLE_S strided samples of the keys (0 where excluded), read by 32 blocks: the random
+// reads of g spread over 32 SMs instead of queueing in one.
+constexpr int SAMPLE_BLOCKS = 32;
+__global__ void __launch_bounds__(SAMPLE_S / SAMPLE_BLOCKS) sel_sample_kernel(
+    const float* __restrict__ g, int64_t N, const uint32_t* __restrict__ excl,
+    uint32_t* __restrict__ samples) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  const int64_t pos = (int64_t)(((unsigned long long)i * (unsigned long long)N) / SAMPLE_S);
+  samples[i] = excluded(excl, pos) ? 0u : abs_key(g[pos]);
+}
+
 // Set-up and threshold of the sampled path in one block of 1024 threads: the control block and
-// the region counts are cleared (as sel_init_kernel does), each thread reads 32 strided samples
-// of the keys straight from g (0 where excluded), and the q-th largest sample (1-based) is found
-// by 4 digit rounds over per-warp shared histograms; tau0 := that key.
+// the region counts are cleared (as sel_init_kernel does), each thread takes 32 of the samples,
+// and the top 16 bits of the q-th largest sample (1-based) are found by 2 digit rounds over
+// per-warp shared histograms; tau0 := those bits (the lower edge of the sample quantile's bin).
 __global__ void __launch_bounds__(1024) sel_sample_tau_kernel(
-    const float* __restrict__ g, int64_t N, const uint32_t* __restrict__ excl, int q, SelCtrl* c,
-    int64_t K, uint32_t* ccnt, int G) {
+    const uint32_t* __restrict__ samples, int q, SelCtrl* c, int64_t K, uint32_t* ccnt, int G) {
   constexpr int PER = SAMPLE_S / 1024;
   __shared__ uint32_t wh[32][257];
   __shared__ uint32_t hist[256];
@@ -267,11 +282,7 @@ __global__ void __launch_bounds__(1024) sel_sample_tau_kernel(
   const int wid = threadIdx.x >> 5;
   uint32_t key[PER];
 #pragma unroll
-  for (int j = 0; j < PER; ++j) {
-    const int i = j * 1024 + threadIdx.x;
-    const int64_t pos = (int64_t)(((unsigned long long)i * (unsigned long long)N) / SAMPLE_S);
-    key[j] = excluded(excl, pos) ? 0u : abs_key(g[pos]);
-  }
+  for (int j = 0; j < PER; ++j) key[j] = samples[j * 1024 + threadIdx.x];
   for (int i = threadIdx.x; i < MAX_BINS; i += blockDim.x) c->hist[i] = 0;
   for (int i = threadIdx.x; i < G; i += blockDim.x) ccnt[i] = 0;
   if (threadIdx.x == 0) {
@@ -287,7 +298,9 @@ __global__ void __launch_bounds__(1024) sel_sample_tau_kernel(
     s_prefix = 0;
     s_krem = (uint32_t)q;
   }
-  for (int r = 0; r < 4; ++r) {
+  // the top 16 bits of the q-th largest sample: tau0 is the lower edge of its 2^15-wide bin, a
+  // little below the sample quantile, so the candidates only gain the keys of that bin
+  for (int r = 0; r < 2; ++r) {
     const int shift = round_shift(r), bits = round_bits(r);
     const uint32_t dmask = (1u << bits) - 1;
     for (int i = threadIdx.x; i < 32 * 257; i += blockDim.x) (&wh[0][0])[i] = 0;
@@ -580,6 +593,79 @@ __global__ void __launch_bounds__(SEL_THREADS) sel_write_kernel(Src s, const Sel
   });
 }
 
+// The same count and ordered write with one warp per region (the sampled path, where a region
+// holds about a thousand candidates): ranks come from ballots, so no block barrier is needed.
+// Mode 0 (a region overflowed, the whole array) walks the region's elements 128 at a time.
+template <typename F>
+__device__ __forceinline__ void for_region_warp(const Src& s, int mode, int b, int lane, F f) {
+  if (mode == 1) {
+    const int64_t n = s.ccnt[b];
+    const uint32_t* kk = s.ckeys + (int64_t)b * s.cap;
+    const uint32_t* ii = s.cids + (int64_t)b * s.cap;
+    for (int64_t j0 = 0; j0 < n; j0 += 32) {
+      const int64_t j = j0 + lane;
+      const bool ok = j < n;
+      f(ok ? kk[j] : 0u, ok ? s.base + (int64_t)ii[j] : 0, ok);
+    }
+  } else {
+    const int64_t lo = (int64_t)b * s.L;
+    const int64_t hi = min(s.n, lo + s.L);
+    for (int64_t i0 = lo; i0 < hi; i0 += 128) {
+      uint32_t key[4];
+      bool ok[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int64_t i = i0 + u * 32 + lane;
+        ok[u] = i < hi && !(mode == 0 && excluded(s.excl, i));
+        key[u] = ok[u] ? src_key(s, i) : 0u;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) f(key[u], s.base + i0 + u * 32 + lane, ok[u]);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) sel_count_warp_kernel(Src s, const SelCtrl* c,
+                                                            uint32_t* blk_gt, uint32_t* blk_eq) {
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (b >= s.G) return;
+  const int mode = (int)c->mode;
+  const uint32_t tau = c->prefix;
+  uint32_t gt = 0, eq = 0;
+  for_region_warp(s, mode, b, lane, [&](uint32_t key, int64_t, bool ok) {
+    gt += __popc(__ballot_sync(0xffffffffu, ok && key > tau));
+    eq += __popc(__ballot_sync(0xffffffffu, ok && key == tau));
+  });
+  if (lane == 0) {
+    blk_gt[b] = gt;
+    blk_eq[b] = eq;
+  }
+}
+
+__global__ void __launch_bounds__(256) sel_write_warp_kernel(Src s, const SelCtrl* c,
+                                                            const uint32_t* base_gt,
+                                                            const uint32_t* base_eq,
+                                                            int64_t* __restrict__ out) {
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (b >= s.G) return;
+  const int mode = (int)c->mode;
+  const uint32_t tau = c->prefix;
+  const uint32_t need = c->k_rem;
+  const uint32_t below = (1u << lane) - 1u;
+  uint32_t gt_run = base_gt[b], eq_run = base_eq[b];
+  for_region_warp(s, mode, b, lane, [&](uint32_t key, int64_t id, bool ok) {
+    const bool isgt = ok && key > tau, iseq = ok && key == tau;
+    const uint32_t mg = __ballot_sync(0xffffffffu, isgt);
+    const uint32_t me = __ballot_sync(0xffffffffu, iseq);
+    const uint32_t pg = gt_run + __popc(mg & below), pe = eq_run + __popc(me & below);
+    if (isgt || (iseq && pe < need)) out[pg + min(pe, need)] = id;
+    gt_run += __popc(mg);
+    eq_run += __popc(me);
+  });
+}
+
 __global__ void bitmap_zero_kernel(uint32_t* bm, int64_t words) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < words;
        i += (int64_t)gridDim.x * blockDim.x)
@@ -602,13 +688,39 @@ __global__ void bitmap_set_kernel(const int64_t* __restrict__ idx, int64_t K, in
   flag_status_warp(dev_status, bad, USAF_DEV_BAD_INDEX);
 }
 
+// Count, scan and ordered write of the selected entries: one warp per region on the sampled
+// path (the mode taken on the device), one block per region otherwise.
+usaf_status ordered_write(const SelPlan& p, const SelWs& w, const Src& s, int64_t* out, int fm,
+                          bool warp_regions, cudaStream_t st) {
+  if (warp_regions) {
+    const unsigned nb = (unsigned)ceil_div(p.G, 8);
+    sel_count_warp_kernel<<<nb, 256, 0, st>>>(s, w.ctrl, w.blk_gt, w.blk_eq);
+    USAF_CHECK_LAUNCH();
+    sel_scan_kernel<<<1, 1024, 0, st>>>(w.blk_gt, w.blk_eq, p.G, w.base_gt, w.base_eq);
+    USAF_CHECK_LAUNCH();
+    sel_write_warp_kernel<<<nb, 256, 0, st>>>(s, w.ctrl, w.base_gt, w.base_eq, out);
+    USAF_CHECK_LAUNCH();
+    return USAF_OK;
+  }
+  sel_count_kernel<<<p.G, SEL_THREADS, 0, st>>>(s, w.ctrl, w.blk_gt, w.blk_eq, fm);
+  USAF_CHECK_LAUNCH();
+  sel_scan_kernel<<<1, 1024, 0, st>>>(w.blk_gt, w.blk_eq, p.G, w.base_gt, w.base_eq);
+  USAF_CHECK_LAUNCH();
+  sel_write_kernel<<<p.G, SEL_THREADS, 0, st>>>(s, w.ctrl, w.base_gt, w.base_eq, out, fm);
+  USAF_CHECK_LAUNCH();
+  return USAF_OK;
+}
+
 // The fixed sequence of launches that selects the top-K of `s` (see file comment).
 usaf_status run_select(const SelPlan& p, const SelWs& w, Src s, int64_t K, int64_t* out,
                        uint32_t* dev_status, bool fixed_drop, cudaStream_t st) {
   if (p.sampling && !fixed_drop) {
     {
       USAF_TRACE("select_sample", st);
-      sel_sample_tau_kernel<<<1, 1024, 0, st>>>(s.g, s.n, s.excl, p.q, w.ctrl, K, w.ccnt, p.G);
+      sel_sample_kernel<<<SAMPLE_BLOCKS, SAMPLE_S / SAMPLE_BLOCKS, 0, st>>>(s.g, s.n, s.excl,
+                                                                             w.samples);
+      USAF_CHECK_LAUNCH();
+      sel_sample_tau_kernel<<<1, 1024, 0, st>>>(w.samples, p.q, w.ctrl, K, w.ccnt, p.G);
       USAF_CHECK_LAUNCH();
     }
     USAF_TRACE("select_compact", st);
@@ -638,13 +750,7 @@ usaf_status run_select(const SelPlan& p, const SelWs& w, Src s, int64_t K, int64
     }
   }
   USAF_TRACE("select_write", st);
-  sel_count_kernel<<<p.G, SEL_THREADS, 0, st>>>(s, w.ctrl, w.blk_gt, w.blk_eq, fm);
-  USAF_CHECK_LAUNCH();
-  sel_scan_kernel<<<1, 1024, 0, st>>>(w.blk_gt, w.blk_eq, p.G, w.base_gt, w.base_eq);
-  USAF_CHECK_LAUNCH();
-  sel_write_kernel<<<p.G, SEL_THREADS, 0, st>>>(s, w.ctrl, w.base_gt, w.base_eq, out, fm);
-  USAF_CHECK_LAUNCH();
-  return USAF_OK;
+  return ordered_write(p, w, s, out, fm, p.sampling && !fixed_drop, st);
 }
 
 // Entries of the sorted a[0, n) below key, found by one warp with 32 probes per step (about four
@@ -1149,13 +1255,7 @@ usaf_status shard_emit_launch(const float* g, int64_t n, const uint32_t* excl, u
     s.cap = p.cap;
     fm = -1;
   }
-  sel_count_kernel<<<p.G, SEL_THREADS, 0, st>>>(s, w.ctrl, w.blk_gt, w.blk_eq, fm);
-  USAF_CHECK_LAUNCH();
-  sel_scan_kernel<<<1, 1024, 0, st>>>(w.blk_gt, w.blk_eq, p.G, w.base_gt, w.base_eq);
-  USAF_CHECK_LAUNCH();
-  sel_write_kernel<<<p.G, SEL_THREADS, 0, st>>>(s, w.ctrl, w.base_gt, w.base_eq, out, fm);
-  USAF_CHECK_LAUNCH();
-  return USAF_OK;
+  return ordered_write(p, w, s, out, fm, p.sampling, st);
 }
 
 usaf_status bitmap_range_launch(const int64_t* idx, int64_t K, int64_t lo, int64_t n,
