@@ -576,7 +576,7 @@ __device__ __forceinline__ void cp_async_wait_dyn(int n) {
     default: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
   }
 }
-template <typename T>
+template <typename T, bool RING>
 __global__ void __launch_bounds__(SD_WARPS * 32, SD_BLOCKS_PER_SM) sddmm_kernel(
     const int64_t* __restrict__ act, int64_t K, const int32_t* __restrict__ cnt,
     const int32_t* __restrict__ off, int E, int H, int I, int64_t Ngu, int64_t rcap,
@@ -656,34 +656,77 @@ __global__ void __launch_bounds__(SD_WARPS * 32, SD_BLOCKS_PER_SM) sddmm_kernel(
       float part[SD_G];
 #pragma unroll
       for (int i = 0; i < SD_G; ++i) part[i] = 0.f;
-      if (passes > 0) {
-        // Each entry's vectors come through a per-warp ring of SD_RING slots by cp.async, so the
-        // loads of the next SD_RING entries are in flight while one entry's products run (no
-        // registers are held for them). A lane copies, and reads back, only its own vector.
-        uint8_t* ring = sd_ring + (size_t)wid * SD_RING * 2 * 512 + lane * 16;
+      if constexpr (RING) {
+        if (passes > 0) {
+          // Each entry's vectors come through a per-warp ring of SD_RING slots by cp.async, so
+          // the loads of the next SD_RING entries are in flight while one entry's products run
+          // (no registers are held for them). A lane copies, and reads back, only its own vector.
+          uint8_t* ring = sd_ring + (size_t)wid * SD_RING * 2 * 512 + lane * 16;
+          RowVec<T> rowv;
+          for (uint32_t p = 0; p < passes; ++p) {
+            const uint32_t v = p * 32u + (uint32_t)lane;
+            auto issue = [&](int i) {
+              const int4 m = mh[i];
+              const uint32_t vv = filled ? v : min(v, (uint32_t)m.w);  // in bounds
+              uint8_t* slot = ring + (i % SD_RING) * 1024;
+              cp_async16(slot, Bm + ((uint32_t)m.y + vv));
+              if (fresh & (1u << i)) cp_async16(slot + 512, A + ((uint32_t)m.x + vv));
+              cp_async_commit();
+            };
+#pragma unroll
+            for (int i = 0; i < SD_RING; ++i) issue(i);
+#pragma unroll
+            for (int i = 0; i < SD_G; ++i) {
+              // groups committed after entry i's: min(SD_G, i + SD_RING) - (i + 1)
+              cp_async_wait_dyn(min(SD_G, i + SD_RING) - (i + 1));
+              const uint8_t* slot = ring + (i % SD_RING) * 1024;
+              const uint4 bv = *reinterpret_cast<const uint4*>(slot);
+              if (fresh & (1u << i)) rowv.set(*reinterpret_cast<const uint4*>(slot + 512));
+              const float d = rowv.dot_acc(bv, part[i]);
+              if (filled || v < (uint32_t)mh[i].z) part[i] = d;
+              if (i + SD_RING < SD_G) issue(i + SD_RING);
+            }
+          }
+        }
+      } else if (passes > 0) {
+        // Long rows (thousands of tokens per expert): the walk takes U entries at a time through
+        // all their passes, their loads in flight together (registers).
+        constexpr int U = 2;
         RowVec<T> rowv;
-        for (uint32_t p = 0; p < passes; ++p) {
-          const uint32_t v = p * 32u + (uint32_t)lane;
-          auto issue = [&](int i) {
-            const int4 m = mh[i];
-            const uint32_t vv = filled ? v : min(v, (uint32_t)m.w);  // in bounds
-            uint8_t* slot = ring + (i % SD_RING) * 1024;
-            cp_async16(slot, Bm + ((uint32_t)m.y + vv));
-            if (fresh & (1u << i)) cp_async16(slot + 512, A + ((uint32_t)m.x + vv));
-            cp_async_commit();
-          };
 #pragma unroll
-          for (int i = 0; i < SD_RING; ++i) issue(i);
+        for (int i0 = 0; i0 < SD_G; i0 += U) {
+          for (uint32_t p = 0; p < passes; ++p) {
+            const uint32_t v = p * 32u + (uint32_t)lane;
+            uint4 av[U], bv[U];
+            if (filled) {
 #pragma unroll
-          for (int i = 0; i < SD_G; ++i) {
-            // groups committed after entry i's: min(SD_G, i + SD_RING) - (i + 1)
-            cp_async_wait_dyn(min(SD_G, i + SD_RING) - (i + 1));
-            const uint8_t* slot = ring + (i % SD_RING) * 1024;
-            const uint4 bv = *reinterpret_cast<const uint4*>(slot);
-            if (fresh & (1u << i)) rowv.set(*reinterpret_cast<const uint4*>(slot + 512));
-            const float d = rowv.dot_acc(bv, part[i]);
-            if (filled || v < (uint32_t)mh[i].z) part[i] = d;
-            if (i + SD_RING < SD_G) issue(i + SD_RING);
+              for (int u = 0; u < U; ++u) {
+                const int4 m = mh[i0 + u];
+                if (fresh & (1u << (i0 + u))) av[u] = __ldg(A + ((uint32_t)m.x + v));
+                bv[u] = __ldg(Bm + ((uint32_t)m.y + v));
+              }
+#pragma unroll
+              for (int u = 0; u < U; ++u) {
+                if (fresh & (1u << (i0 + u))) rowv.set(av[u]);
+                part[i0 + u] = rowv.dot_acc(bv[u], part[i0 + u]);
+              }
+            } else {
+              uint32_t ok = 0;  // bit u: entry i0 + u has vector v
+#pragma unroll
+              for (int u = 0; u < U; ++u) {
+                const int4 m = mh[i0 + u];
+                ok |= (uint32_t)(v < (uint32_t)m.z) << u;
+                const uint32_t vv = min(v, (uint32_t)m.w);
+                if (fresh & (1u << (i0 + u))) av[u] = __ldg(A + ((uint32_t)m.x + vv));
+                bv[u] = __ldg(Bm + ((uint32_t)m.y + vv));
+              }
+#pragma unroll
+              for (int u = 0; u < U; ++u) {
+                if (fresh & (1u << (i0 + u))) rowv.set(av[u]);
+                const float d = rowv.dot_acc(bv[u], part[i0 + u]);
+                if (ok & (1u << u)) part[i0 + u] = d;
+              }
+            }
           }
         }
       }
@@ -1296,16 +1339,26 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
       USAF_TRACE("wgrad_sddmm", st);
       const unsigned blocks = (unsigned)std::min<int64_t>(ceil_div(K, SD_WARPS * 32),
                                                           device_sm_count() * SD_BLOCKS_PER_SM);
-      static bool ring_attr = false;  // the ring plus the static metadata exceed 48 KB
-      if (!ring_attr) {
-        if (cudaFuncSetAttribute(sddmm_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SD_RING_BYTES) != cudaSuccess)
-          return USAF_ERR_CUDA;
-        ring_attr = true;
+      // the cp.async ring where experts hold up to about a thousand routed rows on average;
+      // the register walk where rows run to thousands of tokens (there the ring's restart per
+      // 256-token pass costs more than it hides)
+      if ((int64_t)s.T * s.k <= (int64_t)1024 * E) {
+        static bool ring_attr = false;  // the ring plus the static metadata exceed 48 KB
+        if (!ring_attr) {
+          if (cudaFuncSetAttribute(sddmm_kernel<T, true>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   SD_RING_BYTES) != cudaSuccess)
+            return USAF_ERR_CUDA;
+          ring_attr = true;
+        }
+        sddmm_kernel<T, true><<<blocks, SD_WARPS * 32, SD_RING_BYTES, st>>>(
+            act_idx, K, cnt, off, E, H, I, Ngu, a.R_cap, dhT, xT, dyT, waT, g_act, accumulate,
+            dev_status, use_plan ? plan->dense_flag : nullptr);
+      } else {
+        sddmm_kernel<T, false><<<blocks, SD_WARPS * 32, 0, st>>>(
+            act_idx, K, cnt, off, E, H, I, Ngu, a.R_cap, dhT, xT, dyT, waT, g_act, accumulate,
+            dev_status, use_plan ? plan->dense_flag : nullptr);
       }
-      sddmm_kernel<T><<<blocks, SD_WARPS * 32, SD_RING_BYTES, st>>>(
-          act_idx, K, cnt, off, E, H, I, Ngu, a.R_cap, dhT, xT, dyT, waT, g_act, accumulate,
-          dev_status, use_plan ? plan->dense_flag : nullptr);
       USAF_CHECK_LAUNCH();
     }
     if (use_plan) {
