@@ -379,6 +379,19 @@ def run(args):
     ev[1].record()
     torch.cuda.synchronize()
     rigl_ms = ev[0].elapsed_time(ev[1]) / reps
+    # both from one pass over g: the top-K of |g| and the RigL swap of the current set
+    sel2 = torch.empty(cfg.K, dtype=torch.int64, device=dev)
+    ws_fused = torch.empty(B.select_and_swap_workspace_size(cfg.N, cfg.K, cfg.K, D),
+                           dtype=torch.uint8, device=dev)
+    fused = lambda: B.select_and_swap(g_dense, sel2, act, D, layer.p, layer.m, layer.v, wgu,
+                                      cfg.N_gu, wd, *outs, ns, dev_status=st, ws=ws_fused)
+    fused()
+    ev[0].record()
+    for _ in range(reps):
+        fused()
+    ev[1].record()
+    torch.cuda.synchronize()
+    fused_ms = ev[0].elapsed_time(ev[1]) / reps
     # dense gradient pass of the importance phase: one micro-batch's dense expert gradient added
     # into the accumulated g (route, forward, dense backward)
     st_d = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -421,13 +434,22 @@ def run(args):
     rigl()
     torch.cuda.synchronize()
     rigl_stages = {n: 1e3 * t for n, c, t in B.trace_summary()}
+    B.trace_enable(True)
+    fused()
+    torch.cuda.synchronize()
+    fused_stages = {n: 1e3 * t for n, c, t in B.trace_summary()}
     B.trace_enable(False)
-    del ws_rigl, ws_sel, outs, ws_res
+    del ws_rigl, ws_sel, outs, ws_res, ws_fused, sel2
     g_bytes = cfg.N * 4
     importance = {
         "select_ms": sel_ms, "select_gbs": g_bytes / sel_ms / 1e6,
         "select_frac": g_bytes / sel_ms / 1e6 / hbm,
         "rigl_ms": rigl_ms, "rigl_gbs": (g_bytes + cfg.N / 8 + cfg.K * 40) / rigl_ms / 1e6,
+        "rigl_frac": (g_bytes + cfg.N / 8 + cfg.K * 40) / rigl_ms / 1e6 / hbm,
+        # one read of g for both: its bytes as RigL's plus the K selected indices written
+        "select_and_swap_ms": fused_ms, "separate_select_plus_swap_ms": sel_ms + rigl_ms,
+        "select_and_swap_frac": (g_bytes + cfg.N / 8 + cfg.K * 48) / fused_ms / 1e6 / hbm,
+        "select_and_swap_stages_us": fused_stages,
         "reselect_full_ms": resel_ms, "reselect_full_kept": int(nk.item()),
         "dense_grad_bwd_ms": dense_ms,
         "select_exact_path": bool(int(st.item()) & B.DEV_SELECT_EXACT_PATH),

@@ -378,6 +378,29 @@ usaf_status usaf_rigl_swap(const float* g, int64_t N, const int64_t* act_idx, in
                            size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * usaf_select_and_swap - the importance selection and the RigL swap of one dense gradient from
+ * one pass over g (USAF README, "Not all weights matter" and "Sparsity adapts"): sel_idx gets
+ * exactly what usaf_importance_select(g, N, K_sel) writes, and new_idx, p_out, m_out, v_out and
+ * n_swapped exactly what usaf_rigl_swap(g, N, act_idx, K, D, ...) writes. Both selections are
+ * found among one set of candidates compacted in a single read of g; where either selection would
+ * not take the sampled path (small N, K_sel or D a large part of N, D = 0), the call runs the two
+ * selections one after the other instead (same results).
+ *   g          [N] fp32 dense gradient
+ *   sel_idx    [K_sel] int64 out, sorted ascending; must not overlap the other outputs or inputs
+ *   the rest   as for usaf_rigl_swap
+ * Limits: 1 <= K_sel <= N; 0 <= D <= K, D <= N - K; N < 2^32.
+ * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
+ * ------------------------------------------------------------------------------------------- */
+size_t usaf_select_and_swap_workspace_size(int64_t N, int64_t K_sel, int64_t K, int64_t D);
+usaf_status usaf_select_and_swap(const float* g, int64_t N, int64_t K_sel, int64_t* sel_idx,
+                                 const int64_t* act_idx, int64_t K, int64_t D, const float* p_in,
+                                 const float* m_in, const float* v_in, const void* w_seg0,
+                                 int64_t n_seg0, const void* w_seg1, usaf_dtype w_dtype,
+                                 int64_t* new_idx, float* p_out, float* m_out, float* v_out,
+                                 int64_t* n_swapped, uint32_t* dev_status, void* ws,
+                                 size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
  * usaf_reselect_full - reselection by re-ranking (USAF README, "Sparsity adapts": the active set
  * is chosen again from fresh gradient magnitudes, with the large turnover the README reports at
  * the first reselections): new_idx = the K entries with the largest |g| (ties: lower flat index

@@ -79,6 +79,9 @@ _SIGS = {
     "usaf_trace_summary": (_INT, [_P, _INT]),
     "usaf_rigl_swap": (_INT, [_P, _I64, _P, _I64, _I64, _P, _P, _P, _P, _I64, _P, _INT, _P, _P, _P,
                               _P, _P, _P, _P, _SZ, _P]),
+    "usaf_select_and_swap_workspace_size": (_SZ, [_I64, _I64, _I64, _I64]),
+    "usaf_select_and_swap": (_INT, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P, _P, _P, _I64, _P,
+                                    _INT, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "usaf_moe_bwd_sparse_accumulate": (_INT, [_P, _INT, _INT, _P, _P, _P, _P, _P, _P, _P, _P,
                                               _P, _P, _P, _I64, _P, _P, _P, _P, _P, _P, _SZ,
                                               _P]),
@@ -377,6 +380,24 @@ def rigl_swap(g, act_idx, D, p_in, m_in, v_in, w_seg0, n_seg0, w_seg1, new_idx, 
         _ptr(g), N, _ptr(act_idx), K, int(D), _ptr(p_in), _ptr(m_in), _ptr(v_in), _ptr(w_seg0),
         int(n_seg0), _ptr(w_seg1), _dt(w_seg0), _ptr(new_idx), _ptr(p_out), _ptr(m_out),
         _ptr(v_out), _ptr(n_swapped), _ptr(dev_status), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+def select_and_swap_workspace_size(N: int, K_sel: int, K: int, D: int) -> int:
+    return int(lib().usaf_select_and_swap_workspace_size(int(N), int(K_sel), int(K), int(D)))
+
+
+def select_and_swap(g, sel_idx, act_idx, D, p_in, m_in, v_in, w_seg0, n_seg0, w_seg1, new_idx,
+                    p_out, m_out, v_out, n_swapped, dev_status=None, ws=None, stream=None):
+    """usaf_select_and_swap: importance_select into sel_idx (K_sel = its length) and rigl_swap of
+    act_idx, from one pass over g."""
+    N, K, K_sel = g.numel(), act_idx.numel(), sel_idx.numel()
+    if ws is None:
+        ws = _ws(select_and_swap_workspace_size(N, K_sel, K, D), g.device)
+    _check("usaf_select_and_swap", lib().usaf_select_and_swap(
+        _ptr(g), N, K_sel, _ptr(sel_idx), _ptr(act_idx), K, int(D), _ptr(p_in), _ptr(m_in),
+        _ptr(v_in), _ptr(w_seg0), int(n_seg0), _ptr(w_seg1), _dt(w_seg0), _ptr(new_idx),
+        _ptr(p_out), _ptr(m_out), _ptr(v_out), _ptr(n_swapped), _ptr(dev_status), _ptr(ws),
+        ws.numel(), _stream(stream)))
 
 
 def reselect_full_workspace_size(N: int, K: int) -> int:

@@ -491,6 +491,44 @@ usaf_status usaf_rigl_swap(const float* g, int64_t N, const int64_t* act_idx, in
                      static_cast<cudaStream_t>(stream));
 }
 
+size_t usaf_select_and_swap_workspace_size(int64_t N, int64_t K_sel, int64_t K, int64_t D) {
+  if (usaf_rigl_swap_workspace_size(N, K, D) == 0 || K_sel < 1 || K_sel > N) return 0;
+  return select_and_swap_ws_bytes(N, K_sel, K, D);
+}
+
+usaf_status usaf_select_and_swap(const float* g, int64_t N, int64_t K_sel, int64_t* sel_idx,
+                                 const int64_t* act_idx, int64_t K, int64_t D, const float* p_in,
+                                 const float* m_in, const float* v_in, const void* w_seg0,
+                                 int64_t n_seg0, const void* w_seg1, usaf_dtype w_dtype,
+                                 int64_t* new_idx, float* p_out, float* m_out, float* v_out,
+                                 int64_t* n_swapped, uint32_t* dev_status, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  if (!g || N < 1 || K < 0 || K > N || D < 0 || D > K || D > N - K || !n_swapped)
+    return USAF_ERR_INVALID_ARG;
+  if (K_sel < 1 || K_sel > N || !sel_idx) return USAF_ERR_INVALID_ARG;
+  if (!dtype_ok(w_dtype) || n_seg0 < 0) return USAF_ERR_INVALID_ARG;
+  if (K > 0 && (!act_idx || !p_in || !m_in || !v_in || !new_idx || !p_out || !m_out || !v_out))
+    return USAF_ERR_INVALID_ARG;
+  if (D > 0 && (!w_seg0 || (N > n_seg0 && !w_seg1))) return USAF_ERR_INVALID_ARG;
+  if (N >= (int64_t(1) << 32)) return USAF_ERR_UNSUPPORTED;
+  const size_t kb = size_t(K) * 4;
+  const void* ins[5] = {p_in, m_in, v_in, act_idx, g};
+  const size_t insz[5] = {kb, kb, kb, size_t(K) * 8, size_t(N) * 4};
+  const void* outs[5] = {p_out, m_out, v_out, new_idx, sel_idx};
+  const size_t outsz[5] = {kb, kb, kb, size_t(K) * 8, size_t(K_sel) * 8};
+  for (int i = 0; i < 5; ++i)
+    for (int j = 0; j < 5; ++j)
+      if (overlaps(ins[i], insz[i], outs[j], outsz[j])) return USAF_ERR_INVALID_ARG;
+  for (int j = 0; j < 4; ++j)
+    if (overlaps(sel_idx, size_t(K_sel) * 8, outs[j], outsz[j])) return USAF_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < usaf_select_and_swap_workspace_size(N, K_sel, K, D))
+    return USAF_ERR_WORKSPACE;
+  USAF_TRY(debug_validate(act_idx, K, N, dev_status, stream));
+  return select_and_swap_launch(g, N, K_sel, sel_idx, act_idx, K, D, p_in, m_in, v_in, w_seg0,
+                                n_seg0, w_seg1, w_dtype, new_idx, p_out, m_out, v_out, n_swapped,
+                                dev_status, ws, static_cast<cudaStream_t>(stream));
+}
+
 size_t usaf_reselect_full_workspace_size(int64_t N, int64_t K) {
   if (N < 1 || K < 0 || K > N || N >= (int64_t(1) << 32)) return 0;
   return reselect_ws_bytes(N, K);

@@ -156,6 +156,14 @@ usaf_status rigl_launch(const float* g, int64_t N, const int64_t* act_idx, int64
                         float* p_out, float* m_out, float* v_out, int64_t* n_swapped,
                         uint32_t* dev_status, void* ws, cudaStream_t st,
                         const int64_t* grown_in = nullptr);
+size_t select_and_swap_ws_bytes(int64_t N, int64_t Ksel, int64_t K, int64_t D);
+usaf_status select_and_swap_launch(const float* g, int64_t N, int64_t Ksel, int64_t* sel_idx,
+                                   const int64_t* act_idx, int64_t K, int64_t D,
+                                   const float* p_in, const float* m_in, const float* v_in,
+                                   const void* w0, int64_t n0, const void* w1, usaf_dtype wdt,
+                                   int64_t* new_idx, float* p_out, float* m_out, float* v_out,
+                                   int64_t* n_swapped, uint32_t* dev_status, void* ws,
+                                   cudaStream_t st);
 usaf_status reselect_carry_launch(const int64_t* new_idx, int64_t K, int64_t N,
                                   const int64_t* old_idx, int64_t K_old, const float* p_in,
                                   const float* m_in, const float* v_in, const void* w0, int64_t n0,

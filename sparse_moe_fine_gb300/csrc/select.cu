@@ -58,6 +58,8 @@ struct Src {
   const uint32_t* ccnt;
   int64_t cap;
   int drop;                // 1: keys are complemented |p| (mode 2 source)
+  int skip_tagged;         // mode 1: candidates whose key carries bit 31 (an excluded entry of a
+                           // shared candidate set) are not part of this selection
   int G;                   // parts (regions)
   int64_t base;            // modes 0, 2: added to the element index an ordered write emits
 };
@@ -175,8 +177,9 @@ __device__ __forceinline__ void for_part(const Src& s, int mode, int b, F f) {
     const uint32_t* ii = s.cids + (int64_t)b * s.cap;
     for (int64_t j0 = 0; j0 < n; j0 += blockDim.x) {
       const int64_t j = j0 + threadIdx.x;
-      const bool ok = j < n;
-      f(ok ? kk[j] : 0u, ok ? s.base + (int64_t)ii[j] : 0, ok);
+      const uint32_t kj = j < n ? kk[j] : 0u;
+      const bool ok = j < n && !(s.skip_tagged && (kj >> 31));
+      f(kj & 0x7FFFFFFFu, ok ? s.base + (int64_t)ii[j] : 0, ok);
     }
   } else {
     const int64_t lo = (int64_t)b * s.L;
@@ -259,32 +262,50 @@ __device__ __forceinline__ void pick_digit_warp(const uint32_t* hist, uint32_t* 
 }
 
 // The SAMPLE_S strided samples of the keys (0 where excluded), read by 32 blocks: the random
-// reads of g spread over 32 SMs instead of queueing in one.
+// reads of g spread over 32 SMs instead of queueing in one. With samples_all (two selections
+// sharing one pass), the same positions' keys are also written there without the exclusion.
 constexpr int SAMPLE_BLOCKS = 32;
 __global__ void __launch_bounds__(SAMPLE_S / SAMPLE_BLOCKS) sel_sample_kernel(
     const float* __restrict__ g, int64_t N, const uint32_t* __restrict__ excl,
-    uint32_t* __restrict__ samples) {
+    uint32_t* __restrict__ samples, uint32_t* __restrict__ samples_all) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   const int64_t pos = (int64_t)(((unsigned long long)i * (unsigned long long)N) / SAMPLE_S);
-  samples[i] = excluded(excl, pos) ? 0u : abs_key(g[pos]);
+  const uint32_t k = abs_key(g[pos]);
+  samples[i] = excluded(excl, pos) ? 0u : k;
+  if (samples_all) samples_all[i] = k;
 }
 
-// Set-up and threshold of the sampled path in one block of 1024 threads: the control block and
-// the region counts are cleared (as sel_init_kernel does), each thread takes 32 of the samples,
-// and the top 16 bits of the q-th largest sample (1-based) are found by 2 digit rounds over
-// per-warp shared histograms; tau0 := those bits (the lower edge of the sample quantile's bin).
-__global__ void __launch_bounds__(1024) sel_sample_tau_kernel(
-    const uint32_t* __restrict__ samples, int q, SelCtrl* c, int64_t K, uint32_t* ccnt, int G) {
+// One selection's threshold job: its samples, sample rank, control block and K.
+struct TauJob {
+  const uint32_t* samples;
+  int q;
+  SelCtrl* c;
+  int64_t K;
+};
+
+// Set-up and threshold of the sampled path, one block of 1024 threads per selection (block b
+// takes job b): the control block and (block 0) the region counts are cleared (as sel_init_kernel
+// does), each thread takes 32 of the samples, and the top 16 bits of the q-th largest sample
+// (1-based) are found by 2 digit rounds over per-warp shared histograms; tau0 := those bits (the
+// lower edge of the sample quantile's bin).
+__global__ void __launch_bounds__(1024) sel_sample_tau_kernel(TauJob j0, TauJob j1,
+                                                              uint32_t* ccnt, int G) {
   constexpr int PER = SAMPLE_S / 1024;
   __shared__ uint32_t wh[32][257];
   __shared__ uint32_t hist[256];
   __shared__ uint32_t s_prefix, s_krem;
+  const TauJob& jb = blockIdx.x ? j1 : j0;
+  const uint32_t* __restrict__ samples = jb.samples;
+  SelCtrl* c = jb.c;
+  const int q = jb.q;
+  const int64_t K = jb.K;
   const int wid = threadIdx.x >> 5;
   uint32_t key[PER];
 #pragma unroll
   for (int j = 0; j < PER; ++j) key[j] = samples[j * 1024 + threadIdx.x];
   for (int i = threadIdx.x; i < MAX_BINS; i += blockDim.x) c->hist[i] = 0;
-  for (int i = threadIdx.x; i < G; i += blockDim.x) ccnt[i] = 0;
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < G; i += blockDim.x) ccnt[i] = 0;
   if (threadIdx.x == 0) {
     c->tau0 = 0;
     c->mode = 0;
@@ -325,114 +346,136 @@ __global__ void __launch_bounds__(1024) sel_sample_tau_kernel(
   if (threadIdx.x == 0) c->tau0 = s_prefix;
 }
 
-// Four consecutive elements of g from i0 (zeros past hi), one 16-byte load when possible.
-__device__ __forceinline__ float4 load4(const float* __restrict__ g, int64_t i0, int64_t hi,
-                                        int vec_ok) {
-  if (vec_ok && i0 + 3 < hi) return __ldg(reinterpret_cast<const float4*>(g + i0));
-  float4 v;
-  v.x = i0 < hi ? g[i0] : 0.f;
-  v.y = i0 + 1 < hi ? g[i0 + 1] : 0.f;
-  v.z = i0 + 2 < hi ? g[i0 + 2] : 0.f;
-  v.w = i0 + 3 < hi ? g[i0 + 3] : 0.f;
-  return v;
-}
-
 // The one pass over g: every warp compacts the (key, index) pairs with key >= tau0 (and not
-// excluded) of its own contiguous part of g into its own region, in index order. The loads of the
-// next 512 elements are issued before the current 512 are examined; a warp scan places the
-// candidates only when some lane has one.
+// excluded) of its own contiguous part of g into its own region, in index order. A step is 512
+// elements, taken as 16 rows of 32: lane l holds element 32 r + l of row r, so one ballot per row
+// gives each lane with a candidate its place (the candidates of lower lanes of the row) and the
+// region stays in index order without a scan. The next step's loads are issued before the current
+// one is examined; a row is examined only when some lane of its 128-element group holds a key at
+// or above tau0 (the groups of the sampled path mostly hold none or one).
+// The exclusion bitmap (EX != EX_NONE) streams beside g: the 16 words of a step (parts start on
+// multiples of 1024) are loaded one step ahead by lanes 0-15, and row r's word, whose bit l is
+// lane l's element, is shuffled out only for rows with a candidate.
+// EX_TAG (two selections from one pass, `c` without and `cg` with the exclusion): the threshold
+// is the lower of the two tau0 and excluded entries stay candidates with bit 31 of their stored
+// key set; the first-digit histogram and count of the excluded ones are kept apart, and `cg`
+// receives the differences (the non-excluded candidates').
+enum { EX_NONE = 0, EX_SKIP = 1, EX_TAG = 2 };
+template <int EX>
 __global__ void __launch_bounds__(COMPACT_WARPS * 32) sel_compact_kernel(
     const float* __restrict__ g, int64_t N, int64_t L, const uint32_t* __restrict__ excl,
     int64_t cap, uint32_t* __restrict__ ckeys, uint32_t* __restrict__ cids,
-    uint32_t* __restrict__ ccnt, SelCtrl* c, int vec_ok, uint32_t* dev_status) {
-  constexpr int UN = 4;
+    uint32_t* __restrict__ ccnt, SelCtrl* c, SelCtrl* cg, uint32_t* dev_status) {
+  constexpr bool TAG = EX == EX_TAG;
+  constexpr int UN = 4;  // groups of 4 rows per step
   constexpr int STEP = 128 * UN;
   __shared__ uint32_t dhist[256];  // first radix digit (bits 30..23) of this block's candidates
-  for (int i = threadIdx.x; i < 256; i += blockDim.x) dhist[i] = 0;
+  __shared__ uint32_t dhist_x[TAG ? 256 : 1];  // the same over the excluded ones
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+    dhist[i] = 0;
+    if (TAG) dhist_x[i] = 0;
+  }
   __syncthreads();
-  const uint32_t tau0 = c->tau0;
+  const uint32_t tau0 = TAG ? min(c->tau0, cg->tau0) : c->tau0;
   const int lane = threadIdx.x & 31;
+  const uint32_t below = (1u << lane) - 1u;
   const int64_t r = (int64_t)blockIdx.x * COMPACT_WARPS + (threadIdx.x >> 5);
   const int64_t lo = r * L;
   const int64_t hi = min(N, lo + L);
   uint32_t* rk = ckeys + r * cap;
   uint32_t* ri = cids + r * cap;
-  uint32_t count = 0, kmax = 0;  // kmax: largest key seen, for the non-finite check
+  uint32_t count = 0, count_x = 0, kmax = 0;  // kmax: largest key seen, for the non-finite check
   bool over = false;
-  float4 nxt[UN];
+  // lane l < 16: the bitmap word of elements [t + 32 l, t + 32 l + 32) (words past hi are not read)
+  auto load_bw = [&](int64_t t) -> uint32_t {
+    return EX != EX_NONE && lane < 16 && t + lane * 32 < hi ? __ldg(excl + (t >> 5) + lane) : 0u;
+  };
+  // the 16 rows of the step at t (zeros past hi)
+  auto load_step = [&](int64_t t, float (&v)[UN][4]) {
+    if (t + STEP <= hi) {
 #pragma unroll
-  for (int u = 0; u < UN; ++u) nxt[u] = load4(g, lo + u * 128 + lane * 4, hi, vec_ok);
+      for (int u = 0; u < UN; ++u)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[u][j] = __ldg(g + t + u * 128 + j * 32 + lane);
+    } else {
+#pragma unroll
+      for (int u = 0; u < UN; ++u)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int64_t i = t + u * 128 + j * 32 + lane;
+          v[u][j] = i < hi ? __ldg(g + i) : 0.f;
+        }
+    }
+  };
+  float nxt[UN][4];
+  load_step(lo, nxt);
+  uint32_t bw_nxt = load_bw(lo);
   for (int64_t t0 = lo; t0 < hi; t0 += STEP) {
-    float4 cur[UN];
+    float cur[UN][4];
 #pragma unroll
-    for (int u = 0; u < UN; ++u) cur[u] = nxt[u];
+    for (int u = 0; u < UN; ++u)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) cur[u][j] = nxt[u][j];
+    const uint32_t bw = bw_nxt;
     if (t0 + STEP < hi) {
-#pragma unroll
-      for (int u = 0; u < UN; ++u) nxt[u] = load4(g, t0 + STEP + u * 128 + lane * 4, hi, vec_ok);
+      load_step(t0 + STEP, nxt);
+      bw_nxt = load_bw(t0 + STEP);
     }
     const bool full = t0 + STEP <= hi;  // no range tests
 #pragma unroll
     for (int u = 0; u < UN; ++u) {
-      const int64_t i0 = t0 + u * 128 + lane * 4;
-      const uint32_t key[4] = {abs_key(cur[u].x), abs_key(cur[u].y), abs_key(cur[u].z),
-                               abs_key(cur[u].w)};
-      uint32_t okm = 0;
-      if (full) {
-        const uint32_t m4 = max(max(key[0], key[1]), max(key[2], key[3]));
-        kmax = max(kmax, m4);
-        if (!__any_sync(0xffffffffu, m4 >= tau0)) continue;
-        // the exclusion set is looked up only for keys above the threshold
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          okm |= (uint32_t)(key[j] >= tau0 && !excluded(excl, i0 + j)) << j;
-        if (excl && !__any_sync(0xffffffffu, okm != 0)) continue;
-      } else {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const bool in = i0 + j < hi;
-          if (in) kmax = max(kmax, key[j]);
-          if (in && key[j] >= tau0 && !excluded(excl, i0 + j)) okm |= 1u << j;
-        }
-        if (!__any_sync(0xffffffffu, okm != 0)) continue;
-      }
-      const uint32_t mine = __popc(okm);
-      uint32_t x = mine;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-      }
-      uint32_t pos = count + x - mine;
+      const uint32_t key[4] = {abs_key(cur[u][0]), abs_key(cur[u][1]), abs_key(cur[u][2]),
+                               abs_key(cur[u][3])};
+      const uint32_t m4 = max(max(key[0], key[1]), max(key[2], key[3]));
+      kmax = max(kmax, m4);  // elements past hi read as 0
+      if (!__any_sync(0xffffffffu, m4 >= tau0)) continue;
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        if (okm & (1u << j)) {
+        const int64_t i = t0 + u * 128 + j * 32 + lane;
+        uint32_t b = __ballot_sync(0xffffffffu, key[j] >= tau0 && (full || i < hi));
+        if (!b) continue;
+        uint32_t word = 0;  // bit l: lane l's element is excluded
+        if (EX != EX_NONE) word = __shfl_sync(0xffffffffu, bw, u * 4 + j);
+        if (EX == EX_SKIP) {
+          b &= ~word;
+          if (!b) continue;
+        }
+        if ((b >> lane) & 1u) {
+          const uint32_t pos = count + __popc(b & below);
+          const bool ex = TAG && ((word >> lane) & 1u);
           if (pos < cap) {
-            rk[pos] = key[j];
-            ri[pos] = (uint32_t)(i0 + j);
+            rk[pos] = key[j] | (ex ? 0x80000000u : 0u);
+            ri[pos] = (uint32_t)i;
           } else {
             over = true;
           }
-          ++pos;
           atomicAdd(&dhist[key[j] >> sel_shift(0)], 1u);
+          if (ex) atomicAdd(&dhist_x[key[j] >> sel_shift(0)], 1u);
         }
+        count += __popc(b);
+        if (TAG) count_x += __popc(b & word);
       }
-      count += __shfl_sync(0xffffffffu, x, 31);
     }
   }
   __syncthreads();
-  for (int i = threadIdx.x; i < 256; i += blockDim.x)
+  for (int i = threadIdx.x; i < 256; i += blockDim.x) {
     if (dhist[i]) atomicAdd(&c->hist[i], dhist[i]);
+    if (TAG && dhist[i] - dhist_x[i]) atomicAdd(&cg->hist[i], dhist[i] - dhist_x[i]);
+  }
   if (lane == 0 && lo < N) {
     ccnt[r] = count < cap ? count : (uint32_t)cap;
     atomicAdd(&c->total, (unsigned long long)count);
+    if (TAG) atomicAdd(&cg->total, (unsigned long long)(count - count_x));
   }
   if (over) c->overflow = 1;
+  if (TAG && over) cg->overflow = 1;
   flag_status_warp(dev_status, kmax >= 0x7F800000u, USAF_DEV_NONFINITE);
 }
 
 // One block of 256 threads: the candidate path or the exact path, and on the candidate path the
 // first radix digit from the histogram the compacting pass built (so the first round is skipped).
-__global__ void sel_decide_kernel(SelCtrl* c, int64_t K, int sampling, uint32_t* dev_status) {
+__device__ __forceinline__ void decide_body(SelCtrl* c, int64_t K, int sampling,
+                                            uint32_t* dev_status) {
   __shared__ uint32_t h[256];
   __shared__ bool ok;
   if (threadIdx.x == 0) {
@@ -462,13 +505,26 @@ __global__ void sel_decide_kernel(SelCtrl* c, int64_t K, int sampling, uint32_t*
   }
 }
 
+__global__ void sel_decide_kernel(SelCtrl* c, int64_t K, int sampling, uint32_t* dev_status) {
+  decide_body(c, K, sampling, dev_status);
+}
+
+// Two selections over one candidate set: block b decides selection b.
+__global__ void sel_decide2_kernel(SelCtrl* c0, int64_t K0, SelCtrl* c1, int64_t K1,
+                                   uint32_t* dev_status) {
+  if (blockIdx.x == 0)
+    decide_body(c0, K0, 1, dev_status);
+  else
+    decide_body(c1, K1, 1, dev_status);
+}
+
 // One radix round over the source (digits of up to 12 bits). Each block counts the digits of the
 // keys that match the prefix found so far into a shared histogram and adds it to the global one;
 // the last block to finish picks the digit with a block-wide scan from the top. The first round's
 // digits (the exponent) fall in few bins, so a warp adds equal digits once; later rounds' digits
 // are spread out and each key adds its own.
-__global__ void __launch_bounds__(ROUND_THREADS) sel_round_kernel(Src s, SelCtrl* c, int shift,
-                                                                int bits, int fixed_mode) {
+__device__ __forceinline__ void round_body(const Src& s, SelCtrl* c, int shift, int bits,
+                                           int fixed_mode, int bid, int nblk) {
   __shared__ uint32_t hist[MAX_BINS];
   __shared__ bool last;
   __shared__ int pick;
@@ -481,7 +537,7 @@ __global__ void __launch_bounds__(ROUND_THREADS) sel_round_kernel(Src s, SelCtrl
   for (int i = threadIdx.x; i < nb; i += blockDim.x) hist[i] = 0;
   __syncthreads();
   const bool first = shift == sel_shift(0);  // exponent digits: few bins, aggregate per warp
-  for (int b = blockIdx.x; b < s.G; b += gridDim.x)
+  for (int b = bid; b < s.G; b += nblk)
   for_part(s, mode, b, [&](uint32_t key, int64_t, bool ok) {
     const bool m = ok && (hs >= 32 || (key >> hs) == (prefix >> hs));
     const int d = (int)((key >> shift) & dmask);
@@ -497,7 +553,7 @@ __global__ void __launch_bounds__(ROUND_THREADS) sel_round_kernel(Src s, SelCtrl
     if (hist[i]) atomicAdd(&c->hist[i], hist[i]);
   __threadfence();
   __syncthreads();
-  if (threadIdx.x == 0) last = atomicAdd(&c->ticket, 1u) == gridDim.x - 1;
+  if (threadIdx.x == 0) last = atomicAdd(&c->ticket, 1u) == (uint32_t)nblk - 1;
   __syncthreads();
   if (!last) return;
   __threadfence();
@@ -533,6 +589,24 @@ __global__ void __launch_bounds__(ROUND_THREADS) sel_round_kernel(Src s, SelCtrl
   }
 }
 
+__global__ void __launch_bounds__(ROUND_THREADS) sel_round_kernel(Src s, SelCtrl* c, int shift,
+                                                                int bits, int fixed_mode) {
+  round_body(s, c, shift, bits, fixed_mode, blockIdx.x, gridDim.x);
+}
+
+// One round of two selections over one candidate set: the first half of the blocks runs
+// selection 0, the second half selection 1.
+__global__ void __launch_bounds__(ROUND_THREADS) sel_round2_kernel(Src s0, SelCtrl* c0, Src s1,
+                                                                 SelCtrl* c1, int shift,
+                                                                 int bits) {
+  const int half = (int)gridDim.x / 2;
+  if ((int)blockIdx.x < half)
+    round_body(s0, c0, shift, bits, -1, blockIdx.x, half);
+  else
+    round_body(s1, c1, shift, bits, -1, blockIdx.x - half, gridDim.x - half);
+
+}
+
 // Per block: elements strictly above tau and equal to tau.
 __global__ void __launch_bounds__(SEL_THREADS) sel_count_kernel(Src s, const SelCtrl* c,
                                                                 uint32_t* blk_gt, uint32_t* blk_eq,
@@ -553,9 +627,8 @@ __global__ void __launch_bounds__(SEL_THREADS) sel_count_kernel(Src s, const Sel
   }
 }
 
-__global__ void __launch_bounds__(1024) sel_scan_kernel(const uint32_t* blk_gt,
-                                                        const uint32_t* blk_eq, int G,
-                                                        uint32_t* base_gt, uint32_t* base_eq) {
+__device__ __forceinline__ void scan_body(const uint32_t* blk_gt, const uint32_t* blk_eq, int G,
+                                          uint32_t* base_gt, uint32_t* base_eq) {
   uint32_t run_gt = 0, run_eq = 0;
   for (int c0 = 0; c0 < G; c0 += blockDim.x) {
     const int i = c0 + threadIdx.x;
@@ -570,6 +643,12 @@ __global__ void __launch_bounds__(1024) sel_scan_kernel(const uint32_t* blk_gt,
     run_gt += ta;
     run_eq += tb;
   }
+}
+
+__global__ void __launch_bounds__(1024) sel_scan_kernel(const uint32_t* blk_gt,
+                                                        const uint32_t* blk_eq, int G,
+                                                        uint32_t* base_gt, uint32_t* base_eq) {
+  scan_body(blk_gt, blk_eq, G, base_gt, base_eq);
 }
 
 // Ordered write: selected = key > tau, or key == tau among the first need_eq such (by index).
@@ -604,8 +683,9 @@ __device__ __forceinline__ void for_region_warp(const Src& s, int mode, int b, i
     const uint32_t* ii = s.cids + (int64_t)b * s.cap;
     for (int64_t j0 = 0; j0 < n; j0 += 32) {
       const int64_t j = j0 + lane;
-      const bool ok = j < n;
-      f(ok ? kk[j] : 0u, ok ? s.base + (int64_t)ii[j] : 0, ok);
+      const uint32_t kj = j < n ? kk[j] : 0u;
+      const bool ok = j < n && !(s.skip_tagged && (kj >> 31));
+      f(kj & 0x7FFFFFFFu, ok ? s.base + (int64_t)ii[j] : 0, ok);
     }
   } else {
     const int64_t lo = (int64_t)b * s.L;
@@ -625,10 +705,9 @@ __device__ __forceinline__ void for_region_warp(const Src& s, int mode, int b, i
   }
 }
 
-__global__ void __launch_bounds__(256) sel_count_warp_kernel(Src s, const SelCtrl* c,
-                                                            uint32_t* blk_gt, uint32_t* blk_eq) {
+__device__ __forceinline__ void count_warp_body(const Src& s, const SelCtrl* c, uint32_t* blk_gt,
+                                                uint32_t* blk_eq, int b) {
   const int lane = threadIdx.x & 31;
-  const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (b >= s.G) return;
   const int mode = (int)c->mode;
   const uint32_t tau = c->prefix;
@@ -643,12 +722,15 @@ __global__ void __launch_bounds__(256) sel_count_warp_kernel(Src s, const SelCtr
   }
 }
 
-__global__ void __launch_bounds__(256) sel_write_warp_kernel(Src s, const SelCtrl* c,
-                                                            const uint32_t* base_gt,
-                                                            const uint32_t* base_eq,
-                                                            int64_t* __restrict__ out) {
+__global__ void __launch_bounds__(256) sel_count_warp_kernel(Src s, const SelCtrl* c,
+                                                            uint32_t* blk_gt, uint32_t* blk_eq) {
+  count_warp_body(s, c, blk_gt, blk_eq, blockIdx.x * 8 + (threadIdx.x >> 5));
+}
+
+__device__ __forceinline__ void write_warp_body(const Src& s, const SelCtrl* c,
+                                                const uint32_t* base_gt, const uint32_t* base_eq,
+                                                int64_t* __restrict__ out, int b) {
   const int lane = threadIdx.x & 31;
-  const int b = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (b >= s.G) return;
   const int mode = (int)c->mode;
   const uint32_t tau = c->prefix;
@@ -664,6 +746,42 @@ __global__ void __launch_bounds__(256) sel_write_warp_kernel(Src s, const SelCtr
     gt_run += __popc(mg);
     eq_run += __popc(me);
   });
+}
+
+__global__ void __launch_bounds__(256) sel_write_warp_kernel(Src s, const SelCtrl* c,
+                                                            const uint32_t* base_gt,
+                                                            const uint32_t* base_eq,
+                                                            int64_t* __restrict__ out) {
+  write_warp_body(s, c, base_gt, base_eq, out, blockIdx.x * 8 + (threadIdx.x >> 5));
+}
+
+// The ordered write's arrays of one selection.
+struct WriteJob {
+  Src s;
+  const SelCtrl* c;
+  uint32_t *blk_gt, *blk_eq, *base_gt, *base_eq;
+  int64_t* out;
+};
+
+// Count, scan and write of two selections over one candidate set: the first nb blocks (or, for
+// the scan, block 0) take job 0, the rest job 1.
+__global__ void __launch_bounds__(256) sel_count_warp2_kernel(WriteJob j0, WriteJob j1, int nb) {
+  const bool second = (int)blockIdx.x >= nb;
+  const WriteJob& j = second ? j1 : j0;
+  count_warp_body(j.s, j.c, j.blk_gt, j.blk_eq, ((int)blockIdx.x - (second ? nb : 0)) * 8 +
+                                                    (int)(threadIdx.x >> 5));
+}
+
+__global__ void __launch_bounds__(256) sel_write_warp2_kernel(WriteJob j0, WriteJob j1, int nb) {
+  const bool second = (int)blockIdx.x >= nb;
+  const WriteJob& j = second ? j1 : j0;
+  write_warp_body(j.s, j.c, j.base_gt, j.base_eq, j.out,
+                  ((int)blockIdx.x - (second ? nb : 0)) * 8 + (int)(threadIdx.x >> 5));
+}
+
+__global__ void __launch_bounds__(1024) sel_scan2_kernel(WriteJob j0, WriteJob j1, int G) {
+  const WriteJob& j = blockIdx.x ? j1 : j0;
+  scan_body(j.blk_gt, j.blk_eq, G, j.base_gt, j.base_eq);
 }
 
 __global__ void bitmap_zero_kernel(uint32_t* bm, int64_t words) {
@@ -711,6 +829,22 @@ usaf_status ordered_write(const SelPlan& p, const SelWs& w, const Src& s, int64_
   return USAF_OK;
 }
 
+// The same for two selections over one candidate set (the warp-per-region form), in one launch
+// per stage.
+usaf_status ordered_write2(const SelPlan& p, const SelWs& w0, const Src& s0, int64_t* out0,
+                           const SelWs& w1, const Src& s1, int64_t* out1, cudaStream_t st) {
+  const WriteJob j0{s0, w0.ctrl, w0.blk_gt, w0.blk_eq, w0.base_gt, w0.base_eq, out0};
+  const WriteJob j1{s1, w1.ctrl, w1.blk_gt, w1.blk_eq, w1.base_gt, w1.base_eq, out1};
+  const int nb = (int)ceil_div(p.G, 8);
+  sel_count_warp2_kernel<<<2 * nb, 256, 0, st>>>(j0, j1, nb);
+  USAF_CHECK_LAUNCH();
+  sel_scan2_kernel<<<2, 1024, 0, st>>>(j0, j1, p.G);
+  USAF_CHECK_LAUNCH();
+  sel_write_warp2_kernel<<<2 * nb, 256, 0, st>>>(j0, j1, nb);
+  USAF_CHECK_LAUNCH();
+  return USAF_OK;
+}
+
 // The fixed sequence of launches that selects the top-K of `s` (see file comment).
 usaf_status run_select(const SelPlan& p, const SelWs& w, Src s, int64_t K, int64_t* out,
                        uint32_t* dev_status, bool fixed_drop, cudaStream_t st) {
@@ -718,15 +852,21 @@ usaf_status run_select(const SelPlan& p, const SelWs& w, Src s, int64_t K, int64
     {
       USAF_TRACE("select_sample", st);
       sel_sample_kernel<<<SAMPLE_BLOCKS, SAMPLE_S / SAMPLE_BLOCKS, 0, st>>>(s.g, s.n, s.excl,
-                                                                             w.samples);
+                                                                             w.samples, nullptr);
       USAF_CHECK_LAUNCH();
-      sel_sample_tau_kernel<<<1, 1024, 0, st>>>(w.samples, p.q, w.ctrl, K, w.ccnt, p.G);
+      const TauJob job{w.samples, p.q, w.ctrl, K};
+      sel_sample_tau_kernel<<<1, 1024, 0, st>>>(job, job, w.ccnt, p.G);
       USAF_CHECK_LAUNCH();
     }
     USAF_TRACE("select_compact", st);
-    const int vec_ok = (reinterpret_cast<uintptr_t>(s.g) & 15) == 0;
-    sel_compact_kernel<<<p.G / COMPACT_WARPS, COMPACT_WARPS * 32, 0, st>>>(
-        s.g, s.n, p.L, s.excl, p.cap, w.ckeys, w.cids, w.ccnt, w.ctrl, vec_ok, dev_status);
+    if (s.excl)
+      sel_compact_kernel<EX_SKIP><<<p.G / COMPACT_WARPS, COMPACT_WARPS * 32, 0, st>>>(
+          s.g, s.n, p.L, s.excl, p.cap, w.ckeys, w.cids, w.ccnt, w.ctrl, nullptr,
+          dev_status);
+    else
+      sel_compact_kernel<EX_NONE><<<p.G / COMPACT_WARPS, COMPACT_WARPS * 32, 0, st>>>(
+          s.g, s.n, p.L, nullptr, p.cap, w.ckeys, w.cids, w.ccnt, w.ctrl, nullptr,
+          dev_status);
     USAF_CHECK_LAUNCH();
   } else {
     USAF_TRACE("select_init", st);
@@ -970,6 +1110,107 @@ size_t rigl_ws_bytes(int64_t N, int64_t K, int64_t D) {
   return c.size();
 }
 
+namespace {
+
+// The arguments of a RigL swap that the drop selection and the merge use.
+struct RiglIo {
+  int64_t N, K, D;
+  const int64_t* act_idx;
+  const float *p_in, *m_in, *v_in;
+  const void *w0, *w1;
+  int64_t n0;
+  usaf_dtype wdt;
+  int64_t* new_idx;
+  float *p_out, *m_out, *v_out;
+  int64_t* n_swapped;
+  uint32_t* dev_status;
+};
+
+// Drop selection (the D smallest |p| among the K actives: complemented keys, exact path), the
+// grow selection that `grow` issues on `st` (when given: the drop selection then runs on a stream
+// of its own, forked from and joined back to `st`, so that its chain of small launches overlaps
+// the pass over g), and the merge of the kept and grown entries.
+template <class GrowFn>
+usaf_status rigl_swap_around(const RiglIo& io, int64_t* dpos, const int64_t* grown, char* ws_drop,
+                             bool has_grow, GrowFn grow, cudaStream_t st) {
+  const int64_t Ks = io.K > 0 ? io.K : 1, Ds = io.D > 0 ? io.D : 1;
+  const SelPlan pd = make_plan(Ks, Ds);
+  Carver cd(ws_drop);
+  SelWs wd;
+  sel_layout(pd, cd, wd);
+  Src sd{};
+  sd.g = io.p_in;
+  sd.n = io.K;
+  sd.L = pd.L;
+  sd.drop = 1;
+  if (io.D <= 0) {
+    sel_init_kernel<<<1, 256, 0, st>>>(wd.ctrl, 0, wd.ccnt, pd.G);
+    USAF_CHECK_LAUNCH();
+  } else if (!has_grow) {
+    USAF_TRY(run_select(pd, wd, sd, io.D, dpos, io.dev_status, true, st));
+  } else {
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    auto release = [&]() {
+      if (fork) cudaEventDestroy(fork);
+      if (join) cudaEventDestroy(join);
+      if (side) cudaStreamDestroy(side);  // its work still completes
+    };
+    if (cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventRecord(fork, st) != cudaSuccess || cudaStreamWaitEvent(side, fork, 0) != cudaSuccess) {
+      release();
+      return USAF_ERR_CUDA;
+    }
+    const usaf_status sdrop = run_select(pd, wd, sd, io.D, dpos, io.dev_status, true, side);
+    if (sdrop != USAF_OK || cudaEventRecord(join, side) != cudaSuccess) {
+      release();
+      return sdrop != USAF_OK ? sdrop : USAF_ERR_CUDA;
+    }
+    const usaf_status sgrow = grow();
+    const bool joined = cudaStreamWaitEvent(st, join, 0) == cudaSuccess;
+    release();
+    if (sgrow != USAF_OK) return sgrow;
+    if (!joined) return USAF_ERR_CUDA;
+  }
+  USAF_TRACE("rigl_merge", st);
+  if (io.K > 0) {
+    const unsigned nb = (unsigned)ceil_div(io.K, MG_TILE);
+    if (io.wdt == USAF_BF16)
+      rigl_merge_tile_kernel<__nv_bfloat16><<<nb, MG_THREADS, 0, st>>>(
+          io.act_idx, io.K, dpos, grown, io.D, io.p_in, io.m_in, io.v_in,
+          static_cast<const __nv_bfloat16*>(io.w0), io.n0,
+          static_cast<const __nv_bfloat16*>(io.w1), io.new_idx, io.p_out, io.m_out, io.v_out,
+          wd.ctrl, io.N, io.dev_status);
+    else
+      rigl_merge_tile_kernel<float><<<nb, MG_THREADS, 0, st>>>(
+          io.act_idx, io.K, dpos, grown, io.D, io.p_in, io.m_in, io.v_in,
+          static_cast<const float*>(io.w0), io.n0, static_cast<const float*>(io.w1), io.new_idx,
+          io.p_out, io.m_out, io.v_out, wd.ctrl, io.N, io.dev_status);
+    USAF_CHECK_LAUNCH();
+  }
+  rigl_finish_kernel<<<1, 32, 0, st>>>(wd.ctrl, io.n_swapped);
+  USAF_CHECK_LAUNCH();
+  return USAF_OK;
+}
+
+// The bitmap of the active set (excluded from the grow selection).
+usaf_status active_bitmap(const int64_t* act_idx, int64_t K, int64_t N, uint32_t* bitmap,
+                          uint32_t* dev_status, cudaStream_t st) {
+  USAF_TRACE("rigl_bitmap", st);
+  const int64_t words = ceil_div(N, 32);
+  bitmap_zero_kernel<<<grid_dim_for(words), 256, 0, st>>>(bitmap, words);
+  USAF_CHECK_LAUNCH();
+  if (K > 0) {
+    bitmap_set_kernel<<<grid_dim_for(K), 256, 0, st>>>(act_idx, K, N, bitmap, dev_status);
+    USAF_CHECK_LAUNCH();
+  }
+  return USAF_OK;
+}
+
+}  // namespace
+
 usaf_status rigl_launch(const float* g, int64_t N, const int64_t* act_idx, int64_t K, int64_t D,
                         const float* p_in, const float* m_in, const float* v_in, const void* w0,
                         int64_t n0, const void* w1, usaf_dtype wdt, int64_t* new_idx,
@@ -979,129 +1220,164 @@ usaf_status rigl_launch(const float* g, int64_t N, const int64_t* act_idx, int64
   Carver c(ws);
   int64_t* dpos = c.take<int64_t>(D);
   int64_t* grown = c.take<int64_t>(D);
-  if (grown_in) {
-    // the grow set is given (chosen across ranks): drop selection and merge only
-    const int64_t Ks = K > 0 ? K : 1, Ds = D > 0 ? D : 1;
-    char* ws_drop = c.take<char>(select_ws_bytes(Ks, Ds, false));
-    const SelPlan pd = make_plan(Ks, Ds);
-    Carver cd(ws_drop);
-    SelWs wd;
-    sel_layout(pd, cd, wd);
-    if (D > 0) {
-      Src sd{};
-      sd.g = p_in;
-      sd.n = K;
-      sd.L = pd.L;
-      sd.drop = 1;
-      USAF_TRY(run_select(pd, wd, sd, D, dpos, dev_status, true, st));
-    } else {
-      sel_init_kernel<<<1, 256, 0, st>>>(wd.ctrl, 0, wd.ccnt, pd.G);
-      USAF_CHECK_LAUNCH();
-    }
-    USAF_TRACE("rigl_merge", st);
-    if (K > 0) {
-      const unsigned nb = (unsigned)ceil_div(K, MG_TILE);
-      if (wdt == USAF_BF16)
-        rigl_merge_tile_kernel<__nv_bfloat16><<<nb, MG_THREADS, 0, st>>>(
-            act_idx, K, dpos, grown_in, D, p_in, m_in, v_in,
-            static_cast<const __nv_bfloat16*>(w0), n0, static_cast<const __nv_bfloat16*>(w1),
-            new_idx, p_out, m_out, v_out, wd.ctrl, N, dev_status);
-      else
-        rigl_merge_tile_kernel<float><<<nb, MG_THREADS, 0, st>>>(
-            act_idx, K, dpos, grown_in, D, p_in, m_in, v_in, static_cast<const float*>(w0), n0,
-            static_cast<const float*>(w1), new_idx, p_out, m_out, v_out, wd.ctrl, N, dev_status);
-      USAF_CHECK_LAUNCH();
-    }
-    rigl_finish_kernel<<<1, 32, 0, st>>>(wd.ctrl, n_swapped);
-    USAF_CHECK_LAUNCH();
-    return USAF_OK;
-  }
   const int64_t Ks = K > 0 ? K : 1, Ds = D > 0 ? D : 1;
   char* ws_drop = c.take<char>(select_ws_bytes(Ks, Ds, false));
+  const RiglIo io{N, K, D, act_idx, p_in, m_in, v_in, w0, w1, n0, wdt, new_idx, p_out,
+                  m_out, v_out, n_swapped, dev_status};
+  // the grow set is given (chosen across ranks): drop selection and merge only
+  if (grown_in) return rigl_swap_around(io, dpos, grown_in, ws_drop, false, [] { return USAF_OK; }, st);
   char* ws_grow = c.take<char>(select_ws_bytes(N, Ds, true));
-  // drop: the D smallest |p| among the K actives (complemented keys, exact path)
-  const SelPlan pd = make_plan(Ks, Ds);
-  Carver cd(ws_drop);
-  SelWs wd;
-  sel_layout(pd, cd, wd);
   // grow: the D largest |g| outside the active set (sampled path with an exclusion bitmap)
-  const SelPlan pg = make_plan(N, Ds);
-  Carver cg(ws_grow);
-  SelWs wg;
-  sel_layout(pg, cg, wg);
-  uint32_t* bitmap = cg.take<uint32_t>(ceil_div(N, 32));
-  // the drop selection (over the K values of |p|, a chain of small launches) runs on a stream of
-  // its own, forked from and joined back to `st`, so it overlaps the pass over g
-  cudaStream_t side = nullptr;
-  cudaEvent_t fork = nullptr, join = nullptr;
-  auto release = [&]() {
-    if (fork) cudaEventDestroy(fork);
-    if (join) cudaEventDestroy(join);
-    if (side) cudaStreamDestroy(side);  // its work still completes
-  };
-  if (D > 0) {
-    if (cudaStreamCreateWithFlags(&side, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaEventCreateWithFlags(&fork, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&join, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventRecord(fork, st) != cudaSuccess || cudaStreamWaitEvent(side, fork, 0) != cudaSuccess) {
-      release();
-      return USAF_ERR_CUDA;
-    }
-    Src sd{};
-    sd.g = p_in;
-    sd.n = K;
-    sd.L = pd.L;
-    sd.drop = 1;
-    const usaf_status sdrop = run_select(pd, wd, sd, D, dpos, dev_status, true, side);
-    if (sdrop != USAF_OK || cudaEventRecord(join, side) != cudaSuccess) {
-      release();
-      return sdrop != USAF_OK ? sdrop : USAF_ERR_CUDA;
-    }
-    const int64_t words = ceil_div(N, 32);
-    {
-      USAF_TRACE("rigl_bitmap", st);
-      bitmap_zero_kernel<<<grid_dim_for(words), 256, 0, st>>>(bitmap, words);
-      count_launch();
-      bitmap_set_kernel<<<grid_dim_for(K), 256, 0, st>>>(act_idx, K, N, bitmap, dev_status);
-      count_launch();
-      if (cudaGetLastError() != cudaSuccess) {
-        cudaStreamWaitEvent(st, join, 0);
-        release();
-        return USAF_ERR_CUDA;
-      }
-    }
+  auto grow = [&]() -> usaf_status {
+    const SelPlan pg = make_plan(N, Ds);
+    Carver cg(ws_grow);
+    SelWs wg;
+    sel_layout(pg, cg, wg);
+    uint32_t* bitmap = cg.take<uint32_t>(ceil_div(N, 32));
+    USAF_TRY(active_bitmap(act_idx, K, N, bitmap, dev_status, st));
     Src sg{};
     sg.g = g;
     sg.n = N;
     sg.L = pg.L;
     sg.excl = bitmap;
     sg.drop = 0;
-    const usaf_status sgrow = run_select(pg, wg, sg, D, grown, dev_status, false, st);
-    const bool joined = cudaStreamWaitEvent(st, join, 0) == cudaSuccess;
-    release();
-    if (sgrow != USAF_OK) return sgrow;
-    if (!joined) return USAF_ERR_CUDA;
-  } else {
-    sel_init_kernel<<<1, 256, 0, st>>>(wd.ctrl, 0, wd.ccnt, pd.G);
-    USAF_CHECK_LAUNCH();
+    return run_select(pg, wg, sg, D, grown, dev_status, false, st);
+  };
+  return rigl_swap_around(io, dpos, grown, ws_drop, D > 0, grow, st);
+}
+
+// ------------------------------------------------------------------------------------------------
+// Importance selection and RigL swap from one pass over g. The top-K_sel of |g| and the grow set
+// (the D largest |g| outside the active set) are both found among one set of candidates: the
+// samples give each selection its own tau0, one compacting pass keeps every key at or above the
+// lower of the two (excluded entries tagged by bit 31 of their stored key), and each selection then
+// runs its radix rounds and ordered write over the shared candidates (the grow selection skips the
+// tagged ones). Results equal the two separate calls'.
+// ------------------------------------------------------------------------------------------------
+namespace {
+
+struct FusedPlan {
+  SelPlan p;      // regions, capacity: the candidates of both selections
+  int q_sel, q_grow;
+  bool ok;        // both selections take the sampled path
+};
+
+FusedPlan make_fused_plan(int64_t N, int64_t Ksel, int64_t K, int64_t D) {
+  FusedPlan f{};
+  if (D <= 0 || Ksel <= 0) return f;
+  const SelPlan a = make_plan(N, Ksel), b = make_plan(N, D);
+  // the keys at or above the selection's tau0 are about K_sel; those at or above the grow's are
+  // about D outside the active set plus at most the K active ones: the regions are sized for the
+  // larger count (an overflow still only sends both selections to the exact path)
+  f.p = make_plan(N, std::max(Ksel, K + D));
+  f.q_sel = a.q;
+  f.q_grow = b.q;
+  f.ok = a.sampling && b.sampling && f.p.sampling;
+  return f;
+}
+
+void fused_layout(const FusedPlan& f, Carver& c, SelWs& ws, SelWs& wg) {
+  sel_layout(f.p, c, ws);
+  wg = ws;
+  wg.ctrl = c.take<SelCtrl>(1);
+  wg.blk_gt = c.take<uint32_t>(f.p.G);
+  wg.blk_eq = c.take<uint32_t>(f.p.G);
+  wg.base_gt = c.take<uint32_t>(f.p.G);
+  wg.base_eq = c.take<uint32_t>(f.p.G);
+  wg.samples = c.take<uint32_t>(SAMPLE_S);
+}
+
+}  // namespace
+
+size_t select_and_swap_ws_bytes(int64_t N, int64_t Ksel, int64_t K, int64_t D) {
+  const FusedPlan f = make_fused_plan(N, Ksel, K, D);
+  Carver c(nullptr);
+  if (!f.ok) {
+    c.take<char>(select_ws_bytes(N, Ksel, false));
+    c.take<char>(rigl_ws_bytes(N, K, D));
+    return c.size();
   }
-  USAF_TRACE("rigl_merge", st);
-  if (K > 0) {
-    const unsigned nb = (unsigned)ceil_div(K, MG_TILE);
-    if (wdt == USAF_BF16)
-      rigl_merge_tile_kernel<__nv_bfloat16><<<nb, MG_THREADS, 0, st>>>(
-          act_idx, K, dpos, grown, D, p_in, m_in, v_in, static_cast<const __nv_bfloat16*>(w0),
-          n0, static_cast<const __nv_bfloat16*>(w1), new_idx, p_out, m_out, v_out, wd.ctrl, N,
-          dev_status);
-    else
-      rigl_merge_tile_kernel<float><<<nb, MG_THREADS, 0, st>>>(
-          act_idx, K, dpos, grown, D, p_in, m_in, v_in, static_cast<const float*>(w0), n0,
-          static_cast<const float*>(w1), new_idx, p_out, m_out, v_out, wd.ctrl, N, dev_status);
-    USAF_CHECK_LAUNCH();
+  c.take<int64_t>(D);
+  c.take<int64_t>(D);
+  c.take<char>(select_ws_bytes(K > 0 ? K : 1, D, false));
+  SelWs a, b;
+  fused_layout(f, c, a, b);
+  c.take<uint32_t>(ceil_div(N, 32));
+  return c.size();
+}
+
+usaf_status select_and_swap_launch(const float* g, int64_t N, int64_t Ksel, int64_t* sel_idx,
+                                   const int64_t* act_idx, int64_t K, int64_t D,
+                                   const float* p_in, const float* m_in, const float* v_in,
+                                   const void* w0, int64_t n0, const void* w1, usaf_dtype wdt,
+                                   int64_t* new_idx, float* p_out, float* m_out, float* v_out,
+                                   int64_t* n_swapped, uint32_t* dev_status, void* ws,
+                                   cudaStream_t st) {
+  const FusedPlan f = make_fused_plan(N, Ksel, K, D);
+  Carver c(ws);
+  if (!f.ok) {
+    // a selection on the exact path (small N, or K_sel or D a large part of N): the two calls
+    char* ws_sel = c.take<char>(select_ws_bytes(N, Ksel, false));
+    char* ws_rigl = c.take<char>(rigl_ws_bytes(N, K, D));
+    USAF_TRY(importance_select_launch(g, N, Ksel, sel_idx, dev_status, ws_sel, st));
+    return rigl_launch(g, N, act_idx, K, D, p_in, m_in, v_in, w0, n0, w1, wdt, new_idx, p_out,
+                       m_out, v_out, n_swapped, dev_status, ws_rigl, st);
   }
-  rigl_finish_kernel<<<1, 32, 0, st>>>(wd.ctrl, n_swapped);
-  USAF_CHECK_LAUNCH();
-  return USAF_OK;
+  int64_t* dpos = c.take<int64_t>(D);
+  int64_t* grown = c.take<int64_t>(D);
+  char* ws_drop = c.take<char>(select_ws_bytes(K > 0 ? K : 1, D, false));
+  SelWs w1s, w2s;
+  fused_layout(f, c, w1s, w2s);
+  uint32_t* bitmap = c.take<uint32_t>(ceil_div(N, 32));
+  const RiglIo io{N, K, D, act_idx, p_in, m_in, v_in, w0, w1, n0, wdt, new_idx, p_out,
+                  m_out, v_out, n_swapped, dev_status};
+  const SelPlan& p = f.p;
+  auto both = [&]() -> usaf_status {
+    USAF_TRY(active_bitmap(act_idx, K, N, bitmap, dev_status, st));
+    {
+      USAF_TRACE("select_sample", st);
+      sel_sample_kernel<<<SAMPLE_BLOCKS, SAMPLE_S / SAMPLE_BLOCKS, 0, st>>>(g, N, bitmap,
+                                                                             w2s.samples,
+                                                                             w1s.samples);
+      USAF_CHECK_LAUNCH();
+      const TauJob js{w1s.samples, f.q_sel, w1s.ctrl, Ksel};
+      const TauJob jg{w2s.samples, f.q_grow, w2s.ctrl, D};
+      sel_sample_tau_kernel<<<2, 1024, 0, st>>>(js, jg, w1s.ccnt, p.G);
+      USAF_CHECK_LAUNCH();
+    }
+    {
+      USAF_TRACE("select_compact", st);
+      sel_compact_kernel<EX_TAG><<<p.G / COMPACT_WARPS, COMPACT_WARPS * 32, 0, st>>>(
+          g, N, p.L, bitmap, p.cap, w1s.ckeys, w1s.cids, w1s.ccnt, w1s.ctrl, w2s.ctrl, dev_status);
+      USAF_CHECK_LAUNCH();
+    }
+    sel_decide2_kernel<<<2, 256, 0, st>>>(w1s.ctrl, Ksel, w2s.ctrl, D, dev_status);
+    USAF_CHECK_LAUNCH();
+    Src ss{};
+    ss.g = g;
+    ss.n = N;
+    ss.L = p.L;
+    ss.ckeys = w1s.ckeys;
+    ss.cids = w1s.cids;
+    ss.ccnt = w1s.ccnt;
+    ss.cap = p.cap;
+    ss.G = p.G;
+    Src sg = ss;
+    sg.excl = bitmap;
+    sg.skip_tagged = 1;
+    const int rgrid = (int)std::min<int64_t>(p.G, device_sm_count() * 8);
+    {
+      USAF_TRACE("select_radix", st);
+      for (int r = 0; r < SEL_ROUNDS; ++r) {
+        sel_round2_kernel<<<2 * rgrid, ROUND_THREADS, 0, st>>>(ss, w1s.ctrl, sg, w2s.ctrl,
+                                                               sel_shift(r), sel_bits(r));
+        USAF_CHECK_LAUNCH();
+      }
+    }
+    USAF_TRACE("select_write", st);
+    return ordered_write2(p, w1s, ss, sel_idx, w2s, sg, grown, st);
+  };
+  return rigl_swap_around(io, dpos, grown, ws_drop, true, both, st);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -1243,9 +1519,13 @@ usaf_status shard_emit_launch(const float* g, int64_t n, const uint32_t* excl, u
   s.base = base;
   int fm = 0;
   if (p.sampling) {
-    const int vec_ok = (reinterpret_cast<uintptr_t>(g) & 15) == 0;
-    sel_compact_kernel<<<p.G / COMPACT_WARPS, COMPACT_WARPS * 32, 0, st>>>(
-        g, n, p.L, excl, p.cap, w.ckeys, w.cids, w.ccnt, w.ctrl, vec_ok, dev_status);
+    if (excl)
+      sel_compact_kernel<EX_SKIP><<<p.G / COMPACT_WARPS, COMPACT_WARPS * 32, 0, st>>>(
+          g, n, p.L, excl, p.cap, w.ckeys, w.cids, w.ccnt, w.ctrl, nullptr, dev_status);
+    else
+      sel_compact_kernel<EX_NONE><<<p.G / COMPACT_WARPS, COMPACT_WARPS * 32, 0, st>>>(
+          g, n, p.L, nullptr, p.cap, w.ckeys, w.cids, w.ccnt, w.ctrl, nullptr,
+          dev_status);
     USAF_CHECK_LAUNCH();
     shard_emit_decide_kernel<<<1, 32, 0, st>>>(w.ctrl, dev_status);
     USAF_CHECK_LAUNCH();

@@ -18,7 +18,7 @@ fake_addresses = pytest.mark.skipif(torch.cuda.is_available(),
 def test_library_exports_every_header_symbol():
     L = B.lib()
     syms = B.header_symbols()
-    assert len(syms) == 38
+    assert len(syms) == 40
     for s in syms:
         assert hasattr(L, s), s
     assert L.usaf_abi_version() == 2
@@ -81,6 +81,26 @@ def test_shard_selection_host_checks():
                                  fake, fake, fake, fake, None, None, 0, None) == 3
 
 
+@fake_addresses
+def test_select_and_swap_host_checks():
+    L = B.lib()
+    fake = [ctypes.c_void_p(a) for a in range(1 << 20, 12 << 20, 1 << 20)]  # 1 MiB apart
+    g, sel, act, p, m, v, w, new, po, mo, vo = fake
+    ns, ws = ctypes.c_void_p(256), ctypes.c_void_p(512)
+
+    def call(K_sel, K, D, sel_ptr=sel, new_ptr=new, ws_bytes=1 << 40):
+        return L.usaf_select_and_swap(g, 1000, K_sel, sel_ptr, act, K, D, p, m, v, w, 1000, None,
+                                      1, new_ptr, po, mo, vo, ns, None, ws, ws_bytes, None)
+
+    assert call(0, 100, 10) == 1     # K_sel < 1
+    assert call(1001, 100, 10) == 1  # K_sel > N
+    assert call(50, 100, 101) == 1   # D > K
+    assert call(50, 100, 10, sel_ptr=None) == 1
+    assert call(50, 100, 10, sel_ptr=new) == 1  # the selection overlaps the new active set
+    assert call(50, 100, 10, new_ptr=act) == 1  # an output overlaps an input
+    assert call(50, 100, 10, ws_bytes=16) == 3
+
+
 def test_capacity_and_workspace_queries():
     s = B.shape(4096, 2048, 128, 8, 768)
     cap = B.routed_rows_capacity(s)
@@ -99,6 +119,16 @@ def test_capacity_and_workspace_queries():
     assert B.routed_rows_capacity(bad) == -1
     assert B.importance_select_workspace_size(10, 11) == 0
     assert B.rigl_swap_workspace_size(10, 8, 3) == 0  # D > N - K
+    # one pass for both selections: the shared candidates, less than the two calls' workspaces
+    D = int(0.3 * K)
+    fused = B.select_and_swap_workspace_size(N, K, K, D)
+    assert N // 8 < fused < ws + B.rigl_swap_workspace_size(N, K, D)
+    assert B.select_and_swap_workspace_size(N, 0, K, D) == 0
+    assert B.select_and_swap_workspace_size(10, 11, 2, 1) == 0
+    assert B.select_and_swap_workspace_size(10, 5, 8, 3) == 0  # D > N - K
+    # where the two selections run one after the other, both calls' workspaces
+    assert B.select_and_swap_workspace_size(5000, 700, 700, 200) >= \
+        B.importance_select_workspace_size(5000, 700) + B.rigl_swap_workspace_size(5000, 700, 200)
 
 
 def _call(name, *args):
