@@ -21,7 +21,8 @@ namespace {
 constexpr int SEL_THREADS = 256;
 constexpr int COMPACT_WARPS = 8;  // warps per block of the compacting pass, one region each
 constexpr int ROUND_THREADS = 256;  // radix rounds: eight blocks per SM, parts taken in turn
-constexpr int SAMPLE_S = 32768;
+constexpr int SAMPLE_S = 131072;  // strided samples of the keys for the threshold
+constexpr int TAU_BLOCKS = 32;    // blocks of the threshold's second digit round
 // radix rounds over the 31-bit key, most significant digit first: bits 30..23, 22..15, 14..7, 6..0
 __host__ __device__ constexpr int round_shift(int r) { return r == 0 ? 23 : r == 1 ? 15 : r == 2 ? 7 : 0; }
 __host__ __device__ constexpr int round_bits(int r) { return r == 3 ? 7 : 8; }
@@ -82,6 +83,8 @@ struct SelWs {
   uint32_t* base_gt;
   uint32_t* base_eq;
   uint32_t* samples;  // [SAMPLE_S] sampled keys (sampled path)
+  uint32_t* bhist;    // [SAMPLE_BLOCKS][256] first-digit histograms of the samples, per block
+  uint32_t* bhist2;   // [TAU_BLOCKS][256] second-digit histograms of the threshold, per block
 };
 
 SelPlan make_plan(int64_t N, int64_t K) {
@@ -105,8 +108,10 @@ SelPlan make_plan(int64_t N, int64_t K) {
     const double mean = (double)p.L * (double)p.q / SAMPLE_S;
     p.cap = round_up((int64_t)(mean * 1.5 + 8.0 * std::sqrt(mean)) + 256, 256);
   } else {
-    int64_t G = ceil_div(N, 16384);
-    if (G > sms * 4) G = sms * 4;
+    // exact path: regions of at least 4096 entries, up to eight blocks per SM (a selection over
+    // the K values of |p| still fills the GPU)
+    int64_t G = ceil_div(N, 4096);
+    if (G > sms * 8) G = sms * 8;
     if (G < 1) G = 1;
     p.G = (int)G;
     p.L = round_up(ceil_div(N, G), 1024);
@@ -126,6 +131,8 @@ void sel_layout(const SelPlan& p, Carver& c, SelWs& w) {
   w.base_gt = c.take<uint32_t>(p.G);
   w.base_eq = c.take<uint32_t>(p.G);
   w.samples = p.sampling ? c.take<uint32_t>(SAMPLE_S) : nullptr;
+  w.bhist = p.sampling ? c.take<uint32_t>(SAMPLE_S / 1024 * 256) : nullptr;
+  w.bhist2 = p.sampling ? c.take<uint32_t>(TAU_BLOCKS * 256) : nullptr;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -195,9 +202,9 @@ __device__ __forceinline__ void for_part(const Src& s, int mode, int b, F f) {
 // ------------------------------------------------------------------------------------------------
 // kernels
 // ------------------------------------------------------------------------------------------------
-__global__ void sel_init_kernel(SelCtrl* c, int64_t K, uint32_t* ccnt, int G) {
+// Clear a control block for a selection of K, by one block.
+__device__ __forceinline__ void ctrl_init_block(SelCtrl* c, int64_t K) {
   for (int i = threadIdx.x; i < MAX_BINS; i += blockDim.x) c->hist[i] = 0;
-  for (int i = threadIdx.x; i < G; i += blockDim.x) ccnt[i] = 0;
   if (threadIdx.x == 0) {
     c->tau0 = 0;
     c->mode = 0;
@@ -209,6 +216,11 @@ __global__ void sel_init_kernel(SelCtrl* c, int64_t K, uint32_t* ccnt, int G) {
     c->n_swapped = 0;
     c->r0_done = 0;
   }
+}
+
+__global__ void sel_init_kernel(SelCtrl* c, int64_t K, uint32_t* ccnt, int G) {
+  ctrl_init_block(c, K);
+  for (int i = threadIdx.x; i < G; i += blockDim.x) ccnt[i] = 0;
 }
 
 // The digit of one radix round from a 256-bin histogram (digits above dmask empty), by warp 0:
@@ -261,89 +273,127 @@ __device__ __forceinline__ void pick_digit_warp(const uint32_t* hist, uint32_t* 
   }
 }
 
-// The SAMPLE_S strided samples of the keys (0 where excluded), read by 32 blocks: the random
-// reads of g spread over 32 SMs instead of queueing in one. With samples_all (two selections
-// sharing one pass), the same positions' keys are also written there without the exclusion.
-constexpr int SAMPLE_BLOCKS = 32;
-__global__ void __launch_bounds__(SAMPLE_S / SAMPLE_BLOCKS) sel_sample_kernel(
+// The SAMPLE_S strided samples of the keys (0 where excluded), 1024 per block so that the random
+// reads of g spread over SAMPLE_BLOCKS SMs; each block also writes the histogram of its samples'
+// first digit (bits 30..23). With samples_all (two selections sharing one pass), the same
+// positions' keys and their histogram are also written without the exclusion. Block 0 also
+// clears the control blocks (c for the samples, c_all for samples_all) and the region counts.
+constexpr int SAMPLE_BLOCKS = SAMPLE_S / 1024;
+__global__ void __launch_bounds__(1024) sel_sample_kernel(
     const float* __restrict__ g, int64_t N, const uint32_t* __restrict__ excl,
-    uint32_t* __restrict__ samples, uint32_t* __restrict__ samples_all) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    uint32_t* __restrict__ samples, uint32_t* __restrict__ bhist,
+    uint32_t* __restrict__ samples_all, uint32_t* __restrict__ bhist_all, SelCtrl* c, int64_t K,
+    SelCtrl* c_all, int64_t K_all, uint32_t* ccnt, int G) {
+  __shared__ uint32_t h[256], ha[256];
+  if (threadIdx.x < 256) {
+    h[threadIdx.x] = 0;
+    ha[threadIdx.x] = 0;
+  }
+  if (blockIdx.x == 0) {
+    ctrl_init_block(c, K);
+    if (c_all) ctrl_init_block(c_all, K_all);
+    for (int i = threadIdx.x; i < G; i += blockDim.x) ccnt[i] = 0;
+  }
+  __syncthreads();
+  const int i = blockIdx.x * 1024 + threadIdx.x;
   const int64_t pos = (int64_t)(((unsigned long long)i * (unsigned long long)N) / SAMPLE_S);
   const uint32_t k = abs_key(g[pos]);
-  samples[i] = excluded(excl, pos) ? 0u : k;
-  if (samples_all) samples_all[i] = k;
+  const uint32_t ks = excluded(excl, pos) ? 0u : k;
+  samples[i] = ks;
+  atomicAdd(&h[ks >> sel_shift(0)], 1u);
+  if (samples_all) {
+    samples_all[i] = k;
+    atomicAdd(&ha[k >> sel_shift(0)], 1u);
+  }
+  __syncthreads();
+  if (threadIdx.x < 256) {
+    bhist[blockIdx.x * 256 + threadIdx.x] = h[threadIdx.x];
+    if (samples_all) bhist_all[blockIdx.x * 256 + threadIdx.x] = ha[threadIdx.x];
+  }
 }
 
-// One selection's threshold job: its samples, sample rank, control block and K.
+// One selection's threshold job: its samples, their per-block histograms, the second round's
+// per-block histograms, the sample rank and the control block.
 struct TauJob {
   const uint32_t* samples;
+  const uint32_t* bhist;
+  uint32_t* bhist2;
   int q;
   SelCtrl* c;
-  int64_t K;
 };
 
-// Set-up and threshold of the sampled path, one block of 1024 threads per selection (block b
-// takes job b): the control block and (block 0) the region counts are cleared (as sel_init_kernel
-// does), each thread takes 32 of the samples, and the top 16 bits of the q-th largest sample
-// (1-based) are found by 2 digit rounds over per-warp shared histograms; tau0 := those bits (the
-// lower edge of the sample quantile's bin).
-__global__ void __launch_bounds__(1024) sel_sample_tau_kernel(TauJob j0, TauJob j1,
-                                                              uint32_t* ccnt, int G) {
-  constexpr int PER = SAMPLE_S / 1024;
-  __shared__ uint32_t wh[32][257];
+// The threshold of the sampled path: the top 16 bits of the q-th largest sample (1-based), found
+// in two digit rounds by TAU_BLOCKS blocks of 1024 threads per selection (blocks [TAU_BLOCKS j,
+// TAU_BLOCKS (j + 1)) take job j). Every block sums the sample blocks' first-digit histograms
+// (four threads per bin, 32 histograms each) and picks the first digit; each then counts the
+// second digit of the samples of its own slice that carry the first, and the last block to finish
+// sums those counts and picks the second. tau0 := the two digits (the lower edge of the sample
+// quantile's bin).
+constexpr int TAU_THREADS = 1024;
+__global__ void __launch_bounds__(TAU_THREADS) sel_sample_tau_kernel(TauJob j0, TauJob j1) {
+  constexpr int PARTS = TAU_THREADS / 256;
+  __shared__ uint32_t part[PARTS][256];
   __shared__ uint32_t hist[256];
   __shared__ uint32_t s_prefix, s_krem;
-  const TauJob& jb = blockIdx.x ? j1 : j0;
-  const uint32_t* __restrict__ samples = jb.samples;
+  __shared__ bool last;
+  const bool second = blockIdx.x >= TAU_BLOCKS;
+  const TauJob& jb = second ? j1 : j0;
+  const int bid = (int)blockIdx.x - (second ? TAU_BLOCKS : 0);
   SelCtrl* c = jb.c;
-  const int q = jb.q;
-  const int64_t K = jb.K;
-  const int wid = threadIdx.x >> 5;
+  const int wid = threadIdx.x >> 5, bin = threadIdx.x & 255, pr = threadIdx.x >> 8;
+  {
+    constexpr int PER_PART = SAMPLE_BLOCKS / PARTS;
+    uint32_t t = 0;
+#pragma unroll
+    for (int b = 0; b < PER_PART; ++b) t += __ldg(jb.bhist + (pr * PER_PART + b) * 256 + bin);
+    part[pr][bin] = t;
+  }
+  if (threadIdx.x == 0) {
+    s_prefix = 0;
+    s_krem = (uint32_t)jb.q;
+  }
+  __syncthreads();
+  if (threadIdx.x < 256) {
+    uint32_t t = 0;
+#pragma unroll
+    for (int r = 0; r < PARTS; ++r) t += part[r][threadIdx.x];
+    hist[threadIdx.x] = t;
+  }
+  __syncthreads();
+  if (wid == 0) pick_digit_warp(hist, &s_krem, &s_prefix, round_shift(0));
+  __syncthreads();
+  const uint32_t d0 = s_prefix >> round_shift(0);
+  if (threadIdx.x < 256) hist[threadIdx.x] = 0;
+  __syncthreads();
+  constexpr int PER = SAMPLE_S / TAU_BLOCKS / TAU_THREADS;
   uint32_t key[PER];
 #pragma unroll
-  for (int j = 0; j < PER; ++j) key[j] = samples[j * 1024 + threadIdx.x];
-  for (int i = threadIdx.x; i < MAX_BINS; i += blockDim.x) c->hist[i] = 0;
-  if (blockIdx.x == 0)
-    for (int i = threadIdx.x; i < G; i += blockDim.x) ccnt[i] = 0;
-  if (threadIdx.x == 0) {
-    c->tau0 = 0;
-    c->mode = 0;
-    c->overflow = 0;
-    c->ticket = 0;
-    c->total = 0;
-    c->prefix = 0;
-    c->k_rem = (uint32_t)K;
-    c->n_swapped = 0;
-    c->r0_done = 0;
-    s_prefix = 0;
-    s_krem = (uint32_t)q;
-  }
-  // the top 16 bits of the q-th largest sample: tau0 is the lower edge of its 2^15-wide bin, a
-  // little below the sample quantile, so the candidates only gain the keys of that bin
-  for (int r = 0; r < 2; ++r) {
-    const int shift = round_shift(r), bits = round_bits(r);
-    const uint32_t dmask = (1u << bits) - 1;
-    for (int i = threadIdx.x; i < 32 * 257; i += blockDim.x) (&wh[0][0])[i] = 0;
-    __syncthreads();
-    const uint32_t prefix = s_prefix;
-    const int hs = shift + bits;
+  for (int j = 0; j < PER; ++j)
+    key[j] = __ldg(jb.samples + (bid * PER + j) * TAU_THREADS + threadIdx.x);
 #pragma unroll
-    for (int j = 0; j < PER; ++j)
-      if (hs >= 32 || (key[j] >> hs) == (prefix >> hs))
-        atomicAdd(&wh[wid][(key[j] >> shift) & dmask], 1u);
-    __syncthreads();
-    if (threadIdx.x < 256) {
-      uint32_t t = 0;
-#pragma unroll 8
-      for (int w = 0; w < 32; ++w) t += wh[w][threadIdx.x];
-      hist[threadIdx.x] = t;
-    }
-    __syncthreads();
-    if (wid == 0) pick_digit_warp(hist, &s_krem, &s_prefix, shift);
-    __syncthreads();
+  for (int j = 0; j < PER; ++j)
+    if ((key[j] >> round_shift(0)) == d0) atomicAdd(&hist[(key[j] >> round_shift(1)) & 255u], 1u);
+  __syncthreads();
+  if (threadIdx.x < 256) jb.bhist2[bid * 256 + threadIdx.x] = hist[threadIdx.x];
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(&c->ticket, 1u) == TAU_BLOCKS - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  if (threadIdx.x < 256) {
+    uint32_t t = 0;
+#pragma unroll
+    for (int b = 0; b < TAU_BLOCKS; ++b) t += __ldcg(jb.bhist2 + b * 256 + threadIdx.x);
+    hist[threadIdx.x] = t;
   }
-  if (threadIdx.x == 0) c->tau0 = s_prefix;
+  __syncthreads();
+  if (wid == 0) pick_digit_warp(hist, &s_krem, &s_prefix, round_shift(1));
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    c->tau0 = s_prefix;
+    c->ticket = 0;
+  }
 }
 
 // The one pass over g: every warp compacts the (key, index) pairs with key >= tau0 (and not
@@ -851,11 +901,12 @@ usaf_status run_select(const SelPlan& p, const SelWs& w, Src s, int64_t K, int64
   if (p.sampling && !fixed_drop) {
     {
       USAF_TRACE("select_sample", st);
-      sel_sample_kernel<<<SAMPLE_BLOCKS, SAMPLE_S / SAMPLE_BLOCKS, 0, st>>>(s.g, s.n, s.excl,
-                                                                             w.samples, nullptr);
+      sel_sample_kernel<<<SAMPLE_BLOCKS, 1024, 0, st>>>(s.g, s.n, s.excl, w.samples, w.bhist,
+                                                         nullptr, nullptr, w.ctrl, K, nullptr, 0,
+                                                         w.ccnt, p.G);
       USAF_CHECK_LAUNCH();
-      const TauJob job{w.samples, p.q, w.ctrl, K};
-      sel_sample_tau_kernel<<<1, 1024, 0, st>>>(job, job, w.ccnt, p.G);
+      const TauJob job{w.samples, w.bhist, w.bhist2, p.q, w.ctrl};
+      sel_sample_tau_kernel<<<TAU_BLOCKS, TAU_THREADS, 0, st>>>(job, job);
       USAF_CHECK_LAUNCH();
     }
     USAF_TRACE("select_compact", st);
@@ -1285,6 +1336,8 @@ void fused_layout(const FusedPlan& f, Carver& c, SelWs& ws, SelWs& wg) {
   wg.base_gt = c.take<uint32_t>(f.p.G);
   wg.base_eq = c.take<uint32_t>(f.p.G);
   wg.samples = c.take<uint32_t>(SAMPLE_S);
+  wg.bhist = c.take<uint32_t>(SAMPLE_S / 1024 * 256);
+  wg.bhist2 = c.take<uint32_t>(TAU_BLOCKS * 256);
 }
 
 }  // namespace
@@ -1336,13 +1389,13 @@ usaf_status select_and_swap_launch(const float* g, int64_t N, int64_t Ksel, int6
     USAF_TRY(active_bitmap(act_idx, K, N, bitmap, dev_status, st));
     {
       USAF_TRACE("select_sample", st);
-      sel_sample_kernel<<<SAMPLE_BLOCKS, SAMPLE_S / SAMPLE_BLOCKS, 0, st>>>(g, N, bitmap,
-                                                                             w2s.samples,
-                                                                             w1s.samples);
+      sel_sample_kernel<<<SAMPLE_BLOCKS, 1024, 0, st>>>(g, N, bitmap, w2s.samples, w2s.bhist,
+                                                         w1s.samples, w1s.bhist, w2s.ctrl, D,
+                                                         w1s.ctrl, Ksel, w1s.ccnt, p.G);
       USAF_CHECK_LAUNCH();
-      const TauJob js{w1s.samples, f.q_sel, w1s.ctrl, Ksel};
-      const TauJob jg{w2s.samples, f.q_grow, w2s.ctrl, D};
-      sel_sample_tau_kernel<<<2, 1024, 0, st>>>(js, jg, w1s.ccnt, p.G);
+      const TauJob js{w1s.samples, w1s.bhist, w1s.bhist2, f.q_sel, w1s.ctrl};
+      const TauJob jg{w2s.samples, w2s.bhist, w2s.bhist2, f.q_grow, w2s.ctrl};
+      sel_sample_tau_kernel<<<2 * TAU_BLOCKS, TAU_THREADS, 0, st>>>(js, jg);
       USAF_CHECK_LAUNCH();
     }
     {
