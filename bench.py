@@ -105,20 +105,23 @@ def algorithmic(cfg, sddmm_pairs=None):
     return fl, by
 
 
-def kernel_units(cfg, sddmm_pairs=None):
+def kernel_units(cfg, sddmm_pairs=None, split=None):
     """Per-launch algorithmic work of the main kernels: (flops, HBM bytes).
 
     Tensor-core GEMMs count 2*M*N*K over the routed rows (no padding) and each operand read or
     result written once; the gathers count one read of the source rows and one write of the
     transposed rows; the masked expert gradient counts 2 flops per (active entry, routed token)
     pair (`sddmm_pairs`, from the live routing) and one read of its four operands, the active
-    indices and the gradient it writes.
+    indices and the gradient it writes. With `split` (from `masked_split`: the experts whose
+    entries the masked-gradient plan reads out of dense tensor-core tiles), the masked-gradient
+    kernel counts only the other experts, and the two dense-tile kernels count each listed
+    expert's whole gradient (2 * rows * cols * routed rows) and one read of its operands.
     """
     T, H, E, k, I, K = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I, cfg.K
     R = T * k
     Wgu, Wd = E * 2 * I * H * 2, E * H * I * 2
     pairs = sddmm_pairs if sddmm_pairs is not None else K * R / E
-    return {
+    units = {
         "tc_gate_up_swiglu": (2 * R * 2 * I * H, Wgu + R * H * 2 + R * 2 * I * 2 + R * I * 2),
         "tc_down_combine": (2 * R * I * H, Wd + R * I * 2),
         "tc_gvec_swiglu_bwd": (2 * R * I * H, Wd + R * H * 2 + 2 * R * 2 * I * 2),
@@ -127,6 +130,36 @@ def kernel_units(cfg, sddmm_pairs=None):
         "gather_dy": (0, T * H * 2 + R * H * 2),
         "wgrad_sddmm": (2 * pairs, R * (2 * I + H + H + I) * 2 + K * (8 + 4)),
     }
+    if split is not None and split["dense"].any():
+        n, kgu, kd, dense = split["rows"], split["k_gu"], split["k_down"], split["dense"]
+        sp = ~dense
+        rows_sp = int(n[sp & ((kgu + kd) > 0)].sum())
+        k_sp = int((kgu + kd)[sp].sum())
+        units["wgrad_sddmm"] = (2 * int((n * (kgu + kd))[sp].sum()),
+                                rows_sp * (2 * I + H + H + I) * 2 + k_sp * (8 + 4))
+        nd = int(n[dense].sum())
+        units["tc_wgrad_gather_gate_up"] = (2 * nd * 2 * I * H,
+                                            nd * (2 * I + H) * 2 + int(kgu[dense].sum()) * 12)
+        units["tc_wgrad_gather_down"] = (2 * nd * H * I,
+                                         nd * (H + I) * 2 + int(kd[dense].sum()) * 12)
+    return units
+
+
+def masked_split(layer, cfg):
+    """Per expert: routed rows, active entries in gate_up and in down, and whether the layer's
+    masked-gradient plan lists it (at least dense_density * 3*I*H active entries, bf16 layers
+    with a non-empty plan)."""
+    import numpy as np
+    a = layer.act
+    gu = a < cfg.N_gu
+    e = torch.where(gu, a // (2 * cfg.I * cfg.H), (a - cfg.N_gu) // (cfg.H * cfg.I))
+    kgu = torch.bincount(e[gu], minlength=cfg.E).cpu().numpy()
+    kd = torch.bincount(e[~gu], minlength=cfg.E).cpu().numpy()
+    dense = np.zeros(cfg.E, bool)
+    if getattr(layer, "n_dense", 0):
+        dense = (kgu + kd) >= layer.dense_density * 3 * cfg.I * cfg.H
+    return {"rows": layer.rt.expert_count.to(torch.int64).cpu().numpy(), "k_gu": kgu, "k_down": kd,
+            "dense": dense}
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of one ncu capture of the
@@ -502,7 +535,7 @@ def run_steps(args, B, MoELayer, dist, ws, rank, local, dev, cfg, inp, x, dy, wg
     B.trace_enable(False)
     tot = sum(t for _, _, t in trace)
     pairs = sddmm_pairs(layer, cfg)
-    units = kernel_units(cfg, pairs)
+    units = kernel_units(cfg, pairs, masked_split(layer, cfg))
     dominant = max(trace, key=lambda r: r[2])
     name, nl, tms = dominant
     avg_ms = tms / nl

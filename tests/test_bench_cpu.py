@@ -80,6 +80,32 @@ def test_kernel_bytes_match_the_operands(bench):
     assert u["tc_down_combine"][0] == u["tc_gvec_swiglu_bwd"][0] == 2 * 32_768 * 768 * 2048
 
 
+def test_masked_gradient_units_split_between_the_two_kernels(bench):
+    """With the plan listing some experts, the masked-gradient kernel counts only the others'
+    pairs and operands; the dense-tile kernels count the listed experts' whole gradients."""
+    import numpy as np
+    E = CFG.E
+    rows = np.full(E, CFG.T * CFG.k // E, np.int64)
+    kgu = np.full(E, 10, np.int64)
+    kd = np.full(E, 5, np.int64)
+    dense = np.zeros(E, bool)
+    dense[:3] = True
+    kgu[:3] = 100_000
+    kd[:3] = 50_000
+    split = {"rows": rows, "k_gu": kgu, "k_down": kd, "dense": dense}
+    u = bench.kernel_units(CFG, int((rows * (kgu + kd)).sum()), split)
+    n = 256
+    I, H = CFG.I, CFG.H
+    assert u["wgrad_sddmm"][0] == 2 * n * 15 * (E - 3)
+    assert u["wgrad_sddmm"][1] == n * (E - 3) * (2 * I + H + H + I) * 2 + 15 * (E - 3) * 12
+    assert u["tc_wgrad_gather_gate_up"][0] == 2 * 3 * n * 2 * I * H
+    assert u["tc_wgrad_gather_down"][0] == 2 * 3 * n * H * I
+    assert u["tc_wgrad_gather_gate_up"][1] == 3 * n * (2 * I + H) * 2 + 300_000 * 12
+    # no listed expert: the masked-gradient kernel counts everything, as without a split
+    split["dense"] = np.zeros(E, bool)
+    assert bench.kernel_units(CFG, 7, split) == bench.kernel_units(CFG, 7)
+
+
 def test_traffic_is_reported_only_for_captured_kernels(bench):
     assert bench.ncu_traffic("gather_x") is None
     assert set(bench.NCU_TRAFFIC) <= set(bench.kernel_units(CFG))

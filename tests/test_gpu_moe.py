@@ -121,6 +121,38 @@ def test_small_bf16_layers(dims):
     compare(cfg, got, idx, b, g, 1e-2)
 
 
+# experts averaging more than 1,024 routed rows take the masked gradient's long-row walk (the
+# weight row's vectors kept in a per-warp cache across its adjacent entries): about 2,050 tokens
+# per expert (ragged last vectors), about 3,500 (more passes than the cache holds), and a dense
+# mask whose rows run across several groups of entries
+LONG_ROWS = [
+    (dict(T=4100, H=128, E=4, k=2, I=128), 0.05),
+    (dict(T=7000, H=192, E=4, k=2, I=128), 0.05),
+    (dict(T=4100, H=128, E=4, k=2, I=64), 0.6),
+]
+
+
+@pytest.mark.parametrize("dims,frac", LONG_ROWS)
+def test_long_row_masked_gradient(dims, frac):
+    dev = device()
+    cfg = synth.small_config("long", bf16=True, frac=frac, dy_std=1e-2, **dims)
+    inp = synth.moe_inputs(cfg, seed=6)
+    logits = oracle.router_logits(inp["x"], inp["w_router"])
+    act = synth.uniform_mask(cfg.N, cfg.K, seed=6)
+    got = run_layer(cfg, inp, act, logits, dev)
+    assert (got["count"] > 1024).all()
+    idx, b, g = oracle_layer(cfg, inp, act, logits)
+    compare(cfg, got, idx, b, g, 1e-2)
+    # entry by entry against the bf16-emulating oracle: what is left is the fp32 accumulation
+    # over a few thousand tokens and the odd dh element whose bf16 rounding falls the other way
+    # (measured: about 1e-3 of the gradients' RMS at most), while an entry that read another
+    # row's vectors would be off by about the RMS itself
+    idx, w = oracle.route_topk(logits, cfg.k)
+    ge = oracle.masked_expert_grad(act, inp["x"], inp["w_gate_up"], inp["w_down"], idx, w,
+                                   inp["dy"], rnd=oracle.bf16_round)
+    assert np.abs(got["g_act"] - ge).max() <= 2e-2 * np.sqrt(np.mean(ge ** 2))
+
+
 @pytest.mark.parametrize("dims", SMALL_BF16)
 def test_small_bf16_layers_against_the_bf16_emulating_oracle(dims):
     """The same layers against the oracle's bf16-emulating mode (h, w*A and dh rounded to bf16
