@@ -166,8 +166,8 @@ def masked_split(layer, cfg):
 # kernel on this workload (profiles/), with the SHA-256 of the source file at capture time; a
 # kernel whose source has changed since reports traffic null.
 NCU_TRAFFIC = {
-    "wgrad_sddmm": (452653568 + 14011904, "sparse_moe_fine_gb300/csrc/moe.cu",
-                    "0f3dd5f8893a392c9b3c0e9ccf074ccab5753ac924ea76f716bcedc8857f1235"),
+    "wgrad_sddmm": (456482560 + 13689344, "sparse_moe_fine_gb300/csrc/moe.cu",
+                    "a16abe7656b4c7ffbad0b605d80699cd11cb1e2aea57bcd7e18144c23ab1d75a"),
     "tc_gate_up_swiglu": (946807808 + 140072704, "sparse_moe_fine_gb300/csrc/moe_tc.cu",
                           "09b3f6edd25128d85ed5df16d125b3f4c7f081890aea944cce53f1f7891ea79c"),
     "tc_dx": (1122077000 + 156789504, "sparse_moe_fine_gb300/csrc/moe_tc.cu",
