@@ -184,6 +184,30 @@ usaf_status usaf_moe_fwd_wait(const usaf_moe_shape* shape, usaf_dtype dtype, con
                               void* weights_ready, uint32_t* dev_status, void* ws,
                               size_t ws_bytes, void* stream);
 
+/* usaf_moe_fwd_wait2 - usaf_moe_fwd_wait with one event per weight tensor: the gate_up GEMM waits
+ * for gate_up_ready, the down GEMM for down_ready (either may be NULL), so an optimizer update of
+ * w_down (issued after that of w_gate_up, on another stream) overlaps the gate_up GEMM. Same
+ * results and errors as usaf_moe_fwd. */
+usaf_status usaf_moe_fwd_wait2(const usaf_moe_shape* shape, usaf_dtype dtype, const void* x,
+                               const void* w_gate_up, const void* w_down, const usaf_routing* rt,
+                               void* x_perm_save, void* h_save, void* wa_save, void* y,
+                               void* gate_up_ready, void* down_ready, uint32_t* dev_status,
+                               void* ws, size_t ws_bytes, void* stream);
+
+/* usaf_moe_fwd_stage - the stages of usaf_moe_fwd run on their own, for callers that order other
+ * work between them (one CUDA graph per stage, say, with waits for a weight update between their
+ * replays). stages is a bit set: 1 the token gather into x_perm_save (it also clears the combine
+ * accumulator and writes the tile plan, in ws), 2 the gate_up GEMM + SwiGLU (h_save, wa_save),
+ * 4 the down GEMM and the combine into y; 7 is usaf_moe_fwd. A later stage reads what the earlier
+ * ones left in x_perm_save, h_save, wa_save and ws: run them in order, on one stream, with the
+ * same routing and workspace. fp32 layers run stages 2 and 4 only together (UNSUPPORTED
+ * otherwise). Errors: INVALID_ARG (stages outside 1..7), the errors of usaf_moe_fwd. */
+usaf_status usaf_moe_fwd_stage(const usaf_moe_shape* shape, usaf_dtype dtype, const void* x,
+                               const void* w_gate_up, const void* w_down, const usaf_routing* rt,
+                               void* x_perm_save, void* h_save, void* wa_save, void* y,
+                               int stages, uint32_t* dev_status, void* ws, size_t ws_bytes,
+                               void* stream);
+
 /* ---------------------------------------------------------------------------------------------
  * usaf_moe_bwd_sparse - sparse backward of the layer for upstream gradient dy = dL/dY.
  * Per slot: gvec = down_proj[e]^T dy[t], dw = <gvec, A>, dA = w*gvec, dgate = dA*up*silu'(gate),
@@ -326,10 +350,13 @@ usaf_status usaf_moe_wgrad_dense(const usaf_moe_shape* shape, usaf_dtype dtype,
  *   lr, beta1, beta2, eps  host scalars; 1-b1, 1-b2 and the bias-corrected step size are formed
  *                in double on the host and passed to the kernel as fp32
  *   step         1-based step count
- *   skip_if_nonfinite  if nonzero, the entry point first scans g, and no entry is updated when
- *                this scan or an earlier call found a non-finite gradient, or an earlier call
- *                timed out or saw a bad active index (any bit of USAF_DEV_SKIP_MASK already set
- *                in *dev_status, e.g. by usaf_moe_bwd_sparse) (the README's NaN step skip)
+ *   skip_if_nonfinite  1: the entry point first scans g, and no entry is updated when this
+ *                scan or an earlier call found a non-finite gradient, or an earlier call timed
+ *                out or saw a bad active index (any bit of USAF_DEV_SKIP_MASK already set in
+ *                *dev_status, e.g. by usaf_moe_bwd_sparse) (the README's NaN step skip);
+ *                2: the same without the scan, for a gradient the caller has scanned whole with
+ *                usaf_scan_nonfinite before updating it in parts (so that a non-finite entry in
+ *                any part skips every part); 0: no check
  *   dev_status   with USAF_DEV_BAD_INDEX already set, no entry is updated whatever
  *                skip_if_nonfinite says (the indices would address memory outside the weights)
  * Errors: INVALID_ARG, CUDA.
@@ -339,6 +366,11 @@ usaf_status usaf_sparse_adam_step(int64_t n, const int64_t* idx, const float* g,
                                   usaf_dtype w_dtype, double lr, double beta1, double beta2,
                                   double eps, int64_t step, int skip_if_nonfinite,
                                   uint32_t* dev_status, void* stream);
+
+/* usaf_scan_nonfinite - sets USAF_DEV_NONFINITE in *dev_status when any of g[0, n) is NaN or
+ * infinite (the scan of usaf_sparse_adam_step's skip_if_nonfinite = 1, on its own).
+ * Errors: INVALID_ARG (n < 0, g NULL with n > 0, dev_status NULL), CUDA. */
+usaf_status usaf_scan_nonfinite(const float* g, int64_t n, uint32_t* dev_status, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
  * usaf_importance_select - the importance phase of the USAF README ("Not all weights matter":

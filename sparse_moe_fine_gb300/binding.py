@@ -79,6 +79,11 @@ _SIGS = {
     "usaf_trace_summary": (_INT, [_P, _INT]),
     "usaf_rigl_swap": (_INT, [_P, _I64, _P, _I64, _I64, _P, _P, _P, _P, _I64, _P, _INT, _P, _P, _P,
                               _P, _P, _P, _P, _SZ, _P]),
+    "usaf_moe_fwd_wait2": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                  _SZ, _P]),
+    "usaf_moe_fwd_stage": (_INT, [_P, _INT, _P, _P, _P, _P, _P, _P, _P, _P, _INT, _P, _P, _SZ,
+                                  _P]),
+    "usaf_scan_nonfinite": (_INT, [_P, _I64, _P, _P]),
     "usaf_select_and_swap_workspace_size": (_SZ, [_I64, _I64, _I64, _I64]),
     "usaf_select_and_swap": (_INT, [_P, _I64, _I64, _P, _P, _I64, _I64, _P, _P, _P, _P, _I64, _P,
                                     _INT, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -233,18 +238,39 @@ def moe_fwd_workspace_size(s: Shape, dt: int) -> int:
 
 
 def moe_fwd(s: Shape, x, w_gate_up, w_down, rt: Routing, x_perm, h, wa, y, ws=None, stream=None,
-            weights_ready=None, dev_status=None):
+            weights_ready=None, dev_status=None, down_ready=None):
     """weights_ready: a recorded torch.cuda.Event that the reads of the expert weights wait for
-    (the token gather before them does not)."""
+    (the token gather before them does not); with down_ready, weights_ready is waited for before
+    the gate_up GEMM and down_ready before the down GEMM (usaf_moe_fwd_wait2)."""
     dt = _dt(x)
     if ws is None:
         ws = _ws(moe_fwd_workspace_size(s, dt), x.device)
     r = rt.c()
-    ev = None if weights_ready is None else ctypes.c_void_p(weights_ready.cuda_event)
-    _check("usaf_moe_fwd_wait", lib().usaf_moe_fwd_wait(
-        ctypes.byref(s), dt, _ptr(x), _ptr(w_gate_up), _ptr(w_down), ctypes.byref(r),
-        _ptr(x_perm), _ptr(h), _ptr(wa), _ptr(y), ev, _ptr(dev_status), _ptr(ws), ws.numel(),
-        _stream(stream)))
+    ev = lambda e: None if e is None else ctypes.c_void_p(e.cuda_event)
+    if down_ready is None:
+        _check("usaf_moe_fwd_wait", lib().usaf_moe_fwd_wait(
+            ctypes.byref(s), dt, _ptr(x), _ptr(w_gate_up), _ptr(w_down), ctypes.byref(r),
+            _ptr(x_perm), _ptr(h), _ptr(wa), _ptr(y), ev(weights_ready), _ptr(dev_status),
+            _ptr(ws), ws.numel(), _stream(stream)))
+    else:
+        _check("usaf_moe_fwd_wait2", lib().usaf_moe_fwd_wait2(
+            ctypes.byref(s), dt, _ptr(x), _ptr(w_gate_up), _ptr(w_down), ctypes.byref(r),
+            _ptr(x_perm), _ptr(h), _ptr(wa), _ptr(y), ev(weights_ready), ev(down_ready),
+            _ptr(dev_status), _ptr(ws), ws.numel(), _stream(stream)))
+
+
+FWD_GATHER, FWD_GATE_UP, FWD_DOWN = 1, 2, 4
+
+
+def moe_fwd_stage(s: Shape, x, w_gate_up, w_down, rt: Routing, x_perm, h, wa, y, stages, ws,
+                  stream=None, dev_status=None):
+    """usaf_moe_fwd_stage: the forward's stages in the bit set `stages` (FWD_GATHER,
+    FWD_GATE_UP, FWD_DOWN), in order, on the workspace the earlier stages used."""
+    r = rt.c()
+    _check("usaf_moe_fwd_stage", lib().usaf_moe_fwd_stage(
+        ctypes.byref(s), _dt(x), _ptr(x), _ptr(w_gate_up), _ptr(w_down), ctypes.byref(r),
+        _ptr(x_perm), _ptr(h), _ptr(wa), _ptr(y), int(stages), _ptr(dev_status), _ptr(ws),
+        ws.numel(), _stream(stream)))
 
 
 def moe_bwd_workspace_size(s: Shape, dt: int, K: int) -> int:
@@ -352,6 +378,13 @@ def sparse_adam_step(idx, g, p, m, v, w_seg0, n_seg0, w_seg1, lr, beta1, beta2, 
         int(n), _ptr(idx), _ptr(g), _ptr(p), _ptr(m), _ptr(v), _ptr(w_seg0), int(n_seg0),
         _ptr(w_seg1), _dt(w_seg0), float(lr), float(beta1), float(beta2), float(eps), int(step),
         int(skip_if_nonfinite), _ptr(dev_status), _stream(stream)))
+
+
+def scan_nonfinite(g, dev_status, stream=None, n=None):
+    """usaf_scan_nonfinite: sets DEV_NONFINITE in dev_status when g[:n] holds a NaN or inf."""
+    n = g.numel() if n is None else n
+    _check("usaf_scan_nonfinite", lib().usaf_scan_nonfinite(_ptr(g), int(n), _ptr(dev_status),
+                                                            _stream(stream)))
 
 
 def importance_select_workspace_size(N: int, K: int) -> int:

@@ -226,11 +226,12 @@ static usaf_status fill_args(MoeArgs& a, const usaf_moe_shape* s, usaf_dtype dt,
   return USAF_OK;
 }
 
-usaf_status usaf_moe_fwd_wait(const usaf_moe_shape* s, usaf_dtype dt, const void* x,
-                              const void* w_gate_up, const void* w_down, const usaf_routing* rt,
-                              void* x_perm_save, void* h_save, void* wa_save, void* y,
-                              void* weights_ready, uint32_t* dev_status, void* ws,
-                              size_t ws_bytes, void* stream) {
+static usaf_status moe_fwd_entry(const usaf_moe_shape* s, usaf_dtype dt, const void* x,
+                                 const void* w_gate_up, const void* w_down,
+                                 const usaf_routing* rt, void* x_perm_save, void* h_save,
+                                 void* wa_save, void* y, void* gate_up_ready, void* down_ready,
+                                 int stages, uint32_t* dev_status, void* ws, size_t ws_bytes,
+                                 void* stream) {
   MoeArgs a{};
   USAF_TRY(fill_args(a, s, dt, x, nullptr, w_gate_up, w_down, rt));
   a.status = dev_status;
@@ -240,8 +241,37 @@ usaf_status usaf_moe_fwd_wait(const usaf_moe_shape* s, usaf_dtype dt, const void
   FwdWs w;
   fwd_ws_layout(*s, dt, c, w);
   return moe_fwd_launch(a, x_perm_save, h_save, wa_save, y, w,
-                        static_cast<cudaEvent_t>(weights_ready),
+                        static_cast<cudaEvent_t>(gate_up_ready),
+                        static_cast<cudaEvent_t>(down_ready), stages,
                         static_cast<cudaStream_t>(stream));
+}
+
+usaf_status usaf_moe_fwd_wait2(const usaf_moe_shape* s, usaf_dtype dt, const void* x,
+                               const void* w_gate_up, const void* w_down, const usaf_routing* rt,
+                               void* x_perm_save, void* h_save, void* wa_save, void* y,
+                               void* gate_up_ready, void* down_ready, uint32_t* dev_status,
+                               void* ws, size_t ws_bytes, void* stream) {
+  return moe_fwd_entry(s, dt, x, w_gate_up, w_down, rt, x_perm_save, h_save, wa_save, y,
+                       gate_up_ready, down_ready, FWD_ALL, dev_status, ws, ws_bytes, stream);
+}
+
+usaf_status usaf_moe_fwd_stage(const usaf_moe_shape* s, usaf_dtype dt, const void* x,
+                               const void* w_gate_up, const void* w_down, const usaf_routing* rt,
+                               void* x_perm_save, void* h_save, void* wa_save, void* y,
+                               int stages, uint32_t* dev_status, void* ws, size_t ws_bytes,
+                               void* stream) {
+  if (stages < 1 || stages > FWD_ALL) return USAF_ERR_INVALID_ARG;
+  return moe_fwd_entry(s, dt, x, w_gate_up, w_down, rt, x_perm_save, h_save, wa_save, y, nullptr,
+                       nullptr, stages, dev_status, ws, ws_bytes, stream);
+}
+
+usaf_status usaf_moe_fwd_wait(const usaf_moe_shape* s, usaf_dtype dt, const void* x,
+                              const void* w_gate_up, const void* w_down, const usaf_routing* rt,
+                              void* x_perm_save, void* h_save, void* wa_save, void* y,
+                              void* weights_ready, uint32_t* dev_status, void* ws,
+                              size_t ws_bytes, void* stream) {
+  return usaf_moe_fwd_wait2(s, dt, x, w_gate_up, w_down, rt, x_perm_save, h_save, wa_save, y,
+                            weights_ready, nullptr, dev_status, ws, ws_bytes, stream);
 }
 
 usaf_status usaf_moe_fwd(const usaf_moe_shape* s, usaf_dtype dt, const void* x,
@@ -426,6 +456,7 @@ usaf_status usaf_sparse_adam_step(int64_t n, const int64_t* idx, const float* g,
   if (n < 0 || step < 1 || !dtype_ok(w_dtype) || n_seg0 < 0) return USAF_ERR_INVALID_ARG;
   if (n > 0 && (!g || !p || !m || !v || !w_seg0)) return USAF_ERR_INVALID_ARG;
   if (!idx && n > n_seg0) return USAF_ERR_INVALID_ARG;
+  if (skip_if_nonfinite < 0 || skip_if_nonfinite > 2) return USAF_ERR_INVALID_ARG;
   if (skip_if_nonfinite && !dev_status) return USAF_ERR_INVALID_ARG;
   if (!(beta1 >= 0.0 && beta1 < 1.0 && beta2 >= 0.0 && beta2 < 1.0 && eps >= 0.0))
     return USAF_ERR_INVALID_ARG;
@@ -433,6 +464,11 @@ usaf_status usaf_sparse_adam_step(int64_t n, const int64_t* idx, const float* g,
   USAF_TRY(debug_validate(idx, n, INT64_MAX, dev_status, stream));
   return adam_launch(n, idx, g, p, m, v, w_seg0, n_seg0, w_seg1, w_dtype, lr, beta1, beta2, eps,
                      step, skip_if_nonfinite, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+usaf_status usaf_scan_nonfinite(const float* g, int64_t n, uint32_t* dev_status, void* stream) {
+  if (n < 0 || (n > 0 && !g) || !dev_status) return USAF_ERR_INVALID_ARG;
+  return nonfinite_scan_launch(g, n, dev_status, static_cast<cudaStream_t>(stream));
 }
 
 size_t usaf_importance_select_workspace_size(int64_t N, int64_t K) {

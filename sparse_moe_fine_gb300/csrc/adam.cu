@@ -94,6 +94,16 @@ usaf_status validate_launch(const int64_t* idx, int64_t K, int64_t N, uint32_t* 
   return USAF_OK;
 }
 
+usaf_status nonfinite_scan_launch(const float* g, int64_t n, uint32_t* dev_status,
+                                  cudaStream_t st) {
+  if (n == 0) return USAF_OK;
+  USAF_TRACE("nonfinite_scan", st);
+  const int64_t blocks = std::min<int64_t>(ceil_div(n, 256), device_sm_count() * 8);
+  nonfinite_scan_kernel<<<(unsigned)blocks, 256, 0, st>>>(g, n, dev_status);
+  USAF_CHECK_LAUNCH();
+  return USAF_OK;
+}
+
 usaf_status adam_launch(int64_t n, const int64_t* idx, const float* g, float* p, float* m,
                         float* v, void* w0, int64_t n0, void* w1, usaf_dtype wdt, double lr,
                         double b1, double b2, double eps, int64_t step, int skip,
@@ -107,7 +117,7 @@ usaf_status adam_launch(int64_t n, const int64_t* idx, const float* g, float* p,
   const auto al = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
   const int vec = al(g) && al(p) && al(m) && al(v) ? 1 : 0;
   const int64_t ublocks = std::max<int64_t>(1, ceil_div(vec ? ceil_div(n, 4) : n, threads));
-  if (skip) {
+  if (skip == 1) {  // 2: the caller scanned (usaf_scan_nonfinite); only the status is checked
     nonfinite_scan_kernel<<<(unsigned)blocks, threads, 0, st>>>(g, n, dev_status);
     USAF_CHECK_LAUNCH();
   }

@@ -80,8 +80,11 @@ usaf_status masked_plan_build_launch(const usaf_moe_shape& s, const int64_t* act
 
 // weights_ready (may be null): the kernels that read the expert weights wait for it; the token
 // gather before them does not
+// forward stages (usaf_moe_fwd_stage)
+constexpr int FWD_GATHER = 1, FWD_GATE_UP = 2, FWD_DOWN = 4, FWD_ALL = 7;
 usaf_status moe_fwd_launch(const MoeArgs& a, void* x_perm, void* h, void* wa, void* y, FwdWs& w,
-                           cudaEvent_t weights_ready, cudaStream_t st);
+                           cudaEvent_t weights_ready, cudaEvent_t down_ready, int stages,
+                           cudaStream_t st);
 // plan / n_dense: the masked-gradient plan of act_idx and its number of dense experts as the
 // host read it (0: every entry by the sparse kernel, plan unused)
 usaf_status moe_bwd_launch(const MoeArgs& a, int renorm, const float* logits, const void* x_perm,
@@ -121,6 +124,8 @@ usaf_status diag_wait_launch(int64_t limit_cycles, uint32_t* status, cudaStream_
 
 
 // ---------------------------------------------------------------- optimizer
+usaf_status nonfinite_scan_launch(const float* g, int64_t n, uint32_t* dev_status,
+                                  cudaStream_t st);
 usaf_status adam_launch(int64_t n, const int64_t* idx, const float* g, float* p, float* m,
                         float* v, void* w0, int64_t n0, void* w1, usaf_dtype wdt, double lr,
                         double b1, double b2, double eps, int64_t step, int skip,

@@ -1171,46 +1171,69 @@ static usaf_status fwd_simt(const MoeArgs& a, T* xT, T* hT, T* waT, float* yacc,
   return USAF_OK;
 }
 
+// Make `st` wait for `ev` (NULL: no wait).
+static usaf_status wait_event(cudaStream_t st, cudaEvent_t ev) {
+  if (!ev) return USAF_OK;
+  return cudaStreamWaitEvent(st, ev, 0) == cudaSuccess ? USAF_OK : USAF_ERR_CUDA;
+}
+
+// The forward's stages (FWD_* bits): the token gather (which also clears the combine accumulator
+// and writes the tile plan), the gate_up GEMM, the down GEMM with the combine into y.
 template <typename T>
 static usaf_status moe_fwd_t(const MoeArgs& a, T* xT, T* hT, T* waT, T* y, FwdWs& w,
-                             cudaEvent_t weights_ready, cudaStream_t st) {
+                             cudaEvent_t weights_ready, cudaEvent_t down_ready, int stages,
+                             cudaStream_t st) {
   const auto& s = a.s;
   const int64_t TH = s.T * s.H;
   MoeArgs aw = a;
   aw.wperm = w.wperm;
-  {
+  if (a.dt != USAF_BF16 && (stages & (FWD_GATE_UP | FWD_DOWN)) != 0 &&
+      (stages & (FWD_GATE_UP | FWD_DOWN)) != (FWD_GATE_UP | FWD_DOWN))
+    return USAF_ERR_UNSUPPORTED;  // the fp32 layers' GEMMs run as one stage
+  if (stages & FWD_GATHER) {
     USAF_TRACE("gather_x", st);
-    // also zeroes the combine accumulator and writes the tile plan
     const GatherExtra ex{w.y_acc, TH, nullptr, 0, a.rt.expert_offset, (int)s.E,
                          a.dt == USAF_BF16 ? w.plan : nullptr};
     USAF_TRY(gather_t<T>(aw, static_cast<const T*>(a.x), xT, st, ex));
   }
-  // the expert weights are read from here on: wait for their last update only now
-  if (weights_ready && cudaStreamWaitEvent(st, weights_ready, 0) != cudaSuccess)
-    return USAF_ERR_CUDA;
+  // the expert weights are read from here on: wait for their last update only now (gate_up's
+  // before its GEMM, down_proj's before the down GEMM)
   if (a.dt == USAF_BF16) {
     MoeArgs b = aw;
     b.plan = w.plan;
-    USAF_TRY(tc_fwd_gate_up(b, xT, hT, waT, st));
-    USAF_TRY(tc_fwd_down(b, waT, w.y_acc, st));
-  } else {
+    if (stages & FWD_GATE_UP) {
+      USAF_TRY(wait_event(st, weights_ready));
+      USAF_TRY(tc_fwd_gate_up(b, xT, hT, waT, st));
+    }
+    if (stages & FWD_DOWN) {
+      USAF_TRY(wait_event(st, down_ready));
+      USAF_TRY(tc_fwd_down(b, waT, w.y_acc, st));
+    }
+  } else if (stages & FWD_GATE_UP) {
+    USAF_TRY(wait_event(st, weights_ready));
+    USAF_TRY(wait_event(st, down_ready));
     USAF_TRY(fwd_simt<T>(a, xT, hT, waT, w.y_acc, st));
   }
-  USAF_TRACE("combine_finalize", st);
-  f32_to_kernel<T><<<grid_dim_for(TH), 256, 0, st>>>(w.y_acc, y, TH);
-  USAF_CHECK_LAUNCH();
+  if (stages & FWD_DOWN) {
+    USAF_TRACE("combine_finalize", st);
+    f32_to_kernel<T><<<grid_dim_for(TH), 256, 0, st>>>(w.y_acc, y, TH);
+    USAF_CHECK_LAUNCH();
+  }
   return USAF_OK;
 }
 
 usaf_status moe_fwd_launch(const MoeArgs& a, void* x_perm, void* h, void* wa, void* y, FwdWs& w,
-                           cudaEvent_t weights_ready, cudaStream_t st) {
+                           cudaEvent_t weights_ready, cudaEvent_t down_ready, int stages,
+                           cudaStream_t st) {
   if (a.dt == USAF_BF16)
     return moe_fwd_t<__nv_bfloat16>(a, static_cast<__nv_bfloat16*>(x_perm),
                                     static_cast<__nv_bfloat16*>(h),
                                     static_cast<__nv_bfloat16*>(wa),
-                                    static_cast<__nv_bfloat16*>(y), w, weights_ready, st);
+                                    static_cast<__nv_bfloat16*>(y), w, weights_ready, down_ready,
+                                    stages, st);
   return moe_fwd_t<float>(a, static_cast<float*>(x_perm), static_cast<float*>(h),
-                          static_cast<float*>(wa), static_cast<float*>(y), w, weights_ready, st);
+                          static_cast<float*>(wa), static_cast<float*>(y), w, weights_ready,
+                          down_ready, stages, st);
 }
 
 // Dense expert weight gradient on CUDA cores (fp32 layers): one thread per entry of

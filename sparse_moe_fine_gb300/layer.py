@@ -85,7 +85,12 @@ class MoELayer:
         # the expert SparseAdam update runs on a side stream, overlapping the next step's routing
         self.side = torch.cuda.Stream(device=d)
         self.ev_bwd = torch.cuda.Event()
+        # the update is issued in two parts, gate_up's entries first: ev_gu marks that part (the
+        # forward's gate_up GEMM waits for it), ev_opt the whole update (its down GEMM waits)
+        self.ev_gu = torch.cuda.Event()
         self.ev_opt = torch.cuda.Event()
+        for e in (self.ev_gu, self.ev_opt):  # create the events now: captured waits need them
+            e.record(self.side)
         self.pending_opt = False
         self.replayed_kernels = 0  # library kernels run by graph replays (graphed_train_step)
         self.ws_route = torch.empty(B.route_topk_workspace_size(self.s), dtype=torch.uint8,
@@ -111,6 +116,9 @@ class MoELayer:
         self.act = act
         K = self.act.numel()
         self.K = K
+        # the first part of the split update: every gate_up entry, rounded up to four entries so
+        # that the second part's state starts on a 16-byte boundary
+        self.k_split = min(K, -(-int((act < self.N_gu).sum().item()) // 4) * 4)
         if p is None:
             flat_gu = self.w_gate_up.reshape(-1)
             flat_d = self.w_down.reshape(-1)
@@ -197,9 +205,10 @@ class MoELayer:
         """The token gather overlaps the last expert update; the GEMMs wait for it."""
         y = self.y if y is None else y
         self._check_tokens(x=x, y=y)
-        ready = self.ev_opt if self.pending_opt else None
+        gu, dn = (self.ev_gu, self.ev_opt) if self.pending_opt else (None, None)
         B.moe_fwd(self.s, x, self.w_gate_up, self.w_down, self.rt, self.x_perm, self.h, self.wa,
-                  y, ws=self.ws_fwd, stream=stream, weights_ready=ready, dev_status=self.status)
+                  y, ws=self.ws_fwd, stream=stream, weights_ready=gu, down_ready=dn,
+                  dev_status=self.status)
         self.pending_opt = False  # the stream is ordered after the update from here on
         return y
 
@@ -230,10 +239,19 @@ class MoELayer:
                 allreduce_grads(self.g_act, self.g_router, self.status, self.group)
         self.ev_bwd.record(main)
         self.side.wait_event(self.ev_bwd)
-        B.sparse_adam_step(self.act, self.g_act, self.p, self.m, self.v, self.w_gate_up,
-                           self.N_gu, self.w_down, self.lr, b1, b2, self.eps, self.step_count,
-                           skip_if_nonfinite, self.status, stream=self.side)
-        self.ev_opt.record(self.side)
+        # one scan of the whole gradient, then the update in two parts that only check the status
+        # word (a non-finite entry anywhere skips both): gate_up's entries, then down_proj's, so
+        # that the next forward's gate_up GEMM waits only for the first part
+        if skip_if_nonfinite:
+            B.scan_nonfinite(self.g_act, self.status, stream=self.side)
+        skip = 2 if skip_if_nonfinite else 0
+        for lo, hi, ev in ((0, self.k_split, self.ev_gu), (self.k_split, self.K, self.ev_opt)):
+            if hi > lo:
+                B.sparse_adam_step(self.act[lo:hi], self.g_act[lo:hi], self.p[lo:hi],
+                                   self.m[lo:hi], self.v[lo:hi], self.w_gate_up, self.N_gu,
+                                   self.w_down, self.lr, b1, b2, self.eps, self.step_count, skip,
+                                   self.status, stream=self.side)
+            ev.record(self.side)
         self.pending_opt = True
         B.sparse_adam_step(None, self.g_router, self.r_p, self.r_m, self.r_v, self.w_router,
                            self.E * self.H, None, self.lr, b1, b2, self.eps, self.step_count,
@@ -257,7 +275,8 @@ class MoELayer:
         """train_step with the routing and the forward + sparse backward replayed from CUDA graphs,
         captured on first use for these x and dy buffers (one pair per status-word parity), so
         their dependent launches run without per-launch gaps. The expert update of the previous
-        step overlaps the routing graph; the forward graph starts after it. The two SparseAdam
+        step overlaps the routing and token-gather graph; the gate_up GEMM's graph waits for the
+        update's gate_up part only, and the rest of the step's graph for its down_proj part. The two SparseAdam
         updates stay ordinary launches, since their step sizes change every step. Outputs are
         the layer's own y and dx buffers. One graph pair is kept per distinct (x, dy) buffer pair
         and parity, so a caller cycles through a fixed set of input buffers."""
@@ -267,12 +286,17 @@ class MoELayer:
         key = (x.data_ptr(), dy.data_ptr(), par)
         if key not in self._graphs:
             self._graphs[key] = self._capture(x, dy, par, main)
-        g_route, g_body, n_kernels = self._graphs[key]
+        g_route, g_up, g_body, n_kernels = self._graphs[key]
         self.status = self.status2[par:par + 1]
         with torch.cuda.stream(main):
-            g_route.replay()
-            self.wait_optimizer(main)
+            g_route.replay()  # routing and the token gather, beside the last expert update
+            if self.pending_opt:
+                main.wait_event(self.ev_gu)
+            g_up.replay()     # the gate_up GEMM, beside the update's down_proj part
+            if self.pending_opt:
+                main.wait_event(self.ev_opt)
             g_body.replay()
+        self.pending_opt = False
         self.replayed_kernels += n_kernels
         self.optimizer_step(main)
         return self.y, self.dx
@@ -281,18 +305,26 @@ class MoELayer:
         status = self.status2[par:par + 1]
         cs = torch.cuda.Stream(device=self.dev)
         cs.wait_stream(main)
-        g_route, g_body = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        g_route, g_up, g_body = (torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph(),
+                                 torch.cuda.CUDAGraph())
         n0 = B.launch_count()
+        fwd = lambda stages: B.moe_fwd_stage(self.s, x, self.w_gate_up, self.w_down, self.rt,
+                                             self.x_perm, self.h, self.wa, self.y, stages,
+                                             self.ws_fwd, stream=cs, dev_status=status)
+        # three graphs, so that the replays can wait for the expert update's two parts between
+        # them: routing + token gather | gate_up GEMM | down GEMM + combine + sparse backward
         with torch.cuda.graph(g_route, stream=cs):
             status.zero_()
             B.route_topk(self.s, x, self.w_router, self.rt, logits_out=self.logits,
                          renorm=self.renorm, dev_status=status, ws=self.ws_route, stream=cs)
+            fwd(B.FWD_GATHER)
+        with torch.cuda.graph(g_up, stream=cs):
+            fwd(B.FWD_GATE_UP)
         with torch.cuda.graph(g_body, stream=cs):
-            B.moe_fwd(self.s, x, self.w_gate_up, self.w_down, self.rt, self.x_perm, self.h,
-                      self.wa, self.y, ws=self.ws_fwd, stream=cs, dev_status=status)
+            fwd(B.FWD_DOWN)
             self.backward_into(x, dy, accumulate=0, dx=self.dx, stream=cs, dev_status=status)
         main.wait_stream(cs)
-        return g_route, g_body, B.launch_count() - n0  # library kernels in the two graphs
+        return g_route, g_up, g_body, B.launch_count() - n0  # library kernels in the graphs
 
     def train_step_host(self, x_host, dy_host, y_host, dx_host, x_dev, dy_dev, stream=None):
         """The same step fed from (pinned) host memory: copy x and dy in, run, copy y and dx out,

@@ -18,7 +18,7 @@ fake_addresses = pytest.mark.skipif(torch.cuda.is_available(),
 def test_library_exports_every_header_symbol():
     L = B.lib()
     syms = B.header_symbols()
-    assert len(syms) == 40
+    assert len(syms) == 43
     for s in syms:
         assert hasattr(L, s), s
     assert L.usaf_abi_version() == 2
@@ -99,6 +99,24 @@ def test_select_and_swap_host_checks():
     assert call(50, 100, 10, sel_ptr=new) == 1  # the selection overlaps the new active set
     assert call(50, 100, 10, new_ptr=act) == 1  # an output overlaps an input
     assert call(50, 100, 10, ws_bytes=16) == 3
+
+
+@fake_addresses
+def test_forward_stage_and_scan_host_checks():
+    L = B.lib()
+    s = B.shape(8, 64, 4, 2, 64)
+    fake = ctypes.c_void_p(256)  # never dereferenced: every call below fails on the host
+    r = B._Routing(*[256] * 7)
+    for bad in (0, 8, -1):  # stage sets outside 1..7
+        assert L.usaf_moe_fwd_stage(ctypes.byref(s), 1, fake, fake, fake, ctypes.byref(r), fake,
+                                    fake, fake, fake, bad, None, fake, 1 << 30, None) == 1
+    assert L.usaf_scan_nonfinite(fake, -1, fake, None) == 1
+    assert L.usaf_scan_nonfinite(None, 4, fake, None) == 1
+    assert L.usaf_scan_nonfinite(fake, 4, None, None) == 1
+    assert L.usaf_scan_nonfinite(None, 0, fake, None) == 0  # nothing to scan
+    # skip modes beyond 2 are refused
+    assert L.usaf_sparse_adam_step(4, None, fake, fake, fake, fake, fake, 4, None, 0, 1e-3, 0.9,
+                                   0.999, 1e-8, 1, 3, fake, None) == 1
 
 
 def test_capacity_and_workspace_queries():

@@ -353,6 +353,77 @@ def test_fwd_waits_for_weights_ready():
     assert rel_l2(y_old.float().cpu().numpy(), y_new.float().cpu().numpy()) > 1e-2
 
 
+def test_fwd_stages_and_split_waits():
+    """usaf_moe_fwd_stage: the gather, gate_up and down stages run one by one give the forward
+    bit for bit; usaf_moe_fwd_wait2: the down GEMM waits for its own event, here recorded behind
+    a delayed update of w_down while the gate_up event is already complete; an fp32 layer refuses
+    its GEMM stages apart."""
+    dev = device()
+    cfg = synth.small_config("stages", T=256, H=128, E=8, k=2, I=64, bf16=True)
+    inp = synth.moe_inputs(cfg, seed=7)
+    s = B.shape(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I)
+    x = to_dev(inp["x"], dev, True)
+    wr = to_dev(inp["w_router"], dev)
+    wgu = to_dev(inp["w_gate_up"], dev, True)
+    wd = to_dev(inp["w_down"], dev, True)
+    rt = B.Routing.empty(s, dev)
+    B.route_topk(s, x, wr, rt)
+    cap = B.routed_rows_capacity(s)
+    bufs = lambda: (torch.empty(cfg.H, cap, dtype=torch.bfloat16, device=dev),
+                    torch.empty(2 * cfg.I, cap, dtype=torch.bfloat16, device=dev),
+                    torch.empty(cfg.I, cap, dtype=torch.bfloat16, device=dev),
+                    torch.empty(cfg.T, cfg.H, dtype=torch.bfloat16, device=dev))
+    ws = torch.empty(B.moe_fwd_workspace_size(s, B.BF16), dtype=torch.uint8, device=dev)
+    full = bufs()
+    B.moe_fwd(s, x, wgu, wd, rt, *full, ws=ws)
+    staged = bufs()
+    for st in (B.FWD_GATHER, B.FWD_GATE_UP, B.FWD_DOWN):
+        B.moe_fwd_stage(s, x, wgu, wd, rt, *staged, st, ws)
+    torch.cuda.synchronize()
+    off, cnt = rt.expert_offset.cpu(), rt.expert_count.cpu()
+    cols = torch.cat([torch.arange(int(off[e]), int(off[e]) + int(cnt[e]))
+                      for e in range(cfg.E)]).to(dev)  # the routed rows (not the padding)
+    for a, b in zip(full[:3], staged[:3]):
+        assert torch.equal(a[:, cols], b[:, cols])
+    assert torch.equal(full[3], staged[3])
+    # the down GEMM waits for down_ready
+    wd_new = wd * 2
+    side = torch.cuda.Stream(device=dev)
+    ev_gu, ev_d = torch.cuda.Event(), torch.cuda.Event()
+    with torch.cuda.stream(side):
+        ev_gu.record(side)
+        torch.cuda._sleep(100_000_000)  # tens of milliseconds: the update lands late
+        wd.copy_(wd_new)
+        ev_d.record(side)
+    got = bufs()
+    B.moe_fwd(s, x, wgu, wd, rt, *got, weights_ready=ev_gu, down_ready=ev_d)
+    torch.cuda.synchronize()
+    want = bufs()
+    B.moe_fwd(s, x, wgu, wd_new, rt, *want)
+    old = bufs()
+    B.moe_fwd(s, x, wgu, wd_new / 2, rt, *old)
+    torch.cuda.synchronize()
+    assert rel_l2(got[3].float().cpu().numpy(), want[3].float().cpu().numpy()) <= 1e-4
+    assert rel_l2(old[3].float().cpu().numpy(), want[3].float().cpu().numpy()) > 1e-2
+    # fp32 layers: the two GEMMs form one stage
+    cf = synth.small_config("stages32", T=64, H=64, E=4, k=2, I=64, bf16=False)
+    i32 = synth.moe_inputs(cf, seed=7)
+    s32 = B.shape(cf.T, cf.H, cf.E, cf.k, cf.I)
+    x32 = to_dev(i32["x"], dev)
+    rt32 = B.Routing.empty(s32, dev)
+    B.route_topk(s32, x32, to_dev(i32["w_router"], dev), rt32)
+    c32 = B.routed_rows_capacity(s32)
+    b32 = (torch.empty(cf.H, c32, device=dev), torch.empty(2 * cf.I, c32, device=dev),
+           torch.empty(cf.I, c32, device=dev), torch.empty(cf.T, cf.H, device=dev))
+    ws32 = torch.empty(B.moe_fwd_workspace_size(s32, B.F32), dtype=torch.uint8, device=dev)
+    B.moe_fwd_stage(s32, x32, to_dev(i32["w_gate_up"], dev), to_dev(i32["w_down"], dev), rt32,
+                    *b32, B.FWD_GATHER, ws32)
+    with pytest.raises(B.UsafError):
+        B.moe_fwd_stage(s32, x32, to_dev(i32["w_gate_up"], dev), to_dev(i32["w_down"], dev),
+                        rt32, *b32, B.FWD_GATE_UP, ws32)
+    torch.cuda.synchronize()
+
+
 def run_dense(cfg, inp, logits, dev, twice=False):
     """Route, forward and the dense backward; with twice=True a second call accumulates."""
     s = B.shape(cfg.T, cfg.H, cfg.E, cfg.k, cfg.I)
