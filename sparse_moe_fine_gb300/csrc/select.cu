@@ -411,6 +411,13 @@ __global__ void __launch_bounds__(TAU_THREADS) sel_sample_tau_kernel(TauJob j0, 
 // key set; the first-digit histogram and count of the excluded ones are kept apart, and `cg`
 // receives the differences (the non-excluded candidates').
 enum { EX_NONE = 0, EX_SKIP = 1, EX_TAG = 2 };
+
+// max of a and b, NaN when either is NaN (max.NaN)
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
 template <int EX>
 __global__ void __launch_bounds__(COMPACT_WARPS * 32) sel_compact_kernel(
     const float* __restrict__ g, int64_t N, int64_t L, const uint32_t* __restrict__ excl,
@@ -427,6 +434,10 @@ __global__ void __launch_bounds__(COMPACT_WARPS * 32) sel_compact_kernel(
   }
   __syncthreads();
   const uint32_t tau0 = TAG ? min(c->tau0, cg->tau0) : c->tau0;
+  // a group is examined when some |x| >= tau0 as floats, or is NaN: a superset of the groups
+  // holding a key >= tau0 (a threshold in the NaN range tests against +inf; the exact integer key
+  // test follows). Every non-finite element's group is examined, so the flag is set there.
+  const float tau_f = __uint_as_float(min(tau0, 0x7F800000u));
   const int lane = threadIdx.x & 31;
   const uint32_t below = (1u << lane) - 1u;
   const int64_t r = (int64_t)blockIdx.x * COMPACT_WARPS + (threadIdx.x >> 5);
@@ -434,7 +445,7 @@ __global__ void __launch_bounds__(COMPACT_WARPS * 32) sel_compact_kernel(
   const int64_t hi = min(N, lo + L);
   uint32_t* rk = ckeys + r * cap;
   uint32_t* ri = cids + r * cap;
-  uint32_t count = 0, count_x = 0, kmax = 0;  // kmax: largest key seen, for the non-finite check
+  uint32_t count = 0, count_x = 0, kmax = 0;  // kmax: largest key of the examined groups
   bool over = false;
   // lane l < 16: the bitmap word of elements [t + 32 l, t + 32 l + 32) (words past hi are not read)
   auto load_bw = [&](int64_t t) -> uint32_t {
@@ -474,11 +485,12 @@ __global__ void __launch_bounds__(COMPACT_WARPS * 32) sel_compact_kernel(
     const bool full = t0 + STEP <= hi;  // no range tests
 #pragma unroll
     for (int u = 0; u < UN; ++u) {
+      const float f4 = max_nan(max_nan(fabsf(cur[u][0]), fabsf(cur[u][1])),
+                               max_nan(fabsf(cur[u][2]), fabsf(cur[u][3])));
+      if (!__any_sync(0xffffffffu, !(f4 < tau_f))) continue;  // elements past hi read as 0
       const uint32_t key[4] = {abs_key(cur[u][0]), abs_key(cur[u][1]), abs_key(cur[u][2]),
                                abs_key(cur[u][3])};
-      const uint32_t m4 = max(max(key[0], key[1]), max(key[2], key[3]));
-      kmax = max(kmax, m4);  // elements past hi read as 0
-      if (!__any_sync(0xffffffffu, m4 >= tau0)) continue;
+      kmax = max(kmax, max(max(key[0], key[1]), max(key[2], key[3])));
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int64_t i = t0 + u * 128 + j * 32 + lane;

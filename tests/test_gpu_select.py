@@ -59,6 +59,32 @@ def test_select_sampled_path_with_threshold_ties():
     assert st & B.DEV_SELECT_EXACT_PATH == 0
 
 
+def test_select_with_nonfinite_gradients():
+    """NaN and infinite magnitudes rank above every finite one (the key is the bit pattern with the
+    sign cleared: a NaN above inf), and the call flags the non-finite gradient: a few of each on
+    the sampled path, then so many NaNs that the threshold falls among them."""
+    dev = device()
+    n = 1 << 23
+    g = synth.student_t3(n, seed=4)
+    K = math.ceil(0.005 * n)
+    rng = np.random.default_rng(4)
+    pos = rng.choice(n, 200, replace=False)
+    g[pos[:100]] = np.inf
+    g[pos[100:150]] = -np.inf
+    g[pos[150:]] = np.nan
+    got, st = gpu_select(g, K, dev)
+    assert (got == oracle.importance_select_threshold(g, K)).all()
+    assert st & B.DEV_NONFINITE
+    g2 = g.copy()
+    g2[rng.choice(n, 2 * K, replace=False)] = np.nan
+    got, st = gpu_select(g2, K, dev)
+    assert (got == oracle.importance_select_threshold(g2, K)).all()
+    assert st & B.DEV_NONFINITE
+    # no non-finite value: no flag
+    _, st = gpu_select(synth.student_t3(n, seed=5), K, dev)
+    assert not st & B.DEV_NONFINITE
+
+
 @pytest.mark.parametrize("kind", ["sorted", "constant"])
 def test_select_adversarial_inputs_take_exact_path(kind):
     dev = device()
