@@ -229,6 +229,11 @@ usaf_status usaf_moe_fwd_stage(const usaf_moe_shape* shape, usaf_dtype dtype, co
  *   dev_status   gets USAF_DEV_NONFINITE if any produced gradient is NaN/Inf, USAF_DEV_TIMEOUT if
  *                a tensor-core kernel gave up a wait, USAF_DEV_BAD_INDEX if an active index does
  *                not address an expert weight (that entry's g_act is left 0) (may be NULL)
+ * bf16 layers with renorm = 1 form g_router on a side stream of the library (one per calling
+ * thread and device, created by usaf_moe_bwd_workspace_size or by an uncaptured call and kept for
+ * the thread's life), forked from `stream` after dlogit and joined back before the call returns:
+ * the call's work as a whole stays ordered on `stream`, and in a stream capture it becomes two
+ * branches of the graph. A call captured on a thread that has no side stream yet runs it in line.
  * Errors: INVALID_ARG, UNSUPPORTED, WORKSPACE, CUDA.
  * ------------------------------------------------------------------------------------------- */
 size_t usaf_moe_bwd_workspace_size(const usaf_moe_shape* shape, usaf_dtype dtype, int64_t K);

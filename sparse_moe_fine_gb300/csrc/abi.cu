@@ -25,6 +25,55 @@ int device_sm_count() {
   return n;
 }
 
+// ------------------------------------------------------------------ per-thread side stream
+namespace {
+struct SideSlot {
+  bool made = false;
+  SideStream ss{};
+};
+thread_local SideSlot t_side[16];
+
+bool make_side(SideSlot& sl) {
+  if (cudaStreamCreateWithFlags(&sl.ss.s, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaEventCreateWithFlags(&sl.ss.fork, cudaEventDisableTiming) != cudaSuccess ||
+      cudaEventCreateWithFlags(&sl.ss.join, cudaEventDisableTiming) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  sl.made = true;
+  return true;
+}
+
+SideSlot* side_slot() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  return &t_side[dev];
+}
+}  // namespace
+
+void side_stream_setup() {
+  SideSlot* sl = side_slot();
+  if (sl && !sl->made) make_side(*sl);
+}
+
+bool side_stream(SideStream& out, cudaStream_t st) {
+  SideSlot* sl = side_slot();
+  if (!sl) return false;
+  if (!sl->made) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cs) != cudaSuccess) {
+      cudaGetLastError();
+      return false;
+    }
+    if (cs != cudaStreamCaptureStatusNone || !make_side(*sl)) return false;
+  }
+  out = sl->ss;
+  return true;
+}
+
 // ------------------------------------------------------------------ kernel timing trace
 namespace {
 struct TraceRec {
@@ -284,6 +333,7 @@ usaf_status usaf_moe_fwd(const usaf_moe_shape* s, usaf_dtype dt, const void* x,
 
 size_t usaf_moe_bwd_workspace_size(const usaf_moe_shape* s, usaf_dtype dt, int64_t K) {
   if (!shape_ok(s) || !dtype_ok(dt) || K < 0) return 0;
+  side_stream_setup();  // a host-only call: the backward's side stream is created here
   Carver c(nullptr);
   BwdWs w;
   bwd_ws_layout(*s, dt, K, c, w);

@@ -105,6 +105,17 @@ __device__ __forceinline__ float silu_grad_f(float z) {
 
 int device_sm_count();
 
+// A side stream with a fork and a join event, one per calling thread and device (created once and
+// kept for the thread's life), for work that a call runs beside its main stream and joins back
+// before it returns. side_stream_setup() creates it from a host-only call; side_stream() hands it
+// out, creating it first unless `st` is being captured (then false: run the work on `st`).
+struct SideStream {
+  cudaStream_t s;
+  cudaEvent_t fork, join;
+};
+void side_stream_setup();
+bool side_stream(SideStream& out, cudaStream_t st);
+
 // Optional per-kernel timing: while usaf_trace_enable(1) is in force, a TraceScope records a
 // CUDA event pair around the launches inside it.
 bool trace_on();

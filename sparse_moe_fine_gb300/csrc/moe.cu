@@ -1275,6 +1275,8 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
   T* dhT = static_cast<T*>(w.dh);
   T* dyT = static_cast<T*>(w.dy_perm);
   const int64_t Ngu = s.E * 2 * s.I * s.H;
+  SideStream side{};
+  bool forked = false;  // the router gradient runs beside dx and the masked gradient
 
   // S6: gvec, dw, dh
   {
@@ -1311,13 +1313,22 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
       USAF_CHECK_LAUNCH();
       constexpr int FB = 32 * (16 / (int)sizeof(T));
       if (a.dt == USAF_BF16) {
+        // g_router needs only dl (dx's epilogue reads dl too, nothing reads g_router before the
+        // call returns): it runs on a side stream beside dx and the masked gradient, forked here
+        // and joined back at the end of the call (two branches of a captured graph)
+        forked = side_stream(side, st);
+        if (forked && (cudaEventRecord(side.fork, st) != cudaSuccess ||
+                       cudaStreamWaitEvent(side.s, side.fork, 0) != cudaSuccess))
+          return USAF_ERR_CUDA;
+        const cudaStream_t rs = forked ? side.s : st;
+        USAF_TRACE("router_grad", rs);
         // token tiles of at most 256 rows: ceil(R_cap / 256) + E bounds their count
         const unsigned ntile = (unsigned)(ceil_div(a.R_cap, TC_TOKEN_TILE) + E);
-        g_router_part_kernel<T><<<dim3((unsigned)ceil_div(H, FB), ntile), 256, 0, st>>>(
+        g_router_part_kernel<T><<<dim3((unsigned)ceil_div(H, FB), ntile), 256, 0, rs>>>(
             static_cast<const T*>(a.x), a.rt.perm_tok, w.dl_perm, cnt, off, w.plan, E, H,
             w.g_part, g_router, accumulate, dev_status);
         USAF_CHECK_LAUNCH();
-        g_router_reduce_kernel<<<grid_dim_for((int64_t)E * H), 256, 0, st>>>(
+        g_router_reduce_kernel<<<grid_dim_for((int64_t)E * H), 256, 0, rs>>>(
             w.g_part, w.plan, E, H, g_router, accumulate, dev_status);
       } else {
         g_router_sel_kernel<T><<<dim3((unsigned)ceil_div(H, FB), (unsigned)E), 256, 0, st>>>(
@@ -1406,6 +1417,9 @@ static usaf_status moe_bwd_t(const MoeArgs& a0, int renorm, const float* logits,
       USAF_CHECK_LAUNCH();
     }
   }
+  if (forked && (cudaEventRecord(side.join, side.s) != cudaSuccess ||
+                 cudaStreamWaitEvent(st, side.join, 0) != cudaSuccess))
+    return USAF_ERR_CUDA;
   return USAF_OK;
 }
 
