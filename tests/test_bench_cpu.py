@@ -129,7 +129,8 @@ def test_json_line_carries_every_contract_key(bench):
     clk.lines = ["2070, 2070, 900, 0x0, Not Active, Not Active, Not Active, Not Active"]
     fl, by = bench.algorithmic(CFG)
     units = bench.kernel_units(CFG)
-    trace = [("tc_dx", 200, 48.7), ("wgrad_sddmm", 200, 41.1), ("route_topk", 200, 2.4)]
+    trace = [("tc_dx", 200, 48.7), ("wgrad_sddmm", 200, 41.1), ("route_topk", 200, 2.4),
+             ("router_grad", 200, 52.0)]
     nbytes = CFG.T * CFG.H * 2
     roof = {"bound": "hbm", "achieved": 3700.0, "peak": 6779.0, "unit": "GB/s", "frac": 0.55,
             "traffic": None}
@@ -148,6 +149,9 @@ def test_json_line_carries_every_contract_key(bench):
     dx = next(k for k in line["kernels"] if k["name"] == "tc_dx")
     assert dx["gbs"] == pytest.approx(units["tc_dx"][1] / (48.7 / 200 / 1e3) / 1e9)
     assert "gbs" not in next(k for k in line["kernels"] if k["name"] == "route_topk")
+    # a side-stream scope spans the kernels it runs beside: flagged, no share of the step
+    rg = next(k for k in line["kernels"] if k["name"] == "router_grad")
+    assert rg["overlapped"] and rg["share"] is None
     skipped = bench.make_line(args, CFG, 1, 1.31, 3.1e6, 0.464, fl, by, roof, trace, 92.2, None,
                               None, nbytes, 22, clk, units, 6779.0, 1918.6)
     assert skipped["e2e"] is None
