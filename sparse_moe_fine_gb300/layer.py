@@ -84,6 +84,9 @@ class MoELayer:
         self.status = self.status2[0:1]
         # the expert SparseAdam update runs on a side stream, overlapping the next step's routing
         self.side = torch.cuda.Stream(device=d)
+        # the routing graph is replayed on a stream of the greatest priority, so that its blocks
+        # are placed ahead of the expert update's (which runs beside it at the default priority)
+        self.hp = torch.cuda.Stream(device=d, priority=torch.cuda.Stream.priority_range()[1])
         self.ev_bwd = torch.cuda.Event()
         # the update is issued in two parts, gate_up's entries first: ev_gu marks that part (the
         # forward's gate_up GEMM waits for it), ev_opt the whole update (its down GEMM waits)
@@ -289,7 +292,11 @@ class MoELayer:
         g_route, g_up, g_body, n_kernels = self._graphs[key]
         self.status = self.status2[par:par + 1]
         with torch.cuda.stream(main):
-            g_route.replay()  # routing and the token gather, beside the last expert update
+            # routing and the token gather, beside the last expert update, at high priority
+            self.hp.wait_stream(main)
+            with torch.cuda.stream(self.hp):
+                g_route.replay()
+            main.wait_stream(self.hp)
             if self.pending_opt:
                 main.wait_event(self.ev_gu)
             g_up.replay()     # the gate_up GEMM, beside the update's down_proj part
