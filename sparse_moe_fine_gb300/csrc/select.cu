@@ -1,16 +1,19 @@
 // Exact top-K selection by magnitude (the importance phase) and RigL drop/grow.
 //
 // USAF README: "Not all weights matter" (the importance phase keeps the 0.5% of weights with the
-// highest gradient magnitude) and "Sparsity adapts" (every 50 steps RigL swaps active weights
-// that contribute little for inactive ones with large gradients). Order: key descending, flat index ascending among equal keys; the key
-// of |g| is its fp32 bit pattern with the sign cleared.
+// highest gradient magnitude) and "Sparsity adapts" (every 50 steps RigL swaps active weights that
+// contribute little for inactive ones with large gradients). Order: key descending, flat index
+// ascending among equal keys; the key of |g| is its fp32 bit pattern with the sign cleared.
 //
-// Fast path, one read of g: a strided sample gives a candidate threshold tau0 a safe margin below
-// the K-th largest key; one coalesced pass compacts every (key, index) with key >= tau0 into
-// per-warp regions in index order; an exact radix select (4 digit rounds) and an ordered
-// compaction then run on the candidates only, one block per region. If a region overflows or fewer than K candidates
-// exist, the same kernels run on the full array instead (exact multi-pass path); the choice is
-// taken on the device, so the launch sequence is fixed and needs no host synchronisation.
+// Fast path, one read of g: 131,072 strided samples give a candidate threshold tau0 a safe margin
+// below the K-th largest key; one coalesced pass compacts every (key, index) with key >= tau0 into
+// per-warp regions in index order and counts the candidates' first radix digit; the remaining
+// digit rounds and the ordered count, scan and write then run on the candidates only (one warp per
+// region). If a region overflows or fewer than K candidates exist, the same kernels run on the
+// full array instead (exact multi-pass path); the choice is taken on the device, so the launch
+// sequence is fixed and needs no host synchronisation. RigL's grow selection is the same with an
+// exclusion bitmap of the active set; the selection and the swap of one importance pass can share
+// one pass over g (usaf_select_and_swap).
 #include "common.cuh"
 #include "kernels.cuh"
 
