@@ -163,22 +163,27 @@ def masked_split(layer, cfg):
 
 
 # DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) of one ncu capture of the
-# kernel on this workload (profiles/), with the SHA-256 of the source file at capture time; a
-# kernel whose source has changed since reports traffic null.
+# kernel on the workload named (profiles/), with the SHA-256 of the kernel's source file at capture
+# time; on another workload, or once that file has changed, the traffic is reported null.
 NCU_TRAFFIC = {
-    "wgrad_sddmm": (456482560 + 13689344, "sparse_moe_fine_gb300/csrc/moe.cu",
-                    "a16abe7656b4c7ffbad0b605d80699cd11cb1e2aea57bcd7e18144c23ab1d75a"),
-    "tc_gate_up_swiglu": (946807808 + 140072704, "sparse_moe_fine_gb300/csrc/moe_tc.cu",
+    # the masked-gradient kernel's code is unchanged since its capture; the file's later changes
+    # are host sequencing (staged forward, router gradient on a side stream)
+    "wgrad_sddmm": (456482560 + 13689344, "qwen3_30b_a3b", "sparse_moe_fine_gb300/csrc/moe.cu",
+                    "cd08276a7866c3678fb154013b547e0b331e89f6e014d22f04436d3b3a7bde2a"),
+    "tc_gate_up_swiglu": (946807808 + 140072704, "qwen3_30b_a3b",
+                          "sparse_moe_fine_gb300/csrc/moe_tc.cu",
                           "09b3f6edd25128d85ed5df16d125b3f4c7f081890aea944cce53f1f7891ea79c"),
-    "tc_dx": (1122077000 + 156789504, "sparse_moe_fine_gb300/csrc/moe_tc.cu",
+    "tc_dx": (1122077000 + 156789504, "qwen3_30b_a3b", "sparse_moe_fine_gb300/csrc/moe_tc.cu",
               "09b3f6edd25128d85ed5df16d125b3f4c7f081890aea944cce53f1f7891ea79c"),
 }
 
 
-def ncu_traffic(name):
+def ncu_traffic(name, workload="qwen3_30b_a3b"):
     if name not in NCU_TRAFFIC:
         return None
-    nbytes, src, sha = NCU_TRAFFIC[name]
+    nbytes, wl, src, sha = NCU_TRAFFIC[name]
+    if wl != workload:
+        return None
     import hashlib
     try:
         with open(os.path.join(os.path.dirname(os.path.abspath(__file__)), src), "rb") as f:
@@ -554,7 +559,8 @@ def run_steps(args, B, MoELayer, dist, ws, rank, local, dev, cfg, inp, x, dy, wg
     else:
         roof = {"bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"] if roof["achieved"] else None
-    roof.update({"kernel": name, "kernel_ms": avg_ms, "traffic": ncu_traffic(name),
+    roof.update({"kernel": name, "kernel_ms": avg_ms,
+                 "traffic": ncu_traffic(name, args.workload),
                  "peak_source": peak_src, "share": tms / tot if tot else None})
     fl, by = algorithmic(cfg, pairs)
     step_roof_ms = max(fl / (tf_sus * 1e12), by / (hbm * 1e9)) * 1e3
@@ -605,11 +611,11 @@ def e2e_time(args, layer, x, dy, e0, e1, stream, dist, dev):
 OVERLAPPED = {"router_grad"}
 
 
-def kernel_entry(n, l, t, tot, units, hbm, tf_burst):
+def kernel_entry(n, l, t, tot, units, hbm, tf_burst, workload="qwen3_30b_a3b"):
     e = {"name": n, "launches": l, "ms": t, "share": None if n in OVERLAPPED else t / tot}
     if n in OVERLAPPED:
         e["overlapped"] = True  # the span beside the main stream's kernels, not its own time
-    tr = ncu_traffic(n)
+    tr = ncu_traffic(n, workload)
     if tr is not None:
         e["traffic"] = tr
     if n in units:
@@ -653,7 +659,8 @@ def make_line(args, cfg, ws, ms, value, step_roof_ms, fl, by, roof, trace, tot, 
         "step_roofline": {"ms": step_roof_ms, "frac": step_roof_ms / ms,
                           "algorithmic_gflop": fl / 1e9, "algorithmic_gb": by / 1e9},
         "roofline": roof,
-        "kernels": [kernel_entry(n, l, t, tot, units, hbm, tf_burst) for n, l, t in trace],
+        "kernels": [kernel_entry(n, l, t, tot, units, hbm, tf_burst, args.workload)
+                    for n, l, t in trace],
         "importance_pass": importance,
         "e2e": None if e2e_ms is None else {
             "value": ws * cfg.T / (e2e_ms / 1e3), "unit": "tokens/s",

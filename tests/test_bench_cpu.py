@@ -108,6 +108,8 @@ def test_masked_gradient_units_split_between_the_two_kernels(bench):
 
 def test_traffic_is_reported_only_for_captured_kernels(bench):
     assert bench.ncu_traffic("gather_x") is None
+    # a capture's bytes belong to its workload only
+    assert bench.ncu_traffic("tc_dx", "mixtral_8x7b") is None
     assert set(bench.NCU_TRAFFIC) <= set(bench.kernel_units(CFG))
 
 
