@@ -796,8 +796,12 @@ __device__ __forceinline__ void umma_commit_local_pair(uint32_t bar) {
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
       : "memory");
 }
+// The epilogue's release of an accumulator buffer to the pair's MMA thread. Relaxed: what the MMA
+// must not overtake are this warp's tensor-memory reads, which have completed into registers
+// (tcgen05.wait::ld) and are ordered by the tcgen05 fences around the barrier; a release would
+// also wait for the warp's global stores and reductions, which nothing on the MMA side reads.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(
                    bar_cluster_addr)
                : "memory");
 }
